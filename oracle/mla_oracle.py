@@ -1,0 +1,304 @@
+"""CPU oracle of the multi-head latent attention (MLA) sublayer.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import this
+module: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg
+of ``bench.py`` use it.  It shares no code with the CUDA library and imports
+nothing from it.
+
+What it computes is the plain definition, in float64, with numpy matmul as
+the only library primitive and no blocking or fusion:
+
+* Kimi K2 "Dense transformer block" page, equation list: x_attn =
+  RMSNorm(x_n); c^Q = x W_DQ; c^Q-hat = RMSNorm(c^Q); c^KV = x W_DKV;
+  c^KV-hat = RMSNorm(c^KV); q^C, q^pe from c^Q-hat (W_UQ, W_QR); k^C, v from
+  c^KV-hat (W_UK, W_UV); k^pe = x W_KR; RoPE on q^pe and k^pe; Q = [Q^C; Q^R];
+  K_i = [K^C_i; k^R]; x'_n = x_n + Delta_attn.
+* "Mix and project" page (decode, P = 1000), code excerpt: scores =
+  Q K^T * softmax_scale, plus the additive mask, softmax in float32 (here:
+  float64), P V, heads merged head-major, o_proj.
+* "Key-value compression" page, code excerpt: one kv_a_proj_with_mqa matrix
+  produces 512 latent + 64 rotary-key features, split after the product; only
+  the 512-wide latent is normalised (kv_a_layernorm), the rotary key is not.
+
+Readings where the pages are silent (each also listed in the design doc):
+* RMSNorm(x; g) = g * x / sqrt(mean(x^2) + eps) with eps = 1e-6 for all three
+  norms (the module bodies are not printed).
+* q_b_proj output per head is [128 "nope" | 64 "pe"] in 192-wide blocks, the
+  same view-then-split the pages print for kv_b_proj ([128 k_nope | 128 v]).
+* RoPE is rotate-half on pairs (i, i + 32) with theta_i = base^(-2i/64),
+  base 10000, no frequency scaling; position t rotates pair i by t*theta_i.
+* Mask: causal (key j visible to query i iff j <= i) in prefill; none in
+  decode, where the new token sits at position P and attends to all P + 1 keys.
+* softmax_scale = 1/sqrt(192); dropout is the identity (inference).
+* The latent cache holds the normalised c^KV-hat and the rotated k^R.
+
+Every function below names the passage it follows.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+
+@dataclass(frozen=True)
+class Dims:
+    """Sizes of one MLA instance (defaults: Kimi K2, checked against the
+    101,124,096-parameter count in the dense-block page's parameter table)."""
+    d: int = 7168
+    H: int = 64
+    q_lora: int = 1536
+    kv_lora: int = 512
+    nope: int = 128
+    rope: int = 64
+    v: int = 128
+
+    @property
+    def qk(self) -> int:
+        return self.nope + self.rope
+
+
+KIMI_K2 = Dims()
+DEFAULT_EPS = 1e-6
+DEFAULT_ROPE_BASE = 10000.0
+
+
+def default_scale(dims: Dims = KIMI_K2) -> float:
+    return 1.0 / np.sqrt(dims.qk)
+
+
+def weight_shapes(dims: Dims = KIMI_K2) -> dict:
+    """nn.Linear weights are [out, in] (key-value compression page, MLA
+    __init__ excerpt); gains are vectors.  g_in is the block's attention
+    RMSNorm, counted outside the MLA total on the dense-block page."""
+    return {
+        "g_in": (dims.d,),
+        "w_q_a": (dims.q_lora, dims.d),
+        "g_qa": (dims.q_lora,),
+        "w_q_b": (dims.H * dims.qk, dims.q_lora),
+        "w_kv_a": (dims.kv_lora + dims.rope, dims.d),
+        "g_kva": (dims.kv_lora,),
+        "w_kv_b": (dims.H * (dims.nope + dims.v), dims.kv_lora),
+        "w_o": (dims.d, dims.H * dims.v),
+    }
+
+
+def mla_param_count(dims: Dims = KIMI_K2) -> int:
+    """Learned parameters of one MLA sublayer (everything but g_in)."""
+    return sum(int(np.prod(s)) for k, s in weight_shapes(dims).items() if k != "g_in")
+
+
+def rms_norm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm over the last axis (dense-block page: x_attn = RMSNorm(x_n),
+    c^Q-hat = RMSNorm(c^Q), c^KV-hat = RMSNorm(c^KV))."""
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return g * (x / np.sqrt(ms + eps))
+
+
+def rope_inv_freq(rope: int, base: float) -> np.ndarray:
+    """theta_i = base^(-2i/rope) for i = 0 .. rope/2 - 1 (one per pair)."""
+    i = np.arange(rope // 2, dtype=np.float64)
+    return base ** (-2.0 * i / rope)
+
+
+def rope_rotate(x: np.ndarray, pos: np.ndarray, base: float) -> np.ndarray:
+    """RoPE(x, R_t) of the dense-block page: rotate-half on pairs (i, i+half).
+
+    ``pos`` broadcasts against x[..., 0].
+    y_i = x_i cos(t th_i) - x_{i+half} sin(t th_i)
+    y_{i+half} = x_{i+half} cos(t th_i) + x_i sin(t th_i)
+    """
+    half = x.shape[-1] // 2
+    ang = np.asarray(pos, dtype=np.float64)[..., None] * rope_inv_freq(x.shape[-1], base)
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def _linear(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """nn.Linear without bias: x W^T (attention_bias absent: the parameter
+    count 101,124,096 holds only without biases)."""
+    return x @ w.T
+
+
+def project_tokens(w: dict, x: np.ndarray, pos: np.ndarray, dims: Dims, eps: float,
+                   base: float, want_q: bool = True) -> dict:
+    """Per-token part of MLA for tokens x [..., d] at positions ``pos``.
+
+    Dense-block page equations c^Q .. v, and the key-value compression page's
+    split of kv_a_proj_with_mqa into the 512 latent and the 64-wide rotary key
+    (only the latent is normalised).  Returns per-head K rows [..., H, qk],
+    V rows [..., H, v], the latent c^KV-hat [..., kv_lora], the rotated rotary
+    key k^R [..., rope] and (if want_q) Q rows [..., H, qk].
+    """
+    x_attn = rms_norm(x, w["g_in"], eps)
+    ckv_full = _linear(x_attn, w["w_kv_a"])
+    ckv = ckv_full[..., :dims.kv_lora]
+    kpe_raw = ckv_full[..., dims.kv_lora:]
+    ckv_hat = rms_norm(ckv, w["g_kva"], eps)
+    kv = _linear(ckv_hat, w["w_kv_b"]).reshape(x.shape[:-1] + (dims.H, dims.nope + dims.v))
+    k_nope = kv[..., :dims.nope]
+    v = kv[..., dims.nope:]
+    k_r = rope_rotate(kpe_raw, pos, base)
+    # K_i = [K^C_i ; k^R]: the one rotary key is shared by every head
+    k_r_heads = np.broadcast_to(k_r[..., None, :], k_nope.shape[:-1] + (dims.rope,))
+    out = {
+        "K": np.concatenate([k_nope, k_r_heads], axis=-1),
+        "V": v,
+        "ckv": ckv_hat,
+        "kpe": k_r,
+    }
+    if want_q:
+        cq_hat = rms_norm(_linear(x_attn, w["w_q_a"]), w["g_qa"], eps)
+        q = _linear(cq_hat, w["w_q_b"]).reshape(x.shape[:-1] + (dims.H, dims.qk))
+        q_nope = q[..., :dims.nope]
+        q_pe = rope_rotate(q[..., dims.nope:], np.asarray(pos)[..., None], base)
+        out["Q"] = np.concatenate([q_nope, q_pe], axis=-1)
+    return out
+
+
+def softmax(s: np.ndarray) -> np.ndarray:
+    """softmax over the last axis with max subtraction (masked entries are
+    -inf and contribute exp(-inf) = 0)."""
+    m = np.max(s, axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    return e / np.sum(e, axis=-1, keepdims=True)
+
+
+def attend(Q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float,
+           q_pos: np.ndarray | None) -> np.ndarray:
+    """One head: softmax(Q K^T * scale + M) V ("Mix and project" page code).
+
+    Q [nq, qk], K [nk, qk], V [nk, v].  q_pos gives each query's position for
+    the causal mask M (key j visible iff j <= q_pos); None means no mask.
+    """
+    s = (Q @ K.T) * scale
+    if q_pos is not None:
+        j = np.arange(K.shape[0])
+        s = np.where(j[None, :] <= np.asarray(q_pos)[:, None], s, -np.inf)
+    return softmax(s) @ V
+
+
+def prefill(w: dict, x: np.ndarray, dims: Dims = KIMI_K2, eps: float = DEFAULT_EPS,
+            base: float = DEFAULT_ROPE_BASE, scale: float | None = None,
+            query_rows=None) -> dict:
+    """Causal prefill of x [B, T, d] at positions 0..T-1.
+
+    Returns out = x + Delta [B, nq, d], Delta, the rebuilt caches
+    K [B, H, T, qk], V [B, H, T, v], the latent cache ckv [B, T, kv_lora] and
+    kpe [B, T, rope].  ``query_rows`` restricts the queries (and out/Delta
+    rows) to those positions; keys and values always cover all T tokens.
+    """
+    if scale is None:
+        scale = default_scale(dims)
+    B, T, _ = x.shape
+    rows = np.arange(T) if query_rows is None else np.asarray(query_rows)
+    pos = np.arange(T)
+    kv = project_tokens(w, x, pos[None, :], dims, eps, base, want_q=False)
+    qp = project_tokens(w, x[:, rows], rows[None, :], dims, eps, base, want_q=True)
+    O = np.empty((B, len(rows), dims.H, dims.v))
+    for b in range(B):
+        for h in range(dims.H):
+            O[b, :, h] = attend(qp["Q"][b, :, h], kv["K"][b, :, h], kv["V"][b, :, h], scale, rows)
+    delta = _linear(O.reshape(B, len(rows), dims.H * dims.v), w["w_o"])
+    return {
+        "out": x[:, rows] + delta,
+        "delta": delta,
+        "K": np.ascontiguousarray(kv["K"].transpose(0, 2, 1, 3)),
+        "V": np.ascontiguousarray(kv["V"].transpose(0, 2, 1, 3)),
+        "ckv": kv["ckv"],
+        "kpe": kv["kpe"],
+    }
+
+
+def decode(w: dict, x_new: np.ndarray, K_cache: np.ndarray, V_cache: np.ndarray,
+           dims: Dims = KIMI_K2, eps: float = DEFAULT_EPS, base: float = DEFAULT_ROPE_BASE,
+           scale: float | None = None) -> dict:
+    """One decode step against the rebuilt per-head cache.
+
+    x_new [B, d] is the token at position P = K_cache.shape[2]; K_cache
+    [B, H, P, qk] and V_cache [B, H, P, v] hold positions 0..P-1 (post-RoPE).
+    The cache update appends the new K/V and the query attends to all P + 1
+    keys with no mask ("Mix and project" page: past_key_value.update, then
+    scores over kv_seq_len = P + 1).
+    """
+    if scale is None:
+        scale = default_scale(dims)
+    B = x_new.shape[0]
+    P = K_cache.shape[2]
+    t = project_tokens(w, x_new, np.full((B,), P), dims, eps, base, want_q=True)
+    O = np.empty((B, dims.H, dims.v))
+    for b in range(B):
+        for h in range(dims.H):
+            K = np.concatenate([K_cache[b, h], t["K"][b, h][None]], axis=0)
+            V = np.concatenate([V_cache[b, h], t["V"][b, h][None]], axis=0)
+            O[b, h] = attend(t["Q"][b, h][None], K, V, scale, None)[0]
+    delta = _linear(O.reshape(B, dims.H * dims.v), w["w_o"])
+    return {"out": x_new + delta, "delta": delta, "k_new": t["K"], "v_new": t["V"],
+            "ckv_new": t["ckv"], "kpe_new": t["kpe"]}
+
+
+def rebuild_kv(w: dict, ckv: np.ndarray, kpe: np.ndarray, dims: Dims = KIMI_K2):
+    """Per-head K/V from the latent cache (key-value compression page: the key
+    content and values of all heads are rebuilt from one latent per position).
+    ckv [..., P, kv_lora], kpe [..., P, rope] -> K [..., H, P, qk], V [..., H, P, v]."""
+    kv = _linear(ckv, w["w_kv_b"]).reshape(ckv.shape[:-1] + (dims.H, dims.nope + dims.v))
+    k_nope = kv[..., :dims.nope]
+    k_r = np.broadcast_to(kpe[..., None, :], k_nope.shape[:-1] + (dims.rope,))
+    K = np.concatenate([k_nope, k_r], axis=-1)
+    V = kv[..., dims.nope:]
+    return np.moveaxis(K, -2, -3), np.moveaxis(V, -2, -3)
+
+
+def decode_latent(w: dict, x_new: np.ndarray, ckv_cache: np.ndarray, kpe_cache: np.ndarray,
+                  dims: Dims = KIMI_K2, eps: float = DEFAULT_EPS,
+                  base: float = DEFAULT_ROPE_BASE, scale: float | None = None) -> dict:
+    """Decode against the 576-value latent cache: rebuild, then attend.
+
+    ckv_cache [B, P, kv_lora] (normalised latent) and kpe_cache [B, P, rope]
+    (rotated rotary key) hold positions 0..P-1.  The per-head K/V are rebuilt
+    from the latent exactly as in prefill, then ``decode`` runs.
+    """
+    K_cache, V_cache = rebuild_kv(w, ckv_cache, kpe_cache, dims)
+    return decode(w, x_new, K_cache, V_cache, dims, eps, base, scale)
+
+
+def decode_latent_absorbed(w: dict, x_new: np.ndarray, ckv_cache: np.ndarray,
+                           kpe_cache: np.ndarray, dims: Dims = KIMI_K2,
+                           eps: float = DEFAULT_EPS, base: float = DEFAULT_ROPE_BASE,
+                           scale: float | None = None) -> dict:
+    """Same step with W_UK / W_UV absorbed (the design the key-value
+    compression page attributes to DeepSeek-V2: cache the latent instead of
+    per-head K/V).  Used only as an invariant: it equals ``decode_latent`` up
+    to float64 rounding, since q.(W_UK c) = (W_UK^T q).c and
+    sum_j p_j W_UV c_j = W_UV sum_j p_j c_j.
+    """
+    if scale is None:
+        scale = default_scale(dims)
+    B = x_new.shape[0]
+    P = ckv_cache.shape[1]
+    t = project_tokens(w, x_new, np.full((B,), P), dims, eps, base, want_q=True)
+    wkvb = w["w_kv_b"].reshape(dims.H, dims.nope + dims.v, dims.kv_lora)
+    w_uk, w_uv = wkvb[:, :dims.nope], wkvb[:, dims.nope:]
+    O = np.empty((B, dims.H, dims.v))
+    for b in range(B):
+        C = np.concatenate([ckv_cache[b], t["ckv"][b][None]], axis=0)      # [P+1, kv_lora]
+        R = np.concatenate([kpe_cache[b], t["kpe"][b][None]], axis=0)      # [P+1, rope]
+        for h in range(dims.H):
+            q_lat = w_uk[h].T @ t["Q"][b, h, :dims.nope]
+            s = (C @ q_lat + R @ t["Q"][b, h, dims.nope:]) * scale
+            p = softmax(s[None])[0]
+            O[b, h] = w_uv[h] @ (p @ C)
+    delta = _linear(O.reshape(B, dims.H * dims.v), w["w_o"])
+    return {"out": x_new + delta, "delta": delta}
+
+
+def cache_from_tokens(w: dict, x: np.ndarray, dims: Dims = KIMI_K2, eps: float = DEFAULT_EPS,
+                      base: float = DEFAULT_ROPE_BASE) -> dict:
+    """Both caches for tokens x [B, P, d] at positions 0..P-1 (what a prefill
+    writes): K [B, H, P, qk], V [B, H, P, v], ckv [B, P, kv_lora], kpe [B, P, rope]."""
+    P = x.shape[1]
+    t = project_tokens(w, x, np.arange(P)[None, :], dims, eps, base, want_q=False)
+    return {"K": np.ascontiguousarray(t["K"].transpose(0, 2, 1, 3)),
+            "V": np.ascontiguousarray(t["V"].transpose(0, 2, 1, 3)),
+            "ckv": t["ckv"], "kpe": t["kpe"]}
