@@ -1,0 +1,176 @@
+/*
+ * mla.h -- C ABI of the GB300 (sm_103a) multi-head latent attention sublayer.
+ *
+ * The operation is the MLA sublayer of a Kimi K2 / DeepSeek-V3 style block:
+ *   Kimi K2 "Dense transformer block" page, equation list (x_attn = RMSNorm(x),
+ *     c^Q, c^KV, q^C/q^pe, k^C/k^pe, v, RoPE, Q = [Q^C; Q^R], K_i = [K^C_i; k^R],
+ *     x' = x + Delta_attn);
+ *   "Mix and project" page (decode, P = 1,000), code excerpt: scores scaled and
+ *     masked, float32 softmax, P.V, heads merged head-major, o_proj;
+ *   "Key-value compression" page: kv_a_proj_with_mqa gives a 512-wide latent
+ *     and one 64-wide rotary key (576 features, split after the product); the
+ *     latent alone is normalised; 576 cached values per position for the
+ *     latent form versus 20,480 for rebuilt per-head keys and values.
+ *
+ * Fixed sizes (checked against the pages' 101,124,096 MLA parameters):
+ *   d = 7168, H = 64 heads, q_lora = 1536, kv_lora = 512,
+ *   qk = 128 (nope) + 64 (rope, 32 pairs) = 192, v = 128, no biases.
+ * Other sizes are not supported.
+ *
+ * Conventions for every entry point
+ *   - All tensors are bf16, row-major, in device memory, owned by the caller.
+ *     Weights use the nn.Linear layout [out, in].
+ *   - Every pointer must be 16-byte aligned (MLA_ERR_ALIGNMENT otherwise).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  The library never synchronises and allocates no
+ *     device memory: all scratch lives in the caller's workspace, sized by
+ *     mla_workspace_size().  A workspace must not be shared by calls that may
+ *     run concurrently.
+ *   - Positions are implicit: prefill tokens sit at positions 0..T-1 with a
+ *     causal mask (key j visible to query i iff j <= i); a decode token sits
+ *     at position P and attends to all P + 1 keys.
+ *   - RoPE is rotate-half on pairs (i, i+32), theta_i = rope_base^(-2i/64).
+ *   - `out` may be the same buffer as `x` (in-place residual); any other
+ *     overlap between out and x is rejected.
+ *   - Arguments are checked on the host before anything is enqueued; a
+ *     failed check returns a negative status and enqueues nothing.  This
+ *     mirrors the shape checks (ValueError / assert) of the pages' code.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define MLA_OK 0
+#define MLA_ERR_INVALID_ARG (-1)  /* null pointer, B/T/P out of range, cap too small, overlap */
+#define MLA_ERR_ALIGNMENT (-2)    /* a pointer is not 16-byte aligned */
+#define MLA_ERR_WORKSPACE (-3)    /* workspace NULL or smaller than mla_workspace_size() */
+#define MLA_ERR_UNSUPPORTED (-4)  /* a size or mode the library does not implement */
+#define MLA_ERR_CUDA (-5)         /* a CUDA call or kernel launch failed */
+#define MLA_ERR_TIMEOUT (-6)      /* a bounded device-side wait gave up (see mla_device_status) */
+
+/* ---- fixed sizes -------------------------------------------------------- */
+#define MLA_D 7168
+#define MLA_HEADS 64
+#define MLA_Q_LORA 1536
+#define MLA_KV_LORA 512
+#define MLA_QK_NOPE 128
+#define MLA_QK_ROPE 64
+#define MLA_QK 192
+#define MLA_V 128
+
+/* ---- modes for mla_workspace_size ---------------------------------------- */
+#define MLA_MODE_PREFILL 0
+#define MLA_MODE_DECODE 1
+#define MLA_MODE_DECODE_LATENT 2
+
+/* Weights of one MLA sublayer: device pointers to bf16, nn.Linear [out, in].
+ * Key-value compression page, MLA __init__ excerpt, for the projections;
+ * w_in_norm is the block's input RMSNorm gain (dense-block page). */
+typedef struct {
+  const void* w_in_norm;   /* [7168]          input RMSNorm gain            */
+  const void* w_q_a;       /* [1536, 7168]    q_a_proj (W_DQ)               */
+  const void* w_q_a_norm;  /* [1536]          q_a_layernorm gain            */
+  const void* w_q_b;       /* [12288, 1536]   q_b_proj; per head [128 nope | 64 pe] */
+  const void* w_kv_a;      /* [576, 7168]     kv_a_proj_with_mqa (W_DKV ; W_KR) */
+  const void* w_kv_a_norm; /* [512]           kv_a_layernorm gain           */
+  const void* w_kv_b;      /* [16384, 512]    kv_b_proj; per head [128 k_nope | 128 v] */
+  const void* w_o;         /* [7168, 8192]    o_proj                        */
+} mla_weights_t;
+
+/* Stage ids for optional per-stage timing. */
+#define MLA_STAGE_INPUT_NORM 0   /* RMSNorm(x) and the RoPE table            */
+#define MLA_STAGE_A_PROJ 1       /* x_attn . [W_DQ ; W_DKV ; W_KR]^T          */
+#define MLA_STAGE_LATENT 2       /* split, q/kv latent RMSNorm, RoPE(k), latent cache write */
+#define MLA_STAGE_Q_B 3          /* q_b_proj + RoPE(q)                       */
+#define MLA_STAGE_KV_B 4         /* kv_b_proj + per-head K/V cache write     */
+#define MLA_STAGE_ATTN 5         /* attention (prefill, decode or latent decode) */
+#define MLA_STAGE_COMBINE 6      /* split-KV combine                         */
+#define MLA_STAGE_ABSORB_Q 7     /* latent decode: q_nope . W_UK             */
+#define MLA_STAGE_ABSORB_O 8     /* latent decode: o_latent . W_UV^T         */
+#define MLA_STAGE_O_PROJ 9       /* o_proj + residual                        */
+#define MLA_MAX_STAGES 10
+
+/* Optional per-stage timing.  start[s] / stop[s] are cudaEvent_t handles
+ * created by the caller (or NULL to skip stage s); the library records them
+ * on `stream` around stage s.  n_launches is written with the number of
+ * kernels the call enqueued. */
+typedef struct {
+  void* start[MLA_MAX_STAGES];
+  void* stop[MLA_MAX_STAGES];
+  int n_launches;
+} mla_timing_t;
+
+/* Runtime parameters.  Passing NULL for the whole struct selects
+ * eps = 1e-6, rope_base = 10000, softmax_scale = 1/sqrt(192). */
+typedef struct {
+  float eps;            /* RMSNorm epsilon, used by all three norms        */
+  float rope_base;      /* RoPE base                                       */
+  float softmax_scale;  /* multiplies Q.K before the softmax               */
+  float* delta_out;     /* optional: float32 [N_tok, 7168] receives Delta_attn
+                           (o_proj output before the residual); NULL = off */
+  mla_timing_t* timing; /* optional per-stage events; NULL = off            */
+} mla_params_t;
+
+/* Bytes of workspace an entry point needs.
+ *   mode = MLA_MODE_PREFILL:       B sequences of T = t_or_p tokens; `cap` is
+ *                                  ignored (pass the cache capacity or 0).
+ *   mode = MLA_MODE_DECODE / _LATENT: B sequences, P = t_or_p cached positions.
+ * Returns 0 when the arguments are out of range. */
+size_t mla_workspace_size(int mode, int B, int t_or_p, int cap);
+
+/* Causal prefill of x [B, T, 7168] at positions 0..T-1.
+ *   out       [B, T, 7168]        x + Delta_attn (may alias x exactly)
+ *   k_cache   [B, 64, cap, 192]   optional (NULL): receives K rows 0..T-1, post-RoPE
+ *   v_cache   [B, 64, cap, 128]   optional, given together with k_cache
+ *   ckv_cache [B, cap, 512]       optional (NULL): receives the normalised latent c^KV-hat
+ *   kpe_cache [B, cap, 64]        optional, given together with ckv_cache: rotated k^R
+ *   cap       cache capacity in positions; must be >= T when a cache is given
+ * Errors: INVALID_ARG (B < 1, T < 1, null x/out/weights, only one of a cache
+ * pair, cap < T, partial x/out overlap), ALIGNMENT, WORKSPACE, CUDA. */
+int mla_prefill(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int T,
+                void* out, void* k_cache, void* v_cache, void* ckv_cache, void* kpe_cache, int cap,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/* One decode step against the rebuilt per-head cache (the pinned
+ * implementation's cache, "Mix and project" page at P = 1,000).
+ *   x        [B, 7168]           the new token of each sequence, at position P
+ *   k_cache  [B, 64, cap, 192]   positions 0..P-1 are read; row P is written
+ *   v_cache  [B, 64, cap, 128]   same
+ *   out      [B, 7168]           x + Delta_attn (may alias x exactly)
+ * Requires 0 <= P and P + 1 <= cap.
+ * Errors: INVALID_ARG, ALIGNMENT, WORKSPACE, CUDA. */
+int mla_decode(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int P,
+               void* k_cache, void* v_cache, int cap, void* out,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/* One decode step against the 576-value latent cache, with W_UK absorbed
+ * into the query and W_UV applied after attention (the latent-caching design
+ * the key-value compression page describes).
+ *   ckv_cache [B, cap, 512]  normalised latent; positions 0..P-1 read, row P written
+ *   kpe_cache [B, cap, 64]   rotated rotary key; same
+ * Other arguments as mla_decode. */
+int mla_decode_latent(const mla_weights_t* w, const mla_params_t* params, const void* x, int B,
+                      int P, void* ckv_cache, void* kpe_cache, int cap, void* out,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream` and reads the device status word the last call on
+ * this workspace left: MLA_OK, or MLA_ERR_TIMEOUT if a bounded device wait
+ * gave up (the kernel then skipped its remaining work and returned).
+ * MLA_ERR_CUDA if the synchronisation itself fails. */
+int mla_device_status(const void* workspace, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* mla_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

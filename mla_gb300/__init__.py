@@ -1,0 +1,188 @@
+"""Python binding of libmla.so (the GB300 MLA sublayer).
+
+Argument marshalling only: each function takes torch tensors for device
+memory and the current torch stream, and calls the C entry point of the same
+name (include/mla.h).  Every step of the computation runs in the library's
+CUDA kernels; there is no fallback.  If the library has not been built the
+import of ``lib()`` fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmla.so")
+
+D, HEADS, Q_LORA, KV_LORA, QK_NOPE, QK_ROPE, QK, V = 7168, 64, 1536, 512, 128, 64, 192, 128
+MODE_PREFILL, MODE_DECODE, MODE_DECODE_LATENT = 0, 1, 2
+STAGES = ["input_norm", "a_proj", "latent", "q_b", "kv_b", "attn", "combine", "absorb_q", "absorb_o", "o_proj"]
+MAX_STAGES = len(STAGES)
+
+STATUS = {0: "MLA_OK", -1: "MLA_ERR_INVALID_ARG", -2: "MLA_ERR_ALIGNMENT", -3: "MLA_ERR_WORKSPACE",
+          -4: "MLA_ERR_UNSUPPORTED", -5: "MLA_ERR_CUDA", -6: "MLA_ERR_TIMEOUT"}
+
+WEIGHT_NAMES = ["w_in_norm", "w_q_a", "w_q_a_norm", "w_q_b", "w_kv_a", "w_kv_a_norm", "w_kv_b", "w_o"]
+WEIGHT_SHAPES = {
+    "w_in_norm": (D,), "w_q_a": (Q_LORA, D), "w_q_a_norm": (Q_LORA,), "w_q_b": (HEADS * QK, Q_LORA),
+    "w_kv_a": (KV_LORA + QK_ROPE, D), "w_kv_a_norm": (KV_LORA,), "w_kv_b": (HEADS * (QK_NOPE + V), KV_LORA),
+    "w_o": (D, HEADS * V),
+}
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+class MlaWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_NAMES]
+
+
+class MlaTiming(ctypes.Structure):
+    _fields_ = [("start", ctypes.c_void_p * MAX_STAGES), ("stop", ctypes.c_void_p * MAX_STAGES),
+                ("n_launches", ctypes.c_int)]
+
+
+class MlaParams(ctypes.Structure):
+    _fields_ = [("eps", ctypes.c_float), ("rope_base", ctypes.c_float), ("softmax_scale", ctypes.c_float),
+                ("delta_out", ctypes.c_void_p), ("timing", ctypes.POINTER(MlaTiming))]
+
+
+_lib = None
+
+_VP, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_SIGS = {
+    "mla_workspace_size": (_SZ, [_I, _I, _I, _I]),
+    "mla_prefill": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _VP, _VP, _VP, _VP,
+                         _VP, _I, _VP, _SZ, _VP]),
+    "mla_decode": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _VP, _VP, _I, _VP,
+                        _VP, _SZ, _VP]),
+    "mla_decode_latent": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _VP, _VP, _I,
+                               _VP, _VP, _SZ, _VP]),
+    "mla_device_status": (_I, [_VP, _VP]),
+    "mla_status_string": (ctypes.c_char_p, [_I]),
+    "mla_debug_gemm": (_I, [_VP, _I, _VP, _I, _I, _VP, _I, _I, _I, _I, _VP]),
+    "mla_debug_wait_timeout": (_I, [_VP, ctypes.c_uint64, _VP]),
+    "mla_debug_umma_probe": (_I, [_VP, _I, _VP]),
+}
+
+
+def lib():
+    """The loaded libmla.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} not found: the CUDA library must be built "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise MlaError(rc, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_weights(w: dict) -> MlaWeights:
+    """Pack a dict of bf16 CUDA tensors (names of WEIGHT_NAMES) into the C struct."""
+    import torch
+    for n in WEIGHT_NAMES:
+        t = w[n]
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != WEIGHT_SHAPES[n]:
+            raise ValueError(f"weight {n}: need contiguous bf16 CUDA tensor of shape {WEIGHT_SHAPES[n]}")
+    return MlaWeights(*[w[n].data_ptr() for n in WEIGHT_NAMES])
+
+
+def make_params(eps=1e-6, rope_base=10000.0, softmax_scale=None, delta_out=None, timing=None) -> MlaParams:
+    if softmax_scale is None:
+        softmax_scale = 1.0 / (QK ** 0.5)
+    return MlaParams(eps, rope_base, softmax_scale,
+                     None if delta_out is None else delta_out.data_ptr(),
+                     None if timing is None else ctypes.pointer(timing))
+
+
+def workspace_size(mode: int, B: int, t_or_p: int, cap: int = 0) -> int:
+    n = lib().mla_workspace_size(mode, B, t_or_p, cap)
+    if n == 0:
+        raise MlaError(-1, "mla_workspace_size")
+    return n
+
+
+def alloc_workspace(mode: int, B: int, t_or_p: int, device="cuda"):
+    import torch
+    return torch.empty(workspace_size(mode, B, t_or_p), dtype=torch.uint8, device=device)
+
+
+def mla_prefill(weights: MlaWeights, x, out, workspace, k_cache=None, v_cache=None, ckv_cache=None,
+                kpe_cache=None, cap=0, params: MlaParams | None = None, stream=None):
+    """x, out: bf16 [B, T, 7168]; caches as in include/mla.h."""
+    B, T = x.shape[0], x.shape[1]
+    rc = lib().mla_prefill(ctypes.byref(weights), None if params is None else ctypes.byref(params), _ptr(x), B, T,
+                           _ptr(out), _ptr(k_cache), _ptr(v_cache), _ptr(ckv_cache), _ptr(kpe_cache), cap,
+                           _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "mla_prefill")
+
+
+def mla_decode(weights: MlaWeights, x, P: int, k_cache, v_cache, out, workspace,
+               params: MlaParams | None = None, stream=None):
+    """x, out: bf16 [B, 7168]; k_cache [B, 64, cap, 192], v_cache [B, 64, cap, 128]."""
+    B = x.shape[0]
+    cap = k_cache.shape[2]
+    rc = lib().mla_decode(ctypes.byref(weights), None if params is None else ctypes.byref(params), _ptr(x), B, P,
+                          _ptr(k_cache), _ptr(v_cache), cap, _ptr(out), _ptr(workspace), workspace.numel(),
+                          _stream(stream))
+    _check(rc, "mla_decode")
+
+
+def mla_decode_latent(weights: MlaWeights, x, P: int, ckv_cache, kpe_cache, out, workspace,
+                      params: MlaParams | None = None, stream=None):
+    """x, out: bf16 [B, 7168]; ckv_cache [B, cap, 512], kpe_cache [B, cap, 64]."""
+    B = x.shape[0]
+    cap = ckv_cache.shape[1]
+    rc = lib().mla_decode_latent(ctypes.byref(weights), None if params is None else ctypes.byref(params), _ptr(x),
+                                 B, P, _ptr(ckv_cache), _ptr(kpe_cache), cap, _ptr(out), _ptr(workspace),
+                                 workspace.numel(), _stream(stream))
+    _check(rc, "mla_decode_latent")
+
+
+def mla_device_status(workspace, stream=None) -> int:
+    return lib().mla_device_status(_ptr(workspace), _stream(stream))
+
+
+def mla_status_string(status: int) -> str:
+    return lib().mla_status_string(status).decode()
+
+
+# ---- test hooks (include/mla_debug.h) -------------------------------------
+def mla_debug_gemm(A, B, C, b_mn_major=False, stream=None):
+    """C = A @ B^T (B [N, K]) or A @ B (B [K, N] when b_mn_major)."""
+    M, K = A.shape
+    N = B.shape[0] if not b_mn_major else B.shape[1]
+    rc = lib().mla_debug_gemm(_ptr(A), A.stride(0), _ptr(B), B.stride(0), int(b_mn_major), _ptr(C), C.stride(0),
+                              M, N, K, _stream(stream))
+    _check(rc, "mla_debug_gemm")
+
+
+def mla_debug_wait_timeout(status_word, limit_ns: int, stream=None):
+    _check(lib().mla_debug_wait_timeout(_ptr(status_word), limit_ns, _stream(stream)), "mla_debug_wait_timeout")
+
+
+def mla_debug_umma_probe(out, m: int, stream=None):
+    _check(lib().mla_debug_umma_probe(_ptr(out), m, _stream(stream)), "mla_debug_umma_probe")

@@ -1,0 +1,484 @@
+// C ABI of the MLA sublayer: argument checks, workspace layout and the
+// launch sequence of each entry point.  Every compute step runs in the
+// kernels of this library; nothing here touches tensor data on the host.
+#include "common.cuh"
+#include "internal.h"
+#include "../../include/mla.h"
+
+#include <math.h>
+#include <string.h>
+
+namespace mla {
+namespace {
+
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+constexpr int kMaxSmsForSizing = 256;                     // workspace upper bound
+constexpr int64_t kMaxTokens = 1 << 24;
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Workspace carve-up.  Offsets are computed identically by the size query
+// and by the entry points.
+struct Layout {
+  size_t status, cs, xn, ca, cq, ckv, kpe, q, o, kscr, vscr, qlat, olat, part_o, part_ml, total;
+};
+
+Layout make_layout(int mode, int B, int t_or_p, int num_sms) {
+  Layout L{};
+  const size_t n = (mode == MLA_MODE_PREFILL) ? (size_t)B * t_or_p : (size_t)B;
+  const size_t npos = (mode == MLA_MODE_PREFILL) ? (size_t)t_or_p : 1;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off = align256(off + bytes);
+    return at;
+  };
+  L.status = take(256);
+  L.cs = take(npos * 32 * sizeof(float2));
+  L.xn = take(n * MLA_D * 2);
+  L.ca = take(n * 2112 * 2);
+  L.cq = take(n * MLA_Q_LORA * 2);
+  L.ckv = take(n * MLA_KV_LORA * 2);
+  L.kpe = take(n * MLA_QK_ROPE * 2);
+  L.q = take(n * MLA_HEADS * MLA_QK * 2);
+  L.o = take(n * MLA_HEADS * MLA_V * 2);
+  if (mode == MLA_MODE_PREFILL) {
+    L.kscr = take((size_t)B * MLA_HEADS * t_or_p * MLA_QK * 2);
+    L.vscr = take((size_t)B * MLA_HEADS * t_or_p * MLA_V * 2);
+  } else if (mode == MLA_MODE_DECODE) {
+    const int s = decode_splits(B, t_or_p + 1, num_sms);
+    L.part_o = take((size_t)B * MLA_HEADS * s * MLA_V * sizeof(float));
+    L.part_ml = take((size_t)B * MLA_HEADS * s * sizeof(float2));
+  } else {
+    const int s = latent_splits(B, t_or_p + 1, num_sms);
+    L.qlat = take((size_t)B * MLA_HEADS * 576 * 2);
+    L.olat = take((size_t)B * MLA_HEADS * MLA_KV_LORA * 2);
+    L.part_o = take((size_t)B * s * MLA_HEADS * MLA_KV_LORA * sizeof(float));
+    L.part_ml = take((size_t)B * s * MLA_HEADS * sizeof(float2));
+  }
+  L.total = off;
+  return L;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int num_sms_of_current_device() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  return n;
+}
+
+int check_weights(const mla_weights_t* w) {
+  if (!w) return MLA_ERR_INVALID_ARG;
+  const void* ps[] = {w->w_in_norm, w->w_q_a, w->w_q_a_norm, w->w_q_b,
+                      w->w_kv_a,    w->w_kv_a_norm, w->w_kv_b, w->w_o};
+  for (const void* p : ps) {
+    if (!p) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(p)) return MLA_ERR_ALIGNMENT;
+  }
+  return MLA_OK;
+}
+
+// x/out may be the same buffer; any other overlap is rejected.
+bool bad_overlap(const void* x, const void* out, size_t bytes) {
+  if (x == out) return false;
+  const char* a = static_cast<const char*>(x);
+  const char* b = static_cast<const char*>(out);
+  return a < b + bytes && b < a + bytes;
+}
+
+struct Params {
+  float eps, base, scale;
+  float* delta;
+  mla_timing_t* timing;
+};
+
+Params resolve(const mla_params_t* p) {
+  Params r{1e-6f, 10000.f, 1.0f / sqrtf(192.0f), nullptr, nullptr};
+  if (p) {
+    r.eps = p->eps;
+    r.base = p->rope_base;
+    r.scale = p->softmax_scale;
+    r.delta = p->delta_out;
+    r.timing = p->timing;
+  }
+  return r;
+}
+
+bool params_ok(const Params& p) {
+  return p.eps >= 0.f && isfinite(p.eps) && p.base > 1.f && isfinite(p.base) && p.scale > 0.f &&
+         isfinite(p.scale) && (p.delta == nullptr || aligned16(p.delta));
+}
+
+struct Stager {
+  mla_timing_t* t;
+  cudaStream_t s;
+  void start(int id) {
+    if (t && t->start[id]) cudaEventRecord(static_cast<cudaEvent_t>(t->start[id]), s);
+  }
+  void stop(int id) {
+    if (t && t->stop[id]) cudaEventRecord(static_cast<cudaEvent_t>(t->stop[id]), s);
+  }
+};
+
+#define MLA_TRY(expr)                            \
+  do {                                           \
+    cudaError_t e_ = (expr);                     \
+    if (e_ != cudaSuccess) return MLA_ERR_CUDA;  \
+  } while (0)
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+// Projection front end shared by the three entry points: input RMSNorm, RoPE
+// table, A-projection, latent split (+ optional latent cache), q_b + RoPE.
+int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok, int n_pos, int pos0,
+              int t_mod, int t_off, __nv_bfloat16* ckv_cache, __nv_bfloat16* kpe_cache, int cap, void* ws,
+              const Layout& L, const DevStatusHost& st, int sms, cudaStream_t stream, Stager& sg,
+              int* launches) {
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  sg.start(MLA_STAGE_INPUT_NORM);
+  MLA_TRY(launch_rope_table(at<float2>(ws, L.cs), n_pos, pos0, p.base, stream));
+  MLA_TRY(launch_rmsnorm_rows(xb, static_cast<const __nv_bfloat16*>(w->w_in_norm), at<__nv_bfloat16>(ws, L.xn),
+                              n_tok, p.eps, stream));
+  *launches += 2;
+  sg.stop(MLA_STAGE_INPUT_NORM);
+
+  sg.start(MLA_STAGE_A_PROJ);
+  {
+    GemmShape s{n_tok, 2112, MLA_D, 1, 0, 0, 0, 0, MLA_Q_LORA};
+    GemmOperands op{at<__nv_bfloat16>(ws, L.xn), MLA_D, n_tok,
+                    static_cast<const __nv_bfloat16*>(w->w_q_a), MLA_D, MLA_Q_LORA,
+                    static_cast<const __nv_bfloat16*>(w->w_kv_a), MLA_D, 576, false};
+    EpiArgs ea{};
+    ea.out = at<__nv_bfloat16>(ws, L.ca);
+    ea.ldo = 2112;
+    MLA_TRY(launch_gemm(s, op, Epi::kStoreBf16, ea, st, sms, stream));
+    *launches += 1;
+  }
+  sg.stop(MLA_STAGE_A_PROJ);
+
+  sg.start(MLA_STAGE_LATENT);
+  {
+    LatentArgs la{};
+    la.ca = at<__nv_bfloat16>(ws, L.ca);
+    la.g_qa = static_cast<const __nv_bfloat16*>(w->w_q_a_norm);
+    la.g_kva = static_cast<const __nv_bfloat16*>(w->w_kv_a_norm);
+    la.cs = at<float2>(ws, L.cs);
+    la.cq = at<__nv_bfloat16>(ws, L.cq);
+    la.ckv = at<__nv_bfloat16>(ws, L.ckv);
+    la.kpe = at<__nv_bfloat16>(ws, L.kpe);
+    la.ckv_cache = ckv_cache;
+    la.kpe_cache = kpe_cache;
+    la.rows = n_tok;
+    la.t_mod = t_mod;
+    la.t_off = t_off;
+    la.cap = cap;
+    la.eps = p.eps;
+    MLA_TRY(launch_latent_split(la, stream));
+    *launches += 1;
+  }
+  sg.stop(MLA_STAGE_LATENT);
+
+  sg.start(MLA_STAGE_Q_B);
+  {
+    GemmShape s{n_tok, MLA_HEADS * MLA_QK, MLA_Q_LORA, 1, 0, 0, 0, 0, MLA_HEADS * MLA_QK};
+    GemmOperands op{at<__nv_bfloat16>(ws, L.cq), MLA_Q_LORA, n_tok,
+                    static_cast<const __nv_bfloat16*>(w->w_q_b), MLA_Q_LORA, MLA_HEADS * MLA_QK,
+                    nullptr, 0, 0, false};
+    EpiArgs ea{};
+    ea.out = at<__nv_bfloat16>(ws, L.q);
+    ea.ldo = MLA_HEADS * MLA_QK;
+    ea.cs = at<float2>(ws, L.cs);
+    ea.t_mod = t_mod;
+    MLA_TRY(launch_gemm(s, op, Epi::kQRope, ea, st, sms, stream));
+    *launches += 1;
+  }
+  sg.stop(MLA_STAGE_Q_B);
+  return MLA_OK;
+}
+
+int kv_b_stage(const mla_weights_t* w, int n_tok, int t_mod, int t_off, __nv_bfloat16* kc, __nv_bfloat16* vc,
+               int cap, void* ws, const Layout& L, const DevStatusHost& st, int sms, cudaStream_t stream,
+               int* launches) {
+  GemmShape s{n_tok, MLA_HEADS * 256, MLA_KV_LORA, 1, 0, 0, 0, 0, MLA_HEADS * 256};
+  GemmOperands op{at<__nv_bfloat16>(ws, L.ckv), MLA_KV_LORA, n_tok,
+                  static_cast<const __nv_bfloat16*>(w->w_kv_b), MLA_KV_LORA, MLA_HEADS * 256,
+                  nullptr, 0, 0, false};
+  EpiArgs ea{};
+  ea.kc = kc;
+  ea.vc = vc;
+  ea.kpe = at<__nv_bfloat16>(ws, L.kpe);
+  ea.t_mod = t_mod;
+  ea.t_off = t_off;
+  ea.cap = cap;
+  MLA_TRY(launch_gemm(s, op, Epi::kKVCache, ea, st, sms, stream));
+  *launches += 1;
+  return MLA_OK;
+}
+
+int o_proj_stage(const mla_weights_t* w, const Params& p, const void* x, void* out, int n_tok, void* ws,
+                 const Layout& L, const DevStatusHost& st, int sms, cudaStream_t stream, int* launches) {
+  GemmShape s{n_tok, MLA_D, MLA_HEADS * MLA_V, 1, 0, 0, 0, 0, MLA_D};
+  GemmOperands op{at<__nv_bfloat16>(ws, L.o), MLA_HEADS * MLA_V, n_tok,
+                  static_cast<const __nv_bfloat16*>(w->w_o), MLA_HEADS * MLA_V, MLA_D, nullptr, 0, 0, false};
+  EpiArgs ea{};
+  ea.out = static_cast<__nv_bfloat16*>(out);
+  ea.ldo = MLA_D;
+  ea.x = static_cast<const __nv_bfloat16*>(x);
+  ea.delta = p.delta;
+  MLA_TRY(launch_gemm(s, op, Epi::kResidual, ea, st, sms, stream));
+  *launches += 1;
+  return MLA_OK;
+}
+
+int common_checks(const mla_weights_t* w, const Params& p, const void* x, const void* out, size_t n_tok,
+                  void* ws, size_t ws_bytes, size_t need) {
+  int rc = check_weights(w);
+  if (rc) return rc;
+  if (!x || !out) return MLA_ERR_INVALID_ARG;
+  if (!ws) return MLA_ERR_WORKSPACE;
+  if (!params_ok(p)) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out) || !aligned16(ws)) return MLA_ERR_ALIGNMENT;
+  if (bad_overlap(x, out, n_tok * MLA_D * 2)) return MLA_ERR_INVALID_ARG;
+  if (ws_bytes < need) return MLA_ERR_WORKSPACE;
+  return MLA_OK;
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+size_t mla_workspace_size(int mode, int B, int t_or_p, int cap) {
+  (void)cap;
+  if (B < 1) return 0;
+  if (mode == MLA_MODE_PREFILL) {
+    if (t_or_p < 1 || (int64_t)B * t_or_p > kMaxTokens) return 0;
+  } else if (mode == MLA_MODE_DECODE || mode == MLA_MODE_DECODE_LATENT) {
+    if (t_or_p < 0 || B > kMaxTokens || t_or_p >= (1 << 24)) return 0;
+  } else {
+    return 0;
+  }
+  return make_layout(mode, B, t_or_p, kMaxSmsForSizing).total;
+}
+
+const char* mla_status_string(int s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG: invalid argument";
+    case MLA_ERR_ALIGNMENT: return "MLA_ERR_ALIGNMENT: pointer not 16-byte aligned";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: workspace missing or too small";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: size or mode not supported";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA: CUDA call or kernel launch failed";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a bounded device wait gave up";
+    default: return "unknown MLA status";
+  }
+}
+
+int mla_device_status(const void* workspace, void* stream) {
+  if (!workspace) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
+  return (word & kStatusTimeout) ? MLA_ERR_TIMEOUT : MLA_OK;
+}
+
+int mla_prefill(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int T, void* out,
+                void* k_cache, void* v_cache, void* ckv_cache, void* kpe_cache, int cap, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  const Params p = resolve(params);
+  if (B < 1 || T < 1 || (int64_t)B * T > kMaxTokens) return MLA_ERR_INVALID_ARG;
+  if ((k_cache == nullptr) != (v_cache == nullptr)) return MLA_ERR_INVALID_ARG;
+  if ((ckv_cache == nullptr) != (kpe_cache == nullptr)) return MLA_ERR_INVALID_ARG;
+  if ((k_cache || ckv_cache) && cap < T) return MLA_ERR_INVALID_ARG;
+  for (const void* c : {(const void*)k_cache, (const void*)v_cache, (const void*)ckv_cache, (const void*)kpe_cache})
+    if (c && !aligned16(c)) return MLA_ERR_ALIGNMENT;
+  const size_t n_tok = (size_t)B * T;
+  int rc = common_checks(w, p, x, out, n_tok, workspace, workspace_bytes,
+                         make_layout(MLA_MODE_PREFILL, B, T, kMaxSmsForSizing).total);
+  if (rc) return rc;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return MLA_ERR_CUDA;
+  const Layout L = make_layout(MLA_MODE_PREFILL, B, T, sms);
+
+  cudaStream_t stream_ = static_cast<cudaStream_t>(stream);
+  const DevStatusHost st{at<uint32_t>(workspace, L.status), kDefaultWaitLimitNs};
+  Stager sg{p.timing, stream_};
+  int launches = 0;
+  if (cudaMemsetAsync(st.word, 0, sizeof(uint32_t), stream_) != cudaSuccess) return MLA_ERR_CUDA;
+
+  rc = front_end(w, p, x, (int)n_tok, T, 0, T, 0, static_cast<__nv_bfloat16*>(ckv_cache),
+                 static_cast<__nv_bfloat16*>(kpe_cache), cap, workspace, L, st, sms, stream_, sg, &launches);
+  if (rc) return rc;
+
+  __nv_bfloat16* kc = k_cache ? static_cast<__nv_bfloat16*>(k_cache) : at<__nv_bfloat16>(workspace, L.kscr);
+  __nv_bfloat16* vc = v_cache ? static_cast<__nv_bfloat16*>(v_cache) : at<__nv_bfloat16>(workspace, L.vscr);
+  const int kcap = k_cache ? cap : T;
+  sg.start(MLA_STAGE_KV_B);
+  rc = kv_b_stage(w, (int)n_tok, T, 0, kc, vc, kcap, workspace, L, st, sms, stream_, &launches);
+  if (rc) return rc;
+  sg.stop(MLA_STAGE_KV_B);
+
+  sg.start(MLA_STAGE_ATTN);
+  {
+    PrefillAttnArgs a{at<__nv_bfloat16>(workspace, L.q), kc, vc, at<__nv_bfloat16>(workspace, L.o), B, T, kcap,
+                      p.scale};
+    if (launch_prefill_attention(a, st, sms, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+    launches += 1;
+  }
+  sg.stop(MLA_STAGE_ATTN);
+
+  sg.start(MLA_STAGE_O_PROJ);
+  rc = o_proj_stage(w, p, x, out, (int)n_tok, workspace, L, st, sms, stream_, &launches);
+  if (rc) return rc;
+  sg.stop(MLA_STAGE_O_PROJ);
+  if (p.timing) p.timing->n_launches = launches;
+  return MLA_OK;
+}
+
+int mla_decode(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int P, void* k_cache,
+               void* v_cache, int cap, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  const Params p = resolve(params);
+  if (B < 1 || B > kMaxTokens || P < 0 || P >= (1 << 24)) return MLA_ERR_INVALID_ARG;
+  if (!k_cache || !v_cache || cap < P + 1) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return MLA_ERR_ALIGNMENT;
+  int rc = common_checks(w, p, x, out, (size_t)B, workspace, workspace_bytes,
+                         make_layout(MLA_MODE_DECODE, B, P, kMaxSmsForSizing).total);
+  if (rc) return rc;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return MLA_ERR_CUDA;
+  const Layout L = make_layout(MLA_MODE_DECODE, B, P, sms);
+
+  cudaStream_t stream_ = static_cast<cudaStream_t>(stream);
+  const DevStatusHost st{at<uint32_t>(workspace, L.status), kDefaultWaitLimitNs};
+  Stager sg{p.timing, stream_};
+  int launches = 0;
+  if (cudaMemsetAsync(st.word, 0, sizeof(uint32_t), stream_) != cudaSuccess) return MLA_ERR_CUDA;
+  rc = front_end(w, p, x, B, 1, P, 1, P, nullptr, nullptr, cap, workspace, L, st, sms, stream_, sg, &launches);
+  if (rc) return rc;
+
+  __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(k_cache);
+  __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(v_cache);
+  sg.start(MLA_STAGE_KV_B);
+  rc = kv_b_stage(w, B, 1, P, kc, vc, cap, workspace, L, st, sms, stream_, &launches);
+  if (rc) return rc;
+  sg.stop(MLA_STAGE_KV_B);
+
+  sg.start(MLA_STAGE_ATTN);
+  {
+    DecodeAttnArgs a{};
+    a.q = at<__nv_bfloat16>(workspace, L.q);
+    a.k = kc;
+    a.v = vc;
+    a.o = at<__nv_bfloat16>(workspace, L.o);
+    a.part_o = at<float>(workspace, L.part_o);
+    a.part_ml = at<float2>(workspace, L.part_ml);
+    a.B = B;
+    a.L = P + 1;
+    a.cap = cap;
+    a.splits = decode_splits(B, P + 1, sms);
+    a.scale = p.scale;
+    if (launch_decode_attention(a, st, stream_, &launches) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  sg.stop(MLA_STAGE_ATTN);
+
+  sg.start(MLA_STAGE_O_PROJ);
+  rc = o_proj_stage(w, p, x, out, B, workspace, L, st, sms, stream_, &launches);
+  if (rc) return rc;
+  sg.stop(MLA_STAGE_O_PROJ);
+  if (p.timing) p.timing->n_launches = launches;
+  return MLA_OK;
+}
+
+int mla_decode_latent(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int P,
+                      void* ckv_cache, void* kpe_cache, int cap, void* out, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  const Params p = resolve(params);
+  if (B < 1 || B > kMaxTokens || P < 0 || P >= (1 << 24)) return MLA_ERR_INVALID_ARG;
+  if (!ckv_cache || !kpe_cache || cap < P + 1) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(ckv_cache) || !aligned16(kpe_cache)) return MLA_ERR_ALIGNMENT;
+  int rc = common_checks(w, p, x, out, (size_t)B, workspace, workspace_bytes,
+                         make_layout(MLA_MODE_DECODE_LATENT, B, P, kMaxSmsForSizing).total);
+  if (rc) return rc;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return MLA_ERR_CUDA;
+  const Layout L = make_layout(MLA_MODE_DECODE_LATENT, B, P, sms);
+
+  cudaStream_t stream_ = static_cast<cudaStream_t>(stream);
+  const DevStatusHost st{at<uint32_t>(workspace, L.status), kDefaultWaitLimitNs};
+  Stager sg{p.timing, stream_};
+  int launches = 0;
+  if (cudaMemsetAsync(st.word, 0, sizeof(uint32_t), stream_) != cudaSuccess) return MLA_ERR_CUDA;
+  rc = front_end(w, p, x, B, 1, P, 1, P, static_cast<__nv_bfloat16*>(ckv_cache),
+                 static_cast<__nv_bfloat16*>(kpe_cache), cap, workspace, L, st, sms, stream_, sg, &launches);
+  if (rc) return rc;
+
+  const __nv_bfloat16* wkvb = static_cast<const __nv_bfloat16*>(w->w_kv_b);
+  sg.start(MLA_STAGE_ABSORB_Q);
+  {
+    // q_lat[b, h, 0:512] = sum_i q_nope[b, h, i] W_kv_b[h*256 + i, :]  (B operand [K=i, N=c], N contiguous)
+    GemmShape s{B, MLA_KV_LORA, MLA_QK_NOPE, MLA_HEADS, 0, MLA_QK, 0, 256, MLA_KV_LORA};
+    GemmOperands op{at<__nv_bfloat16>(workspace, L.q), MLA_HEADS * MLA_QK, B, wkvb, MLA_KV_LORA, MLA_HEADS * 256,
+                    nullptr, 0, 0, true};
+    EpiArgs ea{};
+    ea.out = at<__nv_bfloat16>(workspace, L.qlat);
+    ea.ldo = MLA_HEADS * 576;
+    ea.c_col0 = 0;
+    ea.c_col_step = 576;
+    MLA_TRY(launch_gemm(s, op, Epi::kStoreBf16, ea, st, sms, stream_));
+    MLA_TRY(launch_copy_qpe(at<__nv_bfloat16>(workspace, L.q), at<__nv_bfloat16>(workspace, L.qlat), B, stream_));
+    launches += 2;
+  }
+  sg.stop(MLA_STAGE_ABSORB_Q);
+
+  sg.start(MLA_STAGE_ATTN);
+  {
+    LatentAttnArgs a{};
+    a.qlat = at<__nv_bfloat16>(workspace, L.qlat);
+    a.ckv = static_cast<const __nv_bfloat16*>(ckv_cache);
+    a.kpe = static_cast<const __nv_bfloat16*>(kpe_cache);
+    a.olat = at<__nv_bfloat16>(workspace, L.olat);
+    a.part_o = at<float>(workspace, L.part_o);
+    a.part_ml = at<float2>(workspace, L.part_ml);
+    a.B = B;
+    a.L = P + 1;
+    a.cap = cap;
+    a.splits = latent_splits(B, P + 1, sms);
+    a.scale = p.scale;
+    if (launch_latent_attention(a, st, stream_, &launches) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  sg.stop(MLA_STAGE_ATTN);
+
+  sg.start(MLA_STAGE_ABSORB_O);
+  {
+    // o[b, h*128 + d] = sum_c o_lat[b, h, c] W_kv_b[h*256 + 128 + d, c]
+    GemmShape s{B, MLA_V, MLA_KV_LORA, MLA_HEADS, 0, MLA_KV_LORA, 128, 256, MLA_V};
+    GemmOperands op{at<__nv_bfloat16>(workspace, L.olat), MLA_HEADS * MLA_KV_LORA, B, wkvb, MLA_KV_LORA,
+                    MLA_HEADS * 256, nullptr, 0, 0, false};
+    EpiArgs ea{};
+    ea.out = at<__nv_bfloat16>(workspace, L.o);
+    ea.ldo = MLA_HEADS * MLA_V;
+    ea.c_col0 = 0;
+    ea.c_col_step = MLA_V;
+    MLA_TRY(launch_gemm(s, op, Epi::kStoreBf16, ea, st, sms, stream_));
+    launches += 1;
+  }
+  sg.stop(MLA_STAGE_ABSORB_O);
+
+  sg.start(MLA_STAGE_O_PROJ);
+  rc = o_proj_stage(w, p, x, out, B, workspace, L, st, sms, stream_, &launches);
+  if (rc) return rc;
+  sg.stop(MLA_STAGE_O_PROJ);
+  if (p.timing) p.timing->n_launches = launches;
+  return MLA_OK;
+}
+
+}  // extern "C"

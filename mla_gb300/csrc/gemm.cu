@@ -1,0 +1,413 @@
+// Persistent tcgen05 GEMM for the MLA projections, sm_103a.
+//
+// D[m, n] = sum_k A[m, k] B[n, k] with bf16 operands staged by TMA (128-byte
+// swizzle) and an f32 accumulator in tensor memory; the epilogue reads the
+// accumulator with tcgen05.ld and applies the step-specific output transform:
+//   kStoreBf16  plain bf16 store (A-projection, latent absorption)
+//   kQRope      q_b_proj: one head (192 columns) per tile, RoPE on the 64
+//               "pe" columns (dense-block page: Q^R_t = RoPE(Q^pe_t, R_t))
+//   kKVCache    kv_b_proj: one head (256 columns) per tile, writes k_nope and
+//               v into the per-head caches and appends the shared rotary key
+//               (dense-block page: K_i = [K^C_i ; k^R])
+//   kResidual   o_proj: out = x + Delta_attn, one bf16 rounding
+//
+// Warp roles (192 threads): warp 0 issues TMA loads into a STAGES-deep ring,
+// warp 1 allocates tensor memory and one lane issues the MMAs, warps 2..5 run
+// the epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).  The accumulator is
+// double buffered in TMEM so the epilogue of one tile overlaps the main loop
+// of the next.  Every wait is bounded (see common.cuh).
+#include "common.cuh"
+#include "internal.h"
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace mla {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+
+__host__ __device__ constexpr uint32_t pow2_cols(uint32_t n) {
+  return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512;
+}
+
+template <int BN, int STAGES>
+struct GemmSmem {
+  static constexpr uint32_t kA = kBM * kBK * 2;
+  static constexpr uint32_t kB = BN * kBK * 2;
+  static constexpr uint32_t kStage = kA + kB;
+  static constexpr uint32_t kBarOff = STAGES * kStage;
+  static constexpr uint32_t kBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
+};
+
+__device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const uint32_t (&r)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    d[j] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1])),
+                      pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
+                      pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
+                      pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7])));
+  }
+}
+
+template <int BN, Epi EPI>
+__device__ __forceinline__ void run_epilogue(const EpiArgs& ea, uint32_t taddr, int batch, int row, int n0,
+                                             bool row_ok) {
+  if constexpr (EPI == Epi::kStoreBf16) {
+    __nv_bfloat16* dst = ea.out + (size_t)row * ea.ldo + ea.c_col0 + batch * ea.c_col_step + n0;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c, r);
+      tmem_wait_ld();
+      if (row_ok) store32_bf16(dst + c, r);
+    }
+  } else if constexpr (EPI == Epi::kQRope) {
+    static_assert(BN == 192, "q_b epilogue works on one 192-wide head per tile");
+    __nv_bfloat16* dst = ea.out + (size_t)row * ea.ldo + n0;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c, r);
+      tmem_wait_ld();
+      if (row_ok) store32_bf16(dst + c, r);
+    }
+    uint32_t x1[32], x2[32];
+    tmem_ld32(taddr + 128, x1);
+    tmem_ld32(taddr + 160, x2);
+    tmem_wait_ld();
+    if (row_ok) {
+      const float2* cs = ea.cs + (size_t)(row % ea.t_mod) * 32;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float2 t = cs[i];
+        float a = __uint_as_float(x1[i]), b = __uint_as_float(x2[i]);
+        x1[i] = __float_as_uint(a * t.x - b * t.y);
+        x2[i] = __float_as_uint(b * t.x + a * t.y);
+      }
+      store32_bf16(dst + 128, x1);
+      store32_bf16(dst + 160, x2);
+    }
+  } else if constexpr (EPI == Epi::kKVCache) {
+    static_assert(BN == 256, "kv_b epilogue works on one 256-wide head per tile");
+    const int h = n0 / 256;
+    const int b = row_ok ? row / ea.t_mod : 0;
+    const int t = ea.t_off + (row_ok ? row % ea.t_mod : 0);
+    const size_t slot = ((size_t)b * 64 + h) * ea.cap + t;
+    __nv_bfloat16* krow = ea.kc + slot * 192;
+    __nv_bfloat16* vrow = ea.vc + slot * 128;
+#pragma unroll 1
+    for (int c = 0; c < 256; c += 32) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c, r);
+      tmem_wait_ld();
+      if (row_ok) store32_bf16(c < 128 ? krow + c : vrow + (c - 128), r);
+    }
+    if (row_ok) {
+      const uint4* src = reinterpret_cast<const uint4*>(ea.kpe + (size_t)row * 64);
+      uint4* dst = reinterpret_cast<uint4*>(krow + 128);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) dst[j] = src[j];
+    }
+  } else {  // kResidual
+    const size_t base = (size_t)row * ea.ldo + n0;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c, r);
+      tmem_wait_ld();
+      if (row_ok) {
+        if (ea.delta) {
+          float4* dd = reinterpret_cast<float4*>(ea.delta + base + c);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dd[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+        const uint4* xs = reinterpret_cast<const uint4*>(ea.x + base + c);
+        uint32_t o[32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint4 xv = xs[j];
+          uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float2 xf = unpack_bf16x2(xw[q]);
+            o[8 * j + 2 * q] = __float_as_uint(xf.x + __uint_as_float(r[8 * j + 2 * q]));
+            o[8 * j + 2 * q + 1] = __float_as_uint(xf.y + __uint_as_float(r[8 * j + 2 * q + 1]));
+          }
+        }
+        store32_bf16(ea.out + base + c, o);
+      }
+    }
+  }
+}
+
+template <int BN, int STAGES, Epi EPI, bool B_MN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                const __grid_constant__ CUtensorMap tmB1, const GemmShape s, const EpiArgs ea,
+                const DevStatus st) {
+  using L = GemmSmem<BN, STAGES>;
+  constexpr uint32_t kTmemCols = pow2_cols(2 * BN);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* empty_bar = full_bar + STAGES;
+  uint64_t* tfull_bar = empty_bar + STAGES;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* drain_bar = tempty_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m_tiles = (s.M + kBM - 1) / kBM;
+  const int n_tiles = s.N / BN;
+  const int num_tiles = s.batches * m_tiles * n_tiles;
+  const int kblocks = s.K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull_bar[i], 1);
+      mbar_init(&tempty_bar[i], 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB0);
+    if (s.n_split < s.N) tma_prefetch_desc(&tmB1);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued[STAGES];
+#pragma unroll
+      for (int i = 0; i < STAGES; ++i) issued[i] = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int n_blk = tile % n_tiles;
+        const int m_blk = (tile / n_tiles) % m_tiles;
+        const int batch = tile / (n_tiles * m_tiles);
+        const int n0 = n_blk * BN;
+        const int a_col = s.a_col0 + batch * s.a_col_step;
+        const int b_row = s.b_row0 + batch * s.b_row_step;
+        const CUtensorMap* mb = (n0 < s.n_split) ? &tmB0 : &tmB1;
+        const int nb = (n0 < s.n_split) ? n0 : n0 - s.n_split;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1, st, abort_flag, 1)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * L::kStage;
+          uint8_t* sb = sa + L::kA;
+          mbar_arrive_expect_tx(&full_bar[stage], L::kStage);
+          tma_load_2d(sa, &tmA, &full_bar[stage], a_col + kb * kBK, m_blk * kBM);
+          if constexpr (B_MN) {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(sb + j * (64 * 128), mb, &full_bar[stage], nb + j * 64, b_row + kb * kBK);
+          } else {
+            tma_load_2d(sb, mb, &full_bar[stage], kb * kBK, b_row + nb);
+          }
+          issued[stage]++;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // make sure no copy into this CTA's shared memory is still in flight
+#pragma unroll
+      for (int i = 0; i < STAGES; ++i)
+        if (issued[i]) mbar_wait(&full_bar[i], (issued[i] - 1) & 1, st, nullptr, 2);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t idesc = idesc_bf16(kBM, BN, false, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, st, abort_flag, 3)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, st, abort_flag, 4)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * L::kStage);
+          const uint32_t b_addr = a_addr + L::kA;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t adesc = sdesc_sw128(a_addr + k * 32, 16, 1024);
+            uint64_t bdesc;
+            if constexpr (B_MN)
+              bdesc = sdesc_sw128(b_addr + k * 2048, 64 * 128, 1024);
+            else
+              bdesc = sdesc_sw128(b_addr + k * 32, 16, 1024);
+            umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty_bar[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull_bar[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      // all MMAs issued by this thread have finished before TMEM is freed
+      umma_commit(drain_bar);
+      mbar_wait(drain_bar, 0, st, nullptr, 5);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int quarter = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int n_blk = tile % n_tiles;
+      const int m_blk = (tile / n_tiles) % m_tiles;
+      const int batch = tile / (n_tiles * m_tiles);
+      bool ok = mbar_wait(&tfull_bar[acc], acc_phase, st, abort_flag, 6);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const int row = m_blk * kBM + quarter * 32 + lane;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+      run_epilogue<BN, EPI>(ea, taddr, batch, row, n_blk * BN, row < s.M);
+      tc_fence_before();
+      mbar_arrive(&tempty_bar[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int BN, int STAGES, Epi EPI, bool B_MN>
+cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArgs& ea, const DevStatusHost& st,
+                        int num_sms, cudaStream_t stream) {
+  using L = GemmSmem<BN, STAGES>;
+  CUtensorMap ta, tb0, tb1;
+  if (!make_tmap_bf16_2d(&ta, op.A, op.a_rows, (uint64_t)op.lda, op.lda, kBM, kBK))
+    return cudaErrorInvalidValue;
+  if (B_MN) {
+    if (!make_tmap_bf16_2d(&tb0, op.B0, op.b0_rows, op.ldb0, op.ldb0, 64, 64)) return cudaErrorInvalidValue;
+  } else {
+    if (!make_tmap_bf16_2d(&tb0, op.B0, op.b0_rows, op.ldb0, op.ldb0, BN, kBK)) return cudaErrorInvalidValue;
+  }
+  tb1 = tb0;
+  if (op.B1 && !make_tmap_bf16_2d(&tb1, op.B1, op.b1_rows, op.ldb1, op.ldb1, BN, kBK))
+    return cudaErrorInvalidValue;
+  auto kern = gemm_kernel<BN, STAGES, EPI, B_MN>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const int tiles = s.batches * ((s.M + kBM - 1) / kBM) * (s.N / BN);
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  DevStatus dst{st.word, st.wait_limit_ns};
+  kern<<<grid, kThreads, L::kBytes, stream>>>(ta, tb0, tb1, s, ea, dst);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, const EpiArgs& ea,
+                        const DevStatusHost& st, int num_sms, cudaStream_t stream) {
+  if (s.M <= 0 || s.K % kBK != 0 || s.batches <= 0) return cudaErrorInvalidValue;
+  switch (epi) {
+    case Epi::kQRope:
+      if (s.N % 192 || op.b_mn_major) return cudaErrorInvalidValue;
+      return launch_impl<192, 5, Epi::kQRope, false>(s, op, ea, st, num_sms, stream);
+    case Epi::kKVCache:
+      if (s.N % 256 || op.b_mn_major) return cudaErrorInvalidValue;
+      return launch_impl<256, 4, Epi::kKVCache, false>(s, op, ea, st, num_sms, stream);
+    case Epi::kResidual:
+      if (s.N % 256 || op.b_mn_major) return cudaErrorInvalidValue;
+      return launch_impl<256, 4, Epi::kResidual, false>(s, op, ea, st, num_sms, stream);
+    case Epi::kStoreBf16:
+    default:
+      if (op.b_mn_major) {
+        if (s.N % 128) return cudaErrorInvalidValue;
+        return launch_impl<128, 6, Epi::kStoreBf16, true>(s, op, ea, st, num_sms, stream);
+      }
+      if (s.N % 192 == 0 && s.n_split % 192 == 0)
+        return launch_impl<192, 5, Epi::kStoreBf16, false>(s, op, ea, st, num_sms, stream);
+      if (s.N % 128 == 0 && s.n_split % 128 == 0)
+        return launch_impl<128, 6, Epi::kStoreBf16, false>(s, op, ea, st, num_sms, stream);
+      return cudaErrorInvalidValue;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// tensor maps (driver entry point looked up once through the runtime)
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                       uint32_t box_rows, uint32_t box_cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace mla

@@ -1,0 +1,142 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mla {
+
+struct DevStatusHost {
+  uint32_t* word;
+  uint64_t wait_limit_ns;
+};
+
+// ---- tensor maps ------------------------------------------------------------
+// 2D bf16 tensor map over a row-major [rows, cols] matrix with row stride
+// `ld` elements, box {box_cols, box_rows}, 128-byte swizzle (box_cols * 2
+// must be 128).  Returns false if the driver rejects it.
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                       uint32_t box_rows, uint32_t box_cols);
+
+// ---- GEMM (tcgen05, TMA, persistent) --------------------------------------
+// D[b][m, n] = sum_k A[m, a_col0 + b*a_col_step + k] * Bmat(b)[n, k]
+// A is K-major.  B is either K-major ([N, K] rows, weight layout) taken from
+// B0 for n < n_split and from B1 (rows n - n_split) otherwise, or MN-major
+// ([K, N] rows, N contiguous).  Row offset b_row0 + b*b_row_step selects the
+// batch's slice of B (along N for K-major, along K for MN-major).
+struct GemmShape {
+  int M, N, K;
+  int batches;
+  int a_col0, a_col_step;
+  int b_row0, b_row_step;
+  int n_split;
+};
+
+struct GemmOperands {
+  const __nv_bfloat16* A;
+  int lda;
+  int a_rows;  // rows of the A tensor (>= M)
+  const __nv_bfloat16* B0;
+  int ldb0;
+  int b0_rows;
+  const __nv_bfloat16* B1;  // may be null
+  int ldb1;
+  int b1_rows;
+  bool b_mn_major;
+};
+
+enum class Epi { kStoreBf16, kQRope, kKVCache, kResidual };
+
+struct EpiArgs {
+  // kStoreBf16: out[row, c_col0 + batch*c_col_step + n]
+  __nv_bfloat16* out;
+  int ldo;
+  int c_col0, c_col_step;
+  // kQRope: q[row, n] with RoPE on columns 128..191 of each 192 block;
+  //         position index of a row = row % t_mod into cs (float2 [.., 32])
+  const float2* cs;
+  int t_mod;
+  // kKVCache: K[b, h, t, 0:128] / V[b, h, t, 0:128] / K[b, h, t, 128:192] = kpe[row]
+  //           b = row / t_mod, t = t_off + row % t_mod
+  __nv_bfloat16* kc;
+  __nv_bfloat16* vc;
+  const __nv_bfloat16* kpe;
+  int t_off;
+  int cap;
+  // kResidual: out[row, n] = x[row, n] + acc; delta[row, n] = acc (optional)
+  const __nv_bfloat16* x;
+  float* delta;
+};
+
+cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, const EpiArgs& ea,
+                        const DevStatusHost& st, int num_sms, cudaStream_t stream);
+
+// ---- row kernels --------------------------------------------------------------
+cudaError_t launch_rope_table(float2* cs, int n_pos, int pos0, float base, cudaStream_t stream);
+cudaError_t launch_rmsnorm_rows(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_bfloat16* y, int rows,
+                                float eps, cudaStream_t stream);
+// Split the A-projection output ca [rows, 2112] into RMSNorm(c^Q) [rows,1536],
+// RMSNorm(c^KV) [rows,512] and RoPE(k_pe) [rows,64]; optional latent cache
+// copies at ckv_cache[b, t_off + t] / kpe_cache[b, t_off + t].
+struct LatentArgs {
+  const __nv_bfloat16* ca;
+  const __nv_bfloat16* g_qa;
+  const __nv_bfloat16* g_kva;
+  const float2* cs;
+  __nv_bfloat16* cq;
+  __nv_bfloat16* ckv;
+  __nv_bfloat16* kpe;
+  __nv_bfloat16* ckv_cache;
+  __nv_bfloat16* kpe_cache;
+  int rows, t_mod, t_off, cap;
+  float eps;
+};
+cudaError_t launch_latent_split(const LatentArgs& a, cudaStream_t stream);
+
+// ---- attention ----------------------------------------------------------------
+struct PrefillAttnArgs {
+  const __nv_bfloat16* q;   // [B*T, 64*192]
+  const __nv_bfloat16* k;   // [B, 64, cap, 192]
+  const __nv_bfloat16* v;   // [B, 64, cap, 128]
+  __nv_bfloat16* o;         // [B*T, 64*128]
+  int B, T, cap;
+  float scale;
+};
+cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, const DevStatusHost& st, int num_sms,
+                                     cudaStream_t stream);
+
+struct DecodeAttnArgs {
+  const __nv_bfloat16* q;   // [B, 64*192]
+  const __nv_bfloat16* k;   // [B, 64, cap, 192]
+  const __nv_bfloat16* v;   // [B, 64, cap, 128]
+  __nv_bfloat16* o;         // [B, 64*128]
+  float* part_o;            // [B*64*splits, 128] split partials
+  float2* part_ml;          // [B*64*splits] (max, sum)
+  int B, L, cap, splits;    // L = keys attended (P + 1)
+  float scale;
+};
+int decode_splits(int B, int L, int num_sms);
+cudaError_t launch_decode_attention(const DecodeAttnArgs& a, const DevStatusHost& st, cudaStream_t stream,
+                                    int* launches);
+
+struct LatentAttnArgs {
+  const __nv_bfloat16* qlat;  // [B, 64, 576] (absorbed q_nope | rotated q_pe)
+  const __nv_bfloat16* ckv;   // [B, cap, 512]
+  const __nv_bfloat16* kpe;   // [B, cap, 64]
+  __nv_bfloat16* olat;        // [B, 64, 512]
+  float* part_o;              // [B*splits, 64, 512]
+  float2* part_ml;            // [B*splits, 64]
+  int B, L, cap, splits;
+  float scale;
+};
+int latent_splits(int B, int L, int num_sms);
+cudaError_t launch_latent_attention(const LatentAttnArgs& a, const DevStatusHost& st, cudaStream_t stream,
+                                    int* launches);
+
+// qlat[b, h, 512:576] = q[b, h*192 + 128 : h*192 + 192]
+cudaError_t launch_copy_qpe(const __nv_bfloat16* q, __nv_bfloat16* qlat, int B, cudaStream_t stream);
+
+}  // namespace mla

@@ -1,0 +1,206 @@
+// Row-wise kernels of the MLA path (HBM-bound, one pass over each row):
+//   * RoPE table R_t: (cos, sin)(t * theta_i), theta_i = base^(-2i/64), the
+//     angle formed in double precision so that positions up to 2^20 keep
+//     full float accuracy (dense-block page: "R [T positions, 32 pairs]");
+//   * input RMSNorm x_attn = g * x / sqrt(mean(x^2) + eps) (dense-block page,
+//     first equation), float32 math, one bf16 rounding;
+//   * split of the A-projection output into c^Q, c^KV and k^pe, with the
+//     q_a / kv_a latent RMSNorms and RoPE on the shared rotary key
+//     (key-value compression page: split after the product, only the
+//     512-wide latent normalised), plus the optional latent-cache write.
+#include "common.cuh"
+#include "internal.h"
+
+namespace mla {
+
+namespace {
+
+__global__ void rope_table_kernel(float2* __restrict__ cs, int n_pos, int pos0, double base) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n_pos * 32) return;
+  const int t = idx >> 5;
+  const int i = idx & 31;
+  const double theta = pow(base, -2.0 * (double)i / 64.0);
+  double s, c;
+  sincos((double)(pos0 + t) * theta, &s, &c);
+  cs[idx] = make_float2((float)c, (float)s);
+}
+
+// One CTA of 128 threads per row of 7168 (= 128 threads x 7 uint4).
+__global__ void __launch_bounds__(128) rmsnorm_7168_kernel(const __nv_bfloat16* __restrict__ x,
+                                                           const __nv_bfloat16* __restrict__ g,
+                                                           __nv_bfloat16* __restrict__ y, float eps) {
+  constexpr int kVec = 7;  // 7168 / 8 / 128
+  const size_t row = blockIdx.x;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + row * 7168);
+  uint4 v[kVec];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < kVec; ++j) {
+    v[j] = xr[threadIdx.x + j * 128];
+    const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float2 f = unpack_bf16x2(w[q]);
+      ss += f.x * f.x + f.y * f.y;
+    }
+  }
+  __shared__ float red[4];
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  const float tot = red[0] + red[1] + red[2] + red[3];
+  const float rstd = rsqrtf(tot * (1.0f / 7168.0f) + eps);
+  const uint4* gr = reinterpret_cast<const uint4*>(g);
+  uint4* yr = reinterpret_cast<uint4*>(y + row * 7168);
+#pragma unroll
+  for (int j = 0; j < kVec; ++j) {
+    const uint4 gv = gr[threadIdx.x + j * 128];
+    const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float2 f = unpack_bf16x2(w[q]);
+      float2 gg = unpack_bf16x2(gw[q]);
+      o[q] = pack_bf16x2(gg.x * (f.x * rstd), gg.y * (f.y * rstd));
+    }
+    yr[threadIdx.x + j * 128] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// One warp per row of ca [rows, 2112] = [c^Q 1536 | c^KV 512 | k^pe 64].
+__global__ void __launch_bounds__(256) latent_split_kernel(const LatentArgs a) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= a.rows) return;
+  const size_t row = warp;
+  const uint4* src = reinterpret_cast<const uint4*>(a.ca + row * 2112);
+
+  // c^Q: 1536 = 192 uint4, 6 per lane
+  {
+    uint4 v[6];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 6; ++j) {
+      v[j] = src[lane + 32 * j];
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float2 f = unpack_bf16x2(w[q]);
+        ss += f.x * f.x + f.y * f.y;
+      }
+    }
+    const float rstd = rsqrtf(warp_sum(ss) * (1.0f / 1536.0f) + a.eps);
+    const uint4* g = reinterpret_cast<const uint4*>(a.g_qa);
+    uint4* dst = reinterpret_cast<uint4*>(a.cq + row * 1536);
+#pragma unroll
+    for (int j = 0; j < 6; ++j) {
+      const uint4 gv = g[lane + 32 * j];
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+      const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float2 f = unpack_bf16x2(w[q]);
+        float2 gg = unpack_bf16x2(gw[q]);
+        o[q] = pack_bf16x2(gg.x * (f.x * rstd), gg.y * (f.y * rstd));
+      }
+      dst[lane + 32 * j] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+  const int b = (int)(row / a.t_mod);
+  const int t = a.t_off + (int)(row % a.t_mod);
+  // c^KV: 512 = 64 uint4, 2 per lane (uint4 index 192 .. 255)
+  {
+    uint4 v[2];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      v[j] = src[192 + lane + 32 * j];
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float2 f = unpack_bf16x2(w[q]);
+        ss += f.x * f.x + f.y * f.y;
+      }
+    }
+    const float rstd = rsqrtf(warp_sum(ss) * (1.0f / 512.0f) + a.eps);
+    const uint4* g = reinterpret_cast<const uint4*>(a.g_kva);
+    uint4* dst = reinterpret_cast<uint4*>(a.ckv + row * 512);
+    uint4* dcache = a.ckv_cache ? reinterpret_cast<uint4*>(a.ckv_cache + ((size_t)b * a.cap + t) * 512) : nullptr;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint4 gv = g[lane + 32 * j];
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+      const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float2 f = unpack_bf16x2(w[q]);
+        float2 gg = unpack_bf16x2(gw[q]);
+        o[q] = pack_bf16x2(gg.x * (f.x * rstd), gg.y * (f.y * rstd));
+      }
+      const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[lane + 32 * j] = ov;
+      if (dcache) dcache[lane + 32 * j] = ov;
+    }
+  }
+  // k^pe: 64 values, lane i rotates pair (i, i + 32) at position t
+  {
+    const __nv_bfloat16* kp = a.ca + row * 2112 + 2048;
+    const float x1 = __bfloat162float(kp[lane]);
+    const float x2 = __bfloat162float(kp[lane + 32]);
+    const float2 cs = a.cs[(size_t)(row % a.t_mod) * 32 + lane];
+    const __nv_bfloat16 y1 = __float2bfloat16_rn(x1 * cs.x - x2 * cs.y);
+    const __nv_bfloat16 y2 = __float2bfloat16_rn(x2 * cs.x + x1 * cs.y);
+    __nv_bfloat16* d = a.kpe + row * 64;
+    d[lane] = y1;
+    d[lane + 32] = y2;
+    if (a.kpe_cache) {
+      __nv_bfloat16* dc = a.kpe_cache + ((size_t)b * a.cap + t) * 64;
+      dc[lane] = y1;
+      dc[lane + 32] = y2;
+    }
+  }
+}
+
+__global__ void copy_qpe_kernel(const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ qlat, int B) {
+  // one thread per (b, h, 16-byte chunk of the 64 pe values): 8 chunks
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= B * 64 * 8) return;
+  const int c = idx & 7;
+  const int bh = idx >> 3;
+  const int b = bh >> 6, h = bh & 63;
+  const uint4* s = reinterpret_cast<const uint4*>(q + (size_t)b * 12288 + h * 192 + 128);
+  uint4* d = reinterpret_cast<uint4*>(qlat + ((size_t)b * 64 + h) * 576 + 512);
+  d[c] = s[c];
+}
+
+}  // namespace
+
+cudaError_t launch_rope_table(float2* cs, int n_pos, int pos0, float base, cudaStream_t stream) {
+  const int n = n_pos * 32;
+  rope_table_kernel<<<(n + 255) / 256, 256, 0, stream>>>(cs, n_pos, pos0, (double)base);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_rows(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_bfloat16* y, int rows,
+                                float eps, cudaStream_t stream) {
+  rmsnorm_7168_kernel<<<rows, 128, 0, stream>>>(x, g, y, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_latent_split(const LatentArgs& a, cudaStream_t stream) {
+  const int warps_per_block = 8;
+  latent_split_kernel<<<(a.rows + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_qpe(const __nv_bfloat16* q, __nv_bfloat16* qlat, int B, cudaStream_t stream) {
+  const int n = B * 64 * 8;
+  copy_qpe_kernel<<<(n + 255) / 256, 256, 0, stream>>>(q, qlat, B);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

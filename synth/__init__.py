@@ -38,23 +38,46 @@ _M2 = 0x94D049BB133111EB
 _ZSCALE = float.fromhex("0x1.bb67ae8584caap-16")
 
 STREAMS = {
-    "x": 0,          # prefill input hidden states
-    "g_in": 1,       # input RMSNorm gain
+    "x": 0,            # prefill input hidden states
+    "w_in_norm": 1,    # input RMSNorm gain
     "w_q_a": 2,
-    "g_qa": 3,
+    "w_q_a_norm": 3,
     "w_q_b": 4,
     "w_kv_a": 5,
-    "g_kva": 6,
+    "w_kv_a_norm": 6,
     "w_kv_b": 7,
     "w_o": 8,
-    "cache_x": 9,    # hidden states whose projections fill a decode cache
-    "new_x": 10,     # the new token's hidden state in decode
+    "cache_x": 9,      # hidden states whose projections fill a decode cache
+    "new_x": 10,       # the new token's hidden state in decode
 }
 
 # Distributions of the synthetic workload: (mean, std)
 WEIGHT_DIST = (0.0, 0.02)
 GAIN_DIST = (1.0, 0.1)
 X_DIST = (0.0, 1.0)
+
+# The eight weight tensors of one MLA sublayer (nn.Linear [out, in]) and the
+# distribution each is drawn from.
+WEIGHT_SPECS = {
+    "w_in_norm": ((7168,), GAIN_DIST),
+    "w_q_a": ((1536, 7168), WEIGHT_DIST),
+    "w_q_a_norm": ((1536,), GAIN_DIST),
+    "w_q_b": ((12288, 1536), WEIGHT_DIST),
+    "w_kv_a": ((576, 7168), WEIGHT_DIST),
+    "w_kv_a_norm": ((512,), GAIN_DIST),
+    "w_kv_b": ((16384, 512), WEIGHT_DIST),
+    "w_o": ((7168, 8192), WEIGHT_DIST),
+}
+
+
+def weight_bits(seed: int = 0) -> dict:
+    """bf16 bits of all weights (about 101 M values; a few seconds)."""
+    return {n: tensor_bits(seed, n, shape, dist) for n, (shape, dist) in WEIGHT_SPECS.items()}
+
+
+def weights_cuda(seed: int = 0, device="cuda") -> dict:
+    """The same weights drawn directly on the GPU (bit-identical)."""
+    return {n: tensor_cuda(seed, n, shape, dist, device) for n, (shape, dist) in WEIGHT_SPECS.items()}
 
 
 def _splitmix64(x: np.ndarray) -> np.ndarray:

@@ -1,0 +1,60 @@
+"""Helpers shared by the tests: seeded inputs for both sides, conversions,
+and the parity check (max abs <= 2e-2 and relative Frobenius <= 1e-2)."""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+
+import synth
+
+# library weight name -> oracle weight name
+ORACLE_NAMES = {"w_in_norm": "g_in", "w_q_a": "w_q_a", "w_q_a_norm": "g_qa", "w_q_b": "w_q_b",
+                "w_kv_a": "w_kv_a", "w_kv_a_norm": "g_kva", "w_kv_b": "w_kv_b", "w_o": "w_o"}
+
+MAX_ABS = 2e-2
+REL_FRO = 1e-2
+
+
+@functools.lru_cache(maxsize=2)
+def weight_bits(seed: int = 0) -> dict:
+    return synth.weight_bits(seed)
+
+
+@functools.lru_cache(maxsize=2)
+def oracle_weights(seed: int = 0) -> dict:
+    return {ORACLE_NAMES[n]: synth.bf16_bits_to_f64(b) for n, b in weight_bits(seed).items()}
+
+
+def bits_to_cuda(bits: np.ndarray):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def cuda_to_f64(t) -> np.ndarray:
+    import torch
+    if t.dtype == torch.float32:
+        return t.detach().cpu().numpy().astype(np.float64)
+    return synth.bf16_bits_to_f64(t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16))
+
+
+def f64_to_bits(a: np.ndarray) -> np.ndarray:
+    """Round oracle values to the bf16 storage a cache buffer holds."""
+    return synth.f32_to_bf16_bits(np.asarray(a, dtype=np.float64).astype(np.float32))
+
+
+def cuda_weights(seed: int = 0) -> dict:
+    return {n: bits_to_cuda(b) for n, b in weight_bits(seed).items()}
+
+
+def parity(got: np.ndarray, ref: np.ndarray, what: str, max_abs: float = MAX_ABS, rel_fro: float = REL_FRO):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, f"{what}: shape {got.shape} vs {ref.shape}"
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    d = got - ref
+    ma = float(np.max(np.abs(d))) if d.size else 0.0
+    nr = float(np.linalg.norm(ref))
+    rf = float(np.linalg.norm(d) / nr) if nr > 0 else float(np.linalg.norm(d))
+    assert ma <= max_abs and rf <= rel_fro, f"{what}: max abs {ma:.3e} (<= {max_abs}), rel Frobenius {rf:.3e} (<= {rel_fro})"
+    return ma, rf

@@ -1,0 +1,109 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function the headers declare, sizes workspaces, and rejects bad
+arguments before enqueueing anything (the pages' code raises ValueError /
+asserts on shape mismatches; here they become status codes)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_gb300 as m
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for h in ("mla.h", "mla_debug.h"):
+        src = open(os.path.join(ROOT, "include", h)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s+\*?([a-z_][a-z0-9_]*)\s*\(", src, re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_function():
+    lib = m.lib()
+    names = declared_functions()
+    assert "mla_prefill" in names and "mla_decode_latent" in names and len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+
+
+def test_status_strings():
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert m.STATUS[code] in m.mla_status_string(code)
+
+
+def test_workspace_sizes():
+    p1 = m.workspace_size(m.MODE_PREFILL, 1, 16)
+    p2 = m.workspace_size(m.MODE_PREFILL, 1, 2048)
+    assert 0 < p1 < p2
+    assert m.workspace_size(m.MODE_DECODE, 64, 1000) > 0
+    assert m.workspace_size(m.MODE_DECODE_LATENT, 128, 8192) > 0
+    assert m.lib().mla_workspace_size(m.MODE_PREFILL, 0, 16, 0) == 0
+    assert m.lib().mla_workspace_size(m.MODE_PREFILL, 1, 0, 0) == 0
+    assert m.lib().mla_workspace_size(7, 1, 16, 0) == 0
+    assert m.lib().mla_workspace_size(m.MODE_DECODE, 1, -1, 0) == 0
+
+
+FAKE = 1 << 40  # never dereferenced: every call below fails its host checks
+
+
+def fake_weights(**override):
+    vals = {n: FAKE + 4096 * i for i, n in enumerate(m.WEIGHT_NAMES)}
+    vals.update(override)
+    return m.MlaWeights(*[vals[n] for n in m.WEIGHT_NAMES])
+
+
+def prefill(w, B=1, T=16, x=FAKE + (1 << 30), out=FAKE + (2 << 30), kc=None, vc=None, ckv=None, kpe=None,
+            cap=0, ws=FAKE + (3 << 30), ws_bytes=None, params=None):
+    if ws_bytes is None:
+        ws_bytes = m.lib().mla_workspace_size(m.MODE_PREFILL, max(B, 1), max(T, 1), cap)
+    return m.lib().mla_prefill(ctypes.byref(w), params, x, B, T, out, kc, vc, ckv, kpe, cap, ws, ws_bytes, None)
+
+
+def test_prefill_argument_checks():
+    w = fake_weights()
+    assert prefill(w, B=0) == -1
+    assert prefill(w, T=0) == -1
+    assert prefill(fake_weights(w_o=None)) == -1
+    assert prefill(fake_weights(w_q_b=FAKE + 8)) == -2
+    assert prefill(w, x=FAKE + (1 << 30) + 2) == -2
+    assert prefill(w, ws=None) == -3
+    assert prefill(w, ws_bytes=1024) == -3
+    # out overlapping x without being the same buffer
+    assert prefill(w, out=FAKE + (1 << 30) + 4096) == -1
+    # only one of a cache pair, or a cache smaller than T
+    assert prefill(w, kc=FAKE + (4 << 30)) == -1
+    assert prefill(w, ckv=FAKE + (4 << 30)) == -1
+    assert prefill(w, kc=FAKE + (4 << 30), vc=FAKE + (5 << 30), cap=15) == -1
+    bad = m.MlaParams(-1.0, 10000.0, 0.07, None, None)
+    assert prefill(w, params=ctypes.byref(bad)) == -1
+
+
+def test_decode_argument_checks():
+    w = fake_weights()
+    L = m.lib()
+    ws_bytes = L.mla_workspace_size(m.MODE_DECODE, 4, 10, 11)
+    args = dict(x=FAKE + (1 << 30), kc=FAKE + (2 << 30), vc=FAKE + (3 << 30), out=FAKE + (4 << 30),
+                ws=FAKE + (5 << 30))
+
+    def dec(B=4, P=10, cap=11, **kw):
+        a = dict(args, **kw)
+        return L.mla_decode(ctypes.byref(w), None, a["x"], B, P, a["kc"], a["vc"], cap, a["out"], a["ws"],
+                            ws_bytes, None)
+
+    assert dec(B=0) == -1
+    assert dec(P=-1) == -1
+    assert dec(cap=10) == -1            # P + 1 > cap
+    assert dec(kc=None) == -1
+    assert dec(vc=FAKE + 8) == -2
+
+    ws_l = L.mla_workspace_size(m.MODE_DECODE_LATENT, 4, 10, 11)
+    assert L.mla_decode_latent(ctypes.byref(w), None, args["x"], 4, 10, args["kc"], None, 11, args["out"],
+                               args["ws"], ws_l, None) == -1
+    assert L.mla_decode_latent(ctypes.byref(w), None, args["x"], 4, 10, args["kc"], args["vc"], 10, args["out"],
+                               args["ws"], ws_l, None) == -1
+    assert L.mla_decode_latent(ctypes.byref(w), None, args["x"], 4, 10, args["kc"], args["vc"], 11, args["out"],
+                               args["ws"], 100, None) == -3

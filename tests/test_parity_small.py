@@ -1,0 +1,164 @@
+"""CUDA path vs the CPU oracle at sizes the oracle finishes in seconds.
+
+Full Kimi K2 dimensions (d = 7168, 64 heads, ...); seeded synthetic inputs
+from ``synth`` on both sides; tolerance max abs <= 2e-2 and relative
+Frobenius <= 1e-2 on out, Delta_attn (o_proj output before the residual)
+and every cache the call writes.  Shapes span several GEMM tiles (128 rows)
+and attention tiles with ragged tails, plus the degenerate cases T = 1,
+P = 0 and out aliasing x.
+"""
+import numpy as np
+import pytest
+
+import synth
+from oracle import mla_oracle as om
+import mla_gb300 as m
+from mla_testlib import (bits_to_cuda, cuda_to_f64, cuda_weights, f64_to_bits, oracle_weights, parity)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def W(gpu_available):
+    return cuda_weights(0), m.make_weights(cuda_weights(0)), oracle_weights(0)
+
+
+def run_prefill(W, B, T, with_cache=True, cap=None, inplace=False):
+    import torch
+    wt, ws_struct, _ = W
+    xb = synth.tensor_bits(0, "x", (B, T, 7168), synth.X_DIST)
+    x = bits_to_cuda(xb)
+    out = x.clone() if inplace else torch.empty_like(x)
+    cap = cap or T
+    kc = torch.zeros((B, 64, cap, 192), dtype=torch.bfloat16, device="cuda") if with_cache else None
+    vc = torch.zeros((B, 64, cap, 128), dtype=torch.bfloat16, device="cuda") if with_cache else None
+    ckv = torch.zeros((B, cap, 512), dtype=torch.bfloat16, device="cuda") if with_cache else None
+    kpe = torch.zeros((B, cap, 64), dtype=torch.bfloat16, device="cuda") if with_cache else None
+    delta = torch.empty((B, T, 7168), dtype=torch.float32, device="cuda")
+    wsp = m.alloc_workspace(m.MODE_PREFILL, B, T)
+    params = m.make_params(delta_out=delta)
+    m.mla_prefill(ws_struct, out if inplace else x, out, wsp, kc, vc, ckv, kpe, cap if with_cache else 0, params)
+    torch.cuda.synchronize()
+    assert m.mla_device_status(wsp) == 0
+    return synth.bf16_bits_to_f64(xb), out, delta, kc, vc, ckv, kpe
+
+
+@pytest.mark.parametrize("B,T", [(1, 16), (2, 300), (1, 1), (3, 129)])
+def test_prefill_parity(W, B, T):
+    x64, out, delta, kc, vc, ckv, kpe = run_prefill(W, B, T)
+    ref = om.prefill(W[2], x64)
+    parity(cuda_to_f64(delta), ref["delta"], "delta")
+    parity(cuda_to_f64(out), ref["out"], "out")
+    parity(cuda_to_f64(kc), ref["K"], "K cache")
+    parity(cuda_to_f64(vc), ref["V"], "V cache")
+    parity(cuda_to_f64(ckv), ref["ckv"], "latent cache")
+    parity(cuda_to_f64(kpe), ref["kpe"], "rotary-key cache")
+
+
+def test_prefill_in_place_and_no_cache(W):
+    B, T = 1, 70
+    x64, out, delta, *_ = run_prefill(W, B, T, with_cache=False, inplace=True)
+    ref = om.prefill(W[2], x64)
+    parity(cuda_to_f64(out), ref["out"], "out (in place)")
+    parity(cuda_to_f64(delta), ref["delta"], "delta")
+
+
+def test_prefill_cache_capacity_larger_than_T(W):
+    import torch
+    B, T, cap = 2, 40, 100
+    x64, out, delta, kc, vc, ckv, kpe = run_prefill(W, B, T, cap=cap)
+    ref = om.prefill(W[2], x64)
+    parity(cuda_to_f64(kc[:, :, :T]), ref["K"], "K cache")
+    parity(cuda_to_f64(ckv[:, :T]), ref["ckv"], "latent cache")
+    assert torch.count_nonzero(kc[:, :, T:]).item() == 0
+    assert torch.count_nonzero(ckv[:, T:]).item() == 0
+
+
+def make_caches(W, B, P, cap):
+    """Caches of positions 0..P-1 built by the oracle from seeded tokens and
+    rounded to bf16 storage; identical bits go to both sides."""
+    import torch
+    wo = W[2]
+    xc = synth.bf16_bits_to_f64(synth.tensor_bits(0, "cache_x", (B, P, 7168), synth.X_DIST)) if P else None
+    Kb = np.zeros((B, 64, cap, 192), np.uint16)
+    Vb = np.zeros((B, 64, cap, 128), np.uint16)
+    Cb = np.zeros((B, cap, 512), np.uint16)
+    Rb = np.zeros((B, cap, 64), np.uint16)
+    if P:
+        c = om.cache_from_tokens(wo, xc)
+        Kb[:, :, :P] = f64_to_bits(c["K"])
+        Vb[:, :, :P] = f64_to_bits(c["V"])
+        Cb[:, :P] = f64_to_bits(c["ckv"])
+        Rb[:, :P] = f64_to_bits(c["kpe"])
+    f = synth.bf16_bits_to_f64
+    return (Kb, Vb, Cb, Rb), (f(Kb[:, :, :P]), f(Vb[:, :, :P]), f(Cb[:, :P]), f(Rb[:, :P]))
+
+
+@pytest.mark.parametrize("B,P", [(3, 37), (2, 0), (1, 300), (5, 1)])
+def test_decode_parity(W, B, P):
+    import torch
+    cap = P + 3
+    (Kb, Vb, _, _), (K64, V64, _, _) = make_caches(W, B, P, cap)
+    xb = synth.tensor_bits(0, "new_x", (B, 7168), synth.X_DIST)
+    x = bits_to_cuda(xb)
+    kc, vc = bits_to_cuda(Kb), bits_to_cuda(Vb)
+    out = torch.empty_like(x)
+    delta = torch.empty((B, 7168), dtype=torch.float32, device="cuda")
+    wsp = m.alloc_workspace(m.MODE_DECODE, B, P)
+    m.mla_decode(W[1], x, P, kc, vc, out, wsp, m.make_params(delta_out=delta))
+    torch.cuda.synchronize()
+    assert m.mla_device_status(wsp) == 0
+    ref = om.decode(W[2], synth.bf16_bits_to_f64(xb), K64, V64)
+    parity(cuda_to_f64(delta), ref["delta"], "delta")
+    parity(cuda_to_f64(out), ref["out"], "out")
+    parity(cuda_to_f64(kc[:, :, P]), ref["k_new"], "new K row")
+    parity(cuda_to_f64(vc[:, :, P]), ref["v_new"], "new V row")
+    # positions other than P are untouched
+    assert np.array_equal(kc[:, :, :P].contiguous().view(torch.int16).cpu().numpy().view(np.uint16), Kb[:, :, :P])
+
+
+@pytest.mark.parametrize("B,P", [(3, 37), (2, 0), (1, 300), (4, 129)])
+def test_decode_latent_parity(W, B, P):
+    import torch
+    cap = P + 2
+    (_, _, Cb, Rb), (_, _, C64, R64) = make_caches(W, B, P, cap)
+    xb = synth.tensor_bits(0, "new_x", (B, 7168), synth.X_DIST)
+    x = bits_to_cuda(xb)
+    ckv, kpe = bits_to_cuda(Cb), bits_to_cuda(Rb)
+    out = torch.empty_like(x)
+    delta = torch.empty((B, 7168), dtype=torch.float32, device="cuda")
+    wsp = m.alloc_workspace(m.MODE_DECODE_LATENT, B, P)
+    m.mla_decode_latent(W[1], x, P, ckv, kpe, out, wsp, m.make_params(delta_out=delta))
+    torch.cuda.synchronize()
+    assert m.mla_device_status(wsp) == 0
+    ref = om.decode_latent(W[2], synth.bf16_bits_to_f64(xb), C64, R64)
+    parity(cuda_to_f64(delta), ref["delta"], "delta")
+    parity(cuda_to_f64(out), ref["out"], "out")
+    parity(cuda_to_f64(ckv[:, P]), ref["ckv_new"], "new latent row")
+    parity(cuda_to_f64(kpe[:, P]), ref["kpe_new"], "new rotary-key row")
+
+
+def test_prefill_then_decode_chain(W):
+    """GPU prefill of T-1 tokens fills the caches; GPU decode of token T-1
+    must match the oracle's prefill row T-1 (both cache forms)."""
+    import torch
+    B, T = 2, 50
+    xb = synth.tensor_bits(0, "x", (B, T, 7168), synth.X_DIST)
+    x = bits_to_cuda(xb)
+    cap = T
+    kc = torch.zeros((B, 64, cap, 192), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros((B, 64, cap, 128), dtype=torch.bfloat16, device="cuda")
+    ckv = torch.zeros((B, cap, 512), dtype=torch.bfloat16, device="cuda")
+    kpe = torch.zeros((B, cap, 64), dtype=torch.bfloat16, device="cuda")
+    xp = x[:, :T - 1].contiguous()
+    outp = torch.empty_like(xp)
+    m.mla_prefill(W[1], xp, outp, m.alloc_workspace(m.MODE_PREFILL, B, T - 1), kc, vc, ckv, kpe, cap)
+    xn = x[:, T - 1].contiguous()
+    o1 = torch.empty_like(xn)
+    o2 = torch.empty_like(xn)
+    m.mla_decode(W[1], xn, T - 1, kc, vc, o1, m.alloc_workspace(m.MODE_DECODE, B, T - 1))
+    m.mla_decode_latent(W[1], xn, T - 1, ckv, kpe, o2, m.alloc_workspace(m.MODE_DECODE_LATENT, B, T - 1))
+    torch.cuda.synchronize()
+    ref = om.prefill(W[2], synth.bf16_bits_to_f64(xb), query_rows=[T - 1])["out"][:, 0]
+    parity(cuda_to_f64(o1), ref, "decode after prefill")
+    parity(cuda_to_f64(o2), ref, "latent decode after prefill")

@@ -43,7 +43,7 @@ def test_cuda_generator_bit_identical(gpu_available):
     import torch
     for (seed, name, start, n, dist) in [(0, "x", 0, 100003, synth.X_DIST),
                                          (0, "w_q_b", 777777, 65536, synth.WEIGHT_DIST),
-                                         (5, "g_qa", 3, 1536, synth.GAIN_DIST)]:
+                                         (5, "w_q_a_norm", 3, 1536, synth.GAIN_DIST)]:
         ref = synth.normal_bf16_bits(seed, synth.STREAMS[name], start, n, *dist)
         t = torch.empty(n, dtype=torch.bfloat16, device="cuda")
         synth.fill_normal_bf16_cuda(t.data_ptr(), n, seed, synth.STREAMS[name], start, *dist,
