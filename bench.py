@@ -1,0 +1,505 @@
+"""Benchmark of the GB300 MLA sublayer (one JSON line on stdout, rank 0).
+
+Headline step: causal prefill of B=1, T=2048 tokens (Kimi K2 MLA dims) with
+seeded synthetic inputs already resident in HBM; metric = tokens/s.  The same
+line carries the decode workloads of the metric (rebuilt cache B=64, P=1000;
+latent cache B=128, P=8192) and the large prefill (B=8, T=4096) as
+sub-objects, a roofline entry for the step's dominant kernel, an end-to-end
+number through the C ABI with host buffers, the CPU-oracle baseline, the GPU
+clocks seen during the timed region and the number of kernel launches.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--quick]
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
+GPU (sequences are independent, no collective on the data path): value =
+all tokens of all ranks / max-over-ranks time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA prefill tokens/s (% bf16 TC peak); decode step µs & HBM GB/s (% of 8 TB/s)"
+NOMINAL_HBM_GBS = 8000.0
+D, H, QL, KVL, NOPE, ROPE, QK, V = 7168, 64, 1536, 512, 128, 64, 192, 128
+WEIGHT_BYTES = 2 * (7168 + 1536 * 7168 + 1536 + 12288 * 1536 + 576 * 7168 + 512 + 16384 * 512 + 7168 * 8192)
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (flops count the causal lower triangle, diagonal included)
+# ---------------------------------------------------------------------------
+def proj_flops_per_token():
+    return 2 * (D * (QL + KVL + ROPE) + QL * H * QK + KVL * H * (NOPE + V) + H * V * D)
+
+
+def prefill_attn_flops(B, T):
+    return B * T * (T + 1) // 2 * 2 * (QK + V) * H
+
+
+def stage_work(name, mode, B, T_or_P):
+    """(kind, amount) of algorithmic work of one stage launch: ("flop", F) or ("byte", Bytes)."""
+    n = B * T_or_P if mode == "prefill" else B
+    if name == "a_proj":
+        return ("flop", 2 * n * D * (QL + KVL + ROPE))
+    if name == "q_b":
+        return ("flop", 2 * n * QL * H * QK)
+    if name == "kv_b":
+        return ("flop", 2 * n * KVL * H * (NOPE + V))
+    if name == "o_proj":
+        return ("flop", 2 * n * H * V * D)
+    if name == "attn" and mode == "prefill":
+        return ("flop", prefill_attn_flops(B, T_or_P))
+    if name == "attn" and mode == "decode":
+        L = T_or_P + 1
+        return ("byte", B * H * L * (QK + V) * 2)
+    if name == "attn" and mode == "latent":
+        L = T_or_P + 1
+        return ("byte", B * L * (KVL + ROPE) * 2)
+    return (None, 0)
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.rows = []
+        if self.proc is None:
+            return False
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for r in csv.reader(io.StringIO(out)):
+            if len(r) >= 9:
+                self.rows.append([c.strip() for c in r])
+        return False
+
+    def summary(self):
+        if not getattr(self, "rows", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_stage, config):
+    """dram bytes per launch of a stage's kernel from the committed ncu summary,
+    only if it was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    e = d.get(f"{config}:{kernel_stage}")
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+class Runner:
+    def __init__(self, device):
+        import torch
+        import mla_gb300 as m
+        import synth
+        self.torch, self.m, self.synth = torch, m, synth
+        self.dev = device
+        self.wt = synth.weights_cuda(0, device=device)
+        self.W = m.make_weights(self.wt)
+        self.stream = torch.cuda.current_stream()
+        self.flush_buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+
+    def flush_l2(self):
+        self.flush_buf.zero_()
+
+    def timing(self):
+        t = self.m.MlaTiming()
+        evs = []
+        for i in range(self.m.MAX_STAGES):
+            a = self.torch.cuda.Event(enable_timing=True)
+            b = self.torch.cuda.Event(enable_timing=True)
+            a.record()
+            b.record()
+            t.start[i] = a.cuda_event
+            t.stop[i] = b.cuda_event
+            evs.append((a, b))
+        return t, evs
+
+    def time_steps(self, step, steps, warmup, flush=True, with_stages=True, stages=None):
+        torch = self.torch
+        for _ in range(warmup):
+            step(None)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        tims = [self.timing() if with_stages else (None, None) for _ in range(steps)]
+        launches = 0
+        for i in range(steps):
+            if flush:
+                self.flush_l2()
+            ev[i][0].record()
+            step(tims[i][0])
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        ms = [a.elapsed_time(b) for a, b in ev]
+        stage_ms = {}
+        if with_stages:
+            launches = tims[0][0].n_launches
+            for si, name in enumerate(self.m.STAGES):
+                if stages is not None and name not in stages:
+                    continue  # the library records only the stages its entry point runs
+                vals = []
+                for t, evs in tims:
+                    a, b = evs[si]
+                    vals.append(a.elapsed_time(b))
+                if max(vals) > 0:
+                    stage_ms[name] = statistics.mean(vals)
+        return ms, stage_ms, launches
+
+    # ---- prefill ----------------------------------------------------------
+    def prefill_setup(self, B, T, with_cache):
+        torch, m = self.torch, self.m
+        x = self.synth.tensor_cuda(0, "x", (B, T, D), self.synth.X_DIST, device=self.dev)
+        out = torch.empty_like(x)
+        ws = m.alloc_workspace(m.MODE_PREFILL, B, T, device=self.dev)
+        caches = (None,) * 4
+        if with_cache:
+            caches = (torch.empty((B, H, T, QK), dtype=torch.bfloat16, device=self.dev),
+                      torch.empty((B, H, T, V), dtype=torch.bfloat16, device=self.dev),
+                      torch.empty((B, T, KVL), dtype=torch.bfloat16, device=self.dev),
+                      torch.empty((B, T, ROPE), dtype=torch.bfloat16, device=self.dev))
+        return x, out, ws, caches
+
+    def prefill_step_fn(self, x, out, ws, caches, T):
+        m = self.m
+        cap = T if caches[0] is not None or caches[2] is not None else 0
+
+        def step(timing):
+            m.mla_prefill(self.W, x, out, ws, *caches, cap, m.make_params(timing=timing))
+        return step
+
+    # ---- decode -------------------------------------------------------------
+    def fill_caches(self, B, P, cap, rebuilt, chunk_tokens=1 << 17):
+        """Caches of positions 0..P-1 written by the library's own prefill
+        (cache-only mode) from the seeded 'cache_x' tokens."""
+        torch, m, synth = self.torch, self.m, self.synth
+        if rebuilt:
+            c1 = torch.empty((B, H, cap, QK), dtype=torch.bfloat16, device=self.dev)
+            c2 = torch.empty((B, H, cap, V), dtype=torch.bfloat16, device=self.dev)
+        else:
+            c1 = torch.empty((B, cap, KVL), dtype=torch.bfloat16, device=self.dev)
+            c2 = torch.empty((B, cap, ROPE), dtype=torch.bfloat16, device=self.dev)
+        bs = max(1, min(B, chunk_tokens // max(P, 1)))
+        ws = m.alloc_workspace(m.MODE_PREFILL, bs, P, device=self.dev)
+        for b0 in range(0, B, bs):
+            nb = min(bs, B - b0)
+            xc = synth.tensor_cuda(0, "cache_x", (nb, P, D), synth.X_DIST, device=self.dev, row_offset=b0)
+            if rebuilt:
+                m.mla_prefill(self.W, xc, None, ws, c1[b0:b0 + nb], c2[b0:b0 + nb], None, None, cap)
+            else:
+                m.mla_prefill(self.W, xc, None, ws, None, None, c1[b0:b0 + nb], c2[b0:b0 + nb], cap)
+        torch.cuda.synchronize()
+        del ws
+        return c1, c2
+
+    def decode_step_fn(self, B, P, rebuilt):
+        torch, m, synth = self.torch, self.m, self.synth
+        c1, c2 = self.fill_caches(B, P, P + 1, rebuilt)
+        x = synth.tensor_cuda(0, "new_x", (B, D), synth.X_DIST, device=self.dev)
+        out = torch.empty_like(x)
+        ws = m.alloc_workspace(m.MODE_DECODE if rebuilt else m.MODE_DECODE_LATENT, B, P, device=self.dev)
+        fn = m.mla_decode if rebuilt else m.mla_decode_latent
+
+        def step(timing):
+            fn(self.W, x, P, c1, c2, out, ws, m.make_params(timing=timing))
+        return step, (c1, c2, x, out, ws)
+
+
+PREFILL_STAGES = ("input_norm", "a_proj", "latent", "q_b", "kv_b", "attn", "o_proj")
+DECODE_STAGES = ("input_norm", "a_proj", "latent", "q_b", "kv_b", "attn", "o_proj")
+LATENT_STAGES = ("input_norm", "a_proj", "latent", "q_b", "absorb_q", "attn", "absorb_o", "o_proj")
+
+
+def roofline_entry(stage_ms, mode, B, TP, pk, config_name):
+    best = max(stage_ms.items(), key=lambda kv: kv[1]) if stage_ms else None
+    if not best:
+        return None
+    name, ms = best
+    kind, amount = stage_work(name, mode, B, TP)
+    if kind == "flop":
+        ach = amount / (ms * 1e-3) / 1e12
+        peak = pk["bf16_tflops"]
+        return {"kernel": name, "bound": "tensor", "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4), "traffic": ncu_traffic(name, config_name), "ms": round(ms, 4),
+                "share": round(ms / sum(stage_ms.values()), 4), "peak_source": pk["source"] + " (burst)"}
+    if kind == "byte":
+        ach = amount / (ms * 1e-3) / 1e9
+        peak = pk["hbm_gbs"]
+        return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "traffic": ncu_traffic(name, config_name), "ms": round(ms, 4),
+                "share": round(ms / sum(stage_ms.values()), 4), "peak_source": pk["source"]}
+    return {"kernel": name, "bound": None, "ms": ms}
+
+
+def cpu_oracle_prefill_sample(n_tokens):
+    """The oracle (float64 numpy) on the first n_tokens of the B=1, T=2048
+    workload; returns (tokens/s, seconds, threads)."""
+    import numpy as np
+    import synth
+    from oracle import mla_oracle as om
+    names = {"w_in_norm": "g_in", "w_q_a": "w_q_a", "w_q_a_norm": "g_qa", "w_q_b": "w_q_b",
+             "w_kv_a": "w_kv_a", "w_kv_a_norm": "g_kva", "w_kv_b": "w_kv_b", "w_o": "w_o"}
+    W = {names[n]: synth.bf16_bits_to_f64(b) for n, b in synth.weight_bits(0).items()}
+    x = synth.bf16_bits_to_f64(synth.tensor_bits(0, "x", (1, 2048, D), synth.X_DIST, rows=[0]))[:, :n_tokens]
+    t0 = time.perf_counter()
+    om.prefill(W, x)
+    dt = time.perf_counter() - t0
+    threads = os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        if info:
+            threads = max(i.get("num_threads", 1) for i in info)
+    except Exception:
+        pass
+    return n_tokens / dt, dt, threads
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if ws > 1 and rank != 0:
+        return
+    n = args.cpu_tokens
+    times = []
+    for _ in range(args.warmup):
+        cpu_oracle_prefill_sample(n)
+    for _ in range(args.steps):
+        v, dt, threads = cpu_oracle_prefill_sample(n)
+        times.append(dt)
+    mean_s = statistics.mean(times)
+    value = n / mean_s
+    sample = (f"first {n} of the 2048 tokens of the B=1 T=2048 prefill (causal), float64 numpy oracle"
+              if n < 2048 else "the whole B=1 T=2048 prefill (causal), float64 numpy oracle")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_s * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "mla_prefill B=1 T=2048 (sampled)", "global_batch": 1, "seq_len": 2048},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true", help="headline prefill only")
+    ap.add_argument("--cpu-tokens", type=int, default=2048,
+                    help="tokens of the headline sequence the CPU oracle baseline runs (0 = skip)")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    def barrier_max(v):
+        if world == 1:
+            return v
+        import torch.distributed as dist
+        t = torch.tensor([v], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    pk = peaks()
+    r = Runner(dev)
+    K, W = args.steps, max(args.warmup, 3)
+
+    # ---- headline: prefill B=1, T=2048 ----------------------------------------
+    B, T = 1, 2048
+    x, out, ws, caches = r.prefill_setup(B, T, with_cache=False)
+    step = r.prefill_step_fn(x, out, ws, caches, T)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        ms, stage_ms, launches = r.time_steps(step, K, W, stages=PREFILL_STAGES)
+        wall = time.perf_counter() - wall0
+    ms_step = barrier_max(statistics.mean(ms))
+    tok = B * T
+    value = world * tok / (ms_step * 1e-3)
+    flops = tok * proj_flops_per_token() + prefill_attn_flops(B, T)
+    roof = roofline_entry(stage_ms, "prefill", B, T, pk, "prefill_b1_t2048")
+
+    # end to end: pinned host x -> device, call, device -> pinned host out
+    xh = x.cpu().pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    xd = torch.empty_like(x)
+
+    def e2e_step(timing):
+        xd.copy_(xh, non_blocking=True)
+        r.m.mla_prefill(r.W, xd, out, ws, *caches, 0, None)
+        oh.copy_(out, non_blocking=True)
+    e2e_ms, _, _ = r.time_steps(e2e_step, K, W, with_stages=False)
+    e2e_ms = barrier_max(statistics.mean(e2e_ms))
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64 / Irwin-Hall inputs)",
+            "config": {"workload": "mla_prefill B=1 T=2048 causal (Kimi K2 MLA dims)", "global_batch": B * world,
+                       "seq_len": T, "parallelism": f"replica{world}" if world > 1 else "single",
+                       "l2": "flushed between timed steps (512 MB write)"},
+            "tflops": round(flops / (ms_step * 1e-3) / 1e12, 2),
+            "frac_bf16_peak": round(flops / (ms_step * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+            "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+            "roofline": roof, "gpu_launches": launches * K,
+            "e2e": {"value": round(world * tok / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": x.numel() * 2, "d2h_bytes_per_step": out.numel() * 2,
+                    "ms_per_step": round(e2e_ms, 4)},
+            "clocks": clk.summary(), "wall_s_timed": round(wall, 3)}
+    del x, out, ws, caches, xh, oh, xd
+    torch.cuda.empty_cache()
+
+    if not args.quick:
+        ks = max(3, min(K, 10))
+        # ---- decode, rebuilt per-head cache: B=64, P=1000 ----------------------
+        try:
+            B3, P3 = 64, 1000
+            step3, keep = r.decode_step_fn(B3, P3, rebuilt=True)
+            ms3, st3, l3 = r.time_steps(step3, ks, W, stages=DECODE_STAGES)
+            us = barrier_max(statistics.mean(ms3)) * 1e3
+            byts = B3 * H * (P3 + 1) * (QK + V) * 2 + WEIGHT_BYTES + 2 * B3 * D * 2
+            line["decode_rebuilt"] = {
+                "workload": "mla_decode B=64 P=1000 (L=1001 keys), rebuilt bf16 K/V cache",
+                "us_per_step": round(us, 2), "hbm_gbs": round(byts / (us * 1e-6) / 1e9, 1),
+                "frac_8tbs": round(byts / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 4),
+                "frac_measured_hbm": round(byts / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
+                "algorithmic_bytes": byts, "stage_ms": {k: round(v, 4) for k, v in st3.items()},
+                "roofline": roofline_entry(st3, "decode", B3, P3, pk, "decode_b64_p1000"), "launches": l3}
+            del step3, keep
+            torch.cuda.empty_cache()
+        except Exception as e:  # report, keep the headline
+            line["decode_rebuilt"] = {"error": repr(e)[:300]}
+        # ---- decode, latent cache: B=128, P=8192 ---------------------------------
+        try:
+            B4, P4 = 128, 8192
+            step4, keep = r.decode_step_fn(B4, P4, rebuilt=False)
+            ms4, st4, l4 = r.time_steps(step4, ks, W, stages=LATENT_STAGES)
+            us = barrier_max(statistics.mean(ms4)) * 1e3
+            byts = B4 * (P4 + 1) * (KVL + ROPE) * 2 + WEIGHT_BYTES + 2 * B4 * D * 2
+            line["decode_latent"] = {
+                "workload": "mla_decode_latent B=128 P=8192, 576-value latent cache, W_UK/W_UV absorbed",
+                "us_per_step": round(us, 2), "hbm_gbs": round(byts / (us * 1e-6) / 1e9, 1),
+                "frac_8tbs": round(byts / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 4),
+                "frac_measured_hbm": round(byts / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
+                "algorithmic_bytes": byts, "stage_ms": {k: round(v, 4) for k, v in st4.items()},
+                "roofline": roofline_entry(st4, "latent", B4, P4, pk, "latent_b128_p8192"), "launches": l4}
+            del step4, keep
+            torch.cuda.empty_cache()
+        except Exception as e:
+            line["decode_latent"] = {"error": repr(e)[:300]}
+        # ---- prefill B=8, T=4096 writing both caches -------------------------------
+        try:
+            B5, T5 = 8, 4096
+            x5, out5, ws5, c5 = r.prefill_setup(B5, T5, with_cache=True)
+            step5 = r.prefill_step_fn(x5, out5, ws5, c5, T5)
+            ms5, st5, l5 = r.time_steps(step5, max(2, min(ks, 5)), 2, stages=PREFILL_STAGES)
+            ms5 = barrier_max(statistics.mean(ms5))
+            fl5 = B5 * T5 * proj_flops_per_token() + prefill_attn_flops(B5, T5)
+            line["prefill_large"] = {
+                "workload": "mla_prefill B=8 T=4096 causal, writes rebuilt K/V and latent caches",
+                "ms_per_step": round(ms5, 3), "tokens_per_s": round(world * B5 * T5 / (ms5 * 1e-3), 1),
+                "tflops": round(fl5 / (ms5 * 1e-3) / 1e12, 2),
+                "frac_bf16_peak": round(fl5 / (ms5 * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+                "stage_ms": {k: round(v, 4) for k, v in st5.items()},
+                "roofline": roofline_entry(st5, "prefill", B5, T5, pk, "prefill_b8_t4096"), "launches": l5}
+            del x5, out5, ws5, c5
+            torch.cuda.empty_cache()
+        except Exception as e:
+            line["prefill_large"] = {"error": repr(e)[:300]}
+
+    # ---- CPU oracle baseline (rank 0, N = 1 only) ----------------------------------
+    if world == 1 and args.cpu_tokens > 0:
+        v, dt, threads = cpu_oracle_prefill_sample(args.cpu_tokens)
+        line["cpu_baseline"] = {"value": round(v, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                "sample": f"first {args.cpu_tokens} of the 2048 tokens of the headline prefill "
+                                          f"(causal; 2048 = the whole step), float64 numpy oracle, {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

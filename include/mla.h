@@ -126,14 +126,18 @@ typedef struct {
 size_t mla_workspace_size(int mode, int B, int t_or_p, int cap);
 
 /* Causal prefill of x [B, T, 7168] at positions 0..T-1.
- *   out       [B, T, 7168]        x + Delta_attn (may alias x exactly)
+ *   out       [B, T, 7168]        x + Delta_attn (may alias x exactly); or NULL:
+ *                                 the call then only fills the caches it is
+ *                                 given (a prompt-cache fill: the query path,
+ *                                 attention and o_proj are skipped)
  *   k_cache   [B, 64, cap, 192]   optional (NULL): receives K rows 0..T-1, post-RoPE
  *   v_cache   [B, 64, cap, 128]   optional, given together with k_cache
  *   ckv_cache [B, cap, 512]       optional (NULL): receives the normalised latent c^KV-hat
  *   kpe_cache [B, cap, 64]        optional, given together with ckv_cache: rotated k^R
  *   cap       cache capacity in positions; must be >= T when a cache is given
- * Errors: INVALID_ARG (B < 1, T < 1, null x/out/weights, only one of a cache
- * pair, cap < T, partial x/out overlap), ALIGNMENT, WORKSPACE, CUDA. */
+ * Errors: INVALID_ARG (B < 1, T < 1, null x or weights, out NULL with no
+ * cache, only one of a cache pair, cap < T, partial x/out overlap),
+ * ALIGNMENT, WORKSPACE, CUDA. */
 int mla_prefill(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int T,
                 void* out, void* k_cache, void* v_cache, void* ckv_cache, void* kpe_cache, int cap,
                 void* workspace, size_t workspace_bytes, void* stream);

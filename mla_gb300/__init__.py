@@ -107,7 +107,9 @@ def make_weights(w: dict) -> MlaWeights:
         t = w[n]
         if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != WEIGHT_SHAPES[n]:
             raise ValueError(f"weight {n}: need contiguous bf16 CUDA tensor of shape {WEIGHT_SHAPES[n]}")
-    return MlaWeights(*[w[n].data_ptr() for n in WEIGHT_NAMES])
+    s = MlaWeights(*[w[n].data_ptr() for n in WEIGHT_NAMES])
+    s._keep = dict(w)  # the struct holds raw pointers: keep the tensors alive with it
+    return s
 
 
 def make_params(eps=1e-6, rope_base=10000.0, softmax_scale=None, delta_out=None, timing=None) -> MlaParams:
@@ -132,7 +134,7 @@ def alloc_workspace(mode: int, B: int, t_or_p: int, device="cuda"):
 
 def mla_prefill(weights: MlaWeights, x, out, workspace, k_cache=None, v_cache=None, ckv_cache=None,
                 kpe_cache=None, cap=0, params: MlaParams | None = None, stream=None):
-    """x, out: bf16 [B, T, 7168]; caches as in include/mla.h."""
+    """x, out: bf16 [B, T, 7168] (out None: fill the given caches only); caches as in include/mla.h."""
     B, T = x.shape[0], x.shape[1]
     rc = lib().mla_prefill(ctypes.byref(weights), None if params is None else ctypes.byref(params), _ptr(x), B, T,
                            _ptr(out), _ptr(k_cache), _ptr(v_cache), _ptr(ckv_cache), _ptr(kpe_cache), cap,

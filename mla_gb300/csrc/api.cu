@@ -36,7 +36,7 @@ Layout make_layout(int mode, int B, int t_or_p, int num_sms) {
   L.status = take(256);
   L.cs = take(npos * 32 * sizeof(float2));
   L.xn = take(n * MLA_D * 2);
-  L.ca = take(n * 2112 * 2);
+  L.ca = take(n * 2112 * 4);
   L.cq = take(n * MLA_Q_LORA * 2);
   L.ckv = take(n * MLA_KV_LORA * 2);
   L.kpe = take(n * MLA_QK_ROPE * 2);
@@ -138,7 +138,7 @@ T* at(void* ws, size_t off) {
 int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok, int n_pos, int pos0,
               int t_mod, int t_off, __nv_bfloat16* ckv_cache, __nv_bfloat16* kpe_cache, int cap, void* ws,
               const Layout& L, const DevStatusHost& st, int sms, cudaStream_t stream, Stager& sg,
-              int* launches) {
+              int* launches, bool with_q = true) {
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   sg.start(MLA_STAGE_INPUT_NORM);
   MLA_TRY(launch_rope_table(at<float2>(ws, L.cs), n_pos, pos0, p.base, stream));
@@ -154,9 +154,9 @@ int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok,
                     static_cast<const __nv_bfloat16*>(w->w_q_a), MLA_D, MLA_Q_LORA,
                     static_cast<const __nv_bfloat16*>(w->w_kv_a), MLA_D, 576, false};
     EpiArgs ea{};
-    ea.out = at<__nv_bfloat16>(ws, L.ca);
+    ea.out_f32 = at<float>(ws, L.ca);
     ea.ldo = 2112;
-    MLA_TRY(launch_gemm(s, op, Epi::kStoreBf16, ea, st, sms, stream));
+    MLA_TRY(launch_gemm(s, op, Epi::kStoreF32, ea, st, sms, stream));
     *launches += 1;
   }
   sg.stop(MLA_STAGE_A_PROJ);
@@ -164,7 +164,7 @@ int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok,
   sg.start(MLA_STAGE_LATENT);
   {
     LatentArgs la{};
-    la.ca = at<__nv_bfloat16>(ws, L.ca);
+    la.ca = at<float>(ws, L.ca);
     la.g_qa = static_cast<const __nv_bfloat16*>(w->w_q_a_norm);
     la.g_kva = static_cast<const __nv_bfloat16*>(w->w_kv_a_norm);
     la.cs = at<float2>(ws, L.cs);
@@ -182,6 +182,7 @@ int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok,
     *launches += 1;
   }
   sg.stop(MLA_STAGE_LATENT);
+  if (!with_q) return MLA_OK;
 
   sg.start(MLA_STAGE_Q_B);
   {
@@ -236,14 +237,14 @@ int o_proj_stage(const mla_weights_t* w, const Params& p, const void* x, void* o
 }
 
 int common_checks(const mla_weights_t* w, const Params& p, const void* x, const void* out, size_t n_tok,
-                  void* ws, size_t ws_bytes, size_t need) {
+                  void* ws, size_t ws_bytes, size_t need, bool out_optional = false) {
   int rc = check_weights(w);
   if (rc) return rc;
-  if (!x || !out) return MLA_ERR_INVALID_ARG;
+  if (!x || (!out && !out_optional)) return MLA_ERR_INVALID_ARG;
   if (!ws) return MLA_ERR_WORKSPACE;
   if (!params_ok(p)) return MLA_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(out) || !aligned16(ws)) return MLA_ERR_ALIGNMENT;
-  if (bad_overlap(x, out, n_tok * MLA_D * 2)) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(x) || (out && !aligned16(out)) || !aligned16(ws)) return MLA_ERR_ALIGNMENT;
+  if (out && bad_overlap(x, out, n_tok * MLA_D * 2)) return MLA_ERR_INVALID_ARG;
   if (ws_bytes < need) return MLA_ERR_WORKSPACE;
   return MLA_OK;
 }
@@ -302,8 +303,10 @@ int mla_prefill(const mla_weights_t* w, const mla_params_t* params, const void* 
   for (const void* c : {(const void*)k_cache, (const void*)v_cache, (const void*)ckv_cache, (const void*)kpe_cache})
     if (c && !aligned16(c)) return MLA_ERR_ALIGNMENT;
   const size_t n_tok = (size_t)B * T;
+  const bool cache_only = (out == nullptr);
+  if (cache_only && !k_cache && !ckv_cache) return MLA_ERR_INVALID_ARG;
   int rc = common_checks(w, p, x, out, n_tok, workspace, workspace_bytes,
-                         make_layout(MLA_MODE_PREFILL, B, T, kMaxSmsForSizing).total);
+                         make_layout(MLA_MODE_PREFILL, B, T, kMaxSmsForSizing).total, true);
   if (rc) return rc;
   const int sms = num_sms_of_current_device();
   if (sms <= 0) return MLA_ERR_CUDA;
@@ -316,8 +319,13 @@ int mla_prefill(const mla_weights_t* w, const mla_params_t* params, const void* 
   if (cudaMemsetAsync(st.word, 0, sizeof(uint32_t), stream_) != cudaSuccess) return MLA_ERR_CUDA;
 
   rc = front_end(w, p, x, (int)n_tok, T, 0, T, 0, static_cast<__nv_bfloat16*>(ckv_cache),
-                 static_cast<__nv_bfloat16*>(kpe_cache), cap, workspace, L, st, sms, stream_, sg, &launches);
+                 static_cast<__nv_bfloat16*>(kpe_cache), cap, workspace, L, st, sms, stream_, sg, &launches,
+                 !cache_only);
   if (rc) return rc;
+  if (cache_only && !k_cache) {
+    if (p.timing) p.timing->n_launches = launches;
+    return MLA_OK;
+  }
 
   __nv_bfloat16* kc = k_cache ? static_cast<__nv_bfloat16*>(k_cache) : at<__nv_bfloat16>(workspace, L.kscr);
   __nv_bfloat16* vc = v_cache ? static_cast<__nv_bfloat16*>(v_cache) : at<__nv_bfloat16>(workspace, L.vscr);
@@ -326,6 +334,10 @@ int mla_prefill(const mla_weights_t* w, const mla_params_t* params, const void* 
   rc = kv_b_stage(w, (int)n_tok, T, 0, kc, vc, kcap, workspace, L, st, sms, stream_, &launches);
   if (rc) return rc;
   sg.stop(MLA_STAGE_KV_B);
+  if (cache_only) {
+    if (p.timing) p.timing->n_launches = launches;
+    return MLA_OK;
+  }
 
   sg.start(MLA_STAGE_ATTN);
   {

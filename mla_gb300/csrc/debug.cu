@@ -54,6 +54,18 @@ __global__ void __launch_bounds__(128) umma_probe_kernel(float* out, int m, uint
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = slot;
+  {
+    // clear all 128 lanes x 64 columns so that lanes the MMA does not write read 0
+    uint32_t z[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = 0u;
+    tmem_st32(tmem + ((uint32_t)(warp * 32) << 16), z);
+    tmem_st32(tmem + ((uint32_t)(warp * 32) << 16) + 32, z);
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
   if (tid == 0) {
     const uint64_t da = sdesc_sw128(smem_u32(sA), 16, 1024);
     const uint64_t db = sdesc_sw128(smem_u32(sB), 16, 1024);

@@ -3,7 +3,9 @@
 // D[m, n] = sum_k A[m, k] B[n, k] with bf16 operands staged by TMA (128-byte
 // swizzle) and an f32 accumulator in tensor memory; the epilogue reads the
 // accumulator with tcgen05.ld and applies the step-specific output transform:
-//   kStoreBf16  plain bf16 store (A-projection, latent absorption)
+//   kStoreBf16  plain bf16 store (latent absorption)
+//   kStoreF32   plain float32 store (A-projection: its columns are normalised
+//               or rotated before they are rounded once to bf16)
 //   kQRope      q_b_proj: one head (192 columns) per tile, RoPE on the 64
 //               "pe" columns (dense-block page: Q^R_t = RoPE(Q^pe_t, R_t))
 //   kKVCache    kv_b_proj: one head (256 columns) per tile, writes k_nope and
@@ -66,6 +68,21 @@ __device__ __forceinline__ void run_epilogue(const EpiArgs& ea, uint32_t taddr, 
       tmem_ld32(taddr + c, r);
       tmem_wait_ld();
       if (row_ok) store32_bf16(dst + c, r);
+    }
+  } else if constexpr (EPI == Epi::kStoreF32) {
+    float* dst = ea.out_f32 + (size_t)row * ea.ldo + n0;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c, r);
+      tmem_wait_ld();
+      if (row_ok) {
+        float4* d = reinterpret_cast<float4*>(dst + c);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          d[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]), __uint_as_float(r[4 * j + 2]),
+                             __uint_as_float(r[4 * j + 3]));
+      }
     }
   } else if constexpr (EPI == Epi::kQRope) {
     static_assert(BN == 192, "q_b epilogue works on one 192-wide head per tile");
@@ -365,6 +382,9 @@ cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, con
     case Epi::kResidual:
       if (s.N % 256 || op.b_mn_major) return cudaErrorInvalidValue;
       return launch_impl<256, 4, Epi::kResidual, false>(s, op, ea, st, num_sms, stream);
+    case Epi::kStoreF32:
+      if (s.N % 192 || s.n_split % 192 || op.b_mn_major) return cudaErrorInvalidValue;
+      return launch_impl<192, 5, Epi::kStoreF32, false>(s, op, ea, st, num_sms, stream);
     case Epi::kStoreBf16:
     default:
       if (op.b_mn_major) {

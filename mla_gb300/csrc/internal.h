@@ -48,11 +48,12 @@ struct GemmOperands {
   bool b_mn_major;
 };
 
-enum class Epi { kStoreBf16, kQRope, kKVCache, kResidual };
+enum class Epi { kStoreBf16, kStoreF32, kQRope, kKVCache, kResidual };
 
 struct EpiArgs {
-  // kStoreBf16: out[row, c_col0 + batch*c_col_step + n]
+  // kStoreBf16: out[row, c_col0 + batch*c_col_step + n]; kStoreF32: out_f32[row, n]
   __nv_bfloat16* out;
+  float* out_f32;
   int ldo;
   int c_col0, c_col_step;
   // kQRope: q[row, n] with RoPE on columns 128..191 of each 192 block;
@@ -78,11 +79,11 @@ cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, con
 cudaError_t launch_rope_table(float2* cs, int n_pos, int pos0, float base, cudaStream_t stream);
 cudaError_t launch_rmsnorm_rows(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_bfloat16* y, int rows,
                                 float eps, cudaStream_t stream);
-// Split the A-projection output ca [rows, 2112] into RMSNorm(c^Q) [rows,1536],
+// Split the A-projection output ca [rows, 2112] (float32) into RMSNorm(c^Q) [rows,1536],
 // RMSNorm(c^KV) [rows,512] and RoPE(k_pe) [rows,64]; optional latent cache
 // copies at ckv_cache[b, t_off + t] / kpe_cache[b, t_off + t].
 struct LatentArgs {
-  const __nv_bfloat16* ca;
+  const float* ca;
   const __nv_bfloat16* g_qa;
   const __nv_bfloat16* g_kva;
   const float2* cs;

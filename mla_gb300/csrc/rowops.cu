@@ -69,99 +69,62 @@ __global__ void __launch_bounds__(128) rmsnorm_7168_kernel(const __nv_bfloat16* 
   }
 }
 
-// One warp per row of ca [rows, 2112] = [c^Q 1536 | c^KV 512 | k^pe 64].
+// One warp per row of ca [rows, 2112] (float32) = [c^Q 1536 | c^KV 512 | k^pe 64].
+__device__ __forceinline__ void norm_store(const float4* src, int n4, const __nv_bfloat16* g, float eps,
+                                           __nv_bfloat16* dst, __nv_bfloat16* dst2, int lane) {
+  // n4 float4 per lane (n4 * 4 * 32 values in the row)
+  float4 v[12];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < 12; ++j) {
+    if (j < n4) {
+      v[j] = src[lane + 32 * j];
+      ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
+    }
+  }
+  const float rstd = rsqrtf(warp_sum(ss) / (float)(n4 * 128) + eps);
+  const uint2* gp = reinterpret_cast<const uint2*>(g);
+  uint2* dp = reinterpret_cast<uint2*>(dst);
+  uint2* dp2 = reinterpret_cast<uint2*>(dst2);
+#pragma unroll
+  for (int j = 0; j < 12; ++j) {
+    if (j < n4) {
+      const uint2 gv = gp[lane + 32 * j];
+      const float2 g0 = unpack_bf16x2(gv.x), g1 = unpack_bf16x2(gv.y);
+      const uint2 o = make_uint2(pack_bf16x2(g0.x * (v[j].x * rstd), g0.y * (v[j].y * rstd)),
+                                 pack_bf16x2(g1.x * (v[j].z * rstd), g1.y * (v[j].w * rstd)));
+      dp[lane + 32 * j] = o;
+      if (dst2) dp2[lane + 32 * j] = o;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(256) latent_split_kernel(const LatentArgs a) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= a.rows) return;
   const size_t row = warp;
-  const uint4* src = reinterpret_cast<const uint4*>(a.ca + row * 2112);
-
-  // c^Q: 1536 = 192 uint4, 6 per lane
-  {
-    uint4 v[6];
-    float ss = 0.f;
-#pragma unroll
-    for (int j = 0; j < 6; ++j) {
-      v[j] = src[lane + 32 * j];
-      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float2 f = unpack_bf16x2(w[q]);
-        ss += f.x * f.x + f.y * f.y;
-      }
-    }
-    const float rstd = rsqrtf(warp_sum(ss) * (1.0f / 1536.0f) + a.eps);
-    const uint4* g = reinterpret_cast<const uint4*>(a.g_qa);
-    uint4* dst = reinterpret_cast<uint4*>(a.cq + row * 1536);
-#pragma unroll
-    for (int j = 0; j < 6; ++j) {
-      const uint4 gv = g[lane + 32 * j];
-      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-      const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float2 f = unpack_bf16x2(w[q]);
-        float2 gg = unpack_bf16x2(gw[q]);
-        o[q] = pack_bf16x2(gg.x * (f.x * rstd), gg.y * (f.y * rstd));
-      }
-      dst[lane + 32 * j] = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-  }
+  const float* src = a.ca + row * 2112;
   const int b = (int)(row / a.t_mod);
   const int t = a.t_off + (int)(row % a.t_mod);
-  // c^KV: 512 = 64 uint4, 2 per lane (uint4 index 192 .. 255)
-  {
-    uint4 v[2];
-    float ss = 0.f;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      v[j] = src[192 + lane + 32 * j];
-      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float2 f = unpack_bf16x2(w[q]);
-        ss += f.x * f.x + f.y * f.y;
-      }
-    }
-    const float rstd = rsqrtf(warp_sum(ss) * (1.0f / 512.0f) + a.eps);
-    const uint4* g = reinterpret_cast<const uint4*>(a.g_kva);
-    uint4* dst = reinterpret_cast<uint4*>(a.ckv + row * 512);
-    uint4* dcache = a.ckv_cache ? reinterpret_cast<uint4*>(a.ckv_cache + ((size_t)b * a.cap + t) * 512) : nullptr;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const uint4 gv = g[lane + 32 * j];
-      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-      const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float2 f = unpack_bf16x2(w[q]);
-        float2 gg = unpack_bf16x2(gw[q]);
-        o[q] = pack_bf16x2(gg.x * (f.x * rstd), gg.y * (f.y * rstd));
-      }
-      const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
-      dst[lane + 32 * j] = ov;
-      if (dcache) dcache[lane + 32 * j] = ov;
-    }
-  }
-  // k^pe: 64 values, lane i rotates pair (i, i + 32) at position t
-  {
-    const __nv_bfloat16* kp = a.ca + row * 2112 + 2048;
-    const float x1 = __bfloat162float(kp[lane]);
-    const float x2 = __bfloat162float(kp[lane + 32]);
-    const float2 cs = a.cs[(size_t)(row % a.t_mod) * 32 + lane];
-    const __nv_bfloat16 y1 = __float2bfloat16_rn(x1 * cs.x - x2 * cs.y);
-    const __nv_bfloat16 y2 = __float2bfloat16_rn(x2 * cs.x + x1 * cs.y);
-    __nv_bfloat16* d = a.kpe + row * 64;
-    d[lane] = y1;
-    d[lane + 32] = y2;
-    if (a.kpe_cache) {
-      __nv_bfloat16* dc = a.kpe_cache + ((size_t)b * a.cap + t) * 64;
-      dc[lane] = y1;
-      dc[lane + 32] = y2;
-    }
+  // c^Q-hat = RMSNorm(c^Q): 1536 values = 12 float4 per lane
+  norm_store(reinterpret_cast<const float4*>(src), 12, a.g_qa, a.eps, a.cq + row * 1536, nullptr, lane);
+  // c^KV-hat = RMSNorm(c^KV): 512 values = 4 float4 per lane; also the latent cache row
+  __nv_bfloat16* dcache = a.ckv_cache ? a.ckv_cache + ((size_t)b * a.cap + t) * 512 : nullptr;
+  norm_store(reinterpret_cast<const float4*>(src + 1536), 4, a.g_kva, a.eps, a.ckv + row * 512, dcache, lane);
+  // k^R = RoPE(k^pe, t): lane i rotates pair (i, i + 32); k^pe is not normalised
+  const float x1 = src[2048 + lane];
+  const float x2 = src[2048 + 32 + lane];
+  const float2 cs = a.cs[(size_t)(row % a.t_mod) * 32 + lane];
+  const __nv_bfloat16 y1 = __float2bfloat16_rn(x1 * cs.x - x2 * cs.y);
+  const __nv_bfloat16 y2 = __float2bfloat16_rn(x2 * cs.x + x1 * cs.y);
+  __nv_bfloat16* d = a.kpe + row * 64;
+  d[lane] = y1;
+  d[lane + 32] = y2;
+  if (a.kpe_cache) {
+    __nv_bfloat16* dc = a.kpe_cache + ((size_t)b * a.cap + t) * 64;
+    dc[lane] = y1;
+    dc[lane + 32] = y2;
   }
 }
 

@@ -13,14 +13,16 @@ import pytest
 import synth
 from oracle import mla_oracle as om
 import mla_gb300 as m
-from mla_testlib import (bits_to_cuda, cuda_to_f64, cuda_weights, f64_to_bits, oracle_weights, parity)
+from mla_testlib import (bits_to_cuda, cuda_to_f64, cuda_weights, f64_to_bits, oracle_weights, parity,
+                         parity_cache)
 
 pytestmark = pytest.mark.gpu
 
 
 @pytest.fixture(scope="module")
 def W(gpu_available):
-    return cuda_weights(0), m.make_weights(cuda_weights(0)), oracle_weights(0)
+    wt = cuda_weights(0)
+    return wt, m.make_weights(wt), oracle_weights(0)
 
 
 def run_prefill(W, B, T, with_cache=True, cap=None, inplace=False):
@@ -49,10 +51,10 @@ def test_prefill_parity(W, B, T):
     ref = om.prefill(W[2], x64)
     parity(cuda_to_f64(delta), ref["delta"], "delta")
     parity(cuda_to_f64(out), ref["out"], "out")
-    parity(cuda_to_f64(kc), ref["K"], "K cache")
-    parity(cuda_to_f64(vc), ref["V"], "V cache")
-    parity(cuda_to_f64(ckv), ref["ckv"], "latent cache")
-    parity(cuda_to_f64(kpe), ref["kpe"], "rotary-key cache")
+    parity_cache(cuda_to_f64(kc), ref["K"], "K cache")
+    parity_cache(cuda_to_f64(vc), ref["V"], "V cache")
+    parity_cache(cuda_to_f64(ckv), ref["ckv"], "latent cache")
+    parity_cache(cuda_to_f64(kpe), ref["kpe"], "rotary-key cache")
 
 
 def test_prefill_in_place_and_no_cache(W):
@@ -68,8 +70,8 @@ def test_prefill_cache_capacity_larger_than_T(W):
     B, T, cap = 2, 40, 100
     x64, out, delta, kc, vc, ckv, kpe = run_prefill(W, B, T, cap=cap)
     ref = om.prefill(W[2], x64)
-    parity(cuda_to_f64(kc[:, :, :T]), ref["K"], "K cache")
-    parity(cuda_to_f64(ckv[:, :T]), ref["ckv"], "latent cache")
+    parity_cache(cuda_to_f64(kc[:, :, :T]), ref["K"], "K cache")
+    parity_cache(cuda_to_f64(ckv[:, :T]), ref["ckv"], "latent cache")
     assert torch.count_nonzero(kc[:, :, T:]).item() == 0
     assert torch.count_nonzero(ckv[:, T:]).item() == 0
 
@@ -111,8 +113,8 @@ def test_decode_parity(W, B, P):
     ref = om.decode(W[2], synth.bf16_bits_to_f64(xb), K64, V64)
     parity(cuda_to_f64(delta), ref["delta"], "delta")
     parity(cuda_to_f64(out), ref["out"], "out")
-    parity(cuda_to_f64(kc[:, :, P]), ref["k_new"], "new K row")
-    parity(cuda_to_f64(vc[:, :, P]), ref["v_new"], "new V row")
+    parity_cache(cuda_to_f64(kc[:, :, P]), ref["k_new"], "new K row")
+    parity_cache(cuda_to_f64(vc[:, :, P]), ref["v_new"], "new V row")
     # positions other than P are untouched
     assert np.array_equal(kc[:, :, :P].contiguous().view(torch.int16).cpu().numpy().view(np.uint16), Kb[:, :, :P])
 
@@ -134,8 +136,8 @@ def test_decode_latent_parity(W, B, P):
     ref = om.decode_latent(W[2], synth.bf16_bits_to_f64(xb), C64, R64)
     parity(cuda_to_f64(delta), ref["delta"], "delta")
     parity(cuda_to_f64(out), ref["out"], "out")
-    parity(cuda_to_f64(ckv[:, P]), ref["ckv_new"], "new latent row")
-    parity(cuda_to_f64(kpe[:, P]), ref["kpe_new"], "new rotary-key row")
+    parity_cache(cuda_to_f64(ckv[:, P]), ref["ckv_new"], "new latent row")
+    parity_cache(cuda_to_f64(kpe[:, P]), ref["kpe_new"], "new rotary-key row")
 
 
 def test_prefill_then_decode_chain(W):
