@@ -164,6 +164,26 @@ int mla_decode_latent(const mla_weights_t* w, const mla_params_t* params, const 
                       int P, void* ckv_cache, void* kpe_cache, int cap, void* out,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* mla_decode without a workspace argument.  The pages have no counterpart
+ * to this entry point: it exists for callers that cannot allocate device
+ * memory (code running under a host framework that owns all device memory
+ * and allows no allocation of its own, such as inference-server plugins or
+ * runtimes with a fixed memory budget, and latency-critical loops that cannot
+ * afford the device synchronisation an allocation may cause).
+ *   Scratch: a 16 MiB static device array inside the library, held by every
+ *   GPU that loads the library until the process exits.  Batches whose
+ *   mla_workspace_size(MLA_MODE_DECODE, B, P, cap) exceeds 16 MiB (about 240
+ *   sequences) are rejected with MLA_ERR_WORKSPACE; nothing is allocated.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   Every call on a device shares the one array and it keeps the last call's
+ *   contents: calls that may overlap on the GPU (different streams without
+ *   ordering between them) race.  A device-side timeout is recorded only in
+ *   the array, not returned.
+ * Arguments, checks and results otherwise as mla_decode. */
+int mla_decode_noalloc(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int P,
+                       void* k_cache, void* v_cache, int cap, void* out, void* stream);
+
 /* Synchronises `stream` and reads the device status word the last call on
  * this workspace left: MLA_OK, or MLA_ERR_TIMEOUT if a bounded device wait
  * gave up (the kernel then skipped its remaining work and returned).

@@ -61,6 +61,8 @@ _SIGS = {
                         _VP, _SZ, _VP]),
     "mla_decode_latent": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _VP, _VP, _I,
                                _VP, _VP, _SZ, _VP]),
+    "mla_decode_noalloc": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _VP, _VP, _I,
+                                _VP, _VP]),
     "mla_device_status": (_I, [_VP, _VP]),
     "mla_status_string": (ctypes.c_char_p, [_I]),
     "mla_debug_gemm": (_I, [_VP, _I, _VP, _I, _I, _VP, _I, _I, _I, _I, _VP]),
@@ -162,6 +164,17 @@ def mla_decode_latent(weights: MlaWeights, x, P: int, ckv_cache, kpe_cache, out,
                                  B, P, _ptr(ckv_cache), _ptr(kpe_cache), cap, _ptr(out), _ptr(workspace),
                                  workspace.numel(), _stream(stream))
     _check(rc, "mla_decode_latent")
+
+
+def mla_decode_noalloc(weights: MlaWeights, x, P: int, k_cache, v_cache, out, params: MlaParams | None = None,
+                       stream=None):
+    """mla_decode with its scratch in the library's fixed static device array
+    (for callers that cannot allocate device memory); no workspace argument."""
+    B = x.shape[0]
+    cap = k_cache.shape[2]
+    rc = lib().mla_decode_noalloc(ctypes.byref(weights), None if params is None else ctypes.byref(params), _ptr(x),
+                                  B, P, _ptr(k_cache), _ptr(v_cache), cap, _ptr(out), _stream(stream))
+    _check(rc, "mla_decode_noalloc")
 
 
 def mla_device_status(workspace, stream=None) -> int:
