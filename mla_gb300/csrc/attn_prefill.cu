@@ -1,14 +1,27 @@
-// Causal prefill attention for MLA heads (qk = 192, v = 128).
+// Causal prefill attention for MLA heads (qk = 192, v = 128) on tcgen05.
 //
 // "Mix and project" page, code excerpt: scores = Q K^T * softmax_scale plus
-// the causal mask, softmax in float32, then P V.  This kernel computes it in
-// the flash form (online softmax over key tiles; the probabilities never
-// reach global memory) on the CUDA cores, in float32.
+// the causal mask, softmax in float32, then P V.  Computed in the flash form
+// (online softmax over 128-key tiles; scores and probabilities never reach
+// global memory).
 //
-// Layout: q [B*T, 64*192] (token-major, head h at columns h*192), k/v caches
-// [B, 64, cap, 192|128], o [B*T, 64*128].
-// CTA = (64-query block, head, batch); 256 threads; thread (qi, sub) owns
-// query qi, keys sub + 4j of each 64-key tile and output dims sub*32..+31.
+// CTA = (128-query tile, head, sequence), heaviest tiles launched first.
+// Warp roles (224 threads):
+//   warp 0   TMA: the Q tile once, then K tiles into a 2-slot ring
+//   warp 6   TMA: V tiles into a 1-slot buffer
+//   warp 1   TMEM allocation; one lane issues the MMAs:
+//              S_j = Q K_j^T   M=128 N=128 K=192, into one of two TMEM buffers
+//              O  += P_j V_j   M=128 N=128 K=128, P from shared memory,
+//                              V read MN-major straight from its TMA tile
+//            issued in the order S_0, S_1, PV_0, S_2, PV_1, ... so the tensor
+//            core computes the next scores while the softmax runs
+//   warps 2..5  one thread per query row: read S_j from TMEM, scale, causal
+//            mask on the diagonal tile, running max with lazy rescaling (O is
+//            rescaled in TMEM only when the max grows by more than 2^8, so P
+//            stays <= 256), P_j to shared memory as bf16 (128-byte swizzle),
+//            and at the end O / l to global memory.
+// Layout: Q [B*T, 64*192], K/V caches [B, 64, cap, 192|128] (TMA 3D views
+// whose position extent is T, so keys >= T read as zeros), O [B*T, 64*128].
 #include "common.cuh"
 #include "internal.h"
 
@@ -16,129 +29,266 @@ namespace mla {
 
 namespace {
 
-constexpr int kQB = 64;                 // queries per CTA
-constexpr int kKB = 64;                 // keys per tile
-constexpr int kKStride = 196;           // bf16 per K row in smem (192 + 4 pad)
-constexpr int kVStride = 136;           // bf16 per V row in smem (128 + 8 pad)
-constexpr int kQStride = 196;
+constexpr int kThreads = 224;
+constexpr uint32_t kAtom = 128 * 128;            // 128 rows x 64 bf16
+constexpr uint32_t kQOff = 0;                    // 3 atoms
+constexpr uint32_t kKOff = 3 * kAtom;            // 2 slots x 3 atoms
+constexpr uint32_t kVOff = 9 * kAtom;            // 2 atoms (vdim 0-63, 64-127)
+constexpr uint32_t kPOff = 11 * kAtom;           // 2 atoms (keys 0-63, 64-127)
+constexpr uint32_t kBarOff = 13 * kAtom;
+constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;
+constexpr float kRescaleThreshold = 8.0f;        // log2 units
 
-struct __align__(16) PrefillSmem {
-  __nv_bfloat16 q[kQB * kQStride];
-  __nv_bfloat16 k[kKB * kKStride];
-  __nv_bfloat16 v[kKB * kVStride];
-  float p[kQB][kKB + 1];
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[2], k_empty[2];
+  uint64_t v_full, v_empty;
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full, pv_done;
+  uint64_t drain;
+  uint32_t tmem_slot;
+  int abort;
 };
 
-__global__ void __launch_bounds__(256) prefill_attn_cuda_core(const PrefillAttnArgs a) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>(smem_raw);
-  const int nqb = (a.T + kQB - 1) / kQB;
-  const int qb = nqb - 1 - (int)blockIdx.x;  // heaviest blocks first
+__device__ __forceinline__ uint32_t p_offset(int r, int k) {
+  return (uint32_t)((k >> 6) * kAtom + r * 128 + ((((k & 63) >> 3) ^ (r & 7)) << 4));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ o, int T, int n_qt,
+                    float sl2, const DevStatus st) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bar = reinterpret_cast<Bars*>(smem + kBarOff);
+  volatile int* abort_flag = &bar->abort;
+
+  const int qt = n_qt - 1 - (int)blockIdx.x;
   const int h = blockIdx.y;
   const int b = blockIdx.z;
-  const int tid = threadIdx.x;
-  const int qi = tid >> 2;
-  const int sub = tid & 3;
-  const int q0 = qb * kQB;
-  const float sl2 = a.scale * 1.4426950408889634f;  // scores in log2 units
+  const int q0 = qt * 128;
+  const int n_kv = qt + 1;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
 
-  // load the Q block (zero rows beyond T)
-  for (int i = tid; i < kQB * 24; i += 256) {
-    const int r = i / 24, c = i % 24;
-    uint4 val = make_uint4(0, 0, 0, 0);
-    if (q0 + r < a.T)
-      val = *reinterpret_cast<const uint4*>(a.q + ((size_t)b * a.T + q0 + r) * 12288 + h * 192 + c * 8);
-    *reinterpret_cast<uint2*>(&sm.q[r * kQStride + c * 8]) = make_uint2(val.x, val.y);
-    *reinterpret_cast<uint2*>(&sm.q[r * kQStride + c * 8 + 4]) = make_uint2(val.z, val.w);
+  if (threadIdx.x == 0) {
+    mbar_init(&bar->q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar->k_full[i], 1);
+      mbar_init(&bar->k_empty[i], 1);
+      mbar_init(&bar->s_full[i], 1);
+      mbar_init(&bar->s_free[i], 128);
+    }
+    mbar_init(&bar->v_full, 1);
+    mbar_init(&bar->v_empty, 1);
+    mbar_init(&bar->p_full, 128);
+    mbar_init(&bar->pv_done, 1);
+    mbar_init(&bar->drain, 1);
+    bar->abort = 0;
+    fence_barrier_init();
   }
+  if (warp == 1) {
+    tmem_alloc(&bar->tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar->tmem_slot;
+  const int kv_row = b * 64 + h;
 
-  float o[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) o[i] = 0.f;
-  float m_run = -INFINITY, l_run = 0.f;
-  const int qpos = q0 + qi;
-  const size_t kv_base = ((size_t)b * 64 + h) * a.cap;
-  const int n_tiles = min(qb + 1, (a.T + kKB - 1) / kKB);
-
-  for (int kt = 0; kt < n_tiles; ++kt) {
-    const int k0 = kt * kKB;
-    __syncthreads();
-    for (int i = tid; i < kKB * 24; i += 256) {
-      const int r = i / 24, c = i % 24;
-      uint4 val = make_uint4(0, 0, 0, 0);
-      if (k0 + r < a.T) val = *reinterpret_cast<const uint4*>(a.k + (kv_base + k0 + r) * 192 + c * 8);
-      *reinterpret_cast<uint2*>(&sm.k[r * kKStride + c * 8]) = make_uint2(val.x, val.y);
-      *reinterpret_cast<uint2*>(&sm.k[r * kKStride + c * 8 + 4]) = make_uint2(val.z, val.w);
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- Q and K producer ----
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      mbar_arrive_expect_tx(&bar->q_full, 3 * kAtom);
+      for (int c = 0; c < 3; ++c) tma_load_3d(smem + kQOff + c * kAtom, &tmQ, &bar->q_full, h * 192 + 64 * c, q0, b);
+      int issued[2] = {0, 0};
+      for (int j = 0; j < n_kv; ++j) {
+        const int slot = j & 1;
+        if (!mbar_wait(&bar->k_empty[slot], ((j >> 1) & 1) ^ 1, st, abort_flag, 40)) break;
+        mbar_arrive_expect_tx(&bar->k_full[slot], 3 * kAtom);
+        for (int c = 0; c < 3; ++c)
+          tma_load_3d(smem + kKOff + (slot * 3 + c) * kAtom, &tmK, &bar->k_full[slot], 64 * c, j * 128, kv_row);
+        issued[slot]++;
+      }
+      mbar_wait(&bar->q_full, 0, st, nullptr, 41);
+      for (int s = 0; s < 2; ++s)
+        if (issued[s]) mbar_wait(&bar->k_full[s], (issued[s] - 1) & 1, st, nullptr, 41);
     }
-    for (int i = tid; i < kKB * 16; i += 256) {
-      const int r = i / 16, c = i % 16;
-      uint4 val = make_uint4(0, 0, 0, 0);
-      if (k0 + r < a.T) val = *reinterpret_cast<const uint4*>(a.v + (kv_base + k0 + r) * 128 + c * 8);
-      *reinterpret_cast<uint4*>(&sm.v[r * kVStride + c * 8]) = val;
+  } else if (warp == 6) {
+    if (lane == 0) {
+      // ---- V producer ----
+      tma_prefetch_desc(&tmV);
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        if (!mbar_wait(&bar->v_empty, (j & 1) ^ 1, st, abort_flag, 42)) break;
+        mbar_arrive_expect_tx(&bar->v_full, 2 * kAtom);
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d(smem + kVOff + c * kAtom, &tmV, &bar->v_full, 64 * c, j * 128, kv_row);
+        issued++;
+      }
+      if (issued) mbar_wait(&bar->v_full, (issued - 1) & 1, st, nullptr, 43);
     }
-    __syncthreads();
-
-    float s[16];
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer ----
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16(128, 128, false, true);
+      const uint32_t q_addr = smem_u32(smem + kQOff);
+      const uint32_t k_addr = smem_u32(smem + kKOff);
+      const uint32_t v_addr = smem_u32(smem + kVOff);
+      const uint32_t p_addr = smem_u32(smem + kPOff);
+      bool ok = mbar_wait(&bar->q_full, 0, st, abort_flag, 44);
+      auto issue_s = [&](int j) -> bool {
+        const int slot = j & 1;
+        if (!mbar_wait(&bar->k_full[slot], (j >> 1) & 1, st, abort_flag, 45)) return false;
+        if (!mbar_wait(&bar->s_free[slot], ((j >> 1) & 1) ^ 1, st, abort_flag, 46)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + slot * 128;
+        const uint32_t kb = k_addr + slot * 3 * kAtom;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) s[j] = 0.f;
-    const __nv_bfloat162* qrow = reinterpret_cast<const __nv_bfloat162*>(&sm.q[qi * kQStride]);
-#pragma unroll 4
-    for (int d2 = 0; d2 < 96; ++d2) {
-      const float2 qv = __bfloat1622float2(qrow[d2]);
+        for (int kk = 0; kk < 12; ++kk) {
+          const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+          umma_bf16(d, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idesc_s,
+                    kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bar->s_full[slot]);
+        umma_commit(&bar->k_empty[slot]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; j < n_kv && ok; ++j) {
+        if (j + 1 < n_kv && !issue_s(j + 1)) break;
+        if (!mbar_wait(&bar->p_full, j & 1, st, abort_flag, 47)) break;
+        if (!mbar_wait(&bar->v_full, j & 1, st, abort_flag, 48)) break;
+        tc_fence_after();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float2 kv = __bfloat1622float2(
-            reinterpret_cast<const __nv_bfloat162*>(&sm.k[(sub + 4 * j) * kKStride])[d2]);
-        s[j] = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, s[j]));
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t adesc = sdesc_sw128(p_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+          const uint64_t bdesc = sdesc_sw128(v_addr + kk * 2048, kAtom, 1024);
+          umma_bf16(tmem + 256, adesc, bdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&bar->pv_done);
+        umma_commit(&bar->v_empty);
+      }
+      umma_commit(&bar->drain);
+      mbar_wait(&bar->drain, 0, st, nullptr, 49);
+    }
+  } else {
+    // ---- softmax / correction / epilogue: warps 2..5, one thread per query row ----
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int qpos = q0 + row;
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    uint8_t* pbuf = smem + kPOff;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int slot = j & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar->s_full[slot], (j >> 1) & 1, st, abort_flag, 50));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s[128];
+      {
+        uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
+        uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
+        uint32_t (&s2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[64]);
+        uint32_t (&s3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[96]);
+        const uint32_t ta = tmem + lane_addr + slot * 128;
+        tmem_ld32(ta, s0);
+        tmem_ld32(ta + 32, s1);
+        tmem_ld32(ta + 64, s2);
+        tmem_ld32(ta + 96, s3);
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      mbar_arrive(&bar->s_free[slot]);
+      const bool diag = (j == n_kv - 1);
+      const int k0 = j * 128;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        float v = __uint_as_float(s[c]) * sl2;
+        if (diag && k0 + c > qpos) v = -INFINITY;
+        s[c] = __float_as_uint(v);
+        mx = fmaxf(mx, v);
+      }
+      const bool need = mx > m + kRescaleThreshold;
+      const float m_new = need ? mx : m;
+      const float alpha = need ? exp2f(m - m_new) : 1.f;
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const float p = exp2f(__uint_as_float(s[c]) - m_new);
+        s[c] = __float_as_uint(p);
+        sum += p;
+      }
+      l = l * alpha + sum;
+      m = m_new;
+      if (j > 0) {
+        // P buffer free and O final for tile j-1
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar->pv_done, (j - 1) & 1, st, abort_flag, 51));
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, need)) {
+          const uint32_t ta = tmem + lane_addr + 256;
+#pragma unroll 1
+          for (int c = 0; c < 128; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(ta + c, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(ta + c, r);
+          }
+          tmem_wait_st();
+        }
+      }
+      // P_j (bf16) into shared memory, K-major with 128-byte swizzle
+#pragma unroll
+      for (int c8 = 0; c8 < 16; ++c8) {
+        const int k = c8 * 8;
+        const uint4 v = make_uint4(pack_bf16x2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])),
+                                   pack_bf16x2(__uint_as_float(s[k + 2]), __uint_as_float(s[k + 3])),
+                                   pack_bf16x2(__uint_as_float(s[k + 4]), __uint_as_float(s[k + 5])),
+                                   pack_bf16x2(__uint_as_float(s[k + 6]), __uint_as_float(s[k + 7])));
+        *reinterpret_cast<uint4*>(pbuf + p_offset(row, k)) = v;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bar->p_full);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar->pv_done, (n_kv - 1) & 1, st, abort_flag, 52));
+    if (ok) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const uint32_t ta = tmem + lane_addr + 256;
+      __nv_bfloat16* dst = o + ((size_t)b * T + qpos) * 8192 + h * 128;
+#pragma unroll 1
+      for (int c = 0; c < 128; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(ta + c, r);
+        tmem_wait_ld();
+        if (qpos < T) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            d4[q] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * q]) * inv, __uint_as_float(r[8 * q + 1]) * inv),
+                               pack_bf16x2(__uint_as_float(r[8 * q + 2]) * inv, __uint_as_float(r[8 * q + 3]) * inv),
+                               pack_bf16x2(__uint_as_float(r[8 * q + 4]) * inv, __uint_as_float(r[8 * q + 5]) * inv),
+                               pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv, __uint_as_float(r[8 * q + 7]) * inv));
+        }
       }
     }
-    float mt = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int key = k0 + sub + 4 * j;
-      s[j] = (key <= qpos && key < a.T) ? s[j] * sl2 : -INFINITY;
-      mt = fmaxf(mt, s[j]);
-    }
-    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
-    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-    const float m_new = fmaxf(m_run, mt);
-    // rows beyond T see only masked keys: keep them finite
-    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-    const float alpha = exp2f(m_run - m_use);
-    float ls = 0.f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float p = exp2f(s[j] - m_use);
-      ls += p;
-      sm.p[qi][sub + 4 * j] = p;
-    }
-    ls += __shfl_xor_sync(0xffffffffu, ls, 1);
-    ls += __shfl_xor_sync(0xffffffffu, ls, 2);
-    l_run = l_run * alpha + ls;
-    m_run = m_new;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) o[i] *= alpha;
-    __syncwarp();
-#pragma unroll 2
-    for (int kj = 0; kj < kKB; ++kj) {
-      const float p = sm.p[qi][kj];
-      const __nv_bfloat162* vr = reinterpret_cast<const __nv_bfloat162*>(&sm.v[kj * kVStride + sub * 32]);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float2 vv = __bfloat1622float2(vr[e]);
-        o[2 * e] = fmaf(p, vv.x, o[2 * e]);
-        o[2 * e + 1] = fmaf(p, vv.y, o[2 * e + 1]);
-      }
-    }
   }
-  if (qpos < a.T) {
-    const float inv = 1.f / l_run;
-    uint32_t packed[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) packed[e] = pack_bf16x2(o[2 * e] * inv, o[2 * e + 1] * inv);
-    uint4* dst = reinterpret_cast<uint4*>(a.o + ((size_t)b * a.T + qpos) * 8192 + h * 128 + sub * 32);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -146,17 +296,23 @@ __global__ void __launch_bounds__(256) prefill_attn_cuda_core(const PrefillAttnA
 
 cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, const DevStatusHost& st, int num_sms,
                                      cudaStream_t stream) {
-  (void)st;
   (void)num_sms;
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_bf16_3d(&tq, a.q, 12288, a.T, a.B, 12288ull * 2, (uint64_t)a.T * 12288 * 2, 64, 128) ||
+      !make_tmap_bf16_3d(&tk, a.k, 192, a.T, (uint64_t)a.B * 64, 384, (uint64_t)a.cap * 384, 64, 128) ||
+      !make_tmap_bf16_3d(&tv, a.v, 128, a.T, (uint64_t)a.B * 64, 256, (uint64_t)a.cap * 256, 64, 128))
+    return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_attn_cuda_core, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)sizeof(PrefillSmem));
+    cudaError_t e = cudaFuncSetAttribute(prefill_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid((a.T + kQB - 1) / kQB, 64, a.B);
-  prefill_attn_cuda_core<<<grid, 256, sizeof(PrefillSmem), stream>>>(a);
+  const int n_qt = (a.T + 127) / 128;
+  dim3 grid(n_qt, 64, a.B);
+  DevStatus dst{st.word, st.wait_limit_ns};
+  prefill_attn_tc<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, a.o, a.T, n_qt, a.scale * 1.4426950408889634f,
+                                                           dst);
   return cudaGetLastError();
 }
 

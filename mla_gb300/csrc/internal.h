@@ -21,6 +21,11 @@ struct DevStatusHost {
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
                        uint32_t box_rows, uint32_t box_cols);
 
+// 3D bf16 tensor map over [outer][mid][inner] with byte strides for mid and
+// outer, box {box_inner, box_mid, 1}, 128-byte swizzle.
+bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid, uint64_t outer,
+                       uint64_t mid_stride_bytes, uint64_t outer_stride_bytes, uint32_t box_inner, uint32_t box_mid);
+
 // ---- GEMM (tcgen05, TMA, persistent) --------------------------------------
 // D[b][m, n] = sum_k A[m, a_col0 + b*a_col_step + k] * Bmat(b)[n, k]
 // A is K-major.  B is either K-major ([N, K] rows, weight layout) taken from
