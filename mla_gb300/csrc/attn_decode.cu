@@ -11,7 +11,7 @@
 // (2) Latent cache (576 values per position, key-value compression page):
 //     scores s_j = (q_lat . c_j + q_pe . k^R_j) * scale with q_lat = W_UK^T
 //     q_nope already formed by a GEMM, o_lat = sum_j p_j c_j; W_UV is applied
-//     afterwards by a GEMM.  CUDA-core version, one CTA per (batch, split).
+//     afterwards by a GEMM.  Tensor cores (tcgen05), one CTA per (batch, split).
 #include "common.cuh"
 #include "internal.h"
 
@@ -20,6 +20,7 @@ namespace mla {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThresholdLatent = 8.0f;  // log2 units
 
 // ---------------------------------------------------------------------------
 // rebuilt-cache decode
@@ -194,153 +195,289 @@ __global__ void combine_kernel(const float* __restrict__ part_o, const float2* _
 }
 
 // ---------------------------------------------------------------------------
-// latent-cache decode (CUDA cores)
+// latent-cache decode on tcgen05
+//
+// CTA = (sequence b, split of the key range), 192 threads:
+//   warp 0     TMA: q_lat [64 heads x 576] once; per 64-key tile the latent
+//              rows c_j [64 x 512] (8 boxes) and rotary keys k^R_j [64 x 64]
+//              into a 2-stage ring (3D tensor maps bound positions to L, so
+//              rows >= L read as zeros)
+//   warp 1     TMEM allocation; one lane issues
+//                S_j   = q_lat . [c_j ; k^R_j]^T      M=64 (heads) N=64 K=576
+//                O^T  += c_j^T . P_j^T               M=128 (latent, 4 blocks)
+//                                                    N=64 (heads) K=64 keys
+//              (O is kept transposed so the 512-wide latent output takes 256
+//              TMEM columns; c_j serves as the K-major B operand of S and the
+//              MN-major A operand of O^T without a copy)
+//   warps 2..5 softmax: head h = 16*(warp%4) + lane (lanes 0..15; an M=64
+//              accumulator row r lives in TMEM lane 32*(r/16) + r%16), lazy
+//              rescaling (O^T columns rescaled only when a head's max grows by
+//              more than 2^8), P_j [64 heads x 64 keys] bf16 to shared memory;
+//              at the end every thread writes the latent rows it holds.
 // ---------------------------------------------------------------------------
-constexpr int kLatChunk = 16;
-constexpr int kLatStages = 2;
-constexpr int kQStride = 584;  // bf16 per q_lat row in smem (576 + 8 pad)
+constexpr int kLatTile = 64;
+constexpr uint32_t kLatBox = 64 * 128;                       // 64 rows x 64 bf16
+constexpr uint32_t kLatQOff = 0;                             // 9 boxes
+constexpr uint32_t kLatCOff = 9 * kLatBox;                   // 2 stages x 8 boxes
+constexpr uint32_t kLatROff = kLatCOff + 16 * kLatBox;       // 2 stages x 1 box
+constexpr uint32_t kLatPOff = kLatROff + 2 * kLatBox;        // 1 box
+constexpr uint32_t kLatBarOff = kLatPOff + kLatBox;
+constexpr uint32_t kLatSmemBytes = kLatBarOff + 1536 + 1024;
 
-struct __align__(128) LatentSmem {
-  __nv_bfloat16 ckv[kLatStages][kLatChunk * 512];
-  __nv_bfloat16 kpe[kLatStages][kLatChunk * 64];
-  __nv_bfloat16 q[64 * kQStride];
-  uint64_t full[kLatStages];
+struct LatBars {
+  uint64_t q_full;
+  uint64_t c_full[2], c_empty[2];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full, pv_done, drain;
+  uint32_t tmem_slot;
+  int abort;
+  int need[2][4];
+  float alpha[2][64];
+  float m[64], l[64];
 };
 
-__global__ void __launch_bounds__(256) latent_attn_cuda_core(const LatentAttnArgs a, const DevStatus st,
-                                                             int chunk_len) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  LatentSmem& sm = *reinterpret_cast<LatentSmem*>(smem_raw);
+__device__ __forceinline__ void named_sync_128() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__global__ void __launch_bounds__(192, 1)
+    latent_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmC,
+                   const __grid_constant__ CUtensorMap tmR, const LatentAttnArgs a, const DevStatus st,
+                   int chunk_len) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  LatBars* bar = reinterpret_cast<LatBars*>(smem + kLatBarOff);
+  volatile int* abort_flag = &bar->abort;
   const int split = blockIdx.x;
   const int b = blockIdx.y;
-  const int tid = threadIdx.x;
-  const int h = tid >> 2;     // head of this thread
-  const int sub = tid & 3;    // key phase (scores) and latent quarter (P.V)
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int key_begin = split * chunk_len;
   const int key_end = min(a.L, key_begin + chunk_len);
-  const int nchunks = (key_end - key_begin + kLatChunk - 1) / kLatChunk;
-  const __nv_bfloat16* cbase = a.ckv + (size_t)b * a.cap * 512;
-  const __nv_bfloat16* rbase = a.kpe + (size_t)b * a.cap * 64;
+  const int n_tiles = (key_end - key_begin + kLatTile - 1) / kLatTile;
 
-  if (tid == 0) {
-    for (int i = 0; i < kLatStages; ++i) mbar_init(&sm.full[i], 1);
+  if (threadIdx.x == 0) {
+    mbar_init(&bar->q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar->c_full[i], 1);
+      mbar_init(&bar->c_empty[i], 1);
+      mbar_init(&bar->s_full[i], 1);
+      mbar_init(&bar->s_free[i], 128);
+    }
+    mbar_init(&bar->p_full, 128);
+    mbar_init(&bar->pv_done, 1);
+    mbar_init(&bar->drain, 1);
+    bar->abort = 0;
     fence_barrier_init();
   }
-  for (int i = tid; i < 64 * 72; i += 256) {
-    const int r = i / 72, c = i % 72;
-    *reinterpret_cast<uint4*>(&sm.q[r * kQStride + c * 8]) =
-        *reinterpret_cast<const uint4*>(a.qlat + ((size_t)b * 64 + r) * 576 + c * 8);
+  if (warp == 1) {
+    tmem_alloc(&bar->tmem_slot, 512);
+    tmem_relinquish();
   }
+  tc_fence_before();
   __syncthreads();
-  auto issue = [&](int c) {
-    const int stg = c % kLatStages;
-    const int k0 = key_begin + c * kLatChunk;
-    const int n = min(kLatChunk, key_end - k0);
-    mbar_arrive_expect_tx(&sm.full[stg], n * 1152);
-    bulk_load(sm.ckv[stg], cbase + (size_t)k0 * 512, n * 1024, &sm.full[stg]);
-    bulk_load(sm.kpe[stg], rbase + (size_t)k0 * 64, n * 128, &sm.full[stg]);
-  };
-  if (tid == 0)
-    for (int c = 0; c < kLatStages && c < nchunks; ++c) issue(c);
+  tc_fence_after();
+  const uint32_t tmem = bar->tmem_slot;
 
-  const float sl2 = a.scale * kLog2e;
-  float m_run = -INFINITY, l_run = 0.f;
-  float o[128];
-#pragma unroll
-  for (int i = 0; i < 128; ++i) o[i] = 0.f;
-  int c_fail = -1;
-  const __nv_bfloat162* qrow = reinterpret_cast<const __nv_bfloat162*>(&sm.q[h * kQStride]);
-
-  for (int c = 0; c < nchunks; ++c) {
-    const int stg = c % kLatStages;
-    const int k0 = key_begin + c * kLatChunk;
-    const int n = min(kLatChunk, key_end - k0);
-    const bool got = mbar_wait(&sm.full[stg], (c / kLatStages) & 1, st, nullptr, 30);
-    if (!__syncthreads_and(got)) {
-      c_fail = c;
-      break;
-    }
-    // scores for keys sub + 4i, i = 0..3
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
-    const __nv_bfloat162* cr = reinterpret_cast<const __nv_bfloat162*>(sm.ckv[stg]);
-    const __nv_bfloat162* rr = reinterpret_cast<const __nv_bfloat162*>(sm.kpe[stg]);
-#pragma unroll 4
-    for (int d2 = 0; d2 < 256; ++d2) {
-      const float2 qv = __bfloat1622float2(qrow[d2]);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 kv = __bfloat1622float2(cr[(sub + 4 * i) * 256 + d2]);
-        s[i] = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, s[i]));
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmC);
+      tma_prefetch_desc(&tmR);
+      mbar_arrive_expect_tx(&bar->q_full, 9 * kLatBox);
+      for (int c = 0; c < 9; ++c) tma_load_2d(smem + kLatQOff + c * kLatBox, &tmQ, &bar->q_full, 64 * c, b * 64);
+      int issued[2] = {0, 0};
+      for (int j = 0; j < n_tiles; ++j) {
+        const int stg = j & 1;
+        if (!mbar_wait(&bar->c_empty[stg], ((j >> 1) & 1) ^ 1, st, abort_flag, 60)) break;
+        const int k0 = key_begin + j * kLatTile;
+        mbar_arrive_expect_tx(&bar->c_full[stg], 9 * kLatBox);
+        for (int c = 0; c < 8; ++c)
+          tma_load_3d(smem + kLatCOff + (stg * 8 + c) * kLatBox, &tmC, &bar->c_full[stg], 64 * c, k0, b);
+        tma_load_3d(smem + kLatROff + stg * kLatBox, &tmR, &bar->c_full[stg], 0, k0, b);
+        issued[stg]++;
       }
+      mbar_wait(&bar->q_full, 0, st, nullptr, 61);
+      for (int i = 0; i < 2; ++i)
+        if (issued[i]) mbar_wait(&bar->c_full[i], (issued[i] - 1) & 1, st, nullptr, 61);
     }
-#pragma unroll 4
-    for (int d2 = 0; d2 < 32; ++d2) {
-      const float2 qv = __bfloat1622float2(qrow[256 + d2]);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(64, 64, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16(128, 64, true, false);
+      const uint32_t q_addr = smem_u32(smem + kLatQOff);
+      const uint32_t c_addr = smem_u32(smem + kLatCOff);
+      const uint32_t r_addr = smem_u32(smem + kLatROff);
+      const uint32_t p_addr = smem_u32(smem + kLatPOff);
+      bool ok = mbar_wait(&bar->q_full, 0, st, abort_flag, 62);
+      auto issue_s = [&](int j) -> bool {
+        const int stg = j & 1;
+        if (!mbar_wait(&bar->c_full[stg], (j >> 1) & 1, st, abort_flag, 63)) return false;
+        if (!mbar_wait(&bar->s_free[stg], ((j >> 1) & 1) ^ 1, st, abort_flag, 64)) return false;
+        tc_fence_after();
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 kv = __bfloat1622float2(rr[(sub + 4 * i) * 32 + d2]);
-        s[i] = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, s[i]));
+        for (int kk = 0; kk < 36; ++kk) {
+          const int box = kk >> 2;
+          const uint32_t koff = (kk & 3) * 32;
+          const uint32_t bb = (box < 8 ? c_addr + (stg * 8 + box) * kLatBox : r_addr + stg * kLatBox) + koff;
+          umma_bf16(tmem + stg * 64, sdesc_sw128(q_addr + box * kLatBox + koff, 16, 1024),
+                    sdesc_sw128(bb, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bar->s_full[stg]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        if (j + 1 < n_tiles && !issue_s(j + 1)) break;
+        if (!mbar_wait(&bar->p_full, j & 1, st, abort_flag, 65)) break;
+        tc_fence_after();
+        const uint32_t cb = c_addr + (j & 1) * 8 * kLatBox;
+#pragma unroll
+        for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t adesc = sdesc_sw128(cb + 2 * mb * kLatBox + kk * 2048, kLatBox, 1024);
+            const uint64_t bdesc = sdesc_sw128(p_addr + kk * 32, 16, 1024);
+            umma_bf16(tmem + 128 + mb * 64, adesc, bdesc, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit(&bar->pv_done);
+        umma_commit(&bar->c_empty[j & 1]);
       }
+      umma_commit(&bar->drain);
+      mbar_wait(&bar->drain, 0, st, nullptr, 66);
     }
-    float mt = -INFINITY;
+  } else {
+    const int quarter = warp & 3;
+    const int tid = threadIdx.x - 64;
+    const bool valid = lane < 16;
+    const int h = quarter * 16 + (lane & 15);
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    uint8_t* pbuf = smem + kLatPOff;
+    const float sl2 = a.scale * kLog2e;
+    float m = -INFINITY, l = 0.f;
+    // Every softmax warp runs every iteration and reaches every named barrier
+    // (bar.sync has no time limit); after a failed wait (ok == false) the
+    // work of the remaining iterations is skipped, the barriers are not.
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int stg = j & 1;
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&bar->s_full[stg], (j >> 1) & 1, st, abort_flag, 67));
+      uint32_t s[64];
+      if (ok) {
+        tc_fence_after();
+        uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
+        uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
+        tmem_ld32(tmem + lane_addr + stg * 64, s0);
+        tmem_ld32(tmem + lane_addr + stg * 64 + 32, s1);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bar->s_free[stg]);
+      } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      s[i] = (sub + 4 * i < n) ? s[i] * sl2 : -INFINITY;
-      mt = fmaxf(mt, s[i]);
-    }
-    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
-    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-    const float m_new = fmaxf(m_run, mt);
-    const float alpha = exp2f(m_run - m_new);
-    float p[4], ls = 0.f;
+        for (int c = 0; c < 64; ++c) s[c] = 0u;
+      }
+      const int k0 = key_begin + j * kLatTile;
+      float mx = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      p[i] = exp2f(s[i] - m_new);
-      ls += p[i];
-    }
-    ls += __shfl_xor_sync(0xffffffffu, ls, 1);
-    ls += __shfl_xor_sync(0xffffffffu, ls, 2);
-    l_run = l_run * alpha + ls;
-    m_run = m_new;
+      for (int c = 0; c < 64; ++c) {
+        const float v = (k0 + c < key_end) ? __uint_as_float(s[c]) * sl2 : -INFINITY;
+        s[c] = __float_as_uint(v);
+        mx = fmaxf(mx, v);
+      }
+      const bool need = valid && mx > m + kRescaleThresholdLatent;
+      const float m_new = need ? mx : m;
+      const float alpha = need ? exp2f(m - m_new) : 1.f;
+      float sum = 0.f;
 #pragma unroll
-    for (int i = 0; i < 128; ++i) o[i] *= alpha;
-    // P.V over latent dims sub*128 .. +127
-    const int lane_base = (threadIdx.x & 31) & ~3;
+      for (int c = 0; c < 64; ++c) {
+        const float p = exp2f(__uint_as_float(s[c]) - m_new);
+        s[c] = __float_as_uint(p);
+        sum += p;
+      }
+      l = l * alpha + sum;
+      m = m_new;
+      if (valid) bar->alpha[stg][h] = alpha;
+      const bool warp_need = __any_sync(0xffffffffu, need);
+      if (lane == 0) bar->need[stg][quarter] = warp_need ? 1 : 0;
+      named_sync_128();
+      const bool any_need = bar->need[stg][0] | bar->need[stg][1] | bar->need[stg][2] | bar->need[stg][3];
+      if (j > 0) ok = ok && __all_sync(0xffffffffu, mbar_wait(&bar->pv_done, (j - 1) & 1, st, abort_flag, 68));
+      if (!ok) continue;
+      if (j > 0) {
+        tc_fence_after();
+        if (any_need) {
 #pragma unroll 1
-    for (int j = 0; j < kLatChunk; ++j) {
-      const int pi = j >> 2;
-      const float psel = pi == 0 ? p[0] : pi == 1 ? p[1] : pi == 2 ? p[2] : p[3];
-      const float pj = __shfl_sync(0xffffffffu, psel, lane_base + (j & 3));
-      if (j < n) {
-        const __nv_bfloat162* vr = cr + j * 256 + sub * 64;
+          for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+              uint32_t r[32];
+              const uint32_t ta = tmem + lane_addr + 128 + mb * 64 + half * 32;
+              tmem_ld32(ta, r);
+              tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          const float2 vv = __bfloat1622float2(vr[e]);
-          o[2 * e] = fmaf(pj, vv.x, o[2 * e]);
-          o[2 * e + 1] = fmaf(pj, vv.y, o[2 * e + 1]);
+              for (int i = 0; i < 32; ++i)
+                r[i] = __float_as_uint(__uint_as_float(r[i]) * bar->alpha[stg][half * 32 + i]);
+              tmem_st32(ta, r);
+            }
+          }
+          tmem_wait_st();
         }
       }
+      if (valid) {
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const int k = c8 * 8;
+          const uint4 v = make_uint4(pack_bf16x2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])),
+                                     pack_bf16x2(__uint_as_float(s[k + 2]), __uint_as_float(s[k + 3])),
+                                     pack_bf16x2(__uint_as_float(s[k + 4]), __uint_as_float(s[k + 5])),
+                                     pack_bf16x2(__uint_as_float(s[k + 6]), __uint_as_float(s[k + 7])));
+          *reinterpret_cast<uint4*>(pbuf + h * 128 + ((c8 ^ (h & 7)) << 4)) = v;
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bar->p_full);
     }
-    __syncthreads();
-    if (tid == 0 && c + kLatStages < nchunks) issue(c + kLatStages);
-  }
-  if (c_fail >= 0) {
-    if (tid == 0)
-      for (int c = c_fail; c < nchunks && c < c_fail + kLatStages; ++c)
-        mbar_wait(&sm.full[c % kLatStages], (c / kLatStages) & 1, st, nullptr, 31);
-    return;
-  }
-  if (a.splits == 1) {
-    const float inv = 1.f / l_run;
-    uint32_t* dst = reinterpret_cast<uint32_t*>(a.olat + ((size_t)b * 64 + h) * 512 + sub * 128);
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar->pv_done, (n_tiles - 1) & 1, st, abort_flag, 69));
+    if (valid) {
+      bar->m[h] = m;
+      bar->l[h] = l;
+    }
+    named_sync_128();
+    if (ok) {
+      tc_fence_after();
+      const size_t prow = (size_t)b * a.splits + split;
+#pragma unroll 1
+      for (int mb = 0; mb < 4; ++mb) {
+        const int latent = mb * 128 + quarter * 32 + lane;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_addr + 128 + mb * 64 + half * 32, r);
+          tmem_wait_ld();
+          if (a.splits == 1) {
 #pragma unroll
-    for (int e = 0; e < 64; ++e) dst[e] = pack_bf16x2(o[2 * e] * inv, o[2 * e + 1] * inv);
-  } else {
-    const size_t pi = ((size_t)b * a.splits + split) * 64 + h;
-    float4* dst = reinterpret_cast<float4*>(a.part_o + pi * 512 + sub * 128);
+            for (int i = 0; i < 32; ++i) {
+              const int hh = half * 32 + i;
+              a.olat[((size_t)b * 64 + hh) * 512 + latent] = __float2bfloat16_rn(__uint_as_float(r[i]) / bar->l[hh]);
+            }
+          } else {
 #pragma unroll
-    for (int e = 0; e < 32; ++e) dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
-    if (sub == 0) a.part_ml[pi] = make_float2(m_run, l_run);
+            for (int i = 0; i < 32; ++i) {
+              const int hh = half * 32 + i;
+              a.part_o[(prow * 64 + hh) * 512 + latent] = __uint_as_float(r[i]);
+            }
+          }
+        }
+      }
+      if (a.splits > 1 && tid < 64) a.part_ml[prow * 64 + tid] = make_float2(bar->m[tid], bar->l[tid]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -411,27 +548,34 @@ cudaError_t launch_decode_attention(const DecodeAttnArgs& a, const DevStatusHost
 }
 
 int latent_splits(int B, int L, int num_sms) {
-  int s = (2 * num_sms + B - 1) / B;
-  const int max_s = (L + 63) / 64;
+  // one wave of CTAs: about one (sequence, split) per SM; the split partials
+  // cost 128 KB per (sequence, split), so large batches use few splits
+  int s = (num_sms + B / 2) / B;
+  const int max_s = (L + 255) / 256;
   if (s > max_s) s = max_s;
   if (s < 1) s = 1;
-  const int cl = chunk_len_for(L, s, kLatChunk);
+  const int cl = chunk_len_for(L, s, kLatTile);
   return (L + cl - 1) / cl;
 }
 
 cudaError_t launch_latent_attention(const LatentAttnArgs& a, const DevStatusHost& st, cudaStream_t stream,
                                     int* launches) {
+  CUtensorMap tq, tc, tr;
+  if (!make_tmap_bf16_2d(&tq, a.qlat, (uint64_t)a.B * 64, 576, 576, 64, 64) ||
+      !make_tmap_bf16_3d(&tc, a.ckv, 512, a.L, a.B, 1024, (uint64_t)a.cap * 1024, 64, 64) ||
+      !make_tmap_bf16_3d(&tr, a.kpe, 64, a.L, a.B, 128, (uint64_t)a.cap * 128, 64, 64))
+    return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(latent_attn_cuda_core, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)sizeof(LatentSmem));
+    cudaError_t e = cudaFuncSetAttribute(latent_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kLatSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int cl = chunk_len_for(a.L, a.splits, kLatChunk);
+  const int cl = chunk_len_for(a.L, a.splits, kLatTile);
   DevStatus dst{st.word, st.wait_limit_ns};
   dim3 grid(a.splits, a.B);
-  latent_attn_cuda_core<<<grid, 256, sizeof(LatentSmem), stream>>>(a, dst, cl);
+  latent_attn_tc<<<grid, 192, kLatSmemBytes, stream>>>(tq, tc, tr, a, dst, cl);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ++*launches;
