@@ -170,10 +170,10 @@ int mla_decode_latent(const mla_weights_t* w, const mla_params_t* params, const 
  * and allows no allocation of its own, such as inference-server plugins or
  * runtimes with a fixed memory budget, and latency-critical loops that cannot
  * afford the device synchronisation an allocation may cause).
- *   Scratch: a 16 MiB static device array inside the library, held by every
+ *   Scratch: a 64 MiB static device array inside the library, held by every
  *   GPU that loads the library until the process exits.  Batches whose
- *   mla_workspace_size(MLA_MODE_DECODE, B, P, cap) exceeds 16 MiB (about 240
- *   sequences) are rejected with MLA_ERR_WORKSPACE; nothing is allocated.
+ *   mla_workspace_size(MLA_MODE_DECODE, B, P, cap) exceeds 64 MiB (more than
+ *   455 sequences) are rejected with MLA_ERR_WORKSPACE; nothing is allocated.
  *   The first call on each device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
  *   Every call on a device shares the one array and it keeps the last call's

@@ -20,8 +20,13 @@ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 // Workspace carve-up.  Offsets are computed identically by the size query
 // and by the entry points.
 struct Layout {
-  size_t status, cs, xn, ca, cq, ckv, kpe, q, o, kscr, vscr, qlat, olat, part_o, part_ml, total;
+  size_t status, cs, xn, ca, cq, ckv, kpe, q, o, kscr, vscr, qlat, olat, part_o, part_ml, split, total;
+  size_t split_bytes;  // split-K partial slots (decode modes), 0 = none
 };
+
+// Status region: the device status word at byte 0, split-K counters from
+// byte 256 (kMaxSplitCounters ints); cleared at the start of every call.
+constexpr size_t kStatusRegion = 256 + kMaxSplitCounters * sizeof(int);
 
 Layout make_layout(int mode, int B, int t_or_p, int num_sms) {
   Layout L{};
@@ -33,7 +38,7 @@ Layout make_layout(int mode, int B, int t_or_p, int num_sms) {
     off = align256(off + bytes);
     return at;
   };
-  L.status = take(256);
+  L.status = take(kStatusRegion);
   L.cs = take(npos * 32 * sizeof(float2));
   L.xn = take(n * MLA_D * 2);
   L.ca = take(n * 2112 * 4);
@@ -56,8 +61,20 @@ Layout make_layout(int mode, int B, int t_or_p, int num_sms) {
     L.part_o = take((size_t)B * s * MLA_HEADS * MLA_KV_LORA * sizeof(float));
     L.part_ml = take((size_t)B * s * MLA_HEADS * sizeof(float2));
   }
+  if (mode != MLA_MODE_PREFILL) {
+    L.split_bytes = split_part_bytes(B);
+    L.split = take(L.split_bytes);
+  }
   L.total = off;
   return L;
+}
+
+// Split-K scratch for the small-M (decode) GEMMs.
+void set_split(EpiArgs& ea, void* ws, const Layout& L) {
+  if (!L.split_bytes) return;
+  ea.part = reinterpret_cast<float*>(static_cast<char*>(ws) + L.split);
+  ea.part_bytes = L.split_bytes;
+  ea.counters = reinterpret_cast<int*>(static_cast<char*>(ws) + L.status + 256);
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -156,6 +173,7 @@ int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok,
     EpiArgs ea{};
     ea.out_f32 = at<float>(ws, L.ca);
     ea.ldo = 2112;
+    set_split(ea, ws, L);
     MLA_TRY(launch_gemm(s, op, Epi::kStoreF32, ea, st, sms, stream));
     *launches += 1;
   }
@@ -195,6 +213,7 @@ int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok,
     ea.ldo = MLA_HEADS * MLA_QK;
     ea.cs = at<float2>(ws, L.cs);
     ea.t_mod = t_mod;
+    set_split(ea, ws, L);
     MLA_TRY(launch_gemm(s, op, Epi::kQRope, ea, st, sms, stream));
     *launches += 1;
   }
@@ -216,6 +235,7 @@ int kv_b_stage(const mla_weights_t* w, int n_tok, int t_mod, int t_off, __nv_bfl
   ea.t_mod = t_mod;
   ea.t_off = t_off;
   ea.cap = cap;
+  set_split(ea, ws, L);
   MLA_TRY(launch_gemm(s, op, Epi::kKVCache, ea, st, sms, stream));
   *launches += 1;
   return MLA_OK;
@@ -231,6 +251,7 @@ int o_proj_stage(const mla_weights_t* w, const Params& p, const void* x, void* o
   ea.ldo = MLA_D;
   ea.x = static_cast<const __nv_bfloat16*>(x);
   ea.delta = p.delta;
+  set_split(ea, ws, L);
   MLA_TRY(launch_gemm(s, op, Epi::kResidual, ea, st, sms, stream));
   *launches += 1;
   return MLA_OK;
@@ -316,7 +337,7 @@ int mla_prefill(const mla_weights_t* w, const mla_params_t* params, const void* 
   const DevStatusHost st{at<uint32_t>(workspace, L.status), kDefaultWaitLimitNs};
   Stager sg{p.timing, stream_};
   int launches = 0;
-  if (cudaMemsetAsync(st.word, 0, sizeof(uint32_t), stream_) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaMemsetAsync(st.word, 0, kStatusRegion, stream_) != cudaSuccess) return MLA_ERR_CUDA;
 
   rc = front_end(w, p, x, (int)n_tok, T, 0, T, 0, static_cast<__nv_bfloat16*>(ckv_cache),
                  static_cast<__nv_bfloat16*>(kpe_cache), cap, workspace, L, st, sms, stream_, sg, &launches,
@@ -373,7 +394,7 @@ int mla_decode(const mla_weights_t* w, const mla_params_t* params, const void* x
   const DevStatusHost st{at<uint32_t>(workspace, L.status), kDefaultWaitLimitNs};
   Stager sg{p.timing, stream_};
   int launches = 0;
-  if (cudaMemsetAsync(st.word, 0, sizeof(uint32_t), stream_) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaMemsetAsync(st.word, 0, kStatusRegion, stream_) != cudaSuccess) return MLA_ERR_CUDA;
   rc = front_end(w, p, x, B, 1, P, 1, P, nullptr, nullptr, cap, workspace, L, st, sms, stream_, sg, &launches);
   if (rc) return rc;
 
@@ -428,7 +449,7 @@ int mla_decode_latent(const mla_weights_t* w, const mla_params_t* params, const 
   const DevStatusHost st{at<uint32_t>(workspace, L.status), kDefaultWaitLimitNs};
   Stager sg{p.timing, stream_};
   int launches = 0;
-  if (cudaMemsetAsync(st.word, 0, sizeof(uint32_t), stream_) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaMemsetAsync(st.word, 0, kStatusRegion, stream_) != cudaSuccess) return MLA_ERR_CUDA;
   rc = front_end(w, p, x, B, 1, P, 1, P, static_cast<__nv_bfloat16*>(ckv_cache),
                  static_cast<__nv_bfloat16*>(kpe_cache), cap, workspace, L, st, sms, stream_, sg, &launches);
   if (rc) return rc;
@@ -445,6 +466,7 @@ int mla_decode_latent(const mla_weights_t* w, const mla_params_t* params, const 
     ea.ldo = MLA_HEADS * 576;
     ea.c_col0 = 0;
     ea.c_col_step = 576;
+    set_split(ea, workspace, L);
     MLA_TRY(launch_gemm(s, op, Epi::kStoreBf16, ea, st, sms, stream_));
     MLA_TRY(launch_copy_qpe(at<__nv_bfloat16>(workspace, L.q), at<__nv_bfloat16>(workspace, L.qlat), B, stream_));
     launches += 2;
@@ -480,6 +502,7 @@ int mla_decode_latent(const mla_weights_t* w, const mla_params_t* params, const 
     ea.ldo = MLA_HEADS * MLA_V;
     ea.c_col0 = 0;
     ea.c_col_step = MLA_V;
+    set_split(ea, workspace, L);
     MLA_TRY(launch_gemm(s, op, Epi::kStoreBf16, ea, st, sms, stream_));
     launches += 1;
   }

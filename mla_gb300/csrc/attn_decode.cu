@@ -308,39 +308,52 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t r_addr = smem_u32(smem + kLatROff);
       const uint32_t p_addr = smem_u32(smem + kLatPOff);
       bool ok = mbar_wait(&bar->q_full, 0, st, abort_flag, 62);
-      auto issue_s = [&](int j) -> bool {
-        const int stg = j & 1;
-        if (!mbar_wait(&bar->c_full[stg], (j >> 1) & 1, st, abort_flag, 63)) return false;
-        if (!mbar_wait(&bar->s_free[stg], ((j >> 1) & 1) ^ 1, st, abort_flag, 64)) return false;
-        tc_fence_after();
+      tc_fence_after();
+      // Event loop: S_j needs its latent tile and a free score buffer; P.V_j
+      // needs P_j.  Issue whichever is ready (S at most two tiles ahead), so
+      // that a P.V never waits behind the load of a later tile.
+      int next_s = 0, next_pv = 0;
+      Watchdog wd;
+      wd.reset();
+      while (ok && next_pv < n_tiles) {
+        bool progress = false;
+        if (next_s < n_tiles && next_s <= next_pv + 1) {
+          const int stg = next_s & 1;
+          const uint32_t ph = (next_s >> 1) & 1;
+          if (mbar_test(&bar->c_full[stg], ph) && mbar_test(&bar->s_free[stg], ph ^ 1)) {
+            tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 36; ++kk) {
-          const int box = kk >> 2;
-          const uint32_t koff = (kk & 3) * 32;
-          const uint32_t bb = (box < 8 ? c_addr + (stg * 8 + box) * kLatBox : r_addr + stg * kLatBox) + koff;
-          umma_bf16(tmem + stg * 64, sdesc_sw128(q_addr + box * kLatBox + koff, 16, 1024),
-                    sdesc_sw128(bb, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&bar->s_full[stg]);
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        if (j + 1 < n_tiles && !issue_s(j + 1)) break;
-        if (!mbar_wait(&bar->p_full, j & 1, st, abort_flag, 65)) break;
-        tc_fence_after();
-        const uint32_t cb = c_addr + (j & 1) * 8 * kLatBox;
-#pragma unroll
-        for (int mb = 0; mb < 4; ++mb) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t adesc = sdesc_sw128(cb + 2 * mb * kLatBox + kk * 2048, kLatBox, 1024);
-            const uint64_t bdesc = sdesc_sw128(p_addr + kk * 32, 16, 1024);
-            umma_bf16(tmem + 128 + mb * 64, adesc, bdesc, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 36; ++kk) {
+              const int box = kk >> 2;
+              const uint32_t koff = (kk & 3) * 32;
+              const uint32_t bb = (box < 8 ? c_addr + (stg * 8 + box) * kLatBox : r_addr + stg * kLatBox) + koff;
+              umma_bf16(tmem + stg * 64, sdesc_sw128(q_addr + box * kLatBox + koff, 16, 1024),
+                        sdesc_sw128(bb, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&bar->s_full[stg]);
+            ++next_s;
+            progress = true;
           }
         }
-        umma_commit(&bar->pv_done);
-        umma_commit(&bar->c_empty[j & 1]);
+        if (next_pv < next_s && mbar_test(&bar->p_full, next_pv & 1)) {
+          tc_fence_after();
+          const uint32_t cb = c_addr + (next_pv & 1) * 8 * kLatBox;
+#pragma unroll
+          for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t adesc = sdesc_sw128(cb + 2 * mb * kLatBox + kk * 2048, kLatBox, 1024);
+              const uint64_t bdesc = sdesc_sw128(p_addr + kk * 32, 16, 1024);
+              umma_bf16(tmem + 128 + mb * 64, adesc, bdesc, idesc_o, (next_pv > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          umma_commit(&bar->pv_done);
+          umma_commit(&bar->c_empty[next_pv & 1]);
+          ++next_pv;
+          progress = true;
+        }
+        if (progress) wd.reset();
+        else if (wd.expired(st, abort_flag, 63)) break;
       }
       umma_commit(&bar->drain);
       mbar_wait(&bar->drain, 0, st, nullptr, 66);

@@ -141,37 +141,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t v_addr = smem_u32(smem + kVOff);
       const uint32_t p_addr = smem_u32(smem + kPOff);
       bool ok = mbar_wait(&bar->q_full, 0, st, abort_flag, 44);
-      auto issue_s = [&](int j) -> bool {
-        const int slot = j & 1;
-        if (!mbar_wait(&bar->k_full[slot], (j >> 1) & 1, st, abort_flag, 45)) return false;
-        if (!mbar_wait(&bar->s_free[slot], ((j >> 1) & 1) ^ 1, st, abort_flag, 46)) return false;
-        tc_fence_after();
-        const uint32_t d = tmem + slot * 128;
-        const uint32_t kb = k_addr + slot * 3 * kAtom;
+      tc_fence_after();
+      // Event loop: issue S_j (needs K_j and a free score buffer) and PV_j
+      // (needs P_j and V_j) in whatever order their inputs become ready, at
+      // most two score tiles ahead of the P.V tiles.
+      int next_s = 0, next_pv = 0;
+      Watchdog wd;
+      wd.reset();
+      while (ok && next_pv < n_kv) {
+        bool progress = false;
+        if (next_s < n_kv && next_s <= next_pv + 1) {
+          const int slot = next_s & 1;
+          const uint32_t ph = (next_s >> 1) & 1;
+          if (mbar_test(&bar->k_full[slot], ph) && mbar_test(&bar->s_free[slot], ph ^ 1)) {
+            tc_fence_after();
+            const uint32_t d = tmem + slot * 128;
+            const uint32_t kb = k_addr + slot * 3 * kAtom;
 #pragma unroll
-        for (int kk = 0; kk < 12; ++kk) {
-          const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-          umma_bf16(d, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idesc_s,
-                    kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 12; ++kk) {
+              const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+              umma_bf16(d, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idesc_s,
+                        kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&bar->s_full[slot]);
+            umma_commit(&bar->k_empty[slot]);
+            ++next_s;
+            progress = true;
+          }
         }
-        umma_commit(&bar->s_full[slot]);
-        umma_commit(&bar->k_empty[slot]);
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; j < n_kv && ok; ++j) {
-        if (j + 1 < n_kv && !issue_s(j + 1)) break;
-        if (!mbar_wait(&bar->p_full, j & 1, st, abort_flag, 47)) break;
-        if (!mbar_wait(&bar->v_full, j & 1, st, abort_flag, 48)) break;
-        tc_fence_after();
+        if (next_pv < next_s && mbar_test(&bar->p_full, next_pv & 1) && mbar_test(&bar->v_full, next_pv & 1)) {
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t adesc = sdesc_sw128(p_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
-          const uint64_t bdesc = sdesc_sw128(v_addr + kk * 2048, kAtom, 1024);
-          umma_bf16(tmem + 256, adesc, bdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t adesc = sdesc_sw128(p_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+            const uint64_t bdesc = sdesc_sw128(v_addr + kk * 2048, kAtom, 1024);
+            umma_bf16(tmem + 256, adesc, bdesc, idesc_pv, (next_pv > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&bar->pv_done);
+          umma_commit(&bar->v_empty);
+          ++next_pv;
+          progress = true;
         }
-        umma_commit(&bar->pv_done);
-        umma_commit(&bar->v_empty);
+        if (progress) wd.reset();
+        else if (wd.expired(st, abort_flag, 45)) break;
       }
       umma_commit(&bar->drain);
       mbar_wait(&bar->drain, 0, st, nullptr, 49);

@@ -67,6 +67,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase of `parity`.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Progress watchdog for event loops that poll several barriers: reports a
+// timeout when no progress was made for the status's time limit.
+struct Watchdog {
+  uint64_t last;
+  __device__ __forceinline__ void reset() { last = globaltimer_ns(); }
+  __device__ __forceinline__ bool expired(const DevStatus& st, volatile int* abort, uint32_t site) {
+    if (abort && *abort) return true;
+    if (globaltimer_ns() - last > st.wait_limit_ns) {
+      report_timeout(st, site);
+      if (abort) *abort = 1;
+      return true;
+    }
+    return false;
+  }
+};
+
 // Wait for the phase of `parity` to complete, giving up after the status's
 // time limit (or as soon as *abort is set by another warp of the CTA).
 // Returns false on give-up; the caller then stops issuing work.

@@ -57,16 +57,69 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const uint32_t 
   }
 }
 
-template <int BN, Epi EPI>
-__device__ __forceinline__ void run_epilogue(const EpiArgs& ea, uint32_t taddr, int batch, int row, int n0,
+// Accumulator sources for the epilogue: the tile in tensor memory, or (after
+// a split-K reduction) the float32 partial slots in global memory.
+struct TmemSrc {
+  uint32_t taddr;
+  __device__ __forceinline__ void operator()(int c, uint32_t (&r)[32]) const {
+    tmem_ld32(taddr + c, r);
+    tmem_wait_ld();
+  }
+};
+
+struct PartSrc {
+  const float* base;    // this row's slot 0
+  size_t slot_stride;   // floats between slots
+  int slots;
+  bool ok;
+  __device__ __forceinline__ void operator()(int c, uint32_t (&r)[32]) const {
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+    if (ok) {
+      int sl = 0;
+      for (; sl + 2 <= slots; sl += 2) {  // two slots (16 loads) in flight
+        float4 v[16];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            v[8 * u + j] = __ldcg(reinterpret_cast<const float4*>(base + (sl + u) * slot_stride + c) + j);
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            acc[4 * j] += v[8 * u + j].x;
+            acc[4 * j + 1] += v[8 * u + j].y;
+            acc[4 * j + 2] += v[8 * u + j].z;
+            acc[4 * j + 3] += v[8 * u + j].w;
+          }
+      }
+      for (; sl < slots; ++sl) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(base + sl * slot_stride + c) + j);
+          acc[4 * j] += v.x;
+          acc[4 * j + 1] += v.y;
+          acc[4 * j + 2] += v.z;
+          acc[4 * j + 3] += v.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(acc[i]);
+  }
+};
+
+template <int BN, Epi EPI, class Src>
+__device__ __forceinline__ void run_epilogue(const EpiArgs& ea, const Src& ld, int batch, int row, int n0,
                                              bool row_ok) {
   if constexpr (EPI == Epi::kStoreBf16) {
     __nv_bfloat16* dst = ea.out + (size_t)row * ea.ldo + ea.c_col0 + batch * ea.c_col_step + n0;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t r[32];
-      tmem_ld32(taddr + c, r);
-      tmem_wait_ld();
+      ld(c, r);
       if (row_ok) store32_bf16(dst + c, r);
     }
   } else if constexpr (EPI == Epi::kStoreF32) {
@@ -74,8 +127,7 @@ __device__ __forceinline__ void run_epilogue(const EpiArgs& ea, uint32_t taddr, 
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t r[32];
-      tmem_ld32(taddr + c, r);
-      tmem_wait_ld();
+      ld(c, r);
       if (row_ok) {
         float4* d = reinterpret_cast<float4*>(dst + c);
 #pragma unroll
@@ -85,47 +137,53 @@ __device__ __forceinline__ void run_epilogue(const EpiArgs& ea, uint32_t taddr, 
       }
     }
   } else if constexpr (EPI == Epi::kQRope) {
-    static_assert(BN == 192, "q_b epilogue works on one 192-wide head per tile");
+    // the tile covers columns o0 .. o0+BN-1 of one 192-wide head:
+    // [128 nope | 64 pe], RoPE pairs (128+i, 160+i) always in the same tile
+    static_assert(BN == 192 || BN == 96, "q_b epilogue works on whole or half heads");
+    const int o0 = n0 % 192;
+    const int nope_cols = (o0 + BN < 128 ? o0 + BN : 128) - o0;
     __nv_bfloat16* dst = ea.out + (size_t)row * ea.ldo + n0;
 #pragma unroll 1
-    for (int c = 0; c < 128; c += 32) {
+    for (int c = 0; c < nope_cols; c += 32) {
       uint32_t r[32];
-      tmem_ld32(taddr + c, r);
-      tmem_wait_ld();
+      ld(c, r);
       if (row_ok) store32_bf16(dst + c, r);
     }
-    uint32_t x1[32], x2[32];
-    tmem_ld32(taddr + 128, x1);
-    tmem_ld32(taddr + 160, x2);
-    tmem_wait_ld();
-    if (row_ok) {
-      const float2* cs = ea.cs + (size_t)(row % ea.t_mod) * 32;
+    if (o0 + BN == 192) {
+      uint32_t x1[32], x2[32];
+      ld(nope_cols, x1);
+      ld(nope_cols + 32, x2);
+      if (row_ok) {
+        const float2* cs = ea.cs + (size_t)(row % ea.t_mod) * 32;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float2 t = cs[i];
-        float a = __uint_as_float(x1[i]), b = __uint_as_float(x2[i]);
-        x1[i] = __float_as_uint(a * t.x - b * t.y);
-        x2[i] = __float_as_uint(b * t.x + a * t.y);
+        for (int i = 0; i < 32; ++i) {
+          float2 t = cs[i];
+          float a = __uint_as_float(x1[i]), b = __uint_as_float(x2[i]);
+          x1[i] = __float_as_uint(a * t.x - b * t.y);
+          x2[i] = __float_as_uint(b * t.x + a * t.y);
+        }
+        store32_bf16(dst + nope_cols, x1);
+        store32_bf16(dst + nope_cols + 32, x2);
       }
-      store32_bf16(dst + 128, x1);
-      store32_bf16(dst + 160, x2);
     }
   } else if constexpr (EPI == Epi::kKVCache) {
-    static_assert(BN == 256, "kv_b epilogue works on one 256-wide head per tile");
+    // the tile covers columns o0 .. o0+BN-1 of one 256-wide head [128 k_nope | 128 v]
+    static_assert(BN == 256 || BN == 128, "kv_b epilogue works on whole or half heads");
     const int h = n0 / 256;
+    const int o0 = n0 % 256;
     const int b = row_ok ? row / ea.t_mod : 0;
     const int t = ea.t_off + (row_ok ? row % ea.t_mod : 0);
     const size_t slot = ((size_t)b * 64 + h) * ea.cap + t;
     __nv_bfloat16* krow = ea.kc + slot * 192;
     __nv_bfloat16* vrow = ea.vc + slot * 128;
 #pragma unroll 1
-    for (int c = 0; c < 256; c += 32) {
+    for (int c = 0; c < BN; c += 32) {
       uint32_t r[32];
-      tmem_ld32(taddr + c, r);
-      tmem_wait_ld();
-      if (row_ok) store32_bf16(c < 128 ? krow + c : vrow + (c - 128), r);
+      ld(c, r);
+      const int col = o0 + c;
+      if (row_ok) store32_bf16(col < 128 ? krow + col : vrow + (col - 128), r);
     }
-    if (row_ok) {
+    if (row_ok && o0 == 0) {
       const uint4* src = reinterpret_cast<const uint4*>(ea.kpe + (size_t)row * 64);
       uint4* dst = reinterpret_cast<uint4*>(krow + 128);
 #pragma unroll
@@ -136,8 +194,7 @@ __device__ __forceinline__ void run_epilogue(const EpiArgs& ea, uint32_t taddr, 
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t r[32];
-      tmem_ld32(taddr + c, r);
-      tmem_wait_ld();
+      ld(c, r);
       if (row_ok) {
         if (ea.delta) {
           float4* dd = reinterpret_cast<float4*>(ea.delta + base + c);
@@ -188,6 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = s.N / BN;
   const int num_tiles = s.batches * m_tiles * n_tiles;
   const int kblocks = s.K / kBK;
+  const int ksplit = s.ksplit;
+  const int num_units = num_tiles * ksplit;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -225,7 +284,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < STAGES; ++i) issued[i] = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
+        const int tile = unit / ksplit;
+        const int kb0 = (unit % ksplit) * s.kb_per;
+        const int kb1 = min(kblocks, kb0 + s.kb_per);
         const int n_blk = tile % n_tiles;
         const int m_blk = (tile / n_tiles) % m_tiles;
         const int batch = tile / (n_tiles * m_tiles);
@@ -234,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b_row = s.b_row0 + batch * s.b_row_step;
         const CUtensorMap* mb = (n0 < s.n_split) ? &tmB0 : &tmB1;
         const int nb = (n0 < s.n_split) ? n0 : n0 - s.n_split;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, st, abort_flag, 1)) {
             ok = false;
             break;
@@ -271,11 +333,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
+        const int kb0 = (unit % ksplit) * s.kb_per;
+        const int kb1 = min(kblocks, kb0 + s.kb_per);
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, st, abort_flag, 3)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, st, abort_flag, 4)) {
             ok = false;
             break;
@@ -291,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               bdesc = sdesc_sw128(b_addr + k * 2048, 64 * 128, 1024);
             else
               bdesc = sdesc_sw128(b_addr + k * 32, 16, 1024);
-            umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_bf16(d_tmem, adesc, bdesc, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           }
           umma_commit(&empty_bar[stage]);
           if (++stage == STAGES) {
@@ -311,20 +375,57 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     const int quarter = warp & 3;
+    const int rit = quarter * 32 + lane;  // row within the tile
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    for (int unit = blockIdx.x; unit < num_units; unit += gridDim.x) {
+      const int tile = unit / ksplit;
+      const int ks = unit % ksplit;
       const int n_blk = tile % n_tiles;
       const int m_blk = (tile / n_tiles) % m_tiles;
       const int batch = tile / (n_tiles * m_tiles);
       bool ok = mbar_wait(&tfull_bar[acc], acc_phase, st, abort_flag, 6);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const int row = m_blk * kBM + quarter * 32 + lane;
+      const int row = m_blk * kBM + rit;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      run_epilogue<BN, EPI>(ea, taddr, batch, row, n_blk * BN, row < s.M);
-      tc_fence_before();
-      mbar_arrive(&tempty_bar[acc]);
+      if (ksplit == 1) {
+        run_epilogue<BN, EPI>(ea, TmemSrc{taddr}, batch, row, n_blk * BN, row < s.M);
+        tc_fence_before();
+        mbar_arrive(&tempty_bar[acc]);
+      } else {
+        // this K slice's partial -> its slot; the last warp of the quarter reduces
+        const int rows_pt = s.M < kBM ? s.M : kBM;
+        const bool in_slot = row < s.M && rit < rows_pt;
+        float* slot = ea.part + ((size_t)(tile * ksplit + ks) * rows_pt + (in_slot ? rit : 0)) * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c, r);
+          tmem_wait_ld();
+          if (in_slot) {
+            float4* d = reinterpret_cast<float4*>(slot + c);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              d[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty_bar[acc]);
+        __threadfence();
+        __syncwarp();
+        int prev = 0;
+        if (lane == 0) prev = atomicAdd(&ea.counters[tile * 4 + quarter], 1);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == ksplit - 1) {
+          __threadfence();
+          const PartSrc src{ea.part + ((size_t)tile * ksplit * rows_pt + (in_slot ? rit : 0)) * BN,
+                            (size_t)rows_pt * BN, ksplit, in_slot};
+          run_epilogue<BN, EPI>(ea, src, batch, row, n_blk * BN, row < s.M);
+          if (lane == 0) ea.counters[tile * 4 + quarter] = 0;  // ready for the next GEMM
+        }
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
@@ -360,10 +461,30 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const int tiles = s.batches * ((s.M + kBM - 1) / kBM) * (s.N / BN);
-  const int grid = tiles < num_sms ? tiles : num_sms;
+  GemmShape sh = s;
+  const int m_tiles = (s.M + kBM - 1) / kBM;
+  const int tiles = s.batches * m_tiles * (s.N / BN);
+  const int kblocks = s.K / kBK;
+  sh.ksplit = 1;
+  sh.kb_per = kblocks;
+  if (ea.part && ea.counters && m_tiles == 1 && tiles * 2 <= num_sms && kblocks >= 2 &&
+      tiles * 4 <= kMaxSplitCounters) {
+    int ks = num_sms / tiles;
+    if (ks > 4) ks = 4;  // the reduction reads every slice: keep it short
+    if (ks > kMaxSplitUnits / tiles) ks = kMaxSplitUnits / tiles;
+    if (ks > kblocks) ks = kblocks;
+    const int kb_per = (kblocks + ks - 1) / ks;
+    ks = (kblocks + kb_per - 1) / kb_per;
+    const size_t need = (size_t)tiles * ks * s.M * BN * sizeof(float);
+    if (ks > 1 && need <= ea.part_bytes) {
+      sh.ksplit = ks;
+      sh.kb_per = kb_per;
+    }
+  }
+  const int units = tiles * sh.ksplit;
+  const int grid = units < num_sms ? units : num_sms;
   DevStatus dst{st.word, st.wait_limit_ns};
-  kern<<<grid, kThreads, L::kBytes, stream>>>(ta, tb0, tb1, s, ea, dst);
+  kern<<<grid, kThreads, L::kBytes, stream>>>(ta, tb0, tb1, sh, ea, dst);
   return cudaGetLastError();
 }
 
@@ -372,18 +493,25 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
 cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, const EpiArgs& ea,
                         const DevStatusHost& st, int num_sms, cudaStream_t stream) {
   if (s.M <= 0 || s.K % kBK != 0 || s.batches <= 0) return cudaErrorInvalidValue;
+  // Few rows (decode: M <= 128): narrower tiles so that enough CTAs stream
+  // the weights; many rows (prefill): wide tiles, fewer re-reads of A.
+  const bool small = s.M <= kBM;
   switch (epi) {
     case Epi::kQRope:
       if (s.N % 192 || op.b_mn_major) return cudaErrorInvalidValue;
+      if (small) return launch_impl<96, 7, Epi::kQRope, false>(s, op, ea, st, num_sms, stream);
       return launch_impl<192, 5, Epi::kQRope, false>(s, op, ea, st, num_sms, stream);
     case Epi::kKVCache:
       if (s.N % 256 || op.b_mn_major) return cudaErrorInvalidValue;
+      if (small) return launch_impl<128, 6, Epi::kKVCache, false>(s, op, ea, st, num_sms, stream);
       return launch_impl<256, 4, Epi::kKVCache, false>(s, op, ea, st, num_sms, stream);
     case Epi::kResidual:
       if (s.N % 256 || op.b_mn_major) return cudaErrorInvalidValue;
+      if (small) return launch_impl<64, 8, Epi::kResidual, false>(s, op, ea, st, num_sms, stream);
       return launch_impl<256, 4, Epi::kResidual, false>(s, op, ea, st, num_sms, stream);
     case Epi::kStoreF32:
       if (s.N % 192 || s.n_split % 192 || op.b_mn_major) return cudaErrorInvalidValue;
+      if (small) return launch_impl<64, 8, Epi::kStoreF32, false>(s, op, ea, st, num_sms, stream);
       return launch_impl<192, 5, Epi::kStoreF32, false>(s, op, ea, st, num_sms, stream);
     case Epi::kStoreBf16:
     default:
@@ -391,6 +519,8 @@ cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, con
         if (s.N % 128) return cudaErrorInvalidValue;
         return launch_impl<128, 6, Epi::kStoreBf16, true>(s, op, ea, st, num_sms, stream);
       }
+      if (small && s.N % 64 == 0 && s.n_split % 64 == 0)
+        return launch_impl<64, 8, Epi::kStoreBf16, false>(s, op, ea, st, num_sms, stream);
       if (s.N % 192 == 0 && s.n_split % 192 == 0)
         return launch_impl<192, 5, Epi::kStoreBf16, false>(s, op, ea, st, num_sms, stream);
       if (s.N % 128 == 0 && s.n_split % 128 == 0)

@@ -38,7 +38,18 @@ struct GemmShape {
   int a_col0, a_col_step;
   int b_row0, b_row_step;
   int n_split;
+  int ksplit;   // set by launch_gemm: K slices per tile (1 = no split)
+  int kb_per;   // set by launch_gemm: 64-wide K blocks per slice
 };
+
+// Split-K (used when a GEMM has too few output tiles to fill the GPU, as
+// the decode projections with M <= 128 do): each CTA of a tile's K slice
+// writes its float32 partial to its own slot; the last warp to finish a
+// 32-row slice of the tile (counter per tile and quarter) sums the slots in
+// slice order and runs the epilogue.  Units = tiles x slices <= kMaxSplitUnits.
+constexpr int kMaxSplitUnits = 160;
+constexpr int kMaxSplitCounters = 960;
+inline size_t split_part_bytes(int M) { return (size_t)kMaxSplitUnits * (M < 128 ? M : 128) * 256 * sizeof(float); }
 
 struct GemmOperands {
   const __nv_bfloat16* A;
@@ -75,6 +86,10 @@ struct EpiArgs {
   // kResidual: out[row, n] = x[row, n] + acc; delta[row, n] = acc (optional)
   const __nv_bfloat16* x;
   float* delta;
+  // split-K scratch (null: no split): partial slots and zeroed counters
+  float* part;
+  size_t part_bytes;
+  int* counters;
 };
 
 cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, const EpiArgs& ea,
