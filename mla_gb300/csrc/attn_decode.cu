@@ -390,19 +390,21 @@ __global__ void __launch_bounds__(192, 1)
       }
       const int k0 = key_begin + j * kLatTile;
       float mx = -INFINITY;
+      if (k0 + kLatTile > key_end) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float v = (k0 + c < key_end) ? __uint_as_float(s[c]) * sl2 : -INFINITY;
-        s[c] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
+        for (int c = 0; c < 64; ++c)
+          if (k0 + c >= key_end) s[c] = __float_as_uint(-INFINITY);
       }
+#pragma unroll
+      for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+      mx *= sl2;  // log2 units (the scale is positive)
       const bool need = valid && mx > m + kRescaleThresholdLatent;
       const float m_new = need ? mx : m;
-      const float alpha = need ? exp2f(m - m_new) : 1.f;
+      const float alpha = need ? ex2_approx(m - m_new) : 1.f;
       float sum = 0.f;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float p = exp2f(__uint_as_float(s[c]) - m_new);
+        const float p = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -m_new));
         s[c] = __float_as_uint(p);
         sum += p;
       }

@@ -7,8 +7,9 @@
 //
 // CTA = (128-query tile, head, sequence), heaviest tiles launched first.
 // Warp roles (224 threads):
-//   warp 0   TMA: the Q tile once, then K tiles into a 2-slot ring
-//   warp 6   TMA: V tiles into a 1-slot buffer
+//   warp 0   TMA: the Q tile once, then K tiles into a 1-slot buffer
+//   warp 6   TMA: V tiles into a 2-slot ring (each V tile is requested a
+//            whole tile ahead of the P.V that reads it)
 //   warp 1   TMEM allocation; one lane issues the MMAs:
 //              S_j = Q K_j^T   M=128 N=128 K=192, into one of two TMEM buffers
 //              O  += P_j V_j   M=128 N=128 K=128, P from shared memory,
@@ -32,17 +33,17 @@ namespace {
 constexpr int kThreads = 224;
 constexpr uint32_t kAtom = 128 * 128;            // 128 rows x 64 bf16
 constexpr uint32_t kQOff = 0;                    // 3 atoms
-constexpr uint32_t kKOff = 3 * kAtom;            // 2 slots x 3 atoms
-constexpr uint32_t kVOff = 9 * kAtom;            // 2 atoms (vdim 0-63, 64-127)
-constexpr uint32_t kPOff = 11 * kAtom;           // 2 atoms (keys 0-63, 64-127)
-constexpr uint32_t kBarOff = 13 * kAtom;
+constexpr uint32_t kKOff = 3 * kAtom;            // 1 slot x 3 atoms
+constexpr uint32_t kVOff = 6 * kAtom;            // 2 slots x 2 atoms (vdim 0-63, 64-127)
+constexpr uint32_t kPOff = 10 * kAtom;           // 2 atoms (keys 0-63, 64-127)
+constexpr uint32_t kBarOff = 12 * kAtom;
 constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[2], k_empty[2];
-  uint64_t v_full, v_empty;
+  uint64_t k_full, k_empty;
+  uint64_t v_full[2], v_empty[2];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full, pv_done;
   uint64_t drain;
@@ -74,13 +75,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bar->q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar->k_full[i], 1);
-      mbar_init(&bar->k_empty[i], 1);
+      mbar_init(&bar->v_full[i], 1);
+      mbar_init(&bar->v_empty[i], 1);
       mbar_init(&bar->s_full[i], 1);
       mbar_init(&bar->s_free[i], 128);
     }
-    mbar_init(&bar->v_full, 1);
-    mbar_init(&bar->v_empty, 1);
+    mbar_init(&bar->k_full, 1);
+    mbar_init(&bar->k_empty, 1);
     mbar_init(&bar->p_full, 128);
     mbar_init(&bar->pv_done, 1);
     mbar_init(&bar->drain, 1);
@@ -104,32 +105,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmK);
       mbar_arrive_expect_tx(&bar->q_full, 3 * kAtom);
       for (int c = 0; c < 3; ++c) tma_load_3d(smem + kQOff + c * kAtom, &tmQ, &bar->q_full, h * 192 + 64 * c, q0, b);
-      int issued[2] = {0, 0};
+      int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
-        const int slot = j & 1;
-        if (!mbar_wait(&bar->k_empty[slot], ((j >> 1) & 1) ^ 1, st, abort_flag, 40)) break;
-        mbar_arrive_expect_tx(&bar->k_full[slot], 3 * kAtom);
+        if (!mbar_wait(&bar->k_empty, (j & 1) ^ 1, st, abort_flag, 40)) break;
+        mbar_arrive_expect_tx(&bar->k_full, 3 * kAtom);
         for (int c = 0; c < 3; ++c)
-          tma_load_3d(smem + kKOff + (slot * 3 + c) * kAtom, &tmK, &bar->k_full[slot], 64 * c, j * 128, kv_row);
-        issued[slot]++;
+          tma_load_3d(smem + kKOff + c * kAtom, &tmK, &bar->k_full, 64 * c, j * 128, kv_row);
+        issued++;
       }
       mbar_wait(&bar->q_full, 0, st, nullptr, 41);
-      for (int s = 0; s < 2; ++s)
-        if (issued[s]) mbar_wait(&bar->k_full[s], (issued[s] - 1) & 1, st, nullptr, 41);
+      if (issued) mbar_wait(&bar->k_full, (issued - 1) & 1, st, nullptr, 41);
     }
   } else if (warp == 6) {
     if (lane == 0) {
       // ---- V producer ----
       tma_prefetch_desc(&tmV);
-      int issued = 0;
+      int issued[2] = {0, 0};
       for (int j = 0; j < n_kv; ++j) {
-        if (!mbar_wait(&bar->v_empty, (j & 1) ^ 1, st, abort_flag, 42)) break;
-        mbar_arrive_expect_tx(&bar->v_full, 2 * kAtom);
+        const int slot = j & 1;
+        if (!mbar_wait(&bar->v_empty[slot], ((j >> 1) & 1) ^ 1, st, abort_flag, 42)) break;
+        mbar_arrive_expect_tx(&bar->v_full[slot], 2 * kAtom);
         for (int c = 0; c < 2; ++c)
-          tma_load_3d(smem + kVOff + c * kAtom, &tmV, &bar->v_full, 64 * c, j * 128, kv_row);
-        issued++;
+          tma_load_3d(smem + kVOff + (slot * 2 + c) * kAtom, &tmV, &bar->v_full[slot], 64 * c, j * 128, kv_row);
+        issued[slot]++;
       }
-      if (issued) mbar_wait(&bar->v_full, (issued - 1) & 1, st, nullptr, 43);
+      for (int i = 0; i < 2; ++i)
+        if (issued[i]) mbar_wait(&bar->v_full[i], (issued[i] - 1) & 1, st, nullptr, 43);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -153,10 +154,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (next_s < n_kv && next_s <= next_pv + 1) {
           const int slot = next_s & 1;
           const uint32_t ph = (next_s >> 1) & 1;
-          if (mbar_test(&bar->k_full[slot], ph) && mbar_test(&bar->s_free[slot], ph ^ 1)) {
+          if (mbar_test(&bar->k_full, next_s & 1) && mbar_test(&bar->s_free[slot], ph ^ 1)) {
             tc_fence_after();
             const uint32_t d = tmem + slot * 128;
-            const uint32_t kb = k_addr + slot * 3 * kAtom;
+            const uint32_t kb = k_addr;
 #pragma unroll
             for (int kk = 0; kk < 12; ++kk) {
               const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
@@ -164,21 +165,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         kk > 0 ? 1u : 0u);
             }
             umma_commit(&bar->s_full[slot]);
-            umma_commit(&bar->k_empty[slot]);
+            umma_commit(&bar->k_empty);
             ++next_s;
             progress = true;
           }
         }
-        if (next_pv < next_s && mbar_test(&bar->p_full, next_pv & 1) && mbar_test(&bar->v_full, next_pv & 1)) {
+        if (next_pv < next_s && mbar_test(&bar->p_full, next_pv & 1) &&
+            mbar_test(&bar->v_full[next_pv & 1], (next_pv >> 1) & 1)) {
           tc_fence_after();
+          const uint32_t vb = v_addr + (next_pv & 1) * 2 * kAtom;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t adesc = sdesc_sw128(p_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
-            const uint64_t bdesc = sdesc_sw128(v_addr + kk * 2048, kAtom, 1024);
+            const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, kAtom, 1024);
             umma_bf16(tmem + 256, adesc, bdesc, idesc_pv, (next_pv > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&bar->pv_done);
-          umma_commit(&bar->v_empty);
+          umma_commit(&bar->v_empty[next_pv & 1]);
           ++next_pv;
           progress = true;
         }
@@ -219,21 +222,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bar->s_free[slot]);
       const bool diag = (j == n_kv - 1);
       const int k0 = j * 128;
+      // max of the raw scores (the scale is positive), causal mask on the
+      // diagonal tile only
       float mx = -INFINITY;
+      if (diag) {
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        float v = __uint_as_float(s[c]) * sl2;
-        if (diag && k0 + c > qpos) v = -INFINITY;
-        s[c] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
+        for (int c = 0; c < 128; ++c) {
+          if (k0 + c > qpos) s[c] = __float_as_uint(-INFINITY);
+          mx = fmaxf(mx, __uint_as_float(s[c]));
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
       }
+      mx *= sl2;  // log2 units
       const bool need = mx > m + kRescaleThreshold;
       const float m_new = need ? mx : m;
-      const float alpha = need ? exp2f(m - m_new) : 1.f;
+      const float alpha = need ? ex2_approx(m - m_new) : 1.f;
       float sum = 0.f;
 #pragma unroll
       for (int c = 0; c < 128; ++c) {
-        const float p = exp2f(__uint_as_float(s[c]) - m_new);
+        const float p = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -m_new));
         s[c] = __float_as_uint(p);
         sum += p;
       }

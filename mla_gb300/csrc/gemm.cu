@@ -37,10 +37,14 @@ __host__ __device__ constexpr uint32_t pow2_cols(uint32_t n) {
   return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512;
 }
 
-template <int BN, int STAGES>
+// One pipeline stage holds KSUB consecutive 64-wide K blocks of A and of B,
+// so that each weight row is fetched in runs of KSUB * 128 bytes.
+template <int BM, int BN, int STAGES, int KSUB>
 struct GemmSmem {
-  static constexpr uint32_t kA = kBM * kBK * 2;
-  static constexpr uint32_t kB = BN * kBK * 2;
+  static constexpr uint32_t kA1 = BM * kBK * 2;  // one 64-wide K block of A
+  static constexpr uint32_t kB1 = BN * kBK * 2;
+  static constexpr uint32_t kA = KSUB * kA1;
+  static constexpr uint32_t kB = KSUB * kB1;
   static constexpr uint32_t kStage = kA + kB;
   static constexpr uint32_t kBarOff = STAGES * kStage;
   static constexpr uint32_t kBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
@@ -222,12 +226,14 @@ __device__ __forceinline__ void run_epilogue(const EpiArgs& ea, const Src& ld, i
   }
 }
 
-template <int BN, int STAGES, Epi EPI, bool B_MN>
+// BM = 128: accumulator row r in TMEM lane r.  BM = 64 (few rows, decode):
+// row r in lane 32*(r/16) + r%16, so each epilogue warp holds 16 rows.
+template <int BM, int BN, int STAGES, int KSUB, Epi EPI, bool B_MN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                 const __grid_constant__ CUtensorMap tmB1, const GemmShape s, const EpiArgs ea,
                 const DevStatus st) {
-  using L = GemmSmem<BN, STAGES>;
+  using L = GemmSmem<BM, BN, STAGES, KSUB>;
   constexpr uint32_t kTmemCols = pow2_cols(2 * BN);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -241,10 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int m_tiles = (s.M + kBM - 1) / kBM;
+  const int m_tiles = (s.M + BM - 1) / BM;
   const int n_tiles = s.N / BN;
   const int num_tiles = s.batches * m_tiles * n_tiles;
-  const int kblocks = s.K / kBK;
+  const int kblocks = s.K / (kBK * KSUB);  // stages of KSUB K blocks
   const int ksplit = s.ksplit;
   const int num_units = num_tiles * ksplit;
 
@@ -304,13 +310,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sa = smem + stage * L::kStage;
           uint8_t* sb = sa + L::kA;
           mbar_arrive_expect_tx(&full_bar[stage], L::kStage);
-          tma_load_2d(sa, &tmA, &full_bar[stage], a_col + kb * kBK, m_blk * kBM);
-          if constexpr (B_MN) {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(sb + j * (64 * 128), mb, &full_bar[stage], nb + j * 64, b_row + kb * kBK);
-          } else {
-            tma_load_2d(sb, mb, &full_bar[stage], kb * kBK, b_row + nb);
+          for (int u = 0; u < KSUB; ++u) {
+            const int k0 = (kb * KSUB + u) * kBK;
+            tma_load_2d(sa + u * L::kA1, &tmA, &full_bar[stage], a_col + k0, m_blk * BM);
+            if constexpr (B_MN) {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(sb + u * L::kB1 + j * (64 * 128), mb, &full_bar[stage], nb + j * 64, b_row + k0);
+            } else {
+              tma_load_2d(sb + u * L::kB1, mb, &full_bar[stage], k0, b_row + nb);
+            }
           }
           issued[stage]++;
           if (++stage == STAGES) {
@@ -327,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      constexpr uint32_t idesc = idesc_bf16(kBM, BN, false, B_MN);
+      constexpr uint32_t idesc = idesc_bf16(BM, BN, false, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -345,17 +355,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + stage * L::kStage);
-          const uint32_t b_addr = a_addr + L::kA;
+          const uint32_t a_base = smem_u32(smem + stage * L::kStage);
+          const uint32_t b_base = a_base + L::kA;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t adesc = sdesc_sw128(a_addr + k * 32, 16, 1024);
-            uint64_t bdesc;
-            if constexpr (B_MN)
-              bdesc = sdesc_sw128(b_addr + k * 2048, 64 * 128, 1024);
-            else
-              bdesc = sdesc_sw128(b_addr + k * 32, 16, 1024);
-            umma_bf16(d_tmem, adesc, bdesc, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+          for (int u = 0; u < KSUB; ++u) {
+            const uint32_t a_addr = a_base + u * L::kA1;
+            const uint32_t b_addr = b_base + u * L::kB1;
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              const uint64_t adesc = sdesc_sw128(a_addr + k * 32, 16, 1024);
+              uint64_t bdesc;
+              if constexpr (B_MN)
+                bdesc = sdesc_sw128(b_addr + k * 2048, 64 * 128, 1024);
+              else
+                bdesc = sdesc_sw128(b_addr + k * 32, 16, 1024);
+              umma_bf16(d_tmem, adesc, bdesc, idesc, (kb != kb0 || u != 0 || k != 0) ? 1u : 0u);
+            }
           }
           umma_commit(&empty_bar[stage]);
           if (++stage == STAGES) {
@@ -375,7 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     const int quarter = warp & 3;
-    const int rit = quarter * 32 + lane;  // row within the tile
+    const bool lane_ok = (BM == 128) || lane < 16;
+    const int rit = (BM == 128) ? quarter * 32 + lane : quarter * 16 + (lane & 15);  // row within the tile
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int unit = blockIdx.x; unit < num_units; unit += gridDim.x) {
@@ -387,16 +403,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(&tfull_bar[acc], acc_phase, st, abort_flag, 6);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const int row = m_blk * kBM + rit;
+      const int row = m_blk * BM + rit;
+      const bool row_ok = lane_ok && row < s.M;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
       if (ksplit == 1) {
-        run_epilogue<BN, EPI>(ea, TmemSrc{taddr}, batch, row, n_blk * BN, row < s.M);
+        run_epilogue<BN, EPI>(ea, TmemSrc{taddr}, batch, row, n_blk * BN, row_ok);
         tc_fence_before();
         mbar_arrive(&tempty_bar[acc]);
       } else {
         // this K slice's partial -> its slot; the last warp of the quarter reduces
-        const int rows_pt = s.M < kBM ? s.M : kBM;
-        const bool in_slot = row < s.M && rit < rows_pt;
+        const int rows_pt = s.M < BM ? s.M : BM;
+        const bool in_slot = row_ok && rit < rows_pt;
         float* slot = ea.part + ((size_t)(tile * ksplit + ks) * rows_pt + (in_slot ? rit : 0)) * BN;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
@@ -422,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __threadfence();
           const PartSrc src{ea.part + ((size_t)tile * ksplit * rows_pt + (in_slot ? rit : 0)) * BN,
                             (size_t)rows_pt * BN, ksplit, in_slot};
-          run_epilogue<BN, EPI>(ea, src, batch, row, n_blk * BN, row < s.M);
+          run_epilogue<BN, EPI>(ea, src, batch, row, n_blk * BN, row_ok);
           if (lane == 0) ea.counters[tile * 4 + quarter] = 0;  // ready for the next GEMM
         }
       }
@@ -439,12 +456,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int STAGES, Epi EPI, bool B_MN>
+template <int BM, int BN, int STAGES, Epi EPI, bool B_MN, int KSUB = 1>
 cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArgs& ea, const DevStatusHost& st,
                         int num_sms, cudaStream_t stream) {
-  using L = GemmSmem<BN, STAGES>;
+  using L = GemmSmem<BM, BN, STAGES, KSUB>;
+  if (s.K % (kBK * KSUB)) return cudaErrorInvalidValue;
+  static_assert(L::kBytes <= 232448, "shared memory budget");
   CUtensorMap ta, tb0, tb1;
-  if (!make_tmap_bf16_2d(&ta, op.A, op.a_rows, (uint64_t)op.lda, op.lda, kBM, kBK))
+  if (!make_tmap_bf16_2d(&ta, op.A, op.a_rows, (uint64_t)op.lda, op.lda, BM, kBK))
     return cudaErrorInvalidValue;
   if (B_MN) {
     if (!make_tmap_bf16_2d(&tb0, op.B0, op.b0_rows, op.ldb0, op.ldb0, 64, 64)) return cudaErrorInvalidValue;
@@ -454,7 +473,7 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
   tb1 = tb0;
   if (op.B1 && !make_tmap_bf16_2d(&tb1, op.B1, op.b1_rows, op.ldb1, op.ldb1, BN, kBK))
     return cudaErrorInvalidValue;
-  auto kern = gemm_kernel<BN, STAGES, EPI, B_MN>;
+  auto kern = gemm_kernel<BM, BN, STAGES, KSUB, EPI, B_MN>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -462,9 +481,9 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
   });
   if (attr_err != cudaSuccess) return attr_err;
   GemmShape sh = s;
-  const int m_tiles = (s.M + kBM - 1) / kBM;
+  const int m_tiles = (s.M + BM - 1) / BM;
   const int tiles = s.batches * m_tiles * (s.N / BN);
-  const int kblocks = s.K / kBK;
+  const int kblocks = s.K / (kBK * KSUB);
   sh.ksplit = 1;
   sh.kb_per = kblocks;
   if (ea.part && ea.counters && m_tiles == 1 && tiles * 2 <= num_sms && kblocks >= 2 &&
@@ -493,38 +512,52 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
 cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, const EpiArgs& ea,
                         const DevStatusHost& st, int num_sms, cudaStream_t stream) {
   if (s.M <= 0 || s.K % kBK != 0 || s.batches <= 0) return cudaErrorInvalidValue;
-  // Few rows (decode: M <= 128): narrower tiles so that enough CTAs stream
-  // the weights; many rows (prefill): wide tiles, fewer re-reads of A.
+  // Few rows (decode): narrower N tiles so that enough CTAs stream the
+  // weights, and M = 64 tiles when M <= 64 so that shared memory holds more
+  // weight bytes in flight; many rows (prefill): wide tiles.
+  const bool tiny = s.M <= 64;
   const bool small = s.M <= kBM;
+  const bool k256 = s.K % 256 == 0;
   switch (epi) {
     case Epi::kQRope:
       if (s.N % 192 || op.b_mn_major) return cudaErrorInvalidValue;
-      if (small) return launch_impl<96, 7, Epi::kQRope, false>(s, op, ea, st, num_sms, stream);
-      return launch_impl<192, 5, Epi::kQRope, false>(s, op, ea, st, num_sms, stream);
+      if (tiny && k256) return launch_impl<64, 96, 5, Epi::kQRope, false, 2>(s, op, ea, st, num_sms, stream);
+      if (small && k256) return launch_impl<128, 96, 3, Epi::kQRope, false, 2>(s, op, ea, st, num_sms, stream);
+      if (small) return launch_impl<128, 96, 7, Epi::kQRope, false>(s, op, ea, st, num_sms, stream);
+      return launch_impl<128, 192, 5, Epi::kQRope, false>(s, op, ea, st, num_sms, stream);
     case Epi::kKVCache:
       if (s.N % 256 || op.b_mn_major) return cudaErrorInvalidValue;
-      if (small) return launch_impl<128, 6, Epi::kKVCache, false>(s, op, ea, st, num_sms, stream);
-      return launch_impl<256, 4, Epi::kKVCache, false>(s, op, ea, st, num_sms, stream);
+      if (tiny && k256) return launch_impl<64, 128, 4, Epi::kKVCache, false, 2>(s, op, ea, st, num_sms, stream);
+      if (small && k256) return launch_impl<128, 128, 3, Epi::kKVCache, false, 2>(s, op, ea, st, num_sms, stream);
+      if (small) return launch_impl<128, 128, 6, Epi::kKVCache, false>(s, op, ea, st, num_sms, stream);
+      return launch_impl<128, 256, 4, Epi::kKVCache, false>(s, op, ea, st, num_sms, stream);
     case Epi::kResidual:
       if (s.N % 256 || op.b_mn_major) return cudaErrorInvalidValue;
-      if (small) return launch_impl<64, 8, Epi::kResidual, false>(s, op, ea, st, num_sms, stream);
-      return launch_impl<256, 4, Epi::kResidual, false>(s, op, ea, st, num_sms, stream);
+      if (tiny && k256) return launch_impl<64, 64, 3, Epi::kResidual, false, 4>(s, op, ea, st, num_sms, stream);
+      if (small && k256) return launch_impl<128, 64, 4, Epi::kResidual, false, 2>(s, op, ea, st, num_sms, stream);
+      if (small) return launch_impl<128, 64, 8, Epi::kResidual, false>(s, op, ea, st, num_sms, stream);
+      return launch_impl<128, 256, 4, Epi::kResidual, false>(s, op, ea, st, num_sms, stream);
     case Epi::kStoreF32:
       if (s.N % 192 || s.n_split % 192 || op.b_mn_major) return cudaErrorInvalidValue;
-      if (small) return launch_impl<64, 8, Epi::kStoreF32, false>(s, op, ea, st, num_sms, stream);
-      return launch_impl<192, 5, Epi::kStoreF32, false>(s, op, ea, st, num_sms, stream);
+      if (tiny && k256) return launch_impl<64, 64, 3, Epi::kStoreF32, false, 4>(s, op, ea, st, num_sms, stream);
+      if (small && k256) return launch_impl<128, 64, 4, Epi::kStoreF32, false, 2>(s, op, ea, st, num_sms, stream);
+      if (small) return launch_impl<128, 64, 8, Epi::kStoreF32, false>(s, op, ea, st, num_sms, stream);
+      return launch_impl<128, 192, 5, Epi::kStoreF32, false>(s, op, ea, st, num_sms, stream);
     case Epi::kStoreBf16:
     default:
       if (op.b_mn_major) {
         if (s.N % 128) return cudaErrorInvalidValue;
-        return launch_impl<128, 6, Epi::kStoreBf16, true>(s, op, ea, st, num_sms, stream);
+        if (tiny) return launch_impl<64, 128, 8, Epi::kStoreBf16, true>(s, op, ea, st, num_sms, stream);
+        return launch_impl<128, 128, 6, Epi::kStoreBf16, true>(s, op, ea, st, num_sms, stream);
       }
+      if (tiny && k256 && s.N % 64 == 0 && s.n_split % 64 == 0)
+        return launch_impl<64, 64, 3, Epi::kStoreBf16, false, 4>(s, op, ea, st, num_sms, stream);
       if (small && s.N % 64 == 0 && s.n_split % 64 == 0)
-        return launch_impl<64, 8, Epi::kStoreBf16, false>(s, op, ea, st, num_sms, stream);
+        return launch_impl<128, 64, 8, Epi::kStoreBf16, false>(s, op, ea, st, num_sms, stream);
       if (s.N % 192 == 0 && s.n_split % 192 == 0)
-        return launch_impl<192, 5, Epi::kStoreBf16, false>(s, op, ea, st, num_sms, stream);
+        return launch_impl<128, 192, 5, Epi::kStoreBf16, false>(s, op, ea, st, num_sms, stream);
       if (s.N % 128 == 0 && s.n_split % 128 == 0)
-        return launch_impl<128, 6, Epi::kStoreBf16, false>(s, op, ea, st, num_sms, stream);
+        return launch_impl<128, 128, 6, Epi::kStoreBf16, false>(s, op, ea, st, num_sms, stream);
       return cudaErrorInvalidValue;
   }
 }
