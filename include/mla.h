@@ -85,9 +85,9 @@ typedef struct {
 } mla_weights_t;
 
 /* Stage ids for optional per-stage timing. */
-#define MLA_STAGE_INPUT_NORM 0   /* RMSNorm(x) and the RoPE table            */
+#define MLA_STAGE_INPUT_NORM 0   /* RMSNorm(x)                               */
 #define MLA_STAGE_A_PROJ 1       /* x_attn . [W_DQ ; W_DKV ; W_KR]^T          */
-#define MLA_STAGE_LATENT 2       /* split, q/kv latent RMSNorm, RoPE(k), latent cache write */
+#define MLA_STAGE_LATENT 2       /* split, q/kv latent RMSNorm, RoPE table and RoPE(k), latent cache write */
 #define MLA_STAGE_Q_B 3          /* q_b_proj + RoPE(q)                       */
 #define MLA_STAGE_KV_B 4         /* kv_b_proj + per-head K/V cache write     */
 #define MLA_STAGE_ATTN 5         /* attention (prefill, decode or latent decode) */

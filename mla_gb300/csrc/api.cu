@@ -157,11 +157,11 @@ int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok,
               const Layout& L, const DevStatusHost& st, int sms, cudaStream_t stream, Stager& sg,
               int* launches, bool with_q = true) {
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  (void)n_pos;
   sg.start(MLA_STAGE_INPUT_NORM);
-  MLA_TRY(launch_rope_table(at<float2>(ws, L.cs), n_pos, pos0, p.base, stream));
   MLA_TRY(launch_rmsnorm_rows(xb, static_cast<const __nv_bfloat16*>(w->w_in_norm), at<__nv_bfloat16>(ws, L.xn),
                               n_tok, p.eps, stream));
-  *launches += 2;
+  *launches += 1;
   sg.stop(MLA_STAGE_INPUT_NORM);
 
   sg.start(MLA_STAGE_A_PROJ);
@@ -186,6 +186,8 @@ int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok,
     la.g_qa = static_cast<const __nv_bfloat16*>(w->w_q_a_norm);
     la.g_kva = static_cast<const __nv_bfloat16*>(w->w_kv_a_norm);
     la.cs = at<float2>(ws, L.cs);
+    for (int i = 0; i < 32; ++i) la.inv_freq[i] = pow((double)p.base, -2.0 * i / 64.0);
+    la.pos0 = pos0;
     la.cq = at<__nv_bfloat16>(ws, L.cq);
     la.ckv = at<__nv_bfloat16>(ws, L.ckv);
     la.kpe = at<__nv_bfloat16>(ws, L.kpe);
@@ -232,6 +234,7 @@ int kv_b_stage(const mla_weights_t* w, int n_tok, int t_mod, int t_off, __nv_bfl
   ea.kc = kc;
   ea.vc = vc;
   ea.kpe = at<__nv_bfloat16>(ws, L.kpe);
+  ea.B = (n_tok + t_mod - 1) / t_mod;
   ea.t_mod = t_mod;
   ea.t_off = t_off;
   ea.cap = cap;

@@ -39,14 +39,15 @@ __host__ __device__ constexpr uint32_t pow2_cols(uint32_t n) {
 
 // One pipeline stage holds KSUB consecutive 64-wide K blocks of A and of B,
 // so that each weight row is fetched in runs of KSUB * 128 bytes.
-template <int BM, int BN, int STAGES, int KSUB>
+template <int BM, int BN, int STAGES, int KSUB, bool TMA_ST = false>
 struct GemmSmem {
   static constexpr uint32_t kA1 = BM * kBK * 2;  // one 64-wide K block of A
   static constexpr uint32_t kB1 = BN * kBK * 2;
   static constexpr uint32_t kA = KSUB * kA1;
   static constexpr uint32_t kB = KSUB * kB1;
   static constexpr uint32_t kStage = kA + kB;
-  static constexpr uint32_t kBarOff = STAGES * kStage;
+  static constexpr uint32_t kStagingOff = STAGES * kStage;              // 4 warps x 2 x 4 KB
+  static constexpr uint32_t kBarOff = kStagingOff + (TMA_ST ? 32768 : 0);
   static constexpr uint32_t kBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
 };
 
@@ -226,14 +227,205 @@ __device__ __forceinline__ void run_epilogue(const EpiArgs& ea, const Src& ld, i
   }
 }
 
+// ---------------------------------------------------------------------------
+// Epilogue through shared memory and TMA stores (BM = 128, one tile per
+// pass): each epilogue warp converts a 32-row x 32-column chunk into one of
+// its two 4 KB staging buffers (swizzled so that the 32 row-writes of a
+// chunk hit distinct banks) and one lane stores it with cp.async.bulk.tensor,
+// so global writes leave the SM as whole rows.  Rows at or beyond the
+// tensor's row extent are clipped by the TMA unit.
+// ---------------------------------------------------------------------------
+struct StoreStage {
+  uint8_t* base;  // this warp's two buffers
+  int n;          // chunks issued so far
+  __device__ __forceinline__ uint8_t* next(int lane) {
+    uint8_t* buf = base + (n & 1) * 4096;
+    if (n >= 2) {
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
+    }
+    return buf;
+  }
+  __device__ __forceinline__ void issue2(const CUtensorMap* m, uint8_t* buf, int c0, int c1, int lane) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(m, buf, c0, c1);
+      bulk_commit();
+    }
+    ++n;
+  }
+  __device__ __forceinline__ void issue3(const CUtensorMap* m, uint8_t* buf, int c0, int c1, int c2, int lane) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(m, buf, c0, c1, c2);
+      bulk_commit();
+    }
+    ++n;
+  }
+};
+
+// row `lane` of a 32 x 32 bf16 chunk: 64 bytes, 64-byte swizzle
+__device__ __forceinline__ void stage_bf16(uint8_t* buf, int lane, const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int phys = c ^ ((lane >> 1) & 3);
+    *reinterpret_cast<uint4*>(buf + lane * 64 + phys * 16) =
+        make_uint4(pack_bf16x2(__uint_as_float(r[8 * c + 0]), __uint_as_float(r[8 * c + 1])),
+                   pack_bf16x2(__uint_as_float(r[8 * c + 2]), __uint_as_float(r[8 * c + 3])),
+                   pack_bf16x2(__uint_as_float(r[8 * c + 4]), __uint_as_float(r[8 * c + 5])),
+                   pack_bf16x2(__uint_as_float(r[8 * c + 6]), __uint_as_float(r[8 * c + 7])));
+  }
+}
+
+// row `lane` of a 32 x 32 bf16 chunk from 4 packed uint4 (already bf16)
+__device__ __forceinline__ void stage_bf16_raw(uint8_t* buf, int lane, const uint4 (&v)[4]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) * 16)) = v[c];
+}
+
+// row `lane` of a 32 x 32 float32 chunk: 128 bytes, 128-byte swizzle
+__device__ __forceinline__ void stage_f32(uint8_t* buf, int lane, const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) * 16)) =
+        make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+}
+
+template <int BN, Epi EPI, class Src>
+__device__ __forceinline__ void run_epilogue_tma(const EpiArgs& ea, const Src& ld, StoreStage& ss,
+                                                 const CUtensorMap* m0, const CUtensorMap* m1, int batch,
+                                                 int row0, int row, int n0, bool row_ok, int lane, int M) {
+  if constexpr (EPI == Epi::kStoreF32) {
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      ld(c, r);
+      uint8_t* buf = ss.next(lane);
+      stage_f32(buf, lane, r);
+      ss.issue2(m0, buf, n0 + c, row0, lane);
+    }
+  } else if constexpr (EPI == Epi::kStoreBf16) {
+    const int col0 = ea.c_col0 + batch * ea.c_col_step + n0;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      ld(c, r);
+      uint8_t* buf = ss.next(lane);
+      stage_bf16(buf, lane, r);
+      ss.issue2(m0, buf, col0 + c, row0, lane);
+    }
+  } else if constexpr (EPI == Epi::kQRope) {
+    static_assert(BN == 192 || BN == 96, "q_b epilogue works on whole or half heads");
+    const int o0 = n0 % 192;
+    const int nope_cols = (o0 + BN < 128 ? o0 + BN : 128) - o0;
+#pragma unroll 1
+    for (int c = 0; c < nope_cols; c += 32) {
+      uint32_t r[32];
+      ld(c, r);
+      uint8_t* buf = ss.next(lane);
+      stage_bf16(buf, lane, r);
+      ss.issue2(m0, buf, n0 + c, row0, lane);
+    }
+    if (o0 + BN == 192) {
+      uint32_t x1[32], x2[32];
+      ld(nope_cols, x1);
+      ld(nope_cols + 32, x2);
+      const float2* cs = ea.cs + (size_t)(row % ea.t_mod) * 32;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float2 t = cs[i];
+        const float a = __uint_as_float(x1[i]), b = __uint_as_float(x2[i]);
+        x1[i] = __float_as_uint(a * t.x - b * t.y);
+        x2[i] = __float_as_uint(b * t.x + a * t.y);
+      }
+      uint8_t* buf = ss.next(lane);
+      stage_bf16(buf, lane, x1);
+      ss.issue2(m0, buf, n0 + nope_cols, row0, lane);
+      buf = ss.next(lane);
+      stage_bf16(buf, lane, x2);
+      ss.issue2(m0, buf, n0 + nope_cols + 32, row0, lane);
+    }
+  } else if constexpr (EPI == Epi::kKVCache) {
+    // the 32 rows of this warp are consecutive positions of one sequence
+    // (the host uses this path only when t_mod is a multiple of 32)
+    static_assert(BN == 256 || BN == 128, "kv_b epilogue works on whole or half heads");
+    const int h = n0 / 256;
+    const int o0 = n0 % 256;
+    const bool warp_ok = row0 < M;
+    const int b = row0 / ea.t_mod;
+    const int t0 = ea.t_off + row0 % ea.t_mod;
+    const int plane = b * 64 + h;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      ld(c, r);
+      if (!warp_ok) continue;
+      const int col = o0 + c;
+      uint8_t* buf = ss.next(lane);
+      stage_bf16(buf, lane, r);
+      if (col < 128)
+        ss.issue3(m0, buf, col, t0, plane, lane);
+      else
+        ss.issue3(m1, buf, col - 128, t0, plane, lane);
+    }
+    if (warp_ok && o0 == 0) {
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint4 v[4];
+        const uint4* src = reinterpret_cast<const uint4*>(ea.kpe + (size_t)row * 64 + half * 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = row_ok ? src[j] : make_uint4(0, 0, 0, 0);
+        uint8_t* buf = ss.next(lane);
+        stage_bf16_raw(buf, lane, v);
+        ss.issue3(m0, buf, 128 + 32 * half, t0, plane, lane);
+      }
+    }
+  } else {  // kResidual
+    const size_t base = (size_t)row * ea.ldo + n0;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      ld(c, r);
+      if (row_ok && ea.delta) {
+        float4* dd = reinterpret_cast<float4*>(ea.delta + base + c);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          dd[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+      }
+      if (row_ok) {
+        const uint4* xs = reinterpret_cast<const uint4*>(ea.x + base + c);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 xv = xs[j];
+          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 xf = unpack_bf16x2(xw[q]);
+            r[8 * j + 2 * q] = __float_as_uint(xf.x + __uint_as_float(r[8 * j + 2 * q]));
+            r[8 * j + 2 * q + 1] = __float_as_uint(xf.y + __uint_as_float(r[8 * j + 2 * q + 1]));
+          }
+        }
+      }
+      uint8_t* buf = ss.next(lane);
+      stage_bf16(buf, lane, r);
+      ss.issue2(m0, buf, n0 + c, row0, lane);
+    }
+  }
+}
+
 // BM = 128: accumulator row r in TMEM lane r.  BM = 64 (few rows, decode):
 // row r in lane 32*(r/16) + r%16, so each epilogue warp holds 16 rows.
-template <int BM, int BN, int STAGES, int KSUB, Epi EPI, bool B_MN>
+template <int BM, int BN, int STAGES, int KSUB, Epi EPI, bool B_MN, bool TMA_ST>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                const __grid_constant__ CUtensorMap tmB1, const GemmShape s, const EpiArgs ea,
+                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO0,
+                const __grid_constant__ CUtensorMap tmO1, const GemmShape s, const EpiArgs ea,
                 const DevStatus st) {
-  using L = GemmSmem<BM, BN, STAGES, KSUB>;
+  static_assert(!TMA_ST || BM == 128, "TMA-store epilogue needs 32 rows per warp");
+  using L = GemmSmem<BM, BN, STAGES, KSUB, TMA_ST>;
   constexpr uint32_t kTmemCols = pow2_cols(2 * BN);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -390,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     const int quarter = warp & 3;
+    StoreStage ss{smem + L::kStagingOff + quarter * 8192, 0};
     const bool lane_ok = (BM == 128) || lane < 16;
     const int rit = (BM == 128) ? quarter * 32 + lane : quarter * 16 + (lane & 15);  // row within the tile
     int acc = 0;
@@ -407,7 +600,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = lane_ok && row < s.M;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
       if (ksplit == 1) {
-        run_epilogue<BN, EPI>(ea, TmemSrc{taddr}, batch, row, n_blk * BN, row_ok);
+        if constexpr (TMA_ST) {
+          run_epilogue_tma<BN, EPI>(ea, TmemSrc{taddr}, ss, &tmO0, &tmO1, batch, m_blk * BM + quarter * 32, row,
+                                    n_blk * BN, row_ok, lane, s.M);
+        } else {
+          run_epilogue<BN, EPI>(ea, TmemSrc{taddr}, batch, row, n_blk * BN, row_ok);
+        }
         tc_fence_before();
         mbar_arrive(&tempty_bar[acc]);
       } else {
@@ -446,6 +644,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    if constexpr (TMA_ST) {
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
+    }
   }
 
   tc_fence_before();
@@ -456,10 +658,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BM, int BN, int STAGES, Epi EPI, bool B_MN, int KSUB = 1>
+template <int BM, int BN, int STAGES, Epi EPI, bool B_MN, int KSUB = 1, bool TMA_ST = false>
 cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArgs& ea, const DevStatusHost& st,
                         int num_sms, cudaStream_t stream) {
-  using L = GemmSmem<BM, BN, STAGES, KSUB>;
+  using L = GemmSmem<BM, BN, STAGES, KSUB, TMA_ST>;
   if (s.K % (kBK * KSUB)) return cudaErrorInvalidValue;
   static_assert(L::kBytes <= 232448, "shared memory budget");
   CUtensorMap ta, tb0, tb1;
@@ -473,7 +675,20 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
   tb1 = tb0;
   if (op.B1 && !make_tmap_bf16_2d(&tb1, op.B1, op.b1_rows, op.ldb1, op.ldb1, BN, kBK))
     return cudaErrorInvalidValue;
-  auto kern = gemm_kernel<BM, BN, STAGES, KSUB, EPI, B_MN>;
+  CUtensorMap to0 = ta, to1 = ta;
+  if constexpr (TMA_ST) {
+    bool ok = true;
+    if constexpr (EPI == Epi::kStoreF32) {
+      ok = make_tmap_store_f32_2d(&to0, ea.out_f32, s.M, ea.ldo, ea.ldo);
+    } else if constexpr (EPI == Epi::kKVCache) {
+      ok = make_tmap_store_bf16_3d(&to0, ea.kc, 192, ea.cap, (uint64_t)ea.B * 64, 384, (uint64_t)ea.cap * 384) &&
+           make_tmap_store_bf16_3d(&to1, ea.vc, 128, ea.cap, (uint64_t)ea.B * 64, 256, (uint64_t)ea.cap * 256);
+    } else {
+      ok = make_tmap_store_bf16_2d(&to0, ea.out, s.M, ea.ldo, ea.ldo);
+    }
+    if (!ok) return cudaErrorInvalidValue;
+  }
+  auto kern = gemm_kernel<BM, BN, STAGES, KSUB, EPI, B_MN, TMA_ST>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -503,7 +718,7 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
   const int units = tiles * sh.ksplit;
   const int grid = units < num_sms ? units : num_sms;
   DevStatus dst{st.word, st.wait_limit_ns};
-  kern<<<grid, kThreads, L::kBytes, stream>>>(ta, tb0, tb1, sh, ea, dst);
+  kern<<<grid, kThreads, L::kBytes, stream>>>(ta, tb0, tb1, to0, to1, sh, ea, dst);
   return cudaGetLastError();
 }
 
@@ -524,25 +739,27 @@ cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, con
       if (tiny && k256) return launch_impl<64, 96, 5, Epi::kQRope, false, 2>(s, op, ea, st, num_sms, stream);
       if (small && k256) return launch_impl<128, 96, 3, Epi::kQRope, false, 2>(s, op, ea, st, num_sms, stream);
       if (small) return launch_impl<128, 96, 7, Epi::kQRope, false>(s, op, ea, st, num_sms, stream);
-      return launch_impl<128, 192, 5, Epi::kQRope, false>(s, op, ea, st, num_sms, stream);
+      return launch_impl<128, 192, 4, Epi::kQRope, false, 1, true>(s, op, ea, st, num_sms, stream);
     case Epi::kKVCache:
       if (s.N % 256 || op.b_mn_major) return cudaErrorInvalidValue;
       if (tiny && k256) return launch_impl<64, 128, 4, Epi::kKVCache, false, 2>(s, op, ea, st, num_sms, stream);
       if (small && k256) return launch_impl<128, 128, 3, Epi::kKVCache, false, 2>(s, op, ea, st, num_sms, stream);
       if (small) return launch_impl<128, 128, 6, Epi::kKVCache, false>(s, op, ea, st, num_sms, stream);
+      if (ea.t_mod % 32 == 0 && ea.B > 0)
+        return launch_impl<128, 256, 4, Epi::kKVCache, false, 1, true>(s, op, ea, st, num_sms, stream);
       return launch_impl<128, 256, 4, Epi::kKVCache, false>(s, op, ea, st, num_sms, stream);
     case Epi::kResidual:
       if (s.N % 256 || op.b_mn_major) return cudaErrorInvalidValue;
       if (tiny && k256) return launch_impl<64, 64, 3, Epi::kResidual, false, 4>(s, op, ea, st, num_sms, stream);
       if (small && k256) return launch_impl<128, 64, 4, Epi::kResidual, false, 2>(s, op, ea, st, num_sms, stream);
       if (small) return launch_impl<128, 64, 8, Epi::kResidual, false>(s, op, ea, st, num_sms, stream);
-      return launch_impl<128, 256, 4, Epi::kResidual, false>(s, op, ea, st, num_sms, stream);
+      return launch_impl<128, 256, 4, Epi::kResidual, false, 1, true>(s, op, ea, st, num_sms, stream);
     case Epi::kStoreF32:
       if (s.N % 192 || s.n_split % 192 || op.b_mn_major) return cudaErrorInvalidValue;
       if (tiny && k256) return launch_impl<64, 64, 3, Epi::kStoreF32, false, 4>(s, op, ea, st, num_sms, stream);
       if (small && k256) return launch_impl<128, 64, 4, Epi::kStoreF32, false, 2>(s, op, ea, st, num_sms, stream);
       if (small) return launch_impl<128, 64, 8, Epi::kStoreF32, false>(s, op, ea, st, num_sms, stream);
-      return launch_impl<128, 192, 5, Epi::kStoreF32, false>(s, op, ea, st, num_sms, stream);
+      return launch_impl<128, 192, 4, Epi::kStoreF32, false, 1, true>(s, op, ea, st, num_sms, stream);
     case Epi::kStoreBf16:
     default:
       if (op.b_mn_major) {
@@ -591,6 +808,37 @@ bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+static bool encode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
+                   const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, dt, rank, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tmap_store_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {32, 32};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+bool make_tmap_store_f32_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 4};
+  cuuint32_t box[2] = {32, 32};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool make_tmap_store_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid, uint64_t outer,
+                             uint64_t mid_stride_bytes, uint64_t outer_stride_bytes) {
+  cuuint64_t dims[3] = {inner, mid, outer};
+  cuuint64_t strides[2] = {mid_stride_bytes, outer_stride_bytes};
+  cuuint32_t box[3] = {32, 32, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid, uint64_t outer,

@@ -21,6 +21,13 @@ struct DevStatusHost {
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
                        uint32_t box_rows, uint32_t box_cols);
 
+// Tensor maps for epilogue stores of 32 x 32 chunks: bf16 with 64-byte
+// swizzle (64-byte chunk rows), float32 with 128-byte swizzle.
+bool make_tmap_store_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld);
+bool make_tmap_store_f32_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld);
+bool make_tmap_store_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid, uint64_t outer,
+                             uint64_t mid_stride_bytes, uint64_t outer_stride_bytes);
+
 // 3D bf16 tensor map over [outer][mid][inner] with byte strides for mid and
 // outer, box {box_inner, box_mid, 1}, 128-byte swizzle.
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid, uint64_t outer,
@@ -90,23 +97,27 @@ struct EpiArgs {
   float* part;
   size_t part_bytes;
   int* counters;
+  // rows of the K/V caches the kv_b epilogue may write (t < t_off + t_mod)
+  int B;
 };
 
 cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, const EpiArgs& ea,
                         const DevStatusHost& st, int num_sms, cudaStream_t stream);
 
 // ---- row kernels --------------------------------------------------------------
-cudaError_t launch_rope_table(float2* cs, int n_pos, int pos0, float base, cudaStream_t stream);
 cudaError_t launch_rmsnorm_rows(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_bfloat16* y, int rows,
                                 float eps, cudaStream_t stream);
 // Split the A-projection output ca [rows, 2112] (float32) into RMSNorm(c^Q) [rows,1536],
 // RMSNorm(c^KV) [rows,512] and RoPE(k_pe) [rows,64]; optional latent cache
-// copies at ckv_cache[b, t_off + t] / kpe_cache[b, t_off + t].
+// copies at ckv_cache[b, t_off + t] / kpe_cache[b, t_off + t]; also writes the
+// RoPE table cs[t] = (cos, sin)((pos0 + t) theta_i) that the q_b epilogue reads.
 struct LatentArgs {
   const float* ca;
   const __nv_bfloat16* g_qa;
   const __nv_bfloat16* g_kva;
-  const float2* cs;
+  float2* cs;              // RoPE table [t_mod, 32] written here (rows of batch 0)
+  double inv_freq[32];     // theta_i = base^(-2i/64), computed on the host in double
+  int pos0;                // position of t = 0
   __nv_bfloat16* cq;
   __nv_bfloat16* ckv;
   __nv_bfloat16* kpe;

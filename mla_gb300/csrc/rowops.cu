@@ -1,30 +1,20 @@
 // Row-wise kernels of the MLA path (HBM-bound, one pass over each row):
-//   * RoPE table R_t: (cos, sin)(t * theta_i), theta_i = base^(-2i/64), the
-//     angle formed in double precision so that positions up to 2^20 keep
-//     full float accuracy (dense-block page: "R [T positions, 32 pairs]");
 //   * input RMSNorm x_attn = g * x / sqrt(mean(x^2) + eps) (dense-block page,
 //     first equation), float32 math, one bf16 rounding;
 //   * split of the A-projection output into c^Q, c^KV and k^pe, with the
 //     q_a / kv_a latent RMSNorms and RoPE on the shared rotary key
 //     (key-value compression page: split after the product, only the
-//     512-wide latent normalised), plus the optional latent-cache write.
+//     512-wide latent normalised), plus the optional latent-cache write and
+//     the RoPE table R_t: (cos, sin)(t * theta_i), theta_i = base^(-2i/64)
+//     (dense-block page: "R [T positions, 32 pairs]"), the angle reduced
+//     modulo 2 pi in double precision so that large positions keep float
+//     accuracy.
 #include "common.cuh"
 #include "internal.h"
 
 namespace mla {
 
 namespace {
-
-__global__ void rope_table_kernel(float2* __restrict__ cs, int n_pos, int pos0, double base) {
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= n_pos * 32) return;
-  const int t = idx >> 5;
-  const int i = idx & 31;
-  const double theta = pow(base, -2.0 * (double)i / 64.0);
-  double s, c;
-  sincos((double)(pos0 + t) * theta, &s, &c);
-  cs[idx] = make_float2((float)c, (float)s);
-}
 
 // One CTA of 128 threads per row of 7168 (= 128 threads x 7 uint4).
 __global__ void __launch_bounds__(128) rmsnorm_7168_kernel(const __nv_bfloat16* __restrict__ x,
@@ -112,10 +102,20 @@ __global__ void __launch_bounds__(256) latent_split_kernel(const LatentArgs a) {
   // c^KV-hat = RMSNorm(c^KV): 512 values = 4 float4 per lane; also the latent cache row
   __nv_bfloat16* dcache = a.ckv_cache ? a.ckv_cache + ((size_t)b * a.cap + t) * 512 : nullptr;
   norm_store(reinterpret_cast<const float4*>(src + 1536), 4, a.g_kva, a.eps, a.ckv + row * 512, dcache, lane);
+  // R_t: angle (pos0 + t) * theta_i formed and reduced modulo 2 pi in double
+  // precision (Cody-Waite style, 2 pi split in two doubles), then a float
+  // sincos of the reduced angle
+  const int tm = (int)(row % a.t_mod);
+  const double ang = (double)(a.pos0 + tm) * a.inv_freq[lane];
+  const double kq = rint(ang * 0.15915494309189535);  // 1 / (2 pi)
+  const double red = fma(-kq, 6.283185307179586, ang) - kq * 2.4492935982947064e-16;
+  float sn, cn;
+  sincosf((float)red, &sn, &cn);
+  const float2 cs = make_float2(cn, sn);
+  if (b == 0) a.cs[(size_t)tm * 32 + lane] = cs;
   // k^R = RoPE(k^pe, t): lane i rotates pair (i, i + 32); k^pe is not normalised
   const float x1 = src[2048 + lane];
   const float x2 = src[2048 + 32 + lane];
-  const float2 cs = a.cs[(size_t)(row % a.t_mod) * 32 + lane];
   const __nv_bfloat16 y1 = __float2bfloat16_rn(x1 * cs.x - x2 * cs.y);
   const __nv_bfloat16 y2 = __float2bfloat16_rn(x2 * cs.x + x1 * cs.y);
   __nv_bfloat16* d = a.kpe + row * 64;
@@ -141,12 +141,6 @@ __global__ void copy_qpe_kernel(const __nv_bfloat16* __restrict__ q, __nv_bfloat
 }
 
 }  // namespace
-
-cudaError_t launch_rope_table(float2* cs, int n_pos, int pos0, float base, cudaStream_t stream) {
-  const int n = n_pos * 32;
-  rope_table_kernel<<<(n + 255) / 256, 256, 0, stream>>>(cs, n_pos, pos0, (double)base);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_rmsnorm_rows(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_bfloat16* y, int rows,
                                 float eps, cudaStream_t stream) {
