@@ -79,6 +79,22 @@ def dist_env():
     return ws, rank, local
 
 
+def reduce_max(v, device=None):
+    """Max of a float over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return v
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(units_per_rank, world, ms_max):
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return world * units_per_rank / (ms_max * 1e-3)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -373,12 +389,7 @@ def main():
         dist.init_process_group("nccl")
 
     def barrier_max(v):
-        if world == 1:
-            return v
-        import torch.distributed as dist
-        t = torch.tensor([v], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(v, dev)
 
     pk = peaks()
     r = Runner(dev)
@@ -397,7 +408,7 @@ def main():
         wall = time.perf_counter() - wall0
     ms_step = barrier_max(statistics.mean(ms))
     tok = B * T
-    value = world * tok / (ms_step * 1e-3)
+    value = weak_scaling_value(tok, world, ms_step)
     flops = tok * proj_flops_per_token() + prefill_attn_flops(B, T)
     roof = roofline_entry(stage_ms, "prefill", B, T, pk, "prefill_b1_t2048")
 

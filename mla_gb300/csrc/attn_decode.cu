@@ -352,8 +352,12 @@ __global__ void __launch_bounds__(192, 1)
           ++next_pv;
           progress = true;
         }
-        if (progress) wd.reset();
-        else if (wd.expired(st, abort_flag, 63)) break;
+        if (progress) {
+          wd.reset();
+        } else {
+          if (wd.expired(st, abort_flag, 63)) break;
+          __nanosleep(32);
+        }
       }
       umma_commit(&bar->drain);
       mbar_wait(&bar->drain, 0, st, nullptr, 66);
@@ -395,19 +399,26 @@ __global__ void __launch_bounds__(192, 1)
         for (int c = 0; c < 64; ++c)
           if (k0 + c >= key_end) s[c] = __float_as_uint(-INFINITY);
       }
+      {
+        float mp[8];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+        for (int i = 0; i < 8; ++i) mp[i] = __uint_as_float(s[i]);
+#pragma unroll
+        for (int c = 8; c < 64; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(s[c]));
+        mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      }
       mx *= sl2;  // log2 units (the scale is positive)
       const bool need = valid && mx > m + kRescaleThresholdLatent;
       const float m_new = need ? mx : m;
       const float alpha = need ? ex2_approx(m - m_new) : 1.f;
-      float sum = 0.f;
+      float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const float p = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -m_new));
         s[c] = __float_as_uint(p);
-        sum += p;
+        sp[c & 7] += p;
       }
+      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       l = l * alpha + sum;
       m = m_new;
       if (valid) bar->alpha[stg][h] = alpha;

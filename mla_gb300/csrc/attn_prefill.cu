@@ -7,20 +7,21 @@
 //
 // CTA = (128-query tile, head, sequence), heaviest tiles launched first.
 // Warp roles (224 threads):
-//   warp 0   TMA: the Q tile once, then K tiles into a 1-slot buffer
-//   warp 6   TMA: V tiles into a 2-slot ring (each V tile is requested a
-//            whole tile ahead of the P.V that reads it)
+//   warp 0   TMA: the Q tile once, then K tiles into a 2-slot ring
+//   warp 6   TMA: V tiles into a 2-slot ring (each K and V tile is requested
+//            a whole tile ahead of the MMA that reads it)
 //   warp 1   TMEM allocation; one lane issues the MMAs:
 //              S_j = Q K_j^T   M=128 N=128 K=192, into one of two TMEM buffers
-//              O  += P_j V_j   M=128 N=128 K=128, P from shared memory,
-//                              V read MN-major straight from its TMA tile
+//              O  += P_j V_j   M=128 N=128 K=128, P read from tensor memory
+//                              (row m in lane m, bf16 pairs packed per
+//                              column), V read MN-major from its TMA tile
 //            issued in the order S_0, S_1, PV_0, S_2, PV_1, ... so the tensor
 //            core computes the next scores while the softmax runs
 //   warps 2..5  one thread per query row: read S_j from TMEM, scale, causal
 //            mask on the diagonal tile, running max with lazy rescaling (O is
 //            rescaled in TMEM only when the max grows by more than 2^8, so P
-//            stays <= 256), P_j to shared memory as bf16 (128-byte swizzle),
-//            and at the end O / l to global memory.
+//            stays <= 256), P_j as bf16 into one of two TMEM buffers, and
+//            at the end O / l to global memory.
 // Layout: Q [B*T, 64*192], K/V caches [B, 64, cap, 192|128] (TMA 3D views
 // whose position extent is T, so keys >= T read as zeros), O [B*T, 64*128].
 #include "common.cuh"
@@ -33,27 +34,24 @@ namespace {
 constexpr int kThreads = 224;
 constexpr uint32_t kAtom = 128 * 128;            // 128 rows x 64 bf16
 constexpr uint32_t kQOff = 0;                    // 3 atoms
-constexpr uint32_t kKOff = 3 * kAtom;            // 1 slot x 3 atoms
-constexpr uint32_t kVOff = 6 * kAtom;            // 2 slots x 2 atoms (vdim 0-63, 64-127)
-constexpr uint32_t kPOff = 10 * kAtom;           // 2 atoms (keys 0-63, 64-127)
-constexpr uint32_t kBarOff = 12 * kAtom;
+constexpr uint32_t kKOff = 3 * kAtom;            // 2 slots x 3 atoms
+constexpr uint32_t kVOff = 9 * kAtom;            // 2 slots x 2 atoms (vdim 0-63, 64-127)
+constexpr uint32_t kBarOff = 13 * kAtom;
+// tensor memory columns: S_0, S_1 (fp32), O (fp32), P_0, P_1 (bf16 pairs)
+constexpr uint32_t kTmS = 0, kTmO = 256, kTmP = 384;
 constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full, k_empty;
+  uint64_t k_full[2], k_empty[2];
   uint64_t v_full[2], v_empty[2];
   uint64_t s_full[2], s_free[2];
-  uint64_t p_full, pv_done;
+  uint64_t p_full[2], pv_done[2];
   uint64_t drain;
   uint32_t tmem_slot;
   int abort;
 };
-
-__device__ __forceinline__ uint32_t p_offset(int r, int k) {
-  return (uint32_t)((k >> 6) * kAtom + r * 128 + ((((k & 63) >> 3) ^ (r & 7)) << 4));
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -80,10 +78,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar->s_full[i], 1);
       mbar_init(&bar->s_free[i], 128);
     }
-    mbar_init(&bar->k_full, 1);
-    mbar_init(&bar->k_empty, 1);
-    mbar_init(&bar->p_full, 128);
-    mbar_init(&bar->pv_done, 1);
+    mbar_init(&bar->k_full[0], 1);
+    mbar_init(&bar->k_empty[0], 1);
+    mbar_init(&bar->k_full[1], 1);
+    mbar_init(&bar->k_empty[1], 1);
+    mbar_init(&bar->p_full[0], 128);
+    mbar_init(&bar->p_full[1], 128);
+    mbar_init(&bar->pv_done[0], 1);
+    mbar_init(&bar->pv_done[1], 1);
     mbar_init(&bar->drain, 1);
     bar->abort = 0;
     fence_barrier_init();
@@ -105,16 +107,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmK);
       mbar_arrive_expect_tx(&bar->q_full, 3 * kAtom);
       for (int c = 0; c < 3; ++c) tma_load_3d(smem + kQOff + c * kAtom, &tmQ, &bar->q_full, h * 192 + 64 * c, q0, b);
-      int issued = 0;
+      int issued[2] = {0, 0};
       for (int j = 0; j < n_kv; ++j) {
-        if (!mbar_wait(&bar->k_empty, (j & 1) ^ 1, st, abort_flag, 40)) break;
-        mbar_arrive_expect_tx(&bar->k_full, 3 * kAtom);
+        const int slot = j & 1;
+        if (!mbar_wait(&bar->k_empty[slot], ((j >> 1) & 1) ^ 1, st, abort_flag, 40)) break;
+        mbar_arrive_expect_tx(&bar->k_full[slot], 3 * kAtom);
         for (int c = 0; c < 3; ++c)
-          tma_load_3d(smem + kKOff + c * kAtom, &tmK, &bar->k_full, 64 * c, j * 128, kv_row);
-        issued++;
+          tma_load_3d(smem + kKOff + (slot * 3 + c) * kAtom, &tmK, &bar->k_full[slot], 64 * c, j * 128, kv_row);
+        issued[slot]++;
       }
       mbar_wait(&bar->q_full, 0, st, nullptr, 41);
-      if (issued) mbar_wait(&bar->k_full, (issued - 1) & 1, st, nullptr, 41);
+      for (int i = 0; i < 2; ++i)
+        if (issued[i]) mbar_wait(&bar->k_full[i], (issued[i] - 1) & 1, st, nullptr, 41);
     }
   } else if (warp == 6) {
     if (lane == 0) {
@@ -140,7 +144,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_addr = smem_u32(smem + kQOff);
       const uint32_t k_addr = smem_u32(smem + kKOff);
       const uint32_t v_addr = smem_u32(smem + kVOff);
-      const uint32_t p_addr = smem_u32(smem + kPOff);
       bool ok = mbar_wait(&bar->q_full, 0, st, abort_flag, 44);
       tc_fence_after();
       // Event loop: issue S_j (needs K_j and a free score buffer) and PV_j
@@ -154,10 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (next_s < n_kv && next_s <= next_pv + 1) {
           const int slot = next_s & 1;
           const uint32_t ph = (next_s >> 1) & 1;
-          if (mbar_test(&bar->k_full, next_s & 1) && mbar_test(&bar->s_free[slot], ph ^ 1)) {
+          if (mbar_test(&bar->k_full[slot], ph) && mbar_test(&bar->s_free[slot], ph ^ 1)) {
             tc_fence_after();
-            const uint32_t d = tmem + slot * 128;
-            const uint32_t kb = k_addr;
+            const uint32_t d = tmem + kTmS + slot * 128;
+            const uint32_t kb = k_addr + slot * 3 * kAtom;
 #pragma unroll
             for (int kk = 0; kk < 12; ++kk) {
               const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
@@ -165,28 +168,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                         kk > 0 ? 1u : 0u);
             }
             umma_commit(&bar->s_full[slot]);
-            umma_commit(&bar->k_empty);
+            umma_commit(&bar->k_empty[slot]);
             ++next_s;
             progress = true;
           }
         }
-        if (next_pv < next_s && mbar_test(&bar->p_full, next_pv & 1) &&
+        // P_j arrives on p_full[j & 1]: S_{j+2} (hence P_{j+2}) is issued only
+        // after P.V_j, so a barrier never runs two phases ahead of this test
+        if (next_pv < next_s && mbar_test(&bar->p_full[next_pv & 1], (next_pv >> 1) & 1) &&
             mbar_test(&bar->v_full[next_pv & 1], (next_pv >> 1) & 1)) {
           tc_fence_after();
           const uint32_t vb = v_addr + (next_pv & 1) * 2 * kAtom;
+          const uint32_t pa = tmem + kTmP + (next_pv & 1) * 64;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t adesc = sdesc_sw128(p_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
             const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, kAtom, 1024);
-            umma_bf16(tmem + 256, adesc, bdesc, idesc_pv, (next_pv > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16_ts(tmem + kTmO, pa + kk * 8, bdesc, idesc_pv, (next_pv > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&bar->pv_done);
+          umma_commit(&bar->pv_done[next_pv & 1]);
           umma_commit(&bar->v_empty[next_pv & 1]);
           ++next_pv;
           progress = true;
         }
-        if (progress) wd.reset();
-        else if (wd.expired(st, abort_flag, 45)) break;
+        if (progress) {
+          wd.reset();
+        } else {
+          if (wd.expired(st, abort_flag, 45)) break;
+          __nanosleep(32);  // leave issue slots to the softmax warp on this scheduler
+        }
       }
       umma_commit(&bar->drain);
       mbar_wait(&bar->drain, 0, st, nullptr, 49);
@@ -197,7 +206,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quarter * 32 + lane;
     const int qpos = q0 + row;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    uint8_t* pbuf = smem + kPOff;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
@@ -211,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
         uint32_t (&s2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[64]);
         uint32_t (&s3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[96]);
-        const uint32_t ta = tmem + lane_addr + slot * 128;
+        const uint32_t ta = tmem + lane_addr + kTmS + slot * 128;
         tmem_ld32(ta, s0);
         tmem_ld32(ta + 32, s1);
         tmem_ld32(ta + 64, s2);
@@ -224,37 +232,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k0 = j * 128;
       // max of the raw scores (the scale is positive), causal mask on the
       // diagonal tile only
-      float mx = -INFINITY;
       if (diag) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
+        for (int c = 0; c < 128; ++c)
           if (k0 + c > qpos) s[c] = __float_as_uint(-INFINITY);
-          mx = fmaxf(mx, __uint_as_float(s[c]));
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
       }
+      // eight independent partial maxima / sums keep the reductions off a
+      // single serial dependency chain
+      float mp[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mp[i] = __uint_as_float(s[i]);
+#pragma unroll
+      for (int c = 8; c < 128; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(s[c]));
+      float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       mx *= sl2;  // log2 units
       const bool need = mx > m + kRescaleThreshold;
       const float m_new = need ? mx : m;
       const float alpha = need ? ex2_approx(m - m_new) : 1.f;
-      float sum = 0.f;
+      float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 128; ++c) {
         const float p = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -m_new));
         s[c] = __float_as_uint(p);
-        sum += p;
+        sp[c & 7] += p;
       }
+      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       l = l * alpha + sum;
       m = m_new;
-      if (j > 0) {
-        // P buffer free and O final for tile j-1
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar->pv_done, (j - 1) & 1, st, abort_flag, 51));
+      // P buffer (j & 1) is free once P.V of tile j-2 has completed
+      if (j > 1) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar->pv_done[j & 1], ((j - 2) >> 1) & 1, st, abort_flag, 51));
+        if (!ok) break;
+      }
+      // O may be rescaled only after P.V of tile j-1 has completed
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, st, abort_flag, 53));
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {
-          const uint32_t ta = tmem + lane_addr + 256;
+        {
+          const uint32_t ta = tmem + lane_addr + kTmO;
 #pragma unroll 1
           for (int c = 0; c < 128; c += 32) {
             uint32_t r[32];
@@ -267,25 +283,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_st();
         }
       }
-      // P_j (bf16) into shared memory, K-major with 128-byte swizzle
+      // P_j (bf16 pairs, low half = even key) into tensor memory buffer j & 1
+      {
+        uint32_t pk[64];
 #pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        const int k = c8 * 8;
-        const uint4 v = make_uint4(pack_bf16x2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])),
-                                   pack_bf16x2(__uint_as_float(s[k + 2]), __uint_as_float(s[k + 3])),
-                                   pack_bf16x2(__uint_as_float(s[k + 4]), __uint_as_float(s[k + 5])),
-                                   pack_bf16x2(__uint_as_float(s[k + 6]), __uint_as_float(s[k + 7])));
-        *reinterpret_cast<uint4*>(pbuf + p_offset(row, k)) = v;
+        for (int c = 0; c < 64; ++c) pk[c] = pack_bf16x2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
+        const uint32_t tp = tmem + lane_addr + kTmP + (j & 1) * 64;
+#pragma unroll
+        for (int c = 0; c < 64; c += 16) tmem_st16(tp + c, &pk[c]);
+        tmem_wait_st();
       }
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bar->p_full);
+      mbar_arrive(&bar->p_full[j & 1]);
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar->pv_done, (n_kv - 1) & 1, st, abort_flag, 52));
+    if (ok)
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(&bar->pv_done[(n_kv - 1) & 1], ((n_kv - 1) >> 1) & 1, st, abort_flag, 52));
     if (ok) {
       tc_fence_after();
       const float inv = 1.f / l;
-      const uint32_t ta = tmem + lane_addr + 256;
+      const uint32_t ta = tmem + lane_addr + kTmO;
       __nv_bfloat16* dst = o + ((size_t)b * T + qpos) * 8192 + h * 128;
 #pragma unroll 1
       for (int c = 0; c < 128; c += 32) {
