@@ -357,6 +357,14 @@ __device__ __forceinline__ void run_epilogue_tma(const EpiArgs& ea, const Src& l
     const int b = row0 / ea.t_mod;
     const int t0 = ea.t_off + row0 % ea.t_mod;
     const int plane = b * 64 + h;
+    // the shared rotary key of this row (K columns 128..191), loaded first so
+    // that its latency overlaps the accumulator chunks
+    uint4 kv4[8];
+    if (o0 == 0) {
+      const uint4* src = reinterpret_cast<const uint4*>(ea.kpe + (size_t)row * 64);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) kv4[j] = row_ok ? src[j] : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t r[32];
@@ -371,12 +379,9 @@ __device__ __forceinline__ void run_epilogue_tma(const EpiArgs& ea, const Src& l
         ss.issue3(m1, buf, col - 128, t0, plane, lane);
     }
     if (warp_ok && o0 == 0) {
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        uint4 v[4];
-        const uint4* src = reinterpret_cast<const uint4*>(ea.kpe + (size_t)row * 64 + half * 32);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = row_ok ? src[j] : make_uint4(0, 0, 0, 0);
+      for (int half = 0; half < 2; ++half) {
+        const uint4 v[4] = {kv4[4 * half], kv4[4 * half + 1], kv4[4 * half + 2], kv4[4 * half + 3]};
         uint8_t* buf = ss.next(lane);
         stage_bf16_raw(buf, lane, v);
         ss.issue3(m0, buf, 128 + 32 * half, t0, plane, lane);
@@ -416,6 +421,23 @@ __device__ __forceinline__ void run_epilogue_tma(const EpiArgs& ea, const Src& l
   }
 }
 
+// Tile index -> (batch, row block, column block).  Tiles walk groups of g row
+// blocks; inside a group the row block changes fastest, so one wave of CTAs
+// shares a few column blocks of B and a few row blocks of A (g = 1: column
+// block fastest, every row block of A read once while all of B is reused).
+__device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int g, int& batch, int& m_blk,
+                                            int& n_blk) {
+  const int per_batch = m_tiles * n_tiles;
+  batch = tile / per_batch;
+  const int t = tile % per_batch;
+  const int group_tiles = g * n_tiles;
+  const int grp = t / group_tiles;
+  const int gm = (m_tiles - grp * g) < g ? (m_tiles - grp * g) : g;  // rows in this (last) group
+  const int r = t % group_tiles;
+  m_blk = grp * g + r % gm;
+  n_blk = r / gm;
+}
+
 // BM = 128: accumulator row r in TMEM lane r.  BM = 64 (few rows, decode):
 // row r in lane 32*(r/16) + r%16, so each epilogue warp holds 16 rows.
 template <int BM, int BN, int STAGES, int KSUB, Epi EPI, bool B_MN, bool TMA_ST>
@@ -440,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int m_tiles = (s.M + BM - 1) / BM;
-  const int n_tiles = s.N / BN;
+  const int n_tiles = TMA_ST ? (s.N + BN - 1) / BN : s.N / BN;  // TMA stores clip columns >= N
   const int num_tiles = s.batches * m_tiles * n_tiles;
   const int kblocks = s.K / (kBK * KSUB);  // stages of KSUB K blocks
   const int ksplit = s.ksplit;
@@ -486,9 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tile = unit / ksplit;
         const int kb0 = (unit % ksplit) * s.kb_per;
         const int kb1 = min(kblocks, kb0 + s.kb_per);
-        const int n_blk = tile % n_tiles;
-        const int m_blk = (tile / n_tiles) % m_tiles;
-        const int batch = tile / (n_tiles * m_tiles);
+        int batch, m_blk, n_blk;
+        tile_coords(tile, m_tiles, n_tiles, s.raster_g, batch, m_blk, n_blk);
         const int n0 = n_blk * BN;
         const int a_col = s.a_col0 + batch * s.a_col_step;
         const int b_row = s.b_row0 + batch * s.b_row_step;
@@ -590,9 +611,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int unit = blockIdx.x; unit < num_units; unit += gridDim.x) {
       const int tile = unit / ksplit;
       const int ks = unit % ksplit;
-      const int n_blk = tile % n_tiles;
-      const int m_blk = (tile / n_tiles) % m_tiles;
-      const int batch = tile / (n_tiles * m_tiles);
+      int batch, m_blk, n_blk;
+      tile_coords(tile, m_tiles, n_tiles, s.raster_g, batch, m_blk, n_blk);
       bool ok = mbar_wait(&tfull_bar[acc], acc_phase, st, abort_flag, 6);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
@@ -696,8 +716,9 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
   });
   if (attr_err != cudaSuccess) return attr_err;
   GemmShape sh = s;
+  if (sh.raster_g < 1) sh.raster_g = 1;
   const int m_tiles = (s.M + BM - 1) / BM;
-  const int tiles = s.batches * m_tiles * (s.N / BN);
+  const int tiles = s.batches * m_tiles * (TMA_ST ? (s.N + BN - 1) / BN : s.N / BN);
   const int kblocks = s.K / (kBK * KSUB);
   sh.ksplit = 1;
   sh.kb_per = kblocks;
@@ -748,17 +769,26 @@ cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, con
       if (ea.t_mod % 32 == 0 && ea.B > 0)
         return launch_impl<128, 256, 4, Epi::kKVCache, false, 1, true>(s, op, ea, st, num_sms, stream);
       return launch_impl<128, 256, 4, Epi::kKVCache, false>(s, op, ea, st, num_sms, stream);
-    case Epi::kResidual:
+    case Epi::kResidual: {
       if (s.N % 256 || op.b_mn_major) return cudaErrorInvalidValue;
+      // o_proj: W_o (117 MB) does not stay in L2 -> waves of 16 row blocks
+      GemmShape g16 = s;
+      g16.raster_g = 16;
       if (tiny && k256) return launch_impl<64, 64, 3, Epi::kResidual, false, 4>(s, op, ea, st, num_sms, stream);
       if (small && k256) return launch_impl<128, 64, 4, Epi::kResidual, false, 2>(s, op, ea, st, num_sms, stream);
       if (small) return launch_impl<128, 64, 8, Epi::kResidual, false>(s, op, ea, st, num_sms, stream);
-      return launch_impl<128, 256, 4, Epi::kResidual, false, 1, true>(s, op, ea, st, num_sms, stream);
+      return launch_impl<128, 256, 4, Epi::kResidual, false, 1, true>(g16, op, ea, st, num_sms, stream);
+    }
     case Epi::kStoreF32:
       if (s.N % 192 || s.n_split % 192 || op.b_mn_major) return cudaErrorInvalidValue;
       if (tiny && k256) return launch_impl<64, 64, 3, Epi::kStoreF32, false, 4>(s, op, ea, st, num_sms, stream);
       if (small && k256) return launch_impl<128, 64, 4, Epi::kStoreF32, false, 2>(s, op, ea, st, num_sms, stream);
       if (small) return launch_impl<128, 64, 8, Epi::kStoreF32, false>(s, op, ea, st, num_sms, stream);
+      // Few row blocks: 128-wide tiles (2112 = 16.5 x 128: 17 column tiles, the
+      // last one half empty and clipped on store) give more tiles per wave;
+      // many row blocks: 192-wide tiles read A fewer times.
+      if (((s.M + kBM - 1) / kBM) * 11 < 4 * num_sms)
+        return launch_impl<128, 128, 6, Epi::kStoreF32, false, 1, true>(s, op, ea, st, num_sms, stream);
       return launch_impl<128, 192, 4, Epi::kStoreF32, false, 1, true>(s, op, ea, st, num_sms, stream);
     case Epi::kStoreBf16:
     default:

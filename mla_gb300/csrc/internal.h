@@ -47,6 +47,8 @@ struct GemmShape {
   int n_split;
   int ksplit;   // set by launch_gemm: K slices per tile (1 = no split)
   int kb_per;   // set by launch_gemm: 64-wide K blocks per slice
+  int raster_g; // set by launch_gemm: tiles walk groups of raster_g row blocks,
+                // row block fastest inside a group (1 = column block fastest)
 };
 
 // Split-K (used when a GEMM has too few output tiles to fill the GPU, as
