@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const DecodeAttnArgs a
     fence_barrier_init();
   }
   __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();
 
   auto issue = [&](int c) {
     const int stg = c % kDecStages;
@@ -177,6 +179,8 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const DecodeAttnArgs a
 // out[row, 0:width] = sum_s w_s part_o[row, s] / sum_s w_s l_s,  w_s = 2^(m_s - max m)
 __global__ void combine_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
                                __nv_bfloat16* __restrict__ out, int splits, int width) {
+  pdl_launch_dependents();
+  pdl_wait();
   const size_t row = blockIdx.x;
   float mx = -INFINITY;
   for (int s = 0; s < splits; ++s) mx = fmaxf(mx, part_ml[row * splits + s].x);
@@ -276,6 +280,8 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bar->tmem_slot;
+  pdl_launch_dependents();
+  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -511,6 +517,8 @@ __global__ void __launch_bounds__(192, 1)
 // expects [(row*splits + s), width] with row = (b, h): regroup here.
 __global__ void latent_combine_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
                                       __nv_bfloat16* __restrict__ out, int splits) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int h = blockIdx.x, b = blockIdx.y;
   float mx = -INFINITY;
   for (int s = 0; s < splits; ++s) mx = fmaxf(mx, part_ml[((size_t)b * splits + s) * 64 + h].x);
@@ -561,13 +569,12 @@ cudaError_t launch_decode_attention(const DecodeAttnArgs& a, const DevStatusHost
   const int cl = chunk_len_for(a.L, a.splits, kDecChunk);
   DevStatus dst{st.word, st.wait_limit_ns};
   dim3 grid(a.splits, 64, a.B);
-  decode_attn_kernel<<<grid, 128, sizeof(DecodeSmem), stream>>>(a, dst, cl);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(decode_attn_kernel, grid, dim3(128), sizeof(DecodeSmem), stream, a, dst, cl);
   if (e != cudaSuccess) return e;
   ++*launches;
   if (a.splits > 1) {
-    combine_kernel<<<a.B * 64, 64, 0, stream>>>(a.part_o, a.part_ml, a.o, a.splits, 128);
-    e = cudaGetLastError();
+    e = launch_pdl(combine_kernel, dim3(a.B * 64), dim3(64), 0, stream, (const float*)a.part_o,
+                   (const float2*)a.part_ml, a.o, a.splits, 128);
     ++*launches;
   }
   return e;
@@ -601,13 +608,12 @@ cudaError_t launch_latent_attention(const LatentAttnArgs& a, const DevStatusHost
   const int cl = chunk_len_for(a.L, a.splits, kLatTile);
   DevStatus dst{st.word, st.wait_limit_ns};
   dim3 grid(a.splits, a.B);
-  latent_attn_tc<<<grid, 192, kLatSmemBytes, stream>>>(tq, tc, tr, a, dst, cl);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(latent_attn_tc, grid, dim3(192), kLatSmemBytes, stream, tq, tc, tr, a, dst, cl);
   if (e != cudaSuccess) return e;
   ++*launches;
   if (a.splits > 1) {
-    latent_combine_kernel<<<dim3(64, a.B), 128, 0, stream>>>(a.part_o, a.part_ml, a.olat, a.splits);
-    e = cudaGetLastError();
+    e = launch_pdl(latent_combine_kernel, dim3(64, a.B), dim3(128), 0, stream, (const float*)a.part_o,
+                   (const float2*)a.part_ml, a.olat, a.splits);
     ++*launches;
   }
   return e;

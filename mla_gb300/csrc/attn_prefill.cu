@@ -99,6 +99,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bar->tmem_slot;
   const int kv_row = b * 64 + h;
+  pdl_launch_dependents();
+  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -349,9 +351,8 @@ cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, const DevStatusHo
   const int n_qt = (a.T + 127) / 128;
   dim3 grid(n_qt, 64, a.B);
   DevStatus dst{st.word, st.wait_limit_ns};
-  prefill_attn_tc<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, a.o, a.T, n_qt, a.scale * 1.4426950408889634f,
-                                                           dst);
-  return cudaGetLastError();
+  return launch_pdl(prefill_attn_tc, grid, dim3(kThreads), kSmemBytes, stream, tq, tk, tv, a.o, a.T, n_qt,
+                    a.scale * 1.4426950408889634f, dst);
 }
 
 }  // namespace mla

@@ -494,6 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_launch_dependents();
+  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -739,8 +741,7 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
   const int units = tiles * sh.ksplit;
   const int grid = units < num_sms ? units : num_sms;
   DevStatus dst{st.word, st.wait_limit_ns};
-  kern<<<grid, kThreads, L::kBytes, stream>>>(ta, tb0, tb1, to0, to1, sh, ea, dst);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, stream, ta, tb0, tb1, to0, to1, sh, ea, dst);
 }
 
 }  // namespace

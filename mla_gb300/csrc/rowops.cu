@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(128) rmsnorm_7168_kernel(const __nv_bfloat16* 
                                                            const __nv_bfloat16* __restrict__ g,
                                                            __nv_bfloat16* __restrict__ y, float eps) {
   constexpr int kVec = 7;  // 7168 / 8 / 128
+  pdl_launch_dependents();
+  pdl_wait();
   const size_t row = blockIdx.x;
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * 7168);
   uint4 v[kVec];
@@ -90,6 +92,8 @@ __device__ __forceinline__ void norm_store(const float4* src, int n4, const __nv
 }
 
 __global__ void __launch_bounds__(256) latent_split_kernel(const LatentArgs a) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= a.rows) return;
@@ -129,6 +133,8 @@ __global__ void __launch_bounds__(256) latent_split_kernel(const LatentArgs a) {
 }
 
 __global__ void copy_qpe_kernel(const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ qlat, int B) {
+  pdl_launch_dependents();
+  pdl_wait();
   // one thread per (b, h, 16-byte chunk of the 64 pe values): 8 chunks
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= B * 64 * 8) return;
@@ -144,20 +150,18 @@ __global__ void copy_qpe_kernel(const __nv_bfloat16* __restrict__ q, __nv_bfloat
 
 cudaError_t launch_rmsnorm_rows(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_bfloat16* y, int rows,
                                 float eps, cudaStream_t stream) {
-  rmsnorm_7168_kernel<<<rows, 128, 0, stream>>>(x, g, y, eps);
-  return cudaGetLastError();
+  return launch_pdl(rmsnorm_7168_kernel, dim3(rows), dim3(128), 0, stream, x, g, y, eps);
 }
 
 cudaError_t launch_latent_split(const LatentArgs& a, cudaStream_t stream) {
   const int warps_per_block = 8;
-  latent_split_kernel<<<(a.rows + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(latent_split_kernel, dim3((a.rows + warps_per_block - 1) / warps_per_block),
+                    dim3(32 * warps_per_block), 0, stream, a);
 }
 
 cudaError_t launch_copy_qpe(const __nv_bfloat16* q, __nv_bfloat16* qlat, int B, cudaStream_t stream) {
   const int n = B * 64 * 8;
-  copy_qpe_kernel<<<(n + 255) / 256, 256, 0, stream>>>(q, qlat, B);
-  return cudaGetLastError();
+  return launch_pdl(copy_qpe_kernel, dim3((n + 255) / 256), dim3(256), 0, stream, q, qlat, B);
 }
 
 }  // namespace mla
