@@ -55,11 +55,11 @@ Layout make_layout(int mode, int B, int t_or_p, int num_sms) {
     L.part_o = take((size_t)B * MLA_HEADS * s * MLA_V * sizeof(float));
     L.part_ml = take((size_t)B * MLA_HEADS * s * sizeof(float2));
   } else {
-    const int s = latent_splits(B, t_or_p + 1, num_sms);
+    const int g = latent_ctas(B, t_or_p + 1, num_sms);
     L.qlat = take((size_t)B * MLA_HEADS * 576 * 2);
     L.olat = take((size_t)B * MLA_HEADS * MLA_KV_LORA * 2);
-    L.part_o = take((size_t)B * s * MLA_HEADS * MLA_KV_LORA * sizeof(float));
-    L.part_ml = take((size_t)B * s * MLA_HEADS * sizeof(float2));
+    L.part_o = take((size_t)2 * g * MLA_HEADS * MLA_KV_LORA * sizeof(float));
+    L.part_ml = take((size_t)2 * g * MLA_HEADS * sizeof(float2));
   }
   if (mode != MLA_MODE_PREFILL) {
     L.split_bytes = split_part_bytes(B);
@@ -488,7 +488,7 @@ int mla_decode_latent(const mla_weights_t* w, const mla_params_t* params, const 
     a.B = B;
     a.L = P + 1;
     a.cap = cap;
-    a.splits = latent_splits(B, P + 1, sms);
+    a.ctas = latent_ctas(B, P + 1, sms);
     a.scale = p.scale;
     if (launch_latent_attention(a, st, stream_, &launches) != cudaSuccess) return MLA_ERR_CUDA;
   }

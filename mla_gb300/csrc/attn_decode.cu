@@ -201,74 +201,97 @@ __global__ void combine_kernel(const float* __restrict__ part_o, const float2* _
 // ---------------------------------------------------------------------------
 // latent-cache decode on tcgen05
 //
-// CTA = (sequence b, split of the key range), 192 threads:
-//   warp 0     TMA: q_lat [64 heads x 576] once; per 64-key tile the latent
-//              rows c_j [64 x 512] (8 boxes) and rotary keys k^R_j [64 x 64]
-//              into a 2-stage ring (3D tensor maps bound positions to L, so
-//              rows >= L read as zeros)
-//   warp 1     TMEM allocation; one lane issues
-//                S_j   = q_lat . [c_j ; k^R_j]^T      M=64 (heads) N=64 K=576
-//                O^T  += c_j^T . P_j^T               M=128 (latent, 4 blocks)
-//                                                    N=64 (heads) K=64 keys
+// Work: the B sequences' 64-key tiles, flattened in (sequence, tile) order,
+// are cut into G contiguous, equal ranges, one per CTA (G = the SM count, or
+// fewer for small problems).  A range covers the end of one sequence, whole
+// sequences and the start of another; each piece ("segment") is attended
+// with its own online softmax.  A segment that is a whole sequence writes
+// o_lat directly; the pieces of a sequence cut between CTAs are written as
+// unnormalised partials (two slots per CTA: its first and its last segment)
+// and merged by latent_combine_kernel.
+//
+// CTA, 224 threads:
+//   warp 0     TMA: q_lat [64 heads x 576] per segment; per tile the rotary
+//              keys k^R_j [64 x 64] (one box) and the latent rows c_j
+//              [64 x 512] (eight 64x64 boxes) into a 2-stage ring (3D tensor
+//              maps bound positions to L, so rows >= L read as zeros)
+//   warp 1     TMEM allocation; one lane issues S_j = q_lat . [k^R_j ; c_j]^T
+//              (M=64 heads, N=64 keys, K=576), rotary box first: that box is
+//              released as soon as its MMAs are done
+//   warp 6     one lane issues O^T += c_j^T . P_j^T (M=128 latent rows in 4
+//              blocks, N=64 heads, K=64 keys); its completion releases the
+//              latent boxes and tells the softmax that P may be rewritten
 //              (O is kept transposed so the 512-wide latent output takes 256
 //              TMEM columns; c_j serves as the K-major B operand of S and the
-//              MN-major A operand of O^T without a copy)
+//              MN-major A operand of O^T without a copy).  Two issuing
+//              threads keep the tensor pipe fed while either one waits.
 //   warps 2..5 softmax: head h = 16*(warp%4) + lane (lanes 0..15; an M=64
 //              accumulator row r lives in TMEM lane 32*(r/16) + r%16), lazy
 //              rescaling (O^T columns rescaled only when a head's max grows by
 //              more than 2^8), P_j [64 heads x 64 keys] bf16 to shared memory;
-//              at the end every thread writes the latent rows it holds.
+//              at the end of a segment every thread writes the latent rows it
+//              holds.
 // ---------------------------------------------------------------------------
 constexpr int kLatTile = 64;
 constexpr uint32_t kLatBox = 64 * 128;                       // 64 rows x 64 bf16
 constexpr uint32_t kLatQOff = 0;                             // 9 boxes
-constexpr uint32_t kLatCOff = 9 * kLatBox;                   // 2 stages x 8 boxes
-constexpr uint32_t kLatROff = kLatCOff + 16 * kLatBox;       // 2 stages x 1 box
-constexpr uint32_t kLatPOff = kLatROff + 2 * kLatBox;        // 1 box
+constexpr uint32_t kLatCOff = 9 * kLatBox;                   // 2 stages x 9 boxes (box 8 = rotary keys)
+constexpr uint32_t kLatPOff = kLatCOff + 18 * kLatBox;       // 1 box
 constexpr uint32_t kLatBarOff = kLatPOff + kLatBox;
 constexpr uint32_t kLatSmemBytes = kLatBarOff + 1536 + 1024;
+constexpr int kLatThreads = 224;
 
 struct LatBars {
-  uint64_t q_full;
-  uint64_t c_full[2], c_empty[2];
+  uint64_t q_full, q_free;
+  uint64_t kpe_full[2], kpe_empty[2], ckv_full[2], ckv_empty[2];
   uint64_t s_full[2], s_free[2];
-  uint64_t p_full, pv_done, drain;
+  uint64_t p_full, drain_s, drain_pv;
   uint32_t tmem_slot;
   int abort;
   int need[2][4];
   float alpha[2][64];
   float m[64], l[64];
 };
+static_assert(sizeof(LatBars) <= 1536, "barrier block");
+
+// First flattened tile of CTA g's range (ranges are [start(g), start(g+1))).
+__device__ __forceinline__ long long lat_range_start(int g, long long total, int G) {
+  return (long long)g * total / G;
+}
 
 __device__ __forceinline__ void named_sync_128() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kLatThreads, 1)
     latent_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmC,
-                   const __grid_constant__ CUtensorMap tmR, const LatentAttnArgs a, const DevStatus st,
-                   int chunk_len) {
+                   const __grid_constant__ CUtensorMap tmR, const LatentAttnArgs a, const DevStatus st) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   LatBars* bar = reinterpret_cast<LatBars*>(smem + kLatBarOff);
   volatile int* abort_flag = &bar->abort;
-  const int split = blockIdx.x;
-  const int b = blockIdx.y;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int key_begin = split * chunk_len;
-  const int key_end = min(a.L, key_begin + chunk_len);
-  const int n_tiles = (key_end - key_begin + kLatTile - 1) / kLatTile;
+  const int nt = (a.L + kLatTile - 1) / kLatTile;  // tiles per sequence
+  const long long total = (long long)a.B * nt;
+  const int g = blockIdx.x;
+  const long long x0 = lat_range_start(g, total, a.ctas);
+  const int R = (int)(lat_range_start(g + 1, total, a.ctas) - x0);  // tiles of this CTA
+  const int first_seq = (int)(x0 / nt);
+  const int first_t = (int)(x0 - (long long)first_seq * nt);  // tile index of x0 within its sequence
 
   if (threadIdx.x == 0) {
     mbar_init(&bar->q_full, 1);
+    mbar_init(&bar->q_free, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar->c_full[i], 1);
-      mbar_init(&bar->c_empty[i], 1);
+      mbar_init(&bar->kpe_full[i], 1);
+      mbar_init(&bar->kpe_empty[i], 1);
+      mbar_init(&bar->ckv_full[i], 1);
+      mbar_init(&bar->ckv_empty[i], 1);
       mbar_init(&bar->s_full[i], 1);
       mbar_init(&bar->s_free[i], 128);
     }
     mbar_init(&bar->p_full, 128);
-    mbar_init(&bar->pv_done, 1);
-    mbar_init(&bar->drain, 1);
+    mbar_init(&bar->drain_s, 1);
+    mbar_init(&bar->drain_pv, 1);
     bar->abort = 0;
     fence_barrier_init();
   }
@@ -288,85 +311,109 @@ __global__ void __launch_bounds__(192, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmC);
       tma_prefetch_desc(&tmR);
-      mbar_arrive_expect_tx(&bar->q_full, 9 * kLatBox);
-      for (int c = 0; c < 9; ++c) tma_load_2d(smem + kLatQOff + c * kLatBox, &tmQ, &bar->q_full, 64 * c, b * 64);
-      int issued[2] = {0, 0};
-      for (int j = 0; j < n_tiles; ++j) {
-        const int stg = j & 1;
-        if (!mbar_wait(&bar->c_empty[stg], ((j >> 1) & 1) ^ 1, st, abort_flag, 60)) break;
-        const int k0 = key_begin + j * kLatTile;
-        mbar_arrive_expect_tx(&bar->c_full[stg], 9 * kLatBox);
-        for (int c = 0; c < 8; ++c)
-          tma_load_3d(smem + kLatCOff + (stg * 8 + c) * kLatBox, &tmC, &bar->c_full[stg], 64 * c, k0, b);
-        tma_load_3d(smem + kLatROff + stg * kLatBox, &tmR, &bar->c_full[stg], 0, k0, b);
-        issued[stg]++;
+      int seg = 0;
+      int kpe_used[2] = {0, 0}, ckv_used[2] = {0, 0};  // loads issued per stage
+      int b = first_seq, t = first_t - 1;
+      for (int i = 0; i < R; ++i) {
+        if (++t == nt) {
+          t = 0;
+          ++b;
+        }
+        const int stg = i & 1;
+        const uint32_t eph = ((i >> 1) & 1) ^ 1;
+        const int k0 = t * kLatTile;
+        uint8_t* cbase = smem + kLatCOff + stg * 9 * kLatBox;
+        // the rotary box first: it frees earliest and S starts with it
+        if (!mbar_wait(&bar->kpe_empty[stg], eph, st, abort_flag, 61)) break;
+        mbar_arrive_expect_tx(&bar->kpe_full[stg], kLatBox);
+        tma_load_3d(cbase + 8 * kLatBox, &tmR, &bar->kpe_full[stg], 0, k0, b);
+        kpe_used[stg]++;
+        if (!mbar_wait(&bar->ckv_empty[stg], eph, st, abort_flag, 62)) break;
+        mbar_arrive_expect_tx(&bar->ckv_full[stg], 8 * kLatBox);
+        for (int c = 0; c < 8; ++c) tma_load_3d(cbase + c * kLatBox, &tmC, &bar->ckv_full[stg], 64 * c, k0, b);
+        ckv_used[stg]++;
+        if (i == 0 || t == 0) {
+          // a new segment: reload q_lat once every S of the previous one is done
+          if (seg > 0 && !mbar_wait(&bar->q_free, (seg - 1) & 1, st, abort_flag, 60)) break;
+          mbar_arrive_expect_tx(&bar->q_full, 9 * kLatBox);
+          for (int c = 0; c < 9; ++c) tma_load_2d(smem + kLatQOff + c * kLatBox, &tmQ, &bar->q_full, 64 * c, b * 64);
+          ++seg;
+        }
       }
-      mbar_wait(&bar->q_full, 0, st, nullptr, 61);
-      for (int i = 0; i < 2; ++i)
-        if (issued[i]) mbar_wait(&bar->c_full[i], (issued[i] - 1) & 1, st, nullptr, 61);
+      // never leave with copies in flight (matters only after a failed wait)
+      if (seg > 0) mbar_wait(&bar->q_full, (seg - 1) & 1, st, nullptr, 64);
+      for (int sg = 0; sg < 2; ++sg) {
+        if (kpe_used[sg]) mbar_wait(&bar->kpe_full[sg], (kpe_used[sg] - 1) & 1, st, nullptr, 65);
+        if (ckv_used[sg]) mbar_wait(&bar->ckv_full[sg], (ckv_used[sg] - 1) & 1, st, nullptr, 65);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      // S issuer
       constexpr uint32_t idesc_s = idesc_bf16(64, 64, false, false);
-      constexpr uint32_t idesc_o = idesc_bf16(128, 64, true, false);
       const uint32_t q_addr = smem_u32(smem + kLatQOff);
       const uint32_t c_addr = smem_u32(smem + kLatCOff);
-      const uint32_t r_addr = smem_u32(smem + kLatROff);
-      const uint32_t p_addr = smem_u32(smem + kLatPOff);
-      bool ok = mbar_wait(&bar->q_full, 0, st, abort_flag, 62);
-      tc_fence_after();
-      // Event loop: S_j needs its latent tile and a free score buffer; P.V_j
-      // needs P_j.  Issue whichever is ready (S at most two tiles ahead), so
-      // that a P.V never waits behind the load of a later tile.
-      int next_s = 0, next_pv = 0;
-      Watchdog wd;
-      wd.reset();
-      while (ok && next_pv < n_tiles) {
-        bool progress = false;
-        if (next_s < n_tiles && next_s <= next_pv + 1) {
-          const int stg = next_s & 1;
-          const uint32_t ph = (next_s >> 1) & 1;
-          if (mbar_test(&bar->c_full[stg], ph) && mbar_test(&bar->s_free[stg], ph ^ 1)) {
-            tc_fence_after();
+      int seg = 0, t = first_t - 1;
+      for (int i = 0; i < R; ++i) {
+        if (++t == nt) t = 0;
+        const bool seg_first = i == 0 || t == 0;
+        const bool seg_last = i == R - 1 || t == nt - 1;
+        const int stg = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        if (!mbar_wait(&bar->s_free[stg], ph ^ 1, st, abort_flag, 70)) break;
+        if (seg_first && !mbar_wait(&bar->q_full, seg & 1, st, abort_flag, 71)) break;
+        if (!mbar_wait(&bar->kpe_full[stg], ph, st, abort_flag, 72)) break;
+        tc_fence_after();
+        const uint32_t cb = c_addr + stg * 9 * kLatBox;
 #pragma unroll
-            for (int kk = 0; kk < 36; ++kk) {
-              const int box = kk >> 2;
-              const uint32_t koff = (kk & 3) * 32;
-              const uint32_t bb = (box < 8 ? c_addr + (stg * 8 + box) * kLatBox : r_addr + stg * kLatBox) + koff;
-              umma_bf16(tmem + stg * 64, sdesc_sw128(q_addr + box * kLatBox + koff, 16, 1024),
-                        sdesc_sw128(bb, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(&bar->s_full[stg]);
-            ++next_s;
-            progress = true;
-          }
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(tmem + stg * 64, sdesc_sw128(q_addr + 8 * kLatBox + kk * 32, 16, 1024),
+                    sdesc_sw128(cb + 8 * kLatBox + kk * 32, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        umma_commit(&bar->kpe_empty[stg]);
+        if (!mbar_wait(&bar->ckv_full[stg], ph, st, abort_flag, 73)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 32; ++kk) {
+          const uint32_t off = (kk >> 2) * kLatBox + (kk & 3) * 32;
+          umma_bf16(tmem + stg * 64, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(cb + off, 16, 1024), idesc_s,
+                    1u);
         }
-        if (next_pv < next_s && mbar_test(&bar->p_full, next_pv & 1)) {
-          tc_fence_after();
-          const uint32_t cb = c_addr + (next_pv & 1) * 8 * kLatBox;
-#pragma unroll
-          for (int mb = 0; mb < 4; ++mb) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t adesc = sdesc_sw128(cb + 2 * mb * kLatBox + kk * 2048, kLatBox, 1024);
-              const uint64_t bdesc = sdesc_sw128(p_addr + kk * 32, 16, 1024);
-              umma_bf16(tmem + 128 + mb * 64, adesc, bdesc, idesc_o, (next_pv > 0 || kk > 0) ? 1u : 0u);
-            }
-          }
-          umma_commit(&bar->pv_done);
-          umma_commit(&bar->c_empty[next_pv & 1]);
-          ++next_pv;
-          progress = true;
-        }
-        if (progress) {
-          wd.reset();
-        } else {
-          if (wd.expired(st, abort_flag, 63)) break;
-          __nanosleep(32);
+        umma_commit(&bar->s_full[stg]);
+        if (seg_last) {
+          umma_commit(&bar->q_free);
+          ++seg;
         }
       }
-      umma_commit(&bar->drain);
-      mbar_wait(&bar->drain, 0, st, nullptr, 66);
+      umma_commit(&bar->drain_s);
+      mbar_wait(&bar->drain_s, 0, st, nullptr, 66);
+    }
+  } else if (warp == 6) {
+    if (lane == 0) {
+      // P.V issuer
+      constexpr uint32_t idesc_o = idesc_bf16(128, 64, true, false);
+      const uint32_t c_addr = smem_u32(smem + kLatCOff);
+      const uint32_t p_addr = smem_u32(smem + kLatPOff);
+      int t = first_t - 1;
+      for (int i = 0; i < R; ++i) {
+        if (++t == nt) t = 0;
+        const bool seg_first = i == 0 || t == 0;
+        const int stg = i & 1;
+        if (!mbar_wait(&bar->p_full, i & 1, st, abort_flag, 74)) break;
+        tc_fence_after();
+        const uint32_t cb = c_addr + stg * 9 * kLatBox;
+#pragma unroll
+        for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t adesc = sdesc_sw128(cb + 2 * mb * kLatBox + kk * 2048, kLatBox, 1024);
+            const uint64_t bdesc = sdesc_sw128(p_addr + kk * 32, 16, 1024);
+            umma_bf16(tmem + 128 + mb * 64, adesc, bdesc, idesc_o, (!seg_first || kk > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit(&bar->ckv_empty[stg]);
+      }
+      umma_commit(&bar->drain_pv);
+      mbar_wait(&bar->drain_pv, 0, st, nullptr, 66);
     }
   } else {
     const int quarter = warp & 3;
@@ -381,9 +428,20 @@ __global__ void __launch_bounds__(192, 1)
     // (bar.sync has no time limit); after a failed wait (ok == false) the
     // work of the remaining iterations is skipped, the barriers are not.
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int stg = j & 1;
-      ok = ok && __all_sync(0xffffffffu, mbar_wait(&bar->s_full[stg], (j >> 1) & 1, st, abort_flag, 67));
+    int b = first_seq, t = first_t - 1;
+    for (int i = 0; i < R; ++i) {
+      if (++t == nt) {
+        t = 0;
+        ++b;
+      }
+      const bool seg_first = i == 0 || t == 0;
+      const bool seg_last = i == R - 1 || t == nt - 1;
+      const int stg = i & 1;
+      if (seg_first) {
+        m = -INFINITY;
+        l = 0.f;
+      }
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&bar->s_full[stg], (i >> 1) & 1, st, abort_flag, 67));
       uint32_t s[64];
       if (ok) {
         tc_fence_after();
@@ -398,17 +456,17 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) s[c] = 0u;
       }
-      const int k0 = key_begin + j * kLatTile;
-      float mx = -INFINITY;
-      if (k0 + kLatTile > key_end) {
+      const int k0 = t * kLatTile;
+      if (k0 + kLatTile > a.L) {
 #pragma unroll
         for (int c = 0; c < 64; ++c)
-          if (k0 + c >= key_end) s[c] = __float_as_uint(-INFINITY);
+          if (k0 + c >= a.L) s[c] = __float_as_uint(-INFINITY);
       }
+      float mx;
       {
         float mp[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mp[i] = __uint_as_float(s[i]);
+        for (int c = 0; c < 8; ++c) mp[c] = __uint_as_float(s[c]);
 #pragma unroll
         for (int c = 8; c < 64; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(s[c]));
         mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
@@ -431,30 +489,32 @@ __global__ void __launch_bounds__(192, 1)
       const bool warp_need = __any_sync(0xffffffffu, need);
       if (lane == 0) bar->need[stg][quarter] = warp_need ? 1 : 0;
       named_sync_128();
-      const bool any_need = bar->need[stg][0] | bar->need[stg][1] | bar->need[stg][2] | bar->need[stg][3];
-      if (j > 0) ok = ok && __all_sync(0xffffffffu, mbar_wait(&bar->pv_done, (j - 1) & 1, st, abort_flag, 68));
-      if (!ok) continue;
-      if (j > 0) {
+      // O^T is rescaled only between two P.V of the same segment
+      const bool any_need =
+          !seg_first && (bar->need[stg][0] | bar->need[stg][1] | bar->need[stg][2] | bar->need[stg][3]);
+      // P.V of the previous tile must be done: it reads the P buffer and writes O^T
+      if (i > 0)
+        ok = ok && __all_sync(0xffffffffu,
+                              mbar_wait(&bar->ckv_empty[(i - 1) & 1], ((i - 1) >> 1) & 1, st, abort_flag, 68));
+      if (ok && any_need) {
         tc_fence_after();
-        if (any_need) {
 #pragma unroll 1
-          for (int mb = 0; mb < 4; ++mb) {
+        for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-              uint32_t r[32];
-              const uint32_t ta = tmem + lane_addr + 128 + mb * 64 + half * 32;
-              tmem_ld32(ta, r);
-              tmem_wait_ld();
+          for (int half = 0; half < 2; ++half) {
+            uint32_t r[32];
+            const uint32_t ta = tmem + lane_addr + 128 + mb * 64 + half * 32;
+            tmem_ld32(ta, r);
+            tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                r[i] = __float_as_uint(__uint_as_float(r[i]) * bar->alpha[stg][half * 32 + i]);
-              tmem_st32(ta, r);
-            }
+            for (int c = 0; c < 32; ++c)
+              r[c] = __float_as_uint(__uint_as_float(r[c]) * bar->alpha[stg][half * 32 + c]);
+            tmem_st32(ta, r);
           }
-          tmem_wait_st();
         }
+        tmem_wait_st();
       }
-      if (valid) {
+      if (ok && valid) {
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
           const int k = c8 * 8;
@@ -468,40 +528,47 @@ __global__ void __launch_bounds__(192, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bar->p_full);
-    }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar->pv_done, (n_tiles - 1) & 1, st, abort_flag, 69));
-    if (valid) {
-      bar->m[h] = m;
-      bar->l[h] = l;
-    }
-    named_sync_128();
-    if (ok) {
-      tc_fence_after();
-      const size_t prow = (size_t)b * a.splits + split;
+      if (!seg_last) continue;
+
+      // end of a segment: O^T complete after this tile's P.V
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&bar->ckv_empty[stg], (i >> 1) & 1, st, abort_flag, 69));
+      if (valid) {
+        bar->m[h] = m;
+        bar->l[h] = l;
+      }
+      named_sync_128();
+      const bool whole = t == nt - 1 && i >= t;  // the sequence's tile 0 is in this CTA too
+      const int slot = (b == first_seq) ? 2 * g : 2 * g + 1;
+      if (ok) {
+        tc_fence_after();
 #pragma unroll 1
-      for (int mb = 0; mb < 4; ++mb) {
-        const int latent = mb * 128 + quarter * 32 + lane;
+        for (int mb = 0; mb < 4; ++mb) {
+          const int latent = mb * 128 + quarter * 32 + lane;
 #pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_addr + 128 + mb * 64 + half * 32, r);
-          tmem_wait_ld();
-          if (a.splits == 1) {
+          for (int half = 0; half < 2; ++half) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_addr + 128 + mb * 64 + half * 32, r);
+            tmem_wait_ld();
+            if (whole) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int hh = half * 32 + i;
-              a.olat[((size_t)b * 64 + hh) * 512 + latent] = __float2bfloat16_rn(__uint_as_float(r[i]) / bar->l[hh]);
-            }
-          } else {
+              for (int c = 0; c < 32; ++c) {
+                const int hh = half * 32 + c;
+                a.olat[((size_t)b * 64 + hh) * 512 + latent] =
+                    __float2bfloat16_rn(__uint_as_float(r[c]) / bar->l[hh]);
+              }
+            } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int hh = half * 32 + i;
-              a.part_o[(prow * 64 + hh) * 512 + latent] = __uint_as_float(r[i]);
+              for (int c = 0; c < 32; ++c) {
+                const int hh = half * 32 + c;
+                a.part_o[((size_t)slot * 64 + hh) * 512 + latent] = __uint_as_float(r[c]);
+              }
             }
           }
         }
+        if (!whole && tid < 64) a.part_ml[(size_t)slot * 64 + tid] = make_float2(bar->m[tid], bar->l[tid]);
       }
-      if (a.splits > 1 && tid < 64) a.part_ml[prow * 64 + tid] = make_float2(bar->m[tid], bar->l[tid]);
+      tc_fence_before();
+      named_sync_128();  // m/l are rewritten by the next segment's end
     }
   }
 
@@ -513,25 +580,32 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-// latent partials are laid out [(b*splits + s), 64, 512]; the generic combine
-// expects [(row*splits + s), width] with row = (b, h): regroup here.
+// Merge the partials of the sequences cut between CTAs (the others were
+// written by latent_attn_tc directly).  Block = (head, sequence).
 __global__ void latent_combine_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
-                                      __nv_bfloat16* __restrict__ out, int splits) {
+                                      __nv_bfloat16* __restrict__ out, int L, int B, int G) {
   pdl_launch_dependents();
   pdl_wait();
   const int h = blockIdx.x, b = blockIdx.y;
+  const int nt = (L + kLatTile - 1) / kLatTile;
+  const long long total = (long long)B * nt;
+  // CTA holding flattened tile x: the largest g with start(g) <= x
+  auto owner = [&](long long xx) { return (int)(((xx + 1) * G - 1) / total); };
+  const int g0 = owner((long long)b * nt), g1 = owner((long long)b * nt + nt - 1);
+  if (g0 == g1) return;  // whole sequence in one CTA: written directly
+  auto slot = [&](int gg) { return (b == (int)(lat_range_start(gg, total, G) / nt)) ? 2 * gg : 2 * gg + 1; };
   float mx = -INFINITY;
-  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, part_ml[((size_t)b * splits + s) * 64 + h].x);
+  for (int gg = g0; gg <= g1; ++gg) mx = fmaxf(mx, part_ml[(size_t)slot(gg) * 64 + h].x);
   float den = 0.f;
-  for (int s = 0; s < splits; ++s) {
-    const float2 ml = part_ml[((size_t)b * splits + s) * 64 + h];
+  for (int gg = g0; gg <= g1; ++gg) {
+    const float2 ml = part_ml[(size_t)slot(gg) * 64 + h];
     den += exp2f(ml.x - mx) * ml.y;
   }
   const float inv = 1.f / den;
   for (int d = threadIdx.x; d < 512; d += blockDim.x) {
     float acc = 0.f;
-    for (int s = 0; s < splits; ++s) {
-      const size_t pi = ((size_t)b * splits + s) * 64 + h;
+    for (int gg = g0; gg <= g1; ++gg) {
+      const size_t pi = (size_t)slot(gg) * 64 + h;
       acc += exp2f(part_ml[pi].x - mx) * part_o[pi * 512 + d];
     }
     out[((size_t)b * 64 + h) * 512 + d] = __float2bfloat16_rn(acc * inv);
@@ -580,15 +654,13 @@ cudaError_t launch_decode_attention(const DecodeAttnArgs& a, const DevStatusHost
   return e;
 }
 
-int latent_splits(int B, int L, int num_sms) {
-  // one wave of CTAs: about one (sequence, split) per SM; the split partials
-  // cost 128 KB per (sequence, split), so large batches use few splits
-  int s = (num_sms + B / 2) / B;
-  const int max_s = (L + 255) / 256;
-  if (s > max_s) s = max_s;
-  if (s < 1) s = 1;
-  const int cl = chunk_len_for(L, s, kLatTile);
-  return (L + cl - 1) / cl;
+int latent_ctas(int B, int L, int num_sms) {
+  // one CTA per SM (persistent over its range of tiles), at least two tiles each
+  const long long total = (long long)B * ((L + kLatTile - 1) / kLatTile);
+  long long g = total / 2;
+  if (g > num_sms) g = num_sms;
+  if (g < 1) g = 1;
+  return (int)g;
 }
 
 cudaError_t launch_latent_attention(const LatentAttnArgs& a, const DevStatusHost& st, cudaStream_t stream,
@@ -605,15 +677,13 @@ cudaError_t launch_latent_attention(const LatentAttnArgs& a, const DevStatusHost
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int cl = chunk_len_for(a.L, a.splits, kLatTile);
   DevStatus dst{st.word, st.wait_limit_ns};
-  dim3 grid(a.splits, a.B);
-  cudaError_t e = launch_pdl(latent_attn_tc, grid, dim3(192), kLatSmemBytes, stream, tq, tc, tr, a, dst, cl);
+  cudaError_t e = launch_pdl(latent_attn_tc, dim3(a.ctas), dim3(kLatThreads), kLatSmemBytes, stream, tq, tc, tr, a, dst);
   if (e != cudaSuccess) return e;
   ++*launches;
-  if (a.splits > 1) {
+  if (a.ctas > 1) {
     e = launch_pdl(latent_combine_kernel, dim3(64, a.B), dim3(128), 0, stream, (const float*)a.part_o,
-                   (const float2*)a.part_ml, a.olat, a.splits);
+                   (const float2*)a.part_ml, a.olat, a.L, a.B, a.ctas);
     ++*launches;
   }
   return e;

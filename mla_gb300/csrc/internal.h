@@ -181,12 +181,12 @@ struct LatentAttnArgs {
   const __nv_bfloat16* ckv;   // [B, cap, 512]
   const __nv_bfloat16* kpe;   // [B, cap, 64]
   __nv_bfloat16* olat;        // [B, 64, 512]
-  float* part_o;              // [B*splits, 64, 512]
-  float2* part_ml;            // [B*splits, 64]
-  int B, L, cap, splits;
+  float* part_o;              // [2*ctas, 64, 512]: two partial slots per CTA
+  float2* part_ml;            // [2*ctas, 64]
+  int B, L, cap, ctas;        // ctas = latent_ctas(B, L, SMs)
   float scale;
 };
-int latent_splits(int B, int L, int num_sms);
+int latent_ctas(int B, int L, int num_sms);
 cudaError_t launch_latent_attention(const LatentAttnArgs& a, const DevStatusHost& st, cudaStream_t stream,
                                     int* launches);
 

@@ -140,6 +140,30 @@ def test_decode_latent_parity(W, B, P):
     parity_cache(cuda_to_f64(kpe[:, P]), ref["kpe_new"], "new rotary-key row")
 
 
+def test_decode_latent_many_sequences(W):
+    """B=500, P=70 (two 64-key tiles per sequence): each CTA's range of tiles
+    covers the end of one sequence, whole sequences and the start of another,
+    so the direct writes and the merged partials are both exercised.  The
+    caches hold seeded bf16 values; the oracle runs on sampled sequences."""
+    import torch
+    B, P = 500, 70
+    cap = P + 1
+    Cb = synth.tensor_bits(0, "cache_x", (B, cap, 512), (0.0, 1.0))
+    Rb = synth.tensor_bits(1, "cache_x", (B, cap, 64), (0.0, 1.7))
+    xb = synth.tensor_bits(0, "new_x", (B, 7168), synth.X_DIST)
+    x = bits_to_cuda(xb)
+    ckv, kpe = bits_to_cuda(Cb), bits_to_cuda(Rb)
+    out = torch.empty_like(x)
+    wsp = m.alloc_workspace(m.MODE_DECODE_LATENT, B, P)
+    m.mla_decode_latent(W[1], x, P, ckv, kpe, out, wsp)
+    torch.cuda.synchronize()
+    assert m.mla_device_status(wsp) == 0
+    f = synth.bf16_bits_to_f64
+    for b in [0, 1, 2, 3, 4, 131, 132, 133, 250, 251, 497, 498, 499]:
+        ref = om.decode_latent(W[2], f(xb[b:b + 1]), f(Cb[b:b + 1, :P]), f(Rb[b:b + 1, :P]))
+        parity(cuda_to_f64(out[b:b + 1]), ref["out"], f"out b={b}")
+
+
 def test_prefill_then_decode_chain(W):
     """GPU prefill of T-1 tokens fills the caches; GPU decode of token T-1
     must match the oracle's prefill row T-1 (both cache forms)."""
