@@ -581,35 +581,64 @@ __global__ void __launch_bounds__(kLatThreads, 1)
 }
 
 // Merge the partials of the sequences cut between CTAs (the others were
-// written by latent_attn_tc directly).  Block = (head, sequence).
-__global__ void latent_combine_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
-                                      __nv_bfloat16* __restrict__ out, int L, int B, int G) {
+// written by latent_attn_tc directly).  Block = (head, sequence), 128 threads,
+// four latent columns per thread.
+constexpr int kLatMaxCtas = 1024;
+
+__global__ void __launch_bounds__(128) latent_combine_kernel(const float* __restrict__ part_o,
+                                                             const float2* __restrict__ part_ml,
+                                                             __nv_bfloat16* __restrict__ out, int L, int B, int G) {
+  __shared__ int s_slot[kLatMaxCtas];
+  __shared__ float s_w[kLatMaxCtas];
+  __shared__ float s_red[2][4];
   pdl_launch_dependents();
   pdl_wait();
   const int h = blockIdx.x, b = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nt = (L + kLatTile - 1) / kLatTile;
   const long long total = (long long)B * nt;
   // CTA holding flattened tile x: the largest g with start(g) <= x
-  auto owner = [&](long long xx) { return (int)(((xx + 1) * G - 1) / total); };
-  const int g0 = owner((long long)b * nt), g1 = owner((long long)b * nt + nt - 1);
+  const long long xa = (long long)b * nt, xb = xa + nt - 1;  // the sequence's first and last tile
+  const int g0 = (int)(((xa + 1) * G - 1) / total);
+  const int g1 = (int)(((xb + 1) * G - 1) / total);
   if (g0 == g1) return;  // whole sequence in one CTA: written directly
-  auto slot = [&](int gg) { return (b == (int)(lat_range_start(gg, total, G) / nt)) ? 2 * gg : 2 * gg + 1; };
-  float mx = -INFINITY;
-  for (int gg = g0; gg <= g1; ++gg) mx = fmaxf(mx, part_ml[(size_t)slot(gg) * 64 + h].x);
-  float den = 0.f;
-  for (int gg = g0; gg <= g1; ++gg) {
-    const float2 ml = part_ml[(size_t)slot(gg) * 64 + h];
-    den += exp2f(ml.x - mx) * ml.y;
+  const int n = g1 - g0 + 1;
+  float mloc = -INFINITY;
+  for (int k = tid; k < n; k += 128) {
+    const int gg = g0 + k;
+    const int slot = (b == (int)(lat_range_start(gg, total, G) / nt)) ? 2 * gg : 2 * gg + 1;
+    const float2 ml = part_ml[(size_t)slot * 64 + h];
+    s_slot[k] = slot;
+    s_w[k] = ml.x;
+    mloc = fmaxf(mloc, ml.x);
   }
-  const float inv = 1.f / den;
-  for (int d = threadIdx.x; d < 512; d += blockDim.x) {
-    float acc = 0.f;
-    for (int gg = g0; gg <= g1; ++gg) {
-      const size_t pi = (size_t)slot(gg) * 64 + h;
-      acc += exp2f(part_ml[pi].x - mx) * part_o[pi * 512 + d];
-    }
-    out[((size_t)b * 64 + h) * 512 + d] = __float2bfloat16_rn(acc * inv);
+  mloc = warp_max(mloc);
+  if (lane == 0) s_red[0][warp] = mloc;
+  __syncthreads();
+  const float mx = fmaxf(fmaxf(s_red[0][0], s_red[0][1]), fmaxf(s_red[0][2], s_red[0][3]));
+  float dloc = 0.f;
+  for (int k = tid; k < n; k += 128) {
+    const float w = exp2f(s_w[k] - mx);
+    dloc += w * part_ml[(size_t)s_slot[k] * 64 + h].y;
+    s_w[k] = w;
   }
+  dloc = warp_sum(dloc);
+  if (lane == 0) s_red[1][warp] = dloc;
+  __syncthreads();
+  const float inv = 1.f / ((s_red[1][0] + s_red[1][1]) + (s_red[1][2] + s_red[1][3]));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < n; ++k) {
+    const float w = s_w[k];
+    const float4 v = *reinterpret_cast<const float4*>(part_o + ((size_t)s_slot[k] * 64 + h) * 512 + tid * 4);
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
+  }
+  uint2 o;
+  o.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  o.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(out + ((size_t)b * 64 + h) * 512 + tid * 4) = o;
 }
 
 int chunk_len_for(int L, int splits, int granule) {
@@ -659,6 +688,7 @@ int latent_ctas(int B, int L, int num_sms) {
   const long long total = (long long)B * ((L + kLatTile - 1) / kLatTile);
   long long g = total / 2;
   if (g > num_sms) g = num_sms;
+  if (g > kLatMaxCtas) g = kLatMaxCtas;  // the combine's per-sequence tables
   if (g < 1) g = 1;
   return (int)g;
 }

@@ -37,17 +37,20 @@ __global__ void __launch_bounds__(128) rmsnorm_7168_kernel(const __nv_bfloat16* 
       ss += f.x * f.x + f.y * f.y;
     }
   }
+  const uint4* gr = reinterpret_cast<const uint4*>(g);
+  uint4 gvs[kVec];  // gains fetched before the reduction (its latency overlaps the loads')
+#pragma unroll
+  for (int j = 0; j < kVec; ++j) gvs[j] = gr[threadIdx.x + j * 128];
   __shared__ float red[4];
   ss = warp_sum(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
   const float tot = red[0] + red[1] + red[2] + red[3];
   const float rstd = rsqrtf(tot * (1.0f / 7168.0f) + eps);
-  const uint4* gr = reinterpret_cast<const uint4*>(g);
   uint4* yr = reinterpret_cast<uint4*>(y + row * 7168);
 #pragma unroll
   for (int j = 0; j < kVec; ++j) {
-    const uint4 gv = gr[threadIdx.x + j * 128];
+    const uint4 gv = gvs[j];
     const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
     const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
     uint32_t o[4];
@@ -61,74 +64,81 @@ __global__ void __launch_bounds__(128) rmsnorm_7168_kernel(const __nv_bfloat16* 
   }
 }
 
-// One warp per row of ca [rows, 2112] (float32) = [c^Q 1536 | c^KV 512 | k^pe 64].
-__device__ __forceinline__ void norm_store(const float4* src, int n4, const __nv_bfloat16* g, float eps,
-                                           __nv_bfloat16* dst, __nv_bfloat16* dst2, int lane) {
-  // n4 float4 per lane (n4 * 4 * 32 values in the row)
-  float4 v[12];
-  float ss = 0.f;
-#pragma unroll
-  for (int j = 0; j < 12; ++j) {
-    if (j < n4) {
-      v[j] = src[lane + 32 * j];
-      ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
-    }
-  }
-  const float rstd = rsqrtf(warp_sum(ss) / (float)(n4 * 128) + eps);
-  const uint2* gp = reinterpret_cast<const uint2*>(g);
-  uint2* dp = reinterpret_cast<uint2*>(dst);
-  uint2* dp2 = reinterpret_cast<uint2*>(dst2);
-#pragma unroll
-  for (int j = 0; j < 12; ++j) {
-    if (j < n4) {
-      const uint2 gv = gp[lane + 32 * j];
-      const float2 g0 = unpack_bf16x2(gv.x), g1 = unpack_bf16x2(gv.y);
-      const uint2 o = make_uint2(pack_bf16x2(g0.x * (v[j].x * rstd), g0.y * (v[j].y * rstd)),
-                                 pack_bf16x2(g1.x * (v[j].z * rstd), g1.y * (v[j].w * rstd)));
-      dp[lane + 32 * j] = o;
-      if (dst2) dp2[lane + 32 * j] = o;
-    }
-  }
+// One CTA of 128 threads per row of ca [rows, 2112] (float32) =
+// [c^Q 1536 | c^KV 512 | k^pe 64]; every load (row and gains) is issued
+// before the two reductions.
+__device__ __forceinline__ uint2 scale_pack4(const float4 v, const uint2 gv, float rstd) {
+  const float2 g0 = unpack_bf16x2(gv.x), g1 = unpack_bf16x2(gv.y);
+  return make_uint2(pack_bf16x2(g0.x * (v.x * rstd), g0.y * (v.y * rstd)),
+                    pack_bf16x2(g1.x * (v.z * rstd), g1.y * (v.w * rstd)));
 }
 
-__global__ void __launch_bounds__(256) latent_split_kernel(const LatentArgs a) {
+__global__ void __launch_bounds__(128) latent_split_kernel(const LatentArgs a) {
   pdl_launch_dependents();
   pdl_wait();
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (warp >= a.rows) return;
-  const size_t row = warp;
-  const float* src = a.ca + row * 2112;
-  const int b = (int)(row / a.t_mod);
-  const int t = a.t_off + (int)(row % a.t_mod);
-  // c^Q-hat = RMSNorm(c^Q): 1536 values = 12 float4 per lane
-  norm_store(reinterpret_cast<const float4*>(src), 12, a.g_qa, a.eps, a.cq + row * 1536, nullptr, lane);
-  // c^KV-hat = RMSNorm(c^KV): 512 values = 4 float4 per lane; also the latent cache row
-  __nv_bfloat16* dcache = a.ckv_cache ? a.ckv_cache + ((size_t)b * a.cap + t) * 512 : nullptr;
-  norm_store(reinterpret_cast<const float4*>(src + 1536), 4, a.g_kva, a.eps, a.ckv + row * 512, dcache, lane);
-  // R_t: angle (pos0 + t) * theta_i formed and reduced modulo 2 pi in double
-  // precision (Cody-Waite style, 2 pi split in two doubles), then a float
-  // sincos of the reduced angle
-  const int tm = (int)(row % a.t_mod);
-  const double ang = (double)(a.pos0 + tm) * a.inv_freq[lane];
-  const double kq = rint(ang * 0.15915494309189535);  // 1 / (2 pi)
-  const double red = fma(-kq, 6.283185307179586, ang) - kq * 2.4492935982947064e-16;
-  float sn, cn;
-  sincosf((float)red, &sn, &cn);
-  const float2 cs = make_float2(cn, sn);
-  if (b == 0) a.cs[(size_t)tm * 32 + lane] = cs;
-  // k^R = RoPE(k^pe, t): lane i rotates pair (i, i + 32); k^pe is not normalised
-  const float x1 = src[2048 + lane];
-  const float x2 = src[2048 + 32 + lane];
-  const __nv_bfloat16 y1 = __float2bfloat16_rn(x1 * cs.x - x2 * cs.y);
-  const __nv_bfloat16 y2 = __float2bfloat16_rn(x2 * cs.x + x1 * cs.y);
-  __nv_bfloat16* d = a.kpe + row * 64;
-  d[lane] = y1;
-  d[lane + 32] = y2;
-  if (a.kpe_cache) {
-    __nv_bfloat16* dc = a.kpe_cache + ((size_t)b * a.cap + t) * 64;
-    dc[lane] = y1;
-    dc[lane + 32] = y2;
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float* src = a.ca + (size_t)row * 2112;
+  const float4* src4 = reinterpret_cast<const float4*>(src);
+  float4 q[3];
+#pragma unroll
+  for (int j = 0; j < 3; ++j) q[j] = src4[tid + 128 * j];  // c^Q: 384 float4
+  const float4 kv = src4[384 + tid];                       // c^KV: 128 float4
+  float x1 = 0.f, x2 = 0.f;
+  if (tid < 32) {  // k^pe pair (tid, tid + 32)
+    x1 = src[2048 + tid];
+    x2 = src[2048 + 32 + tid];
+  }
+  uint2 gq[3];
+#pragma unroll
+  for (int j = 0; j < 3; ++j) gq[j] = reinterpret_cast<const uint2*>(a.g_qa)[tid + 128 * j];
+  const uint2 gk = reinterpret_cast<const uint2*>(a.g_kva)[tid];
+  float ssq = 0.f;
+#pragma unroll
+  for (int j = 0; j < 3; ++j) ssq += q[j].x * q[j].x + q[j].y * q[j].y + q[j].z * q[j].z + q[j].w * q[j].w;
+  float ssk = kv.x * kv.x + kv.y * kv.y + kv.z * kv.z + kv.w * kv.w;
+  __shared__ float red[2][4];
+  ssq = warp_sum(ssq);
+  ssk = warp_sum(ssk);
+  if (lane == 0) {
+    red[0][warp] = ssq;
+    red[1][warp] = ssk;
+  }
+  __syncthreads();
+  const int b = row / a.t_mod;
+  const int tm = row - b * a.t_mod;
+  const int t = a.t_off + tm;
+  // c^Q-hat = RMSNorm(c^Q); c^KV-hat = RMSNorm(c^KV) (also the latent cache row)
+  const float rq = rsqrtf(((red[0][0] + red[0][1]) + (red[0][2] + red[0][3])) * (1.0f / 1536.0f) + a.eps);
+  const float rk = rsqrtf(((red[1][0] + red[1][1]) + (red[1][2] + red[1][3])) * (1.0f / 512.0f) + a.eps);
+  uint2* dq = reinterpret_cast<uint2*>(a.cq + (size_t)row * 1536);
+#pragma unroll
+  for (int j = 0; j < 3; ++j) dq[tid + 128 * j] = scale_pack4(q[j], gq[j], rq);
+  const uint2 ok = scale_pack4(kv, gk, rk);
+  reinterpret_cast<uint2*>(a.ckv + (size_t)row * 512)[tid] = ok;
+  if (a.ckv_cache) reinterpret_cast<uint2*>(a.ckv_cache + ((size_t)b * a.cap + t) * 512)[tid] = ok;
+  if (tid < 32) {
+    // R_t: angle (pos0 + t) * theta_i formed and reduced modulo 2 pi in double
+    // precision (Cody-Waite style, 2 pi split in two doubles), then a float
+    // sincos of the reduced angle
+    const double ang = (double)(a.pos0 + tm) * a.inv_freq[lane];
+    const double kq = rint(ang * 0.15915494309189535);  // 1 / (2 pi)
+    const double red2 = fma(-kq, 6.283185307179586, ang) - kq * 2.4492935982947064e-16;
+    float sn, cn;
+    sincosf((float)red2, &sn, &cn);
+    const float2 cs = make_float2(cn, sn);
+    if (b == 0) a.cs[(size_t)tm * 32 + lane] = cs;
+    // k^R = RoPE(k^pe, t): lane i rotates pair (i, i + 32); k^pe is not normalised
+    const __nv_bfloat16 y1 = __float2bfloat16_rn(x1 * cs.x - x2 * cs.y);
+    const __nv_bfloat16 y2 = __float2bfloat16_rn(x2 * cs.x + x1 * cs.y);
+    __nv_bfloat16* d = a.kpe + (size_t)row * 64;
+    d[lane] = y1;
+    d[lane + 32] = y2;
+    if (a.kpe_cache) {
+      __nv_bfloat16* dc = a.kpe_cache + ((size_t)b * a.cap + t) * 64;
+      dc[lane] = y1;
+      dc[lane + 32] = y2;
+    }
   }
 }
 
@@ -154,9 +164,7 @@ cudaError_t launch_rmsnorm_rows(const __nv_bfloat16* x, const __nv_bfloat16* g, 
 }
 
 cudaError_t launch_latent_split(const LatentArgs& a, cudaStream_t stream) {
-  const int warps_per_block = 8;
-  return launch_pdl(latent_split_kernel, dim3((a.rows + warps_per_block - 1) / warps_per_block),
-                    dim3(32 * warps_per_block), 0, stream, a);
+  return launch_pdl(latent_split_kernel, dim3(a.rows), dim3(128), 0, stream, a);
 }
 
 cudaError_t launch_copy_qpe(const __nv_bfloat16* q, __nv_bfloat16* qlat, int B, cudaStream_t stream) {
