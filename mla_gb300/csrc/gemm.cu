@@ -785,12 +785,13 @@ cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, con
       if (tiny && k256) return launch_impl<64, 64, 3, Epi::kStoreF32, false, 4>(s, op, ea, st, num_sms, stream);
       if (small && k256) return launch_impl<128, 64, 4, Epi::kStoreF32, false, 2>(s, op, ea, st, num_sms, stream);
       if (small) return launch_impl<128, 64, 8, Epi::kStoreF32, false>(s, op, ea, st, num_sms, stream);
-      // Few row blocks: 128-wide tiles (2112 = 16.5 x 128: 17 column tiles, the
-      // last one half empty and clipped on store) give more tiles per wave;
-      // many row blocks: 192-wide tiles read A fewer times.
-      if (((s.M + kBM - 1) / kBM) * 11 < 4 * num_sms)
-        return launch_impl<128, 128, 6, Epi::kStoreF32, false, 1, true>(s, op, ea, st, num_sms, stream);
-      return launch_impl<128, 192, 4, Epi::kStoreF32, false, 1, true>(s, op, ea, st, num_sms, stream);
+      // 256-wide tiles (2112 = 8.25 x 256: 9 column tiles, the last one
+      // clipped on store; the c^Q / c^KV split at 1536 is tile-aligned) read
+      // the fewest operand bytes from L2 per MMA, and 16 row blocks make 144
+      // tiles, one wave; 128-wide tiles when there are too few tiles for a wave.
+      if (s.n_split % 256 == 0 && ((s.M + kBM - 1) / kBM) * 9 >= num_sms / 2)
+        return launch_impl<128, 256, 4, Epi::kStoreF32, false, 1, true>(s, op, ea, st, num_sms, stream);
+      return launch_impl<128, 128, 6, Epi::kStoreF32, false, 1, true>(s, op, ea, st, num_sms, stream);
     case Epi::kStoreBf16:
     default:
       if (op.b_mn_major) {
