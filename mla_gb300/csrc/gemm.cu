@@ -39,10 +39,10 @@ __host__ __device__ constexpr uint32_t pow2_cols(uint32_t n) {
 
 // One pipeline stage holds KSUB consecutive 64-wide K blocks of A and of B,
 // so that each weight row is fetched in runs of KSUB * 128 bytes.
-template <int BM, int BN, int STAGES, int KSUB, bool TMA_ST = false>
+template <int BM, int BN, int STAGES, int KSUB, bool TMA_ST = false, bool PAIR = false>
 struct GemmSmem {
   static constexpr uint32_t kA1 = BM * kBK * 2;  // one 64-wide K block of A
-  static constexpr uint32_t kB1 = BN * kBK * 2;
+  static constexpr uint32_t kB1 = (PAIR ? BN / 2 : BN) * kBK * 2;  // CTA pair: half of the B rows each
   static constexpr uint32_t kA = KSUB * kA1;
   static constexpr uint32_t kB = KSUB * kB1;
   static constexpr uint32_t kStage = kA + kB;
@@ -293,46 +293,50 @@ __device__ __forceinline__ void stage_f32(uint8_t* buf, int lane, const uint32_t
         make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
 }
 
-template <int BN, Epi EPI, class Src>
-__device__ __forceinline__ void run_epilogue_tma(const EpiArgs& ea, const Src& ld, StoreStage& ss,
+template <int BN, Epi EPI>
+__device__ __forceinline__ void run_epilogue_tma(const EpiArgs& ea, const TmemSrc& src, StoreStage& ss,
                                                  const CUtensorMap* m0, const CUtensorMap* m1, int batch,
                                                  int row0, int row, int n0, bool row_ok, int lane, int M) {
+  const uint32_t taddr = src.taddr;
   if constexpr (EPI == Epi::kStoreF32) {
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t r[32];
-      ld(c, r);
+    tmem_chunk_loop(taddr, 0, BN, [&](int c, uint32_t (&r)[32]) {
       uint8_t* buf = ss.next(lane);
       stage_f32(buf, lane, r);
       ss.issue2(m0, buf, n0 + c, row0, lane);
-    }
+    });
   } else if constexpr (EPI == Epi::kStoreBf16) {
     const int col0 = ea.c_col0 + batch * ea.c_col_step + n0;
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t r[32];
-      ld(c, r);
+    tmem_chunk_loop(taddr, 0, BN, [&](int c, uint32_t (&r)[32]) {
       uint8_t* buf = ss.next(lane);
       stage_bf16(buf, lane, r);
       ss.issue2(m0, buf, col0 + c, row0, lane);
-    }
+    });
   } else if constexpr (EPI == Epi::kQRope) {
     static_assert(BN == 192 || BN == 96, "q_b epilogue works on whole or half heads");
     const int o0 = n0 % 192;
     const int nope_cols = (o0 + BN < 128 ? o0 + BN : 128) - o0;
-#pragma unroll 1
-    for (int c = 0; c < nope_cols; c += 32) {
-      uint32_t r[32];
-      ld(c, r);
+    // the RoPE table row of this token, fetched while the "nope" chunks are stored
+    float2 cs[32];
+    const bool has_pe = o0 + BN == 192;
+    if (has_pe) {
+      const float4* csr = reinterpret_cast<const float4*>(ea.cs + (size_t)(row % ea.t_mod) * 32);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float4 v = csr[i];
+        cs[2 * i] = make_float2(v.x, v.y);
+        cs[2 * i + 1] = make_float2(v.z, v.w);
+      }
+    }
+    tmem_chunk_loop(taddr, 0, nope_cols, [&](int c, uint32_t (&r)[32]) {
       uint8_t* buf = ss.next(lane);
       stage_bf16(buf, lane, r);
       ss.issue2(m0, buf, n0 + c, row0, lane);
-    }
-    if (o0 + BN == 192) {
+    });
+    if (has_pe) {
       uint32_t x1[32], x2[32];
-      ld(nope_cols, x1);
-      ld(nope_cols + 32, x2);
-      const float2* cs = ea.cs + (size_t)(row % ea.t_mod) * 32;
+      tmem_ld32(taddr + nope_cols, x1);
+      tmem_ld32(taddr + nope_cols + 32, x2);
+      tmem_wait_ld();
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const float2 t = cs[i];
@@ -361,22 +365,20 @@ __device__ __forceinline__ void run_epilogue_tma(const EpiArgs& ea, const Src& l
     // that its latency overlaps the accumulator chunks
     uint4 kv4[8];
     if (o0 == 0) {
-      const uint4* src = reinterpret_cast<const uint4*>(ea.kpe + (size_t)row * 64);
+      const uint4* kp = reinterpret_cast<const uint4*>(ea.kpe + (size_t)row * 64);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) kv4[j] = row_ok ? src[j] : make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < 8; ++j) kv4[j] = row_ok ? kp[j] : make_uint4(0, 0, 0, 0);
     }
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t r[32];
-      ld(c, r);
-      if (!warp_ok) continue;
-      const int col = o0 + c;
-      uint8_t* buf = ss.next(lane);
-      stage_bf16(buf, lane, r);
-      if (col < 128)
-        ss.issue3(m0, buf, col, t0, plane, lane);
-      else
-        ss.issue3(m1, buf, col - 128, t0, plane, lane);
+    if (warp_ok) {
+      tmem_chunk_loop(taddr, 0, BN, [&](int c, uint32_t (&r)[32]) {
+        const int col = o0 + c;
+        uint8_t* buf = ss.next(lane);
+        stage_bf16(buf, lane, r);
+        if (col < 128)
+          ss.issue3(m0, buf, col, t0, plane, lane);
+        else
+          ss.issue3(m1, buf, col - 128, t0, plane, lane);
+      });
     }
     if (warp_ok && o0 == 0) {
 #pragma unroll
@@ -389,10 +391,7 @@ __device__ __forceinline__ void run_epilogue_tma(const EpiArgs& ea, const Src& l
     }
   } else {  // kResidual
     const size_t base = (size_t)row * ea.ldo + n0;
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t r[32];
-      ld(c, r);
+    tmem_chunk_loop(taddr, 0, BN, [&](int c, uint32_t (&r)[32]) {
       if (row_ok && ea.delta) {
         float4* dd = reinterpret_cast<float4*>(ea.delta + base + c);
 #pragma unroll
@@ -417,7 +416,7 @@ __device__ __forceinline__ void run_epilogue_tma(const EpiArgs& ea, const Src& l
       uint8_t* buf = ss.next(lane);
       stage_bf16(buf, lane, r);
       ss.issue2(m0, buf, n0 + c, row0, lane);
-    }
+    });
   }
 }
 
@@ -440,14 +439,15 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
 
 // BM = 128: accumulator row r in TMEM lane r.  BM = 64 (few rows, decode):
 // row r in lane 32*(r/16) + r%16, so each epilogue warp holds 16 rows.
-template <int BM, int BN, int STAGES, int KSUB, Epi EPI, bool B_MN, bool TMA_ST>
+template <int BM, int BN, int STAGES, int KSUB, Epi EPI, bool B_MN, bool TMA_ST, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                 const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO0,
                 const __grid_constant__ CUtensorMap tmO1, const GemmShape s, const EpiArgs ea,
                 const DevStatus st) {
   static_assert(!TMA_ST || BM == 128, "TMA-store epilogue needs 32 rows per warp");
-  using L = GemmSmem<BM, BN, STAGES, KSUB, TMA_ST>;
+  static_assert(!PAIR || (!B_MN && KSUB == 1 && BM == 128), "pair mode: K-major B, one K block per stage");
+  using L = GemmSmem<BM, BN, STAGES, KSUB, TMA_ST, PAIR>;
   constexpr uint32_t kTmemCols = pow2_cols(2 * BN);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -463,10 +463,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int m_tiles = (s.M + BM - 1) / BM;
   const int n_tiles = TMA_ST ? (s.N + BN - 1) / BN : s.N / BN;  // TMA stores clip columns >= N
-  const int num_tiles = s.batches * m_tiles * n_tiles;
+  // Pair mode (cta_group::2): the two CTAs of a cluster compute one 256-row
+  // tile, row blocks 2p (even CTA) and 2p + 1 (odd CTA) of one column block;
+  // each stages its own 128 rows of A and half of the B rows, so every SM
+  // reads half of B from shared memory per MMA.  The even CTA issues the
+  // MMAs; both run the epilogue of their own rows (the host guarantees an
+  // even m_tiles).
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0;
+  const bool leader = crank == 0;
+  const int m_units = PAIR ? m_tiles / 2 : m_tiles;
+  const int num_tiles = s.batches * m_units * n_tiles;
   const int kblocks = s.K / (kBK * KSUB);  // stages of KSUB K blocks
   const int ksplit = s.ksplit;
   const int num_units = num_tiles * ksplit;
+  const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int ustep = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -475,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull_bar[i], 1);
-      mbar_init(&tempty_bar[i], 128);
+      mbar_init(&tempty_bar[i], PAIR ? 256 : 128);  // pair: both CTAs' epilogue threads
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -487,11 +498,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (s.n_split < s.N) tma_prefetch_desc(&tmB1);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_slot, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // both CTAs' barriers exist before any remote signal
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_launch_dependents();
@@ -506,12 +523,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < STAGES; ++i) issued[i] = 0;
       bool ok = true;
-      for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
+      for (int unit = unit0; unit < num_units && ok; unit += ustep) {
         const int tile = unit / ksplit;
         const int kb0 = (unit % ksplit) * s.kb_per;
         const int kb1 = min(kblocks, kb0 + s.kb_per);
         int batch, m_blk, n_blk;
-        tile_coords(tile, m_tiles, n_tiles, s.raster_g, batch, m_blk, n_blk);
+        tile_coords(tile, m_units, n_tiles, s.raster_g, batch, m_blk, n_blk);
+        if (PAIR) m_blk = 2 * m_blk + (int)crank;
         const int n0 = n_blk * BN;
         const int a_col = s.a_col0 + batch * s.a_col_step;
         const int b_row = s.b_row0 + batch * s.b_row_step;
@@ -524,6 +542,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sa = smem + stage * L::kStage;
           uint8_t* sb = sa + L::kA;
+          if constexpr (PAIR) {
+            // both CTAs' halves complete on the even CTA's barrier
+            if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * L::kStage);
+            const uint32_t fb = mapa_rank(smem_u32(&full_bar[stage]), 0);
+            const int k0 = kb * kBK;
+            tma_load_2d_pair(sa, &tmA, fb, a_col + k0, m_blk * BM);
+            tma_load_2d_pair(sb, mb, fb, k0, b_row + nb + (int)crank * (BN / 2));
+            issued[stage]++;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+            continue;
+          }
           mbar_arrive_expect_tx(&full_bar[stage], L::kStage);
 #pragma unroll
           for (int u = 0; u < KSUB; ++u) {
@@ -545,20 +577,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // make sure no copy into this CTA's shared memory is still in flight
+      // (pair mode: the odd CTA's copies complete on the even CTA's barriers;
+      // it waits until the MMAs released its last use of every stage)
 #pragma unroll
-      for (int i = 0; i < STAGES; ++i)
-        if (issued[i]) mbar_wait(&full_bar[i], (issued[i] - 1) & 1, st, nullptr, 2);
+      for (int i = 0; i < STAGES; ++i) {
+        if (!issued[i]) continue;
+        if (!PAIR || leader)
+          mbar_wait(&full_bar[i], (issued[i] - 1) & 1, st, nullptr, 2);
+        else
+          mbar_wait(&empty_bar[i], (issued[i] - 1) & 1, st, nullptr, 2);
+      }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
-      constexpr uint32_t idesc = idesc_bf16(BM, BN, false, B_MN);
+    if (lane == 0 && (!PAIR || leader)) {
+      // ---------------- MMA issuer (pair mode: the even CTA) ----------------
+      constexpr uint32_t idesc = idesc_bf16(PAIR ? 2 * BM : BM, BN, false, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
+      for (int unit = unit0; unit < num_units && ok; unit += ustep) {
         const int kb0 = (unit % ksplit) * s.kb_per;
         const int kb1 = min(kblocks, kb0 + s.kb_per);
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, st, abort_flag, 3)) break;
@@ -584,22 +623,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bdesc = sdesc_sw128(b_addr + k * 2048, 64 * 128, 1024);
               else
                 bdesc = sdesc_sw128(b_addr + k * 32, 16, 1024);
-              umma_bf16(d_tmem, adesc, bdesc, idesc, (kb != kb0 || u != 0 || k != 0) ? 1u : 0u);
+              if constexpr (PAIR)
+                umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb != kb0 || u != 0 || k != 0) ? 1u : 0u);
+              else
+                umma_bf16(d_tmem, adesc, bdesc, idesc, (kb != kb0 || u != 0 || k != 0) ? 1u : 0u);
             }
           }
-          umma_commit(&empty_bar[stage]);
+          if constexpr (PAIR)
+            umma_commit_pair(&empty_bar[stage], (uint16_t)0x3);  // frees the stage in both CTAs
+          else
+            umma_commit(&empty_bar[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        umma_commit(&tfull_bar[acc]);
+        if constexpr (PAIR)
+          umma_commit_pair(&tfull_bar[acc], (uint16_t)0x3);
+        else
+          umma_commit(&tfull_bar[acc]);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
       }
       // all MMAs issued by this thread have finished before TMEM is freed
-      umma_commit(drain_bar);
+      if constexpr (PAIR)
+        umma_commit_pair(drain_bar, (uint16_t)0x1);
+      else
+        umma_commit(drain_bar);
       mbar_wait(drain_bar, 0, st, nullptr, 5);
     }
   } else {
@@ -610,11 +661,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rit = (BM == 128) ? quarter * 32 + lane : quarter * 16 + (lane & 15);  // row within the tile
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int unit = blockIdx.x; unit < num_units; unit += gridDim.x) {
+    for (int unit = unit0; unit < num_units; unit += ustep) {
       const int tile = unit / ksplit;
       const int ks = unit % ksplit;
       int batch, m_blk, n_blk;
-      tile_coords(tile, m_tiles, n_tiles, s.raster_g, batch, m_blk, n_blk);
+      tile_coords(tile, m_units, n_tiles, s.raster_g, batch, m_blk, n_blk);
+      if (PAIR) m_blk = 2 * m_blk + (int)crank;
       bool ok = mbar_wait(&tfull_bar[acc], acc_phase, st, abort_flag, 6);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
@@ -629,7 +681,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           run_epilogue<BN, EPI>(ea, TmemSrc{taddr}, batch, row, n_blk * BN, row_ok);
         }
         tc_fence_before();
-        mbar_arrive(&tempty_bar[acc]);
+        if constexpr (PAIR)
+          mbar_arrive_cluster(mapa_rank(smem_u32(&tempty_bar[acc]), 0));  // the even CTA's accumulator barrier
+        else
+          mbar_arrive(&tempty_bar[acc]);
       } else {
         // this K slice's partial -> its slot; the last warp of the quarter reduces
         const int rows_pt = s.M < BM ? s.M : BM;
@@ -674,16 +729,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+  if constexpr (PAIR) {
+    // every MMA of the pair has finished (the even CTA drained them) and no
+    // remote arrive or copy is still in flight before the collective free
+    cluster_sync();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+  } else {
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem_base, kTmemCols);
+    }
   }
 }
 
-template <int BM, int BN, int STAGES, Epi EPI, bool B_MN, int KSUB = 1, bool TMA_ST = false>
+template <int BM, int BN, int STAGES, Epi EPI, bool B_MN, int KSUB = 1, bool TMA_ST = false, bool PAIR = false>
 cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArgs& ea, const DevStatusHost& st,
                         int num_sms, cudaStream_t stream) {
-  using L = GemmSmem<BM, BN, STAGES, KSUB, TMA_ST>;
+  using L = GemmSmem<BM, BN, STAGES, KSUB, TMA_ST, PAIR>;
   if (s.K % (kBK * KSUB)) return cudaErrorInvalidValue;
   static_assert(L::kBytes <= 232448, "shared memory budget");
   CUtensorMap ta, tb0, tb1;
@@ -692,10 +757,11 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
   if (B_MN) {
     if (!make_tmap_bf16_2d(&tb0, op.B0, op.b0_rows, op.ldb0, op.ldb0, 64, 64)) return cudaErrorInvalidValue;
   } else {
-    if (!make_tmap_bf16_2d(&tb0, op.B0, op.b0_rows, op.ldb0, op.ldb0, BN, kBK)) return cudaErrorInvalidValue;
+    constexpr uint32_t box_rows = PAIR ? BN / 2 : BN;  // pair mode: each CTA loads half the rows
+    if (!make_tmap_bf16_2d(&tb0, op.B0, op.b0_rows, op.ldb0, op.ldb0, box_rows, kBK)) return cudaErrorInvalidValue;
   }
   tb1 = tb0;
-  if (op.B1 && !make_tmap_bf16_2d(&tb1, op.B1, op.b1_rows, op.ldb1, op.ldb1, BN, kBK))
+  if (op.B1 && !make_tmap_bf16_2d(&tb1, op.B1, op.b1_rows, op.ldb1, op.ldb1, PAIR ? BN / 2 : BN, kBK))
     return cudaErrorInvalidValue;
   CUtensorMap to0 = ta, to1 = ta;
   if constexpr (TMA_ST) {
@@ -710,11 +776,27 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
     }
     if (!ok) return cudaErrorInvalidValue;
   }
-  auto kern = gemm_kernel<BM, BN, STAGES, KSUB, EPI, B_MN, TMA_ST>;
+  auto kern = gemm_kernel<BM, BN, STAGES, KSUB, EPI, B_MN, TMA_ST, PAIR>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
+  static int max_clusters = 0;  // pair mode: clusters of 2 that fit at once
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes);
+    if (attr_err == cudaSuccess && PAIR) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * num_sms);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = L::kBytes;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = 2;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+      if (attr_err == cudaSuccess && max_clusters < 1) attr_err = cudaErrorInvalidConfiguration;
+    }
   });
   if (attr_err != cudaSuccess) return attr_err;
   GemmShape sh = s;
@@ -724,7 +806,7 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
   const int kblocks = s.K / (kBK * KSUB);
   sh.ksplit = 1;
   sh.kb_per = kblocks;
-  if (ea.part && ea.counters && m_tiles == 1 && tiles * 2 <= num_sms && kblocks >= 2 &&
+  if (!PAIR && ea.part && ea.counters && m_tiles == 1 && tiles * 2 <= num_sms && kblocks >= 2 &&
       tiles * 4 <= kMaxSplitCounters) {
     int ks = num_sms / tiles;
     if (ks > 4) ks = 4;  // the reduction reads every slice: keep it short
@@ -738,10 +820,18 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
       sh.kb_per = kb_per;
     }
   }
-  const int units = tiles * sh.ksplit;
-  const int grid = units < num_sms ? units : num_sms;
   DevStatus dst{st.word, st.wait_limit_ns};
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, stream, ta, tb0, tb1, to0, to1, sh, ea, dst);
+  if constexpr (PAIR) {
+    if (m_tiles % 2 || sh.ksplit != 1) return cudaErrorInvalidValue;
+    const int pairs = tiles / 2;
+    const int clusters = pairs < max_clusters ? pairs : max_clusters;
+    return launch_pdl_cluster2(kern, dim3(2 * clusters), dim3(kThreads), L::kBytes, stream, ta, tb0, tb1, to0, to1,
+                               sh, ea, dst);
+  } else {
+    const int units = tiles * sh.ksplit;
+    const int grid = units < num_sms ? units : num_sms;
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, stream, ta, tb0, tb1, to0, to1, sh, ea, dst);
+  }
 }
 
 }  // namespace
@@ -755,18 +845,23 @@ cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, con
   const bool tiny = s.M <= 64;
   const bool small = s.M <= kBM;
   const bool k256 = s.K % 256 == 0;
+  // many rows: CTA pairs run 256-row MMAs (an even number of row blocks)
+  const bool pairs = ((s.M + kBM - 1) / kBM) % 2 == 0 && s.M > 2 * kBM;
   switch (epi) {
     case Epi::kQRope:
       if (s.N % 192 || op.b_mn_major) return cudaErrorInvalidValue;
       if (tiny && k256) return launch_impl<64, 96, 5, Epi::kQRope, false, 2>(s, op, ea, st, num_sms, stream);
       if (small && k256) return launch_impl<128, 96, 3, Epi::kQRope, false, 2>(s, op, ea, st, num_sms, stream);
       if (small) return launch_impl<128, 96, 7, Epi::kQRope, false>(s, op, ea, st, num_sms, stream);
+      if (pairs) return launch_impl<128, 192, 6, Epi::kQRope, false, 1, true, true>(s, op, ea, st, num_sms, stream);
       return launch_impl<128, 192, 4, Epi::kQRope, false, 1, true>(s, op, ea, st, num_sms, stream);
     case Epi::kKVCache:
       if (s.N % 256 || op.b_mn_major) return cudaErrorInvalidValue;
       if (tiny && k256) return launch_impl<64, 128, 4, Epi::kKVCache, false, 2>(s, op, ea, st, num_sms, stream);
       if (small && k256) return launch_impl<128, 128, 3, Epi::kKVCache, false, 2>(s, op, ea, st, num_sms, stream);
       if (small) return launch_impl<128, 128, 6, Epi::kKVCache, false>(s, op, ea, st, num_sms, stream);
+      if (ea.t_mod % 32 == 0 && ea.B > 0 && pairs)
+        return launch_impl<128, 256, 6, Epi::kKVCache, false, 1, true, true>(s, op, ea, st, num_sms, stream);
       if (ea.t_mod % 32 == 0 && ea.B > 0)
         return launch_impl<128, 256, 4, Epi::kKVCache, false, 1, true>(s, op, ea, st, num_sms, stream);
       return launch_impl<128, 256, 4, Epi::kKVCache, false>(s, op, ea, st, num_sms, stream);
@@ -778,6 +873,11 @@ cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, con
       if (tiny && k256) return launch_impl<64, 64, 3, Epi::kResidual, false, 4>(s, op, ea, st, num_sms, stream);
       if (small && k256) return launch_impl<128, 64, 4, Epi::kResidual, false, 2>(s, op, ea, st, num_sms, stream);
       if (small) return launch_impl<128, 64, 8, Epi::kResidual, false>(s, op, ea, st, num_sms, stream);
+      if (pairs) {
+        GemmShape g8 = s;
+        g8.raster_g = 8;  // groups of 8 row-block pairs
+        return launch_impl<128, 256, 6, Epi::kResidual, false, 1, true, true>(g8, op, ea, st, num_sms, stream);
+      }
       return launch_impl<128, 256, 4, Epi::kResidual, false, 1, true>(g16, op, ea, st, num_sms, stream);
     }
     case Epi::kStoreF32:
@@ -789,8 +889,10 @@ cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, con
       // clipped on store; the c^Q / c^KV split at 1536 is tile-aligned) read
       // the fewest operand bytes from L2 per MMA, and 16 row blocks make 144
       // tiles, one wave; 128-wide tiles when there are too few tiles for a wave.
-      if (s.n_split % 256 == 0 && ((s.M + kBM - 1) / kBM) * 9 >= num_sms / 2)
+      if (s.n_split % 256 == 0 && ((s.M + kBM - 1) / kBM) * 9 >= num_sms / 2) {
+        if (pairs) return launch_impl<128, 256, 6, Epi::kStoreF32, false, 1, true, true>(s, op, ea, st, num_sms, stream);
         return launch_impl<128, 256, 4, Epi::kStoreF32, false, 1, true>(s, op, ea, st, num_sms, stream);
+      }
       return launch_impl<128, 128, 6, Epi::kStoreF32, false, 1, true>(s, op, ea, st, num_sms, stream);
     case Epi::kStoreBf16:
     default:
