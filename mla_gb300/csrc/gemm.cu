@@ -512,7 +512,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_launch_dependents();
-  pdl_wait();
+  // The producer waits for the preceding kernel itself, after it has issued
+  // the weight (B) half of its first stages: the weights are read-only for
+  // the whole step, so their first loads overlap the preceding kernel's tail.
+  if (warp != 0) pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -523,6 +526,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < STAGES; ++i) issued[i] = 0;
       bool ok = true;
+      int pre = 0;  // stages of the first unit whose B half is already in flight
+      if constexpr (!PAIR) {
+        if (unit0 < num_units) {
+          const int tile = unit0 / ksplit;
+          const int kb0 = (unit0 % ksplit) * s.kb_per;
+          const int kb1 = min(kblocks, kb0 + s.kb_per);
+          int batch, m_blk, n_blk;
+          tile_coords(tile, m_units, n_tiles, s.raster_g, batch, m_blk, n_blk);
+          const int n0 = n_blk * BN;
+          const int b_row = s.b_row0 + batch * s.b_row_step;
+          const CUtensorMap* mb = (n0 < s.n_split) ? &tmB0 : &tmB1;
+          const int nb = (n0 < s.n_split) ? n0 : n0 - s.n_split;
+          pre = min(STAGES, kb1 - kb0);
+          for (int i = 0; i < pre; ++i) {  // fresh ring: every stage is free
+            uint8_t* sb = smem + i * L::kStage + L::kA;
+            mbar_arrive_expect_tx(&full_bar[i], L::kStage);
+            issued[i] = 1;  // counted now: the exit wait covers these copies even after an abort
+#pragma unroll
+            for (int u = 0; u < KSUB; ++u) {
+              const int k0 = ((kb0 + i) * KSUB + u) * kBK;
+              if constexpr (B_MN) {
+#pragma unroll
+                for (int j = 0; j < BN / 64; ++j)
+                  tma_load_2d(sb + u * L::kB1 + j * (64 * 128), mb, &full_bar[i], nb + j * 64, b_row + k0);
+              } else {
+                tma_load_2d(sb + u * L::kB1, mb, &full_bar[i], k0, b_row + nb);
+              }
+            }
+          }
+        }
+      }
+      pdl_wait();
       for (int unit = unit0; unit < num_units && ok; unit += ustep) {
         const int tile = unit / ksplit;
         const int kb0 = (unit % ksplit) * s.kb_per;
@@ -556,11 +591,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             continue;
           }
-          mbar_arrive_expect_tx(&full_bar[stage], L::kStage);
+          const bool b_done = unit == unit0 && kb - kb0 < pre;  // B half issued before the wait
+          if (!b_done) mbar_arrive_expect_tx(&full_bar[stage], L::kStage);
 #pragma unroll
           for (int u = 0; u < KSUB; ++u) {
             const int k0 = (kb * KSUB + u) * kBK;
             tma_load_2d(sa + u * L::kA1, &tmA, &full_bar[stage], a_col + k0, m_blk * BM);
+            if (b_done) continue;
             if constexpr (B_MN) {
 #pragma unroll
               for (int j = 0; j < BN / 64; ++j)
@@ -569,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d(sb + u * L::kB1, mb, &full_bar[stage], k0, b_row + nb);
             }
           }
-          issued[stage]++;
+          if (!b_done) issued[stage]++;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
