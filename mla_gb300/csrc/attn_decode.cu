@@ -225,12 +225,13 @@ __global__ void combine_kernel(const float* __restrict__ part_o, const float2* _
 //              TMEM columns; c_j serves as the K-major B operand of S and the
 //              MN-major A operand of O^T without a copy).  Two issuing
 //              threads keep the tensor pipe fed while either one waits.
-//   warps 2..5 softmax: head h = 16*(warp%4) + lane (lanes 0..15; an M=64
-//              accumulator row r lives in TMEM lane 32*(r/16) + r%16), lazy
-//              rescaling (O^T columns rescaled only when a head's max grows by
-//              more than 2^8), P_j [64 heads x 64 keys] bf16 to shared memory;
-//              at the end of a segment every thread writes the latent rows it
-//              holds.
+//   warps 2..5 softmax: head h = 16*(warp%4) + lane%16 (an M=64
+//              accumulator row r lives in TMEM lane 32*(r/16) + r%16), lanes
+//              i and i+16 each take 32 of the head's 64 keys (16x32bx2 loads);
+//              lazy rescaling (O^T columns rescaled only when a head's max
+//              grows by more than 2^8), P_j [64 heads x 64 keys] bf16 to shared
+//              memory; at the end of a segment every thread writes the latent
+//              rows it holds.
 // ---------------------------------------------------------------------------
 constexpr int kLatTile = 64;
 constexpr uint32_t kLatBox = 64 * 128;                       // 64 rows x 64 bf16
@@ -418,12 +419,15 @@ __global__ void __launch_bounds__(kLatThreads, 1)
   } else {
     const int quarter = warp & 3;
     const int tid = threadIdx.x - 64;
-    const bool valid = lane < 16;
+    // head h = 16 * quarter + lane % 16 (an M=64 accumulator row r lives in
+    // TMEM lane 32*(r/16) + r%16); lanes i and i + 16 take keys 0..31 and
+    // 32..63 of the head's 64 scores
     const int h = quarter * 16 + (lane & 15);
+    const int kh = lane >> 4;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     uint8_t* pbuf = smem + kLatPOff;
     const float sl2 = a.scale * kLog2e;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;  // l: this thread's half of the head's sum
     // Every softmax warp runs every iteration and reaches every named barrier
     // (bar.sync has no time limit); after a failed wait (ok == false) the
     // work of the remaining iterations is skipped, the barriers are not.
@@ -442,24 +446,21 @@ __global__ void __launch_bounds__(kLatThreads, 1)
         l = 0.f;
       }
       ok = ok && __all_sync(0xffffffffu, mbar_wait(&bar->s_full[stg], (i >> 1) & 1, st, abort_flag, 67));
-      uint32_t s[64];
+      uint32_t s[32];
       if (ok) {
         tc_fence_after();
-        uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
-        uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
-        tmem_ld32(tmem + lane_addr + stg * 64, s0);
-        tmem_ld32(tmem + lane_addr + stg * 64 + 32, s1);
+        tmem_ld16x2_32<32>(tmem + lane_addr + stg * 64, s);
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&bar->s_free[stg]);
       } else {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) s[c] = 0u;
+        for (int c = 0; c < 32; ++c) s[c] = 0u;
       }
-      const int k0 = t * kLatTile;
-      if (k0 + kLatTile > a.L) {
+      const int k0 = t * kLatTile + kh * 32;  // first key of this thread's half
+      if (k0 + 32 > a.L) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < 32; ++c)
           if (k0 + c >= a.L) s[c] = __float_as_uint(-INFINITY);
       }
       float mx;
@@ -468,24 +469,24 @@ __global__ void __launch_bounds__(kLatThreads, 1)
 #pragma unroll
         for (int c = 0; c < 8; ++c) mp[c] = __uint_as_float(s[c]);
 #pragma unroll
-        for (int c = 8; c < 64; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(s[c]));
+        for (int c = 8; c < 32; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(s[c]));
         mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // the head's other half
       }
       mx *= sl2;  // log2 units (the scale is positive)
-      const bool need = valid && mx > m + kRescaleThresholdLatent;
+      const bool need = mx > m + kRescaleThresholdLatent;
       const float m_new = need ? mx : m;
       const float alpha = need ? ex2_approx(m - m_new) : 1.f;
-      float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float sp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
+      for (int c = 0; c < 32; ++c) {
         const float p = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -m_new));
         s[c] = __float_as_uint(p);
-        sp[c & 7] += p;
+        sp[c & 3] += p;
       }
-      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-      l = l * alpha + sum;
+      l = l * alpha + ((sp[0] + sp[1]) + (sp[2] + sp[3]));
       m = m_new;
-      if (valid) bar->alpha[stg][h] = alpha;
+      if (kh == 0) bar->alpha[stg][h] = alpha;
       const bool warp_need = __any_sync(0xffffffffu, need);
       if (lane == 0) bar->need[stg][quarter] = warp_need ? 1 : 0;
       named_sync_128();
@@ -514,15 +515,16 @@ __global__ void __launch_bounds__(kLatThreads, 1)
         }
         tmem_wait_st();
       }
-      if (ok && valid) {
+      if (ok) {
+        // this thread's 32 keys of row h: 16-byte chunks kh*4 .. kh*4+3 (128-byte swizzle)
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          const int k = c8 * 8;
+        for (int j = 0; j < 4; ++j) {
+          const int k = j * 8;
           const uint4 v = make_uint4(pack_bf16x2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])),
                                      pack_bf16x2(__uint_as_float(s[k + 2]), __uint_as_float(s[k + 3])),
                                      pack_bf16x2(__uint_as_float(s[k + 4]), __uint_as_float(s[k + 5])),
                                      pack_bf16x2(__uint_as_float(s[k + 6]), __uint_as_float(s[k + 7])));
-          *reinterpret_cast<uint4*>(pbuf + h * 128 + ((c8 ^ (h & 7)) << 4)) = v;
+          *reinterpret_cast<uint4*>(pbuf + h * 128 + (((kh * 4 + j) ^ (h & 7)) << 4)) = v;
         }
       }
       fence_proxy_async_smem();
@@ -532,9 +534,10 @@ __global__ void __launch_bounds__(kLatThreads, 1)
 
       // end of a segment: O^T complete after this tile's P.V
       ok = ok && __all_sync(0xffffffffu, mbar_wait(&bar->ckv_empty[stg], (i >> 1) & 1, st, abort_flag, 69));
-      if (valid) {
+      const float l_head = l + __shfl_xor_sync(0xffffffffu, l, 16);
+      if (kh == 0) {
         bar->m[h] = m;
-        bar->l[h] = l;
+        bar->l[h] = l_head;
       }
       named_sync_128();
       const bool whole = t == nt - 1 && i >= t;  // the sequence's tile 0 is in this CTA too
