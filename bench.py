@@ -395,6 +395,35 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """Set up one configuration, run the warm-up steps, then one step between
+    cudaProfilerStart and cudaProfilerStop (nothing is timed or reported)."""
+    import re
+    import torch
+    mt = re.fullmatch(r"(prefill|decode|latent)_b(\d+)_([tp])(\d+)(_cache)?", args.profile)
+    if not mt:
+        raise SystemExit(f"--profile: unknown configuration {args.profile!r}")
+    kind, B, n, cache = mt.group(1), int(mt.group(2)), int(mt.group(4)), bool(mt.group(5))
+    torch.cuda.set_device(0)
+    r = Runner("cuda:0")
+    keep = None
+    if kind == "prefill":
+        x, out, ws, caches = r.prefill_setup(B, n, with_cache=cache)
+        step = r.prefill_step_fn(x, out, ws, caches, n)
+        keep = (x, out, ws, caches)
+    else:
+        step, keep = r.decode_step_fn(B, n, rebuilt=(kind == "decode"))
+    for _ in range(args.warmup):
+        step(None)
+    torch.cuda.synchronize()
+    torch.cuda.profiler.start()
+    step(None)
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    print(json.dumps({"profile": args.profile, "warmup": args.warmup, "ok": True}), flush=True)
+    del keep
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -404,9 +433,15 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline prefill only")
     ap.add_argument("--cpu-tokens", type=int, default=2048,
                     help="tokens of the headline sequence the CPU oracle baseline runs (0 = skip)")
+    ap.add_argument("--profile", default=None,
+                    help="run one step of one configuration for a profiler and exit: prefill_bB_tT[_cache], "
+                         "decode_bB_pP (rebuilt cache) or latent_bB_pP; only that step lies between "
+                         "cudaProfilerStart/Stop (ncu --profile-from-start off)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile:
+        return run_profile(args)
 
     import torch
     world, rank, local = dist_env()
