@@ -6,22 +6,25 @@
 // global memory).
 //
 // CTA = (128-query tile, head, sequence), heaviest tiles launched first.
-// Warp roles (224 threads):
+// Warp roles (256 threads):
 //   warp 0   TMA: the Q tile once, then K tiles into a 2-slot ring
 //   warp 6   TMA: V tiles into a 2-slot ring (each K and V tile is requested
 //            a whole tile ahead of the MMA that reads it)
-//   warp 1   TMEM allocation; one lane issues the MMAs:
-//              S_j = Q K_j^T   M=128 N=128 K=192, into one of two TMEM buffers
-//              O  += P_j V_j   M=128 N=128 K=128, P read from tensor memory
-//                              (row m in lane m, bf16 pairs packed per
-//                              column), V read MN-major from its TMA tile
-//            issued in the order S_0, S_1, PV_0, S_2, PV_1, ... so the tensor
-//            core computes the next scores while the softmax runs
-//   warps 2..5  one thread per query row: read S_j from TMEM, scale, causal
-//            mask on the diagonal tile, running max with lazy rescaling (O is
-//            rescaled in TMEM only when the max grows by more than 2^8, so P
-//            stays <= 256), P_j as bf16 into one of two TMEM buffers, and
-//            at the end O / l to global memory.
+//   warp 1   TMEM allocation; one lane issues S_j = Q K_j^T (M=128 N=128
+//            K=192) into score buffer j & 1, Q read from tensor memory (the
+//            softmax warps copy it there once), K from its TMA tile
+//   warp 7   one lane issues O += P_j V_j (M=128 N=128 K=128), P read from
+//            tensor memory (row m in lane m, bf16 pairs packed per column,
+//            written over the first 64 columns of score buffer j & 1), V read
+//            MN-major from its TMA tile; a score buffer is reused once the
+//            P.V that read its P has finished
+//   (two issuing threads, each on blocking waits, keep the tensor pipe fed
+//   while either one waits; only K and V are read from shared memory)
+//   warps 2..5  one thread per query row: copy the Q row into tensor memory;
+//            read S_j from TMEM, scale, causal mask on the diagonal tile,
+//            running max with lazy rescaling (O is rescaled in TMEM only when
+//            the max grows by more than 2^8, so P stays <= 256), P_j as bf16
+//            over S_j, and at the end O / l to global memory.
 // Layout: Q [B*T, 64*192], K/V caches [B, 64, cap, 192|128] (TMA 3D views
 // whose position extent is T, so keys >= T read as zeros), O [B*T, 64*128].
 #include "common.cuh"
@@ -31,24 +34,25 @@ namespace mla {
 
 namespace {
 
-constexpr int kThreads = 224;
+constexpr int kThreads = 256;
 constexpr uint32_t kAtom = 128 * 128;            // 128 rows x 64 bf16
 constexpr uint32_t kQOff = 0;                    // 3 atoms
 constexpr uint32_t kKOff = 3 * kAtom;            // 2 slots x 3 atoms
 constexpr uint32_t kVOff = 9 * kAtom;            // 2 slots x 2 atoms (vdim 0-63, 64-127)
 constexpr uint32_t kBarOff = 13 * kAtom;
-// tensor memory columns: S_0, S_1 (fp32), O (fp32), P_0, P_1 (bf16 pairs)
-constexpr uint32_t kTmS = 0, kTmO = 256, kTmP = 384;
+// tensor memory columns: S_0, S_1 (fp32; P_j bf16 pairs over the first 64 of
+// S_j), O (fp32), Q (bf16 pairs, 192 values per row)
+constexpr uint32_t kTmS = 0, kTmO = 256, kTmQ = 384;
 constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 
 struct Bars {
-  uint64_t q_full;
+  uint64_t q_full, q_tmem;
   uint64_t k_full[2], k_empty[2];
   uint64_t v_full[2], v_empty[2];
-  uint64_t s_full[2], s_free[2];
+  uint64_t s_full[2];
   uint64_t p_full[2], pv_done[2];
-  uint64_t drain;
+  uint64_t drain_s, drain_pv;
   uint32_t tmem_slot;
   int abort;
 };
@@ -72,11 +76,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bar->q_full, 1);
+    mbar_init(&bar->q_tmem, 128);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->v_full[i], 1);
       mbar_init(&bar->v_empty[i], 1);
       mbar_init(&bar->s_full[i], 1);
-      mbar_init(&bar->s_free[i], 128);
     }
     mbar_init(&bar->k_full[0], 1);
     mbar_init(&bar->k_empty[0], 1);
@@ -86,7 +90,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar->p_full[1], 128);
     mbar_init(&bar->pv_done[0], 1);
     mbar_init(&bar->pv_done[1], 1);
-    mbar_init(&bar->drain, 1);
+    mbar_init(&bar->drain_s, 1);
+    mbar_init(&bar->drain_pv, 1);
     bar->abort = 0;
     fence_barrier_init();
   }
@@ -140,67 +145,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---- MMA issuer ----
+      // ---- S issuer: S_j = Q K_j^T into score buffer j & 1 ----
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16(128, 128, false, true);
-      const uint32_t q_addr = smem_u32(smem + kQOff);
       const uint32_t k_addr = smem_u32(smem + kKOff);
-      const uint32_t v_addr = smem_u32(smem + kVOff);
-      bool ok = mbar_wait(&bar->q_full, 0, st, abort_flag, 44);
-      tc_fence_after();
-      // Event loop: issue S_j (needs K_j and a free score buffer) and PV_j
-      // (needs P_j and V_j) in whatever order their inputs become ready, at
-      // most two score tiles ahead of the P.V tiles.
-      int next_s = 0, next_pv = 0;
-      Watchdog wd;
-      wd.reset();
-      while (ok && next_pv < n_kv) {
-        bool progress = false;
-        if (next_s < n_kv && next_s <= next_pv + 1) {
-          const int slot = next_s & 1;
-          const uint32_t ph = (next_s >> 1) & 1;
-          if (mbar_test(&bar->k_full[slot], ph) && mbar_test(&bar->s_free[slot], ph ^ 1)) {
-            tc_fence_after();
-            const uint32_t d = tmem + kTmS + slot * 128;
-            const uint32_t kb = k_addr + slot * 3 * kAtom;
+      const uint32_t q_tm = tmem + kTmQ;
+      bool ok = mbar_wait(&bar->q_tmem, 0, st, abort_flag, 44);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int slot = j & 1;
+        if (!mbar_wait(&bar->k_full[slot], (j >> 1) & 1, st, abort_flag, 45)) break;
+        // the buffer's previous P (tile j-2) has been read by its P.V
+        if (j > 1 && !mbar_wait(&bar->pv_done[slot], ((j - 2) >> 1) & 1, st, abort_flag, 46)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + kTmS + slot * 128;
+        const uint32_t kb = k_addr + slot * 3 * kAtom;
 #pragma unroll
-            for (int kk = 0; kk < 12; ++kk) {
-              const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-              umma_bf16(d, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idesc_s,
-                        kk > 0 ? 1u : 0u);
-            }
-            umma_commit(&bar->s_full[slot]);
-            umma_commit(&bar->k_empty[slot]);
-            ++next_s;
-            progress = true;
-          }
+        for (int kk = 0; kk < 12; ++kk) {
+          const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+          umma_bf16_ts(d, q_tm + kk * 8, sdesc_sw128(kb + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
         }
-        // P_j arrives on p_full[j & 1]: S_{j+2} (hence P_{j+2}) is issued only
-        // after P.V_j, so a barrier never runs two phases ahead of this test
-        if (next_pv < next_s && mbar_test(&bar->p_full[next_pv & 1], (next_pv >> 1) & 1) &&
-            mbar_test(&bar->v_full[next_pv & 1], (next_pv >> 1) & 1)) {
-          tc_fence_after();
-          const uint32_t vb = v_addr + (next_pv & 1) * 2 * kAtom;
-          const uint32_t pa = tmem + kTmP + (next_pv & 1) * 64;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, kAtom, 1024);
-            umma_bf16_ts(tmem + kTmO, pa + kk * 8, bdesc, idesc_pv, (next_pv > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(&bar->pv_done[next_pv & 1]);
-          umma_commit(&bar->v_empty[next_pv & 1]);
-          ++next_pv;
-          progress = true;
-        }
-        if (progress) {
-          wd.reset();
-        } else {
-          if (wd.expired(st, abort_flag, 45)) break;
-          __nanosleep(32);  // leave issue slots to the softmax warp on this scheduler
-        }
+        umma_commit(&bar->s_full[slot]);
+        umma_commit(&bar->k_empty[slot]);
       }
-      umma_commit(&bar->drain);
-      mbar_wait(&bar->drain, 0, st, nullptr, 49);
+      umma_commit(&bar->drain_s);
+      mbar_wait(&bar->drain_s, 0, st, nullptr, 49);
+    }
+  } else if (warp == 7) {
+    if (lane == 0) {
+      // ---- P.V issuer: O += P_j V_j ----
+      constexpr uint32_t idesc_pv = idesc_bf16(128, 128, false, true);
+      const uint32_t v_addr = smem_u32(smem + kVOff);
+      for (int j = 0; j < n_kv; ++j) {
+        const int slot = j & 1;
+        if (!mbar_wait(&bar->p_full[slot], (j >> 1) & 1, st, abort_flag, 47)) break;
+        if (!mbar_wait(&bar->v_full[slot], (j >> 1) & 1, st, abort_flag, 48)) break;
+        tc_fence_after();
+        const uint32_t vb = v_addr + slot * 2 * kAtom;
+        const uint32_t pa = tmem + kTmS + slot * 128;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, kAtom, 1024);
+          umma_bf16_ts(tmem + kTmO, pa + kk * 8, bdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&bar->pv_done[slot]);
+        umma_commit(&bar->v_empty[slot]);
+      }
+      umma_commit(&bar->drain_pv);
+      mbar_wait(&bar->drain_pv, 0, st, nullptr, 49);
     }
   } else {
     // ---- softmax / correction / epilogue: warps 2..5, one thread per query row ----
@@ -209,8 +199,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qpos = q0 + row;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bar->q_full, 0, st, abort_flag, 54));
+    if (ok) {
+      // this row of Q (three 128-byte-swizzled 64-column atoms) into tensor
+      // memory as bf16 pairs, the A operand of every S_j
+      const uint8_t* qrow = smem + kQOff + row * 128;
+#pragma unroll
+      for (int c = 0; c < 3; ++c) {
+        uint32_t v[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 w = *reinterpret_cast<const uint4*>(qrow + c * kAtom + ((q ^ (row & 7)) << 4));
+          v[4 * q] = w.x;
+          v[4 * q + 1] = w.y;
+          v[4 * q + 2] = w.z;
+          v[4 * q + 3] = w.w;
+        }
+        tmem_st32(tmem + lane_addr + kTmQ + c * 32, v);
+      }
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    mbar_arrive(&bar->q_tmem);
+    for (int j = 0; ok && j < n_kv; ++j) {
       const int slot = j & 1;
       ok = __all_sync(0xffffffffu, mbar_wait(&bar->s_full[slot], (j >> 1) & 1, st, abort_flag, 50));
       if (!ok) break;
@@ -228,8 +239,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(ta + 96, s3);
         tmem_wait_ld();
       }
-      tc_fence_before();
-      mbar_arrive(&bar->s_free[slot]);
       const bool diag = (j == n_kv - 1);
       const int k0 = j * 128;
       // max of the raw scores (the scale is positive), causal mask on the
@@ -261,11 +270,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       l = l * alpha + sum;
       m = m_new;
-      // P buffer (j & 1) is free once P.V of tile j-2 has completed
-      if (j > 1) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar->pv_done[j & 1], ((j - 2) >> 1) & 1, st, abort_flag, 51));
-        if (!ok) break;
-      }
       // O may be rescaled only after P.V of tile j-1 has completed
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         ok = __all_sync(0xffffffffu, mbar_wait(&bar->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, st, abort_flag, 53));
@@ -285,12 +289,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_st();
         }
       }
-      // P_j (bf16 pairs, low half = even key) into tensor memory buffer j & 1
+      // P_j (bf16 pairs, low half = even key) over the first 64 columns of
+      // score buffer j & 1 (S_j is entirely in registers by now)
       {
         uint32_t pk[64];
 #pragma unroll
         for (int c = 0; c < 64; ++c) pk[c] = pack_bf16x2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
-        const uint32_t tp = tmem + lane_addr + kTmP + (j & 1) * 64;
+        const uint32_t tp = tmem + lane_addr + kTmS + (j & 1) * 128;
 #pragma unroll
         for (int c = 0; c < 64; c += 16) tmem_st16(tp + c, &pk[c]);
         tmem_wait_st();
