@@ -211,6 +211,45 @@ def prefill(w: dict, x: np.ndarray, dims: Dims = KIMI_K2, eps: float = DEFAULT_E
     }
 
 
+def prefill_with_past(w: dict, x: np.ndarray, K_cache: np.ndarray, V_cache: np.ndarray,
+                      dims: Dims = KIMI_K2, eps: float = DEFAULT_EPS, base: float = DEFAULT_ROPE_BASE,
+                      scale: float | None = None, query_rows=None) -> dict:
+    """Chunked prefill: x [B, T, d] are the tokens at positions P0..P0+T-1,
+    P0 = K_cache.shape[2]; K_cache [B, H, P0, qk] and V_cache [B, H, P0, v]
+    hold positions 0..P0-1 (post-RoPE).
+
+    "Mix and project" page: the cache update concatenates the new keys and
+    values after the cached ones (past_key_value.update), and the additive
+    mask of shape (B, 1, q_len, kv_seq_len) with kv_seq_len = P0 + T keeps the
+    causal order: query t (position P0 + t) sees keys 0..P0+t.  Returns out,
+    Delta and the new cache rows K/V [B, H, T, .], ckv, kpe [B, T, .].
+    ``query_rows`` (indices into the chunk) restricts the queries.
+    """
+    if scale is None:
+        scale = default_scale(dims)
+    B, T, _ = x.shape
+    P0 = K_cache.shape[2]
+    rows = np.arange(T) if query_rows is None else np.asarray(query_rows)
+    pos = P0 + np.arange(T)
+    kv = project_tokens(w, x, pos[None, :], dims, eps, base, want_q=False)
+    qp = project_tokens(w, x[:, rows], (P0 + rows)[None, :], dims, eps, base, want_q=True)
+    O = np.empty((B, len(rows), dims.H, dims.v))
+    for b in range(B):
+        for h in range(dims.H):
+            K = np.concatenate([K_cache[b, h], kv["K"][b, :, h]], axis=0)
+            V = np.concatenate([V_cache[b, h], kv["V"][b, :, h]], axis=0)
+            O[b, :, h] = attend(qp["Q"][b, :, h], K, V, scale, P0 + rows)
+    delta = _linear(O.reshape(B, len(rows), dims.H * dims.v), w["w_o"])
+    return {
+        "out": x[:, rows] + delta,
+        "delta": delta,
+        "K": np.ascontiguousarray(kv["K"].transpose(0, 2, 1, 3)),
+        "V": np.ascontiguousarray(kv["V"].transpose(0, 2, 1, 3)),
+        "ckv": kv["ckv"],
+        "kpe": kv["kpe"],
+    }
+
+
 def decode(w: dict, x_new: np.ndarray, K_cache: np.ndarray, V_cache: np.ndarray,
            dims: Dims = KIMI_K2, eps: float = DEFAULT_EPS, base: float = DEFAULT_ROPE_BASE,
            scale: float | None = None) -> dict:

@@ -316,6 +316,50 @@ def test_prefill_last_row_equals_decode(T):
     np.testing.assert_allclose(lat["out"], pre["out"][:, T - 1], rtol=1e-11, atol=1e-12)
 
 
+@pytest.mark.parametrize("T1,T2", [(1, 5), (4, 3), (6, 1)])
+def test_chunked_prefill_equals_whole_prefill(T1, T2):
+    """Prefill of T1 tokens, then a chunk of T2 tokens against the first
+    T1's cache, reproduces one prefill of all T1 + T2 tokens: the chunk's
+    positions start at T1 and its causal mask is offset by T1."""
+    dims = TINY2
+    w = rand_weights(dims, 61)
+    x = rand_x((2, T1 + T2, dims.d), 62)
+    whole = om.prefill(w, x, dims)
+    cache = om.cache_from_tokens(w, x[:, :T1], dims)
+    ch = om.prefill_with_past(w, x[:, T1:], cache["K"], cache["V"], dims)
+    np.testing.assert_allclose(ch["out"], whole["out"][:, T1:], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(ch["K"], whole["K"][:, :, T1:], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(ch["V"], whole["V"][:, :, T1:], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(ch["ckv"], whole["ckv"][:, T1:], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(ch["kpe"], whole["kpe"][:, T1:], rtol=1e-12, atol=1e-13)
+
+
+def test_one_token_chunk_equals_decode():
+    dims = TINY2
+    w = rand_weights(dims, 63)
+    cache = om.cache_from_tokens(w, rand_x((3, 7, dims.d), 64), dims)
+    xn = rand_x((3, dims.d), 65)
+    dec = om.decode(w, xn, cache["K"], cache["V"], dims)
+    ch = om.prefill_with_past(w, xn[:, None], cache["K"], cache["V"], dims)
+    np.testing.assert_allclose(ch["out"][:, 0], dec["out"], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(ch["K"][:, :, 0], dec["k_new"], rtol=1e-12, atol=1e-13)
+
+
+def test_chunk_mask_without_offset_fails_the_pin(monkeypatch):
+    """A planted mistake (the chunk's causal mask not offset by the past
+    length) is caught by the whole-prefill pin."""
+    dims = TINY2
+    w = rand_weights(dims, 66)
+    x = rand_x((1, 7, dims.d), 67)
+    whole = om.prefill(w, x, dims)
+    cache = om.cache_from_tokens(w, x[:, :4], dims)
+    real_attend = om.attend
+    monkeypatch.setattr(om, "attend", lambda Q, K, V, scale, q_pos: real_attend(
+        Q, K, V, scale, None if q_pos is None else np.asarray(q_pos) - K.shape[0] + Q.shape[0]))
+    bad = om.prefill_with_past(w, x[:, 4:], cache["K"], cache["V"], dims)
+    assert not np.allclose(bad["out"], whole["out"][:, 4:], rtol=1e-6, atol=1e-8)
+
+
 def test_latent_absorbed_equals_rebuilt():
     dims = TINY2
     w = rand_weights(dims, 39)
