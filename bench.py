@@ -43,11 +43,12 @@ def proj_flops_per_token():
     return 2 * (D * (QL + KVL + ROPE) + QL * H * QK + KVL * H * (NOPE + V) + H * V * D)
 
 
-def prefill_attn_flops(B, T):
-    return B * T * (T + 1) // 2 * 2 * (QK + V) * H
+def prefill_attn_flops(B, T, P0=0):
+    """Query t of a chunk after P0 cached positions scores P0 + t + 1 keys."""
+    return B * (T * P0 + T * (T + 1) // 2) * 2 * (QK + V) * H
 
 
-def stage_work(name, mode, B, T_or_P):
+def stage_work(name, mode, B, T_or_P, past=0):
     """(kind, amount) of algorithmic work of one stage launch: ("flop", F) or ("byte", Bytes)."""
     n = B * T_or_P if mode == "prefill" else B
     if name == "a_proj":
@@ -59,7 +60,7 @@ def stage_work(name, mode, B, T_or_P):
     if name == "o_proj":
         return ("flop", 2 * n * H * V * D)
     if name == "attn" and mode == "prefill":
-        return ("flop", prefill_attn_flops(B, T_or_P))
+        return ("flop", prefill_attn_flops(B, T_or_P, past))
     if name == "attn" and mode == "decode":
         L = T_or_P + 1
         return ("byte", B * H * L * (QK + V) * 2)
@@ -277,6 +278,20 @@ class Runner:
             m.mla_prefill(self.W, x, out, ws, *caches, cap, m.make_params(timing=timing))
         return step
 
+    def chunk_step_fn(self, B, P0, T):
+        """Chunked prefill of T tokens after P0 positions already in the
+        rebuilt cache (written by the library's cache-only prefill of the
+        seeded 'cache_x' tokens); every step rewrites rows P0..P0+T-1."""
+        torch, m, synth = self.torch, self.m, self.synth
+        kc, vc = self.fill_caches(B, P0, P0 + T, rebuilt=True)
+        x = synth.tensor_cuda(0, "x", (B, T, D), synth.X_DIST, device=self.dev)
+        out = torch.empty_like(x)
+        ws = m.alloc_workspace(m.MODE_PREFILL, B, T, device=self.dev)
+
+        def step(timing):
+            m.mla_prefill_chunk(self.W, x, P0, out, kc, vc, ws, params=m.make_params(timing=timing))
+        return step, (kc, vc, x, out, ws)
+
     # ---- decode -------------------------------------------------------------
     def fill_caches(self, B, P, cap, rebuilt, chunk_tokens=1 << 17):
         """Caches of positions 0..P-1 written by the library's own prefill
@@ -319,14 +334,14 @@ DECODE_STAGES = ("input_norm", "a_proj", "latent", "q_b", "kv_b", "attn", "o_pro
 LATENT_STAGES = ("input_norm", "a_proj", "latent", "q_b", "absorb_q", "attn", "absorb_o", "o_proj")
 
 
-def roofline_entry(stage_ms, mode, B, TP, pk, config_name):
+def roofline_entry(stage_ms, mode, B, TP, pk, config_name, past=0):
     """Roofline of the dominant stage, timed by events around it in every
     timed step."""
     if "_dominant_timed" not in stage_ms:
         return None
     name, ms = stage_ms["_dominant_timed"]
     total = sum(v for k, v in stage_ms.items() if not k.startswith("_"))
-    kind, amount = stage_work(name, mode, B, TP)
+    kind, amount = stage_work(name, mode, B, TP, past)
     if kind == "flop":
         ach = amount / (ms * 1e-3) / 1e12
         peak = pk["bf16_tflops"]
@@ -400,19 +415,23 @@ def run_profile(args):
     cudaProfilerStart and cudaProfilerStop (nothing is timed or reported)."""
     import re
     import torch
-    mt = re.fullmatch(r"(prefill|decode|latent)_b(\d+)_([tp])(\d+)(_cache)?", args.profile)
-    if not mt:
-        raise SystemExit(f"--profile: unknown configuration {args.profile!r}")
-    kind, B, n, cache = mt.group(1), int(mt.group(2)), int(mt.group(4)), bool(mt.group(5))
     torch.cuda.set_device(0)
     r = Runner("cuda:0")
     keep = None
-    if kind == "prefill":
-        x, out, ws, caches = r.prefill_setup(B, n, with_cache=cache)
-        step = r.prefill_step_fn(x, out, ws, caches, n)
-        keep = (x, out, ws, caches)
+    mc = re.fullmatch(r"chunk_b(\d+)_p(\d+)_t(\d+)", args.profile)
+    mt = re.fullmatch(r"(prefill|decode|latent)_b(\d+)_([tp])(\d+)(_cache)?", args.profile)
+    if mc:
+        step, keep = r.chunk_step_fn(int(mc.group(1)), int(mc.group(2)), int(mc.group(3)))
+    elif not mt:
+        raise SystemExit(f"--profile: unknown configuration {args.profile!r}")
     else:
-        step, keep = r.decode_step_fn(B, n, rebuilt=(kind == "decode"))
+        kind, B, n, cache = mt.group(1), int(mt.group(2)), int(mt.group(4)), bool(mt.group(5))
+        if kind == "prefill":
+            x, out, ws, caches = r.prefill_setup(B, n, with_cache=cache)
+            step = r.prefill_step_fn(x, out, ws, caches, n)
+            keep = (x, out, ws, caches)
+        else:
+            step, keep = r.decode_step_fn(B, n, rebuilt=(kind == "decode"))
     for _ in range(args.warmup):
         step(None)
     torch.cuda.synchronize()
@@ -435,6 +454,7 @@ def main():
                     help="tokens of the headline sequence the CPU oracle baseline runs (0 = skip)")
     ap.add_argument("--profile", default=None,
                     help="run one step of one configuration for a profiler and exit: prefill_bB_tT[_cache], "
+                         "chunk_bB_pP0_tT (chunked prefill after P0 cached positions), "
                          "decode_bB_pP (rebuilt cache) or latent_bB_pP; only that step lies between "
                          "cudaProfilerStart/Stop (ncu --profile-from-start off)")
     args = ap.parse_args()
@@ -562,6 +582,25 @@ def main():
             torch.cuda.empty_cache()
         except Exception as e:
             line["prefill_large"] = {"error": repr(e)[:300]}
+        # ---- chunked prefill: B=1, 2048 tokens after 2048 cached positions ----------
+        try:
+            B6, P6, T6 = 1, 2048, 2048
+            step6, keep = r.chunk_step_fn(B6, P6, T6)
+            ms6, st6, l6 = r.time_steps(step6, ks, W, stages=PREFILL_STAGES)
+            ms6 = barrier_max(statistics.mean(ms6))
+            fl6 = B6 * T6 * proj_flops_per_token() + prefill_attn_flops(B6, T6, P6)
+            line["prefill_chunk"] = {
+                "workload": "mla_prefill_chunk B=1 T=2048 after P0=2048 cached positions (rebuilt K/V cache)",
+                "ms_per_step": round(ms6, 4), "tokens_per_s": round(world * B6 * T6 / (ms6 * 1e-3), 1),
+                "tflops": round(fl6 / (ms6 * 1e-3) / 1e12, 2),
+                "frac_bf16_peak": round(fl6 / (ms6 * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+                "stage_ms": _stages_out(st6),
+                "roofline": roofline_entry(st6, "prefill", B6, T6, pk, "chunk_b1_p2048_t2048", past=P6),
+                "launches": l6}
+            del step6, keep
+            torch.cuda.empty_cache()
+        except Exception as e:
+            line["prefill_chunk"] = {"error": repr(e)[:300]}
 
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----------------------------------
     if world == 1 and args.cpu_tokens > 0:

@@ -142,6 +142,25 @@ int mla_prefill(const mla_weights_t* w, const mla_params_t* params, const void* 
                 void* out, void* k_cache, void* v_cache, void* ckv_cache, void* kpe_cache, int cap,
                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* Chunked prefill: T new tokens per sequence at positions P0..P0+T-1, after
+ * P0 tokens already in the rebuilt cache ("Mix and project" page: the cache
+ * update appends the new keys and values after the cached ones, and the
+ * additive mask of shape (B, 1, q_len, kv_seq_len), kv_seq_len = P0 + T,
+ * keeps the causal order: token t sees keys 0..P0+t).
+ *   x         [B, T, 7168]        the chunk's tokens
+ *   out       [B, T, 7168]        x + Delta_attn (may alias x exactly)
+ *   k_cache   [B, 64, cap, 192]   rows 0..P0-1 are read, rows P0..P0+T-1 written
+ *   v_cache   [B, 64, cap, 128]   same (both required)
+ *   ckv_cache, kpe_cache          optional latent cache, rows P0..P0+T-1 written
+ * Requires P0 >= 0 and P0 + T <= cap; the workspace is that of
+ * mla_workspace_size(MLA_MODE_PREFILL, B, T, cap).  P0 = 0 computes what
+ * mla_prefill computes with caches.
+ * Errors: INVALID_ARG (null or missing K/V cache, P0 < 0, P0 + T > cap),
+ * ALIGNMENT, WORKSPACE, CUDA. */
+int mla_prefill_chunk(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int T,
+                      int P0, void* out, void* k_cache, void* v_cache, void* ckv_cache, void* kpe_cache,
+                      int cap, void* workspace, size_t workspace_bytes, void* stream);
+
 /* One decode step against the rebuilt per-head cache (the pinned
  * implementation's cache, "Mix and project" page at P = 1,000).
  *   x        [B, 7168]           the new token of each sequence, at position P

@@ -57,6 +57,8 @@ _SIGS = {
     "mla_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "mla_prefill": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _VP, _VP, _VP, _VP,
                          _VP, _I, _VP, _SZ, _VP]),
+    "mla_prefill_chunk": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _I, _VP, _VP,
+                               _VP, _VP, _VP, _I, _VP, _SZ, _VP]),
     "mla_decode": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _VP, _VP, _I, _VP,
                         _VP, _SZ, _VP]),
     "mla_decode_latent": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _VP, _VP, _I,
@@ -142,6 +144,18 @@ def mla_prefill(weights: MlaWeights, x, out, workspace, k_cache=None, v_cache=No
                            _ptr(out), _ptr(k_cache), _ptr(v_cache), _ptr(ckv_cache), _ptr(kpe_cache), cap,
                            _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "mla_prefill")
+
+
+def mla_prefill_chunk(weights: MlaWeights, x, P0: int, out, k_cache, v_cache, workspace, ckv_cache=None,
+                      kpe_cache=None, params: MlaParams | None = None, stream=None):
+    """x, out: bf16 [B, T, 7168], the chunk at positions P0..P0+T-1; k_cache [B, 64, cap, 192] and
+    v_cache [B, 64, cap, 128] hold rows 0..P0-1 and receive rows P0..P0+T-1."""
+    B, T = x.shape[0], x.shape[1]
+    cap = k_cache.shape[2]
+    rc = lib().mla_prefill_chunk(ctypes.byref(weights), None if params is None else ctypes.byref(params), _ptr(x),
+                                 B, T, P0, _ptr(out), _ptr(k_cache), _ptr(v_cache), _ptr(ckv_cache),
+                                 _ptr(kpe_cache), cap, _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "mla_prefill_chunk")
 
 
 def mla_decode(weights: MlaWeights, x, P: int, k_cache, v_cache, out, workspace,

@@ -316,14 +316,21 @@ int mla_device_status(const void* workspace, void* stream) {
   return (word & kStatusTimeout) ? MLA_ERR_TIMEOUT : MLA_OK;
 }
 
-int mla_prefill(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int T, void* out,
-                void* k_cache, void* v_cache, void* ckv_cache, void* kpe_cache, int cap, void* workspace,
-                size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Prefill of T tokens per sequence at positions P0..P0+T-1; P0 > 0 (chunked
+// prefill) attends to the P0 cached keys before the chunk's own.
+int prefill_impl(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int T, int P0,
+                 void* out, void* k_cache, void* v_cache, void* ckv_cache, void* kpe_cache, int cap,
+                 void* workspace, size_t workspace_bytes, void* stream) {
   const Params p = resolve(params);
-  if (B < 1 || T < 1 || (int64_t)B * T > kMaxTokens) return MLA_ERR_INVALID_ARG;
+  if (B < 1 || T < 1 || P0 < 0 || (int64_t)B * T > kMaxTokens) return MLA_ERR_INVALID_ARG;
   if ((k_cache == nullptr) != (v_cache == nullptr)) return MLA_ERR_INVALID_ARG;
   if ((ckv_cache == nullptr) != (kpe_cache == nullptr)) return MLA_ERR_INVALID_ARG;
-  if ((k_cache || ckv_cache) && cap < T) return MLA_ERR_INVALID_ARG;
+  if ((k_cache || ckv_cache) && (int64_t)P0 + T > cap) return MLA_ERR_INVALID_ARG;
+  if (P0 > 0 && (!k_cache || !out)) return MLA_ERR_INVALID_ARG;
   for (const void* c : {(const void*)k_cache, (const void*)v_cache, (const void*)ckv_cache, (const void*)kpe_cache})
     if (c && !aligned16(c)) return MLA_ERR_ALIGNMENT;
   const size_t n_tok = (size_t)B * T;
@@ -342,7 +349,7 @@ int mla_prefill(const mla_weights_t* w, const mla_params_t* params, const void* 
   int launches = 0;
   if (cudaMemsetAsync(st.word, 0, kStatusRegion, stream_) != cudaSuccess) return MLA_ERR_CUDA;
 
-  rc = front_end(w, p, x, (int)n_tok, T, 0, T, 0, static_cast<__nv_bfloat16*>(ckv_cache),
+  rc = front_end(w, p, x, (int)n_tok, T, P0, T, P0, static_cast<__nv_bfloat16*>(ckv_cache),
                  static_cast<__nv_bfloat16*>(kpe_cache), cap, workspace, L, st, sms, stream_, sg, &launches,
                  !cache_only);
   if (rc) return rc;
@@ -355,7 +362,7 @@ int mla_prefill(const mla_weights_t* w, const mla_params_t* params, const void* 
   __nv_bfloat16* vc = v_cache ? static_cast<__nv_bfloat16*>(v_cache) : at<__nv_bfloat16>(workspace, L.vscr);
   const int kcap = k_cache ? cap : T;
   sg.start(MLA_STAGE_KV_B);
-  rc = kv_b_stage(w, (int)n_tok, T, 0, kc, vc, kcap, workspace, L, st, sms, stream_, &launches);
+  rc = kv_b_stage(w, (int)n_tok, T, P0, kc, vc, kcap, workspace, L, st, sms, stream_, &launches);
   if (rc) return rc;
   sg.stop(MLA_STAGE_KV_B);
   if (cache_only) {
@@ -366,7 +373,7 @@ int mla_prefill(const mla_weights_t* w, const mla_params_t* params, const void* 
   sg.start(MLA_STAGE_ATTN);
   {
     PrefillAttnArgs a{at<__nv_bfloat16>(workspace, L.q), kc, vc, at<__nv_bfloat16>(workspace, L.o), B, T, kcap,
-                      p.scale};
+                      p.scale, P0};
     if (launch_prefill_attention(a, st, sms, stream_) != cudaSuccess) return MLA_ERR_CUDA;
     launches += 1;
   }
@@ -378,6 +385,25 @@ int mla_prefill(const mla_weights_t* w, const mla_params_t* params, const void* 
   sg.stop(MLA_STAGE_O_PROJ);
   if (p.timing) p.timing->n_launches = launches;
   return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_prefill(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int T, void* out,
+                void* k_cache, void* v_cache, void* ckv_cache, void* kpe_cache, int cap, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  return prefill_impl(w, params, x, B, T, 0, out, k_cache, v_cache, ckv_cache, kpe_cache, cap, workspace,
+                      workspace_bytes, stream);
+}
+
+int mla_prefill_chunk(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int T, int P0,
+                      void* out, void* k_cache, void* v_cache, void* ckv_cache, void* kpe_cache, int cap,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (!k_cache || !v_cache || !out) return MLA_ERR_INVALID_ARG;
+  return prefill_impl(w, params, x, B, T, P0, out, k_cache, v_cache, ckv_cache, kpe_cache, cap, workspace,
+                      workspace_bytes, stream);
 }
 
 int mla_decode(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int P, void* k_cache,

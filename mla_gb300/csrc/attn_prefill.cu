@@ -6,6 +6,9 @@
 // global memory).
 //
 // CTA = (128-query tile, head, sequence), heaviest tiles launched first.
+// Chunked prefill: the queries sit at positions past..past+T-1 and attend to
+// keys 0..past+T-1 of the cache (the chunk's own keys written after the
+// cached ones), the causal mask offset by past.
 // Warp roles (256 threads):
 //   warp 0   TMA: the Q tile once, then K tiles into a 2-slot ring
 //   warp 6   TMA: V tiles into a 2-slot ring (each K and V tile is requested
@@ -60,7 +63,7 @@ struct Bars {
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ o, int T, int n_qt,
-                    float sl2, const DevStatus st) {
+                    float sl2, int past, const DevStatus st) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bar = reinterpret_cast<Bars*>(smem + kBarOff);
@@ -70,7 +73,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h = blockIdx.y;
   const int b = blockIdx.z;
   const int q0 = qt * 128;
-  const int n_kv = qt + 1;
+  // keys 0 .. past + q0 + 127 (the tile's last query), at most past + T of them
+  const int n_kv = min((past + q0 + 127) / 128 + 1, (past + T + 127) / 128);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -239,14 +243,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(ta + 96, s3);
         tmem_wait_ld();
       }
-      const bool diag = (j == n_kv - 1);
       const int k0 = j * 128;
-      // max of the raw scores (the scale is positive), causal mask on the
-      // diagonal tile only
-      if (diag) {
+      // max of the raw scores (the scale is positive), causal mask (key k
+      // visible to query position past + qpos iff k <= past + qpos) on the
+      // tiles that reach beyond the tile's first query
+      if (k0 + 127 > past + q0) {
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          if (k0 + c > qpos) s[c] = __float_as_uint(-INFINITY);
+          if (k0 + c > past + qpos) s[c] = __float_as_uint(-INFINITY);
       }
       // eight independent partial maxima / sums keep the reductions off a
       // single serial dependency chain
@@ -343,9 +347,10 @@ cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, const DevStatusHo
                                      cudaStream_t stream) {
   (void)num_sms;
   CUtensorMap tq, tk, tv;
+  const uint64_t n_keys = (uint64_t)a.past + a.T;  // key positions beyond read as zeros
   if (!make_tmap_bf16_3d(&tq, a.q, 12288, a.T, a.B, 12288ull * 2, (uint64_t)a.T * 12288 * 2, 64, 128) ||
-      !make_tmap_bf16_3d(&tk, a.k, 192, a.T, (uint64_t)a.B * 64, 384, (uint64_t)a.cap * 384, 64, 128) ||
-      !make_tmap_bf16_3d(&tv, a.v, 128, a.T, (uint64_t)a.B * 64, 256, (uint64_t)a.cap * 256, 64, 128))
+      !make_tmap_bf16_3d(&tk, a.k, 192, n_keys, (uint64_t)a.B * 64, 384, (uint64_t)a.cap * 384, 64, 128) ||
+      !make_tmap_bf16_3d(&tv, a.v, 128, n_keys, (uint64_t)a.B * 64, 256, (uint64_t)a.cap * 256, 64, 128))
     return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
@@ -357,7 +362,7 @@ cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, const DevStatusHo
   dim3 grid(n_qt, 64, a.B);
   DevStatus dst{st.word, st.wait_limit_ns};
   return launch_pdl(prefill_attn_tc, grid, dim3(kThreads), kSmemBytes, stream, tq, tk, tv, a.o, a.T, n_qt,
-                    a.scale * 1.4426950408889634f, dst);
+                    a.scale * 1.4426950408889634f, a.past, dst);
 }
 
 }  // namespace mla

@@ -174,12 +174,13 @@ cudaError_t launch_latent_split(const LatentArgs& a, cudaStream_t stream);
 
 // ---- attention ----------------------------------------------------------------
 struct PrefillAttnArgs {
-  const __nv_bfloat16* q;   // [B*T, 64*192]
-  const __nv_bfloat16* k;   // [B, 64, cap, 192]
+  const __nv_bfloat16* q;   // [B*T, 64*192], queries at positions past..past+T-1
+  const __nv_bfloat16* k;   // [B, 64, cap, 192], keys 0..past+T-1
   const __nv_bfloat16* v;   // [B, 64, cap, 128]
   __nv_bfloat16* o;         // [B*T, 64*128]
   int B, T, cap;
   float scale;
+  int past;                 // keys before the first query (chunked prefill), 0 otherwise
 };
 cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, const DevStatusHost& st, int num_sms,
                                      cudaStream_t stream);

@@ -19,6 +19,11 @@ REL_FRO = 1e-2
 # above 2e-2 for |v| >= 8.  For caches the element bound is therefore
 # 2e-2 + 2^-8 |ref| (one bf16 unit in the last place of the reference).
 CACHE_ULP_REL = 2.0 ** -8
+# The sublayer output out = x + Delta is bf16 storage too: rounding the exact
+# sum moves it by up to half a bf16 unit in the last place (2^-9 |out|), which
+# comes on top of the 2e-2 bound on the computed value (|out| reaches ~6, where
+# half a unit is 0.0156).  Delta itself (float32) is held to 2e-2 alone.
+OUT_ULP_REL = 2.0 ** -9
 
 
 @functools.lru_cache(maxsize=2)
@@ -72,3 +77,7 @@ def parity(got: np.ndarray, ref: np.ndarray, what: str, max_abs: float = MAX_ABS
 
 def parity_cache(got, ref, what):
     return parity(got, ref, what, ulp_rel=CACHE_ULP_REL)
+
+
+def parity_out(got, ref, what):
+    return parity(got, ref, what, ulp_rel=OUT_ULP_REL)

@@ -4,13 +4,15 @@ times, on sampled outputs the oracle can compute one by one.
 * prefill B=1, T=2048 and prefill B=8, T=4096 (both caches written): the
   GPU runs the whole batch; the oracle projects keys/values for every token
   of the sampled sequences and queries only at sampled positions.
+* chunked prefill B=1, T=2048 after P0=2048 cached positions (oracle-built
+  caches), sampled query rows.
 * decode B=64, P=1000 (rebuilt cache) and latent decode B=128, P=8192: the
   GPU fills every cache with its own cache-only prefill of the seeded
   'cache_x' tokens (checked against the oracle's caches for the sampled
   sequences), then the sampled sequences' cache rows are replaced by the
   oracle's bf16 caches so both sides decode from identical inputs.
 Tolerance as in test_parity_small (max abs <= 2e-2, rel. Frobenius <= 1e-2;
-cache entries one bf16 ulp more).
+cache entries one bf16 ulp more, the bf16 output half an ulp more).
 """
 import numpy as np
 import pytest
@@ -18,7 +20,8 @@ import pytest
 import synth
 from oracle import mla_oracle as om
 import mla_gb300 as m
-from mla_testlib import bits_to_cuda, cuda_to_f64, cuda_weights, f64_to_bits, oracle_weights, parity, parity_cache
+from mla_testlib import (bits_to_cuda, cuda_to_f64, cuda_weights, f64_to_bits, oracle_weights, parity, parity_cache,
+                         parity_out)
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +52,7 @@ def _prefill_case(W, B, T, b_samples, t_samples, with_cache):
     for b in b_samples:
         xb = synth.bf16_bits_to_f64(synth.tensor_bits(0, "x", (B, T, D), synth.X_DIST, rows=[b]))
         ref = om.prefill(W[2], xb, query_rows=t_samples)
-        parity(cuda_to_f64(out[b, t_samples]), ref["out"][0], f"out b={b}")
+        parity_out(cuda_to_f64(out[b, t_samples]), ref["out"][0], f"out b={b}")
         parity(cuda_to_f64(delta[b, t_samples]), ref["delta"][0], f"delta b={b}")
         if with_cache:
             kc, vc, ckv, kpe = caches
@@ -65,6 +68,35 @@ def test_prefill_b1_t2048(W):
 
 def test_prefill_b8_t4096_with_caches(W):
     _prefill_case(W, 8, 4096, [0, 5], [0, 129, 2048, 4095], with_cache=True)
+
+
+def test_prefill_chunk_b1_p2048_t2048(W):
+    """Chunked prefill of 2048 tokens after 2048 cached positions (the
+    bench's chunk workload): the caches hold the oracle's bf16 rows of the
+    seeded 'cache_x' tokens; sampled query rows on both sides."""
+    import torch
+    B, P0, T = 1, 2048, 2048
+    cap = P0 + T
+    xc = synth.bf16_bits_to_f64(synth.tensor_bits(0, "cache_x", (B, P0, D), synth.X_DIST))
+    c = om.cache_from_tokens(W[2], xc)
+    Kb, Vb = f64_to_bits(c["K"]), f64_to_bits(c["V"])
+    kc = torch.zeros((B, 64, cap, 192), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros((B, 64, cap, 128), dtype=torch.bfloat16, device="cuda")
+    kc[:, :, :P0].copy_(bits_to_cuda(Kb))
+    vc[:, :, :P0].copy_(bits_to_cuda(Vb))
+    x = synth.tensor_cuda(0, "x", (B, T, D), synth.X_DIST)
+    out = torch.empty_like(x)
+    ws = m.alloc_workspace(m.MODE_PREFILL, B, T)
+    m.mla_prefill_chunk(W[1], x, P0, out, kc, vc, ws)
+    torch.cuda.synchronize()
+    assert m.mla_device_status(ws) == 0
+    rows = [0, 1, 127, 128, 1000, 2046, 2047]
+    xb = synth.bf16_bits_to_f64(synth.tensor_bits(0, "x", (B, T, D), synth.X_DIST))
+    ref = om.prefill_with_past(W[2], xb, synth.bf16_bits_to_f64(Kb), synth.bf16_bits_to_f64(Vb),
+                               query_rows=rows)
+    parity_out(cuda_to_f64(out[0, rows]), ref["out"][0], "chunk out")
+    parity_cache(cuda_to_f64(kc[0][:, [P0 + r for r in rows]]), ref["K"][0][:, rows], "chunk K rows")
+    parity_cache(cuda_to_f64(vc[0][:, [P0 + r for r in rows]]), ref["V"][0][:, rows], "chunk V rows")
 
 
 def _fill_caches(W, B, P, cap, rebuilt):
@@ -117,7 +149,7 @@ def test_decode_b64_p1000(W):
     xn = synth.bf16_bits_to_f64(synth.tensor_bits(0, "new_x", (B, D), synth.X_DIST))
     for b in samples:
         ref = om.decode(W[2], xn[b:b + 1], *refs[b])
-        parity(cuda_to_f64(out[b:b + 1]), ref["out"], f"decode out b={b}")
+        parity_out(cuda_to_f64(out[b:b + 1]), ref["out"], f"decode out b={b}")
         parity(cuda_to_f64(delta[b:b + 1]), ref["delta"], f"decode delta b={b}")
         parity_cache(cuda_to_f64(kc[b:b + 1, :, P]), ref["k_new"], f"new K row b={b}")
         parity_cache(cuda_to_f64(vc[b:b + 1, :, P]), ref["v_new"], f"new V row b={b}")
@@ -149,7 +181,7 @@ def test_decode_latent_b128_p8192(W):
     xn = synth.bf16_bits_to_f64(synth.tensor_bits(0, "new_x", (B, D), synth.X_DIST))
     for b in samples:
         ref = om.decode_latent(W[2], xn[b:b + 1], *refs[b])
-        parity(cuda_to_f64(out[b:b + 1]), ref["out"], f"latent decode out b={b}")
+        parity_out(cuda_to_f64(out[b:b + 1]), ref["out"], f"latent decode out b={b}")
         parity(cuda_to_f64(delta[b:b + 1]), ref["delta"], f"latent decode delta b={b}")
         parity_cache(cuda_to_f64(ckv[b:b + 1, P]), ref["ckv_new"], f"new latent row b={b}")
         parity_cache(cuda_to_f64(kpe[b:b + 1, P]), ref["kpe_new"], f"new rotary-key row b={b}")

@@ -3,7 +3,8 @@
 Full Kimi K2 dimensions (d = 7168, 64 heads, ...); seeded synthetic inputs
 from ``synth`` on both sides; tolerance max abs <= 2e-2 and relative
 Frobenius <= 1e-2 on out, Delta_attn (o_proj output before the residual)
-and every cache the call writes.  Shapes span several GEMM tiles (128 rows)
+and every cache the call writes, plus the rounding of bf16 storage (half a
+unit in the last place for out, one for cache entries).  Shapes span several GEMM tiles (128 rows)
 and attention tiles with ragged tails, plus the degenerate cases T = 1,
 P = 0 and out aliasing x.
 """
@@ -14,7 +15,7 @@ import synth
 from oracle import mla_oracle as om
 import mla_gb300 as m
 from mla_testlib import (bits_to_cuda, cuda_to_f64, cuda_weights, f64_to_bits, oracle_weights, parity,
-                         parity_cache)
+                         parity_cache, parity_out)
 
 pytestmark = pytest.mark.gpu
 
@@ -50,7 +51,7 @@ def test_prefill_parity(W, B, T):
     x64, out, delta, kc, vc, ckv, kpe = run_prefill(W, B, T)
     ref = om.prefill(W[2], x64)
     parity(cuda_to_f64(delta), ref["delta"], "delta")
-    parity(cuda_to_f64(out), ref["out"], "out")
+    parity_out(cuda_to_f64(out), ref["out"], "out")
     parity_cache(cuda_to_f64(kc), ref["K"], "K cache")
     parity_cache(cuda_to_f64(vc), ref["V"], "V cache")
     parity_cache(cuda_to_f64(ckv), ref["ckv"], "latent cache")
@@ -61,7 +62,7 @@ def test_prefill_in_place_and_no_cache(W):
     B, T = 1, 70
     x64, out, delta, *_ = run_prefill(W, B, T, with_cache=False, inplace=True)
     ref = om.prefill(W[2], x64)
-    parity(cuda_to_f64(out), ref["out"], "out (in place)")
+    parity_out(cuda_to_f64(out), ref["out"], "out (in place)")
     parity(cuda_to_f64(delta), ref["delta"], "delta")
 
 
@@ -112,7 +113,7 @@ def test_decode_parity(W, B, P):
     assert m.mla_device_status(wsp) == 0
     ref = om.decode(W[2], synth.bf16_bits_to_f64(xb), K64, V64)
     parity(cuda_to_f64(delta), ref["delta"], "delta")
-    parity(cuda_to_f64(out), ref["out"], "out")
+    parity_out(cuda_to_f64(out), ref["out"], "out")
     parity_cache(cuda_to_f64(kc[:, :, P]), ref["k_new"], "new K row")
     parity_cache(cuda_to_f64(vc[:, :, P]), ref["v_new"], "new V row")
     # positions other than P are untouched
@@ -135,7 +136,7 @@ def test_decode_latent_parity(W, B, P):
     assert m.mla_device_status(wsp) == 0
     ref = om.decode_latent(W[2], synth.bf16_bits_to_f64(xb), C64, R64)
     parity(cuda_to_f64(delta), ref["delta"], "delta")
-    parity(cuda_to_f64(out), ref["out"], "out")
+    parity_out(cuda_to_f64(out), ref["out"], "out")
     parity_cache(cuda_to_f64(ckv[:, P]), ref["ckv_new"], "new latent row")
     parity_cache(cuda_to_f64(kpe[:, P]), ref["kpe_new"], "new rotary-key row")
 
@@ -161,7 +162,76 @@ def test_decode_latent_many_sequences(W):
     f = synth.bf16_bits_to_f64
     for b in [0, 1, 2, 3, 4, 131, 132, 133, 250, 251, 497, 498, 499]:
         ref = om.decode_latent(W[2], f(xb[b:b + 1]), f(Cb[b:b + 1, :P]), f(Rb[b:b + 1, :P]))
-        parity(cuda_to_f64(out[b:b + 1]), ref["out"], f"out b={b}")
+        parity_out(cuda_to_f64(out[b:b + 1]), ref["out"], f"out b={b}")
+
+
+@pytest.mark.parametrize("B,P0,T", [(2, 100, 37), (1, 128, 256), (1, 200, 300), (2, 0, 40), (3, 5, 1)])
+def test_prefill_chunk_parity(W, B, P0, T):
+    """Chunk of T tokens after P0 cached positions (oracle-built bf16 caches
+    on both sides): past % 128 != 0 puts the offset diagonal across two key
+    tiles; P0 = 0 is the plain prefill; T = 1 is a one-token chunk."""
+    import torch
+    cap = P0 + T + 3
+    (Kb, Vb, Cb, Rb), (K64, V64, _, _) = make_caches(W, B, P0, cap)
+    xb = synth.tensor_bits(0, "x", (B, T, 7168), synth.X_DIST)
+    x = bits_to_cuda(xb)
+    kc, vc, ckv, kpe = (bits_to_cuda(t) for t in (Kb, Vb, Cb, Rb))
+    out = torch.empty_like(x)
+    delta = torch.empty((B, T, 7168), dtype=torch.float32, device="cuda")
+    wsp = m.alloc_workspace(m.MODE_PREFILL, B, T)
+    m.mla_prefill_chunk(W[1], x, P0, out, kc, vc, wsp, ckv, kpe, m.make_params(delta_out=delta))
+    torch.cuda.synchronize()
+    assert m.mla_device_status(wsp) == 0
+    ref = om.prefill_with_past(W[2], synth.bf16_bits_to_f64(xb), K64, V64)
+    parity(cuda_to_f64(delta), ref["delta"], "delta")
+    parity_out(cuda_to_f64(out), ref["out"], "out")
+    parity_cache(cuda_to_f64(kc[:, :, P0:P0 + T]), ref["K"], "new K rows")
+    parity_cache(cuda_to_f64(vc[:, :, P0:P0 + T]), ref["V"], "new V rows")
+    parity_cache(cuda_to_f64(ckv[:, P0:P0 + T]), ref["ckv"], "new latent rows")
+    parity_cache(cuda_to_f64(kpe[:, P0:P0 + T]), ref["kpe"], "new rotary-key rows")
+    # rows before P0 and after P0 + T are untouched
+    bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(bits(kc[:, :, :P0]), Kb[:, :, :P0])
+    assert np.array_equal(bits(vc[:, :, :P0]), Vb[:, :, :P0])
+    assert np.array_equal(bits(ckv[:, :P0]), Cb[:, :P0])
+    assert torch.count_nonzero(kc[:, :, P0 + T:]).item() == 0
+    assert torch.count_nonzero(ckv[:, P0 + T:]).item() == 0
+
+
+def test_prefill_in_two_chunks_equals_whole_prefill(W):
+    """GPU prefill of the first T1 tokens, then a GPU chunk of the next T2
+    from the caches it wrote: every output row matches the oracle's prefill
+    of all T1 + T2 tokens."""
+    import torch
+    B, T1, T2 = 2, 70, 90
+    T = T1 + T2
+    xb = synth.tensor_bits(0, "x", (B, T, 7168), synth.X_DIST)
+    x = bits_to_cuda(xb)
+    kc = torch.zeros((B, 64, T, 192), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros((B, 64, T, 128), dtype=torch.bfloat16, device="cuda")
+    x1, x2 = x[:, :T1].contiguous(), x[:, T1:].contiguous()
+    o1, o2 = torch.empty_like(x1), torch.empty_like(x2)
+    m.mla_prefill(W[1], x1, o1, m.alloc_workspace(m.MODE_PREFILL, B, T1), kc, vc, None, None, T)
+    m.mla_prefill_chunk(W[1], x2, T1, o2, kc, vc, m.alloc_workspace(m.MODE_PREFILL, B, T2))
+    torch.cuda.synchronize()
+    ref = om.prefill(W[2], synth.bf16_bits_to_f64(xb))
+    parity_out(cuda_to_f64(torch.cat([o1, o2], dim=1)), ref["out"], "two chunks")
+    parity_cache(cuda_to_f64(kc), ref["K"], "K cache")
+
+
+def test_prefill_chunk_rejects_bad_arguments(W):
+    import torch
+    B, T, P0 = 1, 8, 10
+    x = torch.zeros((B, T, 7168), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(x)
+    kc = torch.zeros((B, 64, P0 + T, 192), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros((B, 64, P0 + T, 128), dtype=torch.bfloat16, device="cuda")
+    wsp = m.alloc_workspace(m.MODE_PREFILL, B, T)
+    for bad_p0 in (-1, P0 + 1):  # negative, or P0 + T beyond the cache capacity
+        with pytest.raises(m.MlaError):
+            m.mla_prefill_chunk(W[1], x, bad_p0, out, kc, vc, wsp)
+    with pytest.raises(m.MlaError):
+        m.mla_prefill_chunk(W[1], x, P0, None, kc, vc, wsp)
 
 
 def test_prefill_then_decode_chain(W):
@@ -186,5 +256,5 @@ def test_prefill_then_decode_chain(W):
     m.mla_decode_latent(W[1], xn, T - 1, ckv, kpe, o2, m.alloc_workspace(m.MODE_DECODE_LATENT, B, T - 1))
     torch.cuda.synchronize()
     ref = om.prefill(W[2], synth.bf16_bits_to_f64(xb), query_rows=[T - 1])["out"][:, 0]
-    parity(cuda_to_f64(o1), ref, "decode after prefill")
-    parity(cuda_to_f64(o2), ref, "latent decode after prefill")
+    parity_out(cuda_to_f64(o1), ref, "decode after prefill")
+    parity_out(cuda_to_f64(o2), ref, "latent decode after prefill")
