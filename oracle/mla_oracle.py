@@ -20,7 +20,7 @@ the only library primitive and no blocking or fusion:
   produces 512 latent + 64 rotary-key features, split after the product; only
   the 512-wide latent is normalised (kv_a_layernorm), the rotary key is not.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 * RMSNorm(x; g) = g * x / sqrt(mean(x^2) + eps) with eps = 1e-6 for all three
   norms (the module bodies are not printed).
 * q_b_proj output per head is [128 "nope" | 64 "pe"] in 192-wide blocks, the
@@ -341,3 +341,78 @@ def cache_from_tokens(w: dict, x: np.ndarray, dims: Dims = KIMI_K2, eps: float =
     return {"K": np.ascontiguousarray(t["K"].transpose(0, 2, 1, 3)),
             "V": np.ascontiguousarray(t["V"].transpose(0, 2, 1, 3)),
             "ckv": t["ckv"], "kpe": t["kpe"]}
+
+
+# ---------------------------------------------------------------------------
+# The block's second half: post-attention RMSNorm and the dense SwiGLU MLP
+# (dense-block page, equation list after x'_n = x_n + Delta_attn; the
+# DecoderLayer forward excerpt of the same page).
+# ---------------------------------------------------------------------------
+@dataclass(frozen=True)
+class FfnDims:
+    """Sizes of the dense SwiGLU MLP.  The pages print its parameter count,
+    396,361,728, not its width: three bias-free matrices d x I give
+    I = 396,361,728 / (3 * 7168) = 18,432."""
+    d: int = 7168
+    inter: int = 18432
+
+
+KIMI_K2_FFN = FfnDims()
+
+
+def ffn_weight_shapes(fd: FfnDims = KIMI_K2_FFN) -> dict:
+    """g_post: the MLP RMSNorm gain; w_1 (gate, g = x_ffn W_1) and w_3 (up,
+    u = x_ffn W_3) map d -> I, w_2 (Delta_ffn = h W_2) maps I -> d; stored
+    nn.Linear style [out, in]."""
+    return {
+        "g_post": (fd.d,),
+        "w_1": (fd.inter, fd.d),
+        "w_3": (fd.inter, fd.d),
+        "w_2": (fd.d, fd.inter),
+    }
+
+
+def ffn_param_count(fd: FfnDims = KIMI_K2_FFN) -> int:
+    """Parameters of the SwiGLU MLP row of the dense-block parameter table
+    (the MLP RMSNorm gain has its own row)."""
+    return sum(int(np.prod(s)) for k, s in ffn_weight_shapes(fd).items() if k != "g_post")
+
+
+def dense_block_param_count(dims: Dims = KIMI_K2, fd: FfnDims = KIMI_K2_FFN) -> int:
+    """Per-instance total of the dense-block parameter table: attention
+    RMSNorm + MLA + MLP RMSNorm + SwiGLU MLP."""
+    return dims.d + mla_param_count(dims) + fd.d + ffn_param_count(fd)
+
+
+def sigmoid(z: np.ndarray) -> np.ndarray:
+    """sigma(z) = 1 / (1 + e^-z), evaluated as (1 + tanh(z/2)) / 2, the same
+    function without overflow for large |z|."""
+    return 0.5 * (1.0 + np.tanh(0.5 * z))
+
+
+def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """The gating step of the SwiGLU MLP: a = g sigma(g) (SiLU of the gate),
+    h = a (.) u."""
+    a = g * sigmoid(g)
+    return a * u
+
+
+def ffn(w: dict, xp: np.ndarray, eps: float = DEFAULT_EPS) -> dict:
+    """x_{n+1} from x'_n (dense-block page): x_ffn = RMSNorm(x'_n);
+    g = x_ffn W_1; u = x_ffn W_3; a = g sigma(g); h = a (.) u;
+    Delta_ffn = h W_2; x_{n+1} = x'_n + Delta_ffn.  Any leading shape."""
+    x_ffn = rms_norm(xp, w["g_post"], eps)
+    g = _linear(x_ffn, w["w_1"])
+    u = _linear(x_ffn, w["w_3"])
+    h = swiglu(g, u)
+    delta = _linear(h, w["w_2"])
+    return {"out": xp + delta, "delta": delta, "h": h}
+
+
+def dense_block_prefill(w: dict, w_ffn: dict, x: np.ndarray, dims: Dims = KIMI_K2, eps: float = DEFAULT_EPS,
+                        base: float = DEFAULT_ROPE_BASE, scale: float | None = None) -> dict:
+    """The whole dense block on x [B, T, d] at positions 0..T-1 (DecoderLayer
+    forward excerpt): x' = x + MLA(RMSNorm(x)), then x_{n+1} = x' + MLP(RMSNorm(x'))."""
+    attn = prefill(w, x, dims, eps, base, scale)
+    f = ffn(w_ffn, attn["out"], eps)
+    return {"out": f["out"], "x_mid": attn["out"], "delta_attn": attn["delta"], "delta_ffn": f["delta"]}

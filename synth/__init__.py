@@ -49,6 +49,11 @@ STREAMS = {
     "w_o": 8,
     "cache_x": 9,      # hidden states whose projections fill a decode cache
     "new_x": 10,       # the new token's hidden state in decode
+    "w_post_norm": 11,  # the block's post-attention RMSNorm gain
+    "w_1": 12,         # SwiGLU MLP gate projection
+    "w_3": 13,         # SwiGLU MLP up projection
+    "w_2": 14,         # SwiGLU MLP down projection
+    "ffn_x": 15,       # hidden states fed to the MLP half on its own
 }
 
 # Distributions of the synthetic workload: (mean, std)
@@ -68,6 +73,25 @@ WEIGHT_SPECS = {
     "w_kv_b": ((16384, 512), WEIGHT_DIST),
     "w_o": ((7168, 8192), WEIGHT_DIST),
 }
+
+
+# The four tensors of the block's MLP half: post-attention RMSNorm gain and
+# the three bias-free SwiGLU matrices (intermediate width 18,432).
+FFN_WEIGHT_SPECS = {
+    "w_post_norm": ((7168,), GAIN_DIST),
+    "w_1": ((18432, 7168), WEIGHT_DIST),
+    "w_3": ((18432, 7168), WEIGHT_DIST),
+    "w_2": ((7168, 18432), WEIGHT_DIST),
+}
+
+
+def ffn_weight_bits(seed: int = 0) -> dict:
+    """bf16 bits of the MLP-half weights (about 396 M values)."""
+    return {n: tensor_bits(seed, n, shape, dist) for n, (shape, dist) in FFN_WEIGHT_SPECS.items()}
+
+
+def ffn_weights_cuda(seed: int = 0, device="cuda") -> dict:
+    return {n: tensor_cuda(seed, n, shape, dist, device) for n, (shape, dist) in FFN_WEIGHT_SPECS.items()}
 
 
 def weight_bits(seed: int = 0) -> dict:

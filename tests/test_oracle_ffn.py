@@ -1,0 +1,229 @@
+"""Pins for the oracle's second block half: post-attention RMSNorm and the
+dense SwiGLU MLP (no GPU).
+
+The oracle's ``ffn`` is checked against things other than itself:
+* the parameter table of the dense-block page (SwiGLU MLP 396,361,728, MLP
+  RMSNorm 7,168, block total 497,500,160; tests/golden/page_counts.json);
+* closed forms of the logistic function;
+* an element-by-element loop implementation at tiny sizes (math.exp, no
+  numpy matmul);
+* the gate's limits: a gate far below zero closes the unit whatever the up
+  projection holds, a gate far above zero leaves the bilinear map g (.) u;
+* the residual (W_2 = 0 gives the identity) and RMSNorm scale invariance;
+* the block composition (DecoderLayer forward): MLA half then MLP half.
+``test_planted_ffn_mistakes_are_caught`` plants plausible mistakes in the
+oracle and checks that these pins fail.
+"""
+import json
+import math
+import os
+
+import numpy as np
+
+from oracle import mla_oracle as om
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_counts.json")))
+
+TINY_FFN = om.FfnDims(d=6, inter=4)
+TINY = om.Dims(d=16, H=2, q_lora=8, kv_lora=8, nope=4, rope=4, v=4)
+
+
+def rand_ffn_weights(fd, seed, wstd=0.3):
+    rng = np.random.default_rng(seed)
+    w = {}
+    for name, shape in om.ffn_weight_shapes(fd).items():
+        w[name] = (1.0 + 0.1 * rng.standard_normal(shape)) if name.startswith("g_") else wstd * rng.standard_normal(shape)
+    return w
+
+
+def rand_x(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+# ---------------------------------------------------------------------------
+# printed numbers
+# ---------------------------------------------------------------------------
+def test_ffn_parameter_counts_match_page():
+    assert om.ffn_param_count() == GOLDEN["swiglu_mlp_parameters"]["value"]
+    assert om.ffn_weight_shapes()["g_post"][0] == GOLDEN["mlp_rmsnorm_parameters"]["value"]
+    assert om.dense_block_param_count() == GOLDEN["dense_block_parameters"]["value"]
+    # gate and up map d -> I, down maps I -> d (stored [out, in])
+    s = om.ffn_weight_shapes()
+    assert s["w_1"] == s["w_3"] == (18432, 7168) and s["w_2"] == (7168, 18432)
+
+
+# ---------------------------------------------------------------------------
+# closed forms
+# ---------------------------------------------------------------------------
+def test_sigmoid_closed_forms():
+    assert om.sigmoid(np.array(0.0)) == 0.5
+    assert abs(om.sigmoid(np.array(1.0)) - math.e / (1.0 + math.e)) < 1e-15
+    assert abs(om.sigmoid(np.array(-2.0)) - 1.0 / (1.0 + math.e ** 2)) < 1e-15
+    z = np.linspace(-30, 30, 121)
+    np.testing.assert_allclose(om.sigmoid(z) + om.sigmoid(-z), 1.0, atol=1e-15)
+    assert om.sigmoid(np.array(-800.0)) == 0.0 and om.sigmoid(np.array(800.0)) == 1.0
+
+
+def test_silu_odd_part_is_identity():
+    # SiLU(z) - SiLU(-z) = z (sigma(z) + sigma(-z) = 1); SiLU(0) = 0
+    z = np.linspace(-12, 12, 97)
+    one = np.ones_like(z)
+    np.testing.assert_allclose(om.swiglu(z, one) - om.swiglu(-z, one), z, atol=1e-13)
+    assert om.swiglu(np.array(0.0), np.array(5.0)) == 0.0
+
+
+# ---------------------------------------------------------------------------
+# brute force
+# ---------------------------------------------------------------------------
+def brute_ffn(w, xp, eps):
+    """Element-by-element loops: RMSNorm, gate/up dot products, SiLU with
+    math.exp, product, down dot products, residual."""
+    d = len(xp)
+    inter = len(w["w_1"])
+    ms = sum(v * v for v in xp) / d
+    r = 1.0 / math.sqrt(ms + eps)
+    xf = [w["g_post"][i] * xp[i] * r for i in range(d)]
+    h = []
+    for j in range(inter):
+        g = sum(xf[i] * w["w_1"][j][i] for i in range(d))
+        u = sum(xf[i] * w["w_3"][j][i] for i in range(d))
+        h.append(g / (1.0 + math.exp(-g)) * u)
+    delta = [sum(h[j] * w["w_2"][i][j] for j in range(inter)) for i in range(d)]
+    return [xp[i] + delta[i] for i in range(d)], delta
+
+
+def test_ffn_matches_brute_force():
+    for seed in range(3):
+        w = rand_ffn_weights(TINY_FFN, seed)
+        x = rand_x((2, 3, TINY_FFN.d), 10 + seed)
+        r = om.ffn(w, x, 1e-6)
+        wl = {k: v.tolist() for k, v in w.items()}
+        for b in range(2):
+            for t in range(3):
+                out, delta = brute_ffn(wl, x[b, t].tolist(), 1e-6)
+                np.testing.assert_allclose(r["out"][b, t], out, rtol=1e-12, atol=1e-12)
+                np.testing.assert_allclose(r["delta"][b, t], delta, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# the gate's limits, residual, scale invariance
+# ---------------------------------------------------------------------------
+def _saturated_gate_weights(sign):
+    w = rand_ffn_weights(TINY_FFN, 5)
+    w["g_post"] = np.ones(TINY_FFN.d)
+    w["w_1"] = sign * 20.0 * np.ones((TINY_FFN.inter, TINY_FFN.d))  # g = sign * 20 * sum(x_ffn)
+    return w
+
+
+def test_gate_far_below_zero_closes_the_unit():
+    w = _saturated_gate_weights(-1.0)
+    xp = np.ones((1, TINY_FFN.d))  # x_ffn ~ 1 everywhere: g ~ -120 for every unit
+    r = om.ffn(w, xp, 1e-6)
+    assert np.max(np.abs(r["delta"])) < 1e-40
+    np.testing.assert_array_equal(r["out"], xp + r["delta"])
+
+
+def test_gate_far_above_zero_leaves_the_bilinear_map():
+    w = _saturated_gate_weights(1.0)
+    xp = np.ones((1, TINY_FFN.d))
+    r = om.ffn(w, xp, 1e-6)
+    xf = xp / np.sqrt(1.0 + 1e-6)
+    g = 20.0 * xf.sum()                     # every unit's gate, ~ +120: SiLU(g) = g
+    u = xf @ w["w_3"].T
+    np.testing.assert_allclose(r["delta"], (g * u) @ w["w_2"].T, rtol=1e-12)
+
+
+def test_zero_down_projection_is_identity():
+    w = rand_ffn_weights(TINY_FFN, 7)
+    w["w_2"] = np.zeros_like(w["w_2"])
+    x = rand_x((3, TINY_FFN.d), 8)
+    np.testing.assert_array_equal(om.ffn(w, x)["out"], x)
+
+
+def test_delta_is_invariant_to_input_scale():
+    w = rand_ffn_weights(TINY_FFN, 9)
+    x = rand_x((4, TINY_FFN.d), 11)
+    d1 = om.ffn(w, x, 0.0)["delta"]
+    d2 = om.ffn(w, 7.5 * x, 0.0)["delta"]
+    np.testing.assert_allclose(d1, d2, rtol=1e-12, atol=1e-14)
+
+
+def test_rows_are_independent():
+    w = rand_ffn_weights(TINY_FFN, 12)
+    x = rand_x((5, TINY_FFN.d), 13)
+    full = om.ffn(w, x)["out"]
+    for i in range(5):
+        np.testing.assert_allclose(om.ffn(w, x[i:i + 1])["out"][0], full[i], rtol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# the block: MLA half then MLP half
+# ---------------------------------------------------------------------------
+def _block_weights():
+    rng = np.random.default_rng(21)
+    w = {}
+    for name, shape in om.weight_shapes(TINY).items():
+        w[name] = (1.0 + 0.1 * rng.standard_normal(shape)) if name.startswith("g_") else 0.3 * rng.standard_normal(shape)
+    wf = rand_ffn_weights(om.FfnDims(d=TINY.d, inter=12), 22)
+    return w, wf
+
+
+def test_block_is_attention_half_then_mlp_half():
+    w, wf = _block_weights()
+    x = rand_x((2, 5, TINY.d), 23)
+    blk = om.dense_block_prefill(w, wf, x, TINY)
+    # without the MLP's output projection the block is the attention half
+    wf0 = dict(wf, w_2=np.zeros_like(wf["w_2"]))
+    np.testing.assert_array_equal(om.dense_block_prefill(w, wf0, x, TINY)["out"], om.prefill(w, x, TINY)["out"])
+    # without o_proj the attention half is the identity: the block is the MLP half of x
+    w0 = dict(w, w_o=np.zeros_like(w["w_o"]))
+    np.testing.assert_allclose(om.dense_block_prefill(w0, wf, x, TINY)["out"], om.ffn(wf, x)["out"], rtol=1e-13)
+    # residual stream: x_{n+1} = x + Delta_attn + Delta_ffn
+    np.testing.assert_allclose(blk["out"], x + blk["delta_attn"] + blk["delta_ffn"], rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes
+# ---------------------------------------------------------------------------
+def _ffn_pins_pass():
+    try:
+        test_sigmoid_closed_forms()
+        test_silu_odd_part_is_identity()
+        test_ffn_matches_brute_force()
+        test_gate_far_below_zero_closes_the_unit()
+        test_gate_far_above_zero_leaves_the_bilinear_map()
+        test_delta_is_invariant_to_input_scale()
+    except AssertionError:
+        return False
+    return True
+
+
+def test_planted_ffn_mistakes_are_caught(monkeypatch):
+    assert _ffn_pins_pass()
+    orig_sig, orig_swiglu, orig_norm = om.sigmoid, om.swiglu, om.rms_norm
+    plants = [
+        ("sigmoid", lambda z: 0.5 * (1.0 - np.tanh(0.5 * z))),       # sign of the exponent
+        ("sigmoid", lambda z: 0.5 * (1.0 + np.tanh(z))),             # sigma(2z)
+        ("swiglu", lambda g, u: orig_swiglu(u, g)),                   # gate and up swapped
+        ("swiglu", lambda g, u: g * u),                               # SiLU dropped
+        ("swiglu", lambda g, u: g * orig_sig(g) + u),                 # sum instead of product
+        ("rms_norm", lambda x, g, eps: orig_norm(x, np.ones_like(g), eps)),  # gain dropped
+    ]
+    for name, fn in plants:
+        monkeypatch.setattr(om, name, fn)
+        assert not _ffn_pins_pass(), f"planted mistake in {name} not caught"
+        monkeypatch.setattr(om, name, {"sigmoid": orig_sig, "swiglu": orig_swiglu, "rms_norm": orig_norm}[name])
+    # down projection applied transposed-and-square (only expressible when d == I)
+    orig_ffn_lin = om._linear
+    sq = om.FfnDims(d=5, inter=5)
+
+    def lin_t(x, w):
+        return x @ w if w.shape[0] == w.shape[1] else orig_ffn_lin(x, w)
+    w = rand_ffn_weights(sq, 3)
+    x = rand_x((2, 5), 4)
+    ref = [brute_ffn({k: v.tolist() for k, v in w.items()}, x[i].tolist(), 1e-6)[0] for i in range(2)]
+    monkeypatch.setattr(om, "_linear", lin_t)
+    assert not np.allclose(om.ffn(w, x, 1e-6)["out"], ref, rtol=1e-9)
+    monkeypatch.setattr(om, "_linear", orig_ffn_lin)
+    np.testing.assert_allclose(om.ffn(w, x, 1e-6)["out"], ref, rtol=1e-12)
+    assert _ffn_pins_pass()
