@@ -33,6 +33,8 @@ sys.path.insert(0, ROOT)
 METRIC = "MLA prefill tokens/s (% bf16 TC peak); decode step µs & HBM GB/s (% of 8 TB/s)"
 NOMINAL_HBM_GBS = 8000.0
 D, H, QL, KVL, NOPE, ROPE, QK, V = 7168, 64, 1536, 512, 128, 64, 192, 128
+FFN_I = 18432  # SwiGLU MLP width
+FFN_WEIGHT_BYTES = 2 * (7168 + 3 * 7168 * FFN_I)
 WEIGHT_BYTES = 2 * (7168 + 1536 * 7168 + 1536 + 12288 * 1536 + 576 * 7168 + 512 + 16384 * 512 + 7168 * 8192)
 
 
@@ -67,6 +69,18 @@ def stage_work(name, mode, B, T_or_P, past=0):
     if name == "attn" and mode == "latent":
         L = T_or_P + 1
         return ("byte", B * L * (KVL + ROPE) * 2)
+    if mode == "ffn":  # MLP half over n = B * T_or_P rows, tensor-bound
+        n = B * T_or_P
+        if name == "gate_up":
+            return ("flop", 2 * n * D * 2 * FFN_I)
+        if name == "down":
+            return ("flop", 2 * n * FFN_I * D)
+    if mode == "ffn_dec":  # few rows: the weights stream once
+        n = B * T_or_P
+        if name == "gate_up":
+            return ("byte", 2 * FFN_I * D * 2 + n * (D + FFN_I) * 2)
+        if name == "down":
+            return ("byte", FFN_I * D * 2 + n * (FFN_I + 2 * D) * 2)
     return (None, 0)
 
 
@@ -278,6 +292,36 @@ class Runner:
             m.mla_prefill(self.W, x, out, ws, *caches, cap, m.make_params(timing=timing))
         return step
 
+    # ---- the block's MLP half ------------------------------------------------
+    def ffn_weights(self):
+        if getattr(self, "WF", None) is None:
+            self.wft = self.synth.ffn_weights_cuda(0, device=self.dev)
+            self.WF = self.m.make_ffn_weights(self.wft)
+        return self.WF
+
+    def ffn_step_fn(self, n):
+        torch, m, synth = self.torch, self.m, self.synth
+        WF = self.ffn_weights()
+        x = synth.tensor_cuda(0, "ffn_x", (n, D), synth.X_DIST, device=self.dev)
+        out = torch.empty_like(x)
+        ws = m.alloc_workspace(m.MODE_FFN, 1, n, device=self.dev)
+
+        def step(timing):
+            m.mla_ffn(WF, x, out, ws, m.make_params(timing=timing))
+        return step, (x, out, ws)
+
+    def block_step_fn(self, B, T):
+        """The dense block: mla_prefill (x -> x') then mla_ffn in place."""
+        torch, m = self.torch, self.m
+        WF = self.ffn_weights()
+        x, mid, ws, caches = self.prefill_setup(B, T, with_cache=False)
+        wsf = m.alloc_workspace(m.MODE_FFN, B, T, device=self.dev)
+
+        def step(timing):
+            m.mla_prefill(self.W, x, mid, ws, *caches, 0, m.make_params(timing=timing))
+            m.mla_ffn(WF, mid, mid, wsf, m.make_params(timing=timing))
+        return step, (x, mid, ws, wsf)
+
     def chunk_step_fn(self, B, P0, T):
         """Chunked prefill of T tokens after P0 positions already in the
         rebuilt cache (written by the library's cache-only prefill of the
@@ -329,6 +373,7 @@ class Runner:
         return step, (c1, c2, x, out, ws)
 
 
+FFN_STAGES = ("ffn_norm", "gate_up", "down")
 PREFILL_STAGES = ("input_norm", "a_proj", "latent", "q_b", "kv_b", "attn", "o_proj")
 DECODE_STAGES = ("input_norm", "a_proj", "latent", "q_b", "kv_b", "attn", "o_proj")
 LATENT_STAGES = ("input_norm", "a_proj", "latent", "q_b", "absorb_q", "attn", "absorb_o", "o_proj")
@@ -419,9 +464,12 @@ def run_profile(args):
     r = Runner("cuda:0")
     keep = None
     mc = re.fullmatch(r"chunk_b(\d+)_p(\d+)_t(\d+)", args.profile)
+    mf = re.fullmatch(r"ffn_n(\d+)", args.profile)
     mt = re.fullmatch(r"(prefill|decode|latent)_b(\d+)_([tp])(\d+)(_cache)?", args.profile)
     if mc:
         step, keep = r.chunk_step_fn(int(mc.group(1)), int(mc.group(2)), int(mc.group(3)))
+    elif mf:
+        step, keep = r.ffn_step_fn(int(mf.group(1)))
     elif not mt:
         raise SystemExit(f"--profile: unknown configuration {args.profile!r}")
     else:
@@ -454,7 +502,7 @@ def main():
                     help="tokens of the headline sequence the CPU oracle baseline runs (0 = skip)")
     ap.add_argument("--profile", default=None,
                     help="run one step of one configuration for a profiler and exit: prefill_bB_tT[_cache], "
-                         "chunk_bB_pP0_tT (chunked prefill after P0 cached positions), "
+                         "chunk_bB_pP0_tT (chunked prefill after P0 cached positions), ffn_nN (MLP half, N rows), "
                          "decode_bB_pP (rebuilt cache) or latent_bB_pP; only that step lies between "
                          "cudaProfilerStart/Stop (ncu --profile-from-start off)")
     args = ap.parse_args()
@@ -601,6 +649,58 @@ def main():
             torch.cuda.empty_cache()
         except Exception as e:
             line["prefill_chunk"] = {"error": repr(e)[:300]}
+        # ---- the block's MLP half: 2048 rows (prefill) and 64 rows (decode) ---------
+        l_ffn = 0
+        try:
+            n7 = 2048
+            step7, keep = r.ffn_step_fn(n7)
+            ms7, st7, l_ffn = r.time_steps(step7, ks, W, stages=FFN_STAGES)
+            ms7 = barrier_max(statistics.mean(ms7))
+            fl7 = 3 * 2 * n7 * D * FFN_I
+            line["ffn_prefill"] = {
+                "workload": "mla_ffn 2048 rows (post-attention RMSNorm + SwiGLU MLP, I=18432, + residual)",
+                "ms_per_step": round(ms7, 4), "tokens_per_s": round(world * n7 / (ms7 * 1e-3), 1),
+                "tflops": round(fl7 / (ms7 * 1e-3) / 1e12, 2),
+                "frac_bf16_peak": round(fl7 / (ms7 * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+                "stage_ms": _stages_out(st7),
+                "roofline": roofline_entry(st7, "ffn", 1, n7, pk, "ffn_n2048"), "launches": l_ffn}
+            del step7, keep
+            torch.cuda.empty_cache()
+        except Exception as e:
+            line["ffn_prefill"] = {"error": repr(e)[:300]}
+        try:
+            n8 = 64
+            step8, keep = r.ffn_step_fn(n8)
+            ms8, st8, l8 = r.time_steps(step8, ks, W, stages=FFN_STAGES)
+            us8 = barrier_max(statistics.mean(ms8)) * 1e3
+            by8 = FFN_WEIGHT_BYTES + 2 * n8 * D * 2
+            line["ffn_decode"] = {
+                "workload": "mla_ffn 64 rows (one decode step of 64 sequences): the 793 MB of MLP weights stream once",
+                "us_per_step": round(us8, 2), "hbm_gbs": round(by8 / (us8 * 1e-6) / 1e9, 1),
+                "frac_measured_hbm": round(by8 / (us8 * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
+                "algorithmic_bytes": by8, "stage_ms": _stages_out(st8),
+                "roofline": roofline_entry(st8, "ffn_dec", 1, n8, pk, "ffn_n64"), "launches": l8}
+            del step8, keep
+            torch.cuda.empty_cache()
+        except Exception as e:
+            line["ffn_decode"] = {"error": repr(e)[:300]}
+        # ---- the whole dense block: prefill B=1 T=2048 then the MLP half ----------
+        try:
+            B9, T9 = 1, 2048
+            step9, keep = r.block_step_fn(B9, T9)
+            ms9, st9, _ = r.time_steps(step9, ks, W, stages=PREFILL_STAGES + FFN_STAGES)
+            ms9 = barrier_max(statistics.mean(ms9))
+            fl9 = flops + 3 * 2 * B9 * T9 * D * FFN_I
+            line["dense_block_prefill"] = {
+                "workload": "dense block B=1 T=2048: mla_prefill (causal MLA + residual) then mla_ffn (in place)",
+                "ms_per_step": round(ms9, 4), "tokens_per_s": round(world * B9 * T9 / (ms9 * 1e-3), 1),
+                "tflops": round(fl9 / (ms9 * 1e-3) / 1e12, 2),
+                "frac_bf16_peak": round(fl9 / (ms9 * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+                "stage_ms": _stages_out(st9), "launches": launches + l_ffn}
+            del step9, keep
+            torch.cuda.empty_cache()
+        except Exception as e:
+            line["dense_block_prefill"] = {"error": repr(e)[:300]}
 
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----------------------------------
     if world == 1 and args.cpu_tokens > 0:

@@ -64,11 +64,13 @@ extern "C" {
 #define MLA_QK_ROPE 64
 #define MLA_QK 192
 #define MLA_V 128
+#define MLA_FFN_INTER 18432  /* SwiGLU MLP width: 396,361,728 parameters / (3 x 7168) */
 
 /* ---- modes for mla_workspace_size ---------------------------------------- */
 #define MLA_MODE_PREFILL 0
 #define MLA_MODE_DECODE 1
 #define MLA_MODE_DECODE_LATENT 2
+#define MLA_MODE_FFN 3
 
 /* Weights of one MLA sublayer: device pointers to bf16, nn.Linear [out, in].
  * Key-value compression page, MLA __init__ excerpt, for the projections;
@@ -95,7 +97,10 @@ typedef struct {
 #define MLA_STAGE_ABSORB_Q 7     /* latent decode: q_nope . W_UK             */
 #define MLA_STAGE_ABSORB_O 8     /* latent decode: o_latent . W_UV^T         */
 #define MLA_STAGE_O_PROJ 9       /* o_proj + residual                        */
-#define MLA_MAX_STAGES 10
+#define MLA_STAGE_FFN_NORM 10    /* mla_ffn: RMSNorm(x')                     */
+#define MLA_STAGE_FFN_GATE_UP 11 /* mla_ffn: [W_1 ; W_3] product + SiLU(g) * u */
+#define MLA_STAGE_FFN_DOWN 12    /* mla_ffn: W_2 product + residual          */
+#define MLA_MAX_STAGES 13
 
 /* Optional per-stage timing.  start[s] / stop[s] are cudaEvent_t handles
  * created by the caller (or NULL to skip stage s); the library records them
@@ -122,6 +127,7 @@ typedef struct {
  *   mode = MLA_MODE_PREFILL:       B sequences of T = t_or_p tokens; `cap` is
  *                                  ignored (pass the cache capacity or 0).
  *   mode = MLA_MODE_DECODE / _LATENT: B sequences, P = t_or_p cached positions.
+ *   mode = MLA_MODE_FFN:           B * t_or_p token rows (mla_ffn).
  * Returns 0 when the arguments are out of range. */
 size_t mla_workspace_size(int mode, int B, int t_or_p, int cap);
 
@@ -202,6 +208,40 @@ int mla_decode_latent(const mla_weights_t* w, const mla_params_t* params, const 
  * Arguments, checks and results otherwise as mla_decode. */
 int mla_decode_noalloc(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int P,
                        void* k_cache, void* v_cache, int cap, void* out, void* stream);
+
+/* ---- the block's second half ---------------------------------------------
+ * Kimi K2 "Dense transformer block" page, equation list after
+ * x'_n = x_n + Delta_attn, and its DecoderLayer forward excerpt: the dense
+ * block applies the MLA sublayer (mla_prefill / mla_decode /
+ * mla_decode_latent: x -> x'), then
+ *   x_ffn = RMSNorm(x'); g = x_ffn W_1; u = x_ffn W_3; a = g sigma(g);
+ *   h = a (.) u; Delta_ffn = h W_2; x_{n+1} = x' + Delta_ffn.
+ * The intermediate width is not printed; the page's parameter table gives
+ * the SwiGLU MLP 396,361,728 parameters = 3 x 7168 x 18,432 (no biases). */
+typedef struct {
+  const void* w_post_norm; /* [7168]          post-attention RMSNorm gain   */
+  const void* w_1;         /* [18432, 7168]   gate projection (g)           */
+  const void* w_3;         /* [18432, 7168]   up projection (u)             */
+  const void* w_2;         /* [7168, 18432]   down projection               */
+} mla_ffn_weights_t;
+
+/* x_{n+1} = x' + Delta_ffn for n_tok token rows (any mix of prefill and
+ * decode rows: every row is independent).
+ *   x    [n_tok, 7168]   x' (the MLA sublayer's output)
+ *   out  [n_tok, 7168]   x_{n+1} (may alias x exactly)
+ *   params: eps (the MLP RMSNorm's), delta_out (optional float32
+ *   [n_tok, 7168] receiving Delta_ffn) and timing (stages
+ *   MLA_STAGE_FFN_*); rope_base and softmax_scale are not used.  NULL
+ *   selects eps = 1e-6.
+ *   workspace: mla_workspace_size(MLA_MODE_FFN, 1, n_tok, 0) bytes (it holds
+ *   RMSNorm(x') and h, n_tok x (7168 + 18432) bf16 values).
+ * g and u accumulate in float32; SiLU(g) u is rounded once to bf16 (h), the
+ * input of the down projection, whose float32 sum is added to x' in float32
+ * and rounded once.
+ * Errors: INVALID_ARG (null pointer, n_tok < 1, partial x/out overlap),
+ * ALIGNMENT, WORKSPACE, CUDA. */
+int mla_ffn(const mla_ffn_weights_t* w, const mla_params_t* params, const void* x, int n_tok, void* out,
+            void* workspace, size_t workspace_bytes, void* stream);
 
 /* Synchronises `stream` and reads the device status word the last call on
  * this workspace left: MLA_OK, or MLA_ERR_TIMEOUT if a bounded device wait

@@ -15,8 +15,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmla.so")
 
 D, HEADS, Q_LORA, KV_LORA, QK_NOPE, QK_ROPE, QK, V = 7168, 64, 1536, 512, 128, 64, 192, 128
-MODE_PREFILL, MODE_DECODE, MODE_DECODE_LATENT = 0, 1, 2
-STAGES = ["input_norm", "a_proj", "latent", "q_b", "kv_b", "attn", "combine", "absorb_q", "absorb_o", "o_proj"]
+FFN_INTER = 18432
+MODE_PREFILL, MODE_DECODE, MODE_DECODE_LATENT, MODE_FFN = 0, 1, 2, 3
+STAGES = ["input_norm", "a_proj", "latent", "q_b", "kv_b", "attn", "combine", "absorb_q", "absorb_o", "o_proj",
+          "ffn_norm", "gate_up", "down"]
 MAX_STAGES = len(STAGES)
 
 STATUS = {0: "MLA_OK", -1: "MLA_ERR_INVALID_ARG", -2: "MLA_ERR_ALIGNMENT", -3: "MLA_ERR_WORKSPACE",
@@ -28,6 +30,8 @@ WEIGHT_SHAPES = {
     "w_kv_a": (KV_LORA + QK_ROPE, D), "w_kv_a_norm": (KV_LORA,), "w_kv_b": (HEADS * (QK_NOPE + V), KV_LORA),
     "w_o": (D, HEADS * V),
 }
+FFN_WEIGHT_NAMES = ["w_post_norm", "w_1", "w_3", "w_2"]
+FFN_WEIGHT_SHAPES = {"w_post_norm": (D,), "w_1": (FFN_INTER, D), "w_3": (FFN_INTER, D), "w_2": (D, FFN_INTER)}
 
 
 class MlaError(RuntimeError):
@@ -38,6 +42,10 @@ class MlaError(RuntimeError):
 
 class MlaWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_NAMES]
+
+
+class MlaFfnWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in FFN_WEIGHT_NAMES]
 
 
 class MlaTiming(ctypes.Structure):
@@ -65,6 +73,7 @@ _SIGS = {
                                _VP, _VP, _SZ, _VP]),
     "mla_decode_noalloc": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _VP, _VP, _I,
                                 _VP, _VP]),
+    "mla_ffn": (_I, [ctypes.POINTER(MlaFfnWeights), ctypes.POINTER(MlaParams), _VP, _I, _VP, _VP, _SZ, _VP]),
     "mla_device_status": (_I, [_VP, _VP]),
     "mla_status_string": (ctypes.c_char_p, [_I]),
     "mla_debug_gemm": (_I, [_VP, _I, _VP, _I, _I, _VP, _I, _I, _I, _I, _VP]),
@@ -113,6 +122,19 @@ def make_weights(w: dict) -> MlaWeights:
             raise ValueError(f"weight {n}: need contiguous bf16 CUDA tensor of shape {WEIGHT_SHAPES[n]}")
     s = MlaWeights(*[w[n].data_ptr() for n in WEIGHT_NAMES])
     s._keep = dict(w)  # the struct holds raw pointers: keep the tensors alive with it
+    return s
+
+
+def make_ffn_weights(w: dict) -> MlaFfnWeights:
+    """Pack a dict of bf16 CUDA tensors (names of FFN_WEIGHT_NAMES) into the C struct."""
+    import torch
+    for n in FFN_WEIGHT_NAMES:
+        t = w[n]
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or \
+                tuple(t.shape) != FFN_WEIGHT_SHAPES[n]:
+            raise ValueError(f"weight {n}: need contiguous bf16 CUDA tensor of shape {FFN_WEIGHT_SHAPES[n]}")
+    s = MlaFfnWeights(*[w[n].data_ptr() for n in FFN_WEIGHT_NAMES])
+    s._keep = dict(w)
     return s
 
 
@@ -189,6 +211,14 @@ def mla_decode_noalloc(weights: MlaWeights, x, P: int, k_cache, v_cache, out, pa
     rc = lib().mla_decode_noalloc(ctypes.byref(weights), None if params is None else ctypes.byref(params), _ptr(x),
                                   B, P, _ptr(k_cache), _ptr(v_cache), cap, _ptr(out), _stream(stream))
     _check(rc, "mla_decode_noalloc")
+
+
+def mla_ffn(weights: MlaFfnWeights, x, out, workspace, params: MlaParams | None = None, stream=None):
+    """x, out: bf16 [..., 7168] (out = x + Delta_ffn, may be x itself)."""
+    n_tok = x.numel() // D
+    rc = lib().mla_ffn(ctypes.byref(weights), None if params is None else ctypes.byref(params), _ptr(x), n_tok,
+                       _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "mla_ffn")
 
 
 def mla_device_status(workspace, stream=None) -> int:

@@ -20,7 +20,7 @@ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 // Workspace carve-up.  Offsets are computed identically by the size query
 // and by the entry points.
 struct Layout {
-  size_t status, cs, xn, ca, cq, ckv, kpe, q, o, kscr, vscr, qlat, olat, part_o, part_ml, split, total;
+  size_t status, cs, xn, ca, cq, ckv, kpe, q, o, kscr, vscr, qlat, olat, part_o, part_ml, split, h, total;
   size_t split_bytes;  // split-K partial slots (decode modes), 0 = none
 };
 
@@ -39,6 +39,13 @@ Layout make_layout(int mode, int B, int t_or_p, int num_sms) {
     return at;
   };
   L.status = take(kStatusRegion);
+  if (mode == MLA_MODE_FFN) {  // B * t_or_p rows: RMSNorm(x') and h
+    const size_t rows = (size_t)B * t_or_p;
+    L.xn = take(rows * MLA_D * 2);
+    L.h = take(rows * MLA_FFN_INTER * 2);
+    L.total = off;
+    return L;
+  }
   L.cs = take(npos * 32 * sizeof(float2));
   L.xn = take(n * MLA_D * 2);
   L.ca = take(n * 2112 * 4);
@@ -287,6 +294,8 @@ size_t mla_workspace_size(int mode, int B, int t_or_p, int cap) {
     if (t_or_p < 1 || (int64_t)B * t_or_p > kMaxTokens) return 0;
   } else if (mode == MLA_MODE_DECODE || mode == MLA_MODE_DECODE_LATENT) {
     if (t_or_p < 0 || B > kMaxTokens || t_or_p >= (1 << 24)) return 0;
+  } else if (mode == MLA_MODE_FFN) {
+    if (t_or_p < 1 || (int64_t)B * t_or_p > kMaxTokens) return 0;
   } else {
     return 0;
   }
@@ -541,6 +550,72 @@ int mla_decode_latent(const mla_weights_t* w, const mla_params_t* params, const 
   rc = o_proj_stage(w, p, x, out, B, workspace, L, st, sms, stream_, &launches);
   if (rc) return rc;
   sg.stop(MLA_STAGE_O_PROJ);
+  if (p.timing) p.timing->n_launches = launches;
+  return MLA_OK;
+}
+
+int mla_ffn(const mla_ffn_weights_t* w, const mla_params_t* params, const void* x, int n_tok, void* out,
+            void* workspace, size_t workspace_bytes, void* stream) {
+  const Params p = resolve(params);
+  if (!w || !x || !out || n_tok < 1 || (int64_t)n_tok > kMaxTokens) return MLA_ERR_INVALID_ARG;
+  for (const void* q : {w->w_post_norm, w->w_1, w->w_3, w->w_2})
+    if (!q) return MLA_ERR_INVALID_ARG;
+  for (const void* q : {w->w_post_norm, w->w_1, w->w_3, w->w_2, x, (const void*)out})
+    if (!aligned16(q)) return MLA_ERR_ALIGNMENT;
+  if (!workspace) return MLA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MLA_ERR_ALIGNMENT;
+  if (!params_ok(p)) return MLA_ERR_INVALID_ARG;
+  if (bad_overlap(x, out, (size_t)n_tok * MLA_D * 2)) return MLA_ERR_INVALID_ARG;
+  const Layout L = make_layout(MLA_MODE_FFN, 1, n_tok, kMaxSmsForSizing);
+  if (workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return MLA_ERR_CUDA;
+
+  cudaStream_t stream_ = static_cast<cudaStream_t>(stream);
+  const DevStatusHost st{at<uint32_t>(workspace, L.status), kDefaultWaitLimitNs};
+  Stager sg{p.timing, stream_};
+  int launches = 0;
+  if (cudaMemsetAsync(st.word, 0, kStatusRegion, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+
+  // x_ffn = RMSNorm(x')
+  sg.start(MLA_STAGE_FFN_NORM);
+  MLA_TRY(launch_rmsnorm_rows(xb, static_cast<const __nv_bfloat16*>(w->w_post_norm), at<__nv_bfloat16>(workspace, L.xn),
+                              n_tok, p.eps, stream_));
+  launches += 1;
+  sg.stop(MLA_STAGE_FFN_NORM);
+
+  // h = SiLU(x_ffn W_1) (.) (x_ffn W_3): one product over [W_1 ; W_3], the
+  // gate and up columns of each intermediate index in the same tile
+  sg.start(MLA_STAGE_FFN_GATE_UP);
+  {
+    GemmShape s{n_tok, 2 * MLA_FFN_INTER, MLA_D, 1, 0, 0, 0, 0, MLA_FFN_INTER};
+    GemmOperands op{at<__nv_bfloat16>(workspace, L.xn), MLA_D, n_tok,
+                    static_cast<const __nv_bfloat16*>(w->w_1), MLA_D, MLA_FFN_INTER,
+                    static_cast<const __nv_bfloat16*>(w->w_3), MLA_D, MLA_FFN_INTER, false};
+    EpiArgs ea{};
+    ea.out = at<__nv_bfloat16>(workspace, L.h);
+    ea.ldo = MLA_FFN_INTER;
+    MLA_TRY(launch_gemm(s, op, Epi::kSwiGLU, ea, st, sms, stream_));
+    launches += 1;
+  }
+  sg.stop(MLA_STAGE_FFN_GATE_UP);
+
+  // x_{n+1} = x' + h W_2
+  sg.start(MLA_STAGE_FFN_DOWN);
+  {
+    GemmShape s{n_tok, MLA_D, MLA_FFN_INTER, 1, 0, 0, 0, 0, MLA_D};
+    GemmOperands op{at<__nv_bfloat16>(workspace, L.h), MLA_FFN_INTER, n_tok,
+                    static_cast<const __nv_bfloat16*>(w->w_2), MLA_FFN_INTER, MLA_D, nullptr, 0, 0, false};
+    EpiArgs ea{};
+    ea.out = static_cast<__nv_bfloat16*>(out);
+    ea.ldo = MLA_D;
+    ea.x = xb;
+    ea.delta = p.delta;
+    MLA_TRY(launch_gemm(s, op, Epi::kResidual, ea, st, sms, stream_));
+    launches += 1;
+  }
+  sg.stop(MLA_STAGE_FFN_DOWN);
   if (p.timing) p.timing->n_launches = launches;
   return MLA_OK;
 }

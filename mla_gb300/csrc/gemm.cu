@@ -62,6 +62,18 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const uint32_t 
   }
 }
 
+// h = SiLU(g) u = g u / (1 + e^-g) on 32 columns, in place in g (float32;
+// e^-g = 2^(-g log2 e); for g far below zero the reciprocal of the infinite
+// denominator is 0 and h = 0).
+__device__ __forceinline__ void swiglu32(uint32_t (&g)[32], const uint32_t (&u)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float gv = __uint_as_float(g[i]);
+    const float e = ex2_approx(-1.4426950408889634f * gv);
+    g[i] = __float_as_uint(gv * __frcp_rn(1.f + e) * __uint_as_float(u[i]));
+  }
+}
+
 // Accumulator sources for the epilogue: the tile in tensor memory, or (after
 // a split-K reduction) the float32 partial slots in global memory.
 struct TmemSrc {
@@ -193,6 +205,17 @@ __device__ __forceinline__ void run_epilogue(const EpiArgs& ea, const Src& ld, i
       uint4* dst = reinterpret_cast<uint4*>(krow + 128);
 #pragma unroll
       for (int j = 0; j < 8; ++j) dst[j] = src[j];
+    }
+  } else if constexpr (EPI == Epi::kSwiGLU) {
+    // columns [0, BN/2) gate, [BN/2, BN) up, both of intermediate j0 + c
+    __nv_bfloat16* dst = ea.out + (size_t)row * ea.ldo + n0 / 2;
+#pragma unroll 1
+    for (int c = 0; c < BN / 2; c += 32) {
+      uint32_t g[32], u[32];
+      ld(c, g);
+      ld(BN / 2 + c, u);
+      swiglu32(g, u);
+      if (row_ok) store32_bf16(dst + c, g);
     }
   } else {  // kResidual
     const size_t base = (size_t)row * ea.ldo + n0;
@@ -389,6 +412,18 @@ __device__ __forceinline__ void run_epilogue_tma(const EpiArgs& ea, const TmemSr
         ss.issue3(m0, buf, 128 + 32 * half, t0, plane, lane);
       }
     }
+  } else if constexpr (EPI == Epi::kSwiGLU) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 2; c += 32) {
+      uint32_t g[32], u[32];
+      tmem_ld32(taddr + c, g);
+      tmem_ld32(taddr + BN / 2 + c, u);
+      tmem_wait_ld();
+      swiglu32(g, u);
+      uint8_t* buf = ss.next(lane);
+      stage_bf16(buf, lane, g);
+      ss.issue2(m0, buf, n0 / 2 + c, row0, lane);
+    }
   } else {  // kResidual
     const size_t base = (size_t)row * ea.ldo + n0;
     tmem_chunk_loop(taddr, 0, BN, [&](int c, uint32_t (&r)[32]) {
@@ -448,6 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(!TMA_ST || BM == 128, "TMA-store epilogue needs 32 rows per warp");
   static_assert(!PAIR || (!B_MN && KSUB == 1 && BM == 128), "pair mode: K-major B, one K block per stage");
   using L = GemmSmem<BM, BN, STAGES, KSUB, TMA_ST, PAIR>;
+  constexpr bool kSwi = EPI == Epi::kSwiGLU;  // B rows: gate half then up half of each tile
+  static_assert(!kSwi || (!B_MN && BN % 64 == 0), "SwiGLU tiles: K-major B, 32-column halves");
   constexpr uint32_t kTmemCols = pow2_cols(2 * BN);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -546,7 +583,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < KSUB; ++u) {
               const int k0 = ((kb0 + i) * KSUB + u) * kBK;
-              if constexpr (B_MN) {
+              if constexpr (kSwi) {
+                tma_load_2d(sb + u * L::kB1, &tmB0, &full_bar[i], k0, b_row + n0 / 2);
+                tma_load_2d(sb + u * L::kB1 + (BN / 2) * 128, &tmB1, &full_bar[i], k0, b_row + n0 / 2);
+              } else if constexpr (B_MN) {
 #pragma unroll
                 for (int j = 0; j < BN / 64; ++j)
                   tma_load_2d(sb + u * L::kB1 + j * (64 * 128), mb, &full_bar[i], nb + j * 64, b_row + k0);
@@ -583,7 +623,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t fb = mapa_rank(smem_u32(&full_bar[stage]), 0);
             const int k0 = kb * kBK;
             tma_load_2d_pair(sa, &tmA, fb, a_col + k0, m_blk * BM);
-            tma_load_2d_pair(sb, mb, fb, k0, b_row + nb + (int)crank * (BN / 2));
+            if constexpr (kSwi)  // even CTA: gate rows, odd CTA: up rows of the same j
+              tma_load_2d_pair(sb, crank ? &tmB1 : &tmB0, fb, k0, b_row + n0 / 2);
+            else
+              tma_load_2d_pair(sb, mb, fb, k0, b_row + nb + (int)crank * (BN / 2));
             issued[stage]++;
             if (++stage == STAGES) {
               stage = 0;
@@ -598,7 +641,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int k0 = (kb * KSUB + u) * kBK;
             tma_load_2d(sa + u * L::kA1, &tmA, &full_bar[stage], a_col + k0, m_blk * BM);
             if (b_done) continue;
-            if constexpr (B_MN) {
+            if constexpr (kSwi) {
+              tma_load_2d(sb + u * L::kB1, &tmB0, &full_bar[stage], k0, b_row + n0 / 2);
+              tma_load_2d(sb + u * L::kB1 + (BN / 2) * 128, &tmB1, &full_bar[stage], k0, b_row + n0 / 2);
+            } else if constexpr (B_MN) {
 #pragma unroll
               for (int j = 0; j < BN / 64; ++j)
                 tma_load_2d(sb + u * L::kB1 + j * (64 * 128), mb, &full_bar[stage], nb + j * 64, b_row + k0);
@@ -794,11 +840,13 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
   if (B_MN) {
     if (!make_tmap_bf16_2d(&tb0, op.B0, op.b0_rows, op.ldb0, op.ldb0, 64, 64)) return cudaErrorInvalidValue;
   } else {
-    constexpr uint32_t box_rows = PAIR ? BN / 2 : BN;  // pair mode: each CTA loads half the rows
+    // pair mode: each CTA loads half the rows; SwiGLU: half the rows from each matrix
+    constexpr uint32_t box_rows = (PAIR || EPI == Epi::kSwiGLU) ? BN / 2 : BN;
     if (!make_tmap_bf16_2d(&tb0, op.B0, op.b0_rows, op.ldb0, op.ldb0, box_rows, kBK)) return cudaErrorInvalidValue;
   }
   tb1 = tb0;
-  if (op.B1 && !make_tmap_bf16_2d(&tb1, op.B1, op.b1_rows, op.ldb1, op.ldb1, PAIR ? BN / 2 : BN, kBK))
+  if (op.B1 && !make_tmap_bf16_2d(&tb1, op.B1, op.b1_rows, op.ldb1, op.ldb1,
+                                  (PAIR || EPI == Epi::kSwiGLU) ? BN / 2 : BN, kBK))
     return cudaErrorInvalidValue;
   CUtensorMap to0 = ta, to1 = ta;
   if constexpr (TMA_ST) {
@@ -916,6 +964,17 @@ cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, con
         return launch_impl<128, 256, 6, Epi::kResidual, false, 1, true, true>(g8, op, ea, st, num_sms, stream);
       }
       return launch_impl<128, 256, 4, Epi::kResidual, false, 1, true>(g16, op, ea, st, num_sms, stream);
+    }
+    case Epi::kSwiGLU: {
+      // N = 2 I output columns of [gate | up]; B0 = W_1, B1 = W_3, both [I, K]
+      if (s.N % 256 || 2 * s.n_split != s.N || op.b_mn_major || !op.B1 || s.batches != 1)
+        return cudaErrorInvalidValue;
+      GemmShape g8 = s;
+      g8.raster_g = 8;  // the gate/up weights do not stay in L2: walk groups of 8 row blocks (pairs)
+      if (tiny && k256) return launch_impl<64, 128, 4, Epi::kSwiGLU, false, 2>(s, op, ea, st, num_sms, stream);
+      if (small) return launch_impl<128, 128, 6, Epi::kSwiGLU, false>(s, op, ea, st, num_sms, stream);
+      if (pairs) return launch_impl<128, 256, 6, Epi::kSwiGLU, false, 1, true, true>(g8, op, ea, st, num_sms, stream);
+      return launch_impl<128, 256, 4, Epi::kSwiGLU, false, 1, true>(g8, op, ea, st, num_sms, stream);
     }
     case Epi::kStoreF32:
       if (s.N % 192 || s.n_split % 192 || op.b_mn_major) return cudaErrorInvalidValue;

@@ -115,7 +115,7 @@ struct GemmOperands {
   bool b_mn_major;
 };
 
-enum class Epi { kStoreBf16, kStoreF32, kQRope, kKVCache, kResidual };
+enum class Epi { kStoreBf16, kStoreF32, kQRope, kKVCache, kResidual, kSwiGLU };
 
 struct EpiArgs {
   // kStoreBf16: out[row, c_col0 + batch*c_col_step + n]; kStoreF32: out_f32[row, n]
@@ -135,6 +135,9 @@ struct EpiArgs {
   int t_off;
   int cap;
   // kResidual: out[row, n] = x[row, n] + acc; delta[row, n] = acc (optional)
+  // kSwiGLU: out[row, j] = SiLU(g) * u for j < N / 2, g from B0 (gate) row j,
+  //          u from B1 (up) row j: each BN-wide tile holds BN / 2 gate columns
+  //          then the BN / 2 up columns of the same j (B0, B1 both [N / 2, K])
   const __nv_bfloat16* x;
   float* delta;
   // split-K scratch (null: no split): partial slots and zeroed counters

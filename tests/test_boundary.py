@@ -107,3 +107,47 @@ def test_decode_argument_checks():
                                args["ws"], ws_l, None) == -1
     assert L.mla_decode_latent(ctypes.byref(w), None, args["x"], 4, 10, args["kc"], args["vc"], 11, args["out"],
                                args["ws"], 100, None) == -3
+
+
+def chunk(w, B=1, T=16, P0=8, out=FAKE + (2 << 30), kc=FAKE + (4 << 30), vc=FAKE + (5 << 30), cap=64):
+    ws_bytes = m.lib().mla_workspace_size(m.MODE_PREFILL, B, T, cap)
+    return m.lib().mla_prefill_chunk(ctypes.byref(w), None, FAKE + (1 << 30), B, T, P0, out, kc, vc, None, None,
+                                     cap, FAKE + (3 << 30), ws_bytes, None)
+
+
+def test_prefill_chunk_argument_checks():
+    w = fake_weights()
+    assert chunk(w, P0=-1) == -1
+    assert chunk(w, P0=49, T=16, cap=64) == -1       # P0 + T > cap
+    assert chunk(w, kc=None, vc=None) == -1          # the rebuilt cache holds the past: required
+    assert chunk(w, vc=None) == -1
+    assert chunk(w, out=None) == -1
+    assert chunk(w, kc=FAKE + (4 << 30) + 8) == -2
+
+
+def fake_ffn_weights(**override):
+    vals = {n: FAKE + 4096 * i for i, n in enumerate(m.FFN_WEIGHT_NAMES)}
+    vals.update(override)
+    return m.MlaFfnWeights(*[vals[n] for n in m.FFN_WEIGHT_NAMES])
+
+
+def ffn(w, n=16, x=FAKE + (1 << 30), out=FAKE + (2 << 30), ws=FAKE + (3 << 30), ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = m.lib().mla_workspace_size(m.MODE_FFN, 1, max(n, 1), 0)
+    return m.lib().mla_ffn(ctypes.byref(w), None, x, n, out, ws, ws_bytes, None)
+
+
+def test_ffn_workspace_and_argument_checks():
+    n = 2048
+    assert m.workspace_size(m.MODE_FFN, 1, n) >= n * (m.D + m.FFN_INTER) * 2
+    assert m.workspace_size(m.MODE_FFN, 4, 512) == m.workspace_size(m.MODE_FFN, 1, 2048)
+    assert m.lib().mla_workspace_size(m.MODE_FFN, 1, 0, 0) == 0
+    w = fake_ffn_weights()
+    assert ffn(w, n=0) == -1
+    assert ffn(fake_ffn_weights(w_2=None)) == -1
+    assert ffn(fake_ffn_weights(w_1=FAKE + 8)) == -2
+    assert ffn(w, x=None) == -1
+    assert ffn(w, out=None) == -1
+    assert ffn(w, ws=None) == -3
+    assert ffn(w, ws_bytes=4096) == -3
+    assert ffn(w, out=FAKE + (1 << 30) + 4096) == -1  # partial overlap with x
