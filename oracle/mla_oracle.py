@@ -332,6 +332,19 @@ def decode_latent_absorbed(w: dict, x_new: np.ndarray, ckv_cache: np.ndarray,
     return {"out": x_new + delta, "delta": delta}
 
 
+def prefill_with_past_latent(w: dict, x: np.ndarray, ckv_cache: np.ndarray, kpe_cache: np.ndarray,
+                             dims: Dims = KIMI_K2, eps: float = DEFAULT_EPS, base: float = DEFAULT_ROPE_BASE,
+                             scale: float | None = None, query_rows=None) -> dict:
+    """Chunked prefill against the 576-value latent cache: ckv_cache
+    [B, P0, kv_lora] and kpe_cache [B, P0, rope] hold positions 0..P0-1.
+    The cached positions' per-head keys and values are rebuilt from the
+    latent (key-value compression page: every head's key content and value
+    come from the one latent of the position), then the chunk attends as in
+    ``prefill_with_past``."""
+    K, V = rebuild_kv(w, ckv_cache, kpe_cache, dims)
+    return prefill_with_past(w, x, K, V, dims, eps, base, scale, query_rows)
+
+
 def cache_from_tokens(w: dict, x: np.ndarray, dims: Dims = KIMI_K2, eps: float = DEFAULT_EPS,
                       base: float = DEFAULT_ROPE_BASE) -> dict:
     """Both caches for tokens x [B, P, d] at positions 0..P-1 (what a prefill

@@ -360,6 +360,35 @@ def test_chunk_mask_without_offset_fails_the_pin(monkeypatch):
     assert not np.allclose(bad["out"], whole["out"][:, 4:], rtol=1e-6, atol=1e-8)
 
 
+@pytest.mark.parametrize("T1,T2", [(3, 4), (5, 1)])
+def test_latent_chunk_equals_whole_prefill(T1, T2):
+    """A chunk against the latent cache of the first T1 tokens reproduces
+    the whole prefill's rows (the past keys and values rebuilt from the
+    latent equal the ones the prefill computed from the tokens)."""
+    dims = TINY2
+    w = rand_weights(dims, 68)
+    x = rand_x((2, T1 + T2, dims.d), 69)
+    whole = om.prefill(w, x, dims)
+    cache = om.cache_from_tokens(w, x[:, :T1], dims)
+    ch = om.prefill_with_past_latent(w, x[:, T1:], cache["ckv"], cache["kpe"], dims)
+    np.testing.assert_allclose(ch["out"], whole["out"][:, T1:], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(ch["ckv"], whole["ckv"][:, T1:], rtol=1e-12, atol=1e-13)
+
+
+def test_latent_chunk_rope_key_not_rebuilt_from_latent_fails(monkeypatch):
+    """A planted mistake (the rebuilt keys' rotary part taken as zeros
+    instead of the cached k^R) is caught by the whole-prefill pin."""
+    dims = TINY2
+    w = rand_weights(dims, 70)
+    x = rand_x((1, 6, dims.d), 71)
+    whole = om.prefill(w, x, dims)
+    cache = om.cache_from_tokens(w, x[:, :4], dims)
+    real = om.rebuild_kv
+    monkeypatch.setattr(om, "rebuild_kv", lambda w_, c, r, d=om.KIMI_K2: real(w_, c, np.zeros_like(r), d))
+    bad = om.prefill_with_past_latent(w, x[:, 4:], cache["ckv"], cache["kpe"], dims)
+    assert not np.allclose(bad["out"], whole["out"][:, 4:], rtol=1e-6, atol=1e-8)
+
+
 def test_latent_absorbed_equals_rebuilt():
     dims = TINY2
     w = rand_weights(dims, 39)
