@@ -336,6 +336,20 @@ class Runner:
             m.mla_prefill_chunk(self.W, x, P0, out, kc, vc, ws, params=m.make_params(timing=timing))
         return step, (kc, vc, x, out, ws)
 
+    def chunk_latent_step_fn(self, B, P0, T):
+        """The same chunk against the latent cache (rows 0..P0-1 written by the
+        library's cache-only prefill of 'cache_x'); every step rewrites latent
+        rows P0..P0+T-1 and rebuilds keys and values of all P0 + T positions."""
+        torch, m, synth = self.torch, self.m, self.synth
+        ckv, kpe = self.fill_caches(B, P0, P0 + T, rebuilt=False)
+        x = synth.tensor_cuda(0, "x", (B, T, D), synth.X_DIST, device=self.dev)
+        out = torch.empty_like(x)
+        ws = m.alloc_workspace(m.MODE_CHUNK_LATENT, B, T, device=self.dev, cap=P0 + T)
+
+        def step(timing):
+            m.mla_prefill_chunk_latent(self.W, x, P0, out, ckv, kpe, ws, params=m.make_params(timing=timing))
+        return step, (ckv, kpe, x, out, ws)
+
     # ---- decode -------------------------------------------------------------
     def fill_caches(self, B, P, cap, rebuilt, chunk_tokens=1 << 17):
         """Caches of positions 0..P-1 written by the library's own prefill
@@ -649,6 +663,27 @@ def main():
             torch.cuda.empty_cache()
         except Exception as e:
             line["prefill_chunk"] = {"error": repr(e)[:300]}
+        try:
+            B6, P6, T6 = 1, 2048, 2048
+            step6, keep = r.chunk_latent_step_fn(B6, P6, T6)
+            ms6, st6, l6 = r.time_steps(step6, ks, W, stages=PREFILL_STAGES)
+            ms6 = barrier_max(statistics.mean(ms6))
+            # algorithmic work as the chunk on the rebuilt cache, plus the kv_b
+            # rebuild of the P0 cached positions
+            fl6 = (B6 * T6 * proj_flops_per_token() + prefill_attn_flops(B6, T6, P6)
+                   + B6 * P6 * 2 * KVL * H * (NOPE + V))
+            line["prefill_chunk_latent"] = {
+                "workload": "mla_prefill_chunk_latent B=1 T=2048 after P0=2048 positions in the 576-value latent cache",
+                "ms_per_step": round(ms6, 4), "tokens_per_s": round(world * B6 * T6 / (ms6 * 1e-3), 1),
+                "tflops": round(fl6 / (ms6 * 1e-3) / 1e12, 2),
+                "frac_bf16_peak": round(fl6 / (ms6 * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+                "stage_ms": _stages_out(st6),
+                "roofline": roofline_entry(st6, "prefill", B6, T6, pk, "chunk_latent_b1_p2048_t2048", past=P6),
+                "launches": l6}
+            del step6, keep
+            torch.cuda.empty_cache()
+        except Exception as e:
+            line["prefill_chunk_latent"] = {"error": repr(e)[:300]}
         # ---- the block's MLP half: 2048 rows (prefill) and 64 rows (decode) ---------
         l_ffn = 0
         try:

@@ -71,6 +71,7 @@ extern "C" {
 #define MLA_MODE_DECODE 1
 #define MLA_MODE_DECODE_LATENT 2
 #define MLA_MODE_FFN 3
+#define MLA_MODE_CHUNK_LATENT 4
 
 /* Weights of one MLA sublayer: device pointers to bf16, nn.Linear [out, in].
  * Key-value compression page, MLA __init__ excerpt, for the projections;
@@ -128,6 +129,11 @@ typedef struct {
  *                                  ignored (pass the cache capacity or 0).
  *   mode = MLA_MODE_DECODE / _LATENT: B sequences, P = t_or_p cached positions.
  *   mode = MLA_MODE_FFN:           B * t_or_p token rows (mla_ffn).
+ *   mode = MLA_MODE_CHUNK_LATENT:  B sequences, chunks of T = t_or_p tokens,
+ *                                  latent caches of `cap` positions
+ *                                  (mla_prefill_chunk_latent; the size grows
+ *                                  with cap: it holds the rebuilt keys and
+ *                                  values of every position, 40 KB each).
  * Returns 0 when the arguments are out of range. */
 size_t mla_workspace_size(int mode, int B, int t_or_p, int cap);
 
@@ -166,6 +172,24 @@ int mla_prefill(const mla_weights_t* w, const mla_params_t* params, const void* 
 int mla_prefill_chunk(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int T,
                       int P0, void* out, void* k_cache, void* v_cache, void* ckv_cache, void* kpe_cache,
                       int cap, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Chunked prefill against the 576-value latent cache (latent-cache serving:
+ * "Key-value compression" page, the per-head keys and values of every
+ * position are rebuilt from its one latent).  T new tokens per sequence at
+ * positions P0..P0+T-1; their latent rows are written to the cache, then the
+ * keys and values of positions 0..P0+T-1 are rebuilt from the cache into the
+ * workspace (kv_b product, rotary key appended) and the chunk attends to them
+ * with the causal mask offset by P0, as mla_prefill_chunk.
+ *   x, out          [B, T, 7168]   (out may alias x exactly; required)
+ *   ckv_cache       [B, cap, 512]  rows 0..P0-1 read, rows P0..P0+T-1 written
+ *   kpe_cache       [B, cap, 64]   same
+ * Requires P0 >= 0, P0 + T <= cap; workspace
+ * mla_workspace_size(MLA_MODE_CHUNK_LATENT, B, T, cap).
+ * Errors: INVALID_ARG (null pointer, P0 < 0, P0 + T > cap), ALIGNMENT,
+ * WORKSPACE, CUDA. */
+int mla_prefill_chunk_latent(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int T,
+                             int P0, void* out, void* ckv_cache, void* kpe_cache, int cap, void* workspace,
+                             size_t workspace_bytes, void* stream);
 
 /* One decode step against the rebuilt per-head cache (the pinned
  * implementation's cache, "Mix and project" page at P = 1,000).

@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(_HERE, "libmla.so")
 
 D, HEADS, Q_LORA, KV_LORA, QK_NOPE, QK_ROPE, QK, V = 7168, 64, 1536, 512, 128, 64, 192, 128
 FFN_INTER = 18432
-MODE_PREFILL, MODE_DECODE, MODE_DECODE_LATENT, MODE_FFN = 0, 1, 2, 3
+MODE_PREFILL, MODE_DECODE, MODE_DECODE_LATENT, MODE_FFN, MODE_CHUNK_LATENT = 0, 1, 2, 3, 4
 STAGES = ["input_norm", "a_proj", "latent", "q_b", "kv_b", "attn", "combine", "absorb_q", "absorb_o", "o_proj",
           "ffn_norm", "gate_up", "down"]
 MAX_STAGES = len(STAGES)
@@ -67,6 +67,8 @@ _SIGS = {
                          _VP, _I, _VP, _SZ, _VP]),
     "mla_prefill_chunk": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _I, _VP, _VP,
                                _VP, _VP, _VP, _I, _VP, _SZ, _VP]),
+    "mla_prefill_chunk_latent": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _I, _VP,
+                                      _VP, _VP, _I, _VP, _SZ, _VP]),
     "mla_decode": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _VP, _VP, _I, _VP,
                         _VP, _SZ, _VP]),
     "mla_decode_latent": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _VP, _VP, _I,
@@ -153,9 +155,9 @@ def workspace_size(mode: int, B: int, t_or_p: int, cap: int = 0) -> int:
     return n
 
 
-def alloc_workspace(mode: int, B: int, t_or_p: int, device="cuda"):
+def alloc_workspace(mode: int, B: int, t_or_p: int, device="cuda", cap: int = 0):
     import torch
-    return torch.empty(workspace_size(mode, B, t_or_p), dtype=torch.uint8, device=device)
+    return torch.empty(workspace_size(mode, B, t_or_p, cap), dtype=torch.uint8, device=device)
 
 
 def mla_prefill(weights: MlaWeights, x, out, workspace, k_cache=None, v_cache=None, ckv_cache=None,
@@ -178,6 +180,19 @@ def mla_prefill_chunk(weights: MlaWeights, x, P0: int, out, k_cache, v_cache, wo
                                  B, T, P0, _ptr(out), _ptr(k_cache), _ptr(v_cache), _ptr(ckv_cache),
                                  _ptr(kpe_cache), cap, _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "mla_prefill_chunk")
+
+
+def mla_prefill_chunk_latent(weights: MlaWeights, x, P0: int, out, ckv_cache, kpe_cache, workspace,
+                             params: MlaParams | None = None, stream=None):
+    """x, out: bf16 [B, T, 7168] at positions P0..P0+T-1; ckv_cache [B, cap, 512] and kpe_cache
+    [B, cap, 64] hold rows 0..P0-1 and receive rows P0..P0+T-1; workspace of MODE_CHUNK_LATENT
+    sized with the same cap."""
+    B, T = x.shape[0], x.shape[1]
+    cap = ckv_cache.shape[1]
+    rc = lib().mla_prefill_chunk_latent(ctypes.byref(weights), None if params is None else ctypes.byref(params),
+                                        _ptr(x), B, T, P0, _ptr(out), _ptr(ckv_cache), _ptr(kpe_cache), cap,
+                                        _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "mla_prefill_chunk_latent")
 
 
 def mla_decode(weights: MlaWeights, x, P: int, k_cache, v_cache, out, workspace,

@@ -28,10 +28,11 @@ struct Layout {
 // byte 256 (kMaxSplitCounters ints); cleared at the start of every call.
 constexpr size_t kStatusRegion = 256 + kMaxSplitCounters * sizeof(int);
 
-Layout make_layout(int mode, int B, int t_or_p, int num_sms) {
+Layout make_layout(int mode, int B, int t_or_p, int num_sms, int cap = 0) {
   Layout L{};
-  const size_t n = (mode == MLA_MODE_PREFILL) ? (size_t)B * t_or_p : (size_t)B;
-  const size_t npos = (mode == MLA_MODE_PREFILL) ? (size_t)t_or_p : 1;
+  const bool pre = mode == MLA_MODE_PREFILL || mode == MLA_MODE_CHUNK_LATENT;
+  const size_t n = pre ? (size_t)B * t_or_p : (size_t)B;
+  const size_t npos = pre ? (size_t)t_or_p : 1;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t at = off;
@@ -54,9 +55,12 @@ Layout make_layout(int mode, int B, int t_or_p, int num_sms) {
   L.kpe = take(n * MLA_QK_ROPE * 2);
   L.q = take(n * MLA_HEADS * MLA_QK * 2);
   L.o = take(n * MLA_HEADS * MLA_V * 2);
-  if (mode == MLA_MODE_PREFILL) {
-    L.kscr = take((size_t)B * MLA_HEADS * t_or_p * MLA_QK * 2);
-    L.vscr = take((size_t)B * MLA_HEADS * t_or_p * MLA_V * 2);
+  if (pre) {
+    // K/V scratch: the chunk's positions (prefill without caches), or every
+    // position up to cap rebuilt from the latent cache (latent chunk)
+    const size_t pos = mode == MLA_MODE_CHUNK_LATENT ? (size_t)cap : (size_t)t_or_p;
+    L.kscr = take((size_t)B * MLA_HEADS * pos * MLA_QK * 2);
+    L.vscr = take((size_t)B * MLA_HEADS * pos * MLA_V * 2);
   } else if (mode == MLA_MODE_DECODE) {
     const int s = decode_splits(B, t_or_p + 1, num_sms);
     L.part_o = take((size_t)B * MLA_HEADS * s * MLA_V * sizeof(float));
@@ -68,7 +72,7 @@ Layout make_layout(int mode, int B, int t_or_p, int num_sms) {
     L.part_o = take((size_t)2 * g * MLA_HEADS * MLA_KV_LORA * sizeof(float));
     L.part_ml = take((size_t)2 * g * MLA_HEADS * sizeof(float2));
   }
-  if (mode != MLA_MODE_PREFILL) {
+  if (!pre) {
     L.split_bytes = split_part_bytes(B);
     L.split = take(L.split_bytes);
   }
@@ -230,17 +234,19 @@ int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok,
   return MLA_OK;
 }
 
-int kv_b_stage(const mla_weights_t* w, int n_tok, int t_mod, int t_off, __nv_bfloat16* kc, __nv_bfloat16* vc,
-               int cap, void* ws, const Layout& L, const DevStatusHost& st, int sms, cudaStream_t stream,
-               int* launches) {
+// kv_b over n_tok latent rows ckv [n_tok, 512] (rotary keys kpe [n_tok, 64]):
+// K/V of row r at sequence r / t_mod, position t_off + r % t_mod.
+int kv_b_rows(const mla_weights_t* w, const __nv_bfloat16* ckv, const __nv_bfloat16* kpe, int n_tok, int t_mod,
+              int t_off, __nv_bfloat16* kc, __nv_bfloat16* vc, int cap, void* ws, const Layout& L,
+              const DevStatusHost& st, int sms, cudaStream_t stream, int* launches) {
   GemmShape s{n_tok, MLA_HEADS * 256, MLA_KV_LORA, 1, 0, 0, 0, 0, MLA_HEADS * 256};
-  GemmOperands op{at<__nv_bfloat16>(ws, L.ckv), MLA_KV_LORA, n_tok,
+  GemmOperands op{ckv, MLA_KV_LORA, n_tok,
                   static_cast<const __nv_bfloat16*>(w->w_kv_b), MLA_KV_LORA, MLA_HEADS * 256,
                   nullptr, 0, 0, false};
   EpiArgs ea{};
   ea.kc = kc;
   ea.vc = vc;
-  ea.kpe = at<__nv_bfloat16>(ws, L.kpe);
+  ea.kpe = kpe;
   ea.B = (n_tok + t_mod - 1) / t_mod;
   ea.t_mod = t_mod;
   ea.t_off = t_off;
@@ -249,6 +255,13 @@ int kv_b_stage(const mla_weights_t* w, int n_tok, int t_mod, int t_off, __nv_bfl
   MLA_TRY(launch_gemm(s, op, Epi::kKVCache, ea, st, sms, stream));
   *launches += 1;
   return MLA_OK;
+}
+
+int kv_b_stage(const mla_weights_t* w, int n_tok, int t_mod, int t_off, __nv_bfloat16* kc, __nv_bfloat16* vc,
+               int cap, void* ws, const Layout& L, const DevStatusHost& st, int sms, cudaStream_t stream,
+               int* launches) {
+  return kv_b_rows(w, at<__nv_bfloat16>(ws, L.ckv), at<__nv_bfloat16>(ws, L.kpe), n_tok, t_mod, t_off, kc, vc, cap,
+                   ws, L, st, sms, stream, launches);
 }
 
 int o_proj_stage(const mla_weights_t* w, const Params& p, const void* x, void* out, int n_tok, void* ws,
@@ -288,10 +301,12 @@ using namespace mla;
 extern "C" {
 
 size_t mla_workspace_size(int mode, int B, int t_or_p, int cap) {
-  (void)cap;
   if (B < 1) return 0;
   if (mode == MLA_MODE_PREFILL) {
     if (t_or_p < 1 || (int64_t)B * t_or_p > kMaxTokens) return 0;
+  } else if (mode == MLA_MODE_CHUNK_LATENT) {
+    if (t_or_p < 1 || (int64_t)B * t_or_p > kMaxTokens || cap < t_or_p || (int64_t)B * cap > (int64_t)1 << 26)
+      return 0;
   } else if (mode == MLA_MODE_DECODE || mode == MLA_MODE_DECODE_LATENT) {
     if (t_or_p < 0 || B > kMaxTokens || t_or_p >= (1 << 24)) return 0;
   } else if (mode == MLA_MODE_FFN) {
@@ -299,7 +314,7 @@ size_t mla_workspace_size(int mode, int B, int t_or_p, int cap) {
   } else {
     return 0;
   }
-  return make_layout(mode, B, t_or_p, kMaxSmsForSizing).total;
+  return make_layout(mode, B, t_or_p, kMaxSmsForSizing, cap).total;
 }
 
 const char* mla_status_string(int s) {
@@ -330,27 +345,33 @@ int mla_device_status(const void* workspace, void* stream) {
 namespace {
 
 // Prefill of T tokens per sequence at positions P0..P0+T-1; P0 > 0 (chunked
-// prefill) attends to the P0 cached keys before the chunk's own.
+// prefill) attends to the P0 cached keys before the chunk's own.  With
+// latent_past the past is the latent cache: after the chunk's latent rows
+// are written there, keys and values of positions 0..P0+T-1 are rebuilt
+// from it into workspace scratch (one kv_b product per sequence).
 int prefill_impl(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int T, int P0,
                  void* out, void* k_cache, void* v_cache, void* ckv_cache, void* kpe_cache, int cap,
-                 void* workspace, size_t workspace_bytes, void* stream) {
+                 void* workspace, size_t workspace_bytes, void* stream, bool latent_past = false) {
   const Params p = resolve(params);
   if (B < 1 || T < 1 || P0 < 0 || (int64_t)B * T > kMaxTokens) return MLA_ERR_INVALID_ARG;
   if ((k_cache == nullptr) != (v_cache == nullptr)) return MLA_ERR_INVALID_ARG;
   if ((ckv_cache == nullptr) != (kpe_cache == nullptr)) return MLA_ERR_INVALID_ARG;
   if ((k_cache || ckv_cache) && (int64_t)P0 + T > cap) return MLA_ERR_INVALID_ARG;
-  if (P0 > 0 && (!k_cache || !out)) return MLA_ERR_INVALID_ARG;
+  if (latent_past && (k_cache || !ckv_cache || !out || (int64_t)B * cap > (int64_t)1 << 26))
+    return MLA_ERR_INVALID_ARG;
+  if (!latent_past && P0 > 0 && (!k_cache || !out)) return MLA_ERR_INVALID_ARG;
+  const int mode = latent_past ? MLA_MODE_CHUNK_LATENT : MLA_MODE_PREFILL;
   for (const void* c : {(const void*)k_cache, (const void*)v_cache, (const void*)ckv_cache, (const void*)kpe_cache})
     if (c && !aligned16(c)) return MLA_ERR_ALIGNMENT;
   const size_t n_tok = (size_t)B * T;
   const bool cache_only = (out == nullptr);
   if (cache_only && !k_cache && !ckv_cache) return MLA_ERR_INVALID_ARG;
   int rc = common_checks(w, p, x, out, n_tok, workspace, workspace_bytes,
-                         make_layout(MLA_MODE_PREFILL, B, T, kMaxSmsForSizing).total, true);
+                         make_layout(mode, B, T, kMaxSmsForSizing, cap).total, true);
   if (rc) return rc;
   const int sms = num_sms_of_current_device();
   if (sms <= 0) return MLA_ERR_CUDA;
-  const Layout L = make_layout(MLA_MODE_PREFILL, B, T, sms);
+  const Layout L = make_layout(mode, B, T, sms, cap);
 
   cudaStream_t stream_ = static_cast<cudaStream_t>(stream);
   const DevStatusHost st{at<uint32_t>(workspace, L.status), kDefaultWaitLimitNs};
@@ -369,9 +390,18 @@ int prefill_impl(const mla_weights_t* w, const mla_params_t* params, const void*
 
   __nv_bfloat16* kc = k_cache ? static_cast<__nv_bfloat16*>(k_cache) : at<__nv_bfloat16>(workspace, L.kscr);
   __nv_bfloat16* vc = v_cache ? static_cast<__nv_bfloat16*>(v_cache) : at<__nv_bfloat16>(workspace, L.vscr);
-  const int kcap = k_cache ? cap : T;
+  const int kcap = (k_cache || latent_past) ? cap : T;
   sg.start(MLA_STAGE_KV_B);
-  rc = kv_b_stage(w, (int)n_tok, T, P0, kc, vc, kcap, workspace, L, st, sms, stream_, &launches);
+  if (latent_past) {
+    const __nv_bfloat16* ckv = static_cast<const __nv_bfloat16*>(ckv_cache);
+    const __nv_bfloat16* kpe = static_cast<const __nv_bfloat16*>(kpe_cache);
+    for (int b = 0; b < B && rc == MLA_OK; ++b)
+      rc = kv_b_rows(w, ckv + (size_t)b * cap * MLA_KV_LORA, kpe + (size_t)b * cap * MLA_QK_ROPE, P0 + T, P0 + T, 0,
+                     kc + (size_t)b * MLA_HEADS * cap * MLA_QK, vc + (size_t)b * MLA_HEADS * cap * MLA_V, cap,
+                     workspace, L, st, sms, stream_, &launches);
+  } else {
+    rc = kv_b_stage(w, (int)n_tok, T, P0, kc, vc, kcap, workspace, L, st, sms, stream_, &launches);
+  }
   if (rc) return rc;
   sg.stop(MLA_STAGE_KV_B);
   if (cache_only) {
@@ -413,6 +443,14 @@ int mla_prefill_chunk(const mla_weights_t* w, const mla_params_t* params, const 
   if (!k_cache || !v_cache || !out) return MLA_ERR_INVALID_ARG;
   return prefill_impl(w, params, x, B, T, P0, out, k_cache, v_cache, ckv_cache, kpe_cache, cap, workspace,
                       workspace_bytes, stream);
+}
+
+int mla_prefill_chunk_latent(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int T,
+                             int P0, void* out, void* ckv_cache, void* kpe_cache, int cap, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (!ckv_cache || !kpe_cache || !out) return MLA_ERR_INVALID_ARG;
+  return prefill_impl(w, params, x, B, T, P0, out, nullptr, nullptr, ckv_cache, kpe_cache, cap, workspace,
+                      workspace_bytes, stream, true);
 }
 
 int mla_decode(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int P, void* k_cache,

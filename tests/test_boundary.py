@@ -151,3 +151,22 @@ def test_ffn_workspace_and_argument_checks():
     assert ffn(w, ws=None) == -3
     assert ffn(w, ws_bytes=4096) == -3
     assert ffn(w, out=FAKE + (1 << 30) + 4096) == -1  # partial overlap with x
+
+
+def test_prefill_chunk_latent_argument_checks():
+    w = fake_weights()
+    cap = 64
+    ws_bytes = m.lib().mla_workspace_size(m.MODE_CHUNK_LATENT, 1, 16, cap)
+    assert ws_bytes > m.lib().mla_workspace_size(m.MODE_PREFILL, 1, 16, cap)  # holds K/V of cap positions
+    assert m.lib().mla_workspace_size(m.MODE_CHUNK_LATENT, 1, 16, 8) == 0     # cap < T
+
+    def call(P0=8, T=16, out=FAKE + (2 << 30), ckv=FAKE + (4 << 30), kpe=FAKE + (5 << 30), nbytes=ws_bytes):
+        return m.lib().mla_prefill_chunk_latent(ctypes.byref(w), None, FAKE + (1 << 30), 1, T, P0, out, ckv, kpe,
+                                                cap, FAKE + (3 << 30), nbytes, None)
+    assert call(P0=-1) == -1
+    assert call(P0=49) == -1           # P0 + T > cap
+    assert call(ckv=None) == -1
+    assert call(kpe=None) == -1
+    assert call(out=None) == -1
+    assert call(kpe=FAKE + (5 << 30) + 8) == -2
+    assert call(nbytes=ws_bytes - 256) == -3

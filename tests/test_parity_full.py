@@ -5,7 +5,7 @@ times, on sampled outputs the oracle can compute one by one.
   GPU runs the whole batch; the oracle projects keys/values for every token
   of the sampled sequences and queries only at sampled positions.
 * chunked prefill B=1, T=2048 after P0=2048 cached positions (oracle-built
-  caches), sampled query rows.
+  caches, rebuilt and latent forms), sampled query rows.
 * decode B=64, P=1000 (rebuilt cache) and latent decode B=128, P=8192: the
   GPU fills every cache with its own cache-only prefill of the seeded
   'cache_x' tokens (checked against the oracle's caches for the sampled
@@ -97,6 +97,34 @@ def test_prefill_chunk_b1_p2048_t2048(W):
     parity_out(cuda_to_f64(out[0, rows]), ref["out"][0], "chunk out")
     parity_cache(cuda_to_f64(kc[0][:, [P0 + r for r in rows]]), ref["K"][0][:, rows], "chunk K rows")
     parity_cache(cuda_to_f64(vc[0][:, [P0 + r for r in rows]]), ref["V"][0][:, rows], "chunk V rows")
+
+
+def test_prefill_chunk_latent_b1_p2048_t2048(W):
+    """The same chunk against the latent cache (the bench's latent chunk
+    workload): the oracle's bf16 latent rows of the seeded 'cache_x' tokens
+    on both sides, sampled query rows."""
+    import torch
+    B, P0, T = 1, 2048, 2048
+    cap = P0 + T
+    xc = synth.bf16_bits_to_f64(synth.tensor_bits(0, "cache_x", (B, P0, D), synth.X_DIST))
+    c = om.cache_from_tokens(W[2], xc)
+    Cb, Rb = f64_to_bits(c["ckv"]), f64_to_bits(c["kpe"])
+    ckv = torch.zeros((B, cap, 512), dtype=torch.bfloat16, device="cuda")
+    kpe = torch.zeros((B, cap, 64), dtype=torch.bfloat16, device="cuda")
+    ckv[:, :P0].copy_(bits_to_cuda(Cb))
+    kpe[:, :P0].copy_(bits_to_cuda(Rb))
+    x = synth.tensor_cuda(0, "x", (B, T, D), synth.X_DIST)
+    out = torch.empty_like(x)
+    ws = m.alloc_workspace(m.MODE_CHUNK_LATENT, B, T, cap=cap)
+    m.mla_prefill_chunk_latent(W[1], x, P0, out, ckv, kpe, ws)
+    torch.cuda.synchronize()
+    assert m.mla_device_status(ws) == 0
+    rows = [0, 1, 127, 128, 1000, 2046, 2047]
+    xb = synth.bf16_bits_to_f64(synth.tensor_bits(0, "x", (B, T, D), synth.X_DIST))
+    ref = om.prefill_with_past_latent(W[2], xb, synth.bf16_bits_to_f64(Cb), synth.bf16_bits_to_f64(Rb),
+                                      query_rows=rows)
+    parity_out(cuda_to_f64(out[0, rows]), ref["out"][0], "latent chunk out")
+    parity_cache(cuda_to_f64(ckv[0, [P0 + r for r in rows]]), ref["ckv"][0][rows], "latent chunk rows")
 
 
 def _fill_caches(W, B, P, cap, rebuilt):

@@ -219,6 +219,54 @@ def test_prefill_in_two_chunks_equals_whole_prefill(W):
     parity_cache(cuda_to_f64(kc), ref["K"], "K cache")
 
 
+@pytest.mark.parametrize("B,P0,T", [(2, 100, 37), (1, 128, 256), (2, 0, 40), (1, 300, 1)])
+def test_prefill_chunk_latent_parity(W, B, P0, T):
+    """Chunk against the latent cache (oracle-built bf16 latent rows on both
+    sides): the past keys and values are rebuilt from the cache."""
+    import torch
+    cap = P0 + T + 5
+    (_, _, Cb, Rb), (_, _, C64, R64) = make_caches(W, B, P0, cap)
+    xb = synth.tensor_bits(0, "x", (B, T, 7168), synth.X_DIST)
+    x = bits_to_cuda(xb)
+    ckv, kpe = bits_to_cuda(Cb), bits_to_cuda(Rb)
+    out = torch.empty_like(x)
+    delta = torch.empty((B, T, 7168), dtype=torch.float32, device="cuda")
+    wsp = m.alloc_workspace(m.MODE_CHUNK_LATENT, B, T, cap=cap)
+    m.mla_prefill_chunk_latent(W[1], x, P0, out, ckv, kpe, wsp, m.make_params(delta_out=delta))
+    torch.cuda.synchronize()
+    assert m.mla_device_status(wsp) == 0
+    ref = om.prefill_with_past_latent(W[2], synth.bf16_bits_to_f64(xb), C64, R64)
+    parity(cuda_to_f64(delta), ref["delta"], "delta")
+    parity_out(cuda_to_f64(out), ref["out"], "out")
+    parity_cache(cuda_to_f64(ckv[:, P0:P0 + T]), ref["ckv"], "new latent rows")
+    parity_cache(cuda_to_f64(kpe[:, P0:P0 + T]), ref["kpe"], "new rotary-key rows")
+    bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(bits(ckv[:, :P0]), Cb[:, :P0])
+    assert np.array_equal(bits(kpe[:, :P0]), Rb[:, :P0])
+    assert torch.count_nonzero(ckv[:, P0 + T:]).item() == 0
+
+
+def test_latent_prefill_then_latent_chunk_equals_whole_prefill(W):
+    """GPU prefill writes the latent cache of the first T1 tokens, a GPU
+    latent chunk runs the next T2: every output row matches the oracle's
+    prefill of all T1 + T2 tokens."""
+    import torch
+    B, T1, T2 = 2, 70, 90
+    T = T1 + T2
+    xb = synth.tensor_bits(0, "x", (B, T, 7168), synth.X_DIST)
+    x = bits_to_cuda(xb)
+    ckv = torch.zeros((B, T, 512), dtype=torch.bfloat16, device="cuda")
+    kpe = torch.zeros((B, T, 64), dtype=torch.bfloat16, device="cuda")
+    x1, x2 = x[:, :T1].contiguous(), x[:, T1:].contiguous()
+    o1, o2 = torch.empty_like(x1), torch.empty_like(x2)
+    m.mla_prefill(W[1], x1, o1, m.alloc_workspace(m.MODE_PREFILL, B, T1), None, None, ckv, kpe, T)
+    m.mla_prefill_chunk_latent(W[1], x2, T1, o2, ckv, kpe, m.alloc_workspace(m.MODE_CHUNK_LATENT, B, T2, cap=T))
+    torch.cuda.synchronize()
+    ref = om.prefill(W[2], synth.bf16_bits_to_f64(xb))
+    parity_out(cuda_to_f64(torch.cat([o1, o2], dim=1)), ref["out"], "two chunks, latent cache")
+    parity_cache(cuda_to_f64(ckv), ref["ckv"], "latent cache")
+
+
 def test_prefill_chunk_rejects_bad_arguments(W):
     import torch
     B, T, P0 = 1, 8, 10
