@@ -166,10 +166,19 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.rows)}
 
 
-def kernel_source_hash():
+# The sources each kernel's code and launch configuration come from.
+KERNEL_SOURCES = {
+    "gemm": ["gemm.cu", "common.cuh", "internal.h"],
+    "attn_prefill": ["attn_prefill.cu", "common.cuh", "internal.h"],
+    "attn_decode": ["attn_decode.cu", "common.cuh", "internal.h"],
+}
+
+
+def kernel_source_hash(files=None):
+    """sha256 (16 hex digits) of the named files under mla_gb300/csrc (all of them by default)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files if files is not None else os.listdir(csrc)):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -182,7 +191,7 @@ def ncu_traffic(kernel_stage, config):
         return None
     d = json.load(open(p))
     e = d.get(f"{config}:{kernel_stage}")
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(KERNEL_SOURCES[e["kernel_sources"]]):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -477,10 +486,13 @@ def run_profile(args):
     torch.cuda.set_device(0)
     r = Runner("cuda:0")
     keep = None
+    mcl = re.fullmatch(r"chunk_latent_b(\d+)_p(\d+)_t(\d+)", args.profile)
     mc = re.fullmatch(r"chunk_b(\d+)_p(\d+)_t(\d+)", args.profile)
     mf = re.fullmatch(r"ffn_n(\d+)", args.profile)
     mt = re.fullmatch(r"(prefill|decode|latent)_b(\d+)_([tp])(\d+)(_cache)?", args.profile)
-    if mc:
+    if mcl:
+        step, keep = r.chunk_latent_step_fn(int(mcl.group(1)), int(mcl.group(2)), int(mcl.group(3)))
+    elif mc:
         step, keep = r.chunk_step_fn(int(mc.group(1)), int(mc.group(2)), int(mc.group(3)))
     elif mf:
         step, keep = r.ffn_step_fn(int(mf.group(1)))
@@ -516,7 +528,7 @@ def main():
                     help="tokens of the headline sequence the CPU oracle baseline runs (0 = skip)")
     ap.add_argument("--profile", default=None,
                     help="run one step of one configuration for a profiler and exit: prefill_bB_tT[_cache], "
-                         "chunk_bB_pP0_tT (chunked prefill after P0 cached positions), ffn_nN (MLP half, N rows), "
+                         "chunk_bB_pP0_tT / chunk_latent_bB_pP0_tT (chunked prefill on either cache), ffn_nN (MLP half, N rows), "
                          "decode_bB_pP (rebuilt cache) or latent_bB_pP; only that step lies between "
                          "cudaProfilerStart/Stop (ncu --profile-from-start off)")
     args = ap.parse_args()

@@ -44,6 +44,10 @@ Layout make_layout(int mode, int B, int t_or_p, int num_sms, int cap = 0) {
     const size_t rows = (size_t)B * t_or_p;
     L.xn = take(rows * MLA_D * 2);
     L.h = take(rows * MLA_FFN_INTER * 2);
+    if (rows <= 128) {  // decode-size rows: split-K slots for the down product
+      L.split_bytes = split_part_bytes((int)rows);
+      L.split = take(L.split_bytes);
+    }
     L.total = off;
     return L;
   }
@@ -650,6 +654,7 @@ int mla_ffn(const mla_ffn_weights_t* w, const mla_params_t* params, const void* 
     ea.ldo = MLA_D;
     ea.x = xb;
     ea.delta = p.delta;
+    set_split(ea, workspace, L);
     MLA_TRY(launch_gemm(s, op, Epi::kResidual, ea, st, sms, stream_));
     launches += 1;
   }

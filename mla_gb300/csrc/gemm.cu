@@ -955,6 +955,10 @@ cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, con
       // o_proj: W_o (117 MB) does not stay in L2 -> waves of 16 row blocks
       GemmShape g16 = s;
       g16.raster_g = 16;
+      // long K (the MLP's down product, K = 18432): 128-wide tiles split in two
+      // K halves stream the weights faster than 64-wide whole-K tiles
+      if (tiny && k256 && s.K >= 16384)
+        return launch_impl<64, 128, 4, Epi::kResidual, false, 2>(s, op, ea, st, num_sms, stream);
       if (tiny && k256) return launch_impl<64, 64, 3, Epi::kResidual, false, 4>(s, op, ea, st, num_sms, stream);
       if (small && k256) return launch_impl<128, 64, 4, Epi::kResidual, false, 2>(s, op, ea, st, num_sms, stream);
       if (small) return launch_impl<128, 64, 8, Epi::kResidual, false>(s, op, ea, st, num_sms, stream);
