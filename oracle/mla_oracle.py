@@ -277,6 +277,30 @@ def decode(w: dict, x_new: np.ndarray, K_cache: np.ndarray, V_cache: np.ndarray,
             "ckv_new": t["ckv"], "kpe_new": t["kpe"]}
 
 
+def decode_varlen(w: dict, x_new: np.ndarray, K_cache: np.ndarray, V_cache: np.ndarray, lengths,
+                  dims: Dims = KIMI_K2, eps: float = DEFAULT_EPS, base: float = DEFAULT_ROPE_BASE,
+                  scale: float | None = None) -> dict:
+    """One decode step for sequences of different lengths: sequence b's new
+    token sits at position P_b = lengths[b] and attends to the P_b + 1 keys
+    of its own cache rows 0..P_b-1 plus itself ("Mix and project" page:
+    every sequence is its own cache update and score row; sequences do not
+    interact).  K_cache [B, H, >= max P_b, qk], V_cache likewise; rows at or
+    beyond P_b are ignored.  Returns the stacked per-sequence results."""
+    res = [decode(w, x_new[b:b + 1], K_cache[b:b + 1, :, :int(P)], V_cache[b:b + 1, :, :int(P)], dims, eps, base,
+                  scale) for b, P in enumerate(lengths)]
+    return {k: np.concatenate([r[k] for r in res], axis=0) for k in res[0]}
+
+
+def decode_latent_varlen(w: dict, x_new: np.ndarray, ckv_cache: np.ndarray, kpe_cache: np.ndarray, lengths,
+                         dims: Dims = KIMI_K2, eps: float = DEFAULT_EPS, base: float = DEFAULT_ROPE_BASE,
+                         scale: float | None = None) -> dict:
+    """``decode_varlen`` against the latent cache (rows 0..P_b-1 of each
+    sequence's ckv / kpe)."""
+    res = [decode_latent(w, x_new[b:b + 1], ckv_cache[b:b + 1, :int(P)], kpe_cache[b:b + 1, :int(P)], dims, eps,
+                         base, scale) for b, P in enumerate(lengths)]
+    return {k: np.concatenate([r[k] for r in res], axis=0) for k in res[0]}
+
+
 def rebuild_kv(w: dict, ckv: np.ndarray, kpe: np.ndarray, dims: Dims = KIMI_K2):
     """Per-head K/V from the latent cache (key-value compression page: the key
     content and values of all heads are rebuilt from one latent per position).

@@ -389,6 +389,46 @@ def test_latent_chunk_rope_key_not_rebuilt_from_latent_fails(monkeypatch):
     assert not np.allclose(bad["out"], whole["out"][:, 4:], rtol=1e-6, atol=1e-8)
 
 
+def test_varlen_decode_equal_lengths_is_batched_decode():
+    dims = TINY2
+    w = rand_weights(dims, 72)
+    cache = om.cache_from_tokens(w, rand_x((3, 6, dims.d), 73), dims)
+    xn = rand_x((3, dims.d), 74)
+    ref = om.decode(w, xn, cache["K"], cache["V"], dims)
+    got = om.decode_varlen(w, xn, cache["K"], cache["V"], [6, 6, 6], dims)
+    for k in ("out", "k_new", "v_new"):
+        np.testing.assert_allclose(got[k], ref[k], rtol=1e-12, atol=1e-13)
+    lat = om.decode_latent_varlen(w, xn, cache["ckv"], cache["kpe"], [6, 6, 6], dims)
+    np.testing.assert_allclose(lat["out"], ref["out"], rtol=1e-10, atol=1e-11)
+
+
+def test_varlen_decode_rows_equal_prefill_rows():
+    """Sequence b of length P_b: its decode output equals row P_b of the
+    prefill of its first P_b + 1 tokens (a ragged batch, both cache forms);
+    rows of the cache beyond P_b (filled with noise) do not matter."""
+    dims = TINY2
+    w = rand_weights(dims, 75)
+    lengths = [2, 7, 4]
+    x = rand_x((3, 8, dims.d), 76)
+    cache = om.cache_from_tokens(w, x, dims)
+    K = cache["K"].copy()
+    V = cache["V"].copy()
+    C = cache["ckv"].copy()
+    R = cache["kpe"].copy()
+    for b, P in enumerate(lengths):  # noise where the sequence has no keys yet
+        K[b, :, P:] = 50.0
+        V[b, :, P:] = -50.0
+        C[b, P:] = 50.0
+        R[b, P:] = 50.0
+    xn = np.stack([x[b, P] for b, P in enumerate(lengths)])
+    got = om.decode_varlen(w, xn, K, V, lengths, dims)
+    lat = om.decode_latent_varlen(w, xn, C, R, lengths, dims)
+    for b, P in enumerate(lengths):
+        ref = om.prefill(w, x[b:b + 1, :P + 1], dims, query_rows=[P])
+        np.testing.assert_allclose(got["out"][b], ref["out"][0, 0], rtol=1e-10, atol=1e-11)
+        np.testing.assert_allclose(lat["out"][b], ref["out"][0, 0], rtol=1e-10, atol=1e-11)
+
+
 def test_latent_absorbed_equals_rebuilt():
     dims = TINY2
     w = rand_weights(dims, 39)
