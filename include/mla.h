@@ -213,6 +213,26 @@ int mla_decode_latent(const mla_weights_t* w, const mla_params_t* params, const 
                       int P, void* ckv_cache, void* kpe_cache, int cap, void* out,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same two decode steps for a batch of sequences of different lengths
+ * (a ragged batch: "Mix and project" page, each sequence its own cache update
+ * and score row).  Sequence b's new token sits at position P[b] and attends
+ * to its P[b] + 1 keys; its cache row P[b] is written.
+ *   P      int [B] in DEVICE memory (4-byte aligned), read by the kernels, so
+ *          a captured CUDA graph can be replayed with new lengths
+ *   P_max  an upper bound of every P[b]; it sizes the launch and the
+ *          workspace: mla_workspace_size(MLA_MODE_DECODE or
+ *          MLA_MODE_DECODE_LATENT, B, P_max, cap); requires P_max + 1 <= cap
+ * A P[b] outside [0, P_max] cannot be checked on the host: the kernels clamp
+ * it into that range (no access leaves the caches) and record it, and
+ * mla_device_status then returns MLA_ERR_INVALID_ARG.
+ * Other arguments, results and errors as mla_decode / mla_decode_latent. */
+int mla_decode_varlen(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, const int* P,
+                      int P_max, void* k_cache, void* v_cache, int cap, void* out, void* workspace,
+                      size_t workspace_bytes, void* stream);
+int mla_decode_latent_varlen(const mla_weights_t* w, const mla_params_t* params, const void* x, int B,
+                             const int* P, int P_max, void* ckv_cache, void* kpe_cache, int cap, void* out,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
 /* mla_decode without a workspace argument.  The pages have no counterpart
  * to this entry point: it exists for callers that cannot allocate device
  * memory (code running under a host framework that owns all device memory
@@ -268,8 +288,10 @@ int mla_ffn(const mla_ffn_weights_t* w, const mla_params_t* params, const void* 
             void* workspace, size_t workspace_bytes, void* stream);
 
 /* Synchronises `stream` and reads the device status word the last call on
- * this workspace left: MLA_OK, or MLA_ERR_TIMEOUT if a bounded device wait
- * gave up (the kernel then skipped its remaining work and returned).
+ * this workspace left: MLA_OK, MLA_ERR_TIMEOUT if a bounded device wait
+ * gave up (the kernel then skipped its remaining work and returned), or
+ * MLA_ERR_INVALID_ARG if a per-sequence position of a _varlen call was
+ * outside [0, P_max].
  * MLA_ERR_CUDA if the synchronisation itself fails. */
 int mla_device_status(const void* workspace, void* stream);
 

@@ -73,6 +73,10 @@ _SIGS = {
                         _VP, _SZ, _VP]),
     "mla_decode_latent": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _VP, _VP, _I,
                                _VP, _VP, _SZ, _VP]),
+    "mla_decode_varlen": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _VP, _I, _VP, _VP,
+                               _I, _VP, _VP, _SZ, _VP]),
+    "mla_decode_latent_varlen": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _VP, _I, _VP,
+                                      _VP, _I, _VP, _VP, _SZ, _VP]),
     "mla_decode_noalloc": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _VP, _VP, _I,
                                 _VP, _VP]),
     "mla_ffn": (_I, [ctypes.POINTER(MlaFfnWeights), ctypes.POINTER(MlaParams), _VP, _I, _VP, _VP, _SZ, _VP]),
@@ -215,6 +219,28 @@ def mla_decode_latent(weights: MlaWeights, x, P: int, ckv_cache, kpe_cache, out,
                                  B, P, _ptr(ckv_cache), _ptr(kpe_cache), cap, _ptr(out), _ptr(workspace),
                                  workspace.numel(), _stream(stream))
     _check(rc, "mla_decode_latent")
+
+
+def mla_decode_varlen(weights: MlaWeights, x, P, P_max: int, k_cache, v_cache, out, workspace,
+                      params: MlaParams | None = None, stream=None):
+    """Ragged decode: P is an int32 CUDA tensor [B] of per-sequence positions (<= P_max)."""
+    B = x.shape[0]
+    cap = k_cache.shape[2]
+    rc = lib().mla_decode_varlen(ctypes.byref(weights), None if params is None else ctypes.byref(params), _ptr(x), B,
+                                 _ptr(P), P_max, _ptr(k_cache), _ptr(v_cache), cap, _ptr(out), _ptr(workspace),
+                                 workspace.numel(), _stream(stream))
+    _check(rc, "mla_decode_varlen")
+
+
+def mla_decode_latent_varlen(weights: MlaWeights, x, P, P_max: int, ckv_cache, kpe_cache, out, workspace,
+                             params: MlaParams | None = None, stream=None):
+    """Ragged latent decode: P is an int32 CUDA tensor [B] of per-sequence positions (<= P_max)."""
+    B = x.shape[0]
+    cap = ckv_cache.shape[1]
+    rc = lib().mla_decode_latent_varlen(ctypes.byref(weights), None if params is None else ctypes.byref(params),
+                                        _ptr(x), B, _ptr(P), P_max, _ptr(ckv_cache), _ptr(kpe_cache), cap, _ptr(out),
+                                        _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "mla_decode_latent_varlen")
 
 
 def mla_decode_noalloc(weights: MlaWeights, x, P: int, k_cache, v_cache, out, params: MlaParams | None = None,

@@ -20,7 +20,7 @@ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 // Workspace carve-up.  Offsets are computed identically by the size query
 // and by the entry points.
 struct Layout {
-  size_t status, cs, xn, ca, cq, ckv, kpe, q, o, kscr, vscr, qlat, olat, part_o, part_ml, split, h, total;
+  size_t status, cs, xn, ca, cq, ckv, kpe, q, o, kscr, vscr, qlat, olat, part_o, part_ml, split, h, plan, total;
   size_t split_bytes;  // split-K partial slots (decode modes), 0 = none
 };
 
@@ -51,7 +51,7 @@ Layout make_layout(int mode, int B, int t_or_p, int num_sms, int cap = 0) {
     L.total = off;
     return L;
   }
-  L.cs = take(npos * 32 * sizeof(float2));
+  if (pre) L.cs = take(npos * 32 * sizeof(float2));
   L.xn = take(n * MLA_D * 2);
   L.ca = take(n * 2112 * 4);
   L.cq = take(n * MLA_Q_LORA * 2);
@@ -59,6 +59,10 @@ Layout make_layout(int mode, int B, int t_or_p, int num_sms, int cap = 0) {
   L.kpe = take(n * MLA_QK_ROPE * 2);
   L.q = take(n * MLA_HEADS * MLA_QK * 2);
   L.o = take(n * MLA_HEADS * MLA_V * 2);
+  // decode: the RoPE table (one row per sequence, 256 B, written by the
+  // latent split and read by the q_b epilogue) lives in the attention output
+  // region, which nothing writes before the attention
+  if (!pre) L.cs = L.o;
   if (pre) {
     // K/V scratch: the chunk's positions (prefill without caches), or every
     // position up to cap rebuilt from the latent cache (latent chunk)
@@ -75,6 +79,7 @@ Layout make_layout(int mode, int B, int t_or_p, int num_sms, int cap = 0) {
     L.olat = take((size_t)B * MLA_HEADS * MLA_KV_LORA * 2);
     L.part_o = take((size_t)2 * g * MLA_HEADS * MLA_KV_LORA * sizeof(float));
     L.part_ml = take((size_t)2 * g * MLA_HEADS * sizeof(float2));
+    L.plan = take(latent_plan_ints(B, g) * sizeof(int));
   }
   if (!pre) {
     L.split_bytes = split_part_bytes(B);
@@ -170,7 +175,7 @@ T* at(void* ws, size_t off) {
 int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok, int n_pos, int pos0,
               int t_mod, int t_off, __nv_bfloat16* ckv_cache, __nv_bfloat16* kpe_cache, int cap, void* ws,
               const Layout& L, const DevStatusHost& st, int sms, cudaStream_t stream, Stager& sg,
-              int* launches, bool with_q = true) {
+              int* launches, bool with_q = true, const int* pos = nullptr, int pos_max = 0) {
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   (void)n_pos;
   sg.start(MLA_STAGE_INPUT_NORM);
@@ -213,6 +218,9 @@ int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok,
     la.t_off = t_off;
     la.cap = cap;
     la.eps = p.eps;
+    la.pos = pos;
+    la.pos_max = pos_max;
+    la.status = st.word;
     MLA_TRY(launch_latent_split(la, stream));
     *launches += 1;
   }
@@ -229,7 +237,7 @@ int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok,
     ea.out = at<__nv_bfloat16>(ws, L.q);
     ea.ldo = MLA_HEADS * MLA_QK;
     ea.cs = at<float2>(ws, L.cs);
-    ea.t_mod = t_mod;
+    ea.t_mod = pos ? n_tok : t_mod;  // per-row positions: one RoPE table row per token
     set_split(ea, ws, L);
     MLA_TRY(launch_gemm(s, op, Epi::kQRope, ea, st, sms, stream));
     *launches += 1;
@@ -242,7 +250,8 @@ int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok,
 // K/V of row r at sequence r / t_mod, position t_off + r % t_mod.
 int kv_b_rows(const mla_weights_t* w, const __nv_bfloat16* ckv, const __nv_bfloat16* kpe, int n_tok, int t_mod,
               int t_off, __nv_bfloat16* kc, __nv_bfloat16* vc, int cap, void* ws, const Layout& L,
-              const DevStatusHost& st, int sms, cudaStream_t stream, int* launches) {
+              const DevStatusHost& st, int sms, cudaStream_t stream, int* launches, const int* pos = nullptr,
+              int pos_max = 0) {
   GemmShape s{n_tok, MLA_HEADS * 256, MLA_KV_LORA, 1, 0, 0, 0, 0, MLA_HEADS * 256};
   GemmOperands op{ckv, MLA_KV_LORA, n_tok,
                   static_cast<const __nv_bfloat16*>(w->w_kv_b), MLA_KV_LORA, MLA_HEADS * 256,
@@ -255,6 +264,8 @@ int kv_b_rows(const mla_weights_t* w, const __nv_bfloat16* ckv, const __nv_bfloa
   ea.t_mod = t_mod;
   ea.t_off = t_off;
   ea.cap = cap;
+  ea.pos = pos;
+  ea.pos_max = pos_max;
   set_split(ea, ws, L);
   MLA_TRY(launch_gemm(s, op, Epi::kKVCache, ea, st, sms, stream));
   *launches += 1;
@@ -263,9 +274,9 @@ int kv_b_rows(const mla_weights_t* w, const __nv_bfloat16* ckv, const __nv_bfloa
 
 int kv_b_stage(const mla_weights_t* w, int n_tok, int t_mod, int t_off, __nv_bfloat16* kc, __nv_bfloat16* vc,
                int cap, void* ws, const Layout& L, const DevStatusHost& st, int sms, cudaStream_t stream,
-               int* launches) {
+               int* launches, const int* pos = nullptr, int pos_max = 0) {
   return kv_b_rows(w, at<__nv_bfloat16>(ws, L.ckv), at<__nv_bfloat16>(ws, L.kpe), n_tok, t_mod, t_off, kc, vc, cap,
-                   ws, L, st, sms, stream, launches);
+                   ws, L, st, sms, stream, launches, pos, pos_max);
 }
 
 int o_proj_stage(const mla_weights_t* w, const Params& p, const void* x, void* out, int n_tok, void* ws,
@@ -341,7 +352,8 @@ int mla_device_status(const void* workspace, void* stream) {
   if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return MLA_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
-  return (word & kStatusTimeout) ? MLA_ERR_TIMEOUT : MLA_OK;
+  if (word & kStatusTimeout) return MLA_ERR_TIMEOUT;
+  return (word & kStatusBadLength) ? MLA_ERR_INVALID_ARG : MLA_OK;
 }
 
 }  // extern "C"
@@ -457,11 +469,19 @@ int mla_prefill_chunk_latent(const mla_weights_t* w, const mla_params_t* params,
                       workspace_bytes, stream, true);
 }
 
-int mla_decode(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int P, void* k_cache,
-               void* v_cache, int cap, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// One decode step, rebuilt cache.  pos = null: every sequence at position P;
+// else sequence b at position pos[b] (device array), P = an upper bound.
+int decode_impl(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int P, const int* pos,
+                void* k_cache, void* v_cache, int cap, void* out, void* workspace, size_t workspace_bytes,
+                void* stream) {
   const Params p = resolve(params);
   if (B < 1 || B > kMaxTokens || P < 0 || P >= (1 << 24)) return MLA_ERR_INVALID_ARG;
   if (!k_cache || !v_cache || cap < P + 1) return MLA_ERR_INVALID_ARG;
+  if (pos && (reinterpret_cast<uintptr_t>(pos) & 3)) return MLA_ERR_ALIGNMENT;
   if (!aligned16(k_cache) || !aligned16(v_cache)) return MLA_ERR_ALIGNMENT;
   int rc = common_checks(w, p, x, out, (size_t)B, workspace, workspace_bytes,
                          make_layout(MLA_MODE_DECODE, B, P, kMaxSmsForSizing).total);
@@ -475,13 +495,14 @@ int mla_decode(const mla_weights_t* w, const mla_params_t* params, const void* x
   Stager sg{p.timing, stream_};
   int launches = 0;
   if (cudaMemsetAsync(st.word, 0, kStatusRegion, stream_) != cudaSuccess) return MLA_ERR_CUDA;
-  rc = front_end(w, p, x, B, 1, P, 1, P, nullptr, nullptr, cap, workspace, L, st, sms, stream_, sg, &launches);
+  rc = front_end(w, p, x, B, 1, P, 1, P, nullptr, nullptr, cap, workspace, L, st, sms, stream_, sg, &launches, true,
+                 pos, P);
   if (rc) return rc;
 
   __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(k_cache);
   __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(v_cache);
   sg.start(MLA_STAGE_KV_B);
-  rc = kv_b_stage(w, B, 1, P, kc, vc, cap, workspace, L, st, sms, stream_, &launches);
+  rc = kv_b_stage(w, B, 1, P, kc, vc, cap, workspace, L, st, sms, stream_, &launches, pos, P);
   if (rc) return rc;
   sg.stop(MLA_STAGE_KV_B);
 
@@ -499,6 +520,7 @@ int mla_decode(const mla_weights_t* w, const mla_params_t* params, const void* x
     a.cap = cap;
     a.splits = decode_splits(B, P + 1, sms);
     a.scale = p.scale;
+    a.lens_pos = pos;
     if (launch_decode_attention(a, st, stream_, &launches) != cudaSuccess) return MLA_ERR_CUDA;
   }
   sg.stop(MLA_STAGE_ATTN);
@@ -511,12 +533,14 @@ int mla_decode(const mla_weights_t* w, const mla_params_t* params, const void* x
   return MLA_OK;
 }
 
-int mla_decode_latent(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int P,
-                      void* ckv_cache, void* kpe_cache, int cap, void* out, void* workspace, size_t workspace_bytes,
-                      void* stream) {
+// One decode step, latent cache; pos as decode_impl.
+int decode_latent_impl(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int P,
+                       const int* pos, void* ckv_cache, void* kpe_cache, int cap, void* out, void* workspace,
+                       size_t workspace_bytes, void* stream) {
   const Params p = resolve(params);
   if (B < 1 || B > kMaxTokens || P < 0 || P >= (1 << 24)) return MLA_ERR_INVALID_ARG;
   if (!ckv_cache || !kpe_cache || cap < P + 1) return MLA_ERR_INVALID_ARG;
+  if (pos && (reinterpret_cast<uintptr_t>(pos) & 3)) return MLA_ERR_ALIGNMENT;
   if (!aligned16(ckv_cache) || !aligned16(kpe_cache)) return MLA_ERR_ALIGNMENT;
   int rc = common_checks(w, p, x, out, (size_t)B, workspace, workspace_bytes,
                          make_layout(MLA_MODE_DECODE_LATENT, B, P, kMaxSmsForSizing).total);
@@ -531,7 +555,8 @@ int mla_decode_latent(const mla_weights_t* w, const mla_params_t* params, const 
   int launches = 0;
   if (cudaMemsetAsync(st.word, 0, kStatusRegion, stream_) != cudaSuccess) return MLA_ERR_CUDA;
   rc = front_end(w, p, x, B, 1, P, 1, P, static_cast<__nv_bfloat16*>(ckv_cache),
-                 static_cast<__nv_bfloat16*>(kpe_cache), cap, workspace, L, st, sms, stream_, sg, &launches);
+                 static_cast<__nv_bfloat16*>(kpe_cache), cap, workspace, L, st, sms, stream_, sg, &launches, true,
+                 pos, P);
   if (rc) return rc;
 
   const __nv_bfloat16* wkvb = static_cast<const __nv_bfloat16*>(w->w_kv_b);
@@ -567,6 +592,8 @@ int mla_decode_latent(const mla_weights_t* w, const mla_params_t* params, const 
     a.cap = cap;
     a.ctas = latent_ctas(B, P + 1, sms);
     a.scale = p.scale;
+    a.pos = pos;
+    a.plan = at<int>(workspace, L.plan);
     if (launch_latent_attention(a, st, stream_, &launches) != cudaSuccess) return MLA_ERR_CUDA;
   }
   sg.stop(MLA_STAGE_ATTN);
@@ -594,6 +621,37 @@ int mla_decode_latent(const mla_weights_t* w, const mla_params_t* params, const 
   sg.stop(MLA_STAGE_O_PROJ);
   if (p.timing) p.timing->n_launches = launches;
   return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int P, void* k_cache,
+               void* v_cache, int cap, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl(w, params, x, B, P, nullptr, k_cache, v_cache, cap, out, workspace, workspace_bytes, stream);
+}
+
+int mla_decode_varlen(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, const int* P,
+                      int P_max, void* k_cache, void* v_cache, int cap, void* out, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (!P) return MLA_ERR_INVALID_ARG;
+  return decode_impl(w, params, x, B, P_max, P, k_cache, v_cache, cap, out, workspace, workspace_bytes, stream);
+}
+
+int mla_decode_latent(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int P,
+                      void* ckv_cache, void* kpe_cache, int cap, void* out, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  return decode_latent_impl(w, params, x, B, P, nullptr, ckv_cache, kpe_cache, cap, out, workspace,
+                            workspace_bytes, stream);
+}
+
+int mla_decode_latent_varlen(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, const int* P,
+                             int P_max, void* ckv_cache, void* kpe_cache, int cap, void* out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (!P) return MLA_ERR_INVALID_ARG;
+  return decode_latent_impl(w, params, x, B, P_max, P, ckv_cache, kpe_cache, cap, out, workspace, workspace_bytes,
+                            stream);
 }
 
 int mla_ffn(const mla_ffn_weights_t* w, const mla_params_t* params, const void* x, int n_tok, void* out,

@@ -44,9 +44,6 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const DecodeAttnArgs a
   const int h = blockIdx.y;
   const int b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int key_begin = split * chunk_len;
-  const int key_end = min(a.L, key_begin + chunk_len);
-  const int nchunks = (key_end - key_begin + kDecChunk - 1) / kDecChunk;
   const size_t slot0 = ((size_t)b * 64 + h) * a.cap;
   const __nv_bfloat16* kbase = a.k + slot0 * 192;
   const __nv_bfloat16* vbase = a.v + slot0 * 128;
@@ -58,6 +55,12 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const DecodeAttnArgs a
   __syncthreads();
   pdl_launch_dependents();
   pdl_wait();
+  // keys of this sequence: L, or P_b + 1 with per-sequence lengths (a split
+  // beyond them has no keys and leaves an empty partial: m = -inf, l = 0)
+  const int Lb = a.lens_pos ? clamp_pos(a.lens_pos[b], a.L - 1) + 1 : a.L;
+  const int key_begin = split * chunk_len;
+  const int key_end = min(Lb, key_begin + chunk_len);
+  const int nchunks = key_end > key_begin ? (key_end - key_begin + kDecChunk - 1) / kDecChunk : 0;
 
   auto issue = [&](int c) {
     const int stg = c % kDecStages;
@@ -262,6 +265,76 @@ __device__ __forceinline__ long long lat_range_start(int g, long long total, int
 
 __device__ __forceinline__ void named_sync_128() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// Walk over a CTA's range of (sequence, tile) work.  Every sequence has
+// L = p_max + 1 keys, or P_b + 1 with per-sequence lengths (read when the
+// walk enters the sequence).
+struct SeqWalk {
+  const int* pos;
+  int p_max, B;
+  int b, t, len, nt;  // current sequence, tile within it, its keys and tiles
+  __device__ __forceinline__ void enter(int s) {
+    b = s;
+    len = !pos ? p_max + 1 : (s < B ? clamp_pos(pos[s], p_max) + 1 : 1);
+    nt = (len + kLatTile - 1) / kLatTile;
+  }
+  __device__ __forceinline__ void start(int first_seq, int first_t) {
+    enter(first_seq);
+    t = first_t - 1;
+  }
+  __device__ __forceinline__ void next() {
+    if (++t == nt) {
+      t = 0;
+      enter(b + 1);
+    }
+  }
+};
+
+// The work plan for per-sequence lengths (one CTA of 1024 threads):
+// flattened tile offsets of the sequences, then each persistent CTA's first
+// sequence, first tile and tile count (the same equal cut of the total as
+// the uniform case).
+__global__ void __launch_bounds__(1024) latent_plan_kernel(const int* __restrict__ pos, int B, int p_max, int G,
+                                                           int* __restrict__ plan) {
+  __shared__ int part[1024];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int tid = threadIdx.x;
+  const int per = (B + 1023) / 1024;
+  const int s0 = min(B, tid * per), s1 = min(B, s0 + per);
+  int sum = 0;
+  for (int s = s0; s < s1; ++s) sum += (clamp_pos(pos[s], p_max) + kLatTile) / kLatTile;
+  part[tid] = sum;
+  __syncthreads();
+  // inclusive scan of the 1024 chunk sums (Hillis-Steele)
+  for (int o = 1; o < 1024; o <<= 1) {
+    const int v = tid >= o ? part[tid - o] : 0;
+    __syncthreads();
+    part[tid] += v;
+    __syncthreads();
+  }
+  int off = part[tid] - sum;
+  for (int s = s0; s < s1; ++s) {
+    plan[s] = off;
+    off += (clamp_pos(pos[s], p_max) + kLatTile) / kLatTile;
+  }
+  const long long total = part[1023];
+  if (tid == 0) plan[B] = (int)total;
+  __syncthreads();
+  for (int g = tid; g < G; g += 1024) {
+    const long long x0 = lat_range_start(g, total, G);
+    const int R = (int)(lat_range_start(g + 1, total, G) - x0);
+    int lo = 0, hi = B - 1;  // the last sequence whose first tile is <= x0
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (plan[mid] <= x0) lo = mid; else hi = mid - 1;
+    }
+    int* r = plan + B + 1 + 3 * g;
+    r[0] = lo;
+    r[1] = (int)(x0 - plan[lo]);
+    r[2] = R;
+  }
+}
+
 __global__ void __launch_bounds__(kLatThreads, 1)
     latent_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmC,
                    const __grid_constant__ CUtensorMap tmR, const LatentAttnArgs a, const DevStatus st) {
@@ -271,13 +344,8 @@ __global__ void __launch_bounds__(kLatThreads, 1)
   volatile int* abort_flag = &bar->abort;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nt = (a.L + kLatTile - 1) / kLatTile;  // tiles per sequence
-  const long long total = (long long)a.B * nt;
+  const int nt = (a.L + kLatTile - 1) / kLatTile;  // tiles per sequence (uniform lengths)
   const int g = blockIdx.x;
-  const long long x0 = lat_range_start(g, total, a.ctas);
-  const int R = (int)(lat_range_start(g + 1, total, a.ctas) - x0);  // tiles of this CTA
-  const int first_seq = (int)(x0 / nt);
-  const int first_t = (int)(x0 - (long long)first_seq * nt);  // tile index of x0 within its sequence
 
   if (threadIdx.x == 0) {
     mbar_init(&bar->q_full, 1);
@@ -306,6 +374,22 @@ __global__ void __launch_bounds__(kLatThreads, 1)
   const uint32_t tmem = bar->tmem_slot;
   pdl_launch_dependents();
   pdl_wait();
+  // this CTA's range of flattened (sequence, tile) work
+  int R, first_seq, first_t;
+  if (a.plan) {
+    const int* r = a.plan + a.B + 1 + 3 * g;
+    first_seq = r[0];
+    first_t = r[1];
+    R = r[2];
+  } else {
+    const long long total = (long long)a.B * nt;
+    const long long x0 = lat_range_start(g, total, a.ctas);
+    R = (int)(lat_range_start(g + 1, total, a.ctas) - x0);
+    first_seq = (int)(x0 / nt);
+    first_t = (int)(x0 - (long long)first_seq * nt);  // tile index of x0 within its sequence
+  }
+  SeqWalk walk{a.pos, a.L - 1, a.B, 0, 0, 0, 0};
+  if (R > 0) walk.start(first_seq, first_t);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -314,12 +398,9 @@ __global__ void __launch_bounds__(kLatThreads, 1)
       tma_prefetch_desc(&tmR);
       int seg = 0;
       int kpe_used[2] = {0, 0}, ckv_used[2] = {0, 0};  // loads issued per stage
-      int b = first_seq, t = first_t - 1;
       for (int i = 0; i < R; ++i) {
-        if (++t == nt) {
-          t = 0;
-          ++b;
-        }
+        walk.next();
+        const int b = walk.b, t = walk.t;
         const int stg = i & 1;
         const uint32_t eph = ((i >> 1) & 1) ^ 1;
         const int k0 = t * kLatTile;
@@ -354,11 +435,12 @@ __global__ void __launch_bounds__(kLatThreads, 1)
       constexpr uint32_t idesc_s = idesc_bf16(64, 64, false, false);
       const uint32_t q_addr = smem_u32(smem + kLatQOff);
       const uint32_t c_addr = smem_u32(smem + kLatCOff);
-      int seg = 0, t = first_t - 1;
+      int seg = 0;
       for (int i = 0; i < R; ++i) {
-        if (++t == nt) t = 0;
+        walk.next();
+        const int t = walk.t;
         const bool seg_first = i == 0 || t == 0;
-        const bool seg_last = i == R - 1 || t == nt - 1;
+        const bool seg_last = i == R - 1 || t == walk.nt - 1;
         const int stg = i & 1;
         const uint32_t ph = (i >> 1) & 1;
         if (!mbar_wait(&bar->s_free[stg], ph ^ 1, st, abort_flag, 70)) break;
@@ -394,10 +476,9 @@ __global__ void __launch_bounds__(kLatThreads, 1)
       constexpr uint32_t idesc_o = idesc_bf16(128, 64, true, false);
       const uint32_t c_addr = smem_u32(smem + kLatCOff);
       const uint32_t p_addr = smem_u32(smem + kLatPOff);
-      int t = first_t - 1;
       for (int i = 0; i < R; ++i) {
-        if (++t == nt) t = 0;
-        const bool seg_first = i == 0 || t == 0;
+        walk.next();
+        const bool seg_first = i == 0 || walk.t == 0;
         const int stg = i & 1;
         if (!mbar_wait(&bar->p_full, i & 1, st, abort_flag, 74)) break;
         tc_fence_after();
@@ -432,14 +513,12 @@ __global__ void __launch_bounds__(kLatThreads, 1)
     // (bar.sync has no time limit); after a failed wait (ok == false) the
     // work of the remaining iterations is skipped, the barriers are not.
     bool ok = true;
-    int b = first_seq, t = first_t - 1;
     for (int i = 0; i < R; ++i) {
-      if (++t == nt) {
-        t = 0;
-        ++b;
-      }
+      walk.next();
+      const int b = walk.b, t = walk.t;
+      const int Lb = walk.len;
       const bool seg_first = i == 0 || t == 0;
-      const bool seg_last = i == R - 1 || t == nt - 1;
+      const bool seg_last = i == R - 1 || t == walk.nt - 1;
       const int stg = i & 1;
       if (seg_first) {
         m = -INFINITY;
@@ -458,10 +537,10 @@ __global__ void __launch_bounds__(kLatThreads, 1)
         for (int c = 0; c < 32; ++c) s[c] = 0u;
       }
       const int k0 = t * kLatTile + kh * 32;  // first key of this thread's half
-      if (k0 + 32 > a.L) {
+      if (k0 + 32 > Lb) {
 #pragma unroll
         for (int c = 0; c < 32; ++c)
-          if (k0 + c >= a.L) s[c] = __float_as_uint(-INFINITY);
+          if (k0 + c >= Lb) s[c] = __float_as_uint(-INFINITY);
       }
       float mx;
       {
@@ -540,7 +619,7 @@ __global__ void __launch_bounds__(kLatThreads, 1)
         bar->l[h] = l_head;
       }
       named_sync_128();
-      const bool whole = t == nt - 1 && i >= t;  // the sequence's tile 0 is in this CTA too
+      const bool whole = t == walk.nt - 1 && i >= t;  // the sequence's tile 0 is in this CTA too
       const int slot = (b == first_seq) ? 2 * g : 2 * g + 1;
       if (ok) {
         tc_fence_after();
@@ -590,7 +669,8 @@ constexpr int kLatMaxCtas = 1024;
 
 __global__ void __launch_bounds__(128) latent_combine_kernel(const float* __restrict__ part_o,
                                                              const float2* __restrict__ part_ml,
-                                                             __nv_bfloat16* __restrict__ out, int L, int B, int G) {
+                                                             __nv_bfloat16* __restrict__ out, int L, int B, int G,
+                                                             const int* __restrict__ plan) {
   __shared__ int s_slot[kLatMaxCtas];
   __shared__ float s_w[kLatMaxCtas];
   __shared__ float s_red[2][4];
@@ -599,9 +679,11 @@ __global__ void __launch_bounds__(128) latent_combine_kernel(const float* __rest
   const int h = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nt = (L + kLatTile - 1) / kLatTile;
-  const long long total = (long long)B * nt;
+  // the sequence's first and last flattened tile (per-sequence lengths: from the plan)
+  const long long total = plan ? (long long)plan[B] : (long long)B * nt;
+  const long long xa = plan ? (long long)plan[b] : (long long)b * nt;
+  const long long xb = plan ? (long long)plan[b + 1] - 1 : xa + nt - 1;
   // CTA holding flattened tile x: the largest g with start(g) <= x
-  const long long xa = (long long)b * nt, xb = xa + nt - 1;  // the sequence's first and last tile
   const int g0 = (int)(((xa + 1) * G - 1) / total);
   const int g1 = (int)(((xb + 1) * G - 1) / total);
   if (g0 == g1) return;  // whole sequence in one CTA: written directly
@@ -609,7 +691,13 @@ __global__ void __launch_bounds__(128) latent_combine_kernel(const float* __rest
   float mloc = -INFINITY;
   for (int k = tid; k < n; k += 128) {
     const int gg = g0 + k;
-    const int slot = (b == (int)(lat_range_start(gg, total, G) / nt)) ? 2 * gg : 2 * gg + 1;
+    if (plan && plan[B + 1 + 3 * gg + 2] == 0) {  // a CTA with no tiles wrote nothing
+      s_slot[k] = -1;
+      s_w[k] = -INFINITY;
+      continue;
+    }
+    const int gseq = plan ? plan[B + 1 + 3 * gg] : (int)(lat_range_start(gg, total, G) / nt);
+    const int slot = (b == gseq) ? 2 * gg : 2 * gg + 1;
     const float2 ml = part_ml[(size_t)slot * 64 + h];
     s_slot[k] = slot;
     s_w[k] = ml.x;
@@ -621,6 +709,10 @@ __global__ void __launch_bounds__(128) latent_combine_kernel(const float* __rest
   const float mx = fmaxf(fmaxf(s_red[0][0], s_red[0][1]), fmaxf(s_red[0][2], s_red[0][3]));
   float dloc = 0.f;
   for (int k = tid; k < n; k += 128) {
+    if (s_slot[k] < 0) {
+      s_w[k] = 0.f;
+      continue;
+    }
     const float w = exp2f(s_w[k] - mx);
     dloc += w * part_ml[(size_t)s_slot[k] * 64 + h].y;
     s_w[k] = w;
@@ -631,6 +723,7 @@ __global__ void __launch_bounds__(128) latent_combine_kernel(const float* __rest
   const float inv = 1.f / ((s_red[1][0] + s_red[1][1]) + (s_red[1][2] + s_red[1][3]));
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int k = 0; k < n; ++k) {
+    if (s_slot[k] < 0) continue;
     const float w = s_w[k];
     const float4 v = *reinterpret_cast<const float4*>(part_o + ((size_t)s_slot[k] * 64 + h) * 512 + tid * 4);
     acc.x = fmaf(w, v.x, acc.x);
@@ -711,12 +804,22 @@ cudaError_t launch_latent_attention(const LatentAttnArgs& a, const DevStatusHost
     attr_set = true;
   }
   DevStatus dst{st.word, st.wait_limit_ns};
-  cudaError_t e = launch_pdl(latent_attn_tc, dim3(a.ctas), dim3(kLatThreads), kLatSmemBytes, stream, tq, tc, tr, a, dst);
+  cudaError_t e;
+  LatentAttnArgs la = a;
+  if (a.pos) {
+    if (!a.plan) return cudaErrorInvalidValue;
+    e = launch_pdl(latent_plan_kernel, dim3(1), dim3(1024), 0, stream, a.pos, a.B, a.L - 1, a.ctas, a.plan);
+    if (e != cudaSuccess) return e;
+    ++*launches;
+  } else {
+    la.plan = nullptr;
+  }
+  e = launch_pdl(latent_attn_tc, dim3(a.ctas), dim3(kLatThreads), kLatSmemBytes, stream, tq, tc, tr, la, dst);
   if (e != cudaSuccess) return e;
   ++*launches;
   if (a.ctas > 1) {
     e = launch_pdl(latent_combine_kernel, dim3(64, a.B), dim3(128), 0, stream, (const float*)a.part_o,
-                   (const float2*)a.part_ml, a.olat, a.L, a.B, a.ctas);
+                   (const float2*)a.part_ml, a.olat, a.L, a.B, a.ctas, (const int*)la.plan);
     ++*launches;
   }
   return e;

@@ -15,6 +15,12 @@ namespace mla {
 // wait that gives up ORs a site bit in and the kernel returns early.
 // ---------------------------------------------------------------------------
 constexpr uint32_t kStatusTimeout = 1u;
+constexpr uint32_t kStatusBadLength = 2u;  // a per-sequence position outside [0, P_max]
+
+// Per-sequence position of the new token (decode with per-sequence lengths),
+// clamped into [0, p_max] so that no access leaves the caches; an
+// out-of-range value is reported once per row by the kernel that owns the check.
+__device__ __forceinline__ int clamp_pos(int p, int p_max) { return p < 0 ? 0 : (p > p_max ? p_max : p); }
 
 struct DevStatus {
   uint32_t* word;        // device pointer, may be null (no reporting)

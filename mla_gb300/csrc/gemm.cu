@@ -189,7 +189,7 @@ __device__ __forceinline__ void run_epilogue(const EpiArgs& ea, const Src& ld, i
     const int h = n0 / 256;
     const int o0 = n0 % 256;
     const int b = row_ok ? row / ea.t_mod : 0;
-    const int t = ea.t_off + (row_ok ? row % ea.t_mod : 0);
+    const int t = ea.pos ? (row_ok ? clamp_pos(ea.pos[b], ea.pos_max) : 0) : ea.t_off + (row_ok ? row % ea.t_mod : 0);
     const size_t slot = ((size_t)b * 64 + h) * ea.cap + t;
     __nv_bfloat16* krow = ea.kc + slot * 192;
     __nv_bfloat16* vrow = ea.vc + slot * 128;
@@ -945,9 +945,9 @@ cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, con
       if (tiny && k256) return launch_impl<64, 128, 4, Epi::kKVCache, false, 2>(s, op, ea, st, num_sms, stream);
       if (small && k256) return launch_impl<128, 128, 3, Epi::kKVCache, false, 2>(s, op, ea, st, num_sms, stream);
       if (small) return launch_impl<128, 128, 6, Epi::kKVCache, false>(s, op, ea, st, num_sms, stream);
-      if (ea.t_mod % 32 == 0 && ea.B > 0 && pairs)
+      if (ea.t_mod % 32 == 0 && ea.B > 0 && !ea.pos && pairs)
         return launch_impl<128, 256, 6, Epi::kKVCache, false, 1, true, true>(s, op, ea, st, num_sms, stream);
-      if (ea.t_mod % 32 == 0 && ea.B > 0)
+      if (ea.t_mod % 32 == 0 && ea.B > 0 && !ea.pos)
         return launch_impl<128, 256, 4, Epi::kKVCache, false, 1, true>(s, op, ea, st, num_sms, stream);
       return launch_impl<128, 256, 4, Epi::kKVCache, false>(s, op, ea, st, num_sms, stream);
     case Epi::kResidual: {

@@ -146,6 +146,10 @@ struct EpiArgs {
   int* counters;
   // rows of the K/V caches the kv_b epilogue may write (t < t_off + t_mod)
   int B;
+  // kKVCache, decode with per-sequence lengths: row b's position pos[b]
+  // (clamped into [0, pos_max]) replaces t_off; null otherwise
+  const int* pos;
+  int pos_max;
 };
 
 cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, const EpiArgs& ea,
@@ -172,6 +176,12 @@ struct LatentArgs {
   __nv_bfloat16* kpe_cache;
   int rows, t_mod, t_off, cap;
   float eps;
+  // decode with per-sequence lengths: row r sits at position pos[r] (cache
+  // row and RoPE angle; cs then holds one entry per row); positions outside
+  // [0, pos_max] set kStatusBadLength in *status and are clamped
+  const int* pos;
+  int pos_max;
+  uint32_t* status;
 };
 cudaError_t launch_latent_split(const LatentArgs& a, cudaStream_t stream);
 
@@ -195,8 +205,9 @@ struct DecodeAttnArgs {
   __nv_bfloat16* o;         // [B, 64*128]
   float* part_o;            // [B*64*splits, 128] split partials
   float2* part_ml;          // [B*64*splits] (max, sum)
-  int B, L, cap, splits;    // L = keys attended (P + 1)
+  int B, L, cap, splits;    // L = keys attended (P + 1); with lens_pos: the largest P_b + 1
   float scale;
+  const int* lens_pos;      // optional per-sequence P_b (keys 0..P_b), clamped into [0, L - 1]
 };
 int decode_splits(int B, int L, int num_sms);
 cudaError_t launch_decode_attention(const DecodeAttnArgs& a, const DevStatusHost& st, cudaStream_t stream,
@@ -209,10 +220,19 @@ struct LatentAttnArgs {
   __nv_bfloat16* olat;        // [B, 64, 512]
   float* part_o;              // [2*ctas, 64, 512]: two partial slots per CTA
   float2* part_ml;            // [2*ctas, 64]
-  int B, L, cap, ctas;        // ctas = latent_ctas(B, L, SMs)
+  int B, L, cap, ctas;        // ctas = latent_ctas(B, L, SMs); with pos: L = the largest P_b + 1
   float scale;
+  // decode with per-sequence lengths: P_b = pos[b] (clamped into [0, L - 1])
+  // and the work plan that latent_plan_kernel writes (null: every sequence L keys)
+  const int* pos;
+  int* plan;                  // [latent_plan_ints(B, ctas)] workspace, written by the launch
 };
 int latent_ctas(int B, int L, int num_sms);
+// Work plan of the latent decode for per-sequence lengths: plan[0..B] =
+// first flattened 64-key tile of each sequence (plan[B] = total), then per
+// CTA g: (first sequence, first tile within it, tile count).  Written by a
+// one-CTA kernel that launch_latent_attention runs first when pos is set.
+inline size_t latent_plan_ints(int B, int ctas) { return (size_t)B + 1 + 3 * (size_t)ctas; }
 cudaError_t launch_latent_attention(const LatentAttnArgs& a, const DevStatusHost& st, cudaStream_t stream,
                                     int* launches);
 

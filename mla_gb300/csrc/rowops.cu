@@ -107,7 +107,14 @@ __global__ void __launch_bounds__(128) latent_split_kernel(const LatentArgs a) {
   __syncthreads();
   const int b = row / a.t_mod;
   const int tm = row - b * a.t_mod;
-  const int t = a.t_off + tm;
+  // position of this row: pos0 + tm (prefill, uniform decode) or its own
+  // (decode with per-sequence lengths, t_mod = 1)
+  int pos_row = a.pos0 + tm, t = a.t_off + tm;
+  if (a.pos) {
+    const int p = a.pos[row];
+    if ((p < 0 || p > a.pos_max) && tid == 0 && a.status) atomicOr(a.status, kStatusBadLength);
+    pos_row = t = clamp_pos(p, a.pos_max);
+  }
   // c^Q-hat = RMSNorm(c^Q); c^KV-hat = RMSNorm(c^KV) (also the latent cache row)
   const float rq = rsqrtf(((red[0][0] + red[0][1]) + (red[0][2] + red[0][3])) * (1.0f / 1536.0f) + a.eps);
   const float rk = rsqrtf(((red[1][0] + red[1][1]) + (red[1][2] + red[1][3])) * (1.0f / 512.0f) + a.eps);
@@ -121,13 +128,16 @@ __global__ void __launch_bounds__(128) latent_split_kernel(const LatentArgs a) {
     // R_t: angle (pos0 + t) * theta_i formed and reduced modulo 2 pi in double
     // precision (Cody-Waite style, 2 pi split in two doubles), then a float
     // sincos of the reduced angle
-    const double ang = (double)(a.pos0 + tm) * a.inv_freq[lane];
+    const double ang = (double)pos_row * a.inv_freq[lane];
     const double kq = rint(ang * 0.15915494309189535);  // 1 / (2 pi)
     const double red2 = fma(-kq, 6.283185307179586, ang) - kq * 2.4492935982947064e-16;
     float sn, cn;
     sincosf((float)red2, &sn, &cn);
     const float2 cs = make_float2(cn, sn);
-    if (b == 0) a.cs[(size_t)tm * 32 + lane] = cs;
+    if (a.pos)
+      a.cs[(size_t)row * 32 + lane] = cs;  // one table row per token
+    else if (b == 0)
+      a.cs[(size_t)tm * 32 + lane] = cs;
     // k^R = RoPE(k^pe, t): lane i rotates pair (i, i + 32); k^pe is not normalised
     const __nv_bfloat16 y1 = __float2bfloat16_rn(x1 * cs.x - x2 * cs.y);
     const __nv_bfloat16 y2 = __float2bfloat16_rn(x2 * cs.x + x1 * cs.y);

@@ -213,3 +213,46 @@ def test_decode_latent_b128_p8192(W):
         parity(cuda_to_f64(delta[b:b + 1]), ref["delta"], f"latent decode delta b={b}")
         parity_cache(cuda_to_f64(ckv[b:b + 1, P]), ref["ckv_new"], f"new latent row b={b}")
         parity_cache(cuda_to_f64(kpe[b:b + 1, P]), ref["kpe_new"], f"new rotary-key row b={b}")
+
+
+def test_decode_latent_varlen_b128_pmax8192(W):
+    """The bench's ragged latent decode: 128 sequences with seeded lengths
+    in [1, 8192] (the first 8192, the second 1), caches of 8192 positions
+    filled by the library's cache-only prefill (rows beyond a sequence's
+    length must be ignored); sampled sequences' rows replaced by the
+    oracle's bf16 latent rows."""
+    import torch
+    B, P_max = 128, 8192
+    cap = P_max + 1
+    lengths = varlen_lengths(B, P_max)
+    ckv, kpe = _fill_caches(W, B, P_max, cap, rebuilt=False)
+    samples = [0, 1, 77]
+    refs = {}
+    for b in samples:
+        Pb = lengths[b]
+        xc = synth.bf16_bits_to_f64(synth.tensor_bits(0, "cache_x", (B, P_max, D), synth.X_DIST, rows=[b]))
+        c = om.cache_from_tokens(W[2], xc[:, :max(Pb, 1)])
+        Cb, Rb = f64_to_bits(c["ckv"][0][:Pb]), f64_to_bits(c["kpe"][0][:Pb])
+        ckv[b, :Pb].copy_(bits_to_cuda(Cb))
+        kpe[b, :Pb].copy_(bits_to_cuda(Rb))
+        refs[b] = (synth.bf16_bits_to_f64(Cb)[None], synth.bf16_bits_to_f64(Rb)[None])
+    x = synth.tensor_cuda(0, "new_x", (B, D), synth.X_DIST)
+    out = torch.empty_like(x)
+    P = torch.tensor(lengths, dtype=torch.int32, device="cuda")
+    ws = m.alloc_workspace(m.MODE_DECODE_LATENT, B, P_max)
+    m.mla_decode_latent_varlen(W[1], x, P, P_max, ckv, kpe, out, ws)
+    torch.cuda.synchronize()
+    assert m.mla_device_status(ws) == 0
+    xn = synth.bf16_bits_to_f64(synth.tensor_bits(0, "new_x", (B, D), synth.X_DIST))
+    for b in samples:
+        ref = om.decode_latent(W[2], xn[b:b + 1], *refs[b])
+        parity_out(cuda_to_f64(out[b:b + 1]), ref["out"], f"ragged latent decode out b={b} (P={lengths[b]})")
+        parity_cache(cuda_to_f64(ckv[b:b + 1, lengths[b]]), ref["ckv_new"], f"new latent row b={b}")
+
+
+def varlen_lengths(B, P_max):
+    """Seeded per-sequence positions in [1, P_max]: the first sequence at
+    P_max, the second at 1, the rest uniform."""
+    lengths = [int(v) for v in np.random.default_rng(7).integers(1, P_max + 1, size=B)]
+    lengths[0], lengths[1] = P_max, 1
+    return lengths

@@ -282,6 +282,126 @@ def test_prefill_chunk_rejects_bad_arguments(W):
         m.mla_prefill_chunk(W[1], x, P0, None, kc, vc, wsp)
 
 
+LENGTHS = [0, 37, 300, 1, 129]  # a ragged batch: P_b per sequence (P_max = 300)
+
+
+def _ragged_caches(W, lengths, cap):
+    """Oracle caches of P_max seeded tokens per sequence, with rows at or
+    beyond each sequence's own length overwritten by noise (they must not
+    be read)."""
+    B, P_max = len(lengths), max(lengths)
+    (Kb, Vb, Cb, Rb), _ = make_caches(W, B, P_max, cap)
+    noise = synth.tensor_bits(3, "cache_x", (B, cap, 640), (0.0, 4.0))
+    for b, P in enumerate(lengths):
+        Kb[b, :, P:] = noise[b, None, P:, :192]
+        Vb[b, :, P:] = noise[b, None, P:, 192:320]
+        Cb[b, P:] = noise[b, P:, :512]
+        Rb[b, P:] = noise[b, P:, 512:576]
+    return Kb, Vb, Cb, Rb
+
+
+def test_decode_varlen_parity(W):
+    import torch
+    B, P_max = len(LENGTHS), max(LENGTHS)
+    cap = P_max + 2
+    Kb, Vb, _, _ = _ragged_caches(W, LENGTHS, cap)
+    xb = synth.tensor_bits(0, "new_x", (B, 7168), synth.X_DIST)
+    x = bits_to_cuda(xb)
+    kc, vc = bits_to_cuda(Kb), bits_to_cuda(Vb)
+    P = torch.tensor(LENGTHS, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(x)
+    delta = torch.empty((B, 7168), dtype=torch.float32, device="cuda")
+    wsp = m.alloc_workspace(m.MODE_DECODE, B, P_max)
+    m.mla_decode_varlen(W[1], x, P, P_max, kc, vc, out, wsp, m.make_params(delta_out=delta))
+    torch.cuda.synchronize()
+    assert m.mla_device_status(wsp) == 0
+    f = synth.bf16_bits_to_f64
+    ref = om.decode_varlen(W[2], f(xb), f(Kb), f(Vb), LENGTHS)
+    parity(cuda_to_f64(delta), ref["delta"], "delta")
+    parity_out(cuda_to_f64(out), ref["out"], "out")
+    bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    kn, vn = bits(kc), bits(vc)
+    for b, Pb in enumerate(LENGTHS):
+        parity_cache(cuda_to_f64(kc[b:b + 1, :, Pb]), ref["k_new"][b:b + 1], f"new K row b={b}")
+        parity_cache(cuda_to_f64(vc[b:b + 1, :, Pb]), ref["v_new"][b:b + 1], f"new V row b={b}")
+        # every other row untouched
+        assert np.array_equal(np.delete(kn[b], Pb, axis=1), np.delete(Kb[b], Pb, axis=1))
+        assert np.array_equal(np.delete(vn[b], Pb, axis=1), np.delete(Vb[b], Pb, axis=1))
+
+
+def test_decode_latent_varlen_parity(W):
+    import torch
+    B, P_max = len(LENGTHS), max(LENGTHS)
+    cap = P_max + 2
+    _, _, Cb, Rb = _ragged_caches(W, LENGTHS, cap)
+    xb = synth.tensor_bits(0, "new_x", (B, 7168), synth.X_DIST)
+    x = bits_to_cuda(xb)
+    ckv, kpe = bits_to_cuda(Cb), bits_to_cuda(Rb)
+    P = torch.tensor(LENGTHS, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(x)
+    delta = torch.empty((B, 7168), dtype=torch.float32, device="cuda")
+    wsp = m.alloc_workspace(m.MODE_DECODE_LATENT, B, P_max)
+    m.mla_decode_latent_varlen(W[1], x, P, P_max, ckv, kpe, out, wsp, m.make_params(delta_out=delta))
+    torch.cuda.synchronize()
+    assert m.mla_device_status(wsp) == 0
+    f = synth.bf16_bits_to_f64
+    ref = om.decode_latent_varlen(W[2], f(xb), f(Cb), f(Rb), LENGTHS)
+    parity(cuda_to_f64(delta), ref["delta"], "delta")
+    parity_out(cuda_to_f64(out), ref["out"], "out")
+    bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    cn = bits(ckv)
+    for b, Pb in enumerate(LENGTHS):
+        parity_cache(cuda_to_f64(ckv[b:b + 1, Pb]), ref["ckv_new"][b:b + 1], f"new latent row b={b}")
+        parity_cache(cuda_to_f64(kpe[b:b + 1, Pb]), ref["kpe_new"][b:b + 1], f"new rotary-key row b={b}")
+        assert np.array_equal(np.delete(cn[b], Pb, axis=0), np.delete(Cb[b], Pb, axis=0))
+
+
+def test_decode_latent_varlen_many_short_sequences(W):
+    """B=300 sequences of 1 to 200 keys: most CTAs' ranges hold several
+    whole sequences, some sequences are cut between CTAs."""
+    import torch
+    B = 300
+    rng = np.random.default_rng(11)
+    lengths = [int(v) for v in rng.integers(0, 200, size=B)]
+    P_max = max(lengths)
+    cap = P_max + 1
+    Cb = synth.tensor_bits(0, "cache_x", (B, cap, 512), (0.0, 1.0))
+    Rb = synth.tensor_bits(1, "cache_x", (B, cap, 64), (0.0, 1.7))
+    xb = synth.tensor_bits(0, "new_x", (B, 7168), synth.X_DIST)
+    x = bits_to_cuda(xb)
+    ckv, kpe = bits_to_cuda(Cb), bits_to_cuda(Rb)
+    P = torch.tensor(lengths, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(x)
+    wsp = m.alloc_workspace(m.MODE_DECODE_LATENT, B, P_max)
+    m.mla_decode_latent_varlen(W[1], x, P, P_max, ckv, kpe, out, wsp)
+    torch.cuda.synchronize()
+    assert m.mla_device_status(wsp) == 0
+    f = synth.bf16_bits_to_f64
+    for b in [0, 1, 2, 57, 150, 151, 298, 299]:
+        Pb = lengths[b]
+        ref = om.decode_latent(W[2], f(xb[b:b + 1]), f(Cb[b:b + 1, :Pb]), f(Rb[b:b + 1, :Pb]))
+        parity_out(cuda_to_f64(out[b:b + 1]), ref["out"], f"out b={b} (P={Pb})")
+
+
+def test_decode_varlen_out_of_range_length_is_reported(W):
+    """A per-sequence position beyond P_max (or negative) cannot be checked
+    on the host: the kernels clamp it, touch nothing outside the caches, and
+    the device status reports the bad argument."""
+    import torch
+    B, P_max = 2, 20
+    cap = P_max + 1
+    kc = torch.zeros((B, 64, cap, 192), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros((B, 64, cap, 128), dtype=torch.bfloat16, device="cuda")
+    x = synth.tensor_cuda(0, "new_x", (B, 7168), synth.X_DIST)
+    out = torch.empty_like(x)
+    for bad in ([5, P_max + 7], [-3, 4]):
+        P = torch.tensor(bad, dtype=torch.int32, device="cuda")
+        wsp = m.alloc_workspace(m.MODE_DECODE, B, P_max)
+        m.mla_decode_varlen(W[1], x, P, P_max, kc, vc, out, wsp)
+        torch.cuda.synchronize()
+        assert m.mla_device_status(wsp) == -1  # MLA_ERR_INVALID_ARG
+
+
 def test_prefill_then_decode_chain(W):
     """GPU prefill of T-1 tokens fills the caches; GPU decode of token T-1
     must match the oracle's prefill row T-1 (both cache forms)."""
