@@ -383,6 +383,21 @@ class Runner:
         del ws
         return c1, c2
 
+    def decode_varlen_step_fn(self, B, P_max, rebuilt, lengths):
+        """Ragged decode: caches of P_max positions per sequence (the library's
+        cache-only prefill), sequence b at position lengths[b]."""
+        torch, m, synth = self.torch, self.m, self.synth
+        c1, c2 = self.fill_caches(B, P_max, P_max + 1, rebuilt)
+        x = synth.tensor_cuda(0, "new_x", (B, D), synth.X_DIST, device=self.dev)
+        out = torch.empty_like(x)
+        P = torch.tensor(lengths, dtype=torch.int32, device=self.dev)
+        ws = m.alloc_workspace(m.MODE_DECODE if rebuilt else m.MODE_DECODE_LATENT, B, P_max, device=self.dev)
+        fn = m.mla_decode_varlen if rebuilt else m.mla_decode_latent_varlen
+
+        def step(timing):
+            fn(self.W, x, P, P_max, c1, c2, out, ws, m.make_params(timing=timing))
+        return step, (c1, c2, x, out, P, ws)
+
     def decode_step_fn(self, B, P, rebuilt):
         torch, m, synth = self.torch, self.m, self.synth
         c1, c2 = self.fill_caches(B, P, P + 1, rebuilt)
@@ -400,6 +415,14 @@ FFN_STAGES = ("ffn_norm", "gate_up", "down")
 PREFILL_STAGES = ("input_norm", "a_proj", "latent", "q_b", "kv_b", "attn", "o_proj")
 DECODE_STAGES = ("input_norm", "a_proj", "latent", "q_b", "kv_b", "attn", "o_proj")
 LATENT_STAGES = ("input_norm", "a_proj", "latent", "q_b", "absorb_q", "attn", "absorb_o", "o_proj")
+
+
+def varlen_lengths(B, P_max):
+    """Seeded per-sequence positions in [1, P_max] (the first P_max, the second 1)."""
+    import numpy as np
+    lengths = [int(v) for v in np.random.default_rng(7).integers(1, P_max + 1, size=B)]
+    lengths[0], lengths[1] = P_max, 1
+    return lengths
 
 
 def roofline_entry(stage_ms, mode, B, TP, pk, config_name, past=0):
@@ -637,6 +660,25 @@ def main():
             torch.cuda.empty_cache()
         except Exception as e:
             line["decode_latent"] = {"error": repr(e)[:300]}
+        # ---- ragged latent decode: 128 sequences, positions in [1, 8192] ---------
+        try:
+            B4v, P4v = 128, 8192
+            lengths = varlen_lengths(B4v, P4v)
+            step4v, keep = r.decode_varlen_step_fn(B4v, P4v, False, lengths)
+            ms4v, st4v, l4v = r.time_steps(step4v, ks, W, stages=LATENT_STAGES)
+            us = barrier_max(statistics.mean(ms4v)) * 1e3
+            keys = sum(p + 1 for p in lengths)
+            byts = keys * (KVL + ROPE) * 2 + WEIGHT_BYTES + 2 * B4v * D * 2
+            line["decode_latent_ragged"] = {
+                "workload": f"mla_decode_latent_varlen B=128, seeded positions in [1, 8192] ({keys} keys in all)",
+                "us_per_step": round(us, 2), "hbm_gbs": round(byts / (us * 1e-6) / 1e9, 1),
+                "frac_8tbs": round(byts / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 4),
+                "frac_measured_hbm": round(byts / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
+                "algorithmic_bytes": byts, "stage_ms": _stages_out(st4v), "launches": l4v}
+            del step4v, keep
+            torch.cuda.empty_cache()
+        except Exception as e:
+            line["decode_latent_ragged"] = {"error": repr(e)[:300]}
         # ---- prefill B=8, T=4096 writing both caches -------------------------------
         try:
             B5, T5 = 8, 4096
