@@ -453,3 +453,95 @@ def dense_block_prefill(w: dict, w_ffn: dict, x: np.ndarray, dims: Dims = KIMI_K
     attn = prefill(w, x, dims, eps, base, scale)
     f = ffn(w_ffn, attn["out"], eps)
     return {"out": f["out"], "x_mid": attn["out"], "delta_attn": attn["delta"], "delta_ffn": f["delta"]}
+
+
+# ---------------------------------------------------------------------------
+# FP8 block-scaled weights.  The dense-block page counts the checkpoint's
+# tensors with its "FP8 block scales" left out, so the weights are stored in
+# FP8 with one scale per block; the block size and the scale format are not
+# printed.  Reading taken: E4M3 (4 exponent bits, bias 7, 3 mantissa bits,
+# no infinities, largest finite 448) with one power-of-two scale per 128 x 128
+# block of the [out, in] matrix: s = 2^k for the smallest k with
+# amax(block) <= 448 * 2^k, q = E4M3 round-to-nearest-even of w / s, and the
+# weight used is q * s (exact in bfloat16 and in float64).
+# ---------------------------------------------------------------------------
+E4M3_MAX = 448.0
+FP8_BLOCK = 128
+
+
+def block_scale_exponent(amax: float) -> int:
+    """Smallest k with amax <= 448 * 2^k (0 for an all-zero block), from the
+    exact binary exponents of amax and 448 = 0.875 * 2^9."""
+    if amax == 0.0:
+        return 0
+    m, e = np.frexp(amax)  # amax = m * 2^e, m in [0.5, 1)
+    return int(e - 9 if m <= 0.875 else e - 8)
+
+
+def e4m3_round(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest E4M3 value (ties to even), saturating at +-448.
+    Normal values 2^e (1 + j/8), e in [-6, 8]; subnormals j 2^-9."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))
+    e = np.maximum(ex - 1, -6)             # binade exponent (subnormals share e = -6)
+    step = np.ldexp(1.0, e - 3)            # spacing of the binade: 3 mantissa bits
+    q = np.minimum(np.rint(a / step) * step, E4M3_MAX)
+    return np.copysign(q, x)  # the sign survives rounding to zero
+
+
+def e4m3_bits(q: np.ndarray) -> np.ndarray:
+    """Encoding of E4M3 values (as produced by e4m3_round): sign, 4-bit
+    exponent field (bias 7, 0 for subnormals), 3-bit mantissa."""
+    q = np.asarray(q, dtype=np.float64)
+    a = np.abs(q)
+    sign = (q < 0) | ((q == 0) & np.signbit(q))
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))
+    e = ex - 1
+    normal = a >= 2.0 ** -6
+    efield = np.where(normal, e + 7, 0)
+    mant = np.where(normal, a / np.ldexp(1.0, e) * 8 - 8, a / 2.0 ** -9)
+    bits = (sign.astype(np.int64) << 7) | (efield.astype(np.int64) << 3) | np.rint(mant).astype(np.int64)
+    return bits.astype(np.uint8)
+
+
+def e4m3_value(bits: np.ndarray) -> np.ndarray:
+    """Value of E4M3 codes (the NaN codes 0x7F / 0xFF are never produced)."""
+    b = np.asarray(bits, dtype=np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    efield = (b >> 3) & 0xF
+    mant = b & 0x7
+    v = np.where(efield == 0, mant * 2.0 ** -9, np.ldexp(1.0 + mant / 8.0, efield - 7))
+    return sign * v
+
+
+def quantize_fp8_blocks(w: np.ndarray) -> dict:
+    """Block quantization of one [rows, cols] matrix: E4M3 codes [rows, cols],
+    scale exponents [ceil(rows/128), ceil(cols/128)], and the dequantized
+    matrix q * s."""
+    rows, cols = w.shape
+    nb_r, nb_c = -(-rows // FP8_BLOCK), -(-cols // FP8_BLOCK)
+    k = np.zeros((nb_r, nb_c), dtype=np.int64)
+    deq = np.empty_like(w, dtype=np.float64)
+    codes = np.empty(w.shape, dtype=np.uint8)
+    for i in range(nb_r):
+        for j in range(nb_c):
+            blk = w[i * FP8_BLOCK:(i + 1) * FP8_BLOCK, j * FP8_BLOCK:(j + 1) * FP8_BLOCK]
+            k[i, j] = block_scale_exponent(float(np.max(np.abs(blk))))
+            q = e4m3_round(np.ldexp(blk, -k[i, j]))
+            codes[i * FP8_BLOCK:(i + 1) * FP8_BLOCK, j * FP8_BLOCK:(j + 1) * FP8_BLOCK] = e4m3_bits(q)
+            deq[i * FP8_BLOCK:(i + 1) * FP8_BLOCK, j * FP8_BLOCK:(j + 1) * FP8_BLOCK] = np.ldexp(q, k[i, j])
+    return {"codes": codes, "exp": k, "w": deq}
+
+
+FP8_MATRICES = ("w_q_a", "w_q_b", "w_kv_a", "w_kv_b", "w_o")
+
+
+def quantize_weights_fp8(w: dict) -> dict:
+    """The MLA weights with the five projection matrices replaced by their
+    block-quantized values (gains unchanged); the decode functions above then
+    compute with exactly the weights the FP8 path stores."""
+    out = dict(w)
+    for n in FP8_MATRICES:
+        out[n] = quantize_fp8_blocks(w[n])["w"]
+    return out
