@@ -660,6 +660,30 @@ def main():
             torch.cuda.empty_cache()
         except Exception as e:
             line["decode_latent"] = {"error": repr(e)[:300]}
+        # ---- decode with FP8 block-scaled weights: B=64, P=1000 -------------------
+        try:
+            B3, P3 = 64, 1000
+            WQ, keepw = r.m.make_weights_fp8(r.wt)
+            kc, vc = r.fill_caches(B3, P3, P3 + 1, True)
+            x3 = r.synth.tensor_cuda(0, "new_x", (B3, D), r.synth.X_DIST, device=r.dev)
+            o3 = torch.empty_like(x3)
+            ws3 = r.m.alloc_workspace(r.m.MODE_DECODE, B3, P3, device=r.dev)
+
+            def step3f(timing):
+                r.m.mla_decode_fp8(WQ, x3, P3, kc, vc, o3, ws3, r.m.make_params(timing=timing))
+            ms3f, st3f, l3f = r.time_steps(step3f, ks, W, stages=DECODE_STAGES)
+            us = barrier_max(statistics.mean(ms3f)) * 1e3
+            wbytes = sum(t.numel() * t.element_size() for t in keepw.values())
+            byts = B3 * H * (P3 + 1) * (QK + V) * 2 + wbytes + 2 * B3 * D * 2
+            line["decode_rebuilt_fp8"] = {
+                "workload": "mla_decode_fp8 B=64 P=1000, E4M3 weights with power-of-two 128x128 block scales",
+                "us_per_step": round(us, 2), "hbm_gbs": round(byts / (us * 1e-6) / 1e9, 1),
+                "frac_measured_hbm": round(byts / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
+                "algorithmic_bytes": byts, "weight_bytes": wbytes, "stage_ms": _stages_out(st3f), "launches": l3f}
+            del WQ, keepw, kc, vc, x3, o3, ws3
+            torch.cuda.empty_cache()
+        except Exception as e:
+            line["decode_rebuilt_fp8"] = {"error": repr(e)[:300]}
         # ---- ragged latent decode: 128 sequences, positions in [1, 8192] ---------
         try:
             B4v, P4v = 128, 8192

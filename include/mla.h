@@ -253,6 +253,49 @@ int mla_decode_latent_varlen(const mla_weights_t* w, const mla_params_t* params,
 int mla_decode_noalloc(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int P,
                        void* k_cache, void* v_cache, int cap, void* out, void* stream);
 
+/* ---- FP8 block-scaled weights ---------------------------------------------
+ * The dense-block page counts the checkpoint's tensors with its "FP8 block
+ * scales" left out: the released weights are FP8 with one scale per block.
+ * Block size and scale format are not printed; this library's format:
+ * E4M3 codes (the OCP FP8 E4M3 encoding, largest finite 448) of the [out, in]
+ * matrix, and one float scale per 128 x 128 block, always a power of two:
+ * the smallest 2^k with amax(block) <= 448 * 2^k.  The weight used is
+ * code * scale, exact in bfloat16, so the FP8 decode computes with exactly
+ * the quantized weights (on the bf16 tensor-core path: the codes are
+ * dequantized in shared memory; the bytes read from HBM halve).
+ *   cols   a multiple of 128
+ *   codes  uint8, block-major: block (i, j) (rows 128i.., columns 128j..) is
+ *          16,384 contiguous bytes at offset (i * cols/128 + j) * 16384,
+ *          row-major inside; ceil(rows/128) * cols/128 * 16384 bytes in all,
+ *          the rows past the matrix zero
+ *   scales [ceil(rows/128), cols/128] float */
+int mla_quantize_fp8(const void* w_bf16, int rows, int cols, void* codes, float* scales, void* stream);
+
+/* The MLA weights with the five projection matrices in that format (gains
+ * stay bf16). */
+typedef struct {
+  const void* w_in_norm;   /* [7168] bf16                                       */
+  const void* w_q_a_norm;  /* [1536] bf16                                       */
+  const void* w_kv_a_norm; /* [512]  bf16                                       */
+  const void* w_q_a;       /* [1536, 7168]   E4M3 codes, block-major; scales [12, 56] */
+  const void* w_q_b;       /* [12288, 1536]  E4M3 codes, block-major; scales [96, 12] */
+  const void* w_kv_a;      /* [576, 7168]    E4M3 codes, block-major (640 rows); scales [5, 56] */
+  const void* w_kv_b;      /* [16384, 512]   E4M3 codes, block-major; scales [128, 4] */
+  const void* w_o;         /* [7168, 8192]   E4M3 codes, block-major; scales [56, 64] */
+  const float* s_q_a;
+  const float* s_q_b;
+  const float* s_kv_a;
+  const float* s_kv_b;
+  const float* s_o;
+} mla_weights_fp8_t;
+
+/* mla_decode with FP8 block-scaled weights: the same step, arguments,
+ * workspace (MLA_MODE_DECODE) and errors; every projection reads its E4M3
+ * codes and scales. */
+int mla_decode_fp8(const mla_weights_fp8_t* w, const mla_params_t* params, const void* x, int B, int P,
+                   void* k_cache, void* v_cache, int cap, void* out, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
 /* ---- the block's second half ---------------------------------------------
  * Kimi K2 "Dense transformer block" page, equation list after
  * x'_n = x_n + Delta_attn, and its DecoderLayer forward excerpt: the dense

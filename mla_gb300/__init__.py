@@ -44,6 +44,14 @@ class MlaWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_NAMES]
 
 
+FP8_NAMES = ["w_q_a", "w_q_b", "w_kv_a", "w_kv_b", "w_o"]
+
+
+class MlaWeightsFp8(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ["w_in_norm", "w_q_a_norm", "w_kv_a_norm"] + FP8_NAMES] + \
+               [("s_" + n[2:], ctypes.c_void_p) for n in FP8_NAMES]
+
+
 class MlaFfnWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in FFN_WEIGHT_NAMES]
 
@@ -80,6 +88,9 @@ _SIGS = {
     "mla_decode_noalloc": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _VP, _VP, _I,
                                 _VP, _VP]),
     "mla_ffn": (_I, [ctypes.POINTER(MlaFfnWeights), ctypes.POINTER(MlaParams), _VP, _I, _VP, _VP, _SZ, _VP]),
+    "mla_quantize_fp8": (_I, [_VP, _I, _I, _VP, _VP, _VP]),
+    "mla_decode_fp8": (_I, [ctypes.POINTER(MlaWeightsFp8), ctypes.POINTER(MlaParams), _VP, _I, _I, _VP, _VP, _I, _VP,
+                            _VP, _SZ, _VP]),
     "mla_device_status": (_I, [_VP, _VP]),
     "mla_status_string": (ctypes.c_char_p, [_I]),
     "mla_debug_gemm": (_I, [_VP, _I, _VP, _I, _I, _VP, _I, _I, _I, _I, _VP]),
@@ -260,6 +271,42 @@ def mla_ffn(weights: MlaFfnWeights, x, out, workspace, params: MlaParams | None 
     rc = lib().mla_ffn(ctypes.byref(weights), None if params is None else ctypes.byref(params), _ptr(x), n_tok,
                        _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "mla_ffn")
+
+
+def mla_quantize_fp8(w, codes, scales, stream=None):
+    """w: bf16 CUDA [rows, cols] (cols % 128 == 0) -> codes uint8 block-major
+    [ceil(rows/128), cols/128, 128, 128], scales float32 [ceil(rows/128), cols/128]."""
+    rows, cols = w.shape
+    _check(lib().mla_quantize_fp8(_ptr(w), rows, cols, _ptr(codes), _ptr(scales), _stream(stream)),
+           "mla_quantize_fp8")
+
+
+def make_weights_fp8(w: dict, stream=None):
+    """FP8 block-scaled copies of the five projection matrices of a bf16
+    weight dict (quantized by the library) packed with the bf16 gains;
+    returns (struct, dict of the tensors it points to)."""
+    import torch
+    t = {n: w[n] for n in ("w_in_norm", "w_q_a_norm", "w_kv_a_norm")}
+    for n in FP8_NAMES:
+        rows, cols = w[n].shape
+        t[n] = torch.empty(((rows + 127) // 128, cols // 128, 128, 128), dtype=torch.uint8, device=w[n].device)
+        t["s_" + n[2:]] = torch.empty(((rows + 127) // 128, (cols + 127) // 128), dtype=torch.float32,
+                                     device=w[n].device)
+        mla_quantize_fp8(w[n], t[n], t["s_" + n[2:]], stream)
+    st = MlaWeightsFp8(*[t[f].data_ptr() for f, _ in MlaWeightsFp8._fields_])
+    st._keep = t
+    return st, t
+
+
+def mla_decode_fp8(weights: MlaWeightsFp8, x, P: int, k_cache, v_cache, out, workspace,
+                   params: MlaParams | None = None, stream=None):
+    """mla_decode with FP8 block-scaled weights (make_weights_fp8)."""
+    B = x.shape[0]
+    cap = k_cache.shape[2]
+    rc = lib().mla_decode_fp8(ctypes.byref(weights), None if params is None else ctypes.byref(params), _ptr(x), B, P,
+                              _ptr(k_cache), _ptr(v_cache), cap, _ptr(out), _ptr(workspace), workspace.numel(),
+                              _stream(stream))
+    _check(rc, "mla_decode_fp8")
 
 
 def mla_device_status(workspace, stream=None) -> int:

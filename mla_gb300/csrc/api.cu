@@ -175,7 +175,8 @@ T* at(void* ws, size_t off) {
 int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok, int n_pos, int pos0,
               int t_mod, int t_off, __nv_bfloat16* ckv_cache, __nv_bfloat16* kpe_cache, int cap, void* ws,
               const Layout& L, const DevStatusHost& st, int sms, cudaStream_t stream, Stager& sg,
-              int* launches, bool with_q = true, const int* pos = nullptr, int pos_max = 0) {
+              int* launches, bool with_q = true, const int* pos = nullptr, int pos_max = 0,
+              const mla_weights_fp8_t* f8 = nullptr) {
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   (void)n_pos;
   sg.start(MLA_STAGE_INPUT_NORM);
@@ -194,7 +195,13 @@ int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok,
     ea.out_f32 = at<float>(ws, L.ca);
     ea.ldo = 2112;
     set_split(ea, ws, L);
-    MLA_TRY(launch_gemm(s, op, Epi::kStoreF32, ea, st, sms, stream));
+    if (f8) {
+      GemmW8Operands o8{at<__nv_bfloat16>(ws, L.xn), MLA_D, n_tok, static_cast<const uint8_t*>(f8->w_q_a),
+                        MLA_Q_LORA, f8->s_q_a, static_cast<const uint8_t*>(f8->w_kv_a), 576, f8->s_kv_a};
+      MLA_TRY(launch_gemm_w8(s, o8, Epi::kStoreF32, ea, st, sms, stream));
+    } else {
+      MLA_TRY(launch_gemm(s, op, Epi::kStoreF32, ea, st, sms, stream));
+    }
     *launches += 1;
   }
   sg.stop(MLA_STAGE_A_PROJ);
@@ -239,7 +246,13 @@ int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok,
     ea.cs = at<float2>(ws, L.cs);
     ea.t_mod = pos ? n_tok : t_mod;  // per-row positions: one RoPE table row per token
     set_split(ea, ws, L);
-    MLA_TRY(launch_gemm(s, op, Epi::kQRope, ea, st, sms, stream));
+    if (f8) {
+      GemmW8Operands o8{at<__nv_bfloat16>(ws, L.cq), MLA_Q_LORA, n_tok, static_cast<const uint8_t*>(f8->w_q_b),
+                        MLA_HEADS * MLA_QK, f8->s_q_b, nullptr, 0, nullptr};
+      MLA_TRY(launch_gemm_w8(s, o8, Epi::kQRope, ea, st, sms, stream));
+    } else {
+      MLA_TRY(launch_gemm(s, op, Epi::kQRope, ea, st, sms, stream));
+    }
     *launches += 1;
   }
   sg.stop(MLA_STAGE_Q_B);
@@ -251,7 +264,7 @@ int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok,
 int kv_b_rows(const mla_weights_t* w, const __nv_bfloat16* ckv, const __nv_bfloat16* kpe, int n_tok, int t_mod,
               int t_off, __nv_bfloat16* kc, __nv_bfloat16* vc, int cap, void* ws, const Layout& L,
               const DevStatusHost& st, int sms, cudaStream_t stream, int* launches, const int* pos = nullptr,
-              int pos_max = 0) {
+              int pos_max = 0, const mla_weights_fp8_t* f8 = nullptr) {
   GemmShape s{n_tok, MLA_HEADS * 256, MLA_KV_LORA, 1, 0, 0, 0, 0, MLA_HEADS * 256};
   GemmOperands op{ckv, MLA_KV_LORA, n_tok,
                   static_cast<const __nv_bfloat16*>(w->w_kv_b), MLA_KV_LORA, MLA_HEADS * 256,
@@ -267,20 +280,28 @@ int kv_b_rows(const mla_weights_t* w, const __nv_bfloat16* ckv, const __nv_bfloa
   ea.pos = pos;
   ea.pos_max = pos_max;
   set_split(ea, ws, L);
-  MLA_TRY(launch_gemm(s, op, Epi::kKVCache, ea, st, sms, stream));
+  if (f8) {
+    GemmW8Operands o8{ckv, MLA_KV_LORA, n_tok, static_cast<const uint8_t*>(f8->w_kv_b), MLA_HEADS * 256,
+                      f8->s_kv_b, nullptr, 0, nullptr};
+    MLA_TRY(launch_gemm_w8(s, o8, Epi::kKVCache, ea, st, sms, stream));
+  } else {
+    MLA_TRY(launch_gemm(s, op, Epi::kKVCache, ea, st, sms, stream));
+  }
   *launches += 1;
   return MLA_OK;
 }
 
 int kv_b_stage(const mla_weights_t* w, int n_tok, int t_mod, int t_off, __nv_bfloat16* kc, __nv_bfloat16* vc,
                int cap, void* ws, const Layout& L, const DevStatusHost& st, int sms, cudaStream_t stream,
-               int* launches, const int* pos = nullptr, int pos_max = 0) {
+               int* launches, const int* pos = nullptr, int pos_max = 0,
+               const mla_weights_fp8_t* f8 = nullptr) {
   return kv_b_rows(w, at<__nv_bfloat16>(ws, L.ckv), at<__nv_bfloat16>(ws, L.kpe), n_tok, t_mod, t_off, kc, vc, cap,
-                   ws, L, st, sms, stream, launches, pos, pos_max);
+                   ws, L, st, sms, stream, launches, pos, pos_max, f8);
 }
 
 int o_proj_stage(const mla_weights_t* w, const Params& p, const void* x, void* out, int n_tok, void* ws,
-                 const Layout& L, const DevStatusHost& st, int sms, cudaStream_t stream, int* launches) {
+                 const Layout& L, const DevStatusHost& st, int sms, cudaStream_t stream, int* launches,
+                 const mla_weights_fp8_t* f8 = nullptr) {
   GemmShape s{n_tok, MLA_D, MLA_HEADS * MLA_V, 1, 0, 0, 0, 0, MLA_D};
   GemmOperands op{at<__nv_bfloat16>(ws, L.o), MLA_HEADS * MLA_V, n_tok,
                   static_cast<const __nv_bfloat16*>(w->w_o), MLA_HEADS * MLA_V, MLA_D, nullptr, 0, 0, false};
@@ -290,7 +311,13 @@ int o_proj_stage(const mla_weights_t* w, const Params& p, const void* x, void* o
   ea.x = static_cast<const __nv_bfloat16*>(x);
   ea.delta = p.delta;
   set_split(ea, ws, L);
-  MLA_TRY(launch_gemm(s, op, Epi::kResidual, ea, st, sms, stream));
+  if (f8) {
+    GemmW8Operands o8{at<__nv_bfloat16>(ws, L.o), MLA_HEADS * MLA_V, n_tok, static_cast<const uint8_t*>(f8->w_o),
+                      MLA_D, f8->s_o, nullptr, 0, nullptr};
+    MLA_TRY(launch_gemm_w8(s, o8, Epi::kResidual, ea, st, sms, stream));
+  } else {
+    MLA_TRY(launch_gemm(s, op, Epi::kResidual, ea, st, sms, stream));
+  }
   *launches += 1;
   return MLA_OK;
 }
@@ -477,7 +504,7 @@ namespace {
 // else sequence b at position pos[b] (device array), P = an upper bound.
 int decode_impl(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int P, const int* pos,
                 void* k_cache, void* v_cache, int cap, void* out, void* workspace, size_t workspace_bytes,
-                void* stream) {
+                void* stream, const mla_weights_fp8_t* f8 = nullptr) {
   const Params p = resolve(params);
   if (B < 1 || B > kMaxTokens || P < 0 || P >= (1 << 24)) return MLA_ERR_INVALID_ARG;
   if (!k_cache || !v_cache || cap < P + 1) return MLA_ERR_INVALID_ARG;
@@ -496,13 +523,13 @@ int decode_impl(const mla_weights_t* w, const mla_params_t* params, const void* 
   int launches = 0;
   if (cudaMemsetAsync(st.word, 0, kStatusRegion, stream_) != cudaSuccess) return MLA_ERR_CUDA;
   rc = front_end(w, p, x, B, 1, P, 1, P, nullptr, nullptr, cap, workspace, L, st, sms, stream_, sg, &launches, true,
-                 pos, P);
+                 pos, P, f8);
   if (rc) return rc;
 
   __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(k_cache);
   __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(v_cache);
   sg.start(MLA_STAGE_KV_B);
-  rc = kv_b_stage(w, B, 1, P, kc, vc, cap, workspace, L, st, sms, stream_, &launches, pos, P);
+  rc = kv_b_stage(w, B, 1, P, kc, vc, cap, workspace, L, st, sms, stream_, &launches, pos, P, f8);
   if (rc) return rc;
   sg.stop(MLA_STAGE_KV_B);
 
@@ -526,7 +553,7 @@ int decode_impl(const mla_weights_t* w, const mla_params_t* params, const void* 
   sg.stop(MLA_STAGE_ATTN);
 
   sg.start(MLA_STAGE_O_PROJ);
-  rc = o_proj_stage(w, p, x, out, B, workspace, L, st, sms, stream_, &launches);
+  rc = o_proj_stage(w, p, x, out, B, workspace, L, st, sms, stream_, &launches, f8);
   if (rc) return rc;
   sg.stop(MLA_STAGE_O_PROJ);
   if (p.timing) p.timing->n_launches = launches;
@@ -630,6 +657,30 @@ extern "C" {
 int mla_decode(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int P, void* k_cache,
                void* v_cache, int cap, void* out, void* workspace, size_t workspace_bytes, void* stream) {
   return decode_impl(w, params, x, B, P, nullptr, k_cache, v_cache, cap, out, workspace, workspace_bytes, stream);
+}
+
+int mla_decode_fp8(const mla_weights_fp8_t* w, const mla_params_t* params, const void* x, int B, int P,
+                   void* k_cache, void* v_cache, int cap, void* out, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  if (!w) return MLA_ERR_INVALID_ARG;
+  for (const void* q : {(const void*)w->s_q_a, (const void*)w->s_q_b, (const void*)w->s_kv_a, (const void*)w->s_kv_b,
+                        (const void*)w->s_o})
+    if (!q) return MLA_ERR_INVALID_ARG;
+  // the gains and code matrices in the bf16 struct's places (checked there; the
+  // projections read the codes and scales through w)
+  const mla_weights_t view{w->w_in_norm, w->w_q_a, w->w_q_a_norm, w->w_q_b,
+                           w->w_kv_a,    w->w_kv_a_norm, w->w_kv_b, w->w_o};
+  return decode_impl(&view, params, x, B, P, nullptr, k_cache, v_cache, cap, out, workspace, workspace_bytes, stream,
+                     w);
+}
+
+int mla_quantize_fp8(const void* w_bf16, int rows, int cols, void* codes, float* scales, void* stream) {
+  if (!w_bf16 || !codes || !scales || rows < 1 || cols < 1 || cols % 128) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(w_bf16) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3)) return MLA_ERR_ALIGNMENT;
+  if (launch_fp8_quantize(static_cast<const __nv_bfloat16*>(w_bf16), rows, cols, static_cast<uint8_t*>(codes), scales,
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
 }
 
 int mla_decode_varlen(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, const int* P,

@@ -18,6 +18,8 @@
 // the epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).  The accumulator is
 // double buffered in TMEM so the epilogue of one tile overlaps the main loop
 // of the next.  Every wait is bounded (see common.cuh).
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -919,6 +921,467 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
   }
 }
 
+// ---------------------------------------------------------------------------
+// GEMM with FP8 block-scaled B (decode-size M).  320 threads:
+//   warp 0      producer: E4M3 tiles of B (BN rows x 128 bytes per 128-wide
+//               K stage; the codes are stored block-major, so a tile's
+//               stage is one or two contiguous bulk copies) into a deep
+//               SF-slot ring, and A (two 64-wide bf16 TMA boxes per stage)
+//               into an SA-slot ring; each ring is refilled as soon as a
+//               slot frees, and the first E4M3 stages are issued before the
+//               wait on the preceding kernel (weights are read-only)
+//   warp 1      TMEM allocation; one lane issues the bf16 MMAs
+//   warps 2..5  epilogue (as gemm_kernel: register stores, split-K fixup)
+//   warps 6..13 dequantization: each E4M3 tile -> bf16 (x its block scale)
+//               in the 128-byte-swizzled K-major layout of a 2-slot ring
+//               that the MMAs read; a unit's block scales are read once
+//               into a shared-memory table
+// ---------------------------------------------------------------------------
+constexpr int kW8Threads = 448;
+constexpr int kW8Deq = 256;    // dequantization threads (warps 6..13)
+constexpr int kW8MaxKb = 64;   // 128-wide K stages per unit whose scales fit the table
+
+template <int BM, int BN, int SA, int SF>
+struct W8Smem {
+  static constexpr uint32_t kA1 = BM * 64 * 2;  // one 64-wide bf16 block of A
+  static constexpr uint32_t kA = 2 * kA1;       // an A stage (128 K)
+  static constexpr uint32_t kF = BN * 128;      // an E4M3 B stage (128 K)
+  static constexpr uint32_t kB1 = BN * 64 * 2;  // one 64-wide bf16 block of B
+  static constexpr uint32_t kB = 2 * kB1;
+  static constexpr uint32_t kFOff = SA * kA;
+  static constexpr uint32_t kBOff = kFOff + SF * kF;
+  static constexpr uint32_t kBarOff = kBOff + 2 * kB;
+  static constexpr uint32_t kScOff = kBarOff + 512;  // [2 row blocks][kW8MaxKb] scales
+  static constexpr uint32_t kBytes = kScOff + 2 * kW8MaxKb * 4 + 1024;
+};
+
+// The (unit, 128-wide K stage) sequence of one persistent CTA.  With one
+// row block every CTA reads the same A panel: each column block starts at a
+// different K stage (as in gemm_kernel) so the CTAs spread over L2.
+struct W8Cursor {
+  int unit, i, nk, kb0, rot;
+  int ustep, num_units, ksplit, kb_per, kstages, m_tiles, n_tiles, raster_g;
+  __device__ __forceinline__ void range() {
+    if (unit < num_units) {
+      kb0 = (unit % ksplit) * kb_per;
+      nk = min(kstages, kb0 + kb_per) - kb0;
+      i = 0;
+      rot = 0;
+      if (m_tiles == 1 && nk > 1) {
+        int bt, mb_, nb_;
+        tile_coords(unit / ksplit, m_tiles, n_tiles, raster_g, bt, mb_, nb_);
+        rot = (nb_ * 7) % nk;
+      }
+    }
+  }
+  __device__ __forceinline__ bool valid() const { return unit < num_units; }
+  __device__ __forceinline__ int kb() const { return kb0 + (i + rot) % nk; }
+  __device__ __forceinline__ void next() {
+    if (++i == nk) {
+      unit += ustep;
+      range();
+    }
+  }
+};
+
+// Four E4M3 codes (one 32-bit word, code 0 in the low byte) -> four bf16
+// values times s (a power of two), exactly, with integer and fp32 multiply
+// instructions only.  A code c = [sign | 4-bit exponent E | 3-bit mantissa m]
+// placed as the bf16 bits (c & 0x80) << 8 | (c & 0x7F) << 4 is a bf16 of the
+// same sign whose exponent field is E and mantissa m / 8: for E > 0 that is
+// 2^(E-127) (1 + m/8) = value * 2^-120, for E = 0 the bf16 subnormal
+// m 2^-129 = value * 2^-120 too.  Widened to fp32 (exact, a shift) and
+// multiplied by 2^120 and then by s (both exact: powers of two, the
+// results normal), the product's upper half is the bf16 result.
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, float s, uint32_t& lo, uint32_t& hi) {
+  // codes 0,1 -> high bytes of two 16-bit halves; codes 2,3 likewise
+  const uint32_t v01 = __byte_perm(w, 0u, 0x1404);
+  const uint32_t v23 = __byte_perm(w, 0u, 0x3424);
+  const uint32_t b01 = ((v01 >> 4) & 0x07F007F0u) | (v01 & 0x80008000u);  // value * 2^-120 as bf16x2
+  const uint32_t b23 = ((v23 >> 4) & 0x07F007F0u) | (v23 & 0x80008000u);
+  const float f0 = (__uint_as_float(b01 << 16) * 0x1p120f) * s;
+  const float f1 = (__uint_as_float(b01 & 0xFFFF0000u) * 0x1p120f) * s;
+  const float f2 = (__uint_as_float(b23 << 16) * 0x1p120f) * s;
+  const float f3 = (__uint_as_float(b23 & 0xFFFF0000u) * 0x1p120f) * s;
+  lo = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
+  hi = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
+}
+
+template <int BM, int BN, int SA, int SF, Epi EPI>
+__global__ void __launch_bounds__(kW8Threads, 1)
+    gemm_w8_kernel(const __grid_constant__ CUtensorMap tmA, const uint8_t* __restrict__ B0,
+                   const uint8_t* __restrict__ B1, const float* __restrict__ s0, const float* __restrict__ s1,
+                   const GemmShape s, const EpiArgs ea, const DevStatus st) {
+  static_assert(SF >= SA && BN % 32 == 0 && BN <= 128, "W8 GEMM configuration");
+  using L = W8Smem<BM, BN, SA, SF>;
+  constexpr uint32_t kTmemCols = pow2_cols(2 * BN);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* a_empty = a_full + SA;
+  uint64_t* f_full = a_empty + SA;
+  uint64_t* f_empty = f_full + SF;
+  uint64_t* b_full = f_empty + SF;
+  uint64_t* b_empty = b_full + 2;
+  uint64_t* tfull = b_empty + 2;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m_tiles = (s.M + BM - 1) / BM;
+  const int n_tiles = s.N / BN;
+  const int kstages = s.K / 128;
+  const int num_units = m_tiles * n_tiles * s.ksplit;
+  const int unit0 = (int)blockIdx.x, ustep = (int)gridDim.x;
+  const int kb_per = s.kb_per;  // 128-wide stages per K slice
+  auto cursor = [&]() {
+    W8Cursor c{unit0, 0, 1, 0, 0, ustep, num_units, s.ksplit, kb_per, kstages, m_tiles, n_tiles, s.raster_g};
+    c.range();
+    return c;
+  };
+  // column block of a unit -> (B rows of the tile, which matrix)
+  auto tile_n0 = [&](int unit, int& m_blk) {
+    int batch, n_blk;
+    tile_coords(unit / s.ksplit, m_tiles, n_tiles, s.raster_g, batch, m_blk, n_blk);
+    return n_blk * BN;
+  };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < SA; ++i) {
+      mbar_init(&a_full[i], 1);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < SF; ++i) {
+      mbar_init(&f_full[i], 1);
+      mbar_init(&f_empty[i], kW8Deq);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&b_full[i], kW8Deq);
+      mbar_init(&b_empty[i], 1);
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) tma_prefetch_desc(&tmA);
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_launch_dependents();
+  // the producer and the dequantization warps touch only weights and shared
+  // memory before the wait; the producer waits itself before loading A
+  if (warp >= 1 && warp <= 5) pdl_wait();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      W8Cursor cf = cursor(), ca = cursor();
+      int nf = 0, na = 0;
+      auto issue_f = [&]() -> bool {
+        const int slot = nf % SF;
+        if (nf >= SF && !mbar_wait(&f_empty[slot], ((nf / SF) & 1) ^ 1, st, abort_flag, 81)) return false;
+        int m_blk;
+        const int n0 = tile_n0(cf.unit, m_blk);
+        const bool first_mat = n0 < s.n_split;
+        const uint8_t* bm = first_mat ? B0 : B1;
+        const int rb = first_mat ? n0 : n0 - s.n_split;
+        uint8_t* dst = smem + L::kFOff + slot * L::kF;
+        mbar_arrive_expect_tx(&f_full[slot], L::kF);
+        // rows rb .. rb+BN-1 of K stage kb: contiguous within each 128-row block
+        const int r_in = rb & 127;
+        const int n1 = BN < 128 - r_in ? BN : 128 - r_in;
+        bulk_load(dst, bm + (((size_t)(rb >> 7) * kstages + cf.kb()) * 128 + r_in) * 128, n1 * 128, &f_full[slot]);
+        if (n1 < BN)
+          bulk_load(dst + n1 * 128, bm + ((size_t)((rb >> 7) + 1) * kstages + cf.kb()) * 128 * 128, (BN - n1) * 128,
+                    &f_full[slot]);
+        ++nf;
+        cf.next();
+        return true;
+      };
+      // weights first, before the wait on the preceding kernel: a fresh ring
+      while (cf.valid() && nf < SF) issue_f();
+      pdl_wait();
+      // Both rings are refilled as soon as a slot frees, tested with
+      // test_wait (never suspends: a full ring must not hold back the other);
+      // the E4M3 loads have a long latency and keep the whole ring in flight.
+      uint64_t t_last = globaltimer_ns();
+      while (cf.valid() || ca.valid()) {
+        bool progress = false;
+        if (cf.valid() && mbar_test(&f_empty[nf % SF], ((nf / SF) & 1) ^ 1)) {
+          issue_f();
+          progress = true;
+        }
+        if (ca.valid() && (na < SA || mbar_test(&a_empty[na % SA], ((na / SA) & 1) ^ 1))) {
+          const int slot = na % SA;
+          int m_blk;
+          tile_n0(ca.unit, m_blk);
+          mbar_arrive_expect_tx(&a_full[slot], L::kA);
+          uint8_t* sa = smem + slot * L::kA;
+          tma_load_2d(sa, &tmA, &a_full[slot], ca.kb() * 128, m_blk * BM);
+          tma_load_2d(sa + L::kA1, &tmA, &a_full[slot], ca.kb() * 128 + 64, m_blk * BM);
+          ++na;
+          ca.next();
+          progress = true;
+        }
+        if (progress) {
+          t_last = globaltimer_ns();
+        } else if (*abort_flag) {
+          break;
+        } else if (globaltimer_ns() - t_last > st.wait_limit_ns) {
+          report_timeout(st, 82);
+          *abort_flag = 1;
+          break;
+        }
+      }
+      // no copy may still be in flight into this CTA's shared memory
+      for (int i = 0; i < SF && i < nf; ++i) {
+        const int uses = (nf - 1 - i) / SF + 1;
+        mbar_wait(&f_full[i], (uses - 1) & 1, st, nullptr, 83);
+      }
+      for (int i = 0; i < SA && i < na; ++i) {
+        const int uses = (na - 1 - i) / SA + 1;
+        mbar_wait(&a_full[i], (uses - 1) & 1, st, nullptr, 83);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BN, false, false);
+      W8Cursor c = cursor();
+      int n = 0, acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      while (ok && c.valid()) {
+        const int unit = c.unit;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, st, abort_flag, 84)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        bool first = true;
+        for (; c.valid() && c.unit == unit; c.next(), ++n) {
+          const int sa = n % SA, sb = n & 1;
+          if (!mbar_wait(&a_full[sa], (n / SA) & 1, st, abort_flag, 85) ||
+              !mbar_wait(&b_full[sb], (n >> 1) & 1, st, abort_flag, 86)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + sa * L::kA);
+          const uint32_t b_base = smem_u32(smem + L::kBOff + sb * L::kB);
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              umma_bf16(d_tmem, sdesc_sw128(a_base + u * L::kA1 + k * 32, 16, 1024),
+                        sdesc_sw128(b_base + u * L::kB1 + k * 32, 16, 1024), idesc, (first && u == 0 && k == 0) ? 0u : 1u);
+          first = false;
+          umma_commit(&a_empty[sa]);
+          umma_commit(&b_empty[sb]);
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      umma_commit(drain);
+      mbar_wait(drain, 0, st, nullptr, 87);
+    }
+  } else if (warp >= 6) {
+    // ---------------- dequantization (warps 6..13) ----------------
+    const int tid = threadIdx.x - 192;
+    const int sld = kstages;  // scale columns (K / 128)
+    float* sc_tab = reinterpret_cast<float*>(smem + L::kScOff);
+    W8Cursor c = cursor();
+    int rb = 0, rb0 = 0;
+    for (int n = 0; c.valid(); c.next(), ++n) {
+      if (c.i == 0) {
+        // a new unit: its rows' block scales for every K stage of its slice
+        int m_blk;
+        const int n0 = tile_n0(c.unit, m_blk);
+        const bool first_mat = n0 < s.n_split;
+        const float* sc = first_mat ? s0 : s1;
+        rb = first_mat ? n0 : n0 - s.n_split;
+        rb0 = rb >> 7;
+        const int nrb = ((rb + BN - 1) >> 7) - rb0 + 1;  // 1 or 2 row blocks
+        asm volatile("bar.sync 2, %0;" ::"n"(kW8Deq) : "memory");  // the previous unit's readers are done
+        for (int e = tid; e < 2 * kW8MaxKb; e += kW8Deq) {
+          const int j = e / kW8MaxKb, i = e % kW8MaxKb;
+          if (j < nrb && i < c.nk) sc_tab[e] = __ldg(sc + (size_t)(rb0 + j) * sld + c.kb0 + i);
+        }
+        asm volatile("bar.sync 2, %0;" ::"n"(kW8Deq) : "memory");
+      }
+      const int fs = n % SF, bs = n & 1;
+      bool ok = mbar_wait(&f_full[fs], (n / SF) & 1, st, abort_flag, 88);
+      ok = ok && mbar_wait(&b_empty[bs], ((n >> 1) & 1) ^ 1, st, abort_flag, 89);
+      // every dequantization thread reaches the next unit's named barriers:
+      // after a failed wait the rest of the work is skipped, not the loop
+      if (!__all_sync(0xffffffffu, ok)) continue;
+      const int kcol = c.kb() - c.kb0;
+      const uint8_t* fst = smem + L::kFOff + fs * L::kF;
+      uint8_t* bst = smem + L::kBOff + bs * L::kB;
+      constexpr int kChunks = BN * 8 / kW8Deq;  // 16-byte E4M3 chunks per thread
+      static_assert(BN * 8 % kW8Deq == 0, "chunks per dequantization thread");
+      uint4 f[kChunks];
+      float sv[kChunks];
+#pragma unroll
+      for (int q = 0; q < kChunks; ++q) {  // every load first: independent chains
+        const int ci = tid + q * kW8Deq, r = ci >> 3;
+        f[q] = *reinterpret_cast<const uint4*>(fst + ci * 16);
+        sv[q] = sc_tab[(((rb + r) >> 7) - rb0) * kW8MaxKb + kcol];
+      }
+#pragma unroll
+      for (int q = 0; q < kChunks; ++q) {
+        const int ci = tid + q * kW8Deq, r = ci >> 3;
+        const int lk = ci & 7;  // 16-element K chunk of row r (the E4M3 stage is not swizzled)
+        uint32_t o[8];
+        e4m3x4_to_bf16x4(f[q].x, sv[q], o[0], o[1]);
+        e4m3x4_to_bf16x4(f[q].y, sv[q], o[2], o[3]);
+        e4m3x4_to_bf16x4(f[q].z, sv[q], o[4], o[5]);
+        e4m3x4_to_bf16x4(f[q].w, sv[q], o[6], o[7]);
+        // 16 bf16 = logical 16-byte chunks 2 (lk % 4) and 2 (lk % 4) + 1 of 64-wide block lk / 4
+        uint8_t* row = bst + (lk >> 2) * L::kB1 + r * 128;
+        const int j0 = (lk & 3) * 2;
+        *reinterpret_cast<uint4*>(row + ((j0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(row + (((j0 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+      fence_proxy_async_smem();  // generic-proxy writes -> the tensor core's reads
+      mbar_arrive(&b_full[bs]);
+      mbar_arrive(&f_empty[fs]);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int quarter = warp & 3;
+    const bool lane_ok = (BM == 128) || lane < 16;
+    const int rit = (BM == 128) ? quarter * 32 + lane : quarter * 16 + (lane & 15);
+    const int ksplit = s.ksplit;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int unit = unit0; unit < num_units; unit += ustep) {
+      const int tile = unit / ksplit;
+      const int ks = unit % ksplit;
+      int m_blk;
+      const int n0 = tile_n0(unit, m_blk);
+      bool ok = mbar_wait(&tfull[acc], acc_phase, st, abort_flag, 90);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const int row = m_blk * BM + rit;
+      const bool row_ok = lane_ok && row < s.M;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+      if (ksplit == 1) {
+        run_epilogue<BN, EPI>(ea, TmemSrc{taddr}, 0, row, n0, row_ok);
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+      } else {
+        const int rows_pt = s.M < BM ? s.M : BM;
+        const bool in_slot = row_ok && rit < rows_pt;
+        float* slot = ea.part + ((size_t)(tile * ksplit + ks) * rows_pt + (in_slot ? rit : 0)) * BN;
+#pragma unroll 1
+        for (int cc = 0; cc < BN; cc += 32) {
+          uint32_t r[32];
+          tmem_ld32(taddr + cc, r);
+          tmem_wait_ld();
+          if (in_slot) {
+            float4* d = reinterpret_cast<float4*>(slot + cc);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              d[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+        __threadfence();
+        __syncwarp();
+        int prev = 0;
+        if (lane == 0) prev = atomicAdd(&ea.counters[tile * 4 + quarter], 1);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == ksplit - 1) {
+          __threadfence();
+          const PartSrc src{ea.part + ((size_t)tile * ksplit * rows_pt + (in_slot ? rit : 0)) * BN,
+                            (size_t)rows_pt * BN, ksplit, in_slot};
+          run_epilogue<BN, EPI>(ea, src, 0, row, n0, row_ok);
+          if (lane == 0) ea.counters[tile * 4 + quarter] = 0;
+        }
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int BM, int BN, int SA, int SF, Epi EPI>
+cudaError_t launch_w8_impl(const GemmShape& s, const GemmW8Operands& op, const EpiArgs& ea, const DevStatusHost& st,
+                           int num_sms, cudaStream_t stream) {
+  using L = W8Smem<BM, BN, SA, SF>;
+  static_assert(L::kBytes <= 232448, "shared memory budget");
+  if (s.K % 128 || s.N % BN || s.n_split % BN || s.batches != 1) return cudaErrorInvalidValue;
+  if (s.K / 128 > kW8MaxKb) return cudaErrorInvalidValue;  // the per-unit scale table
+  if (s.n_split > op.b0_rows || (s.n_split < s.N && (!op.B1 || s.N - s.n_split > op.b1_rows)))
+    return cudaErrorInvalidValue;
+  CUtensorMap ta;
+  if (!make_tmap_bf16_2d(&ta, op.A, op.a_rows, (uint64_t)op.lda, op.lda, BM, 64)) return cudaErrorInvalidValue;
+  auto kern = gemm_w8_kernel<BM, BN, SA, SF, EPI>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  GemmShape sh = s;
+  if (sh.raster_g < 1) sh.raster_g = 1;
+  const int m_tiles = (s.M + BM - 1) / BM;
+  const int tiles = m_tiles * (s.N / BN);
+  const int kstages = s.K / 128;
+  sh.ksplit = 1;
+  sh.kb_per = kstages;
+  // split-K as the bf16 path: too few tiles for the GPU (one row block)
+  if (ea.part && ea.counters && m_tiles == 1 && tiles * 2 <= num_sms && kstages >= 2 &&
+      tiles * 4 <= kMaxSplitCounters) {
+    int ks = num_sms / tiles;
+    if (ks > 4) ks = 4;
+    if (ks > kMaxSplitUnits / tiles) ks = kMaxSplitUnits / tiles;
+    if (ks > kstages) ks = kstages;
+    const int kb_per = (kstages + ks - 1) / ks;
+    ks = (kstages + kb_per - 1) / kb_per;
+    const size_t need = (size_t)tiles * ks * s.M * BN * sizeof(float);
+    if (ks > 1 && need <= ea.part_bytes) {
+      sh.ksplit = ks;
+      sh.kb_per = kb_per;
+    }
+  }
+  DevStatus dst{st.word, st.wait_limit_ns};
+  const int units = tiles * sh.ksplit;
+  const int grid = units < num_sms ? units : num_sms;
+  return launch_pdl(kern, dim3(grid), dim3(kW8Threads), L::kBytes, stream, ta, op.B0, op.B1, op.s0, op.s1, sh, ea,
+                    dst);
+}
+
+template <Epi EPI, int BN>
+cudaError_t launch_w8_bm(const GemmShape& s, const GemmW8Operands& op, const EpiArgs& ea, const DevStatusHost& st,
+                         int num_sms, cudaStream_t stream) {
+  // 64 KB of A stages (L2 latency), two bf16 B stages, and the E4M3 ring
+  // (DRAM latency: several microseconds under load) as deep as the rest of
+  // shared memory allows
+  constexpr int kSA64 = 4, kSF64 = BN == 64 ? 16 : BN == 96 ? 9 : 6;
+  constexpr int kSA128 = 2, kSF128 = BN == 64 ? 16 : BN == 96 ? 9 : 6;
+  if (s.M <= 64) return launch_w8_impl<64, BN, kSA64, kSF64, EPI>(s, op, ea, st, num_sms, stream);
+  return launch_w8_impl<128, BN, kSA128, kSF128, EPI>(s, op, ea, st, num_sms, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, const EpiArgs& ea,
@@ -1087,6 +1550,18 @@ bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint6
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+cudaError_t launch_gemm_w8(const GemmShape& s, const GemmW8Operands& op, Epi epi, const EpiArgs& ea,
+                           const DevStatusHost& st, int num_sms, cudaStream_t stream) {
+  if (s.M <= 0 || s.K % 128 != 0) return cudaErrorInvalidValue;
+  switch (epi) {
+    case Epi::kStoreF32: return launch_w8_bm<Epi::kStoreF32, 64>(s, op, ea, st, num_sms, stream);
+    case Epi::kQRope: return launch_w8_bm<Epi::kQRope, 96>(s, op, ea, st, num_sms, stream);
+    case Epi::kKVCache: return launch_w8_bm<Epi::kKVCache, 128>(s, op, ea, st, num_sms, stream);
+    case Epi::kResidual: return launch_w8_bm<Epi::kResidual, 64>(s, op, ea, st, num_sms, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace mla

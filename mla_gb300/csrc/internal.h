@@ -155,6 +155,33 @@ struct EpiArgs {
 cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, const EpiArgs& ea,
                         const DevStatusHost& st, int num_sms, cudaStream_t stream);
 
+// The same product with B stored as FP8 (E4M3) codes and one power-of-two
+// scale per 128 x 128 block (scales [rows / 128 rounded up, K / 128]); B is
+// K-major ([N, K]), K a multiple of 128, one batch; the codes are stored
+// block-major: block (i, j) = rows 128i.., columns 128j.. is 16 KB at
+// ((i * K/128 + j) * 128) * 128, row-major inside (rows past the matrix are
+// zero).  The codes are bulk-copied and dequantized to bf16 in shared memory
+// (exact: the scales are powers of two); the product runs on the bf16
+// tensor-core path.  Decode-size M: the weight bytes halve.
+struct GemmW8Operands {
+  const __nv_bfloat16* A;
+  int lda;
+  int a_rows;
+  const uint8_t* B0;  // rows n < n_split
+  int b0_rows;
+  const float* s0;
+  const uint8_t* B1;  // rows n - n_split (may be null)
+  int b1_rows;
+  const float* s1;
+};
+cudaError_t launch_gemm_w8(const GemmShape& s, const GemmW8Operands& op, Epi epi, const EpiArgs& ea,
+                           const DevStatusHost& st, int num_sms, cudaStream_t stream);
+
+// bf16 [rows, cols] (cols a multiple of 128) -> E4M3 codes, block-major with
+// the row count padded to 128 (zeros), and scales [ceil(rows/128), cols/128]
+cudaError_t launch_fp8_quantize(const __nv_bfloat16* w, int rows, int cols, uint8_t* codes, float* scales,
+                                cudaStream_t stream);
+
 // ---- row kernels --------------------------------------------------------------
 cudaError_t launch_rmsnorm_rows(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_bfloat16* y, int rows,
                                 float eps, cudaStream_t stream);
