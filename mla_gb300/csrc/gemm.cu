@@ -922,14 +922,15 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
 }
 
 // ---------------------------------------------------------------------------
-// GEMM with FP8 block-scaled B (decode-size M).  320 threads:
-//   warp 0      producer: E4M3 tiles of B (BN rows x 128 bytes per 128-wide
-//               K stage; the codes are stored block-major, so a tile's
-//               stage is one or two contiguous bulk copies) into a deep
-//               SF-slot ring, and A (two 64-wide bf16 TMA boxes per stage)
-//               into an SA-slot ring; each ring is refilled as soon as a
-//               slot frees, and the first E4M3 stages are issued before the
-//               wait on the preceding kernel (weights are read-only)
+// GEMM with FP8 block-scaled B (decode-size M).  480 threads:
+//   warp 0      code producer: E4M3 tiles of B (BN rows x 128 bytes per
+//               128-wide K stage; the codes are stored block-major, so a
+//               tile's stage is one or two contiguous bulk copies) into a
+//               deep SF-slot ring, from before the wait on the preceding
+//               kernel (weights are read-only)
+//   warp 14     A producer: two 64-wide bf16 TMA boxes per stage into an
+//               SA-slot ring (its own thread, so an A load never waits
+//               behind the issue of a code copy)
 //   warp 1      TMEM allocation; one lane issues the bf16 MMAs
 //   warps 2..5  epilogue (as gemm_kernel: register stores, split-K fixup)
 //   warps 6..13 dequantization: each E4M3 tile -> bf16 (x its block scale)
@@ -937,7 +938,7 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
 //               that the MMAs read; a unit's block scales are read once
 //               into a shared-memory table
 // ---------------------------------------------------------------------------
-constexpr int kW8Threads = 448;
+constexpr int kW8Threads = 480;
 constexpr int kW8Deq = 256;    // dequantization threads (warps 6..13)
 constexpr int kW8MaxKb = 64;   // 128-wide K stages per unit whose scales fit the table
 
@@ -1068,27 +1069,29 @@ __global__ void __launch_bounds__(kW8Threads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) tma_prefetch_desc(&tmA);
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
+  if (warp == kW8Threads / 32 - 1 && lane == 0) tma_prefetch_desc(&tmA);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_launch_dependents();
-  // the producer and the dequantization warps touch only weights and shared
-  // memory before the wait; the producer waits itself before loading A
-  if (warp >= 1 && warp <= 5) pdl_wait();
+  // the code producer and the dequantization warps touch only weights and
+  // shared memory: only the MMA, epilogue and A-producer warps wait for the
+  // preceding kernel
+  if ((warp >= 1 && warp <= 5) || warp == kW8Threads / 32 - 1) pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
-      W8Cursor cf = cursor(), ca = cursor();
-      int nf = 0, na = 0;
-      auto issue_f = [&]() -> bool {
+      // E4M3 code tiles: weights only, so no wait on the preceding kernel
+      W8Cursor cf = cursor();
+      int nf = 0;
+      for (; cf.valid(); cf.next(), ++nf) {
         const int slot = nf % SF;
-        if (nf >= SF && !mbar_wait(&f_empty[slot], ((nf / SF) & 1) ^ 1, st, abort_flag, 81)) return false;
+        if (nf >= SF && !mbar_wait(&f_empty[slot], ((nf / SF) & 1) ^ 1, st, abort_flag, 81)) break;
         int m_blk;
         const int n0 = tile_n0(cf.unit, m_blk);
         const bool first_mat = n0 < s.n_split;
@@ -1103,49 +1106,28 @@ __global__ void __launch_bounds__(kW8Threads, 1)
         if (n1 < BN)
           bulk_load(dst + n1 * 128, bm + ((size_t)((rb >> 7) + 1) * kstages + cf.kb()) * 128 * 128, (BN - n1) * 128,
                     &f_full[slot]);
-        ++nf;
-        cf.next();
-        return true;
-      };
-      // weights first, before the wait on the preceding kernel: a fresh ring
-      while (cf.valid() && nf < SF) issue_f();
-      pdl_wait();
-      // Both rings are refilled as soon as a slot frees, tested with
-      // test_wait (never suspends: a full ring must not hold back the other);
-      // the E4M3 loads have a long latency and keep the whole ring in flight.
-      uint64_t t_last = globaltimer_ns();
-      while (cf.valid() || ca.valid()) {
-        bool progress = false;
-        if (cf.valid() && mbar_test(&f_empty[nf % SF], ((nf / SF) & 1) ^ 1)) {
-          issue_f();
-          progress = true;
-        }
-        if (ca.valid() && (na < SA || mbar_test(&a_empty[na % SA], ((na / SA) & 1) ^ 1))) {
-          const int slot = na % SA;
-          int m_blk;
-          tile_n0(ca.unit, m_blk);
-          mbar_arrive_expect_tx(&a_full[slot], L::kA);
-          uint8_t* sa = smem + slot * L::kA;
-          tma_load_2d(sa, &tmA, &a_full[slot], ca.kb() * 128, m_blk * BM);
-          tma_load_2d(sa + L::kA1, &tmA, &a_full[slot], ca.kb() * 128 + 64, m_blk * BM);
-          ++na;
-          ca.next();
-          progress = true;
-        }
-        if (progress) {
-          t_last = globaltimer_ns();
-        } else if (*abort_flag) {
-          break;
-        } else if (globaltimer_ns() - t_last > st.wait_limit_ns) {
-          report_timeout(st, 82);
-          *abort_flag = 1;
-          break;
-        }
       }
       // no copy may still be in flight into this CTA's shared memory
       for (int i = 0; i < SF && i < nf; ++i) {
         const int uses = (nf - 1 - i) / SF + 1;
         mbar_wait(&f_full[i], (uses - 1) & 1, st, nullptr, 83);
+      }
+    }
+  } else if (warp == kW8Threads / 32 - 1) {
+    if (lane == 0) {
+      // ---------------- A producer (its own warp: an A load never waits
+      // behind the issue of a code copy) ----------------
+      W8Cursor ca = cursor();
+      int na = 0;
+      for (; ca.valid(); ca.next(), ++na) {
+        const int slot = na % SA;
+        if (na >= SA && !mbar_wait(&a_empty[slot], ((na / SA) & 1) ^ 1, st, abort_flag, 82)) break;
+        int m_blk;
+        tile_n0(ca.unit, m_blk);
+        mbar_arrive_expect_tx(&a_full[slot], L::kA);
+        uint8_t* sa = smem + slot * L::kA;
+        tma_load_2d(sa, &tmA, &a_full[slot], ca.kb() * 128, m_blk * BM);
+        tma_load_2d(sa + L::kA1, &tmA, &a_full[slot], ca.kb() * 128 + 64, m_blk * BM);
       }
       for (int i = 0; i < SA && i < na; ++i) {
         const int uses = (na - 1 - i) / SA + 1;
@@ -1373,11 +1355,11 @@ cudaError_t launch_w8_impl(const GemmShape& s, const GemmW8Operands& op, const E
 template <Epi EPI, int BN>
 cudaError_t launch_w8_bm(const GemmShape& s, const GemmW8Operands& op, const EpiArgs& ea, const DevStatusHost& st,
                          int num_sms, cudaStream_t stream) {
-  // 64 KB of A stages (L2 latency), two bf16 B stages, and the E4M3 ring
-  // (DRAM latency: several microseconds under load) as deep as the rest of
-  // shared memory allows
-  constexpr int kSA64 = 4, kSF64 = BN == 64 ? 16 : BN == 96 ? 9 : 6;
-  constexpr int kSA128 = 2, kSF128 = BN == 64 ? 16 : BN == 96 ? 9 : 6;
+  // 64-96 KB of A stages, two bf16 B stages, and the E4M3 ring as deep as
+  // the rest of shared memory allows (both latencies are several
+  // microseconds here: the per-SM copy engine serves both rings)
+  constexpr int kSA64 = BN == 128 ? 4 : 6, kSF64 = BN == 64 ? 12 : 6;
+  constexpr int kSA128 = BN == 128 ? 2 : 3, kSF128 = BN == 64 ? 12 : 6;
   if (s.M <= 64) return launch_w8_impl<64, BN, kSA64, kSF64, EPI>(s, op, ea, st, num_sms, stream);
   return launch_w8_impl<128, BN, kSA128, kSF128, EPI>(s, op, ea, st, num_sms, stream);
 }
