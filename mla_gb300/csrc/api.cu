@@ -176,7 +176,7 @@ int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok,
               int t_mod, int t_off, __nv_bfloat16* ckv_cache, __nv_bfloat16* kpe_cache, int cap, void* ws,
               const Layout& L, const DevStatusHost& st, int sms, cudaStream_t stream, Stager& sg,
               int* launches, bool with_q = true, const int* pos = nullptr, int pos_max = 0,
-              const mla_weights_fp8_t* f8 = nullptr) {
+              const mla_weights_fp8_t* f8 = nullptr, __nv_bfloat16* qpe_out = nullptr) {
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   (void)n_pos;
   sg.start(MLA_STAGE_INPUT_NORM);
@@ -245,6 +245,7 @@ int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok,
     ea.ldo = MLA_HEADS * MLA_QK;
     ea.cs = at<float2>(ws, L.cs);
     ea.t_mod = pos ? n_tok : t_mod;  // per-row positions: one RoPE table row per token
+    ea.qpe_out = qpe_out;
     set_split(ea, ws, L);
     if (f8) {
       GemmW8Operands o8{at<__nv_bfloat16>(ws, L.cq), MLA_Q_LORA, n_tok, static_cast<const uint8_t*>(f8->w_q_b),
@@ -581,9 +582,12 @@ int decode_latent_impl(const mla_weights_t* w, const mla_params_t* params, const
   Stager sg{p.timing, stream_};
   int launches = 0;
   if (cudaMemsetAsync(st.word, 0, kStatusRegion, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+  // up to 128 rows the q_b epilogue (register stores) also writes the rotated
+  // q^pe into q_lat; more rows take the TMA-store epilogue and a copy kernel
+  const bool qpe_in_epilogue = B <= 128;
   rc = front_end(w, p, x, B, 1, P, 1, P, static_cast<__nv_bfloat16*>(ckv_cache),
                  static_cast<__nv_bfloat16*>(kpe_cache), cap, workspace, L, st, sms, stream_, sg, &launches, true,
-                 pos, P);
+                 pos, P, nullptr, qpe_in_epilogue ? at<__nv_bfloat16>(workspace, L.qlat) : nullptr);
   if (rc) return rc;
 
   const __nv_bfloat16* wkvb = static_cast<const __nv_bfloat16*>(w->w_kv_b);
@@ -600,8 +604,11 @@ int decode_latent_impl(const mla_weights_t* w, const mla_params_t* params, const
     ea.c_col_step = 576;
     set_split(ea, workspace, L);
     MLA_TRY(launch_gemm(s, op, Epi::kStoreBf16, ea, st, sms, stream_));
-    MLA_TRY(launch_copy_qpe(at<__nv_bfloat16>(workspace, L.q), at<__nv_bfloat16>(workspace, L.qlat), B, stream_));
-    launches += 2;
+    launches += 1;
+    if (!qpe_in_epilogue) {
+      MLA_TRY(launch_copy_qpe(at<__nv_bfloat16>(workspace, L.q), at<__nv_bfloat16>(workspace, L.qlat), B, stream_));
+      launches += 1;
+    }
   }
   sg.stop(MLA_STAGE_ABSORB_Q);
 

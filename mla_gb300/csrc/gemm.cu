@@ -183,6 +183,11 @@ __device__ __forceinline__ void run_epilogue(const EpiArgs& ea, const Src& ld, i
         }
         store32_bf16(dst + nope_cols, x1);
         store32_bf16(dst + nope_cols + 32, x2);
+        if (ea.qpe_out) {  // latent decode: the rotated q^pe is also q_lat[row, head, 512:576]
+          __nv_bfloat16* qd = ea.qpe_out + ((size_t)row * 64 + n0 / 192) * 576 + 512;
+          store32_bf16(qd, x1);
+          store32_bf16(qd + 32, x2);
+        }
       }
     }
   } else if constexpr (EPI == Epi::kKVCache) {

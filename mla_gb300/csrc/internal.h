@@ -127,6 +127,9 @@ struct EpiArgs {
   //         position index of a row = row % t_mod into cs (float2 [.., 32])
   const float2* cs;
   int t_mod;
+  // kQRope, register epilogue only (decode sizes): when set, the rotated pe
+  // columns of row r, head h are also written to qpe_out[(r*64 + h)*576 + 512 ..]
+  __nv_bfloat16* qpe_out;
   // kKVCache: K[b, h, t, 0:128] / V[b, h, t, 0:128] / K[b, h, t, 128:192] = kpe[row]
   //           b = row / t_mod, t = t_off + row % t_mod
   __nv_bfloat16* kc;
