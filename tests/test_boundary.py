@@ -170,3 +170,39 @@ def test_prefill_chunk_latent_argument_checks():
     assert call(out=None) == -1
     assert call(kpe=FAKE + (5 << 30) + 8) == -2
     assert call(nbytes=ws_bytes - 256) == -3
+
+
+def test_fp8_entry_argument_checks():
+    lib = m.lib()
+    # quantizer: cols must be a multiple of 128, pointers 16-byte aligned (scales 4-byte)
+    assert lib.mla_quantize_fp8(FAKE, 128, 100, FAKE + (1 << 30), FAKE + (2 << 30), None) == -1
+    assert lib.mla_quantize_fp8(None, 128, 128, FAKE + (1 << 30), FAKE + (2 << 30), None) == -1
+    assert lib.mla_quantize_fp8(FAKE + 8, 128, 128, FAKE + (1 << 30), FAKE + (2 << 30), None) == -2
+    assert lib.mla_quantize_fp8(FAKE, 128, 128, FAKE + (1 << 30), FAKE + (2 << 30) + 2, None) == -2
+    # FP8 decode: every scale pointer required
+    vals = {f: FAKE + 4096 * i for i, (f, _) in enumerate(m.MlaWeightsFp8._fields_)}
+    ws_bytes = lib.mla_workspace_size(m.MODE_DECODE, 4, 10, 0)
+    for missing in ("s_q_a", "s_o"):
+        w = m.MlaWeightsFp8(*[None if f == missing else vals[f] for f, _ in m.MlaWeightsFp8._fields_])
+        assert lib.mla_decode_fp8(ctypes.byref(w), None, FAKE + (1 << 30), 4, 10, FAKE + (4 << 30), FAKE + (5 << 30),
+                                  11, FAKE + (2 << 30), FAKE + (3 << 30), ws_bytes, None) == -1
+    w = m.MlaWeightsFp8(*[vals[f] for f, _ in m.MlaWeightsFp8._fields_])
+    assert lib.mla_decode_fp8(ctypes.byref(w), None, FAKE + (1 << 30), 4, 10, FAKE + (4 << 30), FAKE + (5 << 30),
+                              10, FAKE + (2 << 30), FAKE + (3 << 30), ws_bytes, None) == -1  # cap < P + 1
+
+
+def test_varlen_decode_argument_checks():
+    lib = m.lib()
+    w = fake_weights()
+    ws_bytes = lib.mla_workspace_size(m.MODE_DECODE, 4, 10, 0)
+    args = (FAKE + (1 << 30), 4)
+    # the per-sequence positions are required and 4-byte aligned; P_max + 1 <= cap
+    assert lib.mla_decode_varlen(ctypes.byref(w), None, *args, None, 10, FAKE + (4 << 30), FAKE + (5 << 30), 11,
+                                 FAKE + (2 << 30), FAKE + (3 << 30), ws_bytes, None) == -1
+    assert lib.mla_decode_varlen(ctypes.byref(w), None, *args, FAKE + (6 << 30) + 2, 10, FAKE + (4 << 30),
+                                 FAKE + (5 << 30), 11, FAKE + (2 << 30), FAKE + (3 << 30), ws_bytes, None) == -2
+    assert lib.mla_decode_varlen(ctypes.byref(w), None, *args, FAKE + (6 << 30), 11, FAKE + (4 << 30),
+                                 FAKE + (5 << 30), 11, FAKE + (2 << 30), FAKE + (3 << 30), ws_bytes, None) == -1
+    lws = lib.mla_workspace_size(m.MODE_DECODE_LATENT, 4, 10, 0)
+    assert lib.mla_decode_latent_varlen(ctypes.byref(w), None, *args, None, 10, FAKE + (4 << 30), FAKE + (5 << 30),
+                                        11, FAKE + (2 << 30), FAKE + (3 << 30), lws, None) == -1
