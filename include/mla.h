@@ -291,7 +291,8 @@ typedef struct {
 
 /* mla_decode with FP8 block-scaled weights: the same step, arguments,
  * workspace (MLA_MODE_DECODE) and errors; every projection reads its E4M3
- * codes and scales. */
+ * codes and scales (codes 16-byte aligned, scales 4-byte aligned, else
+ * MLA_ERR_ALIGNMENT). */
 int mla_decode_fp8(const mla_weights_fp8_t* w, const mla_params_t* params, const void* x, int B, int P,
                    void* k_cache, void* v_cache, int cap, void* out, void* workspace, size_t workspace_bytes,
                    void* stream);

@@ -671,8 +671,10 @@ int mla_decode_fp8(const mla_weights_fp8_t* w, const mla_params_t* params, const
                    void* stream) {
   if (!w) return MLA_ERR_INVALID_ARG;
   for (const void* q : {(const void*)w->s_q_a, (const void*)w->s_q_b, (const void*)w->s_kv_a, (const void*)w->s_kv_b,
-                        (const void*)w->s_o})
+                        (const void*)w->s_o}) {
     if (!q) return MLA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(q) & 3) return MLA_ERR_ALIGNMENT;
+  }
   // the gains and code matrices in the bf16 struct's places (checked there; the
   // projections read the codes and scales through w)
   const mla_weights_t view{w->w_in_norm, w->w_q_a, w->w_q_a_norm, w->w_q_b,

@@ -206,3 +206,13 @@ def test_varlen_decode_argument_checks():
     lws = lib.mla_workspace_size(m.MODE_DECODE_LATENT, 4, 10, 0)
     assert lib.mla_decode_latent_varlen(ctypes.byref(w), None, *args, None, 10, FAKE + (4 << 30), FAKE + (5 << 30),
                                         11, FAKE + (2 << 30), FAKE + (3 << 30), lws, None) == -1
+
+
+def test_fp8_scales_alignment():
+    lib = m.lib()
+    vals = {f: FAKE + 4096 * i for i, (f, _) in enumerate(m.MlaWeightsFp8._fields_)}
+    vals["s_kv_b"] += 2
+    w = m.MlaWeightsFp8(*[vals[f] for f, _ in m.MlaWeightsFp8._fields_])
+    ws_bytes = lib.mla_workspace_size(m.MODE_DECODE, 4, 10, 0)
+    assert lib.mla_decode_fp8(ctypes.byref(w), None, FAKE + (1 << 30), 4, 10, FAKE + (4 << 30), FAKE + (5 << 30),
+                              11, FAKE + (2 << 30), FAKE + (3 << 30), ws_bytes, None) == -2
