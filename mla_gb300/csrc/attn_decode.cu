@@ -663,21 +663,23 @@ __global__ void __launch_bounds__(kLatThreads, 1)
 }
 
 // Merge the partials of the sequences cut between CTAs (the others were
-// written by latent_attn_tc directly).  Block = (head, sequence), 128 threads,
-// four latent columns per thread.
+// written by latent_attn_tc directly).  Block = (group of 8 heads, sequence),
+// one warp per head, 16 latent columns per lane.  The pieces are taken four
+// at a time: their (m, l) pairs and partial rows are all requested before
+// any is used (one memory round trip per group of four), then folded into
+// a running maximum, denominator and sum.
 constexpr int kLatMaxCtas = 1024;
+constexpr int kCombineHeads = 8;
 
-__global__ void __launch_bounds__(128) latent_combine_kernel(const float* __restrict__ part_o,
-                                                             const float2* __restrict__ part_ml,
-                                                             __nv_bfloat16* __restrict__ out, int L, int B, int G,
-                                                             const int* __restrict__ plan) {
-  __shared__ int s_slot[kLatMaxCtas];
-  __shared__ float s_w[kLatMaxCtas];
-  __shared__ float s_red[2][4];
+__global__ void __launch_bounds__(32 * kCombineHeads) latent_combine_kernel(const float* __restrict__ part_o,
+                                                                             const float2* __restrict__ part_ml,
+                                                                             __nv_bfloat16* __restrict__ out, int L,
+                                                                             int B, int G,
+                                                                             const int* __restrict__ plan) {
   pdl_launch_dependents();
   pdl_wait();
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.x * kCombineHeads + (threadIdx.x >> 5), b = blockIdx.y;
   const int nt = (L + kLatTile - 1) / kLatTile;
   // the sequence's first and last flattened tile (per-sequence lengths: from the plan)
   const long long total = plan ? (long long)plan[B] : (long long)B * nt;
@@ -688,53 +690,68 @@ __global__ void __launch_bounds__(128) latent_combine_kernel(const float* __rest
   const int g1 = (int)(((xb + 1) * G - 1) / total);
   if (g0 == g1) return;  // whole sequence in one CTA: written directly
   const int n = g1 - g0 + 1;
-  float mloc = -INFINITY;
-  for (int k = tid; k < n; k += 128) {
-    const int gg = g0 + k;
-    if (plan && plan[B + 1 + 3 * gg + 2] == 0) {  // a CTA with no tiles wrote nothing
-      s_slot[k] = -1;
-      s_w[k] = -INFINITY;
-      continue;
+  float m_run = -INFINITY, l_run = 0.f;
+  float4 acc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < n; k0 += 4) {
+    float2 ml[4];
+    float4 v[4][4];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const int gg = g0 + k0 + kk;
+      int slot = -1;
+      if (k0 + kk < n && !(plan && plan[B + 1 + 3 * gg + 2] == 0)) {  // a CTA with no tiles wrote nothing
+        const int gseq = plan ? plan[B + 1 + 3 * gg] : (int)(lat_range_start(gg, total, G) / nt);
+        slot = (b == gseq) ? 2 * gg : 2 * gg + 1;
+      }
+      if (slot >= 0) {
+        ml[kk] = part_ml[(size_t)slot * 64 + h];
+        const float* row = part_o + ((size_t)slot * 64 + h) * 512;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[kk][j] = *reinterpret_cast<const float4*>(row + j * 128 + lane * 4);
+      } else {
+        ml[kk] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[kk][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
-    const int gseq = plan ? plan[B + 1 + 3 * gg] : (int)(lat_range_start(gg, total, G) / nt);
-    const int slot = (b == gseq) ? 2 * gg : 2 * gg + 1;
-    const float2 ml = part_ml[(size_t)slot * 64 + h];
-    s_slot[k] = slot;
-    s_w[k] = ml.x;
-    mloc = fmaxf(mloc, ml.x);
-  }
-  mloc = warp_max(mloc);
-  if (lane == 0) s_red[0][warp] = mloc;
-  __syncthreads();
-  const float mx = fmaxf(fmaxf(s_red[0][0], s_red[0][1]), fmaxf(s_red[0][2], s_red[0][3]));
-  float dloc = 0.f;
-  for (int k = tid; k < n; k += 128) {
-    if (s_slot[k] < 0) {
-      s_w[k] = 0.f;
-      continue;
+    float m_new = m_run;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) m_new = fmaxf(m_new, ml[kk].x);
+    // the first piece of a sequence always holds keys, so m_new is finite
+    const float sc = exp2f(m_run - m_new);
+    l_run *= sc;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc[j].x *= sc;
+      acc[j].y *= sc;
+      acc[j].z *= sc;
+      acc[j].w *= sc;
     }
-    const float w = exp2f(s_w[k] - mx);
-    dloc += w * part_ml[(size_t)s_slot[k] * 64 + h].y;
-    s_w[k] = w;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const float w = exp2f(ml[kk].x - m_new);
+      l_run = fmaf(w, ml[kk].y, l_run);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc[j].x = fmaf(w, v[kk][j].x, acc[j].x);
+        acc[j].y = fmaf(w, v[kk][j].y, acc[j].y);
+        acc[j].z = fmaf(w, v[kk][j].z, acc[j].z);
+        acc[j].w = fmaf(w, v[kk][j].w, acc[j].w);
+      }
+    }
+    m_run = m_new;
   }
-  dloc = warp_sum(dloc);
-  if (lane == 0) s_red[1][warp] = dloc;
-  __syncthreads();
-  const float inv = 1.f / ((s_red[1][0] + s_red[1][1]) + (s_red[1][2] + s_red[1][3]));
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k = 0; k < n; ++k) {
-    if (s_slot[k] < 0) continue;
-    const float w = s_w[k];
-    const float4 v = *reinterpret_cast<const float4*>(part_o + ((size_t)s_slot[k] * 64 + h) * 512 + tid * 4);
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
-    acc.z = fmaf(w, v.z, acc.z);
-    acc.w = fmaf(w, v.w, acc.w);
+  const float inv = 1.f / l_run;
+  __nv_bfloat16* o = out + ((size_t)b * 64 + h) * 512;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint2 w;
+    w.x = pack_bf16x2(acc[j].x * inv, acc[j].y * inv);
+    w.y = pack_bf16x2(acc[j].z * inv, acc[j].w * inv);
+    *reinterpret_cast<uint2*>(o + j * 128 + lane * 4) = w;
   }
-  uint2 o;
-  o.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-  o.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  *reinterpret_cast<uint2*>(out + ((size_t)b * 64 + h) * 512 + tid * 4) = o;
 }
 
 int chunk_len_for(int L, int splits, int granule) {
@@ -784,7 +801,7 @@ int latent_ctas(int B, int L, int num_sms) {
   const long long total = (long long)B * ((L + kLatTile - 1) / kLatTile);
   long long g = total / 2;
   if (g > num_sms) g = num_sms;
-  if (g > kLatMaxCtas) g = kLatMaxCtas;  // the combine's per-sequence tables
+  if (g > kLatMaxCtas) g = kLatMaxCtas;  // bounds the partial slots and the plan
   if (g < 1) g = 1;
   return (int)g;
 }
@@ -818,7 +835,8 @@ cudaError_t launch_latent_attention(const LatentAttnArgs& a, const DevStatusHost
   if (e != cudaSuccess) return e;
   ++*launches;
   if (a.ctas > 1) {
-    e = launch_pdl(latent_combine_kernel, dim3(64, a.B), dim3(128), 0, stream, (const float*)a.part_o,
+    e = launch_pdl(latent_combine_kernel, dim3(64 / kCombineHeads, a.B), dim3(32 * kCombineHeads), 0, stream,
+                   (const float*)a.part_o,
                    (const float2*)a.part_ml, a.olat, a.L, a.B, a.ctas, (const int*)la.plan);
     ++*launches;
   }
