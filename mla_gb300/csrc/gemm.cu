@@ -86,8 +86,18 @@ struct TmemSrc {
   }
 };
 
+// Split-K partial slots.  A slot holds one K slice's BM x BN fp32 tile,
+// stored per warp quarter column by column: element (row r of quarter q,
+// column c) at (q * BN + c) * (BM / 4) + r, so that the quarter's threads
+// (one row each) write and read each column as one contiguous run.
+template <int BM, int BN>
+__device__ __forceinline__ float* part_slot(float* part, int slot, int quarter, int lq) {
+  return part + (size_t)slot * BM * BN + (size_t)quarter * BN * (BM / 4) + lq;
+}
+
+template <int RPQ>
 struct PartSrc {
-  const float* base;    // this row's slot 0
+  const float* base;    // this thread's element of column 0 in slot 0
   size_t slot_stride;   // floats between slots
   int slots;
   bool ok;
@@ -96,33 +106,23 @@ struct PartSrc {
 #pragma unroll
     for (int i = 0; i < 32; ++i) acc[i] = 0.f;
     if (ok) {
+      const float* p = base + (size_t)c * RPQ;
       int sl = 0;
-      for (; sl + 2 <= slots; sl += 2) {  // two slots (16 loads) in flight
-        float4 v[16];
+      for (; sl + 2 <= slots; sl += 2) {  // two slots (64 loads) in flight
+        float v[64];
 #pragma unroll
         for (int u = 0; u < 2; ++u)
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            v[8 * u + j] = __ldcg(reinterpret_cast<const float4*>(base + (sl + u) * slot_stride + c) + j);
+          for (int j = 0; j < 32; ++j) v[32 * u + j] = __ldcg(p + (sl + u) * slot_stride + j * RPQ);
 #pragma unroll
-        for (int u = 0; u < 2; ++u)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            acc[4 * j] += v[8 * u + j].x;
-            acc[4 * j + 1] += v[8 * u + j].y;
-            acc[4 * j + 2] += v[8 * u + j].z;
-            acc[4 * j + 3] += v[8 * u + j].w;
-          }
+        for (int j = 0; j < 32; ++j) acc[j] += v[j] + v[32 + j];
       }
       for (; sl < slots; ++sl) {
+        float v[32];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(base + sl * slot_stride + c) + j);
-          acc[4 * j] += v.x;
-          acc[4 * j + 1] += v.y;
-          acc[4 * j + 2] += v.z;
-          acc[4 * j + 3] += v.w;
-        }
+        for (int j = 0; j < 32; ++j) v[j] = __ldcg(p + sl * slot_stride + j * RPQ);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] += v[j];
       }
     }
 #pragma unroll
@@ -777,20 +777,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&tempty_bar[acc]);
       } else {
         // this K slice's partial -> its slot; the last warp of the quarter reduces
-        const int rows_pt = s.M < BM ? s.M : BM;
-        const bool in_slot = row_ok && rit < rows_pt;
-        float* slot = ea.part + ((size_t)(tile * ksplit + ks) * rows_pt + (in_slot ? rit : 0)) * BN;
+        const int lq = rit - quarter * (BM / 4);  // row within the quarter
+        float* slot = part_slot<BM, BN>(ea.part, tile * ksplit + ks, quarter, lq);
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           uint32_t r[32];
           tmem_ld32(taddr + c, r);
           tmem_wait_ld();
-          if (in_slot) {
-            float4* d = reinterpret_cast<float4*>(slot + c);
+          if (row_ok) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              d[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            for (int j = 0; j < 32; ++j) slot[(c + j) * (BM / 4)] = __uint_as_float(r[j]);
           }
         }
         tc_fence_before();
@@ -802,8 +798,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         prev = __shfl_sync(0xffffffffu, prev, 0);
         if (prev == ksplit - 1) {
           __threadfence();
-          const PartSrc src{ea.part + ((size_t)tile * ksplit * rows_pt + (in_slot ? rit : 0)) * BN,
-                            (size_t)rows_pt * BN, ksplit, in_slot};
+          const PartSrc<BM / 4> src{part_slot<BM, BN>(ea.part, tile * ksplit, quarter, lq), (size_t)BM * BN, ksplit,
+                                    row_ok};
           run_epilogue<BN, EPI>(ea, src, batch, row, n_blk * BN, row_ok);
           if (lane == 0) ea.counters[tile * 4 + quarter] = 0;  // ready for the next GEMM
         }
@@ -906,7 +902,7 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
     if (ks > kblocks) ks = kblocks;
     const int kb_per = (kblocks + ks - 1) / ks;
     ks = (kblocks + kb_per - 1) / kb_per;
-    const size_t need = (size_t)tiles * ks * s.M * BN * sizeof(float);
+    const size_t need = (size_t)tiles * ks * BM * BN * sizeof(float);
     if (ks > 1 && need <= ea.part_bytes) {
       sh.ksplit = ks;
       sh.kb_per = kb_per;
@@ -1266,20 +1262,16 @@ __global__ void __launch_bounds__(kW8Threads, 1)
         tc_fence_before();
         mbar_arrive(&tempty[acc]);
       } else {
-        const int rows_pt = s.M < BM ? s.M : BM;
-        const bool in_slot = row_ok && rit < rows_pt;
-        float* slot = ea.part + ((size_t)(tile * ksplit + ks) * rows_pt + (in_slot ? rit : 0)) * BN;
+        const int lq = rit - quarter * (BM / 4);  // row within the quarter
+        float* slot = part_slot<BM, BN>(ea.part, tile * ksplit + ks, quarter, lq);
 #pragma unroll 1
         for (int cc = 0; cc < BN; cc += 32) {
           uint32_t r[32];
           tmem_ld32(taddr + cc, r);
           tmem_wait_ld();
-          if (in_slot) {
-            float4* d = reinterpret_cast<float4*>(slot + cc);
+          if (row_ok) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              d[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            for (int j = 0; j < 32; ++j) slot[(cc + j) * (BM / 4)] = __uint_as_float(r[j]);
           }
         }
         tc_fence_before();
@@ -1291,8 +1283,8 @@ __global__ void __launch_bounds__(kW8Threads, 1)
         prev = __shfl_sync(0xffffffffu, prev, 0);
         if (prev == ksplit - 1) {
           __threadfence();
-          const PartSrc src{ea.part + ((size_t)tile * ksplit * rows_pt + (in_slot ? rit : 0)) * BN,
-                            (size_t)rows_pt * BN, ksplit, in_slot};
+          const PartSrc<BM / 4> src{part_slot<BM, BN>(ea.part, tile * ksplit, quarter, lq), (size_t)BM * BN, ksplit,
+                                    row_ok};
           run_epilogue<BN, EPI>(ea, src, 0, row, n0, row_ok);
           if (lane == 0) ea.counters[tile * 4 + quarter] = 0;
         }
@@ -1344,7 +1336,7 @@ cudaError_t launch_w8_impl(const GemmShape& s, const GemmW8Operands& op, const E
     if (ks > kstages) ks = kstages;
     const int kb_per = (kstages + ks - 1) / ks;
     ks = (kstages + kb_per - 1) / kb_per;
-    const size_t need = (size_t)tiles * ks * s.M * BN * sizeof(float);
+    const size_t need = (size_t)tiles * ks * BM * BN * sizeof(float);
     if (ks > 1 && need <= ea.part_bytes) {
       sh.ksplit = ks;
       sh.kb_per = kb_per;

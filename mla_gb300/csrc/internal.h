@@ -98,9 +98,10 @@ struct GemmShape {
 // writes its float32 partial to its own slot; the last warp to finish a
 // 32-row slice of the tile (counter per tile and quarter) sums the slots in
 // slice order and runs the epilogue.  Units = tiles x slices <= kMaxSplitUnits.
+// A slot holds a whole BM x BN tile (BM = 64 for M <= 64, else 128).
 constexpr int kMaxSplitUnits = 160;
 constexpr int kMaxSplitCounters = 960;
-inline size_t split_part_bytes(int M) { return (size_t)kMaxSplitUnits * (M < 128 ? M : 128) * 256 * sizeof(float); }
+inline size_t split_part_bytes(int M) { return (size_t)kMaxSplitUnits * (M <= 64 ? 64 : 128) * 256 * sizeof(float); }
 
 struct GemmOperands {
   const __nv_bfloat16* A;
