@@ -24,8 +24,9 @@ struct Layout {
   size_t split_bytes;  // split-K partial slots (decode modes), 0 = none
 };
 
-// Status region: the device status word at byte 0, split-K counters from
-// byte 256 (kMaxSplitCounters ints); cleared at the start of every call.
+// Status region: the device status word at byte 0, the prefill attention's
+// work counter at word kWorkCounterWord, split-K counters from byte 256
+// (kMaxSplitCounters ints); cleared at the start of every call.
 constexpr size_t kStatusRegion = 256 + kMaxSplitCounters * sizeof(int);
 
 Layout make_layout(int mode, int B, int t_or_p, int num_sms, int cap = 0) {

@@ -5,12 +5,18 @@
 // (online softmax over 128-key tiles; scores and probabilities never reach
 // global memory).
 //
-// CTA = (128-query tile, head, sequence), heaviest tiles launched first.
+// Persistent: one CTA per SM takes work items (128-query tile, head,
+// sequence) from an atomic counter, in the order (sequence, head, query tile
+// from the last, heaviest, to the first) so that the query tiles of one head
+// run together and share its K/V tiles in L2.  Each item's Q load and first
+// scores overlap the previous item's last P.V and epilogue.
 // Chunked prefill: the queries sit at positions past..past+T-1 and attend to
 // keys 0..past+T-1 of the cache (the chunk's own keys written after the
 // cached ones), the causal mask offset by past.
 // Warp roles (256 threads):
-//   warp 0   TMA: the Q tile once, then K tiles into a 2-slot ring
+//   warp 0   work scheduler (atomic counter -> a 4-slot ring of item
+//            indices in shared memory that every role reads), then TMA: the
+//            item's Q tile, then its K tiles into a 2-slot ring
 //   warp 6   TMA: V tiles into a 2-slot ring (each K and V tile is requested
 //            a whole tile ahead of the MMA that reads it)
 //   warp 1   TMEM allocation; one lane issues S_j = Q K_j^T (M=128 N=128
@@ -27,7 +33,8 @@
 //            read S_j from TMEM, scale, causal mask on the diagonal tile,
 //            running max with lazy rescaling (O is rescaled in TMEM only when
 //            the max grows by more than 2^8, so P stays <= 256), P_j as bf16
-//            over S_j, and at the end O / l to global memory.
+//            over S_j, and at the end O / l to global memory (after the
+//            next item's Q has been copied, so its first scores overlap).
 // Layout: Q [B*T, 64*192], K/V caches [B, 64, cap, 192|128] (TMA 3D views
 // whose position extent is T, so keys >= T read as zeros), O [B*T, 64*128].
 #include "common.cuh"
@@ -49,8 +56,12 @@ constexpr uint32_t kTmS = 0, kTmO = 256, kTmQ = 384;
 constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 
+constexpr int kItemRing = 4;
+constexpr int kItemReaders = 3 + 128;  // V producer, S issuer, P.V issuer, softmax threads
+
 struct Bars {
-  uint64_t q_full, q_tmem;
+  uint64_t q_full, q_tmem, q_empty, o_free;
+  uint64_t item_full[kItemRing], item_empty[kItemRing];
   uint64_t k_full[2], k_empty[2];
   uint64_t v_full[2], v_empty[2];
   uint64_t s_full[2];
@@ -58,42 +69,62 @@ struct Bars {
   uint64_t drain_s, drain_pv;
   uint32_t tmem_slot;
   int abort;
+  int item[kItemRing];
 };
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+// Work item w (the order described above) -> its query tile, head, sequence.
+struct Item {
+  int qt, h, b, q0, n_kv;
+  __device__ __forceinline__ Item(int w, int n_qt, int T, int past) {
+    const int hb = w / n_qt;
+    qt = n_qt - 1 - (w - hb * n_qt);
+    h = hb & 63;
+    b = hb >> 6;
+    q0 = qt * 128;
+    // keys 0 .. past + q0 + 127 (the tile's last query), at most past + T of them
+    n_kv = min((past + q0 + 127) / 128 + 1, (past + T + 127) / 128);
+  }
+};
+
+// Every role reads item `it` from the ring (bounded wait), then releases the slot.
+__device__ __forceinline__ bool read_item(Bars* bar, int it, int& w, const DevStatus& st, volatile int* abort_flag) {
+  const int slot = it % kItemRing;
+  if (!mbar_wait(&bar->item_full[slot], (it / kItemRing) & 1, st, abort_flag, 39)) return false;
+  w = *reinterpret_cast<volatile int*>(&bar->item[slot]);
+  mbar_arrive(&bar->item_empty[slot]);
+  return true;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ o, int T, int n_qt,
-                    float sl2, int past, const DevStatus st) {
+                    int n_items, float sl2, int past, int* __restrict__ work, const DevStatus st) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bar = reinterpret_cast<Bars*>(smem + kBarOff);
   volatile int* abort_flag = &bar->abort;
-
-  const int qt = n_qt - 1 - (int)blockIdx.x;
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
-  const int q0 = qt * 128;
-  // keys 0 .. past + q0 + 127 (the tile's last query), at most past + T of them
-  const int n_kv = min((past + q0 + 127) / 128 + 1, (past + T + 127) / 128);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(&bar->q_full, 1);
     mbar_init(&bar->q_tmem, 128);
+    mbar_init(&bar->q_empty, 128);
+    mbar_init(&bar->o_free, 128);
+    for (int i = 0; i < kItemRing; ++i) {
+      mbar_init(&bar->item_full[i], 1);
+      mbar_init(&bar->item_empty[i], kItemReaders);
+    }
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar->k_full[i], 1);
+      mbar_init(&bar->k_empty[i], 1);
       mbar_init(&bar->v_full[i], 1);
       mbar_init(&bar->v_empty[i], 1);
       mbar_init(&bar->s_full[i], 1);
+      mbar_init(&bar->p_full[i], 128);
+      mbar_init(&bar->pv_done[i], 1);
     }
-    mbar_init(&bar->k_full[0], 1);
-    mbar_init(&bar->k_empty[0], 1);
-    mbar_init(&bar->k_full[1], 1);
-    mbar_init(&bar->k_empty[1], 1);
-    mbar_init(&bar->p_full[0], 128);
-    mbar_init(&bar->p_full[1], 128);
-    mbar_init(&bar->pv_done[0], 1);
-    mbar_init(&bar->pv_done[1], 1);
     mbar_init(&bar->drain_s, 1);
     mbar_init(&bar->drain_pv, 1);
     bar->abort = 0;
@@ -107,27 +138,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bar->tmem_slot;
-  const int kv_row = b * 64 + h;
   pdl_launch_dependents();
   pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---- Q and K producer ----
+      // ---- work scheduler, Q and K producer ----
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
-      mbar_arrive_expect_tx(&bar->q_full, 3 * kAtom);
-      for (int c = 0; c < 3; ++c) tma_load_3d(smem + kQOff + c * kAtom, &tmQ, &bar->q_full, h * 192 + 64 * c, q0, b);
       int issued[2] = {0, 0};
-      for (int j = 0; j < n_kv; ++j) {
-        const int slot = j & 1;
-        if (!mbar_wait(&bar->k_empty[slot], ((j >> 1) & 1) ^ 1, st, abort_flag, 40)) break;
-        mbar_arrive_expect_tx(&bar->k_full[slot], 3 * kAtom);
+      int q_loads = 0;
+      int gt = 0;  // this CTA's K tiles so far (ring position)
+      for (int it = 0;; ++it) {
+        const int slot = it % kItemRing;
+        if (it >= kItemRing && !mbar_wait(&bar->item_empty[slot], (it / kItemRing - 1) & 1, st, abort_flag, 38))
+          break;
+        int w = atomicAdd(work, 1);
+        if (w >= n_items) w = -1;
+        bar->item[slot] = w;
+        mbar_arrive(&bar->item_full[slot]);  // release: the index is visible to every waiting role
+        if (w < 0) break;
+        const Item t(w, n_qt, T, past);
+        // the Q tile: its buffer is free once the softmax threads copied the previous Q
+        if (it > 0 && !mbar_wait(&bar->q_empty, (it - 1) & 1, st, abort_flag, 37)) break;
+        mbar_arrive_expect_tx(&bar->q_full, 3 * kAtom);
         for (int c = 0; c < 3; ++c)
-          tma_load_3d(smem + kKOff + (slot * 3 + c) * kAtom, &tmK, &bar->k_full[slot], 64 * c, j * 128, kv_row);
-        issued[slot]++;
+          tma_load_3d(smem + kQOff + c * kAtom, &tmQ, &bar->q_full, t.h * 192 + 64 * c, t.q0, t.b);
+        ++q_loads;
+        const int kv_row = t.b * 64 + t.h;
+        bool ok = true;
+        for (int j = 0; j < t.n_kv; ++j, ++gt) {
+          const int ks = gt & 1;
+          if (!mbar_wait(&bar->k_empty[ks], ((gt >> 1) & 1) ^ 1, st, abort_flag, 40)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bar->k_full[ks], 3 * kAtom);
+          for (int c = 0; c < 3; ++c)
+            tma_load_3d(smem + kKOff + (ks * 3 + c) * kAtom, &tmK, &bar->k_full[ks], 64 * c, j * 128, kv_row);
+          issued[ks]++;
+        }
+        if (!ok) break;
       }
-      mbar_wait(&bar->q_full, 0, st, nullptr, 41);
+      // no copy may still be in flight into shared memory
+      if (q_loads) mbar_wait(&bar->q_full, (q_loads - 1) & 1, st, nullptr, 41);
       for (int i = 0; i < 2; ++i)
         if (issued[i]) mbar_wait(&bar->k_full[i], (issued[i] - 1) & 1, st, nullptr, 41);
     }
@@ -136,39 +190,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- V producer ----
       tma_prefetch_desc(&tmV);
       int issued[2] = {0, 0};
-      for (int j = 0; j < n_kv; ++j) {
-        const int slot = j & 1;
-        if (!mbar_wait(&bar->v_empty[slot], ((j >> 1) & 1) ^ 1, st, abort_flag, 42)) break;
-        mbar_arrive_expect_tx(&bar->v_full[slot], 2 * kAtom);
-        for (int c = 0; c < 2; ++c)
-          tma_load_3d(smem + kVOff + (slot * 2 + c) * kAtom, &tmV, &bar->v_full[slot], 64 * c, j * 128, kv_row);
-        issued[slot]++;
+      int gt = 0;
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        int w;
+        if (!read_item(bar, it, w, st, abort_flag) || w < 0) break;
+        const Item t(w, n_qt, T, past);
+        const int kv_row = t.b * 64 + t.h;
+        for (int j = 0; j < t.n_kv; ++j, ++gt) {
+          const int vs = gt & 1;
+          if (!mbar_wait(&bar->v_empty[vs], ((gt >> 1) & 1) ^ 1, st, abort_flag, 42)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bar->v_full[vs], 2 * kAtom);
+          for (int c = 0; c < 2; ++c)
+            tma_load_3d(smem + kVOff + (vs * 2 + c) * kAtom, &tmV, &bar->v_full[vs], 64 * c, j * 128, kv_row);
+          issued[vs]++;
+        }
       }
       for (int i = 0; i < 2; ++i)
         if (issued[i]) mbar_wait(&bar->v_full[i], (issued[i] - 1) & 1, st, nullptr, 43);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---- S issuer: S_j = Q K_j^T into score buffer j & 1 ----
+      // ---- S issuer: S_j = Q K_j^T into score buffer gt & 1 ----
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       const uint32_t k_addr = smem_u32(smem + kKOff);
       const uint32_t q_tm = tmem + kTmQ;
-      bool ok = mbar_wait(&bar->q_tmem, 0, st, abort_flag, 44);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int slot = j & 1;
-        if (!mbar_wait(&bar->k_full[slot], (j >> 1) & 1, st, abort_flag, 45)) break;
-        // the buffer's previous P (tile j-2) has been read by its P.V
-        if (j > 1 && !mbar_wait(&bar->pv_done[slot], ((j - 2) >> 1) & 1, st, abort_flag, 46)) break;
-        tc_fence_after();
-        const uint32_t d = tmem + kTmS + slot * 128;
-        const uint32_t kb = k_addr + slot * 3 * kAtom;
+      int gt = 0;
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        int w;
+        if (!read_item(bar, it, w, st, abort_flag) || w < 0) break;
+        const Item t(w, n_qt, T, past);
+        if (!mbar_wait(&bar->q_tmem, it & 1, st, abort_flag, 44)) break;  // this item's Q in tensor memory
+        for (int j = 0; j < t.n_kv; ++j, ++gt) {
+          const int sb = gt & 1;
+          if (!mbar_wait(&bar->k_full[sb], (gt >> 1) & 1, st, abort_flag, 45)) {
+            ok = false;
+            break;
+          }
+          // the buffer's previous P (tile gt-2) has been read by its P.V
+          if (gt > 1 && !mbar_wait(&bar->pv_done[sb], ((gt - 2) >> 1) & 1, st, abort_flag, 46)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + kTmS + sb * 128;
+          const uint32_t kb = k_addr + sb * 3 * kAtom;
 #pragma unroll
-        for (int kk = 0; kk < 12; ++kk) {
-          const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-          umma_bf16_ts(d, q_tm + kk * 8, sdesc_sw128(kb + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 12; ++kk) {
+            const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+            umma_bf16_ts(d, q_tm + kk * 8, sdesc_sw128(kb + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&bar->s_full[sb]);
+          umma_commit(&bar->k_empty[sb]);
         }
-        umma_commit(&bar->s_full[slot]);
-        umma_commit(&bar->k_empty[slot]);
       }
       umma_commit(&bar->drain_s);
       mbar_wait(&bar->drain_s, 0, st, nullptr, 49);
@@ -178,20 +256,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- P.V issuer: O += P_j V_j ----
       constexpr uint32_t idesc_pv = idesc_bf16(128, 128, false, true);
       const uint32_t v_addr = smem_u32(smem + kVOff);
-      for (int j = 0; j < n_kv; ++j) {
-        const int slot = j & 1;
-        if (!mbar_wait(&bar->p_full[slot], (j >> 1) & 1, st, abort_flag, 47)) break;
-        if (!mbar_wait(&bar->v_full[slot], (j >> 1) & 1, st, abort_flag, 48)) break;
-        tc_fence_after();
-        const uint32_t vb = v_addr + slot * 2 * kAtom;
-        const uint32_t pa = tmem + kTmS + slot * 128;
+      int gt = 0;
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        int w;
+        if (!read_item(bar, it, w, st, abort_flag) || w < 0) break;
+        const Item t(w, n_qt, T, past);
+        for (int j = 0; j < t.n_kv; ++j, ++gt) {
+          const int sb = gt & 1;
+          if (!mbar_wait(&bar->p_full[sb], (gt >> 1) & 1, st, abort_flag, 47) ||
+              !mbar_wait(&bar->v_full[sb], (gt >> 1) & 1, st, abort_flag, 48) ||
+              // the first P.V of an item overwrites O: the previous item's epilogue has read it
+              (j == 0 && it > 0 && !mbar_wait(&bar->o_free, (it - 1) & 1, st, abort_flag, 55))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t vb = v_addr + sb * 2 * kAtom;
+          const uint32_t pa = tmem + kTmS + sb * 128;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, kAtom, 1024);
-          umma_bf16_ts(tmem + kTmO, pa + kk * 8, bdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, kAtom, 1024);
+            umma_bf16_ts(tmem + kTmO, pa + kk * 8, bdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&bar->pv_done[sb]);
+          umma_commit(&bar->v_empty[sb]);
         }
-        umma_commit(&bar->pv_done[slot]);
-        umma_commit(&bar->v_empty[slot]);
       }
       umma_commit(&bar->drain_pv);
       mbar_wait(&bar->drain_pv, 0, st, nullptr, 49);
@@ -200,86 +290,129 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- softmax / correction / epilogue: warps 2..5, one thread per query row ----
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const int qpos = q0 + row;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    float m = -INFINITY, l = 0.f;
-    bool ok = __all_sync(0xffffffffu, mbar_wait(&bar->q_full, 0, st, abort_flag, 54));
-    if (ok) {
-      // this row of Q (three 128-byte-swizzled 64-column atoms) into tensor
-      // memory as bf16 pairs, the A operand of every S_j
-      const uint8_t* qrow = smem + kQOff + row * 128;
-#pragma unroll
-      for (int c = 0; c < 3; ++c) {
-        uint32_t v[32];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint4 w = *reinterpret_cast<const uint4*>(qrow + c * kAtom + ((q ^ (row & 7)) << 4));
-          v[4 * q] = w.x;
-          v[4 * q + 1] = w.y;
-          v[4 * q + 2] = w.z;
-          v[4 * q + 3] = w.w;
-        }
-        tmem_st32(tmem + lane_addr + kTmQ + c * 32, v);
-      }
-      tmem_wait_st();
-    }
-    tc_fence_before();
-    mbar_arrive(&bar->q_tmem);
-    for (int j = 0; ok && j < n_kv; ++j) {
-      const int slot = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar->s_full[slot], (j >> 1) & 1, st, abort_flag, 50));
+    bool ok = true;
+    int gt = 0;
+    // the previous item, whose O is written out once the next item's Q is in place
+    int prev_qpos = -1, prev_h = 0, prev_b = 0, prev_last = -1;
+    float prev_l = 1.f;
+    for (int it = 0; ok; ++it) {
+      int w = -1;
+      ok = __all_sync(0xffffffffu, read_item(bar, it, w, st, abort_flag));
       if (!ok) break;
-      tc_fence_after();
-      uint32_t s[128];
-      {
-        uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
-        uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
-        uint32_t (&s2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[64]);
-        uint32_t (&s3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[96]);
-        const uint32_t ta = tmem + lane_addr + kTmS + slot * 128;
-        tmem_ld32(ta, s0);
-        tmem_ld32(ta + 32, s1);
-        tmem_ld32(ta + 64, s2);
-        tmem_ld32(ta + 96, s3);
-        tmem_wait_ld();
+      if (w >= 0) {
+        // this item's Q rows (three 128-byte-swizzled 64-column atoms) into
+        // tensor memory as bf16 pairs, the A operand of every S_j; the
+        // previous item's S are all done (its last s_full was consumed)
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar->q_full, it & 1, st, abort_flag, 54));
+        if (!ok) break;
+        const uint8_t* qrow = smem + kQOff + row * 128;
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+          uint32_t v[32];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint4 x = *reinterpret_cast<const uint4*>(qrow + c * kAtom + ((q ^ (row & 7)) << 4));
+            v[4 * q] = x.x;
+            v[4 * q + 1] = x.y;
+            v[4 * q + 2] = x.z;
+            v[4 * q + 3] = x.w;
+          }
+          tmem_st32(tmem + lane_addr + kTmQ + c * 32, v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar->q_tmem);
+        mbar_arrive(&bar->q_empty);
       }
-      const int k0 = j * 128;
-      // max of the raw scores (the scale is positive), causal mask (key k
-      // visible to query position past + qpos iff k <= past + qpos) on the
-      // tiles that reach beyond the tile's first query
-      if (k0 + 127 > past + q0) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (k0 + c > past + qpos) s[c] = __float_as_uint(-INFINITY);
-      }
-      // eight independent partial maxima / sums keep the reductions off a
-      // single serial dependency chain
-      float mp[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mp[i] = __uint_as_float(s[i]);
-#pragma unroll
-      for (int c = 8; c < 128; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(s[c]));
-      float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-      mx *= sl2;  // log2 units
-      const bool need = mx > m + kRescaleThreshold;
-      const float m_new = need ? mx : m;
-      const float alpha = need ? ex2_approx(m - m_new) : 1.f;
-      float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float p = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -m_new));
-        s[c] = __float_as_uint(p);
-        sp[c & 7] += p;
-      }
-      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-      l = l * alpha + sum;
-      m = m_new;
-      // O may be rescaled only after P.V of tile j-1 has completed
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, st, abort_flag, 53));
+      if (prev_last >= 0) {
+        // epilogue of the previous item: O / l once its last P.V is done
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&bar->pv_done[prev_last & 1], (prev_last >> 1) & 1, st, abort_flag, 52));
         if (!ok) break;
         tc_fence_after();
+        const float inv = 1.f / prev_l;
+        const uint32_t ta = tmem + lane_addr + kTmO;
+        __nv_bfloat16* dst = o + ((size_t)prev_b * T + prev_qpos) * 8192 + prev_h * 128;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(ta + c, r);
+          tmem_wait_ld();
+          if (prev_qpos < T) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              d4[q] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * q]) * inv, __uint_as_float(r[8 * q + 1]) * inv),
+                                 pack_bf16x2(__uint_as_float(r[8 * q + 2]) * inv, __uint_as_float(r[8 * q + 3]) * inv),
+                                 pack_bf16x2(__uint_as_float(r[8 * q + 4]) * inv, __uint_as_float(r[8 * q + 5]) * inv),
+                                 pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv, __uint_as_float(r[8 * q + 7]) * inv));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bar->o_free);
+        prev_last = -1;
+      }
+      if (w < 0) break;
+      const Item t(w, n_qt, T, past);
+      const int qpos = t.q0 + row;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < t.n_kv; ++j, ++gt) {
+        const int sb = gt & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar->s_full[sb], (gt >> 1) & 1, st, abort_flag, 50));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t s[128];
         {
+          uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
+          uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
+          uint32_t (&s2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[64]);
+          uint32_t (&s3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[96]);
+          const uint32_t ta = tmem + lane_addr + kTmS + sb * 128;
+          tmem_ld32(ta, s0);
+          tmem_ld32(ta + 32, s1);
+          tmem_ld32(ta + 64, s2);
+          tmem_ld32(ta + 96, s3);
+          tmem_wait_ld();
+        }
+        const int k0 = j * 128;
+        // max of the raw scores (the scale is positive), causal mask (key k
+        // visible to query position past + qpos iff k <= past + qpos) on the
+        // tiles that reach beyond the tile's first query
+        if (k0 + 127 > past + t.q0) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (k0 + c > past + qpos) s[c] = __float_as_uint(-INFINITY);
+        }
+        // eight independent partial maxima / sums keep the reductions off a
+        // single serial dependency chain
+        float mp[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mp[i] = __uint_as_float(s[i]);
+#pragma unroll
+        for (int c = 8; c < 128; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(s[c]));
+        float mx =
+            fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        mx *= sl2;  // log2 units
+        const bool need = mx > m + kRescaleThreshold;
+        const float m_new = need ? mx : m;
+        const float alpha = need ? ex2_approx(m - m_new) : 1.f;
+        float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const float p = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -m_new));
+          s[c] = __float_as_uint(p);
+          sp[c & 7] += p;
+        }
+        const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+        l = l * alpha + sum;
+        m = m_new;
+        // O may be rescaled only after P.V of tile j-1 has completed
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(&bar->pv_done[(gt - 1) & 1], ((gt - 1) >> 1) & 1, st, abort_flag, 53));
+          if (!ok) break;
+          tc_fence_after();
           const uint32_t ta = tmem + lane_addr + kTmO;
 #pragma unroll 1
           for (int c = 0; c < 128; c += 32) {
@@ -292,44 +425,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
-      }
-      // P_j (bf16 pairs, low half = even key) over the first 64 columns of
-      // score buffer j & 1 (S_j is entirely in registers by now)
-      {
-        uint32_t pk[64];
+        // P_j (bf16 pairs, low half = even key) over the first 64 columns of
+        // its score buffer (S_j is entirely in registers by now)
+        {
+          uint32_t pk[64];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) pk[c] = pack_bf16x2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
-        const uint32_t tp = tmem + lane_addr + kTmS + (j & 1) * 128;
+          for (int c = 0; c < 64; ++c) pk[c] = pack_bf16x2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
+          const uint32_t tp = tmem + lane_addr + kTmS + sb * 128;
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) tmem_st16(tp + c, &pk[c]);
-        tmem_wait_st();
-      }
-      tc_fence_before();
-      mbar_arrive(&bar->p_full[j & 1]);
-    }
-    if (ok)
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(&bar->pv_done[(n_kv - 1) & 1], ((n_kv - 1) >> 1) & 1, st, abort_flag, 52));
-    if (ok) {
-      tc_fence_after();
-      const float inv = 1.f / l;
-      const uint32_t ta = tmem + lane_addr + kTmO;
-      __nv_bfloat16* dst = o + ((size_t)b * T + qpos) * 8192 + h * 128;
-#pragma unroll 1
-      for (int c = 0; c < 128; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(ta + c, r);
-        tmem_wait_ld();
-        if (qpos < T) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            d4[q] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * q]) * inv, __uint_as_float(r[8 * q + 1]) * inv),
-                               pack_bf16x2(__uint_as_float(r[8 * q + 2]) * inv, __uint_as_float(r[8 * q + 3]) * inv),
-                               pack_bf16x2(__uint_as_float(r[8 * q + 4]) * inv, __uint_as_float(r[8 * q + 5]) * inv),
-                               pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv, __uint_as_float(r[8 * q + 7]) * inv));
+          for (int c = 0; c < 64; c += 16) tmem_st16(tp + c, &pk[c]);
+          tmem_wait_st();
         }
+        tc_fence_before();
+        mbar_arrive(&bar->p_full[sb]);
       }
+      prev_qpos = qpos;
+      prev_h = t.h;
+      prev_b = t.b;
+      prev_l = l;
+      prev_last = gt - 1;
     }
   }
 
@@ -340,12 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tmem, 512);
   }
 }
-
 }  // namespace
 
 cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, const DevStatusHost& st, int num_sms,
                                      cudaStream_t stream) {
-  (void)num_sms;
   CUtensorMap tq, tk, tv;
   const uint64_t n_keys = (uint64_t)a.past + a.T;  // key positions beyond read as zeros
   if (!make_tmap_bf16_3d(&tq, a.q, 12288, a.T, a.B, 12288ull * 2, (uint64_t)a.T * 12288 * 2, 64, 128) ||
@@ -359,10 +471,15 @@ cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, const DevStatusHo
     attr_set = true;
   }
   const int n_qt = (a.T + 127) / 128;
-  dim3 grid(n_qt, 64, a.B);
+  const long long items = (long long)n_qt * 64 * a.B;
+  if (items > INT32_MAX || !st.word) return cudaErrorInvalidValue;
+  const int n_items = (int)items;
+  const int grid = n_items < num_sms ? n_items : num_sms;
+  // the work counter: an int of the status region (cleared before every call)
+  int* work = reinterpret_cast<int*>(st.word) + kWorkCounterWord;
   DevStatus dst{st.word, st.wait_limit_ns};
-  return launch_pdl(prefill_attn_tc, grid, dim3(kThreads), kSmemBytes, stream, tq, tk, tv, a.o, a.T, n_qt,
-                    a.scale * 1.4426950408889634f, a.past, dst);
+  return launch_pdl(prefill_attn_tc, dim3(grid), dim3(kThreads), kSmemBytes, stream, tq, tk, tv, a.o, a.T, n_qt,
+                    n_items, a.scale * 1.4426950408889634f, a.past, work, dst);
 }
 
 }  // namespace mla

@@ -55,6 +55,10 @@ struct DevStatusHost {
   uint32_t* word;
   uint64_t wait_limit_ns;
 };
+// Words of the status region (256 bytes before the split-K counters, zeroed
+// before every call): 0 = the status word, kWorkCounterWord = the persistent
+// prefill attention's work counter.
+constexpr int kWorkCounterWord = 16;
 
 // ---- tensor maps ------------------------------------------------------------
 // 2D bf16 tensor map over a row-major [rows, cols] matrix with row stride
