@@ -359,6 +359,22 @@ class Runner:
             m.mla_prefill_chunk_latent(self.W, x, P0, out, ckv, kpe, ws, params=m.make_params(timing=timing))
         return step, (ckv, kpe, x, out, ws)
 
+    def chunk_absorbed_step_fn(self, B, P0, T, absorbed=True):
+        """T new tokens per sequence after P0 latent-cache positions, in the
+        absorbed form (one latent decode row per token) or, absorbed=False,
+        the rebuilt form on the same caches."""
+        torch, m, synth = self.torch, self.m, self.synth
+        ckv, kpe = self.fill_caches(B, P0, P0 + T, rebuilt=False)
+        x = synth.tensor_cuda(0, "x", (B, T, D), synth.X_DIST, device=self.dev)
+        out = torch.empty_like(x)
+        mode = m.MODE_CHUNK_ABSORBED if absorbed else m.MODE_CHUNK_LATENT
+        ws = m.alloc_workspace(mode, B, T, device=self.dev, cap=P0 + T)
+        fn = m.mla_prefill_chunk_absorbed if absorbed else m.mla_prefill_chunk_latent
+
+        def step(timing):
+            fn(self.W, x, P0, out, ckv, kpe, ws, params=m.make_params(timing=timing))
+        return step, (ckv, kpe, x, out, ws)
+
     # ---- decode -------------------------------------------------------------
     def fill_caches(self, B, P, cap, rebuilt, chunk_tokens=1 << 17):
         """Caches of positions 0..P-1 written by the library's own prefill
@@ -762,6 +778,31 @@ def main():
             torch.cuda.empty_cache()
         except Exception as e:
             line["prefill_chunk_latent"] = {"error": repr(e)[:300]}
+        # ---- absorbed chunk: 32 sequences, 4 new tokens after 8188 latent positions ---
+        try:
+            B8, P8, T8 = 32, 8188, 4
+            step8, keep = r.chunk_absorbed_step_fn(B8, P8, T8)
+            ms8, st8, l8 = r.time_steps(step8, ks, W, stages=LATENT_STAGES)
+            us = barrier_max(statistics.mean(ms8)) * 1e3
+            keys = B8 * sum(P8 + t + 1 for t in range(T8))
+            byts = keys * (KVL + ROPE) * 2 + WEIGHT_BYTES + 2 * B8 * T8 * D * 2
+            del step8, keep
+            torch.cuda.empty_cache()
+            step8r, keep = r.chunk_absorbed_step_fn(B8, P8, T8, absorbed=False)
+            ms8r, _, _ = r.time_steps(step8r, max(2, min(ks, 5)), 2, with_stages=False)
+            us_r = barrier_max(statistics.mean(ms8r)) * 1e3
+            del step8r, keep
+            torch.cuda.empty_cache()
+            line["prefill_chunk_absorbed"] = {
+                "workload": "mla_prefill_chunk_absorbed B=32 T=4 after P0=8188 latent-cache positions "
+                            "(one latent decode row per new token)",
+                "us_per_step": round(us, 2), "tokens_per_s": round(world * B8 * T8 / (us * 1e-6), 1),
+                "hbm_gbs": round(byts / (us * 1e-6) / 1e9, 1),
+                "frac_measured_hbm": round(byts / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
+                "algorithmic_bytes": byts, "stage_ms": _stages_out(st8), "launches": l8,
+                "rebuilt_form_us_per_step": round(us_r, 1)}
+        except Exception as e:
+            line["prefill_chunk_absorbed"] = {"error": repr(e)[:300]}
         # ---- the block's MLP half: 2048 rows (prefill) and 64 rows (decode) ---------
         l_ffn = 0
         try:

@@ -72,6 +72,7 @@ extern "C" {
 #define MLA_MODE_DECODE_LATENT 2
 #define MLA_MODE_FFN 3
 #define MLA_MODE_CHUNK_LATENT 4
+#define MLA_MODE_CHUNK_ABSORBED 5
 
 /* Weights of one MLA sublayer: device pointers to bf16, nn.Linear [out, in].
  * Key-value compression page, MLA __init__ excerpt, for the projections;
@@ -134,6 +135,10 @@ typedef struct {
  *                                  (mla_prefill_chunk_latent; the size grows
  *                                  with cap: it holds the rebuilt keys and
  *                                  values of every position, 40 KB each).
+ *   mode = MLA_MODE_CHUNK_ABSORBED: B sequences, chunks of T = t_or_p
+ *                                  tokens, latent caches of `cap` positions
+ *                                  (mla_prefill_chunk_absorbed; the size grows
+ *                                  with B * T only).
  * Returns 0 when the arguments are out of range. */
 size_t mla_workspace_size(int mode, int B, int t_or_p, int cap);
 
@@ -190,6 +195,24 @@ int mla_prefill_chunk(const mla_weights_t* w, const mla_params_t* params, const 
 int mla_prefill_chunk_latent(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int T,
                              int P0, void* out, void* ckv_cache, void* kpe_cache, int cap, void* workspace,
                              size_t workspace_bytes, void* stream);
+
+/* The same chunk in the absorbed form (latent-cache serving, "Key-value
+ * compression" page: W_UK folded into the query, W_UV applied after the
+ * attention, so the cached latent is never expanded).  Every new token
+ * (b, t) is one latent decode step at position P0 + t that attends to cache
+ * rows 0..P0+t of sequence b: scores q_lat . [k^R ; c^KV], o_lat = P c^KV,
+ * then W_UV and o_proj.  Results, arguments and errors as
+ * mla_prefill_chunk_latent; the chunk's latent rows are written first.
+ * Cost: the cache is read once per new token (B T (P0 + T) 1152 bytes)
+ * instead of rebuilding the keys and values of every cached position (a
+ * 16384 x 512 product per position), so it is the form for short chunks.
+ * Requires P0 >= 0, P0 + T <= cap; workspace
+ * mla_workspace_size(MLA_MODE_CHUNK_ABSORBED, B, T, cap).
+ * Errors: INVALID_ARG (null pointer, P0 < 0, P0 + T > cap), ALIGNMENT,
+ * WORKSPACE, CUDA. */
+int mla_prefill_chunk_absorbed(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int T,
+                               int P0, void* out, void* ckv_cache, void* kpe_cache, int cap, void* workspace,
+                               size_t workspace_bytes, void* stream);
 
 /* One decode step against the rebuilt per-head cache (the pinned
  * implementation's cache, "Mix and project" page at P = 1,000).

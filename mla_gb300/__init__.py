@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(_HERE, "libmla.so")
 
 D, HEADS, Q_LORA, KV_LORA, QK_NOPE, QK_ROPE, QK, V = 7168, 64, 1536, 512, 128, 64, 192, 128
 FFN_INTER = 18432
-MODE_PREFILL, MODE_DECODE, MODE_DECODE_LATENT, MODE_FFN, MODE_CHUNK_LATENT = 0, 1, 2, 3, 4
+MODE_PREFILL, MODE_DECODE, MODE_DECODE_LATENT, MODE_FFN, MODE_CHUNK_LATENT, MODE_CHUNK_ABSORBED = 0, 1, 2, 3, 4, 5
 STAGES = ["input_norm", "a_proj", "latent", "q_b", "kv_b", "attn", "combine", "absorb_q", "absorb_o", "o_proj",
           "ffn_norm", "gate_up", "down"]
 MAX_STAGES = len(STAGES)
@@ -77,6 +77,8 @@ _SIGS = {
                                _VP, _VP, _VP, _I, _VP, _SZ, _VP]),
     "mla_prefill_chunk_latent": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _I, _VP,
                                       _VP, _VP, _I, _VP, _SZ, _VP]),
+    "mla_prefill_chunk_absorbed": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _I,
+                                        _VP, _VP, _VP, _I, _VP, _SZ, _VP]),
     "mla_decode": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _VP, _VP, _I, _VP,
                         _VP, _SZ, _VP]),
     "mla_decode_latent": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _VP, _VP, _I,
@@ -208,6 +210,18 @@ def mla_prefill_chunk_latent(weights: MlaWeights, x, P0: int, out, ckv_cache, kp
                                         _ptr(x), B, T, P0, _ptr(out), _ptr(ckv_cache), _ptr(kpe_cache), cap,
                                         _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "mla_prefill_chunk_latent")
+
+
+def mla_prefill_chunk_absorbed(weights: MlaWeights, x, P0: int, out, ckv_cache, kpe_cache, workspace,
+                               params: MlaParams | None = None, stream=None):
+    """The same chunk as mla_prefill_chunk_latent in the absorbed form (one latent decode row per new
+    token); workspace of MODE_CHUNK_ABSORBED sized with the same B, T and cap."""
+    B, T = x.shape[0], x.shape[1]
+    cap = ckv_cache.shape[1]
+    rc = lib().mla_prefill_chunk_absorbed(ctypes.byref(weights), None if params is None else ctypes.byref(params),
+                                          _ptr(x), B, T, P0, _ptr(out), _ptr(ckv_cache), _ptr(kpe_cache), cap,
+                                          _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "mla_prefill_chunk_absorbed")
 
 
 def mla_decode(weights: MlaWeights, x, P: int, k_cache, v_cache, out, workspace,

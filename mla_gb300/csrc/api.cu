@@ -20,7 +20,7 @@ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 // Workspace carve-up.  Offsets are computed identically by the size query
 // and by the entry points.
 struct Layout {
-  size_t status, cs, xn, ca, cq, ckv, kpe, q, o, kscr, vscr, qlat, olat, part_o, part_ml, split, h, plan, total;
+  size_t status, cs, xn, ca, cq, ckv, kpe, q, o, kscr, vscr, qlat, olat, part_o, part_ml, split, h, plan, pos, total;
   size_t split_bytes;  // split-K partial slots (decode modes), 0 = none
 };
 
@@ -32,7 +32,9 @@ constexpr size_t kStatusRegion = 256 + kMaxSplitCounters * sizeof(int);
 Layout make_layout(int mode, int B, int t_or_p, int num_sms, int cap = 0) {
   Layout L{};
   const bool pre = mode == MLA_MODE_PREFILL || mode == MLA_MODE_CHUNK_LATENT;
-  const size_t n = pre ? (size_t)B * t_or_p : (size_t)B;
+  // absorbed chunk: one latent decode row per (sequence, new token)
+  const bool absorbed = mode == MLA_MODE_CHUNK_ABSORBED;
+  const size_t n = (pre || absorbed) ? (size_t)B * t_or_p : (size_t)B;
   const size_t npos = pre ? (size_t)t_or_p : 1;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -75,15 +77,19 @@ Layout make_layout(int mode, int B, int t_or_p, int num_sms, int cap = 0) {
     L.part_o = take((size_t)B * MLA_HEADS * s * MLA_V * sizeof(float));
     L.part_ml = take((size_t)B * MLA_HEADS * s * sizeof(float2));
   } else {
-    const int g = latent_ctas(B, t_or_p + 1, num_sms);
-    L.qlat = take((size_t)B * MLA_HEADS * 576 * 2);
-    L.olat = take((size_t)B * MLA_HEADS * MLA_KV_LORA * 2);
+    // latent rows and the keys of the longest one (absorbed chunk: at most cap)
+    const int rows = (int)n;
+    const int keys = absorbed ? cap : t_or_p + 1;
+    const int g = latent_ctas(rows, keys, num_sms);
+    L.qlat = take(n * MLA_HEADS * 576 * 2);
+    L.olat = take(n * MLA_HEADS * MLA_KV_LORA * 2);
     L.part_o = take((size_t)2 * g * MLA_HEADS * MLA_KV_LORA * sizeof(float));
     L.part_ml = take((size_t)2 * g * MLA_HEADS * sizeof(float2));
-    L.plan = take(latent_plan_ints(B, g) * sizeof(int));
+    L.plan = take(latent_plan_ints(rows, g) * sizeof(int));
+    if (absorbed) L.pos = take(n * sizeof(int));
   }
   if (!pre) {
-    L.split_bytes = split_part_bytes(B);
+    L.split_bytes = split_part_bytes((int)n);
     L.split = take(L.split_bytes);
   }
   L.total = off;
@@ -355,6 +361,8 @@ size_t mla_workspace_size(int mode, int B, int t_or_p, int cap) {
     if (t_or_p < 0 || B > kMaxTokens || t_or_p >= (1 << 24)) return 0;
   } else if (mode == MLA_MODE_FFN) {
     if (t_or_p < 1 || (int64_t)B * t_or_p > kMaxTokens) return 0;
+  } else if (mode == MLA_MODE_CHUNK_ABSORBED) {
+    if (t_or_p < 1 || (int64_t)B * t_or_p > kMaxTokens || cap < t_or_p || cap >= (1 << 24)) return 0;
   } else {
     return 0;
   }
@@ -563,6 +571,80 @@ int decode_impl(const mla_weights_t* w, const mla_params_t* params, const void* 
 }
 
 // One decode step, latent cache; pos as decode_impl.
+// W_UK absorption, latent attention, W_UV and o_proj for n latent rows whose
+// RoPE'd queries front_end has written: row i attends to keys 0..pos[i] (or
+// 0..P_max without pos) of cache plane i / kv_div.
+int latent_tail(const mla_weights_t* w, const Params& p, const void* x, void* out, int n, int P_max, const int* pos,
+                int kv_div, const __nv_bfloat16* ckv_cache, const __nv_bfloat16* kpe_cache, int cap, void* workspace,
+                const Layout& L, const DevStatusHost& st, int sms, cudaStream_t stream_, Stager& sg, int* launches,
+                bool qpe_in_epilogue) {
+  const __nv_bfloat16* wkvb = static_cast<const __nv_bfloat16*>(w->w_kv_b);
+  sg.start(MLA_STAGE_ABSORB_Q);
+  {
+    // q_lat[i, h, 0:512] = sum_j q_nope[i, h, j] W_kv_b[h*256 + j, :]  (B operand [K=j, N=c], N contiguous)
+    GemmShape s{n, MLA_KV_LORA, MLA_QK_NOPE, MLA_HEADS, 0, MLA_QK, 0, 256, MLA_KV_LORA};
+    GemmOperands op{at<__nv_bfloat16>(workspace, L.q), MLA_HEADS * MLA_QK, n, wkvb, MLA_KV_LORA, MLA_HEADS * 256,
+                    nullptr, 0, 0, true};
+    EpiArgs ea{};
+    ea.out = at<__nv_bfloat16>(workspace, L.qlat);
+    ea.ldo = MLA_HEADS * 576;
+    ea.c_col0 = 0;
+    ea.c_col_step = 576;
+    set_split(ea, workspace, L);
+    MLA_TRY(launch_gemm(s, op, Epi::kStoreBf16, ea, st, sms, stream_));
+    *launches += 1;
+    if (!qpe_in_epilogue) {
+      MLA_TRY(launch_copy_qpe(at<__nv_bfloat16>(workspace, L.q), at<__nv_bfloat16>(workspace, L.qlat), n, stream_));
+      *launches += 1;
+    }
+  }
+  sg.stop(MLA_STAGE_ABSORB_Q);
+
+  sg.start(MLA_STAGE_ATTN);
+  {
+    LatentAttnArgs a{};
+    a.qlat = at<__nv_bfloat16>(workspace, L.qlat);
+    a.ckv = ckv_cache;
+    a.kpe = kpe_cache;
+    a.olat = at<__nv_bfloat16>(workspace, L.olat);
+    a.part_o = at<float>(workspace, L.part_o);
+    a.part_ml = at<float2>(workspace, L.part_ml);
+    a.B = n;
+    a.L = P_max + 1;
+    a.cap = cap;
+    a.ctas = latent_ctas(n, P_max + 1, sms);
+    a.scale = p.scale;
+    a.pos = pos;
+    a.plan = at<int>(workspace, L.plan);
+    a.kv_div = kv_div;
+    if (launch_latent_attention(a, st, stream_, launches) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  sg.stop(MLA_STAGE_ATTN);
+
+  sg.start(MLA_STAGE_ABSORB_O);
+  {
+    // o[i, h*128 + d] = sum_c o_lat[i, h, c] W_kv_b[h*256 + 128 + d, c]
+    GemmShape s{n, MLA_V, MLA_KV_LORA, MLA_HEADS, 0, MLA_KV_LORA, 128, 256, MLA_V};
+    GemmOperands op{at<__nv_bfloat16>(workspace, L.olat), MLA_HEADS * MLA_KV_LORA, n, wkvb, MLA_KV_LORA,
+                    MLA_HEADS * 256, nullptr, 0, 0, false};
+    EpiArgs ea{};
+    ea.out = at<__nv_bfloat16>(workspace, L.o);
+    ea.ldo = MLA_HEADS * MLA_V;
+    ea.c_col0 = 0;
+    ea.c_col_step = MLA_V;
+    set_split(ea, workspace, L);
+    MLA_TRY(launch_gemm(s, op, Epi::kStoreBf16, ea, st, sms, stream_));
+    *launches += 1;
+  }
+  sg.stop(MLA_STAGE_ABSORB_O);
+
+  sg.start(MLA_STAGE_O_PROJ);
+  int rc = o_proj_stage(w, p, x, out, n, workspace, L, st, sms, stream_, launches);
+  if (rc) return rc;
+  sg.stop(MLA_STAGE_O_PROJ);
+  return MLA_OK;
+}
+
 int decode_latent_impl(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int P,
                        const int* pos, void* ckv_cache, void* kpe_cache, int cap, void* out, void* workspace,
                        size_t workspace_bytes, void* stream) {
@@ -590,70 +672,50 @@ int decode_latent_impl(const mla_weights_t* w, const mla_params_t* params, const
                  static_cast<__nv_bfloat16*>(kpe_cache), cap, workspace, L, st, sms, stream_, sg, &launches, true,
                  pos, P, nullptr, qpe_in_epilogue ? at<__nv_bfloat16>(workspace, L.qlat) : nullptr);
   if (rc) return rc;
-
-  const __nv_bfloat16* wkvb = static_cast<const __nv_bfloat16*>(w->w_kv_b);
-  sg.start(MLA_STAGE_ABSORB_Q);
-  {
-    // q_lat[b, h, 0:512] = sum_i q_nope[b, h, i] W_kv_b[h*256 + i, :]  (B operand [K=i, N=c], N contiguous)
-    GemmShape s{B, MLA_KV_LORA, MLA_QK_NOPE, MLA_HEADS, 0, MLA_QK, 0, 256, MLA_KV_LORA};
-    GemmOperands op{at<__nv_bfloat16>(workspace, L.q), MLA_HEADS * MLA_QK, B, wkvb, MLA_KV_LORA, MLA_HEADS * 256,
-                    nullptr, 0, 0, true};
-    EpiArgs ea{};
-    ea.out = at<__nv_bfloat16>(workspace, L.qlat);
-    ea.ldo = MLA_HEADS * 576;
-    ea.c_col0 = 0;
-    ea.c_col_step = 576;
-    set_split(ea, workspace, L);
-    MLA_TRY(launch_gemm(s, op, Epi::kStoreBf16, ea, st, sms, stream_));
-    launches += 1;
-    if (!qpe_in_epilogue) {
-      MLA_TRY(launch_copy_qpe(at<__nv_bfloat16>(workspace, L.q), at<__nv_bfloat16>(workspace, L.qlat), B, stream_));
-      launches += 1;
-    }
-  }
-  sg.stop(MLA_STAGE_ABSORB_Q);
-
-  sg.start(MLA_STAGE_ATTN);
-  {
-    LatentAttnArgs a{};
-    a.qlat = at<__nv_bfloat16>(workspace, L.qlat);
-    a.ckv = static_cast<const __nv_bfloat16*>(ckv_cache);
-    a.kpe = static_cast<const __nv_bfloat16*>(kpe_cache);
-    a.olat = at<__nv_bfloat16>(workspace, L.olat);
-    a.part_o = at<float>(workspace, L.part_o);
-    a.part_ml = at<float2>(workspace, L.part_ml);
-    a.B = B;
-    a.L = P + 1;
-    a.cap = cap;
-    a.ctas = latent_ctas(B, P + 1, sms);
-    a.scale = p.scale;
-    a.pos = pos;
-    a.plan = at<int>(workspace, L.plan);
-    if (launch_latent_attention(a, st, stream_, &launches) != cudaSuccess) return MLA_ERR_CUDA;
-  }
-  sg.stop(MLA_STAGE_ATTN);
-
-  sg.start(MLA_STAGE_ABSORB_O);
-  {
-    // o[b, h*128 + d] = sum_c o_lat[b, h, c] W_kv_b[h*256 + 128 + d, c]
-    GemmShape s{B, MLA_V, MLA_KV_LORA, MLA_HEADS, 0, MLA_KV_LORA, 128, 256, MLA_V};
-    GemmOperands op{at<__nv_bfloat16>(workspace, L.olat), MLA_HEADS * MLA_KV_LORA, B, wkvb, MLA_KV_LORA,
-                    MLA_HEADS * 256, nullptr, 0, 0, false};
-    EpiArgs ea{};
-    ea.out = at<__nv_bfloat16>(workspace, L.o);
-    ea.ldo = MLA_HEADS * MLA_V;
-    ea.c_col0 = 0;
-    ea.c_col_step = MLA_V;
-    set_split(ea, workspace, L);
-    MLA_TRY(launch_gemm(s, op, Epi::kStoreBf16, ea, st, sms, stream_));
-    launches += 1;
-  }
-  sg.stop(MLA_STAGE_ABSORB_O);
-
-  sg.start(MLA_STAGE_O_PROJ);
-  rc = o_proj_stage(w, p, x, out, B, workspace, L, st, sms, stream_, &launches);
+  rc = latent_tail(w, p, x, out, B, P, pos, 1, static_cast<const __nv_bfloat16*>(ckv_cache),
+                   static_cast<const __nv_bfloat16*>(kpe_cache), cap, workspace, L, st, sms, stream_, sg, &launches,
+                   qpe_in_epilogue);
   if (rc) return rc;
-  sg.stop(MLA_STAGE_O_PROJ);
+  if (p.timing) p.timing->n_launches = launches;
+  return MLA_OK;
+}
+
+// Absorbed chunked prefill: the chunk's B*T tokens through the front end as
+// a chunk (RoPE positions and latent cache rows P0 + t), then one latent
+// decode row per token, row b*T + t reading plane b up to position P0 + t.
+int chunk_absorbed_impl(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int T, int P0,
+                        void* out, void* ckv_cache, void* kpe_cache, int cap, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  const Params p = resolve(params);
+  if (B < 1 || T < 1 || (int64_t)B * T > kMaxTokens || P0 < 0 || cap >= (1 << 24) || (int64_t)P0 + T > cap)
+    return MLA_ERR_INVALID_ARG;
+  if (!ckv_cache || !kpe_cache) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(ckv_cache) || !aligned16(kpe_cache)) return MLA_ERR_ALIGNMENT;
+  const int n = B * T;
+  int rc = common_checks(w, p, x, out, (size_t)n, workspace, workspace_bytes,
+                         make_layout(MLA_MODE_CHUNK_ABSORBED, B, T, kMaxSmsForSizing, cap).total);
+  if (rc) return rc;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return MLA_ERR_CUDA;
+  const Layout L = make_layout(MLA_MODE_CHUNK_ABSORBED, B, T, sms, cap);
+
+  cudaStream_t stream_ = static_cast<cudaStream_t>(stream);
+  const DevStatusHost st{at<uint32_t>(workspace, L.status), kDefaultWaitLimitNs};
+  Stager sg{p.timing, stream_};
+  int launches = 0;
+  if (cudaMemsetAsync(st.word, 0, kStatusRegion, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+  int* pos = at<int>(workspace, L.pos);
+  MLA_TRY(launch_chunk_positions(pos, n, T, P0, stream_));
+  launches += 1;
+  const bool qpe_in_epilogue = n <= 128;
+  rc = front_end(w, p, x, n, T, P0, T, P0, static_cast<__nv_bfloat16*>(ckv_cache),
+                 static_cast<__nv_bfloat16*>(kpe_cache), cap, workspace, L, st, sms, stream_, sg, &launches, true,
+                 nullptr, 0, nullptr, qpe_in_epilogue ? at<__nv_bfloat16>(workspace, L.qlat) : nullptr);
+  if (rc) return rc;
+  rc = latent_tail(w, p, x, out, n, P0 + T - 1, pos, T, static_cast<const __nv_bfloat16*>(ckv_cache),
+                   static_cast<const __nv_bfloat16*>(kpe_cache), cap, workspace, L, st, sms, stream_, sg, &launches,
+                   qpe_in_epilogue);
+  if (rc) return rc;
   if (p.timing) p.timing->n_launches = launches;
   return MLA_OK;
 }
@@ -713,6 +775,14 @@ int mla_decode_latent_varlen(const mla_weights_t* w, const mla_params_t* params,
   if (!P) return MLA_ERR_INVALID_ARG;
   return decode_latent_impl(w, params, x, B, P_max, P, ckv_cache, kpe_cache, cap, out, workspace, workspace_bytes,
                             stream);
+}
+
+int mla_prefill_chunk_absorbed(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int T,
+                               int P0, void* out, void* ckv_cache, void* kpe_cache, int cap, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (!out) return MLA_ERR_INVALID_ARG;
+  return chunk_absorbed_impl(w, params, x, B, T, P0, out, ckv_cache, kpe_cache, cap, workspace, workspace_bytes,
+                             stream);
 }
 
 int mla_ffn(const mla_ffn_weights_t* w, const mla_params_t* params, const void* x, int n_tok, void* out,

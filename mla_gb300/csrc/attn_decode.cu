@@ -404,15 +404,16 @@ __global__ void __launch_bounds__(kLatThreads, 1)
         const int stg = i & 1;
         const uint32_t eph = ((i >> 1) & 1) ^ 1;
         const int k0 = t * kLatTile;
+        const int plane = a.kv_div == 1 ? b : b / a.kv_div;  // the cache plane this sequence reads
         uint8_t* cbase = smem + kLatCOff + stg * 9 * kLatBox;
         // the rotary box first: it frees earliest and S starts with it
         if (!mbar_wait(&bar->kpe_empty[stg], eph, st, abort_flag, 61)) break;
         mbar_arrive_expect_tx(&bar->kpe_full[stg], kLatBox);
-        tma_load_3d(cbase + 8 * kLatBox, &tmR, &bar->kpe_full[stg], 0, k0, b);
+        tma_load_3d(cbase + 8 * kLatBox, &tmR, &bar->kpe_full[stg], 0, k0, plane);
         kpe_used[stg]++;
         if (!mbar_wait(&bar->ckv_empty[stg], eph, st, abort_flag, 62)) break;
         mbar_arrive_expect_tx(&bar->ckv_full[stg], 8 * kLatBox);
-        for (int c = 0; c < 8; ++c) tma_load_3d(cbase + c * kLatBox, &tmC, &bar->ckv_full[stg], 64 * c, k0, b);
+        for (int c = 0; c < 8; ++c) tma_load_3d(cbase + c * kLatBox, &tmC, &bar->ckv_full[stg], 64 * c, k0, plane);
         ckv_used[stg]++;
         if (i == 0 || t == 0) {
           // a new segment: reload q_lat once every S of the previous one is done
@@ -809,9 +810,11 @@ int latent_ctas(int B, int L, int num_sms) {
 cudaError_t launch_latent_attention(const LatentAttnArgs& a, const DevStatusHost& st, cudaStream_t stream,
                                     int* launches) {
   CUtensorMap tq, tc, tr;
+  if (a.kv_div < 1 || a.B % a.kv_div) return cudaErrorInvalidValue;
+  const uint64_t planes = (uint64_t)(a.B / a.kv_div);
   if (!make_tmap_bf16_2d(&tq, a.qlat, (uint64_t)a.B * 64, 576, 576, 64, 64) ||
-      !make_tmap_bf16_3d(&tc, a.ckv, 512, a.L, a.B, 1024, (uint64_t)a.cap * 1024, 64, 64) ||
-      !make_tmap_bf16_3d(&tr, a.kpe, 64, a.L, a.B, 128, (uint64_t)a.cap * 128, 64, 64))
+      !make_tmap_bf16_3d(&tc, a.ckv, 512, a.L, planes, 1024, (uint64_t)a.cap * 1024, 64, 64) ||
+      !make_tmap_bf16_3d(&tr, a.kpe, 64, a.L, planes, 128, (uint64_t)a.cap * 128, 64, 64))
     return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {

@@ -261,6 +261,9 @@ struct LatentAttnArgs {
   // and the work plan that latent_plan_kernel writes (null: every sequence L keys)
   const int* pos;
   int* plan;                  // [latent_plan_ints(B, ctas)] workspace, written by the launch
+  // sequences per cache plane: sequence b reads plane b / kv_div of the
+  // caches (absorbed chunked prefill: each new token is a sequence of its own)
+  int kv_div = 1;
 };
 int latent_ctas(int B, int L, int num_sms);
 // Work plan of the latent decode for per-sequence lengths: plan[0..B] =
@@ -270,6 +273,9 @@ int latent_ctas(int B, int L, int num_sms);
 inline size_t latent_plan_ints(int B, int ctas) { return (size_t)B + 1 + 3 * (size_t)ctas; }
 cudaError_t launch_latent_attention(const LatentAttnArgs& a, const DevStatusHost& st, cudaStream_t stream,
                                     int* launches);
+// pos[i] = p0 + i % t for i < n (the positions of a chunk's tokens, row-major
+// over (sequence, token)).
+cudaError_t launch_chunk_positions(int* pos, int n, int t, int p0, cudaStream_t stream);
 
 // qlat[b, h, 512:576] = q[b, h*192 + 128 : h*192 + 192]
 cudaError_t launch_copy_qpe(const __nv_bfloat16* q, __nv_bfloat16* qlat, int B, cudaStream_t stream);

@@ -166,7 +166,21 @@ __global__ void copy_qpe_kernel(const __nv_bfloat16* __restrict__ q, __nv_bfloat
   d[c] = s[c];
 }
 
+// pos[i] = p0 + i % t: the position of each token of a chunk (rows ordered
+// by sequence, then token)
+__global__ void chunk_positions_kernel(int* __restrict__ pos, int n, int t, int p0) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous call may still read the array
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) pos[i] = p0 + i % t;
+}
+
 }  // namespace
+
+cudaError_t launch_chunk_positions(int* pos, int n, int t, int p0, cudaStream_t stream) {
+  if (n < 1 || t < 1) return cudaErrorInvalidValue;
+  return launch_pdl(chunk_positions_kernel, dim3((n + 255) / 256), dim3(256), 0, stream, pos, n, t, p0);
+}
 
 cudaError_t launch_rmsnorm_rows(const __nv_bfloat16* x, const __nv_bfloat16* g, __nv_bfloat16* y, int rows,
                                 float eps, cudaStream_t stream) {

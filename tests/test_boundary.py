@@ -172,6 +172,32 @@ def test_prefill_chunk_latent_argument_checks():
     assert call(nbytes=ws_bytes - 256) == -3
 
 
+def test_prefill_chunk_absorbed_argument_checks():
+    w = fake_weights()
+    cap = 64
+    ws_bytes = m.lib().mla_workspace_size(m.MODE_CHUNK_ABSORBED, 2, 4, cap)
+    assert ws_bytes > 0
+    # one latent decode row per new token: the same bytes as a latent decode of B * T rows, plus positions
+    assert ws_bytes >= m.lib().mla_workspace_size(m.MODE_DECODE_LATENT, 8, cap - 1, 0)
+    # no rebuilt keys and values: much smaller than the rebuilt form's workspace at a long cache
+    assert m.lib().mla_workspace_size(m.MODE_CHUNK_ABSORBED, 2, 4, 8192) < \
+        m.lib().mla_workspace_size(m.MODE_CHUNK_LATENT, 2, 4, 8192) // 4
+    assert m.lib().mla_workspace_size(m.MODE_CHUNK_ABSORBED, 2, 4, 3) == 0   # cap < T
+    assert m.lib().mla_workspace_size(m.MODE_CHUNK_ABSORBED, 2, 0, cap) == 0  # T < 1
+
+    def call(P0=8, T=4, out=FAKE + (2 << 30), ckv=FAKE + (4 << 30), kpe=FAKE + (5 << 30), nbytes=ws_bytes):
+        return m.lib().mla_prefill_chunk_absorbed(ctypes.byref(w), None, FAKE + (1 << 30), 2, T, P0, out, ckv, kpe,
+                                                  cap, FAKE + (3 << 30), nbytes, None)
+    assert call(P0=-1) == -1
+    assert call(P0=61) == -1           # P0 + T > cap
+    assert call(T=0) == -1
+    assert call(ckv=None) == -1
+    assert call(kpe=None) == -1
+    assert call(out=None) == -1
+    assert call(ckv=FAKE + (4 << 30) + 8) == -2
+    assert call(nbytes=ws_bytes - 256) == -3
+
+
 def test_fp8_entry_argument_checks():
     lib = m.lib()
     # quantizer: cols must be a multiple of 128, pointers 16-byte aligned (scales 4-byte)

@@ -11,6 +11,8 @@ times, on sampled outputs the oracle can compute one by one.
   'cache_x' tokens (checked against the oracle's caches for the sampled
   sequences), then the sampled sequences' cache rows are replaced by the
   oracle's bf16 caches so both sides decode from identical inputs.
+* the absorbed chunk B=32, T=4 after P0=8188 latent positions (the bench's
+  size), caches as for the decodes, sampled sequences.
 Tolerance as in test_parity_small (max abs <= 2e-2, rel. Frobenius <= 1e-2;
 cache entries one bf16 ulp more, the bf16 output half an ulp more).
 """
@@ -213,6 +215,40 @@ def test_decode_latent_b128_p8192(W):
         parity(cuda_to_f64(delta[b:b + 1]), ref["delta"], f"latent decode delta b={b}")
         parity_cache(cuda_to_f64(ckv[b:b + 1, P]), ref["ckv_new"], f"new latent row b={b}")
         parity_cache(cuda_to_f64(kpe[b:b + 1, P]), ref["kpe_new"], f"new rotary-key row b={b}")
+
+
+def test_prefill_chunk_absorbed_b32_p8188_t4(W):
+    """The absorbed chunk at the bench's size: 32 sequences, 4 new tokens
+    after 8188 latent-cache positions.  The GPU prefill fills every cache
+    (checked against the oracle for the sampled sequences, whose rows are
+    then replaced by the oracle's bits); sampled sequences' outputs and new
+    cache rows against the oracle's latent chunk."""
+    import torch
+    B, P0, T = 32, 8188, 4
+    cap = P0 + T
+    ckv, kpe = _fill_caches(W, B, P0, cap, rebuilt=False)
+    samples = [0, 31]
+    refs = {}
+    for b in samples:
+        xc = synth.bf16_bits_to_f64(synth.tensor_bits(0, "cache_x", (B, P0, D), synth.X_DIST, rows=[b]))
+        c = om.cache_from_tokens(W[2], xc)
+        parity_cache(cuda_to_f64(ckv[b, :P0]), c["ckv"][0], f"GPU-filled latent cache b={b}")
+        Cb, Rb = f64_to_bits(c["ckv"][0]), f64_to_bits(c["kpe"][0])
+        ckv[b, :P0].copy_(bits_to_cuda(Cb))
+        kpe[b, :P0].copy_(bits_to_cuda(Rb))
+        refs[b] = (synth.bf16_bits_to_f64(Cb)[None], synth.bf16_bits_to_f64(Rb)[None])
+    x = synth.tensor_cuda(0, "x", (B, T, D), synth.X_DIST)
+    out = torch.empty_like(x)
+    ws = m.alloc_workspace(m.MODE_CHUNK_ABSORBED, B, T, cap=cap)
+    m.mla_prefill_chunk_absorbed(W[1], x, P0, out, ckv, kpe, ws)
+    torch.cuda.synchronize()
+    assert m.mla_device_status(ws) == 0
+    xb = synth.bf16_bits_to_f64(synth.tensor_bits(0, "x", (B, T, D), synth.X_DIST))
+    for b in samples:
+        ref = om.prefill_with_past_latent(W[2], xb[b:b + 1], *refs[b])
+        parity_out(cuda_to_f64(out[b:b + 1]), ref["out"], f"absorbed chunk out b={b}")
+        parity_cache(cuda_to_f64(ckv[b:b + 1, P0:]), ref["ckv"], f"absorbed chunk latent rows b={b}")
+        parity_cache(cuda_to_f64(kpe[b:b + 1, P0:]), ref["kpe"], f"absorbed chunk rotary-key rows b={b}")
 
 
 def test_decode_latent_varlen_b128_pmax8192(W):

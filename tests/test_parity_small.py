@@ -246,6 +246,59 @@ def test_prefill_chunk_latent_parity(W, B, P0, T):
     assert torch.count_nonzero(ckv[:, P0 + T:]).item() == 0
 
 
+@pytest.mark.parametrize("B,P0,T", [(2, 100, 3), (1, 128, 1), (2, 0, 40), (3, 300, 5), (1, 63, 130)])
+def test_prefill_chunk_absorbed_parity(W, B, P0, T):
+    """The absorbed form of the latent chunk (W_UK into the query, W_UV
+    after the attention, the cache never expanded) against the same oracle
+    as the rebuilt form: the two compute the same values.  Rows past the
+    chunk hold noise that must not be read."""
+    import torch
+    cap = P0 + T + 70
+    (_, _, Cb, Rb), (_, _, C64, R64) = make_caches(W, B, P0, cap)
+    noise = synth.tensor_bits(3, "cache_x", (B, cap, 576), (0.0, 4.0))
+    Cb[:, P0 + T:] = noise[:, P0 + T:, :512]
+    Rb[:, P0 + T:] = noise[:, P0 + T:, 512:]
+    xb = synth.tensor_bits(0, "x", (B, T, 7168), synth.X_DIST)
+    x = bits_to_cuda(xb)
+    ckv, kpe = bits_to_cuda(Cb), bits_to_cuda(Rb)
+    out = torch.empty_like(x)
+    delta = torch.empty((B, T, 7168), dtype=torch.float32, device="cuda")
+    wsp = m.alloc_workspace(m.MODE_CHUNK_ABSORBED, B, T, cap=cap)
+    m.mla_prefill_chunk_absorbed(W[1], x, P0, out, ckv, kpe, wsp, m.make_params(delta_out=delta))
+    torch.cuda.synchronize()
+    assert m.mla_device_status(wsp) == 0
+    ref = om.prefill_with_past_latent(W[2], synth.bf16_bits_to_f64(xb), C64[:, :P0], R64[:, :P0])
+    parity(cuda_to_f64(delta), ref["delta"], "delta")
+    parity_out(cuda_to_f64(out), ref["out"], "out")
+    parity_cache(cuda_to_f64(ckv[:, P0:P0 + T]), ref["ckv"], "new latent rows")
+    parity_cache(cuda_to_f64(kpe[:, P0:P0 + T]), ref["kpe"], "new rotary-key rows")
+    bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(bits(ckv[:, :P0]), Cb[:, :P0])
+    assert np.array_equal(bits(ckv[:, P0 + T:]), Cb[:, P0 + T:])
+
+
+def test_prefill_chunk_absorbed_matches_rebuilt_form(W):
+    """Same chunk through both latent-cache forms on the GPU: outputs and the
+    cache rows written agree to rounding (the absorbed form's A-projection
+    runs split-K, the rebuilt form's does not, so the fp32 sums are added in
+    a different order)."""
+    import torch
+    B, P0, T = 2, 200, 4
+    cap = P0 + T
+    (_, _, Cb, Rb), _ = make_caches(W, B, P0, cap)
+    xb = synth.tensor_bits(0, "x", (B, T, 7168), synth.X_DIST)
+    x = bits_to_cuda(xb)
+    c1, r1 = bits_to_cuda(Cb), bits_to_cuda(Rb)
+    c2, r2 = c1.clone(), r1.clone()
+    o1, o2 = torch.empty_like(x), torch.empty_like(x)
+    m.mla_prefill_chunk_latent(W[1], x, P0, o1, c1, r1, m.alloc_workspace(m.MODE_CHUNK_LATENT, B, T, cap=cap))
+    m.mla_prefill_chunk_absorbed(W[1], x, P0, o2, c2, r2, m.alloc_workspace(m.MODE_CHUNK_ABSORBED, B, T, cap=cap))
+    torch.cuda.synchronize()
+    parity_cache(cuda_to_f64(c2), cuda_to_f64(c1), "latent rows")
+    parity_cache(cuda_to_f64(r2), cuda_to_f64(r1), "rotary-key rows")
+    parity_out(cuda_to_f64(o2), cuda_to_f64(o1), "absorbed against rebuilt")
+
+
 def test_latent_prefill_then_latent_chunk_equals_whole_prefill(W):
     """GPU prefill writes the latent cache of the first T1 tokens, a GPU
     latent chunk runs the next T2: every output row matches the oracle's
