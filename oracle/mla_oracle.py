@@ -356,6 +356,47 @@ def decode_latent_absorbed(w: dict, x_new: np.ndarray, ckv_cache: np.ndarray,
     return {"out": x_new + delta, "delta": delta}
 
 
+def fold_wuv_into_wo(w: dict, dims: Dims = KIMI_K2) -> np.ndarray:
+    """W_UV folded into the output projection (the latent-serving design of
+    the key-value compression page carried one step further): head h's value
+    up-projection W_UV[h] [v, kv_lora] and its columns of W_o [d, v] make one
+    [d, kv_lora] block, W_fold[:, h*kv_lora:(h+1)*kv_lora] = W_o[:, h*v:(h+1)*v] W_UV[h],
+    so the sublayer's output is o_lat (all heads' latent attention outputs,
+    [H*kv_lora]) times W_fold^T."""
+    wkvb = w["w_kv_b"].reshape(dims.H, dims.nope + dims.v, dims.kv_lora)
+    w_uv = wkvb[:, dims.nope:]                                   # [H, v, kv_lora]
+    w_o = w["w_o"].reshape(dims.d, dims.H, dims.v)               # [d, H, v]
+    return np.concatenate([w_o[:, h] @ w_uv[h] for h in range(dims.H)], axis=1)
+
+
+def decode_latent_folded(w: dict, w_fold: np.ndarray, x_new: np.ndarray, ckv_cache: np.ndarray,
+                         kpe_cache: np.ndarray, dims: Dims = KIMI_K2, eps: float = DEFAULT_EPS,
+                         base: float = DEFAULT_ROPE_BASE, scale: float | None = None) -> dict:
+    """Decode against the latent cache with W_UK absorbed into the query and
+    W_UV folded into the output projection: per head the latent attention
+    output o_lat[h] = sum_j p_j c_j ([kv_lora]), then
+    Delta = [o_lat[0] .. o_lat[H-1]] W_fold^T.  Equal to ``decode_latent`` up to
+    float64 rounding (associativity); the new token's cache rows as there."""
+    if scale is None:
+        scale = default_scale(dims)
+    B = x_new.shape[0]
+    P = ckv_cache.shape[1]
+    t = project_tokens(w, x_new, np.full((B,), P), dims, eps, base, want_q=True)
+    wkvb = w["w_kv_b"].reshape(dims.H, dims.nope + dims.v, dims.kv_lora)
+    w_uk = wkvb[:, :dims.nope]
+    o_lat = np.empty((B, dims.H, dims.kv_lora))
+    for b in range(B):
+        C = np.concatenate([ckv_cache[b], t["ckv"][b][None]], axis=0)      # [P+1, kv_lora]
+        R = np.concatenate([kpe_cache[b], t["kpe"][b][None]], axis=0)      # [P+1, rope]
+        for h in range(dims.H):
+            q_lat = w_uk[h].T @ t["Q"][b, h, :dims.nope]
+            s = (C @ q_lat + R @ t["Q"][b, h, dims.nope:]) * scale
+            p = softmax(s[None])[0]
+            o_lat[b, h] = p @ C
+    delta = _linear(o_lat.reshape(B, dims.H * dims.kv_lora), w_fold)
+    return {"out": x_new + delta, "delta": delta, "ckv_new": t["ckv"], "kpe_new": t["kpe"]}
+
+
 def prefill_with_past_latent(w: dict, x: np.ndarray, ckv_cache: np.ndarray, kpe_cache: np.ndarray,
                              dims: Dims = KIMI_K2, eps: float = DEFAULT_EPS, base: float = DEFAULT_ROPE_BASE,
                              scale: float | None = None, query_rows=None) -> dict:

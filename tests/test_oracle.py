@@ -439,6 +439,36 @@ def test_latent_absorbed_equals_rebuilt():
     np.testing.assert_allclose(a["delta"], b["delta"], rtol=1e-10, atol=1e-13)
 
 
+def test_wuv_fold_blocks_and_folded_decode():
+    """W_fold's block h is W_o's head-h columns times W_UV[h] (checked
+    element by element against a triple loop), and the decode through the
+    folded matrix equals the rebuilt-cache decode (associativity).  A fold
+    with W_UV's rows and columns swapped per head, or the wrong head's
+    block, fails both."""
+    dims = TINY2
+    w = rand_weights(dims, 45)
+    F = om.fold_wuv_into_wo(w, dims)
+    assert F.shape == (dims.d, dims.H * dims.kv_lora)
+    wkvb = w["w_kv_b"]
+    for h in range(dims.H):
+        for i in range(dims.d):
+            for c in range(dims.kv_lora):
+                ref = sum(w["w_o"][i, h * dims.v + j] * wkvb[h * (dims.nope + dims.v) + dims.nope + j, c]
+                          for j in range(dims.v))
+                assert abs(F[i, h * dims.kv_lora + c] - ref) < 1e-12
+    cache = om.cache_from_tokens(w, rand_x((2, 11, dims.d), 46), dims)
+    xn = rand_x((2, dims.d), 47)
+    a = om.decode_latent(w, xn, cache["ckv"], cache["kpe"], dims)
+    b = om.decode_latent_folded(w, F, xn, cache["ckv"], cache["kpe"], dims)
+    np.testing.assert_allclose(b["delta"], a["delta"], rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(b["ckv_new"], a["ckv_new"], rtol=0, atol=1e-14)
+    # a head-block permutation (each head given the next head's block) is caught
+    Fp = np.concatenate([F[:, ((h + 1) % dims.H) * dims.kv_lora:((h + 1) % dims.H + 1) * dims.kv_lora]
+                         for h in range(dims.H)], axis=1)
+    bp = om.decode_latent_folded(w, Fp, xn, cache["ckv"], cache["kpe"], dims)
+    assert not np.allclose(bp["delta"], a["delta"], rtol=1e-3, atol=1e-6)
+
+
 def test_batch_rows_are_independent():
     dims = TINY
     w = rand_weights(dims, 42)
