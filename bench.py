@@ -414,6 +414,20 @@ class Runner:
             fn(self.W, x, P, P_max, c1, c2, out, ws, m.make_params(timing=timing))
         return step, (c1, c2, x, out, P, ws)
 
+    def decode_folded_step_fn(self, B, P):
+        """Latent decode with W_UV folded into o_proj (W_fold built once)."""
+        torch, m, synth = self.torch, self.m, self.synth
+        wf = torch.empty((D, H * KVL), dtype=torch.bfloat16, device=self.dev)
+        m.mla_fold_wuv_into_wo(self.W, wf, m.alloc_workspace(m.MODE_FOLD, 1, 1, device=self.dev))
+        c1, c2 = self.fill_caches(B, P, P + 1, False)
+        x = synth.tensor_cuda(0, "new_x", (B, D), synth.X_DIST, device=self.dev)
+        out = torch.empty_like(x)
+        ws = m.alloc_workspace(m.MODE_DECODE_LATENT, B, P, device=self.dev)
+
+        def step(timing):
+            m.mla_decode_latent_folded(self.W, wf, x, P, c1, c2, out, ws, m.make_params(timing=timing))
+        return step, (wf, c1, c2, x, out, ws)
+
     def decode_step_fn(self, B, P, rebuilt):
         torch, m, synth = self.torch, self.m, self.synth
         c1, c2 = self.fill_caches(B, P, P + 1, rebuilt)
@@ -676,6 +690,24 @@ def main():
             torch.cuda.empty_cache()
         except Exception as e:
             line["decode_latent"] = {"error": repr(e)[:300]}
+        # ---- latent decode with W_UV folded into o_proj: B=128, P=8192 -----------
+        try:
+            B4, P4 = 128, 8192
+            step4f, keep = r.decode_folded_step_fn(B4, P4)
+            ms4f, st4f, l4f = r.time_steps(step4f, ks, W, stages=LATENT_STAGES)
+            us = barrier_max(statistics.mean(ms4f)) * 1e3
+            wbytes = WEIGHT_BYTES - 2 * (7168 * 8192 + 64 * 128 * 512) + 2 * 7168 * 64 * 512
+            byts = B4 * (P4 + 1) * (KVL + ROPE) * 2 + wbytes + 2 * B4 * D * 2
+            line["decode_latent_folded"] = {
+                "workload": "mla_decode_latent_folded B=128 P=8192: W_UV folded into o_proj (470 MB W_fold "
+                            "in place of 125 MB of W_UV and W_o)",
+                "us_per_step": round(us, 2), "hbm_gbs": round(byts / (us * 1e-6) / 1e9, 1),
+                "frac_measured_hbm": round(byts / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
+                "algorithmic_bytes": byts, "stage_ms": _stages_out(st4f), "launches": l4f}
+            del step4f, keep
+            torch.cuda.empty_cache()
+        except Exception as e:
+            line["decode_latent_folded"] = {"error": repr(e)[:300]}
         # ---- decode with FP8 block-scaled weights: B=64, P=1000 -------------------
         try:
             B3, P3 = 64, 1000

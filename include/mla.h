@@ -73,6 +73,7 @@ extern "C" {
 #define MLA_MODE_FFN 3
 #define MLA_MODE_CHUNK_LATENT 4
 #define MLA_MODE_CHUNK_ABSORBED 5
+#define MLA_MODE_FOLD 6
 
 /* Weights of one MLA sublayer: device pointers to bf16, nn.Linear [out, in].
  * Key-value compression page, MLA __init__ excerpt, for the projections;
@@ -139,6 +140,8 @@ typedef struct {
  *                                  tokens, latent caches of `cap` positions
  *                                  (mla_prefill_chunk_absorbed; the size grows
  *                                  with B * T only).
+ *   mode = MLA_MODE_FOLD:          mla_fold_wuv_into_wo (B, t_or_p, cap
+ *                                  ignored: a status region only).
  * Returns 0 when the arguments are out of range. */
 size_t mla_workspace_size(int mode, int B, int t_or_p, int cap);
 
@@ -194,6 +197,28 @@ int mla_prefill_chunk(const mla_weights_t* w, const mla_params_t* params, const 
  * WORKSPACE, CUDA. */
 int mla_prefill_chunk_latent(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int T,
                              int P0, void* out, void* ckv_cache, void* kpe_cache, int cap, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* W_UV folded into the output projection (latent-cache serving, "Key-value
+ * compression" page: the value up-projection moves past the attention, and
+ * here on into W_o): for every head h,
+ *   W_fold[:, h*512 .. h*512+511] = W_o[:, h*128 .. h*128+127] W_UV[h],
+ * W_UV[h] = rows h*256+128 .. h*256+255 of W_kv_b ([128, 512]).
+ *   w_fold     [7168, 32768] bf16, caller-allocated (470 MB), written
+ *   workspace  mla_workspace_size(MLA_MODE_FOLD, 1, 1, 0) bytes
+ * Errors: INVALID_ARG (null weight or w_fold), ALIGNMENT, WORKSPACE, CUDA. */
+int mla_fold_wuv_into_wo(const mla_weights_t* w, void* w_fold, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/* mla_decode_latent with the output projection through W_fold: the latent
+ * attention output of all heads, o_lat [B, 64*512], times W_fold^T plus the
+ * residual, one GEMM in place of W_UV and o_proj.  Arguments, workspace
+ * (MLA_MODE_DECODE_LATENT) and errors as mla_decode_latent; w_fold from
+ * mla_fold_wuv_into_wo (16-byte aligned).  It streams 470 MB of weights where
+ * W_UV and W_o are 125 MB, so a weight-bound decode step is slower; kept for
+ * comparison. */
+int mla_decode_latent_folded(const mla_weights_t* w, const void* w_fold, const mla_params_t* params, const void* x,
+                             int B, int P, void* ckv_cache, void* kpe_cache, int cap, void* out, void* workspace,
                              size_t workspace_bytes, void* stream);
 
 /* The same chunk in the absorbed form (latent-cache serving, "Key-value

@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libmla.so")
 D, HEADS, Q_LORA, KV_LORA, QK_NOPE, QK_ROPE, QK, V = 7168, 64, 1536, 512, 128, 64, 192, 128
 FFN_INTER = 18432
 MODE_PREFILL, MODE_DECODE, MODE_DECODE_LATENT, MODE_FFN, MODE_CHUNK_LATENT, MODE_CHUNK_ABSORBED = 0, 1, 2, 3, 4, 5
+MODE_FOLD = 6
 STAGES = ["input_norm", "a_proj", "latent", "q_b", "kv_b", "attn", "combine", "absorb_q", "absorb_o", "o_proj",
           "ffn_norm", "gate_up", "down"]
 MAX_STAGES = len(STAGES)
@@ -83,6 +84,9 @@ _SIGS = {
                         _VP, _SZ, _VP]),
     "mla_decode_latent": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _I, _VP, _VP, _I,
                                _VP, _VP, _SZ, _VP]),
+    "mla_fold_wuv_into_wo": (_I, [ctypes.POINTER(MlaWeights), _VP, _VP, _SZ, _VP]),
+    "mla_decode_latent_folded": (_I, [ctypes.POINTER(MlaWeights), _VP, ctypes.POINTER(MlaParams), _VP, _I, _I, _VP,
+                                      _VP, _I, _VP, _VP, _SZ, _VP]),
     "mla_decode_varlen": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _VP, _I, _VP, _VP,
                                _I, _VP, _VP, _SZ, _VP]),
     "mla_decode_latent_varlen": (_I, [ctypes.POINTER(MlaWeights), ctypes.POINTER(MlaParams), _VP, _I, _VP, _I, _VP,
@@ -244,6 +248,25 @@ def mla_decode_latent(weights: MlaWeights, x, P: int, ckv_cache, kpe_cache, out,
                                  B, P, _ptr(ckv_cache), _ptr(kpe_cache), cap, _ptr(out), _ptr(workspace),
                                  workspace.numel(), _stream(stream))
     _check(rc, "mla_decode_latent")
+
+
+def mla_fold_wuv_into_wo(weights: MlaWeights, w_fold, workspace, stream=None):
+    """w_fold: bf16 [7168, 64 * 512] receives W_o's head blocks times W_UV per head; workspace of MODE_FOLD."""
+    rc = lib().mla_fold_wuv_into_wo(ctypes.byref(weights), _ptr(w_fold), _ptr(workspace), workspace.numel(),
+                                    _stream(stream))
+    _check(rc, "mla_fold_wuv_into_wo")
+
+
+def mla_decode_latent_folded(weights: MlaWeights, w_fold, x, P: int, ckv_cache, kpe_cache, out, workspace,
+                             params: MlaParams | None = None, stream=None):
+    """mla_decode_latent with W_UV folded into o_proj (w_fold from mla_fold_wuv_into_wo)."""
+    B = x.shape[0]
+    cap = ckv_cache.shape[1]
+    rc = lib().mla_decode_latent_folded(ctypes.byref(weights), _ptr(w_fold),
+                                        None if params is None else ctypes.byref(params), _ptr(x), B, P,
+                                        _ptr(ckv_cache), _ptr(kpe_cache), cap, _ptr(out), _ptr(workspace),
+                                        workspace.numel(), _stream(stream))
+    _check(rc, "mla_decode_latent_folded")
 
 
 def mla_decode_varlen(weights: MlaWeights, x, P, P_max: int, k_cache, v_cache, out, workspace,

@@ -43,6 +43,10 @@ Layout make_layout(int mode, int B, int t_or_p, int num_sms, int cap = 0) {
     return at;
   };
   L.status = take(kStatusRegion);
+  if (mode == MLA_MODE_FOLD) {  // the fold of W_UV into W_o: the status region only
+    L.total = off;
+    return L;
+  }
   if (mode == MLA_MODE_FFN) {  // B * t_or_p rows: RMSNorm(x') and h
     const size_t rows = (size_t)B * t_or_p;
     L.xn = take(rows * MLA_D * 2);
@@ -363,6 +367,7 @@ size_t mla_workspace_size(int mode, int B, int t_or_p, int cap) {
     if (t_or_p < 1 || (int64_t)B * t_or_p > kMaxTokens) return 0;
   } else if (mode == MLA_MODE_CHUNK_ABSORBED) {
     if (t_or_p < 1 || (int64_t)B * t_or_p > kMaxTokens || cap < t_or_p || cap >= (1 << 24)) return 0;
+  } else if (mode == MLA_MODE_FOLD) {
   } else {
     return 0;
   }
@@ -577,7 +582,7 @@ int decode_impl(const mla_weights_t* w, const mla_params_t* params, const void* 
 int latent_tail(const mla_weights_t* w, const Params& p, const void* x, void* out, int n, int P_max, const int* pos,
                 int kv_div, const __nv_bfloat16* ckv_cache, const __nv_bfloat16* kpe_cache, int cap, void* workspace,
                 const Layout& L, const DevStatusHost& st, int sms, cudaStream_t stream_, Stager& sg, int* launches,
-                bool qpe_in_epilogue) {
+                bool qpe_in_epilogue, const __nv_bfloat16* w_fold = nullptr) {
   const __nv_bfloat16* wkvb = static_cast<const __nv_bfloat16*>(w->w_kv_b);
   sg.start(MLA_STAGE_ABSORB_Q);
   {
@@ -621,6 +626,24 @@ int latent_tail(const mla_weights_t* w, const Params& p, const void* x, void* ou
   }
   sg.stop(MLA_STAGE_ATTN);
 
+  if (w_fold) {
+    // W_UV folded into o_proj: out = x + o_lat [n, 64*512] W_fold^T, one GEMM
+    sg.start(MLA_STAGE_O_PROJ);
+    GemmShape s{n, MLA_D, MLA_HEADS * MLA_KV_LORA, 1, 0, 0, 0, 0, MLA_D};
+    GemmOperands op{at<__nv_bfloat16>(workspace, L.olat), MLA_HEADS * MLA_KV_LORA, n, w_fold,
+                    MLA_HEADS * MLA_KV_LORA, MLA_D, nullptr, 0, 0, false};
+    EpiArgs ea{};
+    ea.out = static_cast<__nv_bfloat16*>(out);
+    ea.ldo = MLA_D;
+    ea.x = static_cast<const __nv_bfloat16*>(x);
+    ea.delta = p.delta;
+    set_split(ea, workspace, L);
+    MLA_TRY(launch_gemm(s, op, Epi::kResidual, ea, st, sms, stream_));
+    *launches += 1;
+    sg.stop(MLA_STAGE_O_PROJ);
+    return MLA_OK;
+  }
+
   sg.start(MLA_STAGE_ABSORB_O);
   {
     // o[i, h*128 + d] = sum_c o_lat[i, h, c] W_kv_b[h*256 + 128 + d, c]
@@ -647,12 +670,12 @@ int latent_tail(const mla_weights_t* w, const Params& p, const void* x, void* ou
 
 int decode_latent_impl(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int P,
                        const int* pos, void* ckv_cache, void* kpe_cache, int cap, void* out, void* workspace,
-                       size_t workspace_bytes, void* stream) {
+                       size_t workspace_bytes, void* stream, const void* w_fold = nullptr) {
   const Params p = resolve(params);
   if (B < 1 || B > kMaxTokens || P < 0 || P >= (1 << 24)) return MLA_ERR_INVALID_ARG;
   if (!ckv_cache || !kpe_cache || cap < P + 1) return MLA_ERR_INVALID_ARG;
   if (pos && (reinterpret_cast<uintptr_t>(pos) & 3)) return MLA_ERR_ALIGNMENT;
-  if (!aligned16(ckv_cache) || !aligned16(kpe_cache)) return MLA_ERR_ALIGNMENT;
+  if (!aligned16(ckv_cache) || !aligned16(kpe_cache) || (w_fold && !aligned16(w_fold))) return MLA_ERR_ALIGNMENT;
   int rc = common_checks(w, p, x, out, (size_t)B, workspace, workspace_bytes,
                          make_layout(MLA_MODE_DECODE_LATENT, B, P, kMaxSmsForSizing).total);
   if (rc) return rc;
@@ -674,7 +697,7 @@ int decode_latent_impl(const mla_weights_t* w, const mla_params_t* params, const
   if (rc) return rc;
   rc = latent_tail(w, p, x, out, B, P, pos, 1, static_cast<const __nv_bfloat16*>(ckv_cache),
                    static_cast<const __nv_bfloat16*>(kpe_cache), cap, workspace, L, st, sms, stream_, sg, &launches,
-                   qpe_in_epilogue);
+                   qpe_in_epilogue, static_cast<const __nv_bfloat16*>(w_fold));
   if (rc) return rc;
   if (p.timing) p.timing->n_launches = launches;
   return MLA_OK;
@@ -775,6 +798,41 @@ int mla_decode_latent_varlen(const mla_weights_t* w, const mla_params_t* params,
   if (!P) return MLA_ERR_INVALID_ARG;
   return decode_latent_impl(w, params, x, B, P_max, P, ckv_cache, kpe_cache, cap, out, workspace, workspace_bytes,
                             stream);
+}
+
+int mla_fold_wuv_into_wo(const mla_weights_t* w, void* w_fold, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  int rc = check_weights(w);
+  if (rc) return rc;
+  if (!w_fold) return MLA_ERR_INVALID_ARG;
+  if (!workspace) return MLA_ERR_WORKSPACE;
+  if (!aligned16(w_fold) || !aligned16(workspace)) return MLA_ERR_ALIGNMENT;
+  const Layout L = make_layout(MLA_MODE_FOLD, 1, 1, kMaxSmsForSizing);
+  if (workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return MLA_ERR_CUDA;
+  cudaStream_t stream_ = static_cast<cudaStream_t>(stream);
+  const DevStatusHost st{at<uint32_t>(workspace, L.status), kDefaultWaitLimitNs};
+  if (cudaMemsetAsync(st.word, 0, kStatusRegion, stream_) != cudaSuccess) return MLA_ERR_CUDA;
+  // per head h: W_fold[:, h*512 .. +512] = W_o[:, h*128 .. +128] W_kv_b[h*256 + 128 .. +128, :]
+  // (A = W_o's head columns, B = the head's W_UV rows as [K = 128, N = 512], N contiguous)
+  GemmShape s{MLA_D, MLA_KV_LORA, MLA_V, MLA_HEADS, 0, MLA_V, MLA_QK_NOPE, 256, MLA_KV_LORA};
+  GemmOperands op{static_cast<const __nv_bfloat16*>(w->w_o), MLA_HEADS * MLA_V, MLA_D,
+                  static_cast<const __nv_bfloat16*>(w->w_kv_b), MLA_KV_LORA, MLA_HEADS * 256, nullptr, 0, 0, true};
+  EpiArgs ea{};
+  ea.out = static_cast<__nv_bfloat16*>(w_fold);
+  ea.ldo = MLA_HEADS * MLA_KV_LORA;
+  ea.c_col0 = 0;
+  ea.c_col_step = MLA_KV_LORA;
+  return launch_gemm(s, op, Epi::kStoreBf16, ea, st, sms, stream_) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_decode_latent_folded(const mla_weights_t* w, const void* w_fold, const mla_params_t* params, const void* x,
+                             int B, int P, void* ckv_cache, void* kpe_cache, int cap, void* out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (!w_fold) return MLA_ERR_INVALID_ARG;
+  return decode_latent_impl(w, params, x, B, P, nullptr, ckv_cache, kpe_cache, cap, out, workspace,
+                            workspace_bytes, stream, w_fold);
 }
 
 int mla_prefill_chunk_absorbed(const mla_weights_t* w, const mla_params_t* params, const void* x, int B, int T,

@@ -198,6 +198,25 @@ def test_prefill_chunk_absorbed_argument_checks():
     assert call(nbytes=ws_bytes - 256) == -3
 
 
+def test_fold_entries_argument_checks():
+    w = fake_weights()
+    ws_bytes = m.lib().mla_workspace_size(m.MODE_FOLD, 1, 1, 0)
+    assert ws_bytes > 0
+    fold = m.lib().mla_fold_wuv_into_wo
+    assert fold(ctypes.byref(w), None, FAKE + (3 << 30), ws_bytes, None) == -1
+    assert fold(ctypes.byref(w), FAKE + (2 << 30) + 8, FAKE + (3 << 30), ws_bytes, None) == -2
+    assert fold(ctypes.byref(w), FAKE + (2 << 30), FAKE + (3 << 30), ws_bytes - 256, None) == -3
+    assert fold(ctypes.byref(w), FAKE + (2 << 30), None, ws_bytes, None) == -3
+    dws = m.lib().mla_workspace_size(m.MODE_DECODE_LATENT, 4, 10, 0)
+
+    def dec(wf=FAKE + (6 << 30), P=10, cap=11):
+        return m.lib().mla_decode_latent_folded(ctypes.byref(w), wf, None, FAKE + (1 << 30), 4, P, FAKE + (4 << 30),
+                                                FAKE + (5 << 30), cap, FAKE + (2 << 30), FAKE + (3 << 30), dws, None)
+    assert dec(wf=None) == -1
+    assert dec(wf=FAKE + (6 << 30) + 8) == -2
+    assert dec(cap=10) == -1           # P + 1 > cap
+
+
 def test_fp8_entry_argument_checks():
     lib = m.lib()
     # quantizer: cols must be a multiple of 128, pointers 16-byte aligned (scales 4-byte)
