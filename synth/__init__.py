@@ -9,12 +9,19 @@ Generator, defined once and implemented twice (numpy here, CUDA in
 ``synth.cu`` with the same steps):
 
 * key      = splitmix64((seed << 32) | stream)
-* r_i      = splitmix64(key + i * GAMMA)           (64-bit wrap-around)
-* z_i      = (k0 + k1 + k2 + k3 - 131070) * sqrt(3) / 65536
-             where k0..k3 are the four 16-bit fields of r_i.  This is the
-             Irwin-Hall sum of four uniforms on (0, 1), centred and scaled to
-             unit variance; every step is exact or a single IEEE rounding, so
-             CPU and GPU agree bit for bit (no transcendental function).
+* r_c      = splitmix64(key + c * GAMMA)           (64-bit wrap-around)
+* value i draws r_{2i} and r_{2i+1}:
+  u1 = ((r_{2i} >> 11) + 1) 2^-53 in (0, 1],  u2 = (r_{2i+1} >> 11) 2^-53 in [0, 1)
+* z_i      = sqrt(-2 ln u1) cos(2 pi u2)        (Box and Muller, 1958: an
+             exact standard normal variate for exact uniforms; |z| < 8.6)
+  with ln and cos evaluated by power series in plain IEEE double operations
+  (add, multiply, divide, square root; no fused multiply-add), so the two
+  copies round identically step for step:
+    ln u1   = e ln 2 + 2 atanh(s): u1 = m 2^e with m in [sqrt(1/2), sqrt(2)),
+              s = (m - 1) / (m + 1), atanh(s) = s sum_k s^(2k) / (2k + 1)
+    cos 2 pi u2 by quarter turns: q = floor(4 u2), phi = (pi/2)(4 u2 - q),
+              cos phi = sum_k (-1)^k phi^(2k) / (2k)!,
+              sin phi = phi sum_k (-1)^k phi^(2k) / (2k + 1)!, k = 0..11
 * value    = bf16_rne(float32_rne(mean + std * z_i))  (double arithmetic, no FMA)
 
 splitmix64 is the mixing function of Steele, Lea and Flood (2014),
@@ -34,8 +41,23 @@ import numpy as np
 GAMMA = 0x9E3779B97F4A7C15
 _M1 = 0xBF58476D1CE4E5B9
 _M2 = 0x94D049BB133111EB
-# sqrt(3)/65536 as an exact double (sqrt is correctly rounded, /2^16 exact)
-_ZSCALE = float.fromhex("0x1.bb67ae8584caap-16")
+# Series coefficients as exact hex doubles (the same literals are in synth.cu):
+# 1 / (2k + 1), (-1)^k / (2k)!, (-1)^k / (2k + 1)! for k = 0..11.
+_ATANH = [float.fromhex(h) for h in (
+    "0x1.0000000000000p+0", "0x1.5555555555555p-2", "0x1.999999999999ap-3", "0x1.2492492492492p-3",
+    "0x1.c71c71c71c71cp-4", "0x1.745d1745d1746p-4", "0x1.3b13b13b13b14p-4", "0x1.1111111111111p-4",
+    "0x1.e1e1e1e1e1e1ep-5", "0x1.af286bca1af28p-5", "0x1.8618618618618p-5", "0x1.642c8590b2164p-5")]
+_COS = [float.fromhex(h) for h in (
+    "0x1.0000000000000p+0", "-0x1.0000000000000p-1", "0x1.5555555555555p-5", "-0x1.6c16c16c16c17p-10",
+    "0x1.a01a01a01a01ap-16", "-0x1.27e4fb7789f5cp-22", "0x1.1eed8eff8d898p-29", "-0x1.93974a8c07c9dp-37",
+    "0x1.ae7f3e733b81fp-45", "-0x1.6827863b97d97p-53", "0x1.e542ba4020225p-62", "-0x1.0ce396db7f853p-70")]
+_SIN = [float.fromhex(h) for h in (
+    "0x1.0000000000000p+0", "-0x1.5555555555555p-3", "0x1.1111111111111p-7", "-0x1.a01a01a01a01ap-13",
+    "0x1.71de3a556c734p-19", "-0x1.ae64567f544e4p-26", "0x1.6124613a86d09p-33", "-0x1.ae7f3e733b81fp-41",
+    "0x1.952c77030ad4ap-49", "-0x1.2f49b46814157p-57", "0x1.71b8ef6dcf572p-66", "-0x1.761b41316381ap-75")]
+_LN2 = float.fromhex("0x1.62e42fefa39efp-1")
+_HALF_PI = float.fromhex("0x1.921fb54442d18p+0")
+_SQRT_HALF = float.fromhex("0x1.6a09e667f3bcdp-1")
 
 STREAMS = {
     "x": 0,            # prefill input hidden states
@@ -111,6 +133,17 @@ def _splitmix64(x: np.ndarray) -> np.ndarray:
     return x ^ (x >> np.uint64(31))
 
 
+def _splitmix64_inplace(x: np.ndarray, t: np.ndarray) -> None:
+    """x <- splitmix64(x) (t: scratch of the same shape)."""
+    x += np.uint64(GAMMA)
+    for shift, mul in ((30, _M1), (27, _M2)):
+        np.right_shift(x, np.uint64(shift), out=t)
+        x ^= t
+        x *= np.uint64(mul)
+    np.right_shift(x, np.uint64(31), out=t)
+    x ^= t
+
+
 def stream_key(seed: int, stream: int) -> int:
     v = np.array([((seed & 0xFFFFFFFF) << 32) | (stream & 0xFFFFFFFF)], dtype=np.uint64)
     return int(_splitmix64(v)[0])
@@ -131,21 +164,94 @@ def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
     return bf16_bits_to_f32(b).astype(np.float64)
 
 
+def _horner(x: np.ndarray, coef, out: np.ndarray) -> np.ndarray:
+    """out <- sum_k coef[k] x^k, Horner's rule from the highest term
+    (p = c_K; p = p x + c_k), one rounding per operation."""
+    np.multiply(x, coef[-1], out=out)
+    out += coef[-2]
+    for c in reversed(coef[:-2]):
+        out *= x
+        out += c
+    return out
+
+
 def normal_bf16_bits(seed: int, stream: int, start: int, count: int,
-                     mean: float, std: float, chunk: int = 1 << 24) -> np.ndarray:
-    """bf16 bit patterns of values start .. start+count-1 of one stream."""
+                     mean: float, std: float, chunk: int = 1 << 16) -> np.ndarray:
+    """bf16 bit patterns of values start .. start+count-1 of one stream
+    (worked in cache-sized chunks with in-place operations)."""
     key = np.uint64(stream_key(seed, stream))
     out = np.empty(count, dtype=np.uint16)
+    m0 = min(chunk, count)
+    if m0 == 0:
+        return out
+    ramp = np.arange(m0, dtype=np.int64).view(np.uint64)
+    c2, r1, r2, t = (np.empty(m0, dtype=np.uint64) for _ in range(4))
+    m, e, s, p, q, x, ps = (np.empty(m0, dtype=np.float64) for _ in range(7))
+    mask = np.empty(m0, dtype=bool)
+    f = np.empty(m0, dtype=np.float32)
+    u = f.view(np.uint32)
+    b = np.empty(m0, dtype=np.uint32)
     for c0 in range(0, count, chunk):
         n = min(chunk, count - c0)
-        idx = np.arange(start + c0, start + c0 + n, dtype=np.uint64)
-        r = _splitmix64(key + idx * np.uint64(GAMMA))
-        ks = ((r & np.uint64(0xFFFF)) + ((r >> np.uint64(16)) & np.uint64(0xFFFF))
-              + ((r >> np.uint64(32)) & np.uint64(0xFFFF)) + (r >> np.uint64(48)))
-        z = (ks.astype(np.int64) - 131070).astype(np.float64) * _ZSCALE
-        v = z * std          # one rounding
-        v = v + mean         # one rounding
-        out[c0:c0 + n] = f32_to_bf16_bits(v.astype(np.float32))
+        c2_, r1_, r2_, t_ = c2[:n], r1[:n], r2[:n], t[:n]
+        m_, e_, s_, p_, q_, x_, ps_, k_ = m[:n], e[:n], s[:n], p[:n], q[:n], x[:n], ps[:n], mask[:n]
+        np.add(ramp[:n], np.uint64(start + c0), out=c2_)
+        c2_ *= np.uint64(2)                          # counter of value i's first draw
+        for j, r_ in ((0, r1_), (1, r2_)):
+            np.add(c2_, np.uint64(j), out=r_)
+            r_ *= np.uint64(GAMMA)
+            r_ += key
+            _splitmix64_inplace(r_, t_)
+            r_ >>= np.uint64(11)                     # 53 random bits
+        # u1 = (r1 + 1) 2^-53 in (0, 1]; its exponent e and mantissa m in [1/2, 1)
+        r1_ += np.uint64(1)
+        np.copyto(m_, r1_, casting="unsafe")         # exact (< 2^53 + 1)
+        m_ *= 2.0 ** -53
+        mb = m_.view(np.uint64)
+        np.right_shift(mb, np.uint64(52), out=t_)
+        np.copyto(e_, t_, casting="unsafe")
+        e_ -= 1022.0
+        mb &= np.uint64(0x000FFFFFFFFFFFFF)
+        mb |= np.uint64(1022 << 52)
+        np.less(m_, _SQRT_HALF, out=k_)              # m in [sqrt(1/2), sqrt(2))
+        np.multiply(m_, 2.0, out=m_, where=k_)
+        np.subtract(e_, 1.0, out=e_, where=k_)
+        # ln u1 = e ln 2 + 2 s sum_k s^2k / (2k + 1),  s = (m - 1) / (m + 1)
+        np.add(m_, 1.0, out=p_)
+        m_ -= 1.0
+        np.divide(m_, p_, out=s_)
+        np.multiply(s_, s_, out=x_)
+        _horner(x_, _ATANH, p_)
+        s_ *= p_
+        s_ *= 2.0
+        e_ *= _LN2
+        e_ += s_                                     # ln u1
+        e_ *= -2.0
+        np.sqrt(e_, out=e_)                          # R = sqrt(-2 ln u1)
+        # cos(2 pi u2) by quarter turns
+        np.copyto(m_, r2_, casting="unsafe")
+        m_ *= 2.0 ** -51                             # 4 u2, exact
+        np.floor(m_, out=q_)
+        m_ -= q_                                     # exact
+        m_ *= _HALF_PI                               # phi
+        np.multiply(m_, m_, out=x_)
+        _horner(x_, _COS, p_)                        # cos phi
+        _horner(x_, _SIN, ps_)
+        ps_ *= m_                                    # sin phi
+        np.negative(ps_, out=ps_, where=(q_ == 1.0))
+        np.negative(p_, out=p_, where=(q_ == 2.0))
+        np.copyto(p_, ps_, where=((q_ == 1.0) | (q_ == 3.0)))
+        e_ *= p_                                     # z = R cos(2 pi u2)
+        e_ *= std                                    # one rounding
+        e_ += mean                                   # one rounding
+        np.copyto(f[:n], e_, casting="same_kind")    # float32, round to nearest even
+        u_, b_ = u[:n], b[:n]
+        np.right_shift(u_, np.uint32(16), out=b_)    # bf16, round to nearest even
+        b_ &= np.uint32(1)
+        b_ += np.uint32(0x7FFF)
+        b_ += u_
+        b_ >>= np.uint32(16)
+        np.copyto(out[c0:c0 + n], b_, casting="unsafe")
     return out
 
 
@@ -161,6 +267,10 @@ def tensor_bits(seed: int, name: str, shape, dist, rows=None) -> np.ndarray:
     mean, std = dist
     if rows is None:
         return normal_bf16_bits(seed, STREAMS[name], 0, int(np.prod(shape)), mean, std).reshape(shape)
+    if isinstance(rows, range) and rows.step == 1:  # a contiguous block: one draw
+        n = max(0, len(rows))
+        return normal_bf16_bits(seed, STREAMS[name], rows.start * inner, n * inner, mean, std).reshape(
+            (n,) + shape[1:])
     rows = list(rows)
     out = np.empty((len(rows),) + shape[1:], dtype=np.uint16)
     for i, r in enumerate(rows):
