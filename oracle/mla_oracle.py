@@ -475,14 +475,32 @@ def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
     return a * u
 
 
-def ffn(w: dict, xp: np.ndarray, eps: float = DEFAULT_EPS) -> dict:
+def round_to_bf16(a: np.ndarray) -> np.ndarray:
+    """The nearest bfloat16 value of each float64 (8 significant bits,
+    ties to even), for values in bfloat16's normal range: the storage of a
+    module output in a bf16 model.  a = m 2^e with 1/2 <= |m| < 1; m is
+    rounded to a multiple of 2^-8 (np.round rounds halves to even)."""
+    m, e = np.frexp(np.asarray(a, dtype=np.float64))
+    return np.ldexp(np.round(m * 256.0) / 256.0, e)
+
+
+def ffn(w: dict, xp: np.ndarray, eps: float = DEFAULT_EPS, bf16_products: bool = False) -> dict:
     """x_{n+1} from x'_n (dense-block page): x_ffn = RMSNorm(x'_n);
     g = x_ffn W_1; u = x_ffn W_3; a = g sigma(g); h = a (.) u;
-    Delta_ffn = h W_2; x_{n+1} = x'_n + Delta_ffn.  Any leading shape."""
+    Delta_ffn = h W_2; x_{n+1} = x'_n + Delta_ffn.  Any leading shape.
+
+    bf16_products: the reading a bf16 model takes of the same equations
+    (the MLP precision reading): the two product inputs, x_ffn and h, are
+    module outputs stored in bfloat16, so each is rounded once to bf16
+    before its product; everything else stays float64."""
     x_ffn = rms_norm(xp, w["g_post"], eps)
+    if bf16_products:
+        x_ffn = round_to_bf16(x_ffn)
     g = _linear(x_ffn, w["w_1"])
     u = _linear(x_ffn, w["w_3"])
     h = swiglu(g, u)
+    if bf16_products:
+        h = round_to_bf16(h)
     delta = _linear(h, w["w_2"])
     return {"out": xp + delta, "delta": delta, "h": h}
 
