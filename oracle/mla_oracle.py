@@ -121,8 +121,23 @@ def _linear(x: np.ndarray, w: np.ndarray) -> np.ndarray:
     return x @ w.T
 
 
+def round_to_bf16(a: np.ndarray) -> np.ndarray:
+    """The nearest bfloat16 value of each float64 (8 significant bits,
+    ties to even), for values in bfloat16's normal range: the storage of a
+    module output in a bf16 model.  a = m 2^e with 1/2 <= |m| < 1; m is
+    rounded to a multiple of 2^-8 (np.round rounds halves to even)."""
+    m, e = np.frexp(np.asarray(a, dtype=np.float64))
+    return np.ldexp(np.round(m * 256.0) / 256.0, e)
+
+
+def _stored(a: np.ndarray, bf16: bool) -> np.ndarray:
+    """a as the next step receives it: rounded to bf16 in the bf16-storage
+    reading, unchanged otherwise."""
+    return round_to_bf16(a) if bf16 else a
+
+
 def project_tokens(w: dict, x: np.ndarray, pos: np.ndarray, dims: Dims, eps: float,
-                   base: float, want_q: bool = True) -> dict:
+                   base: float, want_q: bool = True, bf16_storage: bool = False) -> dict:
     """Per-token part of MLA for tokens x [..., d] at positions ``pos``.
 
     Dense-block page equations c^Q .. v, and the key-value compression page's
@@ -130,16 +145,23 @@ def project_tokens(w: dict, x: np.ndarray, pos: np.ndarray, dims: Dims, eps: flo
     (only the latent is normalised).  Returns per-head K rows [..., H, qk],
     V rows [..., H, v], the latent c^KV-hat [..., kv_lora], the rotated rotary
     key k^R [..., rope] and (if want_q) Q rows [..., H, qk].
+
+    bf16_storage: the activations one step hands to the next are stored in
+    bf16 (x_attn, the normalised latents, the rotated rotary keys, Q after
+    RoPE, the kv_b output), as the pages' module does when it runs in bf16;
+    the A-projection output stays unrounded until it is normalised or
+    rotated (the A-projection precision reading).
     """
-    x_attn = rms_norm(x, w["g_in"], eps)
+    st = bf16_storage
+    x_attn = _stored(rms_norm(x, w["g_in"], eps), st)
     ckv_full = _linear(x_attn, w["w_kv_a"])
     ckv = ckv_full[..., :dims.kv_lora]
     kpe_raw = ckv_full[..., dims.kv_lora:]
-    ckv_hat = rms_norm(ckv, w["g_kva"], eps)
-    kv = _linear(ckv_hat, w["w_kv_b"]).reshape(x.shape[:-1] + (dims.H, dims.nope + dims.v))
+    ckv_hat = _stored(rms_norm(ckv, w["g_kva"], eps), st)
+    kv = _stored(_linear(ckv_hat, w["w_kv_b"]), st).reshape(x.shape[:-1] + (dims.H, dims.nope + dims.v))
     k_nope = kv[..., :dims.nope]
     v = kv[..., dims.nope:]
-    k_r = rope_rotate(kpe_raw, pos, base)
+    k_r = _stored(rope_rotate(kpe_raw, pos, base), st)
     # K_i = [K^C_i ; k^R]: the one rotary key is shared by every head
     k_r_heads = np.broadcast_to(k_r[..., None, :], k_nope.shape[:-1] + (dims.rope,))
     out = {
@@ -149,10 +171,10 @@ def project_tokens(w: dict, x: np.ndarray, pos: np.ndarray, dims: Dims, eps: flo
         "kpe": k_r,
     }
     if want_q:
-        cq_hat = rms_norm(_linear(x_attn, w["w_q_a"]), w["g_qa"], eps)
+        cq_hat = _stored(rms_norm(_linear(x_attn, w["w_q_a"]), w["g_qa"], eps), st)
         q = _linear(cq_hat, w["w_q_b"]).reshape(x.shape[:-1] + (dims.H, dims.qk))
-        q_nope = q[..., :dims.nope]
-        q_pe = rope_rotate(q[..., dims.nope:], np.asarray(pos)[..., None], base)
+        q_nope = _stored(q[..., :dims.nope], st)
+        q_pe = _stored(rope_rotate(q[..., dims.nope:], np.asarray(pos)[..., None], base), st)
         out["Q"] = np.concatenate([q_nope, q_pe], axis=-1)
     return out
 
@@ -166,22 +188,25 @@ def softmax(s: np.ndarray) -> np.ndarray:
 
 
 def attend(Q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float,
-           q_pos: np.ndarray | None) -> np.ndarray:
+           q_pos: np.ndarray | None, bf16_storage: bool = False) -> np.ndarray:
     """One head: softmax(Q K^T * scale + M) V ("Mix and project" page code).
 
     Q [nq, qk], K [nk, qk], V [nk, v].  q_pos gives each query's position for
     the causal mask M (key j visible iff j <= q_pos); None means no mask.
+    bf16_storage: the probabilities are cast to bf16 before P V and the
+    output is stored in bf16, as the page's code casts the float32 softmax
+    to the query dtype.
     """
     s = (Q @ K.T) * scale
     if q_pos is not None:
         j = np.arange(K.shape[0])
         s = np.where(j[None, :] <= np.asarray(q_pos)[:, None], s, -np.inf)
-    return softmax(s) @ V
+    return _stored(_stored(softmax(s), bf16_storage) @ V, bf16_storage)
 
 
 def prefill(w: dict, x: np.ndarray, dims: Dims = KIMI_K2, eps: float = DEFAULT_EPS,
             base: float = DEFAULT_ROPE_BASE, scale: float | None = None,
-            query_rows=None) -> dict:
+            query_rows=None, bf16_storage: bool = False) -> dict:
     """Causal prefill of x [B, T, d] at positions 0..T-1.
 
     Returns out = x + Delta [B, nq, d], Delta, the rebuilt caches
@@ -194,12 +219,13 @@ def prefill(w: dict, x: np.ndarray, dims: Dims = KIMI_K2, eps: float = DEFAULT_E
     B, T, _ = x.shape
     rows = np.arange(T) if query_rows is None else np.asarray(query_rows)
     pos = np.arange(T)
-    kv = project_tokens(w, x, pos[None, :], dims, eps, base, want_q=False)
-    qp = project_tokens(w, x[:, rows], rows[None, :], dims, eps, base, want_q=True)
+    st = bf16_storage
+    kv = project_tokens(w, x, pos[None, :], dims, eps, base, want_q=False, bf16_storage=st)
+    qp = project_tokens(w, x[:, rows], rows[None, :], dims, eps, base, want_q=True, bf16_storage=st)
     O = np.empty((B, len(rows), dims.H, dims.v))
     for b in range(B):
         for h in range(dims.H):
-            O[b, :, h] = attend(qp["Q"][b, :, h], kv["K"][b, :, h], kv["V"][b, :, h], scale, rows)
+            O[b, :, h] = attend(qp["Q"][b, :, h], kv["K"][b, :, h], kv["V"][b, :, h], scale, rows, st)
     delta = _linear(O.reshape(B, len(rows), dims.H * dims.v), w["w_o"])
     return {
         "out": x[:, rows] + delta,
@@ -213,7 +239,7 @@ def prefill(w: dict, x: np.ndarray, dims: Dims = KIMI_K2, eps: float = DEFAULT_E
 
 def prefill_with_past(w: dict, x: np.ndarray, K_cache: np.ndarray, V_cache: np.ndarray,
                       dims: Dims = KIMI_K2, eps: float = DEFAULT_EPS, base: float = DEFAULT_ROPE_BASE,
-                      scale: float | None = None, query_rows=None) -> dict:
+                      scale: float | None = None, query_rows=None, bf16_storage: bool = False) -> dict:
     """Chunked prefill: x [B, T, d] are the tokens at positions P0..P0+T-1,
     P0 = K_cache.shape[2]; K_cache [B, H, P0, qk] and V_cache [B, H, P0, v]
     hold positions 0..P0-1 (post-RoPE).
@@ -231,14 +257,15 @@ def prefill_with_past(w: dict, x: np.ndarray, K_cache: np.ndarray, V_cache: np.n
     P0 = K_cache.shape[2]
     rows = np.arange(T) if query_rows is None else np.asarray(query_rows)
     pos = P0 + np.arange(T)
-    kv = project_tokens(w, x, pos[None, :], dims, eps, base, want_q=False)
-    qp = project_tokens(w, x[:, rows], (P0 + rows)[None, :], dims, eps, base, want_q=True)
+    st = bf16_storage
+    kv = project_tokens(w, x, pos[None, :], dims, eps, base, want_q=False, bf16_storage=st)
+    qp = project_tokens(w, x[:, rows], (P0 + rows)[None, :], dims, eps, base, want_q=True, bf16_storage=st)
     O = np.empty((B, len(rows), dims.H, dims.v))
     for b in range(B):
         for h in range(dims.H):
             K = np.concatenate([K_cache[b, h], kv["K"][b, :, h]], axis=0)
             V = np.concatenate([V_cache[b, h], kv["V"][b, :, h]], axis=0)
-            O[b, :, h] = attend(qp["Q"][b, :, h], K, V, scale, P0 + rows)
+            O[b, :, h] = attend(qp["Q"][b, :, h], K, V, scale, P0 + rows, st)
     delta = _linear(O.reshape(B, len(rows), dims.H * dims.v), w["w_o"])
     return {
         "out": x[:, rows] + delta,
@@ -252,7 +279,7 @@ def prefill_with_past(w: dict, x: np.ndarray, K_cache: np.ndarray, V_cache: np.n
 
 def decode(w: dict, x_new: np.ndarray, K_cache: np.ndarray, V_cache: np.ndarray,
            dims: Dims = KIMI_K2, eps: float = DEFAULT_EPS, base: float = DEFAULT_ROPE_BASE,
-           scale: float | None = None) -> dict:
+           scale: float | None = None, bf16_storage: bool = False) -> dict:
     """One decode step against the rebuilt per-head cache.
 
     x_new [B, d] is the token at position P = K_cache.shape[2]; K_cache
@@ -265,13 +292,13 @@ def decode(w: dict, x_new: np.ndarray, K_cache: np.ndarray, V_cache: np.ndarray,
         scale = default_scale(dims)
     B = x_new.shape[0]
     P = K_cache.shape[2]
-    t = project_tokens(w, x_new, np.full((B,), P), dims, eps, base, want_q=True)
+    t = project_tokens(w, x_new, np.full((B,), P), dims, eps, base, want_q=True, bf16_storage=bf16_storage)
     O = np.empty((B, dims.H, dims.v))
     for b in range(B):
         for h in range(dims.H):
             K = np.concatenate([K_cache[b, h], t["K"][b, h][None]], axis=0)
             V = np.concatenate([V_cache[b, h], t["V"][b, h][None]], axis=0)
-            O[b, h] = attend(t["Q"][b, h][None], K, V, scale, None)[0]
+            O[b, h] = attend(t["Q"][b, h][None], K, V, scale, None, bf16_storage)[0]
     delta = _linear(O.reshape(B, dims.H * dims.v), w["w_o"])
     return {"out": x_new + delta, "delta": delta, "k_new": t["K"], "v_new": t["V"],
             "ckv_new": t["ckv"], "kpe_new": t["kpe"]}
@@ -329,18 +356,22 @@ def decode_latent(w: dict, x_new: np.ndarray, ckv_cache: np.ndarray, kpe_cache: 
 def decode_latent_absorbed(w: dict, x_new: np.ndarray, ckv_cache: np.ndarray,
                            kpe_cache: np.ndarray, dims: Dims = KIMI_K2,
                            eps: float = DEFAULT_EPS, base: float = DEFAULT_ROPE_BASE,
-                           scale: float | None = None) -> dict:
+                           scale: float | None = None, bf16_storage: bool = False) -> dict:
     """Same step with W_UK / W_UV absorbed (the design the key-value
     compression page attributes to DeepSeek-V2: cache the latent instead of
     per-head K/V).  Used only as an invariant: it equals ``decode_latent`` up
     to float64 rounding, since q.(W_UK c) = (W_UK^T q).c and
     sum_j p_j W_UV c_j = W_UV sum_j p_j c_j.
+    bf16_storage: the absorbed query q_lat, the probabilities, the latent
+    output o_lat and the per-head output are stored in bf16 as well (the
+    steps a bf16 implementation of this form hands on).
     """
     if scale is None:
         scale = default_scale(dims)
     B = x_new.shape[0]
     P = ckv_cache.shape[1]
-    t = project_tokens(w, x_new, np.full((B,), P), dims, eps, base, want_q=True)
+    st = bf16_storage
+    t = project_tokens(w, x_new, np.full((B,), P), dims, eps, base, want_q=True, bf16_storage=st)
     wkvb = w["w_kv_b"].reshape(dims.H, dims.nope + dims.v, dims.kv_lora)
     w_uk, w_uv = wkvb[:, :dims.nope], wkvb[:, dims.nope:]
     O = np.empty((B, dims.H, dims.v))
@@ -348,12 +379,12 @@ def decode_latent_absorbed(w: dict, x_new: np.ndarray, ckv_cache: np.ndarray,
         C = np.concatenate([ckv_cache[b], t["ckv"][b][None]], axis=0)      # [P+1, kv_lora]
         R = np.concatenate([kpe_cache[b], t["kpe"][b][None]], axis=0)      # [P+1, rope]
         for h in range(dims.H):
-            q_lat = w_uk[h].T @ t["Q"][b, h, :dims.nope]
+            q_lat = _stored(w_uk[h].T @ t["Q"][b, h, :dims.nope], st)
             s = (C @ q_lat + R @ t["Q"][b, h, dims.nope:]) * scale
-            p = softmax(s[None])[0]
-            O[b, h] = w_uv[h] @ (p @ C)
+            p = _stored(softmax(s[None])[0], st)
+            O[b, h] = _stored(w_uv[h] @ _stored(p @ C, st), st)
     delta = _linear(O.reshape(B, dims.H * dims.v), w["w_o"])
-    return {"out": x_new + delta, "delta": delta}
+    return {"out": x_new + delta, "delta": delta, "ckv_new": t["ckv"], "kpe_new": t["kpe"]}
 
 
 def fold_wuv_into_wo(w: dict, dims: Dims = KIMI_K2) -> np.ndarray:
@@ -473,15 +504,6 @@ def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
     h = a (.) u."""
     a = g * sigmoid(g)
     return a * u
-
-
-def round_to_bf16(a: np.ndarray) -> np.ndarray:
-    """The nearest bfloat16 value of each float64 (8 significant bits,
-    ties to even), for values in bfloat16's normal range: the storage of a
-    module output in a bf16 model.  a = m 2^e with 1/2 <= |m| < 1; m is
-    rounded to a multiple of 2^-8 (np.round rounds halves to even)."""
-    m, e = np.frexp(np.asarray(a, dtype=np.float64))
-    return np.ldexp(np.round(m * 256.0) / 256.0, e)
 
 
 def ffn(w: dict, xp: np.ndarray, eps: float = DEFAULT_EPS, bf16_products: bool = False) -> dict:

@@ -354,8 +354,8 @@ def test_chunk_mask_without_offset_fails_the_pin(monkeypatch):
     whole = om.prefill(w, x, dims)
     cache = om.cache_from_tokens(w, x[:, :4], dims)
     real_attend = om.attend
-    monkeypatch.setattr(om, "attend", lambda Q, K, V, scale, q_pos: real_attend(
-        Q, K, V, scale, None if q_pos is None else np.asarray(q_pos) - K.shape[0] + Q.shape[0]))
+    monkeypatch.setattr(om, "attend", lambda Q, K, V, scale, q_pos, *rest: real_attend(
+        Q, K, V, scale, None if q_pos is None else np.asarray(q_pos) - K.shape[0] + Q.shape[0], *rest))
     bad = om.prefill_with_past(w, x[:, 4:], cache["K"], cache["V"], dims)
     assert not np.allclose(bad["out"], whole["out"][:, 4:], rtol=1e-6, atol=1e-8)
 
@@ -538,8 +538,8 @@ def test_planted_mistakes_are_caught(monkeypatch):
     monkeypatch.setattr(om, "default_scale", orig_default)
 
     # K and V swapped in the kv_b split
-    def project_swapped(w, x, pos, dims, eps, base, want_q=True):
-        r = orig_project(w, x, pos, dims, eps, base, want_q)
+    def project_swapped(w, x, pos, dims, eps, base, want_q=True, bf16_storage=False):
+        r = orig_project(w, x, pos, dims, eps, base, want_q, bf16_storage)
         if dims.nope == dims.v:
             r["V"] = r["K"][..., :dims.nope].copy()
         else:
@@ -550,3 +550,59 @@ def test_planted_mistakes_are_caught(monkeypatch):
     assert not _pins_pass()
     monkeypatch.setattr(om, "project_tokens", orig_project)
     assert _pins_pass()
+
+
+# ---------------------------------------------------------------------------
+# the bf16-storage reading (activations handed on, probabilities and the
+# attention output stored in bf16)
+# ---------------------------------------------------------------------------
+def _bf16_exact(a):
+    return np.array_equal(om.round_to_bf16(a), a)
+
+
+def _storage_cases(dims, seed):
+    w = rand_weights(dims, seed)
+    x = rand_x((2, 6, dims.d), seed + 1)
+    xn = rand_x((2, dims.d), seed + 2)
+    c = om.cache_from_tokens(w, x, dims)
+    return [
+        ("prefill", lambda st: om.prefill(w, x, dims, bf16_storage=st)),
+        ("chunk", lambda st: om.prefill_with_past(w, x[:, 4:], c["K"][:, :, :4], c["V"][:, :, :4], dims,
+                                                  bf16_storage=st)),
+        ("decode", lambda st: om.decode(w, xn, c["K"], c["V"], dims, bf16_storage=st)),
+        ("absorbed", lambda st: om.decode_latent_absorbed(w, xn, c["ckv"], c["kpe"], dims, bf16_storage=st)),
+    ]
+
+
+def test_bf16_storage_only_adds_rounding(monkeypatch):
+    """With the rounding made the identity, the bf16-storage reading is the
+    exact computation term for term; with it, every stored tensor the call
+    returns holds bf16 values and the result stays within bf16-level
+    distance of the exact one."""
+    for name, run in _storage_cases(TINY2, 81):
+        exact = run(False)
+        st = run(True)
+        d = st["delta"] - exact["delta"]
+        rel = np.linalg.norm(d) / np.linalg.norm(exact["delta"])
+        assert 1e-6 < rel < 2e-2, (name, rel)
+        for k in ("K", "V", "ckv", "kpe", "ckv_new", "kpe_new"):
+            if k in st:
+                assert _bf16_exact(st[k]), (name, k)
+    monkeypatch.setattr(om, "round_to_bf16", lambda a: np.asarray(a, dtype=np.float64))
+    for name, run in _storage_cases(TINY2, 81):
+        np.testing.assert_allclose(run(True)["delta"], run(False)["delta"], rtol=1e-12, atol=1e-14, err_msg=name)
+
+
+def test_bf16_storage_rounds_probabilities_before_pv():
+    """attend with bf16 storage: P cast to bf16 before P V and the output
+    stored in bf16 (the page's cast of the float32 softmax to the query
+    dtype).  A case where P is exactly representable (two equal scores, one
+    masked) leaves only the output rounding."""
+    Q = np.array([[1.0, 0.0]])
+    K = np.array([[1.0, 0.0], [1.0, 0.0], [5.0, 0.0]])
+    V = np.array([[1.0 + 2.0 ** -8, 3.0], [1.0, 1.0], [7.0, 7.0]])
+    o = om.attend(Q, K, V, 1.0, np.array([1]), bf16_storage=True)       # keys 0, 1 visible, P = (1/2, 1/2)
+    np.testing.assert_array_equal(o, om.round_to_bf16(np.array([[1.0 + 2.0 ** -9, 2.0]])))
+    np.testing.assert_array_equal(o, np.array([[1.0, 2.0]]))              # 1 + 2^-9 rounds to 1
+    p3 = om.attend(np.array([[0.0, 0.0]]), K, np.eye(3)[:, :2], 1.0, None, bf16_storage=True)
+    np.testing.assert_array_equal(p3, om.round_to_bf16(np.array([[1.0 / 3.0, 1.0 / 3.0]])))
