@@ -6,9 +6,17 @@ Full Kimi K2 sizes (d = 7168, I = 18,432); seeded synthetic inputs from
 ``synth`` on both sides.  Row counts cover every tile configuration of the
 gate/up product: M <= 64 (decode-size tiles), M <= 128, an odd number of
 128-row blocks (single-CTA tiles, ragged last block) and an even number
-above 256 (CTA-pair tiles).  Tolerance: ``parity_scaled`` (the 2e-2 element
-bound relative to the output's RMS where that exceeds 1, relative
-Frobenius <= 1e-2), plus half a bf16 ulp of |out| for the stored output.
+above 256 (CTA-pair tiles).
+
+Tolerance: the element bound 2e-2 max(1, RMS(ref)) (``parity_scaled``)
+and relative Frobenius 1e-2 against the exact float64 oracle, plus half a
+bf16 unit of the stored value for the stored output.  The bare 2e-2 cannot
+hold for any bf16 implementation: storing x_ffn and h in bf16 alone moves
+Delta_ffn by more than that at full size (tests/test_oracle_ffn.py shows it
+on the CPU).  Against the oracle's bf16-products reading
+(``ffn(bf16_products=True)``, those two roundings made) the GPU is also held
+to relative Frobenius 1e-3, ten times below the stated bound; what remains
+is one-unit rounding flips of h (measured about 3e-4).
 """
 import numpy as np
 import pytest
@@ -48,14 +56,16 @@ def test_ffn_parity(WF, n):
     x64, out, delta = run_ffn(WF, n)
     ref = om.ffn(WF[2], x64)
     parity_scaled(cuda_to_f64(delta), ref["delta"], f"Delta_ffn n={n}")
-    parity_scaled(cuda_to_f64(out), ref["out"], f"out n={n}", ulp_rel=OUT_ULP_REL)
+    parity_scaled(cuda_to_f64(out), ref["out"], f"out n={n}", ulp_rel=OUT_ULP_REL, stored_bf16=True)
+    ref_b = om.ffn(WF[2], x64, bf16_products=True)
+    parity_scaled(cuda_to_f64(delta), ref_b["delta"], f"Delta_ffn n={n} (bf16 products)", rel_fro=1e-3)
 
 
 def test_ffn_in_place(WF):
     n = 70
     x64, out, delta = run_ffn(WF, n, inplace=True)
     ref = om.ffn(WF[2], x64)
-    parity_scaled(cuda_to_f64(out), ref["out"], "out (in place)", ulp_rel=OUT_ULP_REL)
+    parity_scaled(cuda_to_f64(out), ref["out"], "out (in place)", ulp_rel=OUT_ULP_REL, stored_bf16=True)
     parity_scaled(cuda_to_f64(delta), ref["delta"], "Delta_ffn (in place)")
 
 
@@ -68,7 +78,9 @@ def test_ffn_b1_t2048_sampled_rows(WF):
     xr = synth.bf16_bits_to_f64(synth.tensor_bits(0, "ffn_x", (n, D), synth.X_DIST, rows=rows))
     ref = om.ffn(WF[2], xr)
     parity_scaled(cuda_to_f64(delta[rows]), ref["delta"], "Delta_ffn sampled rows")
-    parity_scaled(cuda_to_f64(out[rows]), ref["out"], "out sampled rows", ulp_rel=OUT_ULP_REL)
+    parity_scaled(cuda_to_f64(out[rows]), ref["out"], "out sampled rows", ulp_rel=OUT_ULP_REL, stored_bf16=True)
+    ref_b = om.ffn(WF[2], xr, bf16_products=True)
+    parity_scaled(cuda_to_f64(delta[rows]), ref_b["delta"], "Delta_ffn sampled rows (bf16 products)", rel_fro=1e-3)
 
 
 def test_dense_block_prefill(WF):
@@ -87,7 +99,7 @@ def test_dense_block_prefill(WF):
     m.mla_ffn(WF[1], mid, mid, m.alloc_workspace(m.MODE_FFN, B, T))
     torch.cuda.synchronize()
     ref = om.dense_block_prefill(oracle_weights(0), WF[2], synth.bf16_bits_to_f64(xb))
-    parity(cuda_to_f64(x_mid), ref["x_mid"], "x' (attention half)", ulp_rel=OUT_ULP_REL)
+    parity(cuda_to_f64(x_mid), ref["x_mid"], "x' (attention half)", ulp_rel=OUT_ULP_REL, stored_bf16=True)
     # The MLP half's own element-wise bound holds on identical inputs
     # (test_ffn_parity).  In the composition its input x' differs from the
     # oracle's by the attention half's error (within the bound above), which
@@ -96,3 +108,8 @@ def test_dense_block_prefill(WF):
     d = cuda_to_f64(mid) - ref["out"]
     rel = np.linalg.norm(d) / np.linalg.norm(ref["out"])
     assert np.all(np.isfinite(d)) and rel <= 1e-2, f"block: relative Frobenius {rel:.3e}"
+    # element by element: the block's output against the oracle's MLP half
+    # applied to the GPU's own x' (the MLP half's tolerance)
+    ref_mlp = om.ffn(WF[2], cuda_to_f64(x_mid))
+    parity_scaled(cuda_to_f64(mid), ref_mlp["out"], "block out = MLP(x' of the GPU)", ulp_rel=OUT_ULP_REL,
+                  stored_bf16=True)

@@ -43,8 +43,11 @@ def test_fold_rows(FOLD):
     parity_cache(cuda_to_f64(wf[rows]), ref, "W_fold rows")
 
 
-@pytest.mark.parametrize("B,P", [(3, 37), (2, 0), (100, 129)])
+@pytest.mark.parametrize("B,P", [(3, 37), (2, 0), (100, 129), (130, 20)])
 def test_decode_latent_folded_parity(FOLD, B, P):
+    """B = 130 takes the front end for more than 128 rows (the q_b TMA-store
+    epilogue and the separate q^pe copy) and the folded product's M > 128
+    tiles over K = 32768."""
     import torch
     W, wf = FOLD
     cap = P + 3
