@@ -384,6 +384,10 @@ int mla_ffn(const mla_ffn_weights_t* w, const mla_params_t* params, const void* 
  * gave up (the kernel then skipped its remaining work and returned), or
  * MLA_ERR_INVALID_ARG if a per-sequence position of a _varlen call was
  * outside [0, P_max].
+ * The word describes one call only: every entry point clears it (and the
+ * rest of the status region) on its stream before its first kernel, so a
+ * caller that needs the status of a call must read it before enqueueing the
+ * next call on the same workspace.
  * MLA_ERR_CUDA if the synchronisation itself fails. */
 int mla_device_status(const void* workspace, void* stream);
 

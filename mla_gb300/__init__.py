@@ -99,9 +99,6 @@ _SIGS = {
                             _VP, _SZ, _VP]),
     "mla_device_status": (_I, [_VP, _VP]),
     "mla_status_string": (ctypes.c_char_p, [_I]),
-    "mla_debug_gemm": (_I, [_VP, _I, _VP, _I, _I, _VP, _I, _I, _I, _I, _VP]),
-    "mla_debug_wait_timeout": (_I, [_VP, ctypes.c_uint64, _VP]),
-    "mla_debug_umma_probe": (_I, [_VP, _I, _VP]),
 }
 
 
@@ -352,21 +349,3 @@ def mla_device_status(workspace, stream=None) -> int:
 
 def mla_status_string(status: int) -> str:
     return lib().mla_status_string(status).decode()
-
-
-# ---- test hooks (include/mla_debug.h) -------------------------------------
-def mla_debug_gemm(A, B, C, b_mn_major=False, stream=None):
-    """C = A @ B^T (B [N, K]) or A @ B (B [K, N] when b_mn_major)."""
-    M, K = A.shape
-    N = B.shape[0] if not b_mn_major else B.shape[1]
-    rc = lib().mla_debug_gemm(_ptr(A), A.stride(0), _ptr(B), B.stride(0), int(b_mn_major), _ptr(C), C.stride(0),
-                              M, N, K, _stream(stream))
-    _check(rc, "mla_debug_gemm")
-
-
-def mla_debug_wait_timeout(status_word, limit_ns: int, stream=None):
-    _check(lib().mla_debug_wait_timeout(_ptr(status_word), limit_ns, _stream(stream)), "mla_debug_wait_timeout")
-
-
-def mla_debug_umma_probe(out, m: int, stream=None):
-    _check(lib().mla_debug_umma_probe(_ptr(out), m, _stream(stream)), "mla_debug_umma_probe")

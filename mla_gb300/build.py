@@ -1,7 +1,9 @@
 """Build step: compile the CUDA sources for sm_103a into in-tree shared libraries.
 
-  mla_gb300/libmla.so     the MLA library (csrc/*.cu), C ABI in include/mla.h
-  synth/libmlasynth.so    the seeded input generator's GPU copy
+  mla_gb300/libmla.so          the MLA library (csrc/*.cu), C ABI in include/mla.h
+  synth/libmlasynth.so         the seeded input generator's GPU copy
+  tests/hooks/libmla_debug.so  test-only: the library's objects plus the test
+                               hooks of tests/hooks/mla_debug.h
 
 Translation units compile in parallel; only nvcc and the CUDA runtime
 (statically linked) are needed, so the same step runs on the x86 dev host
@@ -22,6 +24,8 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmla.so")
 SYNTH_SRC = os.path.join(ROOT, "synth", "synth.cu")
 SYNTH_LIB = os.path.join(ROOT, "synth", "libmlasynth.so")
+HOOKS_SRC = os.path.join(ROOT, "tests", "hooks", "mla_debug_hooks.cu")
+HOOKS_LIB = os.path.join(ROOT, "tests", "hooks", "libmla_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -66,6 +70,10 @@ def build(verbose: bool = False, ptxas_verbose: bool = False) -> None:
         if _stale(obj, [src] + headers) or ptxas_verbose:
             extra = ["-Xptxas", "-v"] if ptxas_verbose else []
             jobs.append([cc, *ARCH, *CFLAGS, *extra, "-c", src, "-o", obj])
+    hooks_obj = os.path.join(BUILD, "mla_debug_hooks.o")
+    hooks_deps = [HOOKS_SRC, os.path.join(ROOT, "tests", "hooks", "mla_debug.h")] + headers
+    if os.path.exists(HOOKS_SRC) and (_stale(hooks_obj, hooks_deps) or ptxas_verbose):
+        jobs.append([cc, *ARCH, *CFLAGS, "-c", HOOKS_SRC, "-o", hooks_obj])
     synth_job = None
     if _stale(SYNTH_LIB, [SYNTH_SRC]):
         synth_job = [cc, *ARCH, *CFLAGS, "-shared", SYNTH_SRC, "-o", SYNTH_LIB]
@@ -77,6 +85,8 @@ def build(verbose: bool = False, ptxas_verbose: bool = False) -> None:
                     print(out)
     if jobs or _stale(LIB, objs):
         _run([cc, *ARCH, "-shared", "-o", LIB, *objs])
+    if os.path.exists(HOOKS_SRC) and (jobs or _stale(HOOKS_LIB, objs + [hooks_obj])):
+        _run([cc, *ARCH, "-shared", "-o", HOOKS_LIB, *objs, hooks_obj])
 
 
 if __name__ == "__main__":

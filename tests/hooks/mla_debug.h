@@ -1,8 +1,10 @@
 /*
- * mla_debug.h -- test hooks of libmla.so (not part of the MLA operation).
+ * mla_debug.h -- test hooks (not part of the MLA operation, not in libmla.so).
  *
- * These entry points let the test-suite exercise single kernels of the
- * library in isolation: the tcgen05 GEMM used by every projection, the
+ * They live in a test-only library, tests/hooks/libmla_debug.so, linked from
+ * the same compiled kernels as libmla.so plus mla_debug_hooks.cu, so that the
+ * product library ships no test entry points.  They let the test-suite
+ * exercise single kernels of the library in isolation: the tcgen05 GEMM used by every projection, the
  * bounded device-side wait that turns a missing arrival into an error status
  * instead of a hang, and a layout check of the tensor-memory accumulator.
  * Same conventions as mla.h: device pointers, asynchronous on `stream`,

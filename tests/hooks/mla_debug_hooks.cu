@@ -1,9 +1,10 @@
-// Test hooks (include/mla_debug.h): single kernels of the library exposed so
-// that the test-suite can check them in isolation.
-#include "common.cuh"
-#include "internal.h"
+// Test hooks (mla_debug.h): single kernels of the library exposed so that the
+// test-suite can check them in isolation.  Linked into the test-only
+// libmla_debug.so with the library's own objects; libmla.so does not carry them.
+#include "../../mla_gb300/csrc/common.cuh"
+#include "../../mla_gb300/csrc/internal.h"
 #include "../../include/mla.h"
-#include "../../include/mla_debug.h"
+#include "mla_debug.h"
 
 namespace mla {
 namespace {

@@ -13,10 +13,11 @@ import mla_gb300 as m
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def declared_functions():
+def declared_functions(headers=None):
     names = []
-    for h in ("mla.h", "mla_debug.h"):
-        src = open(os.path.join(ROOT, "include", h)).read()
+    for h in headers or [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+                         if f.endswith(".h")]:
+        src = open(h).read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
         names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s+\*?([a-z_][a-z0-9_]*)\s*\(", src, re.M)
     return sorted(set(names))
@@ -28,6 +29,18 @@ def test_library_exports_every_declared_function():
     assert "mla_prefill" in names and "mla_decode_latent" in names and len(names) >= 9
     for n in names:
         assert hasattr(lib, n), f"{n} not exported"
+
+
+def test_product_library_carries_no_test_hooks_and_hooks_library_exports_them():
+    import mla_hooks
+    hooks = declared_functions([os.path.join(ROOT, "tests", "hooks", "mla_debug.h")])
+    assert hooks == ["mla_debug_gemm", "mla_debug_umma_probe", "mla_debug_wait_timeout"]
+    lib = m.lib()
+    for n in hooks:
+        assert not hasattr(lib, n), f"{n} exported by libmla.so"
+    hl = mla_hooks.lib()
+    for n in hooks:
+        assert hasattr(hl, n), f"{n} not exported by the hooks library"
 
 
 def test_status_strings():

@@ -4,7 +4,7 @@ device wait that reports a timeout instead of hanging."""
 import numpy as np
 import pytest
 
-import mla_gb300 as m
+import mla_hooks as m
 
 pytestmark = pytest.mark.gpu
 
