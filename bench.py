@@ -1,12 +1,18 @@
 """Benchmark of the GB300 MLA sublayer (one JSON line on stdout, rank 0).
 
-Headline step: causal prefill of B=1, T=2048 tokens (Kimi K2 MLA dims) with
-seeded synthetic inputs already resident in HBM; metric = tokens/s.  The same
-line carries the decode workloads of the metric (rebuilt cache B=64, P=1000;
-latent cache B=128, P=8192) and the large prefill (B=8, T=4096) as
-sub-objects, a roofline entry for the step's dominant kernel, an end-to-end
-number through the C ABI with host buffers, the CPU-oracle baseline, the GPU
-clocks seen during the timed region and the number of kernel launches.
+Headline step: causal prefill of B=8 sequences of T=4096 tokens (Kimi K2
+MLA dims) that also writes both cache forms (rebuilt per-head K/V and the
+576-value latent cache), with seeded synthetic inputs already resident in
+HBM; metric = tokens/s.  The same line carries the other workloads of the
+metric as sub-objects -- prefill B=1 T=2048, prefill B=1 T=16 (weight-bound),
+decode on the rebuilt cache B=64 P=1000 and on the latent cache B=128
+P=8192 -- and the widened rows (chunked prefill, FP8 weights, ragged and
+folded decode, the MLP half, the dense block), a roofline entry for each
+dominant kernel, an end-to-end number through the C ABI with host buffers,
+the CPU-oracle baseline, the GPU clocks seen during the timed region and the
+number of kernel launches.  A compact "summary" of every configuration ends
+the line; each configuration's summary is also printed to stderr as it
+finishes.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--quick]
 
@@ -31,6 +37,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MLA prefill tokens/s (% bf16 TC peak); decode step µs & HBM GB/s (% of 8 TB/s)"
+WORKLOAD = "mla_prefill B=8 T=4096 causal, writes rebuilt K/V and latent caches (Kimi K2 MLA dims)"
 NOMINAL_HBM_GBS = 8000.0
 D, H, QL, KVL, NOPE, ROPE, QK, V = 7168, 64, 1536, 512, 128, 64, 192, 128
 FFN_I = 18432  # SwiGLU MLP width
@@ -478,20 +485,27 @@ def roofline_entry(stage_ms, mode, B, TP, pk, config_name, past=0):
     return {"kernel": name, "bound": None, "ms": ms}
 
 
+def note(summary, key):
+    """One configuration's compact numbers on stderr as soon as they exist
+    (stdout carries the one JSON line)."""
+    print(json.dumps({key: summary[key]}), file=sys.stderr, flush=True)
+
+
 def _stages_out(stage_ms):
     return {k: round(v, 4) for k, v in stage_ms.items() if not k.startswith("_")}
 
 
 def cpu_oracle_prefill_sample(n_tokens):
-    """The oracle (float64 numpy) on the first n_tokens of the B=1, T=2048
-    workload; returns (tokens/s, seconds, threads)."""
-    import numpy as np
+    """The oracle (float64 numpy) on the first n_tokens of sequence 0 of the
+    headline B=8, T=4096 workload (causal: those rows are the same
+    computation as in the whole step), caches included; returns (tokens/s,
+    seconds, threads)."""
     import synth
     from oracle import mla_oracle as om
     names = {"w_in_norm": "g_in", "w_q_a": "w_q_a", "w_q_a_norm": "g_qa", "w_q_b": "w_q_b",
              "w_kv_a": "w_kv_a", "w_kv_a_norm": "g_kva", "w_kv_b": "w_kv_b", "w_o": "w_o"}
     W = {names[n]: synth.bf16_bits_to_f64(b) for n, b in synth.weight_bits(0).items()}
-    x = synth.bf16_bits_to_f64(synth.tensor_bits(0, "x", (1, 2048, D), synth.X_DIST, rows=[0]))[:, :n_tokens]
+    x = synth.bf16_bits_to_f64(synth.tensor_bits(0, "x", (8, 4096, D), synth.X_DIST, rows=[0]))[:, :n_tokens]
     t0 = time.perf_counter()
     om.prefill(W, x)
     dt = time.perf_counter() - t0
@@ -506,27 +520,32 @@ def cpu_oracle_prefill_sample(n_tokens):
     return n_tokens / dt, dt, threads
 
 
+def cpu_sample_text(n):
+    return (f"the first {n} tokens of sequence 0 of the B=8 T=4096 prefill (causal; its caches included), "
+            "float64 numpy oracle")
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if ws > 1 and rank != 0:
         return
-    n = args.cpu_tokens
+    n = args.ref_tokens
     times = []
     for _ in range(args.warmup):
         cpu_oracle_prefill_sample(n)
+    threads = os.cpu_count()
     for _ in range(args.steps):
         v, dt, threads = cpu_oracle_prefill_sample(n)
         times.append(dt)
     mean_s = statistics.mean(times)
     value = n / mean_s
-    sample = (f"first {n} of the 2048 tokens of the B=1 T=2048 prefill (causal), float64 numpy oracle"
-              if n < 2048 else "the whole B=1 T=2048 prefill (causal), float64 numpy oracle")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_s * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "mla_prefill B=1 T=2048 (sampled)", "global_batch": 1, "seq_len": 2048},
+            "config": {"workload": WORKLOAD, "global_batch": 8 * ws, "seq_len": 4096,
+                       "parallelism": f"replica{ws}" if ws > 1 else "single"},
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                             "sample": sample},
+                             "sample": cpu_sample_text(n) + " per step"},
             "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -577,8 +596,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline prefill only")
-    ap.add_argument("--cpu-tokens", type=int, default=2048,
-                    help="tokens of the headline sequence the CPU oracle baseline runs (0 = skip)")
+    ap.add_argument("--cpu-tokens", type=int, default=4096,
+                    help="tokens of the headline's sequence 0 the CPU oracle baseline runs (0 = skip)")
+    ap.add_argument("--ref-tokens", type=int, default=1024,
+                    help="tokens of the headline's sequence 0 each step of --impl reference runs")
     ap.add_argument("--profile", default=None,
                     help="run one step of one configuration for a profiler and exit: prefill_bB_tT[_cache], "
                          "chunk_bB_pP0_tT / chunk_latent_bB_pP0_tT (chunked prefill on either cache), ffn_nN (MLP half, N rows), "
@@ -604,10 +625,11 @@ def main():
     pk = peaks()
     r = Runner(dev)
     K, W = args.steps, max(args.warmup, 3)
+    summary = {}
 
-    # ---- headline: prefill B=1, T=2048 ----------------------------------------
-    B, T = 1, 2048
-    x, out, ws, caches = r.prefill_setup(B, T, with_cache=False)
+    # ---- headline: prefill B=8, T=4096 writing both caches -----------------------
+    B, T = 8, 4096
+    x, out, ws, caches = r.prefill_setup(B, T, with_cache=True)
     step = r.prefill_step_fn(x, out, ws, caches, T)
     if world > 1:
         torch.distributed.barrier()
@@ -620,28 +642,34 @@ def main():
     tok = B * T
     value = weak_scaling_value(tok, world, ms_step)
     flops = tok * proj_flops_per_token() + prefill_attn_flops(B, T)
-    roof = roofline_entry(stage_ms, "prefill", B, T, pk, "prefill_b1_t2048")
+    roof = roofline_entry(stage_ms, "prefill", B, T, pk, "prefill_b8_t4096")
 
-    # end to end: pinned host x -> device, call, device -> pinned host out
+    # end to end: pinned host x -> device, the call (caches stay resident in
+    # HBM as a serving engine keeps them), device -> pinned host out
     xh = x.cpu().pin_memory()
     oh = torch.empty_like(xh).pin_memory()
     xd = torch.empty_like(x)
 
     def e2e_step(timing):
         xd.copy_(xh, non_blocking=True)
-        r.m.mla_prefill(r.W, xd, out, ws, *caches, 0, None)
+        r.m.mla_prefill(r.W, xd, out, ws, *caches, T, None)
         oh.copy_(out, non_blocking=True)
     e2e_ms, _, _ = r.time_steps(e2e_step, K, W, with_stages=False)
     e2e_ms = barrier_max(statistics.mean(e2e_ms))
+    tf = flops / (ms_step * 1e-3) / 1e12
+    summary["C5"] = {"cfg": "prefill B=8 T=4096 +caches", "ms": round(ms_step, 4), "tok_s": round(value, 1),
+                     "tflops": round(tf, 1), "frac_bf16": round(tf / pk["bf16_tflops"], 4),
+                     "e2e_tok_s": round(world * tok / (e2e_ms * 1e-3), 1)}
+    note(summary, "C5")
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64 / Irwin-Hall inputs)",
-            "config": {"workload": "mla_prefill B=1 T=2048 causal (Kimi K2 MLA dims)", "global_batch": B * world,
-                       "seq_len": T, "parallelism": f"replica{world}" if world > 1 else "single",
-                       "l2": "flushed between timed steps (512 MB write)"},
-            "tflops": round(flops / (ms_step * 1e-3) / 1e12, 2),
-            "frac_bf16_peak": round(flops / (ms_step * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded splitmix64 / Box-Muller N(0,1) inputs, N(0,0.02) weights)",
+            "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": T,
+                       "parallelism": f"replica{world}" if world > 1 else "single",
+                       "l2": "inputs (470 MB) larger than L2, and L2 flushed between timed steps (512 MB write)"},
+            "tflops": round(tf, 2), "frac_bf16_peak": round(tf / pk["bf16_tflops"], 4),
             "stage_ms": _stages_out(stage_ms),
             "roofline": roof, "gpu_launches": launches * K,
             "stage_ms_note": "per-stage times from a separate instrumented pass (events around every stage)",
@@ -652,6 +680,7 @@ def main():
     del x, out, ws, caches, xh, oh, xd
     torch.cuda.empty_cache()
 
+    launches_c2 = 0
     if not args.quick:
         ks = max(3, min(K, 10))
         # ---- decode, rebuilt per-head cache: B=64, P=1000 ----------------------
@@ -668,6 +697,11 @@ def main():
                 "frac_measured_hbm": round(byts / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
                 "algorithmic_bytes": byts, "stage_ms": _stages_out(st3),
                 "roofline": roofline_entry(st3, "decode", B3, P3, pk, "decode_b64_p1000"), "launches": l3}
+            summary["C3"] = {"cfg": "decode B=64 P=1000 rebuilt", "us": round(us, 2),
+                             "hbm_gbs": line["decode_rebuilt"]["hbm_gbs"],
+                             "frac_8tbs": line["decode_rebuilt"]["frac_8tbs"],
+                             "attn_frac_measured": (line["decode_rebuilt"]["roofline"] or {}).get("frac")}
+            note(summary, "C3")
             del step3, keep
             torch.cuda.empty_cache()
         except Exception as e:  # report, keep the headline
@@ -686,6 +720,11 @@ def main():
                 "frac_measured_hbm": round(byts / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
                 "algorithmic_bytes": byts, "stage_ms": _stages_out(st4),
                 "roofline": roofline_entry(st4, "latent", B4, P4, pk, "latent_b128_p8192"), "launches": l4}
+            summary["C4"] = {"cfg": "decode B=128 P=8192 latent", "us": round(us, 2),
+                             "hbm_gbs": line["decode_latent"]["hbm_gbs"],
+                             "frac_8tbs": line["decode_latent"]["frac_8tbs"],
+                             "attn_frac_measured": (line["decode_latent"]["roofline"] or {}).get("frac")}
+            note(summary, "C4")
             del step4, keep
             torch.cuda.empty_cache()
         except Exception as e:
@@ -728,6 +767,9 @@ def main():
                 "us_per_step": round(us, 2), "hbm_gbs": round(byts / (us * 1e-6) / 1e9, 1),
                 "frac_measured_hbm": round(byts / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
                 "algorithmic_bytes": byts, "weight_bytes": wbytes, "stage_ms": _stages_out(st3f), "launches": l3f}
+            summary["C3_fp8"] = {"cfg": "decode B=64 P=1000 rebuilt, FP8 weights", "us": round(us, 2),
+                                 "o_proj_us": round(st3f.get("o_proj", 0.0) * 1e3, 1)}
+            note(summary, "C3_fp8")
             del WQ, keepw, kc, vc, x3, o3, ws3
             torch.cuda.empty_cache()
         except Exception as e:
@@ -751,25 +793,59 @@ def main():
             torch.cuda.empty_cache()
         except Exception as e:
             line["decode_latent_ragged"] = {"error": repr(e)[:300]}
-        # ---- prefill B=8, T=4096 writing both caches -------------------------------
+        # ---- prefill B=1, T=2048 (no caches) ------------------------------------------
         try:
-            B5, T5 = 8, 4096
-            x5, out5, ws5, c5 = r.prefill_setup(B5, T5, with_cache=True)
-            step5 = r.prefill_step_fn(x5, out5, ws5, c5, T5)
-            ms5, st5, l5 = r.time_steps(step5, max(2, min(ks, 5)), 2, stages=PREFILL_STAGES)
-            ms5 = barrier_max(statistics.mean(ms5))
-            fl5 = B5 * T5 * proj_flops_per_token() + prefill_attn_flops(B5, T5)
-            line["prefill_large"] = {
-                "workload": "mla_prefill B=8 T=4096 causal, writes rebuilt K/V and latent caches",
-                "ms_per_step": round(ms5, 3), "tokens_per_s": round(world * B5 * T5 / (ms5 * 1e-3), 1),
-                "tflops": round(fl5 / (ms5 * 1e-3) / 1e12, 2),
-                "frac_bf16_peak": round(fl5 / (ms5 * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
-                "stage_ms": _stages_out(st5),
-                "roofline": roofline_entry(st5, "prefill", B5, T5, pk, "prefill_b8_t4096"), "launches": l5}
-            del x5, out5, ws5, c5
+            B2, T2 = 1, 2048
+            x2, out2, ws2, c2 = r.prefill_setup(B2, T2, with_cache=False)
+            step2 = r.prefill_step_fn(x2, out2, ws2, c2, T2)
+            ms2, st2, l2 = r.time_steps(step2, ks, W, stages=PREFILL_STAGES)
+            launches_c2 = l2
+            ms2 = barrier_max(statistics.mean(ms2))
+            fl2 = B2 * T2 * proj_flops_per_token() + prefill_attn_flops(B2, T2)
+            tf2 = fl2 / (ms2 * 1e-3) / 1e12
+            line["prefill_b1_t2048"] = {
+                "workload": "mla_prefill B=1 T=2048 causal (no caches)",
+                "ms_per_step": round(ms2, 4), "tokens_per_s": round(world * B2 * T2 / (ms2 * 1e-3), 1),
+                "tflops": round(tf2, 2), "frac_bf16_peak": round(tf2 / pk["bf16_tflops"], 4),
+                "stage_ms": _stages_out(st2),
+                "roofline": roofline_entry(st2, "prefill", B2, T2, pk, "prefill_b1_t2048"), "launches": l2}
+            summary["C2"] = {"cfg": "prefill B=1 T=2048", "ms": round(ms2, 4),
+                             "tok_s": line["prefill_b1_t2048"]["tokens_per_s"], "tflops": round(tf2, 1),
+                             "frac_bf16": round(tf2 / pk["bf16_tflops"], 4),
+                             "attn_ms": round(st2.get("attn", 0.0), 4)}
+            note(summary, "C2")
+            del x2, out2, ws2, c2
             torch.cuda.empty_cache()
         except Exception as e:
-            line["prefill_large"] = {"error": repr(e)[:300]}
+            line["prefill_b1_t2048"] = {"error": repr(e)[:300]}
+        # ---- prefill B=1, T=16: the weights stream once (HBM-bound) --------------------
+        try:
+            B1, T1 = 1, 16
+            x1, out1, ws1, c1 = r.prefill_setup(B1, T1, with_cache=False)
+            step1 = r.prefill_step_fn(x1, out1, ws1, c1, T1)
+            ms1, st1, l1 = r.time_steps(step1, max(ks, 10), W, stages=PREFILL_STAGES)
+            us1 = barrier_max(statistics.mean(ms1)) * 1e3
+            fl1 = B1 * T1 * proj_flops_per_token() + prefill_attn_flops(B1, T1)
+            by1 = WEIGHT_BYTES + 2 * B1 * T1 * D * 2
+            gbs1 = by1 / (us1 * 1e-6) / 1e9
+            tf1 = fl1 / (us1 * 1e-6) / 1e12
+            line["prefill_b1_t16"] = {
+                "workload": "mla_prefill B=1 T=16 causal (no caches): every weight byte read once for 16 tokens",
+                "us_per_step": round(us1, 2), "tokens_per_s": round(world * B1 * T1 / (us1 * 1e-6), 1),
+                "hbm_gbs": round(gbs1, 1), "frac_8tbs": round(gbs1 / NOMINAL_HBM_GBS, 4),
+                "frac_measured_hbm": round(gbs1 / pk["hbm_gbs"], 4), "algorithmic_bytes": by1,
+                "tflops": round(tf1, 2), "frac_bf16_peak": round(tf1 / pk["bf16_tflops"], 4),
+                "frac_bf16_peak_note": "meaningless here: 16 flop per weight byte, the step is bound by HBM",
+                "stage_ms": _stages_out(st1), "launches": l1}
+            summary["C1"] = {"cfg": "prefill B=1 T=16", "us": round(us1, 2),
+                             "tok_s": line["prefill_b1_t16"]["tokens_per_s"], "hbm_gbs": round(gbs1, 1),
+                             "frac_8tbs": round(gbs1 / NOMINAL_HBM_GBS, 4),
+                             "frac_bf16": round(tf1 / pk["bf16_tflops"], 4), "tc_note": "meaningless (HBM-bound)"}
+            note(summary, "C1")
+            del x1, out1, ws1, c1
+            torch.cuda.empty_cache()
+        except Exception as e:
+            line["prefill_b1_t16"] = {"error": repr(e)[:300]}
         # ---- chunked prefill: B=1, 2048 tokens after 2048 cached positions ----------
         try:
             B6, P6, T6 = 1, 2048, 2048
@@ -876,13 +952,14 @@ def main():
             step9, keep = r.block_step_fn(B9, T9)
             ms9, st9, _ = r.time_steps(step9, ks, W, stages=PREFILL_STAGES + FFN_STAGES)
             ms9 = barrier_max(statistics.mean(ms9))
-            fl9 = flops + 3 * 2 * B9 * T9 * D * FFN_I
+            fl9 = (B9 * T9 * proj_flops_per_token() + prefill_attn_flops(B9, T9)
+                   + 3 * 2 * B9 * T9 * D * FFN_I)
             line["dense_block_prefill"] = {
                 "workload": "dense block B=1 T=2048: mla_prefill (causal MLA + residual) then mla_ffn (in place)",
                 "ms_per_step": round(ms9, 4), "tokens_per_s": round(world * B9 * T9 / (ms9 * 1e-3), 1),
                 "tflops": round(fl9 / (ms9 * 1e-3) / 1e12, 2),
                 "frac_bf16_peak": round(fl9 / (ms9 * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
-                "stage_ms": _stages_out(st9), "launches": launches + l_ffn}
+                "stage_ms": _stages_out(st9), "launches": launches_c2 + l_ffn}
             del step9, keep
             torch.cuda.empty_cache()
         except Exception as e:
@@ -892,8 +969,9 @@ def main():
     if world == 1 and args.cpu_tokens > 0:
         v, dt, threads = cpu_oracle_prefill_sample(args.cpu_tokens)
         line["cpu_baseline"] = {"value": round(v, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                                "sample": f"first {args.cpu_tokens} of the 2048 tokens of the headline prefill "
-                                          f"(causal; 2048 = the whole step), float64 numpy oracle, {dt:.1f} s"}
+                                "sample": cpu_sample_text(args.cpu_tokens) + f", {dt:.1f} s"}
+    # the per-configuration numbers again, compact, at the end of the line
+    line["summary"] = summary
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
