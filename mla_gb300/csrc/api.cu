@@ -92,7 +92,10 @@ Layout make_layout(int mode, int B, int t_or_p, int num_sms, int cap = 0) {
     L.plan = take(latent_plan_ints(rows, g) * sizeof(int));
     if (absorbed) L.pos = take(n * sizeof(int));
   }
-  if (!pre) {
+  // split-K slots for the small-M projections: decode, and prefill of at
+  // most 128 tokens (whose weight-streaming GEMMs have too few tiles to fill
+  // the GPU otherwise)
+  if (!pre || n <= 128) {
     L.split_bytes = split_part_bytes((int)n);
     L.split = take(L.split_bytes);
   }

@@ -6,9 +6,13 @@
 // global memory).
 //
 // Persistent: one CTA per SM takes work items (128-query tile, head,
-// sequence) from an atomic counter, in the order (sequence, head, query tile
-// from the last, heaviest, to the first) so that the query tiles of one head
-// run together and share its K/V tiles in L2.  Each item's Q load and first
+// sequence) from an atomic counter, in the order (sequence, group of G
+// heads, query tile from the last, heaviest, to the first, head within the
+// group): the query tiles of a few heads run together and share their K/V
+// tiles in L2, and within a group the heavy tiles of every head come first,
+// so the dynamic grab ends on light tiles (G is chosen so that a group holds
+// enough work for every SM to take one of its heaviest tiles early, and so
+// that its heads' K/V fit comfortably in L2).  Each item's Q load and first
 // scores overlap the previous item's last P.V and epilogue.
 // Chunked prefill: the queries sit at positions past..past+T-1 and attend to
 // keys 0..past+T-1 of the cache (the chunk's own keys written after the
@@ -76,11 +80,23 @@ static_assert(sizeof(Bars) <= 256, "barrier block");
 // Work item w (the order described above) -> its query tile, head, sequence.
 struct Item {
   int qt, h, b, q0, n_kv;
-  __device__ __forceinline__ Item(int w, int n_qt, int T, int past) {
-    const int hb = w / n_qt;
-    qt = n_qt - 1 - (w - hb * n_qt);
-    h = hb & 63;
-    b = hb >> 6;
+  __device__ __forceinline__ Item(int w, int n_qt, int T, int past, int G) {
+    const int per_seq = 64 * n_qt;
+    b = w / per_seq;
+    const int r = w - b * per_seq;
+    const int full = 64 / G;                       // groups of G heads, then one of 64 % G
+    int g = r / (G * n_qt), within, gs;
+    if (g < full) {
+      within = r - g * G * n_qt;
+      gs = G;
+    } else {
+      g = full;
+      within = r - full * G * n_qt;
+      gs = 64 - full * G;
+    }
+    const int level = within / gs;
+    h = g * G + (within - level * gs);
+    qt = n_qt - 1 - level;
     q0 = qt * 128;
     // keys 0 .. past + q0 + 127 (the tile's last query), at most past + T of them
     n_kv = min((past + q0 + 127) / 128 + 1, (past + T + 127) / 128);
@@ -99,7 +115,8 @@ __device__ __forceinline__ bool read_item(Bars* bar, int it, int& w, const DevSt
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ o, int T, int n_qt,
-                    int n_items, float sl2, int past, int* __restrict__ work, const DevStatus st) {
+                    int n_items, float sl2, int past, int head_group, int* __restrict__ work,
+                    const DevStatus st) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bar = reinterpret_cast<Bars*>(smem + kBarOff);
@@ -158,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bar->item[slot] = w;
         mbar_arrive(&bar->item_full[slot]);  // release: the index is visible to every waiting role
         if (w < 0) break;
-        const Item t(w, n_qt, T, past);
+        const Item t(w, n_qt, T, past, head_group);
         // the Q tile: its buffer is free once the softmax threads copied the previous Q
         if (it > 0 && !mbar_wait(&bar->q_empty, (it - 1) & 1, st, abort_flag, 37)) break;
         mbar_arrive_expect_tx(&bar->q_full, 3 * kAtom);
@@ -195,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; ok; ++it) {
         int w;
         if (!read_item(bar, it, w, st, abort_flag) || w < 0) break;
-        const Item t(w, n_qt, T, past);
+        const Item t(w, n_qt, T, past, head_group);
         const int kv_row = t.b * 64 + t.h;
         for (int j = 0; j < t.n_kv; ++j, ++gt) {
           const int vs = gt & 1;
@@ -223,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; ok; ++it) {
         int w;
         if (!read_item(bar, it, w, st, abort_flag) || w < 0) break;
-        const Item t(w, n_qt, T, past);
+        const Item t(w, n_qt, T, past, head_group);
         if (!mbar_wait(&bar->q_tmem, it & 1, st, abort_flag, 44)) break;  // this item's Q in tensor memory
         for (int j = 0; j < t.n_kv; ++j, ++gt) {
           const int sb = gt & 1;
@@ -261,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; ok; ++it) {
         int w;
         if (!read_item(bar, it, w, st, abort_flag) || w < 0) break;
-        const Item t(w, n_qt, T, past);
+        const Item t(w, n_qt, T, past, head_group);
         for (int j = 0; j < t.n_kv; ++j, ++gt) {
           const int sb = gt & 1;
           if (!mbar_wait(&bar->p_full[sb], (gt >> 1) & 1, st, abort_flag, 47) ||
@@ -354,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prev_last = -1;
       }
       if (w < 0) break;
-      const Item t(w, n_qt, T, past);
+      const Item t(w, n_qt, T, past, head_group);
       const int qpos = t.q0 + row;
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < t.n_kv; ++j, ++gt) {
@@ -475,11 +492,23 @@ cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, const DevStatusHo
   if (items > INT32_MAX || !st.word) return cudaErrorInvalidValue;
   const int n_items = (int)items;
   const int grid = n_items < num_sms ? n_items : num_sms;
+  // head group G (a power of two, so the groups split the 64 heads evenly):
+  // the smallest whose work (G heads' query tiles, in key tiles) is at least
+  // 1.5x the CTA count times the heaviest item -- the heaviest tiles of the
+  // last group then start early enough -- halved while its heads' K/V exceed
+  // 64 MB of L2
+  const long long past_t = a.past / 128, heavy = past_t + n_qt + 1;
+  const long long per_head = (long long)n_qt * past_t + (long long)n_qt * (n_qt + 1) / 2 + n_qt;
+  const long long need = (3 * (long long)grid * heavy + 2 * per_head - 1) / (2 * per_head);
+  const long long kv_head_bytes = ((long long)a.past + a.T) * (192 + 128) * 2;
+  int G = 1;
+  while (G < need && G < 64) G *= 2;
+  while (G > 1 && (long long)G * kv_head_bytes > (64ll << 20)) G /= 2;
   // the work counter: an int of the status region (cleared before every call)
   int* work = reinterpret_cast<int*>(st.word) + kWorkCounterWord;
   DevStatus dst{st.word, st.wait_limit_ns};
   return launch_pdl(prefill_attn_tc, dim3(grid), dim3(kThreads), kSmemBytes, stream, tq, tk, tv, a.o, a.T, n_qt,
-                    n_items, a.scale * 1.4426950408889634f, a.past, work, dst);
+                    n_items, a.scale * 1.4426950408889634f, a.past, G, work, dst);
 }
 
 }  // namespace mla
