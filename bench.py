@@ -611,7 +611,19 @@ def run_profile(args):
     mc = re.fullmatch(r"chunk_b(\d+)_p(\d+)_t(\d+)", args.profile)
     mf = re.fullmatch(r"ffn_n(\d+)", args.profile)
     mt = re.fullmatch(r"(prefill|decode|latent)_b(\d+)_([tp])(\d+)(_cache)?", args.profile)
-    if mcl:
+    m8 = re.fullmatch(r"decode_fp8_b(\d+)_p(\d+)", args.profile)
+    if m8:
+        B8, P8 = int(m8.group(1)), int(m8.group(2))
+        WQ, keepw = r.m.make_weights_fp8(r.wt)
+        kc, vc = r.fill_caches(B8, P8, P8 + 1, True)
+        x8 = r.synth.tensor_cuda(0, "new_x", (B8, D), r.synth.X_DIST, device=r.dev)
+        o8 = torch.empty_like(x8)
+        ws8 = r.m.alloc_workspace(r.m.MODE_DECODE, B8, P8, device=r.dev)
+
+        def step(timing):
+            r.m.mla_decode_fp8(WQ, x8, P8, kc, vc, o8, ws8, r.m.make_params(timing=timing))
+        keep = (WQ, keepw, kc, vc, x8, o8, ws8)
+    elif mcl:
         step, keep = r.chunk_latent_step_fn(int(mcl.group(1)), int(mcl.group(2)), int(mcl.group(3)))
     elif mc:
         step, keep = r.chunk_step_fn(int(mc.group(1)), int(mc.group(2)), int(mc.group(3)))
@@ -651,6 +663,7 @@ def main():
                     help="tokens of the headline's sequence 0 each step of --impl reference runs")
     ap.add_argument("--profile", default=None,
                     help="run one step of one configuration for a profiler and exit: prefill_bB_tT[_cache], "
+                         "decode_fp8_bB_pP (FP8 weights), "
                          "chunk_bB_pP0_tT / chunk_latent_bB_pP0_tT (chunked prefill on either cache), ffn_nN (MLP half, N rows), "
                          "decode_bB_pP (rebuilt cache) or latent_bB_pP; only that step lies between "
                          "cudaProfilerStart/Stop (ncu --profile-from-start off)")
