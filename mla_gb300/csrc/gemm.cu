@@ -6,8 +6,9 @@
 //   kStoreBf16  plain bf16 store (latent absorption)
 //   kStoreF32   plain float32 store (A-projection: its columns are normalised
 //               or rotated before they are rounded once to bf16)
-//   kQRope      q_b_proj: one head (192 columns) per tile, RoPE on the 64
-//               "pe" columns (dense-block page: Q^R_t = RoPE(Q^pe_t, R_t))
+//   kQRope      q_b_proj: RoPE on the 64 "pe" columns of each 192-column
+//               head (dense-block page: Q^R_t = RoPE(Q^pe_t, R_t)); tiles of
+//               half a head, a head, or 256 columns
 //   kKVCache    kv_b_proj: one head (256 columns) per tile, writes k_nope and
 //               v into the per-head caches and appends the shared rotary key
 //               (dense-block page: K_i = [K^C_i ; k^R])
@@ -156,22 +157,24 @@ __device__ __forceinline__ void run_epilogue(const EpiArgs& ea, const Src& ld, i
       }
     }
   } else if constexpr (EPI == Epi::kQRope) {
-    // the tile covers columns o0 .. o0+BN-1 of one 192-wide head:
-    // [128 nope | 64 pe], RoPE pairs (128+i, 160+i) always in the same tile
-    static_assert(BN == 192 || BN == 96, "q_b epilogue works on whole or half heads");
+    // 192-column heads [128 nope | 64 pe], RoPE pairs (128+i, 160+i); a
+    // tile (half a head, a head, or 256 columns) never splits a pe block
+    static_assert(BN == 192 || BN == 96 || BN == 256, "q_b epilogue tile width");
     const int o0 = n0 % 192;
-    const int nope_cols = (o0 + BN < 128 ? o0 + BN : 128) - o0;
     __nv_bfloat16* dst = ea.out + (size_t)row * ea.ldo + n0;
 #pragma unroll 1
-    for (int c = 0; c < nope_cols; c += 32) {
-      uint32_t r[32];
-      ld(c, r);
-      if (row_ok) store32_bf16(dst + c, r);
-    }
-    if (o0 + BN == 192) {
+    for (int c = 0; c < BN; c += 32) {
+      const int o = (o0 + c) % 192;
+      if (o < 128) {
+        uint32_t r[32];
+        ld(c, r);
+        if (row_ok) store32_bf16(dst + c, r);
+        continue;
+      }
+      // o == 128: the pe block of head (n0 + c) / 192
       uint32_t x1[32], x2[32];
-      ld(nope_cols, x1);
-      ld(nope_cols + 32, x2);
+      ld(c, x1);
+      ld(c + 32, x2);
       if (row_ok) {
         const float2* cs = ea.cs + (size_t)(row % ea.t_mod) * 32;
 #pragma unroll
@@ -181,14 +184,15 @@ __device__ __forceinline__ void run_epilogue(const EpiArgs& ea, const Src& ld, i
           x1[i] = __float_as_uint(a * t.x - b * t.y);
           x2[i] = __float_as_uint(b * t.x + a * t.y);
         }
-        store32_bf16(dst + nope_cols, x1);
-        store32_bf16(dst + nope_cols + 32, x2);
+        store32_bf16(dst + c, x1);
+        store32_bf16(dst + c + 32, x2);
         if (ea.qpe_out) {  // latent decode: the rotated q^pe is also q_lat[row, head, 512:576]
-          __nv_bfloat16* qd = ea.qpe_out + ((size_t)row * 64 + n0 / 192) * 576 + 512;
+          __nv_bfloat16* qd = ea.qpe_out + ((size_t)row * 64 + (n0 + c) / 192) * 576 + 512;
           store32_bf16(qd, x1);
           store32_bf16(qd + 32, x2);
         }
       }
+      c += 32;
     }
   } else if constexpr (EPI == Epi::kKVCache) {
     // the tile covers columns o0 .. o0+BN-1 of one 256-wide head [128 k_nope | 128 v]
@@ -342,12 +346,15 @@ __device__ __forceinline__ void run_epilogue_tma(const EpiArgs& ea, const TmemSr
       ss.issue2(m0, buf, col0 + c, row0, lane);
     });
   } else if constexpr (EPI == Epi::kQRope) {
-    static_assert(BN == 192 || BN == 96, "q_b epilogue works on whole or half heads");
+    // Heads are 192 columns: 128 "nope" then the 64 "pe" columns RoPE
+    // rotates in pairs (i, i + 32).  A tile is a half head, a head, or 256
+    // columns; a pe block never straddles a 256-column boundary
+    // (256 k - 192 h never lies strictly between 128 and 192).
+    static_assert(BN == 192 || BN == 96 || BN == 256, "q_b epilogue tile width");
     const int o0 = n0 % 192;
-    const int nope_cols = (o0 + BN < 128 ? o0 + BN : 128) - o0;
     // the RoPE table row of this token, fetched while the "nope" chunks are stored
     float2 cs[32];
-    const bool has_pe = o0 + BN == 192;
+    const bool has_pe = (128 - o0 + 192) % 192 < BN;
     if (has_pe) {
       const float4* csr = reinterpret_cast<const float4*>(ea.cs + (size_t)(row % ea.t_mod) * 32);
 #pragma unroll
@@ -357,15 +364,24 @@ __device__ __forceinline__ void run_epilogue_tma(const EpiArgs& ea, const TmemSr
         cs[2 * i + 1] = make_float2(v.z, v.w);
       }
     }
-    tmem_chunk_loop(taddr, 0, nope_cols, [&](int c, uint32_t (&r)[32]) {
-      uint8_t* buf = ss.next(lane);
-      stage_bf16(buf, lane, r);
-      ss.issue2(m0, buf, n0 + c, row0, lane);
-    });
-    if (has_pe) {
+    int c = 0;
+#pragma unroll 1
+    while (c < BN) {
+      const int o = (o0 + c) % 192;
+      if (o < 128) {  // a run of nope columns
+        const int run = (128 - o) < (BN - c) ? (128 - o) : (BN - c);
+        tmem_chunk_loop(taddr, c, c + run, [&](int cc, uint32_t (&r)[32]) {
+          uint8_t* buf = ss.next(lane);
+          stage_bf16(buf, lane, r);
+          ss.issue2(m0, buf, n0 + cc, row0, lane);
+        });
+        c += run;
+        continue;
+      }
+      // o == 128: a whole pe block
       uint32_t x1[32], x2[32];
-      tmem_ld32(taddr + nope_cols, x1);
-      tmem_ld32(taddr + nope_cols + 32, x2);
+      tmem_ld32(taddr + c, x1);
+      tmem_ld32(taddr + c + 32, x2);
       tmem_wait_ld();
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
@@ -376,10 +392,11 @@ __device__ __forceinline__ void run_epilogue_tma(const EpiArgs& ea, const TmemSr
       }
       uint8_t* buf = ss.next(lane);
       stage_bf16(buf, lane, x1);
-      ss.issue2(m0, buf, n0 + nope_cols, row0, lane);
+      ss.issue2(m0, buf, n0 + c, row0, lane);
       buf = ss.next(lane);
       stage_bf16(buf, lane, x2);
-      ss.issue2(m0, buf, n0 + nope_cols + 32, row0, lane);
+      ss.issue2(m0, buf, n0 + c + 32, row0, lane);
+      c += 64;
     }
   } else if constexpr (EPI == Epi::kKVCache) {
     // the 32 rows of this warp are consecutive positions of one sequence
@@ -1380,6 +1397,11 @@ cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, con
       if (tiny && k256) return launch_impl<64, 96, 5, Epi::kQRope, false, 2>(s, op, ea, st, num_sms, stream);
       if (small && k256) return launch_impl<128, 96, 3, Epi::kQRope, false, 2>(s, op, ea, st, num_sms, stream);
       if (small) return launch_impl<128, 96, 7, Epi::kQRope, false>(s, op, ea, st, num_sms, stream);
+      // CTA pairs: 256-column tiles (as the A- and o-projections), whose
+      // operand bytes per MMA cycle the TMA ring sustains; 192-column tiles
+      // ask for 14% more
+      if (pairs && s.N % 256 == 0)
+        return launch_impl<128, 256, 6, Epi::kQRope, false, 1, true, true>(s, op, ea, st, num_sms, stream);
       if (pairs) return launch_impl<128, 192, 6, Epi::kQRope, false, 1, true, true>(s, op, ea, st, num_sms, stream);
       return launch_impl<128, 192, 4, Epi::kQRope, false, 1, true>(s, op, ea, st, num_sms, stream);
     case Epi::kKVCache:
