@@ -402,24 +402,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (k0 + c > past + qpos) s[c] = __float_as_uint(-INFINITY);
         }
         // eight independent partial maxima / sums keep the reductions off a
-        // single serial dependency chain
+        // single serial dependency chain; three-input maxima and two-lane
+        // float32 FMA / add halve the instructions of the max, scale and sum
+        // passes (the softmax threads are bound by instruction issue)
         float mp[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mp[i] = __uint_as_float(s[i]);
+        for (int i = 0; i < 8; ++i) mp[i] = fmaxf(__uint_as_float(s[i]), __uint_as_float(s[i + 8]));
 #pragma unroll
-        for (int c = 8; c < 128; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(s[c]));
-        float mx =
-            fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        for (int c = 16; c < 128; c += 16)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mp[i] = fmax3(mp[i], __uint_as_float(s[c + i]), __uint_as_float(s[c + 8 + i]));
+        float mx = fmaxf(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], fmax3(mp[5], mp[6], mp[7])));
         mx *= sl2;  // log2 units
         const bool need = mx > m + kRescaleThreshold;
         const float m_new = need ? mx : m;
         const float alpha = need ? ex2_approx(m - m_new) : 1.f;
         float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const float p = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -m_new));
-          s[c] = __float_as_uint(p);
-          sp[c & 7] += p;
+        for (int c = 0; c < 128; c += 2) {
+          float x0, x1;
+          fma_x2(x0, x1, __uint_as_float(s[c]), __uint_as_float(s[c + 1]), sl2, sl2, -m_new, -m_new);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          s[c] = __float_as_uint(p0);
+          s[c + 1] = __float_as_uint(p1);
+          add_x2(sp[c & 7], sp[(c & 7) + 1], sp[c & 7], sp[(c & 7) + 1], p0, p1);
         }
         const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
         l = l * alpha + sum;
