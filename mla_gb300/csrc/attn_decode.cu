@@ -545,12 +545,14 @@ __global__ void __launch_bounds__(kLatThreads, 1)
       }
       float mx;
       {
+        // three-input maxima and two-lane float32 FMA / add (as the prefill
+        // softmax): fewer instructions on the per-tile chain
         float mp[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) mp[c] = __uint_as_float(s[c]);
+        for (int c = 0; c < 8; ++c) mp[c] = fmaxf(__uint_as_float(s[c]), __uint_as_float(s[c + 8]));
 #pragma unroll
-        for (int c = 8; c < 32; ++c) mp[c & 7] = fmaxf(mp[c & 7], __uint_as_float(s[c]));
-        mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        for (int c = 0; c < 8; ++c) mp[c] = fmax3(mp[c], __uint_as_float(s[16 + c]), __uint_as_float(s[24 + c]));
+        mx = fmaxf(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], fmax3(mp[5], mp[6], mp[7])));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // the head's other half
       }
       mx *= sl2;  // log2 units (the scale is positive)
@@ -559,10 +561,13 @@ __global__ void __launch_bounds__(kLatThreads, 1)
       const float alpha = need ? ex2_approx(m - m_new) : 1.f;
       float sp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -m_new));
-        s[c] = __float_as_uint(p);
-        sp[c & 3] += p;
+      for (int c = 0; c < 32; c += 2) {
+        float x0, x1;
+        fma_x2(x0, x1, __uint_as_float(s[c]), __uint_as_float(s[c + 1]), sl2, sl2, -m_new, -m_new);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        s[c] = __float_as_uint(p0);
+        s[c + 1] = __float_as_uint(p1);
+        add_x2(sp[c & 3], sp[(c & 3) + 1], sp[c & 3], sp[(c & 3) + 1], p0, p1);
       }
       l = l * alpha + ((sp[0] + sp[1]) + (sp[2] + sp[3]));
       m = m_new;
