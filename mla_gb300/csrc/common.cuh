@@ -122,6 +122,49 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// For barriers that another CTA of the cluster completes (CTA pairs: the
+// partner's arrivals, its TMA bytes, multicast MMA commits): acquire at
+// cluster scope (the arrivals release at cluster scope), and a suspend-time
+// hint of 100 ns so that a suspended waiter re-checks soon.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(100u)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const DevStatus& st,
+                                                  volatile int* abort, uint32_t site) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (abort && *abort) return false;
+    if (globaltimer_ns() - t0 > st.wait_limit_ns) {
+      report_timeout(st, site);
+      if (abort) *abort = 1;
+      return false;
+    }
+  }
+}
+
+// mbar_wait, or mbar_wait_cluster in kernels whose barriers a partner CTA completes
+template <bool CLUSTER>
+__device__ __forceinline__ bool mbar_wait_t(uint64_t* bar, uint32_t parity, const DevStatus& st, volatile int* abort,
+                                            uint32_t site) {
+  if constexpr (CLUSTER)
+    return mbar_wait_cluster(bar, parity, st, abort, site);
+  else
+    return mbar_wait(bar, parity, st, abort, site);
+}
+
 // ---------------------------------------------------------------------------
 // TMA (tensor and plain bulk copies), completion counted on an mbarrier
 // ---------------------------------------------------------------------------

@@ -547,7 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull_bar[i], 1);
-      mbar_init(&tempty_bar[i], PAIR ? 256 : 128);  // pair: both CTAs' epilogue threads
+      // pair: one cluster-scope arrival per epilogue warp of both CTAs (in
+      // place of one per thread); single CTA: every epilogue thread
+      mbar_init(&tempty_bar[i], PAIR ? 8 : 128);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -635,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* mb = (n0 < s.n_split) ? &tmB0 : &tmB1;
         const int nb = (n0 < s.n_split) ? n0 : n0 - s.n_split;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1, st, abort_flag, 1)) {
+          if (!mbar_wait_t<PAIR>(&empty_bar[stage], phase ^ 1, st, abort_flag, 1)) {
             ok = false;
             break;
           }
@@ -690,9 +692,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < STAGES; ++i) {
         if (!issued[i]) continue;
         if (!PAIR || leader)
-          mbar_wait(&full_bar[i], (issued[i] - 1) & 1, st, nullptr, 2);
+          mbar_wait_t<PAIR>(&full_bar[i], (issued[i] - 1) & 1, st, nullptr, 2);
         else
-          mbar_wait(&empty_bar[i], (issued[i] - 1) & 1, st, nullptr, 2);
+          mbar_wait_t<PAIR>(&empty_bar[i], (issued[i] - 1) & 1, st, nullptr, 2);
       }
     }
   } else if (warp == 1) {
@@ -707,11 +709,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int unit = unit0; unit < num_units && ok; unit += ustep) {
         const int kb0 = (unit % ksplit) * s.kb_per;
         const int kb1 = min(kblocks, kb0 + s.kb_per);
-        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, st, abort_flag, 3)) break;
+        if (!mbar_wait_t<PAIR>(&tempty_bar[acc], acc_phase ^ 1, st, abort_flag, 3)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, st, abort_flag, 4)) {
+          if (!mbar_wait_t<PAIR>(&full_bar[stage], phase, st, abort_flag, 4)) {
             ok = false;
             break;
           }
@@ -758,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit_pair(drain_bar, (uint16_t)0x1);
       else
         umma_commit(drain_bar);
-      mbar_wait(drain_bar, 0, st, nullptr, 5);
+      mbar_wait_t<PAIR>(drain_bar, 0, st, nullptr, 5);
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
@@ -774,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int batch, m_blk, n_blk;
       tile_coords(tile, m_units, n_tiles, s.raster_g, batch, m_blk, n_blk);
       if (PAIR) m_blk = 2 * m_blk + (int)crank;
-      bool ok = mbar_wait(&tfull_bar[acc], acc_phase, st, abort_flag, 6);
+      bool ok = mbar_wait_t<PAIR>(&tfull_bar[acc], acc_phase, st, abort_flag, 6);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const int row = m_blk * BM + rit;
@@ -788,10 +790,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           run_epilogue<BN, EPI>(ea, TmemSrc{taddr}, batch, row, n_blk * BN, row_ok);
         }
         tc_fence_before();
-        if constexpr (PAIR)
-          mbar_arrive_cluster(mapa_rank(smem_u32(&tempty_bar[acc]), 0));  // the even CTA's accumulator barrier
-        else
+        if constexpr (PAIR) {
+          __syncwarp();  // the warp's accumulator reads are done
+          if (lane == 0) mbar_arrive_cluster(mapa_rank(smem_u32(&tempty_bar[acc]), 0));  // the even CTA's barrier
+        } else {
           mbar_arrive(&tempty_bar[acc]);
+        }
       } else {
         // this K slice's partial -> its slot; the last warp of the quarter reduces
         const int lq = rit - quarter * (BM / 4);  // row within the quarter
