@@ -313,6 +313,27 @@ __device__ __forceinline__ void stage_bf16(uint8_t* buf, int lane, const uint32_
   }
 }
 
+// row `lane` of a 32 x 64 bf16 chunk (columns 0-31 from a, 32-63 from b):
+// 128 bytes, 128-byte swizzle
+__device__ __forceinline__ void stage_bf16_64(uint8_t* buf, int lane, const uint32_t (&a)[32],
+                                              const uint32_t (&b)[32]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t* r = c < 4 ? &a[8 * c] : &b[8 * (c - 4)];
+    *reinterpret_cast<uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) * 16)) =
+        make_uint4(pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1])),
+                   pack_bf16x2(__uint_as_float(r[2]), __uint_as_float(r[3])),
+                   pack_bf16x2(__uint_as_float(r[4]), __uint_as_float(r[5])),
+                   pack_bf16x2(__uint_as_float(r[6]), __uint_as_float(r[7])));
+  }
+}
+
+// row `lane` of a 32 x 64 bf16 chunk from 8 packed uint4 (already bf16)
+__device__ __forceinline__ void stage_bf16_raw_64(uint8_t* buf, int lane, const uint4 (&v)[8]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) * 16)) = v[c];
+}
+
 // row `lane` of a 32 x 32 bf16 chunk from 4 packed uint4 (already bf16)
 __device__ __forceinline__ void stage_bf16_raw(uint8_t* buf, int lane, const uint4 (&v)[4]) {
 #pragma unroll
@@ -416,25 +437,28 @@ __device__ __forceinline__ void run_epilogue_tma(const EpiArgs& ea, const TmemSr
 #pragma unroll
       for (int j = 0; j < 8; ++j) kv4[j] = row_ok ? kp[j] : make_uint4(0, 0, 0, 0);
     }
+    // 64-column chunks (32 rows x 128 bytes, the store maps' box): each row
+    // piece is a whole 128-byte line of a K (384-byte) or V (256-byte) row
     if (warp_ok) {
-      tmem_chunk_loop(taddr, 0, BN, [&](int c, uint32_t (&r)[32]) {
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 64) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(taddr + c, ra);
+        tmem_ld32(taddr + c + 32, rb);
+        tmem_wait_ld();
         const int col = o0 + c;
         uint8_t* buf = ss.next(lane);
-        stage_bf16(buf, lane, r);
+        stage_bf16_64(buf, lane, ra, rb);
         if (col < 128)
           ss.issue3(m0, buf, col, t0, plane, lane);
         else
           ss.issue3(m1, buf, col - 128, t0, plane, lane);
-      });
+      }
     }
     if (warp_ok && o0 == 0) {
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const uint4 v[4] = {kv4[4 * half], kv4[4 * half + 1], kv4[4 * half + 2], kv4[4 * half + 3]};
-        uint8_t* buf = ss.next(lane);
-        stage_bf16_raw(buf, lane, v);
-        ss.issue3(m0, buf, 128 + 32 * half, t0, plane, lane);
-      }
+      uint8_t* buf = ss.next(lane);
+      stage_bf16_raw_64(buf, lane, kv4);
+      ss.issue3(m0, buf, 128, t0, plane, lane);
     }
   } else if constexpr (EPI == Epi::kSwiGLU) {
 #pragma unroll 1
@@ -944,6 +968,298 @@ cudaError_t launch_impl(const GemmShape& s, const GemmOperands& op, const EpiArg
 }
 
 // ---------------------------------------------------------------------------
+// CTA-pair GEMM for a short K (at most kResKb 64-wide blocks) over many rows:
+// the kv_b projection of a long prefill (K = 512).  Each CTA keeps its half
+// of a 256-row B tile for the whole K resident in shared memory while the
+// pair runs a group of row tiles against it, so per tile the SM receives only
+// its 128 rows of A (128 KB at K = 512) and sends 64 KB of cache rows, where
+// the streaming GEMM above also receives its 128 KB half of B again: the
+// tensor-copy engine, which carries both directions, is what bounds this
+// product (about 42 B per cycle per SM measured, against 64 that a 256-wide
+// MMA stream asks for).  Warp roles as gemm_kernel (192 threads): warp 0
+// copies B once per unit and A stage by stage, warp 1 (even CTA) issues the
+// MMAs, warps 2..5 run the TMA-store epilogue of their CTA's 128 rows.
+// ---------------------------------------------------------------------------
+constexpr int kResKb = 8;
+constexpr int kResStages = 4;
+
+struct ResSmem {
+  static constexpr uint32_t kBlk = 128 * kBK * 2;          // 128 rows x 64 bf16 (A stage, or a B block)
+  static constexpr uint32_t kBOff = 0;                     // kResKb resident B blocks
+  static constexpr uint32_t kAOff = kResKb * kBlk;         // kResStages A stages
+  static constexpr uint32_t kStagingOff = kAOff + kResStages * kBlk;
+  static constexpr uint32_t kBarOff = kStagingOff + 32768;
+  static constexpr uint32_t kBytes = kBarOff + 256 + 1024;
+};
+static_assert(ResSmem::kBytes <= 232448, "shared memory budget");
+
+// unit u of a resident-B GEMM: column block u % n_tiles, row-pair tiles
+// [g * G, min((g + 1) * G, m_pairs)) with g = u / n_tiles (the pairs that run
+// at once share one group of A rows in L2), walked from a tile that depends
+// on the column block: pairs that all read the same A tile at the same time
+// left each SM waiting for its A stages (about 16 B per cycle arrived)
+template <Epi EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_resb_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
+                          const GemmShape s, int group, const EpiArgs ea, const DevStatus st) {
+  constexpr int BN = 256;
+  using L = ResSmem;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* a_empty = a_full + kResStages;
+  uint64_t* b_full = a_empty + kResStages;
+  uint64_t* b_empty = b_full + 1;
+  uint64_t* tfull_bar = b_empty + 1;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* drain_bar = tempty_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();
+  const bool leader = crank == 0;
+  const int m_pairs = (s.M + 255) / 256;
+  const int n_tiles = s.N / BN;
+  const int kb_n = s.K / kBK;  // <= kResKb (host-checked)
+  const int groups = (m_pairs + group - 1) / group;
+  const int num_units = groups * n_tiles;
+  const int unit0 = (int)(blockIdx.x >> 1), ustep = (int)(gridDim.x >> 1);
+  // the i-th row-pair tile of unit u
+  auto unit_tile = [&](int u, int i) {
+    const int p0 = (u / n_tiles) * group;
+    const int cnt = min(group, m_pairs - p0);
+    return p0 + (i + u % n_tiles) % cnt;
+  };
+  auto unit_count = [&](int u) { return min(group, m_pairs - (u / n_tiles) * group); };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kResStages; ++i) {
+      mbar_init(&a_full[i], 1);
+      mbar_init(&a_empty[i], 1);
+    }
+    mbar_init(b_full, 1);
+    mbar_init(b_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull_bar[i], 1);
+      mbar_init(&tempty_bar[i], 8);  // one arrival per epilogue warp of both CTAs
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote signal
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_launch_dependents();
+  pdl_wait();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0, nb = 0;
+      uint32_t phase = 0;
+      int a_issued[kResStages] = {};
+      bool ok = true;
+      for (int unit = unit0; unit < num_units && ok; unit += ustep, ++nb) {
+        const int n0 = (unit % n_tiles) * BN;
+        const int cnt = unit_count(unit);
+        // the previous unit's MMAs have read the resident B
+        if (nb > 0 && !mbar_wait_t<true>(b_empty, (nb - 1) & 1, st, abort_flag, 91)) break;
+        const uint32_t bfb = mapa_rank(smem_u32(b_full), 0);
+        if (leader) mbar_arrive_expect_tx(b_full, 2 * kb_n * L::kBlk);
+        for (int kb = 0; kb < kb_n; ++kb)
+          tma_load_2d_pair(smem + L::kBOff + kb * L::kBlk, &tmB, bfb, kb * kBK, n0 + (int)crank * (BN / 2));
+        for (int i = 0; i < cnt && ok; ++i) {
+          const int m_blk = 2 * unit_tile(unit, i) + (int)crank;
+          for (int kb = 0; kb < kb_n; ++kb) {
+            if (!mbar_wait_t<true>(&a_empty[stage], phase ^ 1, st, abort_flag, 92)) {
+              ok = false;
+              break;
+            }
+            if (leader) mbar_arrive_expect_tx(&a_full[stage], 2 * L::kBlk);
+            tma_load_2d_pair(smem + L::kAOff + stage * L::kBlk, &tmA, mapa_rank(smem_u32(&a_full[stage]), 0),
+                             kb * kBK, m_blk * 128);
+            a_issued[stage]++;
+            if (++stage == kResStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+        }
+      }
+      // no copy into this CTA's shared memory may still be in flight: the
+      // even CTA sees them complete on its own barriers, the odd CTA waits
+      // until the MMAs released every buffer it filled
+      for (int i = 0; i < kResStages; ++i) {
+        if (!a_issued[i]) continue;
+        if (leader)
+          mbar_wait_t<true>(&a_full[i], (a_issued[i] - 1) & 1, st, nullptr, 93);
+        else
+          mbar_wait_t<true>(&a_empty[i], (a_issued[i] - 1) & 1, st, nullptr, 93);
+      }
+      if (nb > 0) {
+        if (leader)
+          mbar_wait_t<true>(b_full, (nb - 1) & 1, st, nullptr, 93);
+        else
+          mbar_wait_t<true>(b_empty, (nb - 1) & 1, st, nullptr, 93);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (the even CTA) ----------------
+      constexpr uint32_t idesc = idesc_bf16(256, BN, false, false);
+      int stage = 0, nb = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int unit = unit0; unit < num_units && ok; unit += ustep, ++nb) {
+        const int cnt = unit_count(unit);
+        if (!mbar_wait_t<true>(b_full, nb & 1, st, abort_flag, 94)) break;
+        for (int i = 0; i < cnt; ++i) {
+          if (!mbar_wait_t<true>(&tempty_bar[acc], acc_phase ^ 1, st, abort_flag, 95)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * BN;
+          for (int kb = 0; kb < kb_n; ++kb) {
+            if (!mbar_wait_t<true>(&a_full[stage], phase, st, abort_flag, 96)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(smem + L::kAOff + stage * L::kBlk);
+            const uint32_t b_addr = smem_u32(smem + L::kBOff + kb * L::kBlk);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              umma_bf16_pair(d_tmem, sdesc_sw128(a_addr + k * 32, 16, 1024), sdesc_sw128(b_addr + k * 32, 16, 1024),
+                             idesc, (kb != 0 || k != 0) ? 1u : 0u);
+            umma_commit_pair(&a_empty[stage], (uint16_t)0x3);  // frees the A stage in both CTAs
+            if (++stage == kResStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (!ok) break;
+          umma_commit_pair(&tfull_bar[acc], (uint16_t)0x3);
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1;
+        }
+        if (!ok) break;
+        umma_commit_pair(b_empty, (uint16_t)0x3);  // the resident B may be replaced
+      }
+      umma_commit_pair(drain_bar, (uint16_t)0x1);
+      mbar_wait_t<true>(drain_bar, 0, st, nullptr, 97);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int quarter = warp & 3;
+    StoreStage ss{smem + L::kStagingOff + quarter * 8192, 0};
+    const int rit = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int unit = unit0; unit < num_units && ok; unit += ustep) {
+      const int n0 = (unit % n_tiles) * BN;
+      const int cnt = unit_count(unit);
+      for (int i = 0; i < cnt; ++i) {
+        const int m_blk = 2 * unit_tile(unit, i) + (int)crank;
+        ok = __all_sync(0xffffffffu, mbar_wait_t<true>(&tfull_bar[acc], acc_phase, st, abort_flag, 98));
+        if (!ok) break;
+        tc_fence_after();
+        const int row = m_blk * 128 + rit;
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+        run_epilogue_tma<BN, EPI>(ea, TmemSrc{taddr}, ss, &tmO0, &tmO1, 0, m_blk * 128 + quarter * 32, row, n0,
+                                  row < s.M, lane, s.M);
+        tc_fence_before();
+        __syncwarp();  // the warp's accumulator reads are done
+        if (lane == 0) mbar_arrive_cluster(mapa_rank(smem_u32(&tempty_bar[acc]), 0));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  // every MMA of the pair has finished (the even CTA drained them) and no
+  // remote arrive or copy is still in flight before the collective free
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, 512);
+  }
+}
+
+template <Epi EPI>
+cudaError_t launch_resb_pair(const GemmShape& s, const GemmOperands& op, const EpiArgs& ea, const DevStatusHost& st,
+                             int num_sms, cudaStream_t stream) {
+  constexpr int BN = 256;
+  using L = ResSmem;
+  if (s.K % kBK || s.K / kBK > kResKb || s.N % BN || s.M % 256 || s.batches != 1 || op.b_mn_major)
+    return cudaErrorInvalidValue;
+  CUtensorMap ta, tb, to0, to1;
+  if (!make_tmap_bf16_2d(&ta, op.A, op.a_rows, (uint64_t)op.lda, op.lda, 128, kBK) ||
+      !make_tmap_bf16_2d(&tb, op.B0, op.b0_rows, op.ldb0, op.ldb0, BN / 2, kBK))
+    return cudaErrorInvalidValue;
+  to1 = to0 = ta;
+  bool ok = true;
+  if constexpr (EPI == Epi::kKVCache) {
+    ok = make_tmap_store_bf16_3d(&to0, ea.kc, 192, ea.cap, (uint64_t)ea.B * 64, 384, (uint64_t)ea.cap * 384) &&
+         make_tmap_store_bf16_3d(&to1, ea.vc, 128, ea.cap, (uint64_t)ea.B * 64, 256, (uint64_t)ea.cap * 256);
+  } else {
+    ok = make_tmap_store_bf16_2d(&to0, ea.out, s.M, ea.ldo, ea.ldo);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  auto kern = gemm_resb_pair_kernel<EPI>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  static int max_clusters = 0;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes);
+    if (attr_err != cudaSuccess) return;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * num_sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::kBytes;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+    if (attr_err == cudaSuccess && max_clusters < 1) attr_err = cudaErrorInvalidConfiguration;
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  // row-pair groups: about six units per cluster, at least 4 tiles per unit
+  const int m_pairs = s.M / 256, n_tiles = s.N / BN;
+  int group = (m_pairs * n_tiles) / (6 * max_clusters);
+  if (group < 4) group = 4;
+  if (group > m_pairs) group = m_pairs;
+  const int units = ((m_pairs + group - 1) / group) * n_tiles;
+  const int clusters = units < max_clusters ? units : max_clusters;
+  DevStatus dst{st.word, st.wait_limit_ns};
+  return launch_pdl_cluster2(kern, dim3(2 * clusters), dim3(kThreads), L::kBytes, stream, ta, tb, to0, to1, s,
+                             group, ea, dst);
+}
+
+// ---------------------------------------------------------------------------
 // GEMM with FP8 block-scaled B (decode-size M).  480 threads:
 //   warp 0      code producer: E4M3 tiles of B (BN rows x 128 bytes per
 //               128-wide K stage; the codes are stored block-major, so a
@@ -1413,6 +1729,10 @@ cudaError_t launch_gemm(const GemmShape& s, const GemmOperands& op, Epi epi, con
       if (tiny && k256) return launch_impl<64, 128, 4, Epi::kKVCache, false, 2>(s, op, ea, st, num_sms, stream);
       if (small && k256) return launch_impl<128, 128, 3, Epi::kKVCache, false, 2>(s, op, ea, st, num_sms, stream);
       if (small) return launch_impl<128, 128, 6, Epi::kKVCache, false>(s, op, ea, st, num_sms, stream);
+      // many row pairs: the resident-B pair kernel (K = 512 fits shared memory)
+      if (ea.t_mod % 32 == 0 && ea.B > 0 && !ea.pos && pairs && s.M % 256 == 0 && s.M >= 16 * 256 &&
+          s.K <= kResKb * kBK && s.batches == 1)
+        return launch_resb_pair<Epi::kKVCache>(s, op, ea, st, num_sms, stream);
       if (ea.t_mod % 32 == 0 && ea.B > 0 && !ea.pos && pairs)
         return launch_impl<128, 256, 6, Epi::kKVCache, false, 1, true, true>(s, op, ea, st, num_sms, stream);
       if (ea.t_mod % 32 == 0 && ea.B > 0 && !ea.pos)
@@ -1539,8 +1859,8 @@ bool make_tmap_store_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner,
                              uint64_t mid_stride_bytes, uint64_t outer_stride_bytes) {
   cuuint64_t dims[3] = {inner, mid, outer};
   cuuint64_t strides[2] = {mid_stride_bytes, outer_stride_bytes};
-  cuuint32_t box[3] = {32, 32, 1};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+  cuuint32_t box[3] = {64, 32, 1};  // 32 rows x 64 bf16, 128-byte swizzle
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid, uint64_t outer,

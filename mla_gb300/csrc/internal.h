@@ -67,8 +67,10 @@ constexpr int kWorkCounterWord = 16;
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
                        uint32_t box_rows, uint32_t box_cols);
 
-// Tensor maps for epilogue stores of 32 x 32 chunks: bf16 with 64-byte
-// swizzle (64-byte chunk rows), float32 with 128-byte swizzle.
+// Tensor maps for epilogue stores: 32 x 32 chunks of bf16 with 64-byte
+// swizzle (64-byte chunk rows) and of float32 with 128-byte swizzle; the 3D
+// bf16 map (the per-head K/V caches) stores 32 x 64 chunks with 128-byte
+// swizzle, one whole 128-byte line of a cache row per chunk row.
 bool make_tmap_store_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld);
 bool make_tmap_store_f32_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld);
 bool make_tmap_store_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid, uint64_t outer,
