@@ -24,21 +24,27 @@
 //   warp 6   TMA: V tiles into a 2-slot ring (each K and V tile is requested
 //            a whole tile ahead of the MMA that reads it)
 //   warp 1   TMEM allocation; one lane issues S_j = Q K_j^T (M=128 N=128
-//            K=192) into score buffer j & 1, Q read from tensor memory (the
-//            softmax warps copy it there once), K from its TMA tile
+//            K=192) into score buffer j & 1: the 128 "nope" dimensions of Q
+//            read from tensor memory (the softmax warps copy them there
+//            once), the 64 RoPE dimensions from one of two shared-memory
+//            slots (alternating items), K from its TMA tile; a score buffer
+//            is reused as soon as the softmax has read it
 //   warp 7   one lane issues O += P_j V_j (M=128 N=128 K=128), P read from
-//            tensor memory (row m in lane m, bf16 pairs packed per column,
-//            written over the first 64 columns of score buffer j & 1), V read
-//            MN-major from its TMA tile; a score buffer is reused once the
-//            P.V that read its P has finished
+//            its own tensor-memory buffer (row m in lane m, bf16 pairs
+//            packed per column), V read MN-major from its TMA tile
 //   (two issuing threads, each on blocking waits, keep the tensor pipe fed
-//   while either one waits; only K and V are read from shared memory)
+//   while either one waits.  With P apart from the scores, the chain of a
+//   score buffer is S -> softmax read -> next S; P waits only for the
+//   previous P.V.  The tensor-memory columns this needs come from keeping
+//   Q's RoPE dimensions in shared memory: 4 of the 12 K steps of S read A
+//   from there, 16 KB of operand reads per key tile.)
 //   warps 2..5  one thread per query row: copy the Q row into tensor memory;
 //            read S_j from TMEM, scale, causal mask on the diagonal tile,
 //            running max with lazy rescaling (O is rescaled in TMEM only when
 //            the max grows by more than 2^8, so P stays <= 256), P_j as bf16
-//            over S_j, and at the end O / l to global memory (after the
-//            next item's Q has been copied, so its first scores overlap).
+//            into the P buffer (once the previous P.V has read it), and at
+//            the end O / l to global memory (after the next item's Q has
+//            been copied, so its first scores overlap).
 // Layout: Q [B*T, 64*192], K/V caches [B, 64, cap, 192|128] (TMA 3D views
 // whose position extent is T, so keys >= T read as zeros), O [B*T, 64*128].
 #include "common.cuh"
@@ -50,32 +56,34 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr uint32_t kAtom = 128 * 128;            // 128 rows x 64 bf16
-constexpr uint32_t kQOff = 0;                    // 3 atoms
-constexpr uint32_t kKOff = 3 * kAtom;            // 2 slots x 3 atoms
-constexpr uint32_t kVOff = 9 * kAtom;            // 2 slots x 2 atoms (vdim 0-63, 64-127)
-constexpr uint32_t kBarOff = 13 * kAtom;
-// tensor memory columns: S_0, S_1 (fp32; P_j bf16 pairs over the first 64 of
-// S_j), O (fp32), Q (bf16 pairs, 192 values per row)
-constexpr uint32_t kTmS = 0, kTmO = 256, kTmQ = 384;
-constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;
+constexpr uint32_t kQOff = 0;                    // Q dims 0-127: 2 atoms (staging)
+constexpr uint32_t kQpeOff = 2 * kAtom;          // Q dims 128-191: 2 slots x 1 atom
+constexpr uint32_t kKOff = 4 * kAtom;            // 2 slots x 3 atoms
+constexpr uint32_t kVOff = 10 * kAtom;           // 2 slots x 2 atoms (vdim 0-63, 64-127)
+constexpr uint32_t kBarOff = 14 * kAtom;
+// tensor memory columns: S_0, S_1 (fp32), O (fp32), P (bf16 pairs, 128 keys),
+// Q dims 0-127 (bf16 pairs)
+constexpr uint32_t kTmS = 0, kTmO = 256, kTmP = 384, kTmQ = 448;
+constexpr uint32_t kSmemBytes = kBarOff + 512 + 1024;
+static_assert(kSmemBytes <= 232448, "prefill attention shared memory");
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 
 constexpr int kItemRing = 4;
 constexpr int kItemReaders = 3 + 128;  // V producer, S issuer, P.V issuer, softmax threads
 
 struct Bars {
-  uint64_t q_full, q_tmem, q_empty, o_free;
+  uint64_t q_full, q_tmem, qn_empty, qpe_empty[2];
   uint64_t item_full[kItemRing], item_empty[kItemRing];
   uint64_t k_full[2], k_empty[2];
   uint64_t v_full[2], v_empty[2];
-  uint64_t s_full[2];
-  uint64_t p_full[2], pv_done[2];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full, pv_done;
   uint64_t drain_s, drain_pv;
   uint32_t tmem_slot;
   int abort;
   int item[kItemRing];
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
 // Work item w (the order described above) -> its query tile, head, sequence.
 struct Item {
@@ -127,8 +135,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bar->q_full, 1);
     mbar_init(&bar->q_tmem, 128);
-    mbar_init(&bar->q_empty, 128);
-    mbar_init(&bar->o_free, 128);
+    mbar_init(&bar->qn_empty, 128);
+    mbar_init(&bar->qpe_empty[0], 1);
+    mbar_init(&bar->qpe_empty[1], 1);
+    mbar_init(&bar->p_full, 128);
+    mbar_init(&bar->pv_done, 1);
     for (int i = 0; i < kItemRing; ++i) {
       mbar_init(&bar->item_full[i], 1);
       mbar_init(&bar->item_empty[i], kItemReaders);
@@ -139,8 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar->v_full[i], 1);
       mbar_init(&bar->v_empty[i], 1);
       mbar_init(&bar->s_full[i], 1);
-      mbar_init(&bar->p_full[i], 128);
-      mbar_init(&bar->pv_done[i], 1);
+      mbar_init(&bar->s_free[i], 128);
     }
     mbar_init(&bar->drain_s, 1);
     mbar_init(&bar->drain_pv, 1);
@@ -176,11 +186,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bar->item_full[slot]);  // release: the index is visible to every waiting role
         if (w < 0) break;
         const Item t(w, n_qt, T, past, head_group);
-        // the Q tile: its buffer is free once the softmax threads copied the previous Q
-        if (it > 0 && !mbar_wait(&bar->q_empty, (it - 1) & 1, st, abort_flag, 37)) break;
+        // the Q tile: dims 0-127 into the staging atoms once the softmax threads
+        // copied the previous item's into tensor memory, dims 128-191 into the
+        // slot of this item's parity once the S of the item two back are done
+        if (it > 0 && !mbar_wait(&bar->qn_empty, (it - 1) & 1, st, abort_flag, 37)) break;
+        if (it > 1 && !mbar_wait(&bar->qpe_empty[it & 1], ((it - 2) >> 1) & 1, st, abort_flag, 36)) break;
         mbar_arrive_expect_tx(&bar->q_full, 3 * kAtom);
-        for (int c = 0; c < 3; ++c)
+        for (int c = 0; c < 2; ++c)
           tma_load_3d(smem + kQOff + c * kAtom, &tmQ, &bar->q_full, t.h * 192 + 64 * c, t.q0, t.b);
+        tma_load_3d(smem + kQpeOff + (it & 1) * kAtom, &tmQ, &bar->q_full, t.h * 192 + 128, t.q0, t.b);
         ++q_loads;
         const int kv_row = t.b * 64 + t.h;
         bool ok = true;
@@ -242,28 +256,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!read_item(bar, it, w, st, abort_flag) || w < 0) break;
         const Item t(w, n_qt, T, past, head_group);
         if (!mbar_wait(&bar->q_tmem, it & 1, st, abort_flag, 44)) break;  // this item's Q in tensor memory
+        const uint32_t qpe_addr = smem_u32(smem + kQpeOff + (it & 1) * kAtom);
         for (int j = 0; j < t.n_kv; ++j, ++gt) {
           const int sb = gt & 1;
           if (!mbar_wait(&bar->k_full[sb], (gt >> 1) & 1, st, abort_flag, 45)) {
             ok = false;
             break;
           }
-          // the buffer's previous P (tile gt-2) has been read by its P.V
-          if (gt > 1 && !mbar_wait(&bar->pv_done[sb], ((gt - 2) >> 1) & 1, st, abort_flag, 46)) {
+          // the softmax has read the buffer's previous scores (tile gt-2)
+          if (gt > 1 && !mbar_wait(&bar->s_free[sb], ((gt - 2) >> 1) & 1, st, abort_flag, 46)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t d = tmem + kTmS + sb * 128;
           const uint32_t kb = k_addr + sb * 3 * kAtom;
+          // Q dims 0-127 from tensor memory, dims 128-191 from this item's slot
 #pragma unroll
-          for (int kk = 0; kk < 12; ++kk) {
+          for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
             umma_bf16_ts(d, q_tm + kk * 8, sdesc_sw128(kb + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
           }
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(d, sdesc_sw128(qpe_addr + kk * 32, 16, 1024), sdesc_sw128(kb + 2 * kAtom + kk * 32, 16, 1024),
+                      idesc_s, 1u);
           umma_commit(&bar->s_full[sb]);
           umma_commit(&bar->k_empty[sb]);
         }
+        if (!ok) break;
+        umma_commit(&bar->qpe_empty[it & 1]);  // this item's Q slot may be reloaded
       }
       umma_commit(&bar->drain_s);
       mbar_wait(&bar->drain_s, 0, st, nullptr, 49);
@@ -281,22 +303,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item t(w, n_qt, T, past, head_group);
         for (int j = 0; j < t.n_kv; ++j, ++gt) {
           const int sb = gt & 1;
-          if (!mbar_wait(&bar->p_full[sb], (gt >> 1) & 1, st, abort_flag, 47) ||
-              !mbar_wait(&bar->v_full[sb], (gt >> 1) & 1, st, abort_flag, 48) ||
-              // the first P.V of an item overwrites O: the previous item's epilogue has read it
-              (j == 0 && it > 0 && !mbar_wait(&bar->o_free, (it - 1) & 1, st, abort_flag, 55))) {
+          // P_j is written (and, for an item's first tile, the previous item's
+          // O read out: the softmax threads do that before writing P)
+          if (!mbar_wait(&bar->p_full, gt & 1, st, abort_flag, 47) ||
+              !mbar_wait(&bar->v_full[sb], (gt >> 1) & 1, st, abort_flag, 48)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t vb = v_addr + sb * 2 * kAtom;
-          const uint32_t pa = tmem + kTmS + sb * 128;
+          const uint32_t pa = tmem + kTmP;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, kAtom, 1024);
             umma_bf16_ts(tmem + kTmO, pa + kk * 8, bdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&bar->pv_done[sb]);
+          umma_commit(&bar->pv_done);
           umma_commit(&bar->v_empty[sb]);
         }
       }
@@ -318,14 +340,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, read_item(bar, it, w, st, abort_flag));
       if (!ok) break;
       if (w >= 0) {
-        // this item's Q rows (three 128-byte-swizzled 64-column atoms) into
-        // tensor memory as bf16 pairs, the A operand of every S_j; the
-        // previous item's S are all done (its last s_full was consumed)
+        // this item's Q rows, dims 0-127 (two 128-byte-swizzled 64-column
+        // atoms), into tensor memory as bf16 pairs, the A operand of the
+        // first 8 K steps of every S_j; the previous item's S are all done
+        // (its last s_full was consumed)
         ok = __all_sync(0xffffffffu, mbar_wait(&bar->q_full, it & 1, st, abort_flag, 54));
         if (!ok) break;
         const uint8_t* qrow = smem + kQOff + row * 128;
 #pragma unroll
-        for (int c = 0; c < 3; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
@@ -340,12 +363,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bar->q_tmem);
-        mbar_arrive(&bar->q_empty);
+        mbar_arrive(&bar->qn_empty);
       }
       if (prev_last >= 0) {
         // epilogue of the previous item: O / l once its last P.V is done
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(&bar->pv_done[prev_last & 1], (prev_last >> 1) & 1, st, abort_flag, 52));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar->pv_done, prev_last & 1, st, abort_flag, 52));
         if (!ok) break;
         tc_fence_after();
         const float inv = 1.f / prev_l;
@@ -366,8 +388,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv, __uint_as_float(r[8 * q + 7]) * inv));
           }
         }
-        tc_fence_before();
-        mbar_arrive(&bar->o_free);
         prev_last = -1;
       }
       if (w < 0) break;
@@ -392,6 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(ta + 96, s3);
           tmem_wait_ld();
         }
+        tc_fence_before();
+        mbar_arrive(&bar->s_free[sb]);  // the score buffer may take S_{j+2}
         const int k0 = j * 128;
         // max of the raw scores (the scale is positive), causal mask (key k
         // visible to query position past + qpos iff k <= past + qpos) on the
@@ -430,12 +452,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
         l = l * alpha + sum;
         m = m_new;
-        // O may be rescaled only after P.V of tile j-1 has completed
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(&bar->pv_done[(gt - 1) & 1], ((gt - 1) >> 1) & 1, st, abort_flag, 53));
+        // the previous P.V (this CTA's tile gt-1) has read P and added into O:
+        // P may be rewritten and O rescaled
+        if (gt > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar->pv_done, (gt - 1) & 1, st, abort_flag, 53));
           if (!ok) break;
-          tc_fence_after();
+          tc_fence_after();  // P and O writes below come after that MMA's reads
+        }
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
           const uint32_t ta = tmem + lane_addr + kTmO;
 #pragma unroll 1
           for (int c = 0; c < 128; c += 32) {
@@ -448,19 +472,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
-        // P_j (bf16 pairs, low half = even key) over the first 64 columns of
-        // its score buffer (S_j is entirely in registers by now)
+        // P_j (bf16 pairs, low half = even key) into the P buffer
         {
           uint32_t pk[64];
 #pragma unroll
           for (int c = 0; c < 64; ++c) pk[c] = pack_bf16x2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
-          const uint32_t tp = tmem + lane_addr + kTmS + sb * 128;
+          const uint32_t tp = tmem + lane_addr + kTmP;
 #pragma unroll
           for (int c = 0; c < 64; c += 16) tmem_st16(tp + c, &pk[c]);
           tmem_wait_st();
         }
         tc_fence_before();
-        mbar_arrive(&bar->p_full[sb]);
+        mbar_arrive(&bar->p_full);
       }
       prev_qpos = qpos;
       prev_h = t.h;
