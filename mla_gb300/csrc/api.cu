@@ -184,6 +184,33 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
 }
 
+// q_b over n_tok rows of c^Q with RoPE on the q^pe columns (RoPE table row
+// r % t_mod, or row r with per-row positions); q^pe also into qpe_out if set.
+int q_b_stage(const mla_weights_t* w, int n_tok, int t_mod, const int* pos, const mla_weights_fp8_t* f8,
+              __nv_bfloat16* qpe_out, void* ws, const Layout& L, const DevStatusHost& st, int sms,
+              cudaStream_t stream, int* launches) {
+  GemmShape s{n_tok, MLA_HEADS * MLA_QK, MLA_Q_LORA, 1, 0, 0, 0, 0, MLA_HEADS * MLA_QK};
+  GemmOperands op{at<__nv_bfloat16>(ws, L.cq), MLA_Q_LORA, n_tok,
+                  static_cast<const __nv_bfloat16*>(w->w_q_b), MLA_Q_LORA, MLA_HEADS * MLA_QK,
+                  nullptr, 0, 0, false};
+  EpiArgs ea{};
+  ea.out = at<__nv_bfloat16>(ws, L.q);
+  ea.ldo = MLA_HEADS * MLA_QK;
+  ea.cs = at<float2>(ws, L.cs);
+  ea.t_mod = pos ? n_tok : t_mod;  // per-row positions: one RoPE table row per token
+  ea.qpe_out = qpe_out;
+  set_split(ea, ws, L);
+  if (f8) {
+    GemmW8Operands o8{at<__nv_bfloat16>(ws, L.cq), MLA_Q_LORA, n_tok, static_cast<const uint8_t*>(f8->w_q_b),
+                      MLA_HEADS * MLA_QK, f8->s_q_b, nullptr, 0, nullptr};
+    MLA_TRY(launch_gemm_w8(s, o8, Epi::kQRope, ea, st, sms, stream));
+  } else {
+    MLA_TRY(launch_gemm(s, op, Epi::kQRope, ea, st, sms, stream));
+  }
+  *launches += 1;
+  return MLA_OK;
+}
+
 // Projection front end shared by the three entry points: input RMSNorm, RoPE
 // table, A-projection, latent split (+ optional latent cache), q_b + RoPE.
 int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok, int n_pos, int pos0,
@@ -249,29 +276,9 @@ int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok,
   if (!with_q) return MLA_OK;
 
   sg.start(MLA_STAGE_Q_B);
-  {
-    GemmShape s{n_tok, MLA_HEADS * MLA_QK, MLA_Q_LORA, 1, 0, 0, 0, 0, MLA_HEADS * MLA_QK};
-    GemmOperands op{at<__nv_bfloat16>(ws, L.cq), MLA_Q_LORA, n_tok,
-                    static_cast<const __nv_bfloat16*>(w->w_q_b), MLA_Q_LORA, MLA_HEADS * MLA_QK,
-                    nullptr, 0, 0, false};
-    EpiArgs ea{};
-    ea.out = at<__nv_bfloat16>(ws, L.q);
-    ea.ldo = MLA_HEADS * MLA_QK;
-    ea.cs = at<float2>(ws, L.cs);
-    ea.t_mod = pos ? n_tok : t_mod;  // per-row positions: one RoPE table row per token
-    ea.qpe_out = qpe_out;
-    set_split(ea, ws, L);
-    if (f8) {
-      GemmW8Operands o8{at<__nv_bfloat16>(ws, L.cq), MLA_Q_LORA, n_tok, static_cast<const uint8_t*>(f8->w_q_b),
-                        MLA_HEADS * MLA_QK, f8->s_q_b, nullptr, 0, nullptr};
-      MLA_TRY(launch_gemm_w8(s, o8, Epi::kQRope, ea, st, sms, stream));
-    } else {
-      MLA_TRY(launch_gemm(s, op, Epi::kQRope, ea, st, sms, stream));
-    }
-    *launches += 1;
-  }
+  const int rc = q_b_stage(w, n_tok, t_mod, pos, f8, qpe_out, ws, L, st, sms, stream, launches);
   sg.stop(MLA_STAGE_Q_B);
-  return MLA_OK;
+  return rc;
 }
 
 // kv_b over n_tok latent rows ckv [n_tok, 512] (rotary keys kpe [n_tok, 64]):
@@ -279,7 +286,7 @@ int front_end(const mla_weights_t* w, const Params& p, const void* x, int n_tok,
 int kv_b_rows(const mla_weights_t* w, const __nv_bfloat16* ckv, const __nv_bfloat16* kpe, int n_tok, int t_mod,
               int t_off, __nv_bfloat16* kc, __nv_bfloat16* vc, int cap, void* ws, const Layout& L,
               const DevStatusHost& st, int sms, cudaStream_t stream, int* launches, const int* pos = nullptr,
-              int pos_max = 0, const mla_weights_fp8_t* f8 = nullptr) {
+              int pos_max = 0, const mla_weights_fp8_t* f8 = nullptr, bool split_ok = true) {
   GemmShape s{n_tok, MLA_HEADS * 256, MLA_KV_LORA, 1, 0, 0, 0, 0, MLA_HEADS * 256};
   GemmOperands op{ckv, MLA_KV_LORA, n_tok,
                   static_cast<const __nv_bfloat16*>(w->w_kv_b), MLA_KV_LORA, MLA_HEADS * 256,
@@ -294,7 +301,7 @@ int kv_b_rows(const mla_weights_t* w, const __nv_bfloat16* ckv, const __nv_bfloa
   ea.cap = cap;
   ea.pos = pos;
   ea.pos_max = pos_max;
-  set_split(ea, ws, L);
+  if (split_ok) set_split(ea, ws, L);
   if (f8) {
     GemmW8Operands o8{ckv, MLA_KV_LORA, n_tok, static_cast<const uint8_t*>(f8->w_kv_b), MLA_HEADS * 256,
                       f8->s_kv_b, nullptr, 0, nullptr};
@@ -309,9 +316,80 @@ int kv_b_rows(const mla_weights_t* w, const __nv_bfloat16* ckv, const __nv_bfloa
 int kv_b_stage(const mla_weights_t* w, int n_tok, int t_mod, int t_off, __nv_bfloat16* kc, __nv_bfloat16* vc,
                int cap, void* ws, const Layout& L, const DevStatusHost& st, int sms, cudaStream_t stream,
                int* launches, const int* pos = nullptr, int pos_max = 0,
-               const mla_weights_fp8_t* f8 = nullptr) {
+               const mla_weights_fp8_t* f8 = nullptr, bool split_ok = true) {
   return kv_b_rows(w, at<__nv_bfloat16>(ws, L.ckv), at<__nv_bfloat16>(ws, L.kpe), n_tok, t_mod, t_off, kc, vc, cap,
-                   ws, L, st, sms, stream, launches, pos, pos_max, f8);
+                   ws, L, st, sms, stream, launches, pos, pos_max, f8, split_ok);
+}
+
+// Few rows (decode, short prefill): q_b and kv_b are weight-streaming
+// launches of 128 CTAs each, leaving a sixth of the SMs idle, and neither
+// reads the other's output; kv_b then runs on a second stream beside q_b.
+// One such stream and two events per host thread and device, created by the
+// first call that uses them (never during a stream capture) and kept for
+// the thread's lifetime.
+constexpr int kForkMaxRows = 128;
+
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool failed = false;
+  ~SideStream() {  // at thread exit (before the runtime's own teardown for the main thread)
+    if (s) cudaStreamDestroy(s);
+    if (fork) cudaEventDestroy(fork);
+    if (join) cudaEventDestroy(join);
+  }
+};
+
+SideStream* side_stream(cudaStream_t user) {
+  constexpr int kMaxDevices = 64;
+  thread_local SideStream per_device[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  SideStream& ss = per_device[dev];
+  if (!ss.s && !ss.failed) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(user, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+    if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess) {
+      (void)cudaGetLastError();
+      ss.s = nullptr;
+      ss.failed = true;  // one stream from then on
+    }
+  }
+  return ss.s ? &ss : nullptr;
+}
+
+// kv_b of a few rows on the side stream, ordered after the work already
+// queued on `stream`; join_side() makes `stream` wait for it.
+int kv_b_beside(SideStream* side, const mla_weights_t* w, const Params& p, int n_tok, int t_mod, int t_off,
+                __nv_bfloat16* kc, __nv_bfloat16* vc, int cap, void* ws, const Layout& L, const DevStatusHost& st,
+                int sms, cudaStream_t stream, int* launches, const int* pos, int pos_max,
+                const mla_weights_fp8_t* f8) {
+  cudaStream_t kvs = stream;
+  if (side) {
+    MLA_TRY(cudaEventRecord(side->fork, stream));
+    MLA_TRY(cudaStreamWaitEvent(side->s, side->fork, 0));
+    kvs = side->s;
+  }
+  Stager sk{p.timing, kvs};
+  sk.start(MLA_STAGE_KV_B);
+  // no split-K: its partial slots and counters are those of the concurrent q_b
+  const int rc = kv_b_stage(w, n_tok, t_mod, t_off, kc, vc, cap, ws, L, st, sms, kvs, launches, pos, pos_max, f8,
+                            side == nullptr);
+  if (rc) return rc;
+  sk.stop(MLA_STAGE_KV_B);
+  return MLA_OK;
+}
+
+int join_side(SideStream* side, cudaStream_t stream) {
+  if (!side) return MLA_OK;
+  MLA_TRY(cudaEventRecord(side->join, side->s));
+  MLA_TRY(cudaStreamWaitEvent(stream, side->join, 0));
+  return MLA_OK;
 }
 
 int o_proj_stage(const mla_weights_t* w, const Params& p, const void* x, void* out, int n_tok, void* ws,
@@ -440,9 +518,10 @@ int prefill_impl(const mla_weights_t* w, const mla_params_t* params, const void*
   int launches = 0;
   if (cudaMemsetAsync(st.word, 0, kStatusRegion, stream_) != cudaSuccess) return MLA_ERR_CUDA;
 
+  SideStream* side = (n_tok <= (size_t)kForkMaxRows && !cache_only && !latent_past) ? side_stream(stream_) : nullptr;
   rc = front_end(w, p, x, (int)n_tok, T, P0, T, P0, static_cast<__nv_bfloat16*>(ckv_cache),
                  static_cast<__nv_bfloat16*>(kpe_cache), cap, workspace, L, st, sms, stream_, sg, &launches,
-                 !cache_only);
+                 !cache_only && side == nullptr);
   if (rc) return rc;
   if (cache_only && !k_cache) {
     if (p.timing) p.timing->n_launches = launches;
@@ -452,19 +531,31 @@ int prefill_impl(const mla_weights_t* w, const mla_params_t* params, const void*
   __nv_bfloat16* kc = k_cache ? static_cast<__nv_bfloat16*>(k_cache) : at<__nv_bfloat16>(workspace, L.kscr);
   __nv_bfloat16* vc = v_cache ? static_cast<__nv_bfloat16*>(v_cache) : at<__nv_bfloat16>(workspace, L.vscr);
   const int kcap = (k_cache || latent_past) ? cap : T;
-  sg.start(MLA_STAGE_KV_B);
-  if (latent_past) {
-    const __nv_bfloat16* ckv = static_cast<const __nv_bfloat16*>(ckv_cache);
-    const __nv_bfloat16* kpe = static_cast<const __nv_bfloat16*>(kpe_cache);
-    for (int b = 0; b < B && rc == MLA_OK; ++b)
-      rc = kv_b_rows(w, ckv + (size_t)b * cap * MLA_KV_LORA, kpe + (size_t)b * cap * MLA_QK_ROPE, P0 + T, P0 + T, 0,
-                     kc + (size_t)b * MLA_HEADS * cap * MLA_QK, vc + (size_t)b * MLA_HEADS * cap * MLA_V, cap,
-                     workspace, L, st, sms, stream_, &launches);
+  if (side) {  // kv_b beside q_b
+    rc = kv_b_beside(side, w, p, (int)n_tok, T, P0, kc, vc, kcap, workspace, L, st, sms, stream_, &launches,
+                     nullptr, 0, nullptr);
+    if (rc) return rc;
+    sg.start(MLA_STAGE_Q_B);
+    rc = q_b_stage(w, (int)n_tok, T, nullptr, nullptr, nullptr, workspace, L, st, sms, stream_, &launches);
+    if (rc) return rc;
+    sg.stop(MLA_STAGE_Q_B);
+    rc = join_side(side, stream_);
+    if (rc) return rc;
   } else {
-    rc = kv_b_stage(w, (int)n_tok, T, P0, kc, vc, kcap, workspace, L, st, sms, stream_, &launches);
+    sg.start(MLA_STAGE_KV_B);
+    if (latent_past) {
+      const __nv_bfloat16* ckv = static_cast<const __nv_bfloat16*>(ckv_cache);
+      const __nv_bfloat16* kpe = static_cast<const __nv_bfloat16*>(kpe_cache);
+      for (int b = 0; b < B && rc == MLA_OK; ++b)
+        rc = kv_b_rows(w, ckv + (size_t)b * cap * MLA_KV_LORA, kpe + (size_t)b * cap * MLA_QK_ROPE, P0 + T, P0 + T,
+                       0, kc + (size_t)b * MLA_HEADS * cap * MLA_QK, vc + (size_t)b * MLA_HEADS * cap * MLA_V, cap,
+                       workspace, L, st, sms, stream_, &launches);
+    } else {
+      rc = kv_b_stage(w, (int)n_tok, T, P0, kc, vc, kcap, workspace, L, st, sms, stream_, &launches);
+    }
+    if (rc) return rc;
+    sg.stop(MLA_STAGE_KV_B);
   }
-  if (rc) return rc;
-  sg.stop(MLA_STAGE_KV_B);
   if (cache_only) {
     if (p.timing) p.timing->n_launches = launches;
     return MLA_OK;
@@ -540,16 +631,28 @@ int decode_impl(const mla_weights_t* w, const mla_params_t* params, const void* 
   Stager sg{p.timing, stream_};
   int launches = 0;
   if (cudaMemsetAsync(st.word, 0, kStatusRegion, stream_) != cudaSuccess) return MLA_ERR_CUDA;
-  rc = front_end(w, p, x, B, 1, P, 1, P, nullptr, nullptr, cap, workspace, L, st, sms, stream_, sg, &launches, true,
-                 pos, P, f8);
+  SideStream* side = B <= kForkMaxRows ? side_stream(stream_) : nullptr;
+  rc = front_end(w, p, x, B, 1, P, 1, P, nullptr, nullptr, cap, workspace, L, st, sms, stream_, sg, &launches,
+                 side == nullptr, pos, P, f8);
   if (rc) return rc;
 
   __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(k_cache);
   __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(v_cache);
-  sg.start(MLA_STAGE_KV_B);
-  rc = kv_b_stage(w, B, 1, P, kc, vc, cap, workspace, L, st, sms, stream_, &launches, pos, P, f8);
-  if (rc) return rc;
-  sg.stop(MLA_STAGE_KV_B);
+  if (side) {  // kv_b beside q_b
+    rc = kv_b_beside(side, w, p, B, 1, P, kc, vc, cap, workspace, L, st, sms, stream_, &launches, pos, P, f8);
+    if (rc) return rc;
+    sg.start(MLA_STAGE_Q_B);
+    rc = q_b_stage(w, B, 1, pos, f8, nullptr, workspace, L, st, sms, stream_, &launches);
+    if (rc) return rc;
+    sg.stop(MLA_STAGE_Q_B);
+    rc = join_side(side, stream_);
+    if (rc) return rc;
+  } else {
+    sg.start(MLA_STAGE_KV_B);
+    rc = kv_b_stage(w, B, 1, P, kc, vc, cap, workspace, L, st, sms, stream_, &launches, pos, P, f8);
+    if (rc) return rc;
+    sg.stop(MLA_STAGE_KV_B);
+  }
 
   sg.start(MLA_STAGE_ATTN);
   {
