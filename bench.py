@@ -219,7 +219,11 @@ class Runner:
         self.flush_buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
 
     def flush_l2(self):
+        """Evict every input from L2: write 512 MB (four times the L2), then
+        read it back, so that the lines this writes are also written back to
+        HBM here, not during the next timed step."""
         self.flush_buf.zero_()
+        self.flush_sum = self.flush_buf.sum()
 
     def timing(self):
         t = self.m.MlaTiming()
@@ -234,15 +238,19 @@ class Runner:
             evs.append((a, b))
         return t, evs
 
-    def time_steps(self, step, steps, warmup, flush=True, with_stages=True, stages=None, probe_steps=3):
+    def time_steps(self, step, steps, warmup, flush=True, with_stages=True, stages=None, probe_steps=3,
+                   dominant_events=True):
         """Time `steps` calls of step(timing).
 
         A short instrumented pass first records events around every stage
         (the per-stage breakdown, reported as stage_ms) and picks the
         dominant stage.  The timed region then records events only around
-        the whole step and around the dominant stage, so that the stages
-        are not separated by event records (kernels of one call overlap
-        their start-up with the previous kernel's tail)."""
+        the whole step and, with dominant_events, around the dominant stage,
+        so that the other stages are not separated by event records
+        (kernels of one call overlap their start-up with the previous
+        kernel's tail).  Without dominant_events the timed steps carry no
+        event inside them, and the dominant stage's time is the
+        instrumented pass's."""
         torch = self.torch
         for _ in range(warmup):
             step(None)
@@ -261,6 +269,9 @@ class Runner:
                     continue  # the library records only the stages its entry point runs
                 stage_ms[name] = statistics.mean(evs[si][0].elapsed_time(evs[si][1]) for _, evs in tims)
             dom = max(stage_ms, key=stage_ms.get) if stage_ms else None
+            if dom is not None and not dominant_events:
+                stage_ms["_dominant_probe"] = (dom, stage_ms[dom])
+                dom = None
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         dev_t = []
         for i in range(steps):
@@ -514,9 +525,12 @@ def varlen_lengths(B, P_max):
 def roofline_entry(stage_ms, mode, B, TP, pk, config_name, past=0):
     """Roofline of the dominant stage, timed by events around it in every
     timed step."""
-    if "_dominant_timed" not in stage_ms:
+    if "_dominant_timed" in stage_ms:
+        (name, ms), how = stage_ms["_dominant_timed"], "events around it in every timed step"
+    elif "_dominant_probe" in stage_ms:
+        (name, ms), how = stage_ms["_dominant_probe"], "events around every stage in a separate instrumented pass"
+    else:
         return None
-    name, ms = stage_ms["_dominant_timed"]
     total = sum(v for k, v in stage_ms.items() if not k.startswith("_"))
     kind, amount = stage_work(name, mode, B, TP, past)
     if kind == "flop":
@@ -524,13 +538,13 @@ def roofline_entry(stage_ms, mode, B, TP, pk, config_name, past=0):
         peak = pk["bf16_tflops"]
         return {"kernel": name, "bound": "tensor", "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(ach / peak, 4), "traffic": ncu_traffic(name, config_name), "ms": round(ms, 4),
-                "share": round(stage_ms[name] / total, 4), "peak_source": pk["source"] + " (burst)"}
+                "share": round(stage_ms[name] / total, 4), "peak_source": pk["source"] + " (burst)", "timed": how}
     if kind == "byte":
         ach = amount / (ms * 1e-3) / 1e9
         peak = pk["hbm_gbs"]
         return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4), "traffic": ncu_traffic(name, config_name), "ms": round(ms, 4),
-                "share": round(stage_ms[name] / total, 4), "peak_source": pk["source"]}
+                "share": round(stage_ms[name] / total, 4), "peak_source": pk["source"], "timed": how}
     return {"kernel": name, "bound": None, "ms": ms}
 
 
@@ -722,7 +736,8 @@ def main():
             "data": "synthetic (seeded splitmix64 / Box-Muller N(0,1) inputs, N(0,0.02) weights)",
             "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": T,
                        "parallelism": f"replica{world}" if world > 1 else "single",
-                       "l2": "inputs (470 MB) larger than L2, and L2 flushed between timed steps (512 MB write)"},
+                       "l2": "inputs (470 MB) larger than L2, and L2 flushed between timed steps "
+                             "(512 MB written, then read back)"},
             "tflops": round(tf, 2), "frac_bf16_peak": round(tf / pk["bf16_tflops"], 4),
             "stage_ms": _stages_out(stage_ms),
             "roofline": roof, "gpu_launches": launches * K,
@@ -744,7 +759,7 @@ def main():
         try:
             B3, P3 = 64, 1000
             step3, keep = r.decode_step_fn(B3, P3, rebuilt=True)
-            ms3, st3, l3 = r.time_steps(step3, ks, W, stages=DECODE_STAGES)
+            ms3, st3, l3 = r.time_steps(step3, ks, W, stages=DECODE_STAGES, dominant_events=False)
             us = barrier_max(statistics.mean(ms3)) * 1e3
             byts = B3 * H * (P3 + 1) * (QK + V) * 2 + WEIGHT_BYTES + 2 * B3 * D * 2
             line["decode_rebuilt"] = {
@@ -767,7 +782,7 @@ def main():
         try:
             B4, P4 = 128, 8192
             step4, keep = r.decode_step_fn(B4, P4, rebuilt=False)
-            ms4, st4, l4 = r.time_steps(step4, ks, W, stages=LATENT_STAGES)
+            ms4, st4, l4 = r.time_steps(step4, ks, W, stages=LATENT_STAGES, dominant_events=False)
             us = barrier_max(statistics.mean(ms4)) * 1e3
             byts = B4 * (P4 + 1) * (KVL + ROPE) * 2 + WEIGHT_BYTES + 2 * B4 * D * 2
             line["decode_latent"] = {
@@ -790,7 +805,7 @@ def main():
         try:
             B4, P4 = 128, 8192
             step4f, keep = r.decode_folded_step_fn(B4, P4)
-            ms4f, st4f, l4f = r.time_steps(step4f, ks, W, stages=LATENT_STAGES)
+            ms4f, st4f, l4f = r.time_steps(step4f, ks, W, stages=LATENT_STAGES, dominant_events=False)
             us = barrier_max(statistics.mean(ms4f)) * 1e3
             wbytes = WEIGHT_BYTES - 2 * (7168 * 8192 + 64 * 128 * 512) + 2 * 7168 * 64 * 512
             byts = B4 * (P4 + 1) * (KVL + ROPE) * 2 + wbytes + 2 * B4 * D * 2
@@ -815,7 +830,7 @@ def main():
 
             def step3f(timing):
                 r.m.mla_decode_fp8(WQ, x3, P3, kc, vc, o3, ws3, r.m.make_params(timing=timing))
-            ms3f, st3f, l3f = r.time_steps(step3f, ks, W, stages=DECODE_STAGES)
+            ms3f, st3f, l3f = r.time_steps(step3f, ks, W, stages=DECODE_STAGES, dominant_events=False)
             us = barrier_max(statistics.mean(ms3f)) * 1e3
             wbytes = sum(t.numel() * t.element_size() for t in keepw.values())
             byts = B3 * H * (P3 + 1) * (QK + V) * 2 + wbytes + 2 * B3 * D * 2
@@ -836,7 +851,7 @@ def main():
             B4v, P4v = 128, 8192
             lengths = varlen_lengths(B4v, P4v)
             step4v, keep = r.decode_varlen_step_fn(B4v, P4v, False, lengths)
-            ms4v, st4v, l4v = r.time_steps(step4v, ks, W, stages=LATENT_STAGES)
+            ms4v, st4v, l4v = r.time_steps(step4v, ks, W, stages=LATENT_STAGES, dominant_events=False)
             us = barrier_max(statistics.mean(ms4v)) * 1e3
             keys = sum(p + 1 for p in lengths)
             byts = keys * (KVL + ROPE) * 2 + WEIGHT_BYTES + 2 * B4v * D * 2
@@ -855,7 +870,7 @@ def main():
             B2, T2 = 1, 2048
             x2, out2, ws2, c2 = r.prefill_setup(B2, T2, with_cache=False)
             step2 = r.prefill_step_fn(x2, out2, ws2, c2, T2)
-            ms2, st2, l2 = r.time_steps(step2, ks, W, stages=PREFILL_STAGES)
+            ms2, st2, l2 = r.time_steps(step2, ks, W, stages=PREFILL_STAGES, dominant_events=False)
             launches_c2 = l2
             ms2 = barrier_max(statistics.mean(ms2))
             fl2 = B2 * T2 * proj_flops_per_token() + prefill_attn_flops(B2, T2)
@@ -880,7 +895,7 @@ def main():
             B1, T1 = 1, 16
             x1, out1, ws1, c1 = r.prefill_setup(B1, T1, with_cache=False)
             step1 = r.prefill_step_fn(x1, out1, ws1, c1, T1)
-            ms1, st1, l1 = r.time_steps(step1, max(ks, 10), W, stages=PREFILL_STAGES)
+            ms1, st1, l1 = r.time_steps(step1, max(ks, 10), W, stages=PREFILL_STAGES, dominant_events=False)
             us1 = barrier_max(statistics.mean(ms1)) * 1e3
             fl1 = B1 * T1 * proj_flops_per_token() + prefill_attn_flops(B1, T1)
             by1 = WEIGHT_BYTES + 2 * B1 * T1 * D * 2
@@ -907,7 +922,7 @@ def main():
         try:
             B6, P6, T6 = 1, 2048, 2048
             step6, keep = r.chunk_step_fn(B6, P6, T6)
-            ms6, st6, l6 = r.time_steps(step6, ks, W, stages=PREFILL_STAGES)
+            ms6, st6, l6 = r.time_steps(step6, ks, W, stages=PREFILL_STAGES, dominant_events=False)
             ms6 = barrier_max(statistics.mean(ms6))
             fl6 = B6 * T6 * proj_flops_per_token() + prefill_attn_flops(B6, T6, P6)
             line["prefill_chunk"] = {
@@ -925,7 +940,7 @@ def main():
         try:
             B6, P6, T6 = 1, 2048, 2048
             step6, keep = r.chunk_latent_step_fn(B6, P6, T6)
-            ms6, st6, l6 = r.time_steps(step6, ks, W, stages=PREFILL_STAGES)
+            ms6, st6, l6 = r.time_steps(step6, ks, W, stages=PREFILL_STAGES, dominant_events=False)
             ms6 = barrier_max(statistics.mean(ms6))
             # algorithmic work as the chunk on the rebuilt cache, plus the kv_b
             # rebuild of the P0 cached positions
@@ -947,14 +962,14 @@ def main():
         try:
             B8, P8, T8 = 32, 8188, 4
             step8, keep = r.chunk_absorbed_step_fn(B8, P8, T8)
-            ms8, st8, l8 = r.time_steps(step8, ks, W, stages=LATENT_STAGES)
+            ms8, st8, l8 = r.time_steps(step8, ks, W, stages=LATENT_STAGES, dominant_events=False)
             us = barrier_max(statistics.mean(ms8)) * 1e3
             keys = B8 * sum(P8 + t + 1 for t in range(T8))
             byts = keys * (KVL + ROPE) * 2 + WEIGHT_BYTES + 2 * B8 * T8 * D * 2
             del step8, keep
             torch.cuda.empty_cache()
             step8r, keep = r.chunk_absorbed_step_fn(B8, P8, T8, absorbed=False)
-            ms8r, _, _ = r.time_steps(step8r, max(2, min(ks, 5)), 2, with_stages=False)
+            ms8r, _, _ = r.time_steps(step8r, max(2, min(ks, 5)), 2, with_stages=False, dominant_events=False)
             us_r = barrier_max(statistics.mean(ms8r)) * 1e3
             del step8r, keep
             torch.cuda.empty_cache()
@@ -973,7 +988,7 @@ def main():
         try:
             n7 = 2048
             step7, keep = r.ffn_step_fn(n7)
-            ms7, st7, l_ffn = r.time_steps(step7, ks, W, stages=FFN_STAGES)
+            ms7, st7, l_ffn = r.time_steps(step7, ks, W, stages=FFN_STAGES, dominant_events=False)
             ms7 = barrier_max(statistics.mean(ms7))
             fl7 = 3 * 2 * n7 * D * FFN_I
             line["ffn_prefill"] = {
@@ -990,7 +1005,7 @@ def main():
         try:
             n8 = 64
             step8, keep = r.ffn_step_fn(n8)
-            ms8, st8, l8 = r.time_steps(step8, ks, W, stages=FFN_STAGES)
+            ms8, st8, l8 = r.time_steps(step8, ks, W, stages=FFN_STAGES, dominant_events=False)
             us8 = barrier_max(statistics.mean(ms8)) * 1e3
             by8 = FFN_WEIGHT_BYTES + 2 * n8 * D * 2
             line["ffn_decode"] = {
@@ -1007,7 +1022,8 @@ def main():
         try:
             B9, T9 = 1, 2048
             step9, keep = r.block_step_fn(B9, T9)
-            ms9, st9, _ = r.time_steps(step9, ks, W, stages=PREFILL_STAGES + FFN_STAGES)
+            ms9, st9, _ = r.time_steps(step9, ks, W, stages=PREFILL_STAGES + FFN_STAGES,
+                                       dominant_events=False)
             ms9 = barrier_max(statistics.mean(ms9))
             fl9 = (B9 * T9 * proj_flops_per_token() + prefill_attn_flops(B9, T9)
                    + 3 * 2 * B9 * T9 * D * FFN_I)
