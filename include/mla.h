@@ -26,9 +26,9 @@
  *     device memory: all scratch lives in the caller's workspace, sized by
  *     mla_workspace_size().  A workspace must not be shared by calls that may
  *     run concurrently.
- *   - Decode and prefill calls of at most 128 rows run the kv_b product on a
- *     second stream of the library's own, beside q_b (both stream weights and
- *     neither fills the GPU alone), forked from and joined back into
+ *   - Decode and prefill calls of at most 4096 rows run the kv_b product on a
+ *     second stream of the library's own, beside q_b (neither fills the GPU
+ *     alone, or its last wave of tiles), forked from and joined back into
  *     `stream` with events: the call is still ordered on `stream` as a whole.
  *     That stream and its two events are created by the first such call of
  *     each host thread on each device (not during a stream capture: a call

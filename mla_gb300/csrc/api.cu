@@ -321,13 +321,17 @@ int kv_b_stage(const mla_weights_t* w, int n_tok, int t_mod, int t_off, __nv_bfl
                    ws, L, st, sms, stream, launches, pos, pos_max, f8, split_ok);
 }
 
-// Few rows (decode, short prefill): q_b and kv_b are weight-streaming
-// launches of 128 CTAs each, leaving a sixth of the SMs idle, and neither
-// reads the other's output; kv_b then runs on a second stream beside q_b.
-// One such stream and two events per host thread and device, created by the
-// first call that uses them (never during a stream capture) and kept for
-// the thread's lifetime.
-constexpr int kForkMaxRows = 128;
+// q_b and kv_b read different outputs of the latent split and neither reads
+// the other's, so for up to kForkMaxRows rows kv_b runs on a second stream
+// beside q_b: with few rows (decode, short prefill) each is a
+// weight-streaming launch of 128 CTAs that leaves a sixth of the SMs idle;
+// with a few thousand rows each ends on a partly filled last wave of tiles
+// (q_b at 2048 rows: 384 CTA-pair tiles over 76 pairs), which the other's
+// tiles fill.  Past that the waves are many and full.  One such stream and
+// two events per host thread and device, created by the first call that
+// uses them (never during a stream capture) and kept for the thread's
+// lifetime.
+constexpr int kForkMaxRows = 4096;
 
 struct SideStream {
   cudaStream_t s = nullptr;
