@@ -1,6 +1,6 @@
 """Stream ordering and CUDA-graph capture of the entry points.
 
-Decode and prefill calls of at most 128 rows run the kv_b product on a second
+Decode and prefill calls of at most 4096 rows run the kv_b product on a second
 stream of the library's own, forked from the caller's stream and joined back
 into it with events, so a call is ordered on the caller's stream as a whole.
 Checked here through the C ABI, bit for bit against the same call on the
@@ -12,7 +12,10 @@ inputs give the same bits):
   host thread, which creates the side stream) and replayed, twice, the second
   time with new inputs written into the captured buffers: a rebuilt-cache
   decode step (B = 64, the side stream), a short prefill (T = 16, the side
-  stream) and a latent decode step (one stream throughout).
+  stream) and a latent decode step (one stream throughout);
+- a call captured as the first call of its host thread (no side stream is
+  created during a capture: the call stays on the capturing stream);
+- two host threads calling at the same time on their own streams.
 """
 import pytest
 
@@ -138,3 +141,100 @@ def test_latent_decode_graph_replay_matches_eager(gpu_available):
     for got, (orf, c1, c2) in zip((first, second), refs):
         assert torch.equal(got[0], orf)
         assert torch.equal(got[1], c1) and torch.equal(got[2], c2)
+
+
+def _in_thread(fn):
+    """Run fn() on a new host thread (its own side-stream state) and return
+    its result, re-raising what it raised."""
+    import threading
+    box = {}
+
+    def run():
+        import torch
+        torch.cuda.set_device(0)
+        try:
+            box["value"] = fn()
+        except BaseException as e:  # handed back to the caller
+            box["error"] = e
+    t = threading.Thread(target=run)
+    t.start()
+    t.join()
+    if "error" in box:
+        raise box["error"]
+    return box["value"]
+
+
+def test_capture_as_first_call_of_a_thread(gpu_available):
+    """A thread whose first call is captured: the library creates no stream
+    during the capture, so that call stays on the capturing stream; the
+    replay still matches the eager call bit for bit."""
+    import torch
+    W = m.make_weights(cuda_weights(0))
+    B, P = 64, 50
+    cap = P + 1
+    x, k, v = _decode_inputs(B, P, cap, 18)
+    ws = m.alloc_workspace(m.MODE_DECODE, B, P)
+    kr, vr, orf = k.clone(), v.clone(), torch.empty_like(x)
+    m.mla_decode(W, x, P, kr, vr, orf, ws)
+    torch.cuda.synchronize()
+
+    def captured_first():
+        kg, vg, og = k.clone(), v.clone(), torch.zeros_like(x)
+        ws2 = m.alloc_workspace(m.MODE_DECODE, B, P)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            m.mla_decode(W, x, P, kg, vg, og, ws2)
+        g.replay()
+        torch.cuda.synchronize()
+        return og.clone(), kg.clone(), vg.clone()
+    og, kg, vg = _in_thread(captured_first)
+    assert torch.equal(og, orf)
+    assert torch.equal(kg, kr) and torch.equal(vg, vr)
+
+
+def test_two_threads_on_two_streams(gpu_available):
+    """Two host threads, each with its own stream, workspace and side
+    stream, run decode steps at the same time: each result equals the
+    single-threaded one."""
+    import threading
+    import torch
+    W = m.make_weights(cuda_weights(0))
+    B, P = 64, 80
+    cap = P + 1
+    inputs = [_decode_inputs(B, P, cap, 20 + i) for i in range(2)]
+    refs = []
+    for x, k, v in inputs:
+        kr, vr, orf = k.clone(), v.clone(), torch.empty_like(x)
+        m.mla_decode(W, x, P, kr, vr, orf, m.alloc_workspace(m.MODE_DECODE, B, P))
+        refs.append((orf, kr, vr))
+    torch.cuda.synchronize()
+    results = [None, None]
+    errors = []
+    start = threading.Barrier(2)
+
+    def worker(i):
+        try:
+            torch.cuda.set_device(0)
+            x, k, v = inputs[i]
+            s = torch.cuda.Stream()
+            kg, vg, og = k.clone(), v.clone(), torch.empty_like(x)
+            ws = m.alloc_workspace(m.MODE_DECODE, B, P)
+            torch.cuda.synchronize()
+            start.wait()
+            with torch.cuda.stream(s):
+                for _ in range(5):
+                    m.mla_decode(W, x, P, kg, vg, og, ws)
+            s.synchronize()
+            results[i] = (og, kg, vg)
+        except BaseException as e:
+            errors.append(e)
+    ts = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errors, errors
+    for (og, kg, vg), (orf, kr, vr) in zip(results, refs):
+        assert torch.equal(og, orf)
+        assert torch.equal(kg, kr) and torch.equal(vg, vr)
