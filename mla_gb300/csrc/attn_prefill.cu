@@ -525,14 +525,17 @@ cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, const DevStatusHo
   // the smallest whose work (G heads' query tiles, in key tiles) is at least
   // 1.5x the CTA count times the heaviest item -- the heaviest tiles of the
   // last group then start early enough -- halved while its heads' K/V exceed
-  // 64 MB of L2
+  // 16 MB (measured against 64, 32 and 8 MB caps: at B=8 T=4096 each halving
+  // of the group down to 4 heads made the attention faster, 2.013 -> 1.977 ms,
+  // as the heads in flight read their K/V from L2; at B=1 groups under 8
+  // heads leave heavy tiles of the last groups for the end)
   const long long past_t = a.past / 128, heavy = past_t + n_qt + 1;
   const long long per_head = (long long)n_qt * past_t + (long long)n_qt * (n_qt + 1) / 2 + n_qt;
   const long long need = (3 * (long long)grid * heavy + 2 * per_head - 1) / (2 * per_head);
   const long long kv_head_bytes = ((long long)a.past + a.T) * (192 + 128) * 2;
   int G = 1;
   while (G < need && G < 64) G *= 2;
-  while (G > 1 && (long long)G * kv_head_bytes > (64ll << 20)) G /= 2;
+  while (G > 1 && (long long)G * kv_head_bytes > (16ll << 20)) G /= 2;
   // the work counter: an int of the status region (cleared before every call)
   int* work = reinterpret_cast<int*>(st.word) + kWorkCounterWord;
   DevStatus dst{st.word, st.wait_limit_ns};
