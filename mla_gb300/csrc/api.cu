@@ -367,8 +367,9 @@ SideStream* side_stream(cudaStream_t user) {
   return ss.s ? &ss : nullptr;
 }
 
-// kv_b of a few rows on the side stream, ordered after the work already
-// queued on `stream`; join_side() makes `stream` wait for it.
+// kv_b on the side stream (or on `stream` itself when side is null),
+// ordered after the work already queued on `stream`; join_side() makes
+// `stream` wait for it.
 int kv_b_beside(SideStream* side, const mla_weights_t* w, const Params& p, int n_tok, int t_mod, int t_off,
                 __nv_bfloat16* kc, __nv_bfloat16* vc, int cap, void* ws, const Layout& L, const DevStatusHost& st,
                 int sms, cudaStream_t stream, int* launches, const int* pos, int pos_max,
